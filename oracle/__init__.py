@@ -1,0 +1,275 @@
+"""fp64 CPU oracle for the In-Place TTT fast-weight layer (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this package; the product library never
+does.  The arithmetic lives in ``ittt_oracle.c`` (plain C, double precision,
+OpenMP over output rows); this module only compiles it with gcc, loads it with
+ctypes and converts numpy arrays.
+
+Every function here evaluates the layer as the In-Place TTT pages define it
+("[논문리뷰] In-Place Test-Time Training", Method §1 eq. (2)-(4), §2 eq. (5)-(6),
+§3 "Implementation Details"); see the C file's header for the readings taken
+where the pages are silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ittt_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libittt_oracle.so")
+
+PAD_CHUNK = 0
+PAD_SEQUENCE = 1
+
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_dbl = ctypes.c_double
+_int = ctypes.c_int
+_fp = ctypes.POINTER(ctypes.c_float)
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int64)
+
+
+def build(force: bool = False) -> str:
+    """Compile ittt_oracle.c into a shared library (gcc -O2 -fopenmp)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        # ITTT_ORACLE_LIB lets the oracle's own mutation test load a copy of
+        # this library built from a deliberately broken source.
+        lib = ctypes.CDLL(os.environ.get("ITTT_ORACLE_LIB") or build())
+        lib.oracle_gated_activation.argtypes = [_i64, _i64, _i64, _fp, _fp, _fp, _dp]
+        lib.oracle_conv1d.argtypes = [_i64, _i64, _i64, _int, _fp, _fp, _dp]
+        lib.oracle_value_target.argtypes = [_i64, _i64, _i64, _int, _fp, _fp, _fp, _dp]
+        lib.oracle_forward_sequential.argtypes = [
+            _i64, _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp,
+            _i64, _fp, _fp, _dp, _dp, _dp, _dp]
+        lib.oracle_forward_prefix.argtypes = [
+            _i64, _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp,
+            _i64, _fp, _fp, _dp, _dp]
+        lib.oracle_forward_dual.argtypes = [
+            _i64, _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp,
+            _i64, _fp, _fp, _dp]
+        lib.oracle_z_entries.argtypes = [_i64, _fp, _fp, _fp, _i64, _ip, _ip, _dp]
+        lib.oracle_vhat_entries.argtypes = [_i64, _i64, _i64, _int, _fp, _fp, _fp,
+                                            _i64, _ip, _ip, _dp]
+        lib.oracle_state_entries.argtypes = [
+            _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp, _fp,
+            _fp, _i64, _ip, _ip, _dp]
+        lib.oracle_first_chunk_rows.argtypes = [_i64, _i64, _fp, _fp, _fp, _fp,
+                                                _i64, _ip, _dp]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _f32(a) -> np.ndarray:
+    """C-contiguous float32 view/copy of a numpy array or CPU torch tensor."""
+    if hasattr(a, "detach"):  # torch tensor
+        a = a.detach().to("cpu").float().contiguous().numpy()
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _fptr(a: np.ndarray):
+    return a.ctypes.data_as(_fp)
+
+
+def _dptr(a):
+    return None if a is None else a.ctypes.data_as(_dp)
+
+
+def _iptr(a: np.ndarray):
+    return a.ctypes.data_as(_ip)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def _unpack(inp):
+    H, X0 = _f32(inp["H"]), _f32(inp["X0"])
+    Wg, Wu = _f32(inp["W_gate"]), _f32(inp["W_up"])
+    W0, Wt, cw = _f32(inp["W_down0"]), _f32(inp["W_target"]), _f32(inp["conv_w"])
+    if H.ndim == 2:
+        H, X0 = H[None], X0[None]
+    B, T, d = H.shape
+    f = Wg.shape[0]
+    assert X0.shape == (B, T, d) and Wg.shape == (f, d) and Wu.shape == (f, d)
+    assert Wt.shape == (d, d) and cw.shape == (d, 3)
+    if W0.ndim == 3:  # per-sequence initial state
+        assert W0.shape == (B, d, f)
+        w0_stride = d * f
+    else:
+        assert W0.shape == (d, f)
+        w0_stride = 0
+    return H, X0, Wg, Wu, W0, Wt, cw, B, T, d, f, w0_stride
+
+
+def forward(inp, eta: float, chunk: int, pad_mode: int = PAD_CHUNK,
+            want_z: bool = False, want_vhat: bool = False,
+            want_states: bool = False) -> dict:
+    """Sequential apply-then-update loop over chunks (the defining form).
+
+    Returns {"O": [B,T,d]} plus optional "Z" [B,T,f], "Vhat" [B,T,d] and
+    "states" [B,n+1,d,f] (W^(0)..W^(n)), all float64.
+    """
+    H, X0, Wg, Wu, W0, Wt, cw, B, T, d, f, w0s = _unpack(inp)
+    if chunk <= 0 or T % chunk:
+        raise ValueError("chunk must divide T")
+    n = T // chunk
+    O = np.zeros((B, T, d), np.float64)
+    Z = np.zeros((B, T, f), np.float64) if want_z else None
+    V = np.zeros((B, T, d), np.float64) if want_vhat else None
+    S = np.zeros((B, n + 1, d, f), np.float64) if want_states else None
+    _load().oracle_forward_sequential(
+        B, T, d, f, chunk, float(eta), pad_mode, _fptr(H), _fptr(X0), _fptr(Wg),
+        _fptr(Wu), _fptr(W0), w0s, _fptr(Wt), _fptr(cw), _dptr(O), _dptr(Z),
+        _dptr(V), _dptr(S))
+    out = {"O": O}
+    if want_z:
+        out["Z"] = Z
+    if want_vhat:
+        out["Vhat"] = V
+    if want_states:
+        out["states"] = S
+    return out
+
+
+def forward_prefix(inp, eta: float, chunk: int, pad_mode: int = PAD_CHUNK,
+                   want_states: bool = False) -> dict:
+    """Three-stage form: per-chunk deltas, exclusive prefix sum, apply."""
+    H, X0, Wg, Wu, W0, Wt, cw, B, T, d, f, w0s = _unpack(inp)
+    if chunk <= 0 or T % chunk:
+        raise ValueError("chunk must divide T")
+    n = T // chunk
+    O = np.zeros((B, T, d), np.float64)
+    S = np.zeros((B, n + 1, d, f), np.float64) if want_states else None
+    _load().oracle_forward_prefix(
+        B, T, d, f, chunk, float(eta), pad_mode, _fptr(H), _fptr(X0), _fptr(Wg),
+        _fptr(Wu), _fptr(W0), w0s, _fptr(Wt), _fptr(cw), _dptr(O), _dptr(S))
+    out = {"O": O}
+    if want_states:
+        out["states"] = S
+    return out
+
+
+def forward_dual(inp, eta: float, chunk: int, pad_mode: int = PAD_CHUNK) -> dict:
+    """Dual form O_[i] = Z_[i] W0^T + eta * sum_{j<i} (Z_[i] Z_[j]^T) Vhat_[j]."""
+    H, X0, Wg, Wu, W0, Wt, cw, B, T, d, f, w0s = _unpack(inp)
+    if chunk <= 0 or T % chunk:
+        raise ValueError("chunk must divide T")
+    O = np.zeros((B, T, d), np.float64)
+    _load().oracle_forward_dual(
+        B, T, d, f, chunk, float(eta), pad_mode, _fptr(H), _fptr(X0), _fptr(Wg),
+        _fptr(Wu), _fptr(W0), w0s, _fptr(Wt), _fptr(cw), _dptr(O))
+    return {"O": O}
+
+
+def gated_activation(H, W_gate, W_up) -> np.ndarray:
+    """Z = SiLU(H W_gate^T) * (H W_up^T) for one sequence H [T, d]."""
+    H, Wg, Wu = _f32(H), _f32(W_gate), _f32(W_up)
+    T, d = H.shape
+    f = Wg.shape[0]
+    Z = np.zeros((T, f), np.float64)
+    _load().oracle_gated_activation(T, d, f, _fptr(H), _fptr(Wg), _fptr(Wu), _dptr(Z))
+    return Z
+
+
+def conv1d(X0, conv_w, chunk: int, pad_mode: int = PAD_CHUNK) -> np.ndarray:
+    """Depthwise three-tap convolution of one sequence X0 [T, d]."""
+    X0, cw = _f32(X0), _f32(conv_w)
+    T, d = X0.shape
+    Xc = np.zeros((T, d), np.float64)
+    _load().oracle_conv1d(T, d, chunk, pad_mode, _fptr(X0), _fptr(cw), _dptr(Xc))
+    return Xc
+
+
+def value_target(X0, conv_w, W_target, chunk: int,
+                 pad_mode: int = PAD_CHUNK) -> np.ndarray:
+    """Vhat = Conv1D(X0) W_target^T for one sequence X0 [T, d]."""
+    X0, cw, Wt = _f32(X0), _f32(conv_w), _f32(W_target)
+    T, d = X0.shape
+    V = np.zeros((T, d), np.float64)
+    _load().oracle_value_target(T, d, chunk, pad_mode, _fptr(X0), _fptr(cw),
+                                _fptr(Wt), _dptr(V))
+    return V
+
+
+# --------------------------------------------------------------------------
+# Entry-wise evaluators (full-size workloads).  `H`, `X0` are ONE sequence.
+# --------------------------------------------------------------------------
+
+def z_entries(H, W_gate, W_up, t_idx, j_idx) -> np.ndarray:
+    H, Wg, Wu = _f32(H), _f32(W_gate), _f32(W_up)
+    t = np.ascontiguousarray(t_idx, np.int64)
+    j = np.ascontiguousarray(j_idx, np.int64)
+    out = np.zeros(len(t), np.float64)
+    _load().oracle_z_entries(H.shape[1], _fptr(H), _fptr(Wg), _fptr(Wu), len(t),
+                             _iptr(t), _iptr(j), _dptr(out))
+    return out
+
+
+def vhat_entries(X0, conv_w, W_target, chunk: int, t_idx, m_idx,
+                 pad_mode: int = PAD_CHUNK) -> np.ndarray:
+    X0, cw, Wt = _f32(X0), _f32(conv_w), _f32(W_target)
+    T, d = X0.shape
+    t = np.ascontiguousarray(t_idx, np.int64)
+    m = np.ascontiguousarray(m_idx, np.int64)
+    out = np.zeros(len(t), np.float64)
+    _load().oracle_vhat_entries(T, d, chunk, pad_mode, _fptr(X0), _fptr(cw),
+                                _fptr(Wt), len(t), _iptr(t), _iptr(m), _dptr(out))
+    return out
+
+
+def state_entries(H, X0, W_gate, W_up, w0, W_target, conv_w, eta: float,
+                  chunk: int, m_idx, j_idx, pad_mode: int = PAD_CHUNK) -> np.ndarray:
+    """W^(i)[m, j] for i = 0..n at each (m, j) pair: returns [count, n+1]."""
+    H, X0 = _f32(H), _f32(X0)
+    Wg, Wu, w0 = _f32(W_gate), _f32(W_up), _f32(w0)
+    Wt, cw = _f32(W_target), _f32(conv_w)
+    T, d = H.shape
+    f = Wg.shape[0]
+    n = T // chunk
+    m = np.ascontiguousarray(m_idx, np.int64)
+    j = np.ascontiguousarray(j_idx, np.int64)
+    out = np.zeros((len(m), n + 1), np.float64)
+    _load().oracle_state_entries(T, d, f, chunk, float(eta), pad_mode, _fptr(H),
+                                 _fptr(X0), _fptr(Wg), _fptr(Wu), _fptr(w0),
+                                 _fptr(Wt), _fptr(cw), len(m), _iptr(m), _iptr(j),
+                                 _dptr(out))
+    return out
+
+
+def first_chunk_rows(H, W_gate, W_up, w0, rows) -> np.ndarray:
+    """O[t, :] = Z[t, :] W_down0^T for tokens t of the first chunk: [count, d]."""
+    H, Wg, Wu, w0 = _f32(H), _f32(W_gate), _f32(W_up), _f32(w0)
+    d = H.shape[1]
+    f = Wg.shape[0]
+    r = np.ascontiguousarray(rows, np.int64)
+    out = np.zeros((len(r), d), np.float64)
+    _load().oracle_first_chunk_rows(d, f, _fptr(H), _fptr(Wg), _fptr(Wu),
+                                    _fptr(w0), len(r), _iptr(r), _dptr(out))
+    return out

@@ -1,0 +1,65 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of oracle/ittt_oracle.c (on the CPU,
+in a temporary directory), builds it, and runs the pin suite against that
+copy: the suite has to fail.  The committed oracle is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "ittt_oracle.c")
+
+# (name, exact text in the oracle, replacement)
+MUTANTS = [
+    ("silu_drops_gate_sigmoid", "return x / (1.0 + exp(-x));", "return x;"),
+    ("conv_taps_flipped",
+     "acc += (double)conv_w[c * 3 + (k + 1)] * (double)X0[s * d + c];",
+     "acc += (double)conv_w[c * 3 + (1 - k)] * (double)X0[s * d + c];"),
+    ("conv_ignores_chunk_edges", "lo = (t / C) * C;\n      hi = lo + C;", "lo = 0;\n      hi = T;"),
+    ("target_not_transposed",
+     "acc += Xc[t * d + c] * (double)W_target[m * d + c];",
+     "acc += Xc[t * d + c] * (double)W_target[c * d + m];"),
+    ("update_sign_flipped", "for (int64_t e = 0; e < d * f; ++e) W[e] += eta * dW[e];",
+     "for (int64_t e = 0; e < d * f; ++e) W[e] -= eta * dW[e];"),
+    ("update_before_apply",
+     "      apply_chunk(i * C, C, d, f, Z, W, O + b * T * d);          /* apply  */\n"
+     "      chunk_delta(i * C, C, d, f, Vhat, Z, dW);                  /* update */\n"
+     "      for (int64_t e = 0; e < d * f; ++e) W[e] += eta * dW[e];",
+     "      chunk_delta(i * C, C, d, f, Vhat, Z, dW);\n"
+     "      for (int64_t e = 0; e < d * f; ++e) W[e] += eta * dW[e];\n"
+     "      apply_chunk(i * C, C, d, f, Z, W, O + b * T * d);"),
+    ("initial_weight_dropped", "for (int64_t e = 0; e < d * f; ++e) W[e] = (double)W0[e];",
+     "for (int64_t e = 0; e < d * f; ++e) W[e] = 0.0;"),
+    ("delta_reads_next_chunk", "for (int64_t t = t0; t < t0 + Cn; ++t)\n        acc += Vhat",
+     "for (int64_t t = t0 + 1; t < t0 + Cn + 1 && t < t0 + Cn; ++t)\n        acc += Vhat"),
+    ("delta_uses_Z_for_both_operands", "acc += Vhat[t * d + m] * Z[t * f + j];",
+     "acc += Z[t * f + m] * Z[t * f + j];"),
+    ("prefix_scan_inclusive",
+     "S[i * df + e] = S[(i - 1) * df + e] + dWs[(i - 1) * df + e];",
+     "S[i * df + e] = S[(i - 1) * df + e] + dWs[(i < n ? i : n - 1) * df + e];"),
+    ("dual_includes_current_chunk", "for (int64_t s = 0; s < i * C; ++s) { /* every token",
+     "for (int64_t s = 0; s < (i + 1) * C; ++s) { /* every token"),
+    ("state_entries_skip_eta",
+     "out[q * (n + 1) + i + 1] = (double)w0[m * f + j] + eta * sum;",
+     "out[q * (n + 1) + i + 1] = (double)w0[m * f + j] + sum;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutated = tmp_path / "ittt_oracle_mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "libittt_oracle_mutant.so"
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-o", str(lib),
+                    str(mutated), "-lm"], check=True)
+    env = dict(os.environ, ITTT_ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
