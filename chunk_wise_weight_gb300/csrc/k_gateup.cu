@@ -1,0 +1,129 @@
+// k_gateup.cu -- gate/up GEMM with the SiLU (.) mul epilogue:
+//   Z = SiLU(H W_gate^T) (.) (H W_up^T)
+// ("[논문리뷰] In-Place Test-Time Training", Method §1 eq. (2), phi = SiLU).
+//
+// Each 128 x 256 MMA tile computes 128 gate columns and the matching 128 up
+// columns for the same f-range: the producer stacks the W_gate rows and the
+// W_up rows of that range into one 256-row B tile, so the accumulator holds
+// gate pre-activations in TMEM columns 0..127 and up pre-activations in
+// 128..255.  The epilogue pairs column j with column j + 128 and writes
+// 128 bf16 Z columns.
+#include "kernels.h"
+#include "pipeline.cuh"
+
+namespace ittt {
+namespace {
+
+constexpr int kGateUpTileN = 128;
+
+struct GateUpParams {
+  CUtensorMap tm_h;   // H      [M, K]  box {64, 128}
+  CUtensorMap tm_wg;  // W_gate [f, K]  box {64, 128}
+  CUtensorMap tm_wu;  // W_up   [f, K]  box {64, 128}
+  __nv_bfloat16* z;   // Z      [M, f]
+  int M, f;
+  int m_tiles, n_tiles, kblocks, raster;
+};
+
+struct GateUpSched {
+  using Params = GateUpParams;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, false);
+
+  const Params& p;
+  int m0 = 0, n0 = 0, acc = 0;
+
+  __device__ explicit GateUpSched(const Params& pp) : p(pp) {}
+  __device__ int num_units() const { return p.m_tiles * p.n_tiles; }
+  __device__ void begin_unit(int u, int local) {
+    int m, n;
+    raster_grouped(u, p.m_tiles, p.n_tiles, p.raster, m, n);
+    m0 = m * kBM;
+    n0 = n * kGateUpTileN;
+    acc = local & 1;
+  }
+  __device__ int num_segments() const { return 1; }
+  __device__ int seg_acc(int) const { return acc; }
+  __device__ int seg_kblocks(int) const { return p.kblocks; }
+  __device__ bool seg_fresh(int) const { return true; }
+
+  __device__ void load(int, int kb, void* a, void* b, uint64_t* bar) const {
+    const int k = kb * kBK;
+    tma_load_2d(a, &p.tm_h, bar, k, m0);
+    tma_load_2d(b, &p.tm_wg, bar, k, n0);
+    tma_load_2d(static_cast<uint8_t*>(b) + kBTileBytes / 2, &p.tm_wu, bar, k, n0);
+  }
+
+  // K-major, 128-byte swizzle: the k-th 16-wide slice starts 32 bytes in.
+  static __device__ uint64_t a_desc(uint32_t base, int k) {
+    return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
+  }
+  static __device__ uint64_t b_desc(uint32_t base, int k) {
+    return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
+  }
+
+  __device__ void epilogue(int, int row, uint32_t trow) const {
+    const int gm = m0 + row;
+    const bool row_ok = gm < p.M;
+    __nv_bfloat16* zrow = p.z + size_t(row_ok ? gm : 0) * size_t(p.f);
+#pragma unroll 1
+    for (int c = 0; c < kGateUpTileN; c += 32) {
+      uint32_t g[32], u[32];
+      tmem_ld_32cols(trow + uint32_t(c), g);
+      tmem_ld_32cols(trow + uint32_t(kGateUpTileN + c), u);
+      tmem_wait_ld();
+      pin_regs(g);
+      pin_regs(u);
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+        const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
+        const float z0 = g0 / (1.0f + __expf(-g0)) * u0;
+        const float z1 = g1 / (1.0f + __expf(-g1)) * u1;
+        pk[j] = pack_bf16x2(z0, z1);
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int col = n0 + c + 8 * q;
+          if (col < p.f) {
+            *reinterpret_cast<uint4*>(zrow + col) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+      }
+    }
+  }
+};
+
+__global__ void __launch_bounds__(kNumThreads, 1)
+    gateup_kernel(const __grid_constant__ GateUpParams p, unsigned int* status) {
+  run_pipeline<GateUpSched>(p, status);
+}
+
+}  // namespace
+
+cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h, const CUtensorMap& tm_wg,
+                          const CUtensorMap& tm_wu, __nv_bfloat16* z, int M, int f, int K) {
+  GateUpParams p;
+  p.tm_h = tm_h;
+  p.tm_wg = tm_wg;
+  p.tm_wu = tm_wu;
+  p.z = z;
+  p.M = M;
+  p.f = f;
+  p.m_tiles = (M + kBM - 1) / kBM;
+  p.n_tiles = (f + kGateUpTileN - 1) / kGateUpTileN;
+  p.kblocks = (K + kBK - 1) / kBK;
+  p.raster = p.n_tiles < 16 ? p.n_tiles : 16;
+  const int units = p.m_tiles * p.n_tiles;
+  if (units == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(kPipeSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int grid = units < env.num_sms ? units : env.num_sms;
+  gateup_kernel<<<grid, kNumThreads, kPipeSmemBytes, env.stream>>>(p, env.status);
+  return cudaGetLastError();
+}
+
+}  // namespace ittt

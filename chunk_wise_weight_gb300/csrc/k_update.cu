@@ -1,0 +1,222 @@
+// k_update.cu -- the fast-weight update, walked chunk by chunk:
+//   W_{i+1} = W_i + eta * Vhat_[i]^T Z_[i]
+// ("[논문리뷰] In-Place Test-Time Training", Method §2 eq. (6); the prefix
+// sum of Method §3 stage 2, "In-Place TTT" reading notes 实现细节).
+//
+// The per-chunk deltas do not depend on W (the loss is linear in it), so
+// the prefix sum S_i = sum_{j<i} delta_j is one long contraction over the
+// tokens of a sequence.  A work unit owns a 128 (d_model) x 512 (d_ff)
+// block of one sequence's state, split into two 128 x 256 halves whose fp32
+// running sums live in the two TMEM accumulators for the whole walk.  The
+// MMAs alternate halves chunk by chunk: while the tensor core accumulates
+// chunk i of one half, the epilogue reads the other half's sum at its chunk
+// boundary and writes the bf16 snapshot W_{i+1} = bf16(W_0 + eta * S_{i+1})
+// that the apply kernel reads.  The fp32 state never goes to HBM unless the
+// caller asks for the final state.
+//
+// Both operands are read MN-major: the contraction index (token) is the row
+// index of Vhat [T, d] and of Z [T, f].  A 64-token stage holds, per operand,
+// 64-column TMA boxes of 64 token lines x 128 bytes each.
+#include "kernels.h"
+#include "pipeline.cuh"
+
+namespace ittt {
+namespace {
+
+constexpr uint32_t kMnBoxBytes = 64 * 64 * 2;  // one {64 cols, 64 tokens} box
+
+struct UpdateParams {
+  CUtensorMap tm_v;  // Vhat [B*T, d]  box {64, 64}
+  CUtensorMap tm_z;  // Z    [B*T, f]  box {64, 64}
+  const void* w0;
+  int w0_fp32;
+  int64_t w0_bstride;
+  __nv_bfloat16* snap;  // [B, n, d, f]
+  float* state_out;     // [B, d, f] or nullptr
+  float eta;
+  int B, T, d, f, C, n, n_upd;
+  int mt, np, kb_per_chunk;
+};
+
+struct UpdateSched {
+  using Params = UpdateParams;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true, true);
+
+  const Params& p;
+  int b = 0, m0 = 0, nbase = 0, halves = 1;
+
+  __device__ explicit UpdateSched(const Params& pp) : p(pp) {}
+  __device__ int num_units() const { return p.B * p.mt * p.np; }
+  __device__ void begin_unit(int u, int) {
+    const int np = u % p.np;
+    const int r = u / p.np;
+    const int mt = r % p.mt;
+    b = r / p.mt;
+    m0 = mt * kBM;
+    nbase = np * (2 * kBN);
+    halves = (nbase + kBN < p.f) ? 2 : 1;
+  }
+  __device__ int num_segments() const { return p.n_upd * halves; }
+  __device__ int seg_acc(int s) const { return s % halves; }
+  __device__ int seg_kblocks(int) const { return p.kb_per_chunk; }
+  __device__ bool seg_fresh(int s) const { return s < halves; }
+
+  __device__ void load(int s, int kb, void* a, void* bt, uint64_t* bar) const {
+    const int i = s / halves;
+    const int h = s - i * halves;
+    const int tok = b * p.T + i * p.C + kb * kBK;
+    uint8_t* sa = static_cast<uint8_t*>(a);
+    uint8_t* sb = static_cast<uint8_t*>(bt);
+    tma_load_2d(sa, &p.tm_v, bar, m0, tok);
+    tma_load_2d(sa + kMnBoxBytes, &p.tm_v, bar, m0 + 64, tok);
+    const int n0 = nbase + h * kBN;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kMnBoxBytes, &p.tm_z, bar, n0 + 64 * q, tok);
+  }
+  // MN-major, 128-byte swizzle: a 16-token slice is 16 lines of 128 B; the
+  // 64-column groups of the tile are one box (lbo) apart.
+  static __device__ uint64_t a_desc(uint32_t base, int k) {
+    return sdesc_sw128(base + uint32_t(k) * 2048u, kMnBoxBytes, 1024u);
+  }
+  static __device__ uint64_t b_desc(uint32_t base, int k) {
+    return sdesc_sw128(base + uint32_t(k) * 2048u, kMnBoxBytes, 1024u);
+  }
+
+  __device__ void epilogue(int s, int row, uint32_t trow) const {
+    const int i = s / halves;
+    const int h = s - i * halves;
+    const int m = m0 + row;
+    const bool row_ok = m < p.d;
+    const int n0 = nbase + h * kBN;
+    const bool write_snap = (i + 1) < p.n;
+    float* st = (p.state_out != nullptr && (i + 1) == p.n_upd)
+                    ? p.state_out + (size_t(b) * p.d + size_t(row_ok ? m : 0)) * size_t(p.f)
+                    : nullptr;
+    __nv_bfloat16* snap_row =
+        p.snap + ((size_t(b) * p.n + size_t(i + 1)) * p.d + size_t(row_ok ? m : 0)) * size_t(p.f);
+    const size_t w0_off = size_t(b) * size_t(p.w0_bstride) + size_t(row_ok ? m : 0) * size_t(p.f);
+    const float eta = p.eta;
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 32) {
+      uint32_t v[32];
+      tmem_ld_32cols(trow + uint32_t(c), v);
+      tmem_wait_ld();
+      pin_regs(v);
+      if (!row_ok) continue;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int col = n0 + c + 8 * q;
+        if (col >= p.f) continue;
+        float w[8];
+        if (p.w0_fp32) {
+          const float4* src = reinterpret_cast<const float4*>(
+              static_cast<const float*>(p.w0) + w0_off + col);
+          const float4 lo = __ldg(src), hi = __ldg(src + 1);
+          w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+          w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+        } else {
+          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(p.w0) + w0_off + col));
+          const uint32_t r4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f2 = unpack_bf16x2(r4[j]);
+            w[2 * j] = f2.x;
+            w[2 * j + 1] = f2.y;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = fmaf(eta, __uint_as_float(v[8 * q + j]), w[j]);
+        if (write_snap) {
+          *reinterpret_cast<uint4*>(snap_row + col) =
+              make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                         pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+        }
+        if (st != nullptr) {
+          float4* dst = reinterpret_cast<float4*>(st + col);
+          dst[0] = make_float4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_float4(w[4], w[5], w[6], w[7]);
+        }
+      }
+    }
+  }
+};
+
+__global__ void __launch_bounds__(kNumThreads, 1)
+    update_kernel(const __grid_constant__ UpdateParams p, unsigned int* status) {
+  run_pipeline<UpdateSched>(p, status);
+}
+
+// snap[b, 0] = bf16(W_0 of sequence b): the state the first chunk applies.
+__global__ void __launch_bounds__(256)
+    snapshot0_kernel(const void* __restrict__ w0, int w0_fp32, int64_t w0_bstride,
+                     __nv_bfloat16* __restrict__ snap, int B, int n, int64_t df) {
+  const int64_t per = df >> 3;
+  const int64_t total = int64_t(B) * per;
+  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t b = idx / per;
+    const int64_t e = (idx - b * per) * 8;
+    uint4 out;
+    if (w0_fp32) {
+      const float4* src =
+          reinterpret_cast<const float4*>(static_cast<const float*>(w0) + b * w0_bstride + e);
+      const float4 lo = __ldg(src), hi = __ldg(src + 1);
+      out = make_uint4(pack_bf16x2(lo.x, lo.y), pack_bf16x2(lo.z, lo.w), pack_bf16x2(hi.x, hi.y),
+                       pack_bf16x2(hi.z, hi.w));
+    } else {
+      out = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(w0) +
+                                                 b * w0_bstride + e));
+    }
+    *reinterpret_cast<uint4*>(snap + b * int64_t(n) * df + e) = out;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_snapshot0(const LaunchEnv& env, const void* w0, bool w0_fp32,
+                             int64_t w0_bstride, __nv_bfloat16* snap, int B, int n, int d,
+                             int f) {
+  const int64_t df = int64_t(d) * f;
+  const int64_t total = int64_t(B) * (df / 8);
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = int64_t(env.num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  snapshot0_kernel<<<int(blocks), 256, 0, env.stream>>>(w0, w0_fp32 ? 1 : 0, w0_bstride, snap, B,
+                                                        n, df);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, const CUtensorMap& tm_z,
+                          const UpdateArgs& a) {
+  if (a.n_upd <= 0) return cudaSuccess;
+  UpdateParams p;
+  p.tm_v = tm_vhat;
+  p.tm_z = tm_z;
+  p.w0 = a.w0;
+  p.w0_fp32 = a.w0_fp32 ? 1 : 0;
+  p.w0_bstride = a.w0_bstride;
+  p.snap = a.snap;
+  p.state_out = a.state_out;
+  p.eta = a.eta;
+  p.B = a.B;
+  p.T = a.T;
+  p.d = a.d;
+  p.f = a.f;
+  p.C = a.C;
+  p.n = a.n;
+  p.n_upd = a.n_upd;
+  p.mt = (a.d + kBM - 1) / kBM;
+  p.np = (a.f + 2 * kBN - 1) / (2 * kBN);
+  p.kb_per_chunk = a.C / kBK;
+  const int units = p.B * p.mt * p.np;
+  cudaError_t e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(kPipeSmemBytes));
+  if (e != cudaSuccess) return e;
+  const int grid = units < env.num_sms ? units : env.num_sms;
+  update_kernel<<<grid, kNumThreads, kPipeSmemBytes, env.stream>>>(p, env.status);
+  return cudaGetLastError();
+}
+
+}  // namespace ittt

@@ -1,0 +1,68 @@
+// kernels.h -- internal launchers of libittt.so (host side, C++).  The C-ABI
+// in ittt_api.cu validates arguments, builds the TMA tensor maps and calls
+// these in data-flow order: conv -> target, gate/up -> snapshot 0 -> update
+// -> apply.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ittt {
+
+struct LaunchEnv {
+  cudaStream_t stream;
+  int num_sms;
+  unsigned int* status;  // device status word (kStatusTimeout bits)
+};
+
+// Z[M, f] = SiLU(H W_gate^T) * (H W_up^T).  Tensor maps: H [M, K] box
+// {64,128}; W_gate, W_up [f, K] box {64,128}.  All bf16, K = d_model.
+cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h,
+                          const CUtensorMap& tm_wg, const CUtensorMap& tm_wu,
+                          __nv_bfloat16* z, int M, int f, int K);
+
+// Xc = three-tap depthwise conv of X0 (zero padding at chunk or sequence
+// edges), rounded to bf16.  x0, xc: [B*T, d].
+cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const float* conv_w,
+                        __nv_bfloat16* xc, int64_t rows, int T, int d, int C, int pad_mode);
+
+// Vhat[M, d] = Xc W_target^T.  Tensor maps: Xc [M, d] box {64,128};
+// W_target [d, d] box {64,256}.
+cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_xc,
+                          const CUtensorMap& tm_wt, __nv_bfloat16* vhat, int M, int d);
+
+// snap[b, 0] = bf16(W_0 of sequence b) for every b.  w0 is bf16 or fp32,
+// [d, f] shared (w0_bstride = 0) or [B, d, f].
+cudaError_t launch_snapshot0(const LaunchEnv& env, const void* w0, bool w0_fp32,
+                             int64_t w0_bstride, __nv_bfloat16* snap, int B, int n, int d,
+                             int f);
+
+struct UpdateArgs {
+  int B, T, d, f, C;
+  int n;          // chunks per sequence
+  int n_upd;      // updates to run: n-1, or n when the final state is wanted
+  float eta;
+  const void* w0; // bf16 or fp32 initial state
+  bool w0_fp32;
+  int64_t w0_bstride;
+  __nv_bfloat16* snap;  // [B, n, d, f]: slots 1..n-1 written here
+  float* state_out;     // [B, d, f] fp32 or nullptr
+};
+
+// Fast-weight update walk: for each (sequence, 128 x 512 state tile) the
+// per-chunk deltas Vhat_[i]^T Z_[i] accumulate in TMEM; after chunk i the
+// epilogue writes bf16(W_0 + eta * sum_{j<=i} delta_j) as snapshot i+1.
+// Tensor maps: Vhat [B*T, d] box {64,64}; Z [B*T, f] box {64,64} (both
+// read MN-major).
+cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
+                          const CUtensorMap& tm_z, const UpdateArgs& a);
+
+// O_[i] = Z_[i] snap[b, i]^T for every (sequence, chunk).  Tensor maps:
+// Z [B*T, f] box {64,128}; snapshots [B*n*d, f] box {64,256}.
+cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
+                         const CUtensorMap& tm_snap, void* out, bool out_fp32, int B, int T,
+                         int d, int f, int C);
+
+}  // namespace ittt

@@ -1,0 +1,191 @@
+"""ctypes binding of libittt.so -- argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; this module turns
+torch tensors into ``ittt_tensor`` descriptors (device pointer, dtype, shape,
+strides), passes the current CUDA stream, and raises :class:`IttError` when
+the library returns a non-OK status.  torch only provides device memory and
+streams.  There is no fallback: if libittt.so is missing, loading fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import build as _build
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT = range(6)
+STATUS_NAMES = {0: "ITTT_OK", 1: "ITTT_ERR_INVALID_ARG", 2: "ITTT_ERR_UNSUPPORTED",
+                3: "ITTT_ERR_CUDA", 4: "ITTT_ERR_OOM", 5: "ITTT_ERR_TIMEOUT"}
+BF16, FP32 = 0, 1
+PAD_CHUNK, PAD_SEQUENCE = 0, 1
+PHASES = ("conv", "target", "gateup", "snapshot0", "update", "apply")
+
+_DTYPES = {torch.bfloat16: BF16, torch.float32: FP32}
+
+
+class IttError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [("pad_mode", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("state_in", ctypes.POINTER(Tensor)), ("state_out", ctypes.POINTER(Tensor)),
+                ("z_buf", ctypes.POINTER(Tensor)), ("vhat_buf", ctypes.POINTER(Tensor)),
+                ("snap_buf", ctypes.POINTER(Tensor)), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("events", ctypes.POINTER(ctypes.c_void_p))]
+
+
+_TP = ctypes.POINTER(Tensor)
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load libittt.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                           "or `python -m chunk_wise_weight_gb300.build`")
+    lib = ctypes.CDLL(path)
+    fwd_args = [_TP, _TP, _TP, _TP, _TP, _TP, _TP, ctypes.c_float, ctypes.c_int64, _TP,
+                ctypes.c_void_p]
+    lib.ittt_forward.argtypes = fwd_args
+    lib.ittt_forward.restype = ctypes.c_int
+    lib.ittt_forward_ex.argtypes = fwd_args + [ctypes.POINTER(Opts)]
+    lib.ittt_forward_ex.restype = ctypes.c_int
+    lib.ittt_workspace_bytes.argtypes = [ctypes.c_int64] * 5
+    lib.ittt_workspace_bytes.restype = ctypes.c_size_t
+    lib.ittt_stream_status.argtypes = [ctypes.c_void_p]
+    lib.ittt_stream_status.restype = ctypes.c_int
+    lib.ittt_last_error.argtypes = []
+    lib.ittt_last_error.restype = ctypes.c_char_p
+    lib.ittt_version.argtypes = []
+    lib.ittt_version.restype = ctypes.c_int32
+    lib.ittt_launch_count.argtypes = [ctypes.c_int64] * 5
+    lib.ittt_launch_count.restype = ctypes.c_int32
+    _lib = lib
+    return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the entry points include/ittt.h declares."""
+    with open(os.path.join(_build.INCLUDE, "ittt.h")) as fh:
+        text = fh.read()
+    return re.findall(r"ITTT_API\s+[\w\s\*]+?\b(ittt_\w+)\s*\(", text)
+
+
+def describe(t: torch.Tensor | None) -> Tensor | None:
+    """ittt_tensor descriptor of a torch tensor (no copy, no check)."""
+    if t is None:
+        return None
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    d = Tensor()
+    d.data = t.data_ptr()
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for k in range(t.dim()):
+        d.shape[k] = t.shape[k]
+        d.stride[k] = t.stride(k)
+    return d
+
+
+def _ref(desc):
+    return None if desc is None else ctypes.byref(desc)
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def last_error() -> str:
+    return load().ittt_last_error().decode()
+
+
+def _check(status: int):
+    if status != OK:
+        raise IttError(status, last_error())
+
+
+def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: int,
+            out: torch.Tensor | None = None, *, out_dtype=torch.bfloat16, stream=None,
+            pad_mode: int = PAD_CHUNK, state_in=None, state_out=None, z_buf=None,
+            vhat_buf=None, snap_buf=None, workspace=None, events=None) -> torch.Tensor:
+    """Enqueue one layer forward on `stream` (default: current stream) and
+    return `out` [B,T,d].  Extra keyword buffers map to ittt_opts; `events`
+    is a list of len(PHASES) + 1 torch.cuda.Event(enable_timing=True)."""
+    lib = load()
+    if out is None:
+        out = torch.empty(H.shape, dtype=out_dtype, device=H.device)
+    keep = [describe(x) for x in (H, X0, W_gate, W_up, W_down0, W_target, conv_w, out)]
+    opts = Opts()
+    opts.pad_mode = int(pad_mode)
+    extra = {}
+    for name, t in (("state_in", state_in), ("state_out", state_out), ("z_buf", z_buf),
+                    ("vhat_buf", vhat_buf), ("snap_buf", snap_buf)):
+        if t is not None:
+            extra[name] = describe(t)
+            setattr(opts, name, ctypes.pointer(extra[name]))
+    if workspace is not None:
+        opts.workspace = workspace.data_ptr()
+        opts.workspace_bytes = workspace.numel() * workspace.element_size()
+    ev_arr = None
+    if events is not None:
+        if len(events) != len(PHASES) + 1:
+            raise ValueError(f"events needs {len(PHASES) + 1} entries")
+        ev_arr = (ctypes.c_void_p * len(events))(*[int(e.cuda_event) for e in events])
+        opts.events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
+    s = _stream_handle(stream, H.device)
+    status = lib.ittt_forward_ex(*[_ref(k) for k in keep[:7]], ctypes.c_float(eta),
+                                 ctypes.c_int64(chunk), _ref(keep[7]), ctypes.c_void_p(s),
+                                 ctypes.byref(opts))
+    _check(status)
+    return out
+
+
+def forward_plain(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: int,
+                  out: torch.Tensor, stream=None) -> torch.Tensor:
+    """The plain ittt_forward entry point (no options)."""
+    lib = load()
+    keep = [describe(x) for x in (H, X0, W_gate, W_up, W_down0, W_target, conv_w, out)]
+    s = _stream_handle(stream, H.device)
+    _check(lib.ittt_forward(*[_ref(k) for k in keep[:7]], ctypes.c_float(eta),
+                            ctypes.c_int64(chunk), _ref(keep[7]), ctypes.c_void_p(s)))
+    return out
+
+
+def stream_status(stream=None, device=None) -> None:
+    """Synchronise and raise IttError if a kernel recorded a failure."""
+    _check(load().ittt_stream_status(ctypes.c_void_p(_stream_handle(stream, device))))
+
+
+def workspace_bytes(B: int, T: int, d: int, f: int, chunk: int) -> int:
+    return int(load().ittt_workspace_bytes(B, T, d, f, chunk))
+
+
+def launch_count(B: int, T: int, d: int, f: int, chunk: int) -> int:
+    return int(load().ittt_launch_count(B, T, d, f, chunk))
+
+
+def version() -> int:
+    return int(load().ittt_version())

@@ -1,0 +1,195 @@
+/*
+ * ittt.h -- C-ABI of libittt.so, the In-Place Test-Time Training fast-weight
+ * layer for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (pages: "[논문리뷰] In-Place Test-Time Training", Method §1 eq.
+ * (2)-(4), Method §2 eq. (5)-(6), Method §3 "Implementation Details"):
+ *
+ *   Z     = SiLU(H W_gate^T) (.) (H W_up^T)                  (eq. 2)
+ *   Vhat  = Conv1D(X0) W_target^T                             (eq. 5)
+ *   W_0   = W_down0                    (reset per sequence, Method §3)
+ *   for each chunk i of C tokens, in order:
+ *     O_[i]   = Z_[i] W_i^T                                   (eq. 3, apply)
+ *     W_{i+1} = W_i + eta * Vhat_[i]^T Z_[i]                  (eq. 6, update)
+ *
+ * Conv1D is a depthwise three-tap convolution with taps ordered
+ * (t-1, t, t+1), conv_w[c, k] multiplying X0[t-1+k, c], no bias.  Taps that
+ * reach outside the current chunk read zero (ITTT_PAD_CHUNK, the default: the
+ * pages' "causal padding" that keeps each chunk's update delta isolated to
+ * that chunk) or, with ITTT_PAD_SEQUENCE, only taps outside the sequence read
+ * zero.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are described by ittt_tensor: a DEVICE pointer, a dtype, and
+ *     row-major shapes with element strides.  The last dimension must be
+ *     contiguous (stride 1) and every tensor must be densely packed
+ *     row-major; the data pointer must be 16-byte aligned.
+ *   - Shapes: H, X0 [B,T,d] bf16; W_gate, W_up [f,d] bf16; W_down0 [d,f]
+ *     bf16 or fp32; W_target [d,d] bf16; conv_w [d,3] fp32; out [B,T,d]
+ *     bf16 or fp32.  Weights use the [out_features, in_features] layout.
+ *   - Supported sizes: d and f multiples of 8 (16-byte rows), chunk > 0 a
+ *     multiple of 64 that divides T, B*T < 2^31.  Anything else returns
+ *     ITTT_ERR_UNSUPPORTED or ITTT_ERR_INVALID_ARG before any launch.
+ *   - Ownership: the caller owns every buffer; the library keeps no pointer
+ *     after a call returns.  `out` must not overlap any input.
+ *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and the call returns without synchronising.
+ *     Scratch memory comes from cudaMallocAsync/cudaFreeAsync on the same
+ *     stream unless the caller passes a workspace.
+ *   - Errors: a status code is returned, no exception crosses the ABI, and
+ *     ittt_last_error() describes the most recent failure on this thread.
+ *     Argument errors are detected before anything is enqueued.  Device-side
+ *     failures (a bounded wait that ran out) are reported by
+ *     ittt_stream_status().
+ */
+#ifndef ITTT_H_
+#define ITTT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ITTT_API __attribute__((visibility("default")))
+#else
+#define ITTT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* ittt_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  ITTT_OK = 0,
+  ITTT_ERR_INVALID_ARG = 1, /* bad pointer, dtype, shape, stride or alias */
+  ITTT_ERR_UNSUPPORTED = 2, /* valid, but outside the supported sizes */
+  ITTT_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  ITTT_ERR_OOM = 4,         /* scratch allocation failed */
+  ITTT_ERR_TIMEOUT = 5      /* a kernel's bounded wait ran out */
+} ittt_status;
+
+typedef enum { ITTT_BF16 = 0, ITTT_FP32 = 1 } ittt_dtype;
+
+typedef enum {
+  ITTT_PAD_CHUNK = 0,    /* conv taps outside the current chunk read 0 */
+  ITTT_PAD_SEQUENCE = 1  /* conv taps outside the sequence read 0 */
+} ittt_pad_mode;
+
+/* A dense row-major device tensor.  `stride` is in elements. */
+typedef struct {
+  void* data;
+  int32_t dtype; /* ittt_dtype */
+  int32_t ndim;  /* 1..4 */
+  int64_t shape[4];
+  int64_t stride[4];
+} ittt_tensor;
+
+/*
+ * Options for ittt_forward_ex.  Zero-initialise and set what you need; every
+ * pointer may be NULL.
+ *
+ *   pad_mode   ittt_pad_mode for the convolution boundary.
+ *   state_in   fp32 [B,d,f]: per-sequence initial fast weight.  Replaces
+ *              W_down0 (which may then be NULL) -- continues a stream of
+ *              chunks from a state returned by an earlier call.
+ *   state_out  fp32 [B,d,f]: receives W_n, the fast weight after the LAST
+ *              chunk's update (an update the output itself never needs).
+ *   z_buf      bf16 [B,T,f]: caller buffer used as the Z scratch; after the
+ *              call it holds Z.  Lets tests inspect the intermediate.
+ *   vhat_buf   bf16 [B,T,d]: same for Vhat.
+ *   snap_buf   bf16 [B,n,d,f] (n = T/chunk): same for the bf16 snapshots
+ *              W_0 .. W_{n-1} that the apply step reads.
+ *   workspace  device scratch of workspace_bytes >= ittt_workspace_bytes(...)
+ *              (256-byte aligned); when given, nothing is allocated.
+ *   events     profiling: NULL, or ITTT_NUM_PHASES + 1 cudaEvent_t handles.
+ *              events[0] is recorded on `stream` before the first kernel and
+ *              events[k] after phase k-1 (ittt_phase order), so each
+ *              consecutive pair brackets one phase on the device timeline.
+ *              A phase with nothing to do records its event all the same.
+ */
+typedef struct {
+  int32_t pad_mode;
+  int32_t reserved0;
+  const ittt_tensor* state_in;
+  ittt_tensor* state_out;
+  ittt_tensor* z_buf;
+  ittt_tensor* vhat_buf;
+  ittt_tensor* snap_buf;
+  void* workspace;
+  size_t workspace_bytes;
+  void* const* events;
+} ittt_opts;
+
+/* Kernel phases of one forward call, in launch order. */
+typedef enum {
+  ITTT_PHASE_CONV = 0,      /* depthwise three-tap conv of X0 (CUDA cores) */
+  ITTT_PHASE_TARGET = 1,    /* Vhat = Xc W_target^T (tensor cores) */
+  ITTT_PHASE_GATEUP = 2,    /* Z = SiLU(H W_gate^T) * (H W_up^T) (tensor cores) */
+  ITTT_PHASE_SNAPSHOT0 = 3, /* bf16 copy of the initial fast weight */
+  ITTT_PHASE_UPDATE = 4,    /* prefix walk of Vhat^T Z, snapshots W_1..W_{n-1} */
+  ITTT_PHASE_APPLY = 5      /* O_[i] = Z_[i] W_i^T (tensor cores) */
+} ittt_phase;
+#define ITTT_NUM_PHASES 6
+
+/*
+ * One forward pass of the layer over a batch of B independent sequences,
+ * each starting from W_down0 (pages: Method §1 eq. (1)-(4), §2 eq. (5)-(6),
+ * §3 three-stage parallel form).  eta is the fast-weight learning rate;
+ * chunk is C.  out [B,T,d] receives O in its own dtype (bf16 or fp32).
+ * Arithmetic: bf16 operands, fp32 accumulation, fp32 fast-weight state;
+ * Z, Vhat and the per-chunk weight snapshots are rounded to bf16 (nearest
+ * even) before they enter a tensor-core contraction.
+ */
+ITTT_API ittt_status ittt_forward(const ittt_tensor* H, const ittt_tensor* X0,
+                         const ittt_tensor* W_gate, const ittt_tensor* W_up,
+                         const ittt_tensor* W_down0,
+                         const ittt_tensor* W_target,
+                         const ittt_tensor* conv_w, float eta, int64_t chunk,
+                         ittt_tensor* out, ittt_stream_t stream);
+
+/* ittt_forward with options (see ittt_opts).  opts may be NULL. */
+ITTT_API ittt_status ittt_forward_ex(const ittt_tensor* H, const ittt_tensor* X0,
+                            const ittt_tensor* W_gate,
+                            const ittt_tensor* W_up,
+                            const ittt_tensor* W_down0,
+                            const ittt_tensor* W_target,
+                            const ittt_tensor* conv_w, float eta,
+                            int64_t chunk, ittt_tensor* out,
+                            ittt_stream_t stream, const ittt_opts* opts);
+
+/*
+ * Bytes of device scratch one call needs for these sizes when the caller
+ * supplies no z_buf / vhat_buf / snap_buf (0 if the sizes are unsupported).
+ */
+ITTT_API size_t ittt_workspace_bytes(int64_t B, int64_t T, int64_t d, int64_t f,
+                            int64_t chunk);
+
+/*
+ * Synchronises `stream`, then reports any device-side failure recorded by
+ * this library's kernels on the current device since the previous call
+ * (ITTT_ERR_TIMEOUT when a bounded wait ran out) or a pending CUDA error
+ * (ITTT_ERR_CUDA).  Clears the recorded failure.
+ */
+ITTT_API ittt_status ittt_stream_status(ittt_stream_t stream);
+
+/* Message for the last failure on the calling thread ("" if none).  Valid
+ * until the next call into this library on the same thread. */
+ITTT_API const char* ittt_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+ITTT_API int32_t ittt_version(void);
+
+/*
+ * Kernel launches one ittt_forward / ittt_forward_ex call makes for these
+ * sizes with default options (for launch accounting; 0 if unsupported).
+ */
+ITTT_API int32_t ittt_launch_count(int64_t B, int64_t T, int64_t d, int64_t f,
+                          int64_t chunk);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ITTT_H_ */

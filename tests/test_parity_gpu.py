@@ -1,0 +1,269 @@
+"""GPU path vs the fp64 oracle, through the C-ABI (libittt.so).
+
+Tolerance (the layer's stated bar): relative Frobenius error <= 5e-3 and
+max elementwise error <= 2e-2 * max|reference|, on the same seeded inputs
+(bf16 values widened exactly for the oracle).  The same bar is applied to
+each exported intermediate (Z, Vhat, weight snapshots): they are bf16
+roundings of exact values, so their error is about 1.5e-3 rms.
+
+Small and ragged shapes are compared element by element over the whole
+output.  The full-size workloads are too slow for the CPU oracle, so there
+the oracle evaluates sampled entries one by one (Z, Vhat, the fast-weight
+state W_i at every chunk boundary, first-chunk output rows), and every other
+output row sampled is checked against the identity O_[i] = Z_[i] W_i^T on the
+kernel's own bf16 operands.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunk_wise_weight_gb300 import config_inputs, ittt, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+REL_FRO = 5e-3
+MAX_RATIO = 2e-2
+
+
+def rel_fro(got, ref):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def max_ratio(got, ref):
+    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-300))
+
+
+def assert_parity(got, ref, what):
+    rf, mr = rel_fro(got, ref), max_ratio(got, ref)
+    assert rf <= REL_FRO and mr <= MAX_RATIO, f"{what}: rel_fro={rf:.3e} max_ratio={mr:.3e}"
+
+
+def to_device(inp, dev, w0_dtype=torch.bfloat16):
+    g = {k: inp[k].to(dev, torch.bfloat16) for k in ("H", "X0", "W_gate", "W_up", "W_target")}
+    g["W_down0"] = inp["W_down0"].to(dev, w0_dtype)
+    g["conv_w"] = inp["conv_w"].to(dev, torch.float32)
+    return g
+
+
+def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
+        state_in=None, want_state=False):
+    B, T, d = g["H"].shape
+    f = g["W_gate"].shape[0]
+    dev = g["H"].device
+    kw = {}
+    if intermediates:
+        kw["z_buf"] = torch.empty(B, T, f, dtype=torch.bfloat16, device=dev)
+        kw["vhat_buf"] = torch.empty(B, T, d, dtype=torch.bfloat16, device=dev)
+        kw["snap_buf"] = torch.empty(B, T // C, d, f, dtype=torch.bfloat16, device=dev)
+    if want_state:
+        kw["state_out"] = torch.empty(B, d, f, dtype=torch.float32, device=dev)
+    if state_in is not None:
+        kw["state_in"] = state_in
+    out = ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"],
+                       None if state_in is not None else g["W_down0"], g["W_target"],
+                       g["conv_w"], eta, C, out_dtype=out_dtype, pad_mode=pad_mode, **kw)
+    ittt.stream_status()
+    res = {"O": out}
+    res.update(kw)
+    return res
+
+
+def host(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+# --------------------------------------------------------------------------
+# Whole-output parity at sizes the oracle finishes in seconds
+# --------------------------------------------------------------------------
+
+SHAPES = [
+    # B, T, d, f, C, eta
+    (1, 256, 64, 256, 64, 0.05),     # the tiny named workload's shape
+    (2, 512, 200, 584, 128, 0.05),   # ragged d (partial N tile) and f (odd pair)
+    (1, 1024, 320, 1000, 256, 0.02), # several K blocks, ragged K tail in apply
+    (3, 384, 136, 264, 192, 0.1),    # chunk not a multiple of the 128-row tile
+    (1, 256, 64, 256, 256, 0.3),     # one chunk: no update at all
+    (2, 640, 72, 136, 320, 0.07),    # tiny d and f, two chunks
+]
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", SHAPES)
+def test_full_parity_with_intermediates(cuda_device, B, T, d, f, C, eta):
+    inp = make_inputs(B, T, d, f, seed=100 + T + d)
+    ref = oracle.forward(inp, eta, C, want_z=True, want_vhat=True, want_states=True)
+    got = run(to_device(inp, cuda_device), eta, C, intermediates=True)
+    assert_parity(host(got["z_buf"]), ref["Z"], "Z")
+    assert_parity(host(got["vhat_buf"]), ref["Vhat"], "Vhat")
+    n = T // C
+    assert_parity(host(got["snap_buf"]), ref["states"][:, :n], "snapshots W_0..W_{n-1}")
+    assert_parity(host(got["O"]), ref["O"], "O")
+
+
+def test_tiny_named_workload(cuda_device):
+    cfg, inp = config_inputs(0)
+    ref = oracle.forward(inp, cfg["eta"], cfg["C"])
+    got = run(to_device(inp, cuda_device), cfg["eta"], cfg["C"])
+    assert_parity(host(got["O"]), ref["O"], "O")
+    # Information only: error against the oracle on the unrounded fp32 inputs.
+    _, raw = config_inputs(0, round_bf16=False)
+    raw_ref = oracle.forward(raw, cfg["eta"], cfg["C"])
+    print(f"vs unrounded fp32 inputs: rel_fro={rel_fro(host(got['O']), raw_ref['O']):.3e}")
+
+
+@pytest.mark.parametrize("pad_mode", [ittt.PAD_CHUNK, ittt.PAD_SEQUENCE])
+def test_pad_modes(cuda_device, pad_mode):
+    B, T, d, f, C, eta = 2, 512, 128, 384, 128, 0.05
+    inp = make_inputs(B, T, d, f, seed=7)
+    ref = oracle.forward(inp, eta, C, pad_mode=pad_mode, want_vhat=True)
+    got = run(to_device(inp, cuda_device), eta, C, pad_mode=pad_mode, intermediates=True)
+    assert_parity(host(got["vhat_buf"]), ref["Vhat"], "Vhat")
+    assert_parity(host(got["O"]), ref["O"], "O")
+
+
+def test_fp32_output_and_fp32_initial_weight(cuda_device):
+    B, T, d, f, C, eta = 1, 512, 192, 320, 128, 0.05
+    inp = make_inputs(B, T, d, f, seed=8)
+    inp["W_down0"] = inp["W_down0"] * 1.0  # fp32 values, not bf16-representable below
+    inp["W_down0"] += torch.randn(d, f, generator=torch.Generator().manual_seed(3)) * 1e-4
+    ref = oracle.forward(inp, eta, C, want_states=True)
+    g = to_device(inp, cuda_device, w0_dtype=torch.float32)
+    got = run(g, eta, C, out_dtype=torch.float32, intermediates=True)
+    assert got["O"].dtype == torch.float32
+    assert_parity(host(got["O"]), ref["O"], "O (fp32 out)")
+    assert_parity(host(got["snap_buf"]), ref["states"][:, :T // C], "snapshots")
+
+
+def test_state_out_and_streaming_continuation(cuda_device):
+    """state_out returns W_n (after the last chunk's update); feeding it back
+    as state_in continues the sequence exactly where it stopped (chunk-edge
+    padding makes the split at a chunk boundary exact)."""
+    B, T, d, f, C, eta = 2, 1024, 128, 256, 128, 0.03
+    inp = make_inputs(B, T, d, f, seed=9)
+    ref = oracle.forward(inp, eta, C, want_states=True)
+    g = to_device(inp, cuda_device)
+    half = T // 2
+    first = {k: (v[:, :half].contiguous() if k in ("H", "X0") else v) for k, v in g.items()}
+    second = {k: (v[:, half:].contiguous() if k in ("H", "X0") else v) for k, v in g.items()}
+    a = run(first, eta, C, want_state=True)
+    assert_parity(host(a["state_out"]), ref["states"][:, half // C], "state after first half")
+    b = run(second, eta, C, state_in=a["state_out"], want_state=True)
+    assert_parity(host(b["state_out"]), ref["states"][:, T // C], "final state")
+    O = np.concatenate([host(a["O"]), host(b["O"])], axis=1)
+    assert_parity(O, ref["O"], "O across two calls")
+
+
+# --------------------------------------------------------------------------
+# Structural properties, bit-exact on the GPU path
+# --------------------------------------------------------------------------
+
+def test_deterministic_and_plain_entry_point_identical(cuda_device):
+    B, T, d, f, C, eta = 2, 512, 256, 512, 128, 0.05
+    g = to_device(make_inputs(B, T, d, f, seed=10), cuda_device)
+    o1 = run(g, eta, C)["O"]
+    o2 = run(g, eta, C, intermediates=True)["O"]
+    o3 = torch.empty_like(o1)
+    ittt.forward_plain(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                       g["conv_w"], eta, C, o3)
+    ittt.stream_status()
+    assert torch.equal(o1, o2) and torch.equal(o1, o3)
+
+
+@pytest.mark.parametrize("which", ["H", "X0"])
+@pytest.mark.parametrize("p", [0, 200, 255, 256, 511])
+def test_causality_bitwise(cuda_device, which, p):
+    """Changing H or X0 at token p leaves every output row t < p unchanged."""
+    B, T, d, f, C, eta = 1, 768, 128, 256, 256, 0.05
+    inp = make_inputs(B, T, d, f, seed=11)
+    g = to_device(inp, cuda_device)
+    base = run(g, eta, C)["O"]
+    g2 = dict(g)
+    g2[which] = g[which].clone()
+    g2[which][0, p] += 2.0
+    new = run(g2, eta, C)["O"]
+    assert torch.equal(new[0, :p], base[0, :p])
+    assert not torch.equal(new[0, p:], base[0, p:])
+
+
+def test_batch_rows_independent_bitwise(cuda_device):
+    B, T, d, f, C, eta = 3, 512, 128, 256, 128, 0.05
+    g = to_device(make_inputs(B, T, d, f, seed=12), cuda_device)
+    full = run(g, eta, C)["O"]
+    for b in range(B):
+        one = {k: (v[b:b + 1].contiguous() if k in ("H", "X0") else v) for k, v in g.items()}
+        assert torch.equal(run(one, eta, C)["O"][0], full[b])
+
+
+def test_eta_zero_is_gated_mlp(cuda_device):
+    B, T, d, f, C = 1, 512, 128, 384, 128
+    inp = make_inputs(B, T, d, f, seed=13)
+    ref = oracle.forward(inp, 0.0, C)
+    got = run(to_device(inp, cuda_device), 0.0, C)
+    assert_parity(host(got["O"]), ref["O"], "O (eta = 0)")
+
+
+def test_status_and_argument_errors_on_device(cuda_device):
+    g = to_device(make_inputs(1, 256, 64, 256, seed=14), cuda_device)
+    with pytest.raises(ittt.IttError) as e:
+        ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                     g["conv_w"], 0.1, 100)
+    assert e.value.status == ittt.ERR_INVALID_ARG
+    ittt.stream_status()  # nothing recorded
+
+
+# --------------------------------------------------------------------------
+# Full-size named workloads: sampled entries against the oracle
+# --------------------------------------------------------------------------
+
+def _sampled_checks(index, device, n_state_pairs=24, n_rows=6):
+    cfg, inp = config_inputs(index)
+    B, T, d, f, C, eta = cfg["B"], cfg["T"], cfg["d"], cfg["f"], cfg["C"], cfg["eta"]
+    n = T // C
+    g = to_device(inp, device)
+    got = run(g, eta, C, intermediates=True)
+    plain = torch.empty_like(got["O"])
+    ittt.forward_plain(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                       g["conv_w"], eta, C, plain)
+    ittt.stream_status()
+    assert torch.equal(plain, got["O"]), "bench launch path differs from the checked one"
+    rng = np.random.default_rng(1000 + index)
+    for b in sorted({0, B - 1}):
+        H, X0 = inp["H"][b], inp["X0"][b]
+        # tokens at chunk edges and at random
+        t = np.concatenate([[0, C - 1, C, T - 1], rng.integers(0, T, 60)])
+        j = np.concatenate([[0, f - 1, f // 2, 1], rng.integers(0, f, 60)])
+        m = np.concatenate([[0, d - 1, d // 2, 1], rng.integers(0, d, 60)])
+        zg = host(got["z_buf"][b][torch.as_tensor(t), torch.as_tensor(j)])
+        assert_parity(zg, oracle.z_entries(H, inp["W_gate"], inp["W_up"], t, j), f"Z[b={b}]")
+        vg = host(got["vhat_buf"][b][torch.as_tensor(t), torch.as_tensor(m)])
+        assert_parity(vg, oracle.vhat_entries(X0, inp["conv_w"], inp["W_target"], C, t, m),
+                      f"Vhat[b={b}]")
+        # fast-weight state at every chunk boundary
+        sm, sj = m[:n_state_pairs], j[:n_state_pairs]
+        ws = oracle.state_entries(H, X0, inp["W_gate"], inp["W_up"], inp["W_down0"],
+                                  inp["W_target"], inp["conv_w"], eta, C, sm, sj)
+        sg = host(got["snap_buf"][b][:, torch.as_tensor(sm), torch.as_tensor(sj)]).T
+        assert_parity(sg, ws[:, :n], f"snapshots[b={b}]")
+        # first-chunk output rows, exactly from the oracle
+        rows = np.array([0, 1, C // 2, C - 1][:n_rows])
+        og = host(got["O"][b][torch.as_tensor(rows)])
+        assert_parity(og, oracle.first_chunk_rows(H, inp["W_gate"], inp["W_up"],
+                                                  inp["W_down0"], rows), f"O chunk 0 [b={b}]")
+        # later rows: O_[i] = Z_[i] W_i^T on the kernel's own bf16 operands
+        for tok in (C, T // 2 + 3, T - 1):
+            i = tok // C
+            z = host(got["z_buf"][b][tok])
+            w = host(got["snap_buf"][b][i])
+            assert_parity(host(got["O"][b][tok]), w @ z, f"O row {tok} [b={b}]")
+
+
+@pytest.mark.parametrize("index", [1, 2])
+def test_named_workload_sampled(cuda_device, index):
+    _sampled_checks(index, cuda_device)
+
+
+@pytest.mark.parametrize("index", [3, 4])
+def test_named_workload_sampled_large(cuda_device, index):
+    _sampled_checks(index, cuda_device, n_state_pairs=12)
