@@ -1,0 +1,344 @@
+#!/usr/bin/env python
+"""Benchmark: In-Place TTT fast-weight layer tokens/s on GB300.
+
+One step = one ittt_forward call over one batch of synthetic inputs (the whole
+hot path: conv, target GEMM, gate/up GEMM, snapshot 0, update walk, apply).
+Default workload: the Qwen3-4B-shaped layer, B=2 x T=32768, d=2560,
+d_ff=9728, C=2048, eta=0.01 (bf16 inputs, fp32 state).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 run under torchrun: every rank processes its own batch of
+sequences (independent fast-weight states, no data-path collective) and
+value = all ranks' tokens / the slowest rank's time (weak scaling).
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead (rank 0
+only; other ranks exit at once).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TTT-MLP tokens/s per layer (d2560/ff9728, 32k ctx); % of GB300 bf16 peak"
+DEFAULT_CONFIG = 2
+PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--cpu-tokens", type=int, default=1024,
+                    help="tokens of the CPU-baseline sample (two chunks)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    return dict(PEAK_FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4)
+                          if r[5 + k].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def phase_model(B, T, d, f, C):
+    """Algorithmic work per phase: ('tensor', FLOPs) or ('hbm', bytes)."""
+    n = T // C
+    return {
+        "conv": ("hbm", 2.0 * B * T * d * 2 + d * 3 * 4),
+        "target": ("tensor", 2.0 * B * T * d * d),
+        "gateup": ("tensor", 4.0 * B * T * d * f),
+        "snapshot0": ("hbm", 1.0 * d * f * 2 + B * d * f * 2),
+        "update": ("tensor", 2.0 * B * (T - C) * d * f),
+        "apply": ("tensor", 2.0 * B * T * d * f),
+        "_n": n,
+    }
+
+
+def init_dist(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = init_dist(args)
+    if rank != 0:
+        return 0
+    import oracle
+    from chunk_wise_weight_gb300 import CONFIGS, make_inputs
+    cfg = CONFIGS[args.config]
+    S = max(128, min(256, cfg["T"]))
+    Cs = S // 2
+    inp = make_inputs(1, S, cfg["d"], cfg["f"], seed=1234 + args.config)
+    for _ in range(args.warmup):
+        oracle.forward(inp, cfg["eta"], Cs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(inp, cfg["eta"], Cs)
+    dt = time.perf_counter() - t0
+    tok_s = S * args.steps / dt
+    cores = oracle.num_threads()
+    sample = (f"fp64 oracle, one sequence of {S} tokens in two chunks of {Cs} at "
+              f"d={cfg['d']}, d_ff={cfg['f']} per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg["name"], "B": cfg["B"], "T": cfg["T"], "d": cfg["d"],
+                   "f": cfg["f"], "C": cfg["C"], "eta": cfg["eta"]},
+        "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(cfg, index, tokens):
+    import oracle
+    from chunk_wise_weight_gb300 import make_inputs
+    S = max(128, tokens)
+    Cs = S // 2
+    inp = make_inputs(1, S, cfg["d"], cfg["f"], seed=1234 + index)
+    t0 = time.perf_counter()
+    oracle.forward(inp, cfg["eta"], Cs)
+    dt = time.perf_counter() - t0
+    return {"value": S / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"fp64 oracle on one sequence of {S} tokens in two chunks of {Cs} at "
+                       f"d={cfg['d']}, d_ff={cfg['f']} ({dt:.1f} s)")}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    from chunk_wise_weight_gb300 import CONFIGS, counted_flops, ittt, make_inputs
+    from chunk_wise_weight_gb300 import build as lib_build
+    from chunk_wise_weight_gb300.shard import barrier, max_over_ranks, shard_range
+
+    world, rank, local = init_dist(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    cfg = CONFIGS[args.config]
+    B, T, d, f, C, eta = cfg["B"], cfg["T"], cfg["d"], cfg["f"], cfg["C"], cfg["eta"]
+    peaks, peak_src = load_peaks()
+
+    # CPU baseline first (rank 0, one GPU only), before the device is busy.
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, args.config, args.cpu_tokens)
+
+    lib_build.build()
+    ittt.load()
+
+    # Inputs: the layer's weights are shared; the global batch is B * world
+    # sequences and each rank draws and runs its own contiguous share.
+    first, last = shard_range(B * world, world, rank)
+    assert last - first == B
+    inp = make_inputs(B, T, d, f, seed=1234 + args.config)
+    if first > 0:
+        g = torch.Generator().manual_seed(1234 + args.config + 1000 * first)
+        inp["H"] = torch.randn(B, T, d, generator=g).to(torch.bfloat16).float()
+        inp["X0"] = torch.randn(B, T, d, generator=g).to(torch.bfloat16).float()
+    bf = torch.bfloat16
+    H = inp["H"].to(dev, bf)
+    X0 = inp["X0"].to(dev, bf)
+    Wg, Wu = inp["W_gate"].to(dev, bf), inp["W_up"].to(dev, bf)
+    W0, Wt = inp["W_down0"].to(dev, bf), inp["W_target"].to(dev, bf)
+    cw = inp["conv_w"].to(dev, torch.float32)
+    out = torch.empty(B, T, d, dtype=bf, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, stream=stream, events=events)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    ittt.stream_status(stream)
+
+    nph = len(ittt.PHASES)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)]
+          for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(dev)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(ev[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(dev)
+    ittt.stream_status(stream)
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
+    ms_per_step = elapsed_ms / args.steps
+    tokens = B * T * world * args.steps
+    value = tokens / (elapsed_ms / 1e3)
+
+    # Per-phase device durations from the events between launches.
+    model = phase_model(B, T, d, f, C)
+    phases = {}
+    for p, name in enumerate(ittt.PHASES):
+        ms = sum(ev[k][p].elapsed_time(ev[k][p + 1]) for k in range(args.steps)) / args.steps
+        kind, work = model[name]
+        entry = {"ms": round(ms, 4), "share": round(ms / ms_per_step, 4)}
+        if kind == "tensor":
+            entry["tflops"] = round(work / (ms * 1e-3) / 1e12, 1) if ms > 0 else None
+        else:
+            entry["gbs"] = round(work / (ms * 1e-3) / 1e9, 1) if ms > 0 else None
+        phases[name] = entry
+    dominant = max(ittt.PHASES, key=lambda nm: phases[nm]["ms"])
+    kind, work = model[dominant]
+    dom_ms = phases[dominant]["ms"]
+    if kind == "tensor":
+        achieved = work / (dom_ms * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops_sustained"])
+        roof = {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": None, "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                "frac_of_burst": round(achieved / float(peaks["bf16_tflops"]), 4),
+                "flops_per_launch": work}
+    else:
+        achieved = work / (dom_ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_kind": f"hbm_gbs ({peak_src})", "bytes_per_launch": work}
+    F = counted_flops(B, T, d, f, C)
+    layer_tflops = F / (ms_per_step * 1e-3) / 1e12
+
+    # End to end through the public API with host buffers: every step copies
+    # this step's activations (H, X0) from pinned host memory to the device,
+    # runs the layer and reads O back into pinned host memory.
+    e2e = None
+    if not args.no_e2e:
+        H_h = inp["H"].to(bf).pin_memory()
+        X0_h = inp["X0"].to(bf).pin_memory()
+        O_h = torch.empty(B, T, d, dtype=bf).pin_memory()
+        for _ in range(2):
+            H.copy_(H_h, non_blocking=True)
+            X0.copy_(X0_h, non_blocking=True)
+            step()
+            O_h.copy_(out, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dev)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            H.copy_(H_h, non_blocking=True)
+            X0.copy_(X0_h, non_blocking=True)
+            step()
+            O_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        e2e = {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": H_h.numel() * 2 + X0_h.numel() * 2,
+               "d2h_bytes_per_step": O_h.numel() * 2,
+               "note": "per step: H2D of H and X0 (pinned), ittt_forward, D2H of O; "
+                       "weights stay resident"}
+        ittt.stream_status(stream)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg["name"], "B": B, "T": T, "d": d, "f": f, "C": C,
+                       "eta": eta, "chunks": T // C, "parallelism": f"batch x{world} (replicas)",
+                       "l2": "inputs larger than L2: H+X0 and Z are several GB per step"},
+            "layer_tflops": round(layer_tflops, 1),
+            "layer_frac_of_peak": {
+                "bf16_tflops": round(layer_tflops / float(peaks["bf16_tflops"]), 4),
+                "bf16_tflops_sustained":
+                    round(layer_tflops / float(peaks["bf16_tflops_sustained"]), 4),
+                "peaks": peak_src},
+            "counted_tflop_per_step": round(F / 1e12, 4),
+            "roofline": roof,
+            "phases": phases,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": ittt.launch_count(B, T, d, f, C) * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -67,7 +67,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
+    # Shared cudart: the library and torch use one runtime instance, so
+    # stream and event handles pass between them unchanged.
+    cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-Xlinker",
+                           "-rpath=" + os.path.join(os.path.dirname(os.path.dirname(nvcc)), "lib64"),
+                           "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")

@@ -153,6 +153,9 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
     if events is not None:
         if len(events) != len(PHASES) + 1:
             raise ValueError(f"events needs {len(PHASES) + 1} entries")
+        for e in events:  # torch creates the CUDA event on its first record
+            if not e.cuda_event:
+                e.record(torch.cuda.current_stream(H.device) if stream is None else stream)
         ev_arr = (ctypes.c_void_p * len(events))(*[int(e.cuda_event) for e in events])
         opts.events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
     s = _stream_handle(stream, H.device)
