@@ -334,7 +334,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
                              int(d), int(chunk), int(o.pad_mode))) != cudaSuccess)
     return cuda_fail(e, "conv launch");
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
-  if ((e = ittt::launch_target(env, tm_xc, tm_wt, vhat, int(M), int(d))) != cudaSuccess)
+  if ((e = ittt::launch_target(env, tm_xc, tm_wt, vhat, eta, int(M), int(d))) != cudaSuccess)
     return cuda_fail(e, "target launch");
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
   if ((e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, z, int(M), int(f), int(d))) != cudaSuccess)
@@ -352,7 +352,6 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   ua.C = int(chunk);
   ua.n = int(n);
   ua.n_upd = o.state_out ? int(n) : int(n - 1);
-  ua.eta = eta;
   ua.w0 = w0;
   ua.w0_fp32 = w0_fp32;
   ua.w0_bstride = w0_bstride;

@@ -25,6 +25,7 @@ struct ApplyParams {
 struct ApplySched {
   using Params = ApplyParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, false);
+  static constexpr bool kPreload = false;
 
   const Params& p;
   int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0;

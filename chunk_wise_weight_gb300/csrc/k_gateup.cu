@@ -28,6 +28,7 @@ struct GateUpParams {
 struct GateUpSched {
   using Params = GateUpParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, false);
+  static constexpr bool kPreload = false;
 
   const Params& p;
   int m0 = 0, n0 = 0, acc = 0;

@@ -7,7 +7,11 @@
 // 8 channels of a token row, 128-bit loads of the rows t-1, t, t+1, fp32
 // arithmetic, one rounding to bf16 (the tensor-core operand).  Taps outside
 // the current chunk (or, in sequence mode, outside the sequence) read zero.
-// The projection is a tcgen05 GEMM over the result.
+// The projection is a tcgen05 GEMM over the result.  Its epilogue scales by
+// the fast-weight learning rate before the bf16 rounding, so the tensor
+// stores eta * Vhat: the update's left operand with eta folded in (the
+// identity eta K^T(KW - V) = K~^T(K~W - V~), K~ = sqrt(eta) K, of the "ViT^3"
+// review's design insights, here with the whole eta on the value side).
 #include "kernels.h"
 #include "pipeline.cuh"
 
@@ -70,7 +74,8 @@ __global__ void __launch_bounds__(256)
 struct TargetParams {
   CUtensorMap tm_xc;  // Xc       [M, d]  box {64, 128}
   CUtensorMap tm_wt;  // W_target [d, d]  box {64, 256}
-  __nv_bfloat16* vhat;
+  __nv_bfloat16* vhat;  // eta * Vhat [M, d]
+  float eta;
   int M, d;
   int m_tiles, n_tiles, kblocks, raster;
 };
@@ -78,6 +83,7 @@ struct TargetParams {
 struct TargetSched {
   using Params = TargetParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, false);
+  static constexpr bool kPreload = false;
 
   const Params& p;
   int m0 = 0, n0 = 0, acc = 0;
@@ -121,7 +127,8 @@ struct TargetSched {
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+        pk[j] = pack_bf16x2(p.eta * __uint_as_float(v[2 * j]),
+                            p.eta * __uint_as_float(v[2 * j + 1]));
       if (row_ok) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -154,11 +161,12 @@ cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const flo
 }
 
 cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_xc, const CUtensorMap& tm_wt,
-                          __nv_bfloat16* vhat, int M, int d) {
+                          __nv_bfloat16* vhat, float eta, int M, int d) {
   TargetParams p;
   p.tm_xc = tm_xc;
   p.tm_wt = tm_wt;
   p.vhat = vhat;
+  p.eta = eta;
   p.M = M;
   p.d = d;
   p.m_tiles = (M + kBM - 1) / kBM;

@@ -4,15 +4,17 @@
 // sum of Method §3 stage 2, "In-Place TTT" reading notes 实现细节).
 //
 // The per-chunk deltas do not depend on W (the loss is linear in it), so
-// the prefix sum S_i = sum_{j<i} delta_j is one long contraction over the
-// tokens of a sequence.  A work unit owns a 128 (d_model) x 512 (d_ff)
-// block of one sequence's state, split into two 128 x 256 halves whose fp32
-// running sums live in the two TMEM accumulators for the whole walk.  The
-// MMAs alternate halves chunk by chunk: while the tensor core accumulates
-// chunk i of one half, the epilogue reads the other half's sum at its chunk
-// boundary and writes the bf16 snapshot W_{i+1} = bf16(W_0 + eta * S_{i+1})
-// that the apply kernel reads.  The fp32 state never goes to HBM unless the
-// caller asks for the final state.
+// the state after chunk i is W_0 plus one long contraction over the tokens
+// of chunks 0..i.  A work unit owns a 128 (d_model) x 512 (d_ff) block of
+// one sequence's state, split into two 128 x 256 halves.  Each half's fp32
+// state lives in one TMEM accumulator for the whole walk: the epilogue
+// warps load W_0 into it (tcgen05.st) and the MMAs accumulate
+// (eta Vhat_[i])^T Z_[i] on top, eta having been folded into Vhat by the
+// target kernel.  The MMAs alternate halves chunk by chunk: while the tensor
+// core accumulates chunk i of one half, the epilogue reads the other half's
+// state at its chunk boundary and writes the bf16 snapshot W_{i+1} that the
+// apply kernel reads.  The fp32 state reaches HBM only when the caller asks
+// for the final state.
 //
 // Both operands are read MN-major: the contraction index (token) is the row
 // index of Vhat [T, d] and of Z [T, f].  A 64-token stage holds, per operand,
@@ -26,14 +28,13 @@ namespace {
 constexpr uint32_t kMnBoxBytes = 64 * 64 * 2;  // one {64 cols, 64 tokens} box
 
 struct UpdateParams {
-  CUtensorMap tm_v;  // Vhat [B*T, d]  box {64, 64}
-  CUtensorMap tm_z;  // Z    [B*T, f]  box {64, 64}
+  CUtensorMap tm_v;  // eta*Vhat [B*T, d]  box {64, 64}
+  CUtensorMap tm_z;  // Z        [B*T, f]  box {64, 64}
   const void* w0;
   int w0_fp32;
   int64_t w0_bstride;
   __nv_bfloat16* snap;  // [B, n, d, f]
   float* state_out;     // [B, d, f] or nullptr
-  float eta;
   int B, T, d, f, C, n, n_upd;
   int mt, np, kb_per_chunk;
 };
@@ -41,6 +42,7 @@ struct UpdateParams {
 struct UpdateSched {
   using Params = UpdateParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true, true);
+  static constexpr bool kPreload = true;
 
   const Params& p;
   int b = 0, m0 = 0, nbase = 0, halves = 1;
@@ -57,9 +59,10 @@ struct UpdateSched {
     halves = (nbase + kBN < p.f) ? 2 : 1;
   }
   __device__ int num_segments() const { return p.n_upd * halves; }
+  __device__ int unit_accs() const { return halves; }
   __device__ int seg_acc(int s) const { return s % halves; }
   __device__ int seg_kblocks(int) const { return p.kb_per_chunk; }
-  __device__ bool seg_fresh(int s) const { return s < halves; }
+  __device__ bool seg_fresh(int) const { return false; }  // starts from the preloaded W_0
 
   __device__ void load(int s, int kb, void* a, void* bt, uint64_t* bar) const {
     const int i = s / halves;
@@ -82,6 +85,47 @@ struct UpdateSched {
     return sdesc_sw128(base + uint32_t(k) * 2048u, kMnBoxBytes, 1024u);
   }
 
+  // W_0 rows of this half into its accumulator (zeros outside the state).
+  __device__ void preload(int h, int row, uint32_t trow) const {
+    const int m = m0 + row;
+    const bool row_ok = m < p.d;
+    const int n0 = nbase + h * kBN;
+    const size_t off = size_t(b) * size_t(p.w0_bstride) + size_t(row_ok ? m : 0) * size_t(p.f);
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 32) {
+      uint32_t v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int col = n0 + c + 8 * q;
+        float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (row_ok && col < p.f) {
+          if (p.w0_fp32) {
+            const float4* src =
+                reinterpret_cast<const float4*>(static_cast<const float*>(p.w0) + off + col);
+            const float4 lo = __ldg(src), hi = __ldg(src + 1);
+            w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+            w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+          } else {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+                static_cast<const __nv_bfloat16*>(p.w0) + off + col));
+            const uint32_t r4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 f2 = unpack_bf16x2(r4[j]);
+              w[2 * j] = f2.x;
+              w[2 * j + 1] = f2.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[8 * q + j] = __float_as_uint(w[j]);
+      }
+      tmem_st_32cols(trow + uint32_t(c), v);
+    }
+  }
+
+  // State after chunk i of this half: snapshot W_{i+1} (bf16) and, after
+  // the last update, the fp32 state when the caller wants it.
   __device__ void epilogue(int s, int row, uint32_t trow) const {
     const int i = s / halves;
     const int h = s - i * halves;
@@ -93,9 +137,8 @@ struct UpdateSched {
                     ? p.state_out + (size_t(b) * p.d + size_t(row_ok ? m : 0)) * size_t(p.f)
                     : nullptr;
     __nv_bfloat16* snap_row =
-        p.snap + ((size_t(b) * p.n + size_t(i + 1)) * p.d + size_t(row_ok ? m : 0)) * size_t(p.f);
-    const size_t w0_off = size_t(b) * size_t(p.w0_bstride) + size_t(row_ok ? m : 0) * size_t(p.f);
-    const float eta = p.eta;
+        p.snap + ((size_t(b) * p.n + size_t(write_snap ? i + 1 : 0)) * p.d +
+                  size_t(row_ok ? m : 0)) * size_t(p.f);
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 32) {
       uint32_t v[32];
@@ -107,35 +150,17 @@ struct UpdateSched {
       for (int q = 0; q < 4; ++q) {
         const int col = n0 + c + 8 * q;
         if (col >= p.f) continue;
-        float w[8];
-        if (p.w0_fp32) {
-          const float4* src = reinterpret_cast<const float4*>(
-              static_cast<const float*>(p.w0) + w0_off + col);
-          const float4 lo = __ldg(src), hi = __ldg(src + 1);
-          w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
-          w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
-        } else {
-          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(p.w0) + w0_off + col));
-          const uint32_t r4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f2 = unpack_bf16x2(r4[j]);
-            w[2 * j] = f2.x;
-            w[2 * j + 1] = f2.y;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = fmaf(eta, __uint_as_float(v[8 * q + j]), w[j]);
         if (write_snap) {
-          *reinterpret_cast<uint4*>(snap_row + col) =
-              make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
-                         pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+          *reinterpret_cast<uint4*>(snap_row + col) = make_uint4(
+              pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+              pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+              pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+              pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
         }
         if (st != nullptr) {
-          float4* dst = reinterpret_cast<float4*>(st + col);
-          dst[0] = make_float4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_float4(w[4], w[5], w[6], w[7]);
+          uint4* dst = reinterpret_cast<uint4*>(st + col);
+          dst[0] = make_uint4(v[8 * q], v[8 * q + 1], v[8 * q + 2], v[8 * q + 3]);
+          dst[1] = make_uint4(v[8 * q + 4], v[8 * q + 5], v[8 * q + 6], v[8 * q + 7]);
         }
       }
     }
@@ -199,7 +224,6 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
   p.w0_bstride = a.w0_bstride;
   p.snap = a.snap;
   p.state_out = a.state_out;
-  p.eta = a.eta;
   p.B = a.B;
   p.T = a.T;
   p.d = a.d;

@@ -28,10 +28,11 @@ cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h,
 cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const float* conv_w,
                         __nv_bfloat16* xc, int64_t rows, int T, int d, int C, int pad_mode);
 
-// Vhat[M, d] = Xc W_target^T.  Tensor maps: Xc [M, d] box {64,128};
-// W_target [d, d] box {64,256}.
+// vhat[M, d] = eta * (Xc W_target^T), rounded once to bf16.  Tensor maps:
+// Xc [M, d] box {64,128}; W_target [d, d] box {64,256}.
 cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_xc,
-                          const CUtensorMap& tm_wt, __nv_bfloat16* vhat, int M, int d);
+                          const CUtensorMap& tm_wt, __nv_bfloat16* vhat, float eta, int M,
+                          int d);
 
 // snap[b, 0] = bf16(W_0 of sequence b) for every b.  w0 is bf16 or fp32,
 // [d, f] shared (w0_bstride = 0) or [B, d, f].
@@ -43,7 +44,6 @@ struct UpdateArgs {
   int B, T, d, f, C;
   int n;          // chunks per sequence
   int n_upd;      // updates to run: n-1, or n when the final state is wanted
-  float eta;
   const void* w0; // bf16 or fp32 initial state
   bool w0_fp32;
   int64_t w0_bstride;
@@ -52,10 +52,10 @@ struct UpdateArgs {
 };
 
 // Fast-weight update walk: for each (sequence, 128 x 512 state tile) the
-// per-chunk deltas Vhat_[i]^T Z_[i] accumulate in TMEM; after chunk i the
-// epilogue writes bf16(W_0 + eta * sum_{j<=i} delta_j) as snapshot i+1.
-// Tensor maps: Vhat [B*T, d] box {64,64}; Z [B*T, f] box {64,64} (both
-// read MN-major).
+// fp32 state starts at W_0 in TMEM and the per-chunk deltas
+// (eta Vhat_[i])^T Z_[i] accumulate onto it; after chunk i the epilogue
+// writes bf16(W_{i+1}) as snapshot i+1.  Tensor maps: eta*Vhat [B*T, d] box
+// {64,64}; Z [B*T, f] box {64,64} (both read MN-major).
 cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
                           const CUtensorMap& tm_z, const UpdateArgs& a);
 

@@ -23,8 +23,18 @@
 //   static uint64_t a_desc(uint32_t a_smem, int k16)
 //   static uint64_t b_desc(uint32_t b_smem, int k16)
 //   static constexpr uint32_t kIdesc
+//   static constexpr bool kPreload
 // Segments let one accumulator keep accumulating across several epilogue
 // reads (the fast-weight state walks the chunks of a sequence).
+//
+// With kPreload the epilogue also writes each unit's starting accumulator
+// values into TMEM before the unit's first MMA:
+//   int  unit_accs()                               accumulators the unit uses
+//   void preload(int acc, int row, uint32_t tmem_row_base)   (per thread)
+// Each MMA use of an accumulator then waits for exactly one epilogue arrival:
+// the release after the previous segment's read inside a unit, or the
+// preload at a unit's start (the last read of a unit is not released; the
+// next unit's preload stands for it).
 #pragma once
 
 #include "sm103.cuh"
@@ -141,7 +151,8 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
         const int nseg = sched.num_segments();
         for (int s = 0; s < nseg && ok; ++s) {
           const int h = sched.seg_acc(s);
-          if (!mbar_wait(&sync->acc_empty[h], (acc_use[h] & 1u) ^ 1u, abort_flag)) {
+          const uint32_t empty_parity = S::kPreload ? (acc_use[h] & 1u) : ((acc_use[h] & 1u) ^ 1u);
+          if (!mbar_wait(&sync->acc_empty[h], empty_parity, abort_flag)) {
             raise_abort(abort_flag, status, kStatusTimeout);
             ok = false;
             break;
@@ -192,6 +203,14 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
     for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++local) {
       sched.begin_unit(u, local);
       const int nseg = sched.num_segments();
+      if constexpr (S::kPreload) {
+        for (int h = 0; h < sched.unit_accs(); ++h) {
+          sched.preload(h, row, tmem + (uint32_t(quad * 32) << 16) + uint32_t(h * kBN));
+          tmem_wait_st();
+          tc_fence_before_sync();
+          mbar_arrive(&sync->acc_empty[h]);
+        }
+      }
       for (int s = 0; s < nseg; ++s) {
         const int h = sched.seg_acc(s);
         // The TMEM loads below are warp-collective: the whole warp proceeds
@@ -206,8 +225,12 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
         tc_fence_after_sync();
         const uint32_t trow = tmem + (uint32_t(quad * 32) << 16) + uint32_t(h * kBN);
         sched.epilogue(s, row, trow);
-        tc_fence_before_sync();
-        mbar_arrive(&sync->acc_empty[h]);
+        bool release = true;
+        if constexpr (S::kPreload) release = s < nseg - sched.unit_accs();
+        if (release) {
+          tc_fence_before_sync();
+          mbar_arrive(&sync->acc_empty[h]);
+        }
         ++acc_use[h];
       }
     }

@@ -98,7 +98,8 @@ typedef struct {
  *              chunk's update (an update the output itself never needs).
  *   z_buf      bf16 [B,T,f]: caller buffer used as the Z scratch; after the
  *              call it holds Z.  Lets tests inspect the intermediate.
- *   vhat_buf   bf16 [B,T,d]: same for Vhat.
+ *   vhat_buf   bf16 [B,T,d]: same for the update's left operand, which the
+ *              library stores with eta folded in: it holds eta * Vhat.
  *   snap_buf   bf16 [B,n,d,f] (n = T/chunk): same for the bf16 snapshots
  *              W_0 .. W_{n-1} that the apply step reads.
  *   workspace  device scratch of workspace_bytes >= ittt_workspace_bytes(...)
