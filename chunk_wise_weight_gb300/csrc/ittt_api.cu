@@ -369,6 +369,22 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
 
 }  // namespace
 
+namespace ittt {
+
+// Address of this library's device status word on the current device, for
+// entry points defined in other translation units (no other set-up).
+cudaError_t status_word_address(unsigned int** out) {
+  void* sym = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&sym, g_device_status);
+  if (e == cudaSuccess) *out = static_cast<unsigned int*>(sym);
+  return e;
+}
+
+// Records `msg` as the calling thread's ittt_last_error() text.
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+
+}  // namespace ittt
+
 extern "C" {
 
 ittt_status ittt_forward(const ittt_tensor* H, const ittt_tensor* X0, const ittt_tensor* W_gate,

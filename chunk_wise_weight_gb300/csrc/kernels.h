@@ -65,4 +65,8 @@ cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
                          const CUtensorMap& tm_snap, void* out, bool out_fp32, int B, int T,
                          int d, int f, int C);
 
+// Defined in ittt_api.cu, for entry points in other translation units.
+cudaError_t status_word_address(unsigned int** out);
+void set_last_error(const char* msg);
+
 }  // namespace ittt

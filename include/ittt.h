@@ -161,6 +161,33 @@ ITTT_API ittt_status ittt_forward_ex(const ittt_tensor* H, const ittt_tensor* X0
                             ittt_stream_t stream, const ittt_opts* opts);
 
 /*
+ * ittt_forward for callers that cannot allocate device memory while they
+ * run: a serving loop with a fixed, fully partitioned memory budget, a
+ * process whose device memory belongs to another framework's caching
+ * allocator, a real-time path that forbids allocation after start-up.
+ * The pages have no counterpart: this is a deployment variant of
+ * ittt_forward with the same arguments, kernels and results.
+ *
+ * It calls no allocating routine.  Its scratch lives in one library-wide
+ * device array of ITTT_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU which
+ * loads the library holds until the process exits; a call that needs more
+ * (B*T*(f + 2d)*2 + B*n*d*f*2 bytes, each part rounded up to 256) returns
+ * ITTT_ERR_UNSUPPORTED before anything is enqueued.  All calls share that
+ * array, so calls that overlap on the GPU (other streams, other threads)
+ * race: serialise them on one stream.  The first call on a device does a
+ * one-time set-up (it looks up the array's device address); make that first
+ * call before any stream capture.  Pad mode is ITTT_PAD_CHUNK.  Device-side
+ * failures are reported by ittt_stream_status().
+ */
+#define ITTT_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+ITTT_API ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_tensor* X0,
+                                          const ittt_tensor* W_gate, const ittt_tensor* W_up,
+                                          const ittt_tensor* W_down0,
+                                          const ittt_tensor* W_target,
+                                          const ittt_tensor* conv_w, float eta, int64_t chunk,
+                                          ittt_tensor* out, ittt_stream_t stream);
+
+/*
  * Bytes of device scratch one call needs for these sizes when the caller
  * supplies no z_buf / vhat_buf / snap_buf (0 if the sizes are unsupported).
  */
