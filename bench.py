@@ -48,10 +48,14 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--shape", default=None,
+                    help="B,T,d,f,C,eta instead of the named workload (profiling cases)")
     ap.add_argument("--cpu-tokens", type=int, default=1024,
                     help="tokens of the CPU-baseline sample (two chunks)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fused-conv", action="store_true",
+                    help="compute the convolution inside the target GEMM")
     return ap.parse_args()
 
 
@@ -190,7 +194,12 @@ def main():
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    cfg = CONFIGS[args.config]
+    cfg = dict(CONFIGS[args.config])
+    if args.shape:
+        vals = args.shape.split(",")
+        cfg.update(B=int(vals[0]), T=int(vals[1]), d=int(vals[2]), f=int(vals[3]),
+                   C=int(vals[4]), eta=float(vals[5]))
+        cfg["name"] = "B{B}-T{T}-d{d}-f{f}-C{C}".format(**cfg)
     B, T, d, f, C, eta = cfg["B"], cfg["T"], cfg["d"], cfg["f"], cfg["C"], cfg["eta"]
     peaks, peak_src = load_peaks()
 
@@ -221,14 +230,15 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def step(events=None):
-        ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, stream=stream, events=events)
+        ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, stream=stream, events=events,
+                     fused_conv=args.fused_conv)
 
     for _ in range(max(3, args.warmup)):
         step()
     ittt.stream_status(stream)
 
     nph = len(ittt.PHASES)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nph)]
           for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -254,7 +264,7 @@ def main():
     model = phase_model(B, T, d, f, C)
     phases = {}
     for p, name in enumerate(ittt.PHASES):
-        ms = sum(ev[k][p].elapsed_time(ev[k][p + 1]) for k in range(args.steps)) / args.steps
+        ms = sum(ev[k][2 * p].elapsed_time(ev[k][2 * p + 1]) for k in range(args.steps)) / args.steps
         kind, work = model[name]
         entry = {"ms": round(ms, 4), "share": round(ms / ms_per_step, 4)}
         if kind == "tensor":
@@ -287,35 +297,60 @@ def main():
     layer_tflops = F / (ms_per_step * 1e-3) / 1e12
 
     # End to end through the public API with host buffers: every step copies
-    # this step's activations (H, X0) from pinned host memory to the device,
-    # runs the layer and reads O back into pinned host memory.
+    # its activations (H, X0) from pinned host memory to the device, runs the
+    # layer and reads O back into pinned host memory.  Copies run on their own
+    # streams with two device buffer sets, so step k's compute overlaps the
+    # upload of step k+1 and the download of step k-1.
     e2e = None
     if not args.no_e2e:
         H_h = inp["H"].to(bf).pin_memory()
         X0_h = inp["X0"].to(bf).pin_memory()
-        O_h = torch.empty(B, T, d, dtype=bf).pin_memory()
-        for _ in range(2):
-            H.copy_(H_h, non_blocking=True)
-            X0.copy_(X0_h, non_blocking=True)
-            step()
-            O_h.copy_(out, non_blocking=True)
+        O_h = [torch.empty(B, T, d, dtype=bf).pin_memory() for _ in range(2)]
+        Hs, X0s, Os = [H, torch.empty_like(H)], [X0, torch.empty_like(X0)], [out, torch.empty_like(out)]
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        mk = lambda: [torch.cuda.Event() for _ in range(2)]  # noqa: E731
+        uploaded, computed, downloaded = mk(), mk(), mk()
+
+        def e2e_steps(count, e_start=None, e_end=None):
+            if e_start is not None:
+                e_start.record(up)
+            for k in range(count):
+                j = k % 2
+                if k >= 2:
+                    up.wait_event(computed[j])      # buffers j free again
+                with torch.cuda.stream(up):
+                    Hs[j].copy_(H_h, non_blocking=True)
+                    X0s[j].copy_(X0_h, non_blocking=True)
+                    uploaded[j].record(up)
+                stream.wait_event(uploaded[j])
+                if k >= 2:
+                    stream.wait_event(downloaded[j])  # O_j read back before reuse
+                ittt.forward(Hs[j], X0s[j], Wg, Wu, W0, Wt, cw, eta, C, Os[j], stream=stream,
+                             fused_conv=args.fused_conv)
+                computed[j].record(stream)
+                down.wait_event(computed[j])
+                with torch.cuda.stream(down):
+                    O_h[j].copy_(Os[j], non_blocking=True)
+                    downloaded[j].record(down)
+            if e_end is not None:
+                for j in range(2):
+                    up.wait_event(downloaded[j])
+                e_end.record(up)
+
+        e2e_steps(3)
+        torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(dev)
         torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for _ in range(args.steps):
-            H.copy_(H_h, non_blocking=True)
-            X0.copy_(X0_h, non_blocking=True)
-            step()
-            O_h.copy_(out, non_blocking=True)
-        e1.record(stream)
+        e2e_steps(args.steps, e0, e1)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
         e2e = {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": H_h.numel() * 2 + X0_h.numel() * 2,
-               "d2h_bytes_per_step": O_h.numel() * 2,
-               "note": "per step: H2D of H and X0 (pinned), ittt_forward, D2H of O; "
-                       "weights stay resident"}
+               "d2h_bytes_per_step": O_h[0].numel() * 2,
+               "note": "per step: H2D of H and X0 from pinned host memory, ittt_forward, D2H "
+                       "of O to pinned host memory; copies overlap compute on two buffer "
+                       "sets; weights stay resident"}
         ittt.stream_status(stream)
 
     if rank == 0:
@@ -326,6 +361,7 @@ def main():
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": cfg["name"], "B": B, "T": T, "d": d, "f": f, "C": C,
                        "eta": eta, "chunks": T // C, "parallelism": f"batch x{world} (replicas)",
+                       "conv": "fused into target GEMM" if args.fused_conv else "own kernel",
                        "l2": "inputs larger than L2: H+X0 and Z are several GB per step"},
             "layer_tflops": round(layer_tflops, 1),
             "layer_frac_of_peak": {

@@ -4,8 +4,11 @@
 // it needs (stream-ordered, from a library-private memory pool, or from a
 // caller workspace), encodes the TMA tensor maps and launches the kernels in
 // data-flow order on the caller's stream:
-//   conv3 -> target GEMM (Vhat) ; gate/up GEMM (Z) ; snapshot 0 ;
+//   conv3 (Xc) ; target GEMM (eta*Vhat) ; gate/up GEMM (Z) ; snapshot 0 ;
 //   update walk (snapshots W_1..W_{n-1}) ; apply GEMM (O).
+// With ITTT_FLAG_FUSED_CONV the target GEMM computes the conv itself.  (Run
+// beside the gate/up GEMM on a second stream, the conv slowed that GEMM by
+// more than its own 0.2 ms at the 32k-token workload, so it runs in line.)
 // No host synchronisation happens inside a forward call.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -173,7 +176,7 @@ struct Layout {
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
 
 Layout plan_workspace(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk, bool need_z,
-                      bool need_vhat, bool need_snap) {
+                      bool need_vhat, bool need_xc, bool need_snap) {
   Layout L;
   const int64_t n = T / chunk;
   size_t off = 0;
@@ -185,8 +188,10 @@ Layout plan_workspace(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
     L.vhat = off;
     off += round_up(size_t(B) * T * d * 2);
   }
-  L.xc = off;
-  off += round_up(size_t(B) * T * d * 2);
+  if (need_xc) {
+    L.xc = off;
+    off += round_up(size_t(B) * T * d * 2);
+  }
   if (need_snap) {
     L.snap = off;
     off += round_up(size_t(B) * n * d * f * 2);
@@ -230,6 +235,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if (opts) o = *opts;
   if (o.pad_mode != ITTT_PAD_CHUNK && o.pad_mode != ITTT_PAD_SEQUENCE)
     return fail(ITTT_ERR_INVALID_ARG, "pad_mode %d", int(o.pad_mode));
+  if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV))
+    return fail(ITTT_ERR_INVALID_ARG, "unknown flags 0x%x", unsigned(o.flags));
+  const bool fused = (o.flags & ITTT_FLAG_FUSED_CONV) != 0;
   if (H == nullptr || H->ndim != 3)
     return fail(ITTT_ERR_INVALID_ARG, "H: expected a [B,T,d] descriptor");
   const int64_t B = H->shape[0], T = H->shape[1], d = H->shape[2];
@@ -278,7 +286,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
 
   // Scratch.
   const Layout L = plan_workspace(B, T, d, f, chunk, o.z_buf == nullptr, o.vhat_buf == nullptr,
-                                  o.snap_buf == nullptr);
+                                  !fused, o.snap_buf == nullptr);
   ScratchGuard guard;
   uint8_t* ws = nullptr;
   if (o.workspace) {
@@ -306,11 +314,15 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
 
   // Tensor maps.
   const uint64_t M = uint64_t(B * T);
-  CUtensorMap tm_h, tm_wg, tm_wu, tm_xc, tm_wt, tm_vmn, tm_zmn, tm_zk, tm_snap;
+  CUtensorMap tm_h, tm_wg, tm_wu, tm_a, tm_wt, tm_vmn, tm_zmn, tm_zk, tm_snap;
   if ((s = make_map(&tm_h, H->data, d, M, 64, 128, "H"))) return s;
   if ((s = make_map(&tm_wg, W_gate->data, d, f, 64, 128, "W_gate"))) return s;
   if ((s = make_map(&tm_wu, W_up->data, d, f, 64, 128, "W_up"))) return s;
-  if ((s = make_map(&tm_xc, xc, d, M, 64, 128, "Xc"))) return s;
+  if (fused) {
+    if ((s = make_map(&tm_a, X0->data, d, M, 64, 130, "X0"))) return s;
+  } else if ((s = make_map(&tm_a, xc, d, M, 64, 128, "Xc"))) {
+    return s;
+  }
   if ((s = make_map(&tm_wt, W_target->data, d, d, 64, 256, "W_target"))) return s;
   if ((s = make_map(&tm_vmn, vhat, d, M, 64, 64, "Vhat"))) return s;
   if ((s = make_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
@@ -323,27 +335,36 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   const int64_t w0_bstride = o.state_in ? d * f : 0;
 
   cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(o.events);
-  auto mark = [&](int k) -> cudaError_t {
-    return ev ? cudaEventRecord(ev[k], stream) : cudaSuccess;
+  auto rec = [&](int slot, cudaStream_t st) -> cudaError_t {
+    return ev ? cudaEventRecord(ev[slot], st) : cudaSuccess;
   };
+  const float* cw = static_cast<const float*>(conv_w->data);
 
-  cudaError_t e;
-  if ((e = mark(0)) != cudaSuccess) return cuda_fail(e, "event record");
-  if ((e = ittt::launch_conv(env, static_cast<const __nv_bfloat16*>(X0->data),
-                             static_cast<const float*>(conv_w->data), xc, int64_t(M), int(T),
-                             int(d), int(chunk), int(o.pad_mode))) != cudaSuccess)
-    return cuda_fail(e, "conv launch");
-  if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
-  if ((e = ittt::launch_target(env, tm_xc, tm_wt, vhat, eta, int(M), int(d))) != cudaSuccess)
-    return cuda_fail(e, "target launch");
-  if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
-  if ((e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, z, int(M), int(f), int(d))) != cudaSuccess)
-    return cuda_fail(e, "gate/up launch");
-  if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event record");
-  if ((e = ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride, snap, int(B), int(n), int(d),
-                                  int(f))) != cudaSuccess)
-    return cuda_fail(e, "snapshot launch");
-  if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "event record");
+  cudaError_t e = cudaSuccess;
+  const char* what = nullptr;
+#define ITTT_STEP(call, name) \
+  if (what == nullptr && (e = (call)) != cudaSuccess) what = name
+  ITTT_STEP(rec(2 * ITTT_PHASE_CONV, stream), "event record");
+  if (!fused) {
+    ITTT_STEP(ittt::launch_conv(env, static_cast<const __nv_bfloat16*>(X0->data), cw, xc,
+                                int64_t(M), int(T), int(d), int(chunk), int(o.pad_mode)),
+              "conv launch");
+  }
+  ITTT_STEP(rec(2 * ITTT_PHASE_CONV + 1, stream), "event record");
+  ITTT_STEP(rec(2 * ITTT_PHASE_TARGET, stream), "event record");
+  ITTT_STEP(ittt::launch_target(env, tm_a, tm_wt, cw, vhat, eta, int(M), int(T), int(d),
+                                int(chunk), int(o.pad_mode), fused),
+            "target launch");
+  ITTT_STEP(rec(2 * ITTT_PHASE_TARGET + 1, stream), "event record");
+  ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP, stream), "event record");
+  ITTT_STEP(ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, z, int(M), int(f), int(d)),
+            "gate/up launch");
+  ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP + 1, stream), "event record");
+  ITTT_STEP(rec(2 * ITTT_PHASE_SNAPSHOT0, stream), "event record");
+  ITTT_STEP(ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride, snap, int(B), int(n), int(d),
+                                   int(f)),
+            "snapshot launch");
+  ITTT_STEP(rec(2 * ITTT_PHASE_SNAPSHOT0 + 1, stream), "event record");
   ittt::UpdateArgs ua;
   ua.B = int(B);
   ua.T = int(T);
@@ -357,13 +378,16 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   ua.w0_bstride = w0_bstride;
   ua.snap = snap;
   ua.state_out = o.state_out ? static_cast<float*>(o.state_out->data) : nullptr;
-  if ((e = ittt::launch_update(env, tm_vmn, tm_zmn, ua)) != cudaSuccess)
-    return cuda_fail(e, "update launch");
-  if ((e = mark(5)) != cudaSuccess) return cuda_fail(e, "event record");
-  if ((e = ittt::launch_apply(env, tm_zk, tm_snap, out->data, out->dtype == ITTT_FP32, int(B),
-                              int(T), int(d), int(f), int(chunk))) != cudaSuccess)
-    return cuda_fail(e, "apply launch");
-  if ((e = mark(6)) != cudaSuccess) return cuda_fail(e, "event record");
+  ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");
+  ITTT_STEP(ittt::launch_update(env, tm_vmn, tm_zmn, ua), "update launch");
+  ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
+  ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
+  ITTT_STEP(ittt::launch_apply(env, tm_zk, tm_snap, out->data, out->dtype == ITTT_FP32, int(B),
+                               int(T), int(d), int(f), int(chunk)),
+            "apply launch");
+  ITTT_STEP(rec(2 * ITTT_PHASE_APPLY + 1, stream), "event record");
+#undef ITTT_STEP
+  if (what != nullptr) return cuda_fail(e, what);
   return ITTT_OK;
 }
 
@@ -410,7 +434,7 @@ size_t ittt_workspace_bytes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t 
     g_last_error = saved;
     return 0;
   }
-  return plan_workspace(B, T, d, f, chunk, true, true, true).total;
+  return plan_workspace(B, T, d, f, chunk, true, true, true, true).total;
 }
 
 ittt_status ittt_stream_status(ittt_stream_t stream) {

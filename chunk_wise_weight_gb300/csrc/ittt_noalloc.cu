@@ -237,8 +237,9 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
                              static_cast<const float*>(conv_w->data), xc, int64_t(M), int(T),
                              int(d), int(chunk), ITTT_PAD_CHUNK)) != cudaSuccess) {
     what = "conv";
-  } else if ((e = ittt::launch_target(env, tm_xc, tm_wt, vhat, eta, int(M), int(d))) !=
-             cudaSuccess) {
+  } else if ((e = ittt::launch_target(env, tm_xc, tm_wt, static_cast<const float*>(conv_w->data),
+                                      vhat, eta, int(M), int(T), int(d), int(chunk),
+                                      ITTT_PAD_CHUNK, false)) != cudaSuccess) {
     what = "target";
   } else if ((e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, z, int(M), int(f), int(d))) !=
              cudaSuccess) {

@@ -22,10 +22,9 @@ struct ApplyParams {
   int mt_per_chunk, nt, kblocks;
 };
 
-struct ApplySched {
+struct ApplySched : SchedDefaults {
   using Params = ApplyParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, false);
-  static constexpr bool kPreload = false;
 
   const Params& p;
   int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0;
@@ -50,10 +49,10 @@ struct ApplySched {
   __device__ int seg_kblocks(int) const { return p.kblocks; }
   __device__ bool seg_fresh(int) const { return true; }
 
-  __device__ void load(int, int kb, void* a, void* b, uint64_t* bar) const {
+  __device__ void load(int, int kb, uint8_t* stage, uint64_t* bar) const {
     const int k = kb * kBK;
-    tma_load_2d(a, &p.tm_z, bar, k, arow0);
-    tma_load_2d(b, &p.tm_snap, bar, k, brow0);
+    tma_load_2d(stage, &p.tm_z, bar, k, arow0);
+    tma_load_2d(stage + kATileBytes, &p.tm_snap, bar, k, brow0);
   }
   static __device__ uint64_t a_desc(uint32_t base, int k) {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
@@ -99,7 +98,7 @@ struct ApplySched {
   }
 };
 
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__(PipeShape<ApplySched>::kThreads, 1)
     apply_kernel(const __grid_constant__ ApplyParams p, unsigned int* status) {
   run_pipeline<ApplySched>(p, status);
 }
@@ -125,10 +124,10 @@ cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z, const CU
   const int64_t units = int64_t(B) * p.n * p.mt_per_chunk * p.nt;
   if (units == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(kPipeSmemBytes));
+                                       int(pipe_smem_bytes<ApplySched>()));
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? int(units) : env.num_sms;
-  apply_kernel<<<grid, kNumThreads, kPipeSmemBytes, env.stream>>>(p, env.status);
+  apply_kernel<<<grid, PipeShape<ApplySched>::kThreads, pipe_smem_bytes<ApplySched>(), env.stream>>>(p, env.status);
   return cudaGetLastError();
 }
 

@@ -25,10 +25,9 @@ struct GateUpParams {
   int m_tiles, n_tiles, kblocks, raster;
 };
 
-struct GateUpSched {
+struct GateUpSched : SchedDefaults {
   using Params = GateUpParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, false);
-  static constexpr bool kPreload = false;
 
   const Params& p;
   int m0 = 0, n0 = 0, acc = 0;
@@ -47,11 +46,11 @@ struct GateUpSched {
   __device__ int seg_kblocks(int) const { return p.kblocks; }
   __device__ bool seg_fresh(int) const { return true; }
 
-  __device__ void load(int, int kb, void* a, void* b, uint64_t* bar) const {
+  __device__ void load(int, int kb, uint8_t* stage, uint64_t* bar) const {
     const int k = kb * kBK;
-    tma_load_2d(a, &p.tm_h, bar, k, m0);
-    tma_load_2d(b, &p.tm_wg, bar, k, n0);
-    tma_load_2d(static_cast<uint8_t*>(b) + kBTileBytes / 2, &p.tm_wu, bar, k, n0);
+    tma_load_2d(stage, &p.tm_h, bar, k, m0);
+    tma_load_2d(stage + kATileBytes, &p.tm_wg, bar, k, n0);
+    tma_load_2d(stage + kATileBytes + kBTileBytes / 2, &p.tm_wu, bar, k, n0);
   }
 
   // K-major, 128-byte swizzle: the k-th 16-wide slice starts 32 bytes in.
@@ -97,7 +96,7 @@ struct GateUpSched {
   }
 };
 
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__(PipeShape<GateUpSched>::kThreads, 1)
     gateup_kernel(const __grid_constant__ GateUpParams p, unsigned int* status) {
   run_pipeline<GateUpSched>(p, status);
 }
@@ -120,10 +119,10 @@ cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h, const C
   const int units = p.m_tiles * p.n_tiles;
   if (units == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(kPipeSmemBytes));
+                                       int(pipe_smem_bytes<GateUpSched>()));
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? units : env.num_sms;
-  gateup_kernel<<<grid, kNumThreads, kPipeSmemBytes, env.stream>>>(p, env.status);
+  gateup_kernel<<<grid, PipeShape<GateUpSched>::kThreads, pipe_smem_bytes<GateUpSched>(), env.stream>>>(p, env.status);
   return cudaGetLastError();
 }
 

@@ -1,22 +1,66 @@
 // k_target.cu -- the next-token-aligned value target
-//   Vhat = Conv1D(X0) W_target^T
+//   eta * Vhat = eta * Conv1D(X0) W_target^T
 // ("[논문리뷰] In-Place Test-Time Training", Method §2 eq. (5); causal
-// padding from Method §3).
+// padding from Method §3), in two variants with identical results:
 //
-// The depthwise three-tap convolution runs on CUDA cores: one thread per
-// 8 channels of a token row, 128-bit loads of the rows t-1, t, t+1, fp32
-// arithmetic, one rounding to bf16 (the tensor-core operand).  Taps outside
-// the current chunk (or, in sequence mode, outside the sequence) read zero.
-// The projection is a tcgen05 GEMM over the result.  Its epilogue scales by
-// the fast-weight learning rate before the bf16 rounding, so the tensor
-// stores eta * Vhat: the update's left operand with eta folded in (the
-// identity eta K^T(KW - V) = K~^T(K~W - V~), K~ = sqrt(eta) K, of the "ViT^3"
-// review's design insights, here with the whole eta on the value side).
+// Split (default): conv3_kernel streams X0 once (one thread per 8 channels
+// of a token row, 128-bit loads of rows t-1, t, t+1, fp32 taps, one bf16
+// rounding) into Xc; the host runs it beside the gate/up GEMM, and the
+// target GEMM then TMA-loads Xc as its A operand.
+//
+// Fused: the GEMM builds each A tile itself.  Per 64-channel K block the
+// producer loads, besides the W_target tile, a TMA box of the 130 X0 rows
+// [m0 - 1, m0 + 128] (the tile's rows plus one halo row on each side; rows
+// outside the tensor read zero) and, with a bulk copy, the block's 64 x 3
+// fp32 conv weights.  Eight builder warps turn them into the bf16 A tile in
+// shared memory: each thread owns 8 channels of 4 consecutive rows, reads the
+// 6 X0 rows it needs, applies the taps in fp32, rounds once to bf16 and
+// writes the 128-byte-swizzled K-major layout the tensor core reads.  The
+// convolution never touches HBM, but it is repeated for every 256-column
+// output tile on CUDA cores and the larger stage leaves room for 3 stages
+// instead of 4, which makes this variant slower on GB300.
+//
+// In both, a tap that reaches outside the current chunk (or, in sequence
+// mode, outside the sequence) reads zero, and the epilogue scales by the
+// fast-weight learning rate before the bf16 rounding, so the output is
+// eta * Vhat: the update's left operand with eta folded in (the identity
+// eta K^T(KW - V) = K~^T(K~W - V~) of the "ViT^3" review's design insights,
+// here with the whole eta on the value side).
 #include "kernels.h"
 #include "pipeline.cuh"
 
 namespace ittt {
 namespace {
+
+constexpr int kHaloRows = kBM + 2;                     // 130 X0 rows per stage
+constexpr uint32_t kX0BoxBytes = kHaloRows * 128;      // 16640
+constexpr uint32_t kConvWBytes = kBK * 3 * 4;          // 64 channels x 3 fp32 taps
+constexpr uint32_t kX0StageBytes = kX0BoxBytes + kConvWBytes;  // 17408 = 17 KiB
+
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  return uint64_t(__float_as_uint(lo)) | (uint64_t(__float_as_uint(hi)) << 32);
+}
+
+// bf16x2 word -> two fp32 lanes (exact).
+__device__ __forceinline__ uint64_t bf16x2_widen(uint32_t w) {
+  return uint64_t(w << 16) | (uint64_t(w & 0xffff0000u) << 32);
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(uint64_t v) {
+  return pack_bf16x2(__uint_as_float(uint32_t(v)), __uint_as_float(uint32_t(v >> 32)));
+}
 
 __global__ void __launch_bounds__(256)
     conv3_kernel(const __nv_bfloat16* __restrict__ x0, const float* __restrict__ conv_w,
@@ -72,18 +116,23 @@ __global__ void __launch_bounds__(256)
 }
 
 struct TargetParams {
-  CUtensorMap tm_xc;  // Xc       [M, d]  box {64, 128}
-  CUtensorMap tm_wt;  // W_target [d, d]  box {64, 256}
-  __nv_bfloat16* vhat;  // eta * Vhat [M, d]
+  CUtensorMap tm_a;      // split: Xc [M, d] box {64, 128}; fused: X0 [M, d] box {64, 130}
+  CUtensorMap tm_wt;     // W_target [d, d]  box {64, 256}
+  const float* conv_w;   // [d, 3]
+  __nv_bfloat16* vhat;   // eta * Vhat [M, d]
   float eta;
-  int M, d;
+  int M, T, d, C, pad_mode;
   int m_tiles, n_tiles, kblocks, raster;
 };
 
-struct TargetSched {
+template <bool kFused>
+struct TargetSched : SchedDefaults {
   using Params = TargetParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, false);
-  static constexpr bool kPreload = false;
+  static constexpr int kNumStages = kFused ? 3 : 4;
+  static constexpr uint32_t kExtraStageBytes = kFused ? kX0StageBytes : 0;
+  static constexpr int kBuilderWarps = kFused ? 8 : 0;
+  static_assert(kX0StageBytes % 1024 == 0, "stage alignment");
 
   const Params& p;
   int m0 = 0, n0 = 0, acc = 0;
@@ -102,11 +151,101 @@ struct TargetSched {
   __device__ int seg_kblocks(int) const { return p.kblocks; }
   __device__ bool seg_fresh(int) const { return true; }
 
-  __device__ void load(int, int kb, void* a, void* b, uint64_t* bar) const {
-    const int k = kb * kBK;
-    tma_load_2d(a, &p.tm_xc, bar, k, m0);
-    tma_load_2d(b, &p.tm_wt, bar, k, n0);
+  // Conv weights of the K block's channels (fewer in a ragged last block).
+  __device__ uint32_t conv_w_bytes(int kb) const {
+    return uint32_t(min(kBK, p.d - kb * kBK)) * 12u;
   }
+  __device__ uint32_t tma_bytes(int, int kb) const {
+    if constexpr (kFused) return kBTileBytes + kX0BoxBytes + conv_w_bytes(kb);
+    return kStageBytes;
+  }
+  __device__ void load(int, int kb, uint8_t* stage, uint64_t* bar) const {
+    const int k = kb * kBK;
+    tma_load_2d(stage + kATileBytes, &p.tm_wt, bar, k, n0);
+    if constexpr (kFused) {
+      tma_load_2d(stage + kStageBytes, &p.tm_a, bar, k, m0 - 1);
+      bulk_load(stage + kStageBytes + kX0BoxBytes, p.conv_w + size_t(k) * 3, conv_w_bytes(kb),
+                bar);
+    } else {
+      tma_load_2d(stage, &p.tm_a, bar, k, m0);
+    }
+  }
+
+  // Conv of 8 channels x 4 rows per thread (256 threads cover 128 x 64).
+  __device__ void build_a(int, int kb, uint8_t* stage, int tid) const {
+    const int c8 = tid & 7;          // 16-byte chunk = channels k0 .. k0+7
+    const int r0 = (tid >> 3) * 4;   // first of this thread's 4 rows
+    const int k0 = kb * kBK + c8 * 8;
+    const uint8_t* xbox = stage + kStageBytes;  // box row j = token row m0 - 1 + j
+    uint8_t* atile = stage;
+
+    // Taps of channel pairs (2j, 2j+1): tap index 0 = t-1, 1 = t, 2 = t+1;
+    // the stage carries this K block's weights right after the X0 box.
+    uint64_t w[3][4];
+    if (k0 < p.d) {
+      float wf[24];
+      const float4* src =
+          reinterpret_cast<const float4*>(stage + kStageBytes + kX0BoxBytes + c8 * 96);
+#pragma unroll
+      for (int q = 0; q < 6; ++q) {
+        const float4 v = src[q];
+        wf[4 * q] = v.x;
+        wf[4 * q + 1] = v.y;
+        wf[4 * q + 2] = v.z;
+        wf[4 * q + 3] = v.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int tap = 0; tap < 3; ++tap)
+          w[tap][j] = f32x2_pack(wf[3 * (2 * j) + tap], wf[3 * (2 * j + 1) + tap]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[0][j] = w[1][j] = w[2][j] = 0ull;
+    }
+
+    // Six X0 rows r0-1 .. r0+4 (box rows r0 .. r0+5), widened to fp32.
+    uint64_t x[6][4];
+#pragma unroll
+    for (int j = 0; j < 6; ++j) {
+      const int br = r0 + j;
+      const uint4 q = *reinterpret_cast<const uint4*>(xbox + br * 128 + ((c8 ^ (br & 7)) << 4));
+      x[j][0] = bf16x2_widen(q.x);
+      x[j][1] = bf16x2_widen(q.y);
+      x[j][2] = bf16x2_widen(q.z);
+      x[j][3] = bf16x2_widen(q.w);
+    }
+    // The 4 rows share one chunk (C and m0 are multiples of 64 and 128): only
+    // the halo rows can fall outside it.
+    const int t0 = (m0 + r0) % p.T;  // token index of row r0 in its sequence
+    bool prev_ok, next_ok;
+    if (p.pad_mode == 0) {
+      const int pc = t0 % p.C;
+      prev_ok = pc > 0;
+      next_ok = pc + 4 < p.C;
+    } else {
+      prev_ok = t0 > 0;
+      next_ok = t0 + 4 < p.T;
+    }
+    if (!prev_ok) x[0][0] = x[0][1] = x[0][2] = x[0][3] = 0ull;
+    if (!next_ok) x[5][0] = x[5][1] = x[5][2] = x[5][3] = 0ull;
+
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint64_t y = f32x2_mul(w[0][j], x[i][j]);
+        y = f32x2_fma(w[1][j], x[i + 1][j], y);
+        y = f32x2_fma(w[2][j], x[i + 2][j], y);
+        o[j] = f32x2_to_bf16x2(y);
+      }
+      const int r = r0 + i;
+      *reinterpret_cast<uint4*>(atile + r * 128 + ((c8 ^ (r & 7)) << 4)) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+
   static __device__ uint64_t a_desc(uint32_t base, int k) {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
   }
@@ -142,9 +281,23 @@ struct TargetSched {
   }
 };
 
-__global__ void __launch_bounds__(kNumThreads, 1)
+template <bool kFused>
+__global__ void __launch_bounds__(PipeShape<TargetSched<kFused>>::kThreads, 1)
     target_kernel(const __grid_constant__ TargetParams p, unsigned int* status) {
-  run_pipeline<TargetSched>(p, status);
+  run_pipeline<TargetSched<kFused>>(p, status);
+}
+
+template <bool kFused>
+cudaError_t launch_target_variant(const LaunchEnv& env, const TargetParams& p, int units) {
+  using S = TargetSched<kFused>;
+  cudaError_t e = cudaFuncSetAttribute(target_kernel<kFused>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(pipe_smem_bytes<S>()));
+  if (e != cudaSuccess) return e;
+  const int grid = units < env.num_sms ? units : env.num_sms;
+  target_kernel<kFused><<<grid, PipeShape<S>::kThreads, pipe_smem_bytes<S>(), env.stream>>>(
+      p, env.status);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -160,27 +313,28 @@ cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const flo
   return cudaGetLastError();
 }
 
-cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_xc, const CUtensorMap& tm_wt,
-                          __nv_bfloat16* vhat, float eta, int M, int d) {
+cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a, const CUtensorMap& tm_wt,
+                          const float* conv_w, __nv_bfloat16* vhat, float eta, int M, int T, int d,
+                          int C, int pad_mode, bool fused) {
   TargetParams p;
-  p.tm_xc = tm_xc;
+  p.tm_a = tm_a;
   p.tm_wt = tm_wt;
+  p.conv_w = conv_w;
   p.vhat = vhat;
   p.eta = eta;
   p.M = M;
+  p.T = T;
   p.d = d;
+  p.C = C;
+  p.pad_mode = pad_mode;
   p.m_tiles = (M + kBM - 1) / kBM;
   p.n_tiles = (d + kBN - 1) / kBN;
   p.kblocks = (d + kBK - 1) / kBK;
   p.raster = p.n_tiles < 16 ? p.n_tiles : 16;
   const int units = p.m_tiles * p.n_tiles;
   if (units == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(target_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(kPipeSmemBytes));
-  if (e != cudaSuccess) return e;
-  const int grid = units < env.num_sms ? units : env.num_sms;
-  target_kernel<<<grid, kNumThreads, kPipeSmemBytes, env.stream>>>(p, env.status);
-  return cudaGetLastError();
+  return fused ? launch_target_variant<true>(env, p, units)
+               : launch_target_variant<false>(env, p, units);
 }
 
 }  // namespace ittt

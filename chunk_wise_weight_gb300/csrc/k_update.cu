@@ -39,7 +39,7 @@ struct UpdateParams {
   int mt, np, kb_per_chunk;
 };
 
-struct UpdateSched {
+struct UpdateSched : SchedDefaults {
   using Params = UpdateParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true, true);
   static constexpr bool kPreload = true;
@@ -64,12 +64,12 @@ struct UpdateSched {
   __device__ int seg_kblocks(int) const { return p.kb_per_chunk; }
   __device__ bool seg_fresh(int) const { return false; }  // starts from the preloaded W_0
 
-  __device__ void load(int s, int kb, void* a, void* bt, uint64_t* bar) const {
+  __device__ void load(int s, int kb, uint8_t* stage, uint64_t* bar) const {
     const int i = s / halves;
     const int h = s - i * halves;
     const int tok = b * p.T + i * p.C + kb * kBK;
-    uint8_t* sa = static_cast<uint8_t*>(a);
-    uint8_t* sb = static_cast<uint8_t*>(bt);
+    uint8_t* sa = stage;
+    uint8_t* sb = stage + kATileBytes;
     tma_load_2d(sa, &p.tm_v, bar, m0, tok);
     tma_load_2d(sa + kMnBoxBytes, &p.tm_v, bar, m0 + 64, tok);
     const int n0 = nbase + h * kBN;
@@ -167,7 +167,7 @@ struct UpdateSched {
   }
 };
 
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__(PipeShape<UpdateSched>::kThreads, 1)
     update_kernel(const __grid_constant__ UpdateParams p, unsigned int* status) {
   run_pipeline<UpdateSched>(p, status);
 }
@@ -236,10 +236,10 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
   p.kb_per_chunk = a.C / kBK;
   const int units = p.B * p.mt * p.np;
   cudaError_t e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(kPipeSmemBytes));
+                                       int(pipe_smem_bytes<UpdateSched>()));
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? units : env.num_sms;
-  update_kernel<<<grid, kNumThreads, kPipeSmemBytes, env.stream>>>(p, env.status);
+  update_kernel<<<grid, PipeShape<UpdateSched>::kThreads, pipe_smem_bytes<UpdateSched>(), env.stream>>>(p, env.status);
   return cudaGetLastError();
 }
 

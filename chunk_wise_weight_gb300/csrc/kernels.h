@@ -1,7 +1,7 @@
 // kernels.h -- internal launchers of libittt.so (host side, C++).  The C-ABI
 // in ittt_api.cu validates arguments, builds the TMA tensor maps and calls
-// these in data-flow order: conv -> target, gate/up -> snapshot 0 -> update
-// -> apply.
+// these in data-flow order: conv (beside gate/up) -> target, gate/up ->
+// snapshot 0 -> update -> apply.
 #pragma once
 
 #include <cuda.h>
@@ -23,16 +23,18 @@ cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h,
                           const CUtensorMap& tm_wg, const CUtensorMap& tm_wu,
                           __nv_bfloat16* z, int M, int f, int K);
 
-// Xc = three-tap depthwise conv of X0 (zero padding at chunk or sequence
-// edges), rounded to bf16.  x0, xc: [B*T, d].
+// Xc = three-tap depthwise conv of X0 (zero padding at chunk edges, or only
+// at sequence edges when pad_mode = 1), rounded to bf16.  x0, xc: [B*T, d].
 cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const float* conv_w,
                         __nv_bfloat16* xc, int64_t rows, int T, int d, int C, int pad_mode);
 
-// vhat[M, d] = eta * (Xc W_target^T), rounded once to bf16.  Tensor maps:
-// Xc [M, d] box {64,128}; W_target [d, d] box {64,256}.
-cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_xc,
-                          const CUtensorMap& tm_wt, __nv_bfloat16* vhat, float eta, int M,
-                          int d);
+// vhat[M, d] = eta * (Conv1D(X0) W_target^T), rounded once to bf16.
+// Split (fused = false): tm_a maps Xc [M, d] with box {64,128}.
+// Fused: tm_a maps X0 [M, d] with box {64,130} and the kernel computes the
+// conv itself.  tm_wt: W_target [d, d] box {64,256}.
+cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a,
+                          const CUtensorMap& tm_wt, const float* conv_w, __nv_bfloat16* vhat,
+                          float eta, int M, int T, int d, int C, int pad_mode, bool fused);
 
 // snap[b, 0] = bf16(W_0 of sequence b) for every b.  w0 is bf16 or fp32,
 // [d, f] shared (w0_bstride = 0) or [B, d, f].

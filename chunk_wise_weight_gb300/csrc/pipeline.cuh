@@ -1,16 +1,20 @@
 // pipeline.cuh -- persistent, warp-specialised tcgen05 GEMM pipeline shared by
-// the layer's four tensor-core kernels.
+// the layer's tensor-core kernels.
 //
 // One CTA per SM (the shared-memory footprint forces it).  Roles:
-//   warp 0, lane 0 : TMA producer -- fills a ring of kStages operand stages
+//   warp 0, lane 0 : TMA producer -- fills a ring of operand stages
 //   warp 1         : allocates 512 TMEM columns; lane 0 issues tcgen05.mma
 //   warps 2..5     : epilogue -- drains the fp32 accumulator from TMEM
+//   warps 6..      : optional A-tile builders (S::kBuilderWarps > 0): they
+//                    compute the A tile in shared memory from raw data the
+//                    producer loaded into the stage, instead of TMA loading it
 //
 // Tiles are 128 (M) x 256 (N), K staged 64 at a time with the 128-byte
 // swizzle.  TMEM holds two 128 x 256 fp32 accumulators, so the epilogue of
 // one accumulation overlaps the MMAs of the next.
 //
-// A kernel plugs in a schedule class `S` that describes its work:
+// A kernel plugs in a schedule class `S` (deriving from SchedDefaults) that
+// describes its work:
 //   S(const Params&)                     construct from the kernel parameters
 //   int  num_units()                     persistent work units
 //   void begin_unit(int unit, int local) local = how many units this CTA did
@@ -18,12 +22,13 @@
 //   int  seg_acc(int s)                  accumulator (0/1) segment s uses
 //   int  seg_kblocks(int s)              64-wide K blocks of segment s
 //   bool seg_fresh(int s)                segment starts from a zero accumulator
-//   void load(int s, int kb, void* a, void* b, uint64_t* bar)   (TMA issue)
+//   void load(int s, int kb, uint8_t* stage, uint64_t* bar)     (TMA issue)
 //   void epilogue(int s, int row, uint32_t tmem_row_base)       (per thread)
 //   static uint64_t a_desc(uint32_t a_smem, int k16)
 //   static uint64_t b_desc(uint32_t b_smem, int k16)
 //   static constexpr uint32_t kIdesc
-//   static constexpr bool kPreload
+// A stage holds the A tile at offset 0, the B tile at kATileBytes and
+// S::kExtraStageBytes of kernel-specific data at kStageBytes.
 // Segments let one accumulator keep accumulating across several epilogue
 // reads (the fast-weight state walks the chunks of a sequence).
 //
@@ -35,6 +40,12 @@
 // the release after the previous segment's read inside a unit, or the
 // preload at a unit's start (the last read of a unit is not released; the
 // next unit's preload stands for it).
+//
+// With kBuilderWarps > 0 the producer's copies complete on a `loaded`
+// barrier (tma_bytes(s, kb) per stage); the builder warps wait for it, call
+//   void build_a(int s, int kb, uint8_t* stage, int tid)  (tid < 32*warps)
+// then each makes its writes visible to the tensor core and arrives on
+// `full` (32 * kBuilderWarps arrivals per stage).
 #pragma once
 
 #include "sm103.cuh"
@@ -45,17 +56,35 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kUmmaK = 16;
-constexpr int kStages = 4;
+constexpr int kMaxStages = 4;
 constexpr uint32_t kATileBytes = kBM * kBK * 2;  // 16 KiB
 constexpr uint32_t kBTileBytes = kBN * kBK * 2;  // 32 KiB
 constexpr uint32_t kStageBytes = kATileBytes + kBTileBytes;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kNumThreads = 192;
+constexpr int kBaseThreads = 192;
 constexpr int kEpilogueThreads = 128;
 
+struct SchedDefaults {
+  static constexpr int kNumStages = 4;
+  static constexpr uint32_t kExtraStageBytes = 0;
+  static constexpr int kBuilderWarps = 0;
+  static constexpr bool kPreload = false;
+  // Transaction bytes the producer's copies deliver into a stage.
+  __device__ uint32_t tma_bytes(int, int) const { return kStageBytes; }
+};
+
+template <class S>
+struct PipeShape {
+  static_assert(S::kNumStages >= 2 && S::kNumStages <= kMaxStages, "stage count");
+  static_assert((kStageBytes + S::kExtraStageBytes) % 1024 == 0, "stages stay 1 KiB aligned");
+  static constexpr uint32_t kStageStride = kStageBytes + S::kExtraStageBytes;
+  static constexpr int kThreads = kBaseThreads + 32 * S::kBuilderWarps;
+};
+
 struct __align__(8) PipeSync {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t loaded[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
@@ -63,22 +92,29 @@ struct __align__(8) PipeSync {
   int abort_flag;
 };
 
-constexpr size_t kPipeSmemBytes = 1024 + size_t(kStages) * kStageBytes + sizeof(PipeSync);
+template <class S>
+constexpr size_t pipe_smem_bytes() {
+  return 1024 + size_t(S::kNumStages) * PipeShape<S>::kStageStride + sizeof(PipeSync);
+}
 
 template <class S>
 __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsigned int* status) {
+  constexpr int NS = S::kNumStages;
+  constexpr uint32_t kStride = PipeShape<S>::kStageStride;
+  constexpr bool kBuild = S::kBuilderWarps > 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  PipeSync* sync = reinterpret_cast<PipeSync*>(smem + size_t(kStages) * kStageBytes);
+  PipeSync* sync = reinterpret_cast<PipeSync*>(smem + size_t(NS) * kStride);
   volatile int* abort_flag = &sync->abort_flag;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sync->full[s], 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&sync->full[s], kBuild ? 32 * S::kBuilderWarps : 1);
       mbar_init(&sync->empty[s], 1);
+      mbar_init(&sync->loaded[s], 1);
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&sync->acc_full[h], 1);
@@ -116,11 +152,11 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
               raise_abort(abort_flag, status, kStatusTimeout);
               break;
             }
-            uint8_t* sa = smem + size_t(stage) * kStageBytes;
-            mbar_arrive_expect_tx(&sync->full[stage], kStageBytes);
-            sched.load(s, kb, sa, sa + kATileBytes, &sync->full[stage]);
+            uint64_t* bar = kBuild ? &sync->loaded[stage] : &sync->full[stage];
+            mbar_arrive_expect_tx(bar, sched.tma_bytes(s, kb));
+            sched.load(s, kb, smem + size_t(stage) * kStride, bar);
             ++issued;
-            if (++stage == kStages) {
+            if (++stage == NS) {
               stage = 0;
               phase ^= 1u;
             }
@@ -129,11 +165,12 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
       }
       // Let every load still in flight land before the CTA can exit.
       const int zero = 0;
-      const uint32_t tail = issued < uint32_t(kStages) ? issued : uint32_t(kStages);
+      const uint32_t tail = issued < uint32_t(NS) ? issued : uint32_t(NS);
       for (uint32_t q = issued - tail; q < issued; ++q) {
-        const int st = int(q % kStages);
-        const uint32_t par = (q / kStages) & 1u;
-        if (!mbar_wait(&sync->full[st], par, &zero)) atomicOr(status, kStatusTimeout);
+        const int st = int(q % NS);
+        const uint32_t par = (q / NS) & 1u;
+        uint64_t* bar = kBuild ? &sync->loaded[st] : &sync->full[st];
+        if (!mbar_wait(bar, par, &zero)) atomicOr(status, kStatusTimeout);
       }
     }
   } else if (warp == 1) {
@@ -168,7 +205,7 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
               break;
             }
             tc_fence_after_sync();
-            const uint32_t a_base = smem_u32(smem + size_t(stage) * kStageBytes);
+            const uint32_t a_base = smem_u32(smem + size_t(stage) * kStride);
             const uint32_t b_base = a_base + kATileBytes;
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k) {
@@ -176,7 +213,7 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
                        (fresh && kb == 0 && k == 0) ? 0u : 1u);
             }
             mma_commit(&sync->empty[stage]);
-            if (++stage == kStages) {
+            if (++stage == NS) {
               stage = 0;
               phase ^= 1u;
             }
@@ -191,7 +228,7 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
       const int zero = 0;
       if (!mbar_wait(&sync->drain, 0u, &zero)) atomicOr(status, kStatusTimeout);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------- epilogue
     S sched(p);
     const int quad = warp & 3;  // TMEM lanes this warp may touch: 32*quad..+31
@@ -232,6 +269,38 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
           mbar_arrive(&sync->acc_empty[h]);
         }
         ++acc_use[h];
+      }
+    }
+  } else if constexpr (kBuild) {
+    // ------------------------------------------------------- A-tile builders
+    S sched(p);
+    const int tid = int(threadIdx.x) - kBaseThreads;
+    int stage = 0;
+    uint32_t phase = 0;
+    const int nunits = sched.num_units();
+    int local = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++local) {
+      sched.begin_unit(u, local);
+      const int nseg = sched.num_segments();
+      for (int s = 0; s < nseg && ok; ++s) {
+        const int nkb = sched.seg_kblocks(s);
+        for (int kb = 0; kb < nkb; ++kb) {
+          const bool got =
+              __all_sync(0xffffffffu, mbar_wait(&sync->loaded[stage], phase, abort_flag));
+          if (!got) {
+            raise_abort(abort_flag, status, kStatusTimeout);
+            ok = false;
+            break;
+          }
+          sched.build_a(s, kb, smem + size_t(stage) * kStride, tid);
+          fence_proxy_async_smem();  // generic-proxy writes -> tensor core
+          mbar_arrive(&sync->full[stage]);
+          if (++stage == NS) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
       }
     }
   }

@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "ITTT_OK", 1: "ITTT_ERR_INVALID_ARG", 2: "ITTT_ERR_UNSUPPORTE
 BF16, FP32 = 0, 1
 PAD_CHUNK, PAD_SEQUENCE = 0, 1
 PHASES = ("conv", "target", "gateup", "snapshot0", "update", "apply")
+FLAG_FUSED_CONV = 1
 
 _DTYPES = {torch.bfloat16: BF16, torch.float32: FP32}
 
@@ -38,7 +39,7 @@ class Tensor(ctypes.Structure):
 
 
 class Opts(ctypes.Structure):
-    _fields_ = [("pad_mode", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+    _fields_ = [("pad_mode", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("state_in", ctypes.POINTER(Tensor)), ("state_out", ctypes.POINTER(Tensor)),
                 ("z_buf", ctypes.POINTER(Tensor)), ("vhat_buf", ctypes.POINTER(Tensor)),
                 ("snap_buf", ctypes.POINTER(Tensor)), ("workspace", ctypes.c_void_p),
@@ -130,16 +131,19 @@ def _check(status: int):
 def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: int,
             out: torch.Tensor | None = None, *, out_dtype=torch.bfloat16, stream=None,
             pad_mode: int = PAD_CHUNK, state_in=None, state_out=None, z_buf=None,
-            vhat_buf=None, snap_buf=None, workspace=None, events=None) -> torch.Tensor:
+            vhat_buf=None, snap_buf=None, workspace=None, events=None,
+            fused_conv: bool = False) -> torch.Tensor:
     """Enqueue one layer forward on `stream` (default: current stream) and
     return `out` [B,T,d].  Extra keyword buffers map to ittt_opts; `events`
-    is a list of len(PHASES) + 1 torch.cuda.Event(enable_timing=True)."""
+    is a list of 2 * len(PHASES) torch.cuda.Event(enable_timing=True): a
+    (start, end) pair per phase."""
     lib = load()
     if out is None:
         out = torch.empty(H.shape, dtype=out_dtype, device=H.device)
     keep = [describe(x) for x in (H, X0, W_gate, W_up, W_down0, W_target, conv_w, out)]
     opts = Opts()
     opts.pad_mode = int(pad_mode)
+    opts.flags = FLAG_FUSED_CONV if fused_conv else 0
     extra = {}
     for name, t in (("state_in", state_in), ("state_out", state_out), ("z_buf", z_buf),
                     ("vhat_buf", vhat_buf), ("snap_buf", snap_buf)):
@@ -151,8 +155,8 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
         opts.workspace_bytes = workspace.numel() * workspace.element_size()
     ev_arr = None
     if events is not None:
-        if len(events) != len(PHASES) + 1:
-            raise ValueError(f"events needs {len(PHASES) + 1} entries")
+        if len(events) != 2 * len(PHASES):
+            raise ValueError(f"events needs {2 * len(PHASES)} entries")
         for e in events:  # torch creates the CUDA event on its first record
             if not e.cuda_event:
                 e.record(torch.cuda.current_stream(H.device) if stream is None else stream)

@@ -104,15 +104,16 @@ typedef struct {
  *              W_0 .. W_{n-1} that the apply step reads.
  *   workspace  device scratch of workspace_bytes >= ittt_workspace_bytes(...)
  *              (256-byte aligned); when given, nothing is allocated.
- *   events     profiling: NULL, or ITTT_NUM_PHASES + 1 cudaEvent_t handles.
- *              events[0] is recorded on `stream` before the first kernel and
- *              events[k] after phase k-1 (ittt_phase order), so each
- *              consecutive pair brackets one phase on the device timeline.
- *              A phase with nothing to do records its event all the same.
+ *   events     profiling: NULL, or 2 * ITTT_NUM_PHASES cudaEvent_t handles.
+ *              events[2k] and events[2k+1] are recorded right before and
+ *              right after phase k (ittt_phase order) on `stream`, so each
+ *              pair brackets one phase on the device timeline.  A phase with
+ *              nothing to do records both.
+ *   flags      ITTT_FLAG_* bits.
  */
 typedef struct {
   int32_t pad_mode;
-  int32_t reserved0;
+  int32_t flags;
   const ittt_tensor* state_in;
   ittt_tensor* state_out;
   ittt_tensor* z_buf;
@@ -123,10 +124,18 @@ typedef struct {
   void* const* events;
 } ittt_opts;
 
+/* ittt_opts.flags */
+/* Compute the convolution inside the W_target GEMM (extra warps build each
+ * A tile from raw X0 rows in shared memory) instead of in its own kernel.
+ * Same results; slower on GB300, where the fused convolution is repeated for
+ * every 256-column output tile. */
+#define ITTT_FLAG_FUSED_CONV 1
+
 /* Kernel phases of one forward call, in launch order. */
 typedef enum {
-  ITTT_PHASE_CONV = 0,      /* depthwise three-tap conv of X0 (CUDA cores) */
-  ITTT_PHASE_TARGET = 1,    /* Vhat = Xc W_target^T (tensor cores) */
+  ITTT_PHASE_CONV = 0,      /* Xc = depthwise 3-tap conv of X0 (CUDA cores; empty
+                               when fused into the target GEMM) */
+  ITTT_PHASE_TARGET = 1,    /* eta*Vhat = eta * Xc W_target^T (tensor cores) */
   ITTT_PHASE_GATEUP = 2,    /* Z = SiLU(H W_gate^T) * (H W_up^T) (tensor cores) */
   ITTT_PHASE_SNAPSHOT0 = 3, /* bf16 copy of the initial fast weight */
   ITTT_PHASE_UPDATE = 4,    /* prefix walk of Vhat^T Z, snapshots W_1..W_{n-1} */

@@ -49,7 +49,7 @@ def to_device(inp, dev, w0_dtype=torch.bfloat16):
 
 
 def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
-        state_in=None, want_state=False):
+        state_in=None, want_state=False, fused_conv=False):
     B, T, d = g["H"].shape
     f = g["W_gate"].shape[0]
     dev = g["H"].device
@@ -64,7 +64,8 @@ def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
         kw["state_in"] = state_in
     out = ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"],
                        None if state_in is not None else g["W_down0"], g["W_target"],
-                       g["conv_w"], eta, C, out_dtype=out_dtype, pad_mode=pad_mode, **kw)
+                       g["conv_w"], eta, C, out_dtype=out_dtype, pad_mode=pad_mode,
+                       fused_conv=fused_conv, **kw)
     ittt.stream_status()
     res = {"O": out}
     res.update(kw)
@@ -113,14 +114,27 @@ def test_tiny_named_workload(cuda_device):
     print(f"vs unrounded fp32 inputs: rel_fro={rel_fro(host(got['O']), raw_ref['O']):.3e}")
 
 
+@pytest.mark.parametrize("fused_conv", [False, True])
 @pytest.mark.parametrize("pad_mode", [ittt.PAD_CHUNK, ittt.PAD_SEQUENCE])
-def test_pad_modes(cuda_device, pad_mode):
-    B, T, d, f, C, eta = 2, 512, 128, 384, 128, 0.05
+def test_pad_modes(cuda_device, pad_mode, fused_conv):
+    B, T, d, f, C, eta = 2, 512, 200, 384, 128, 0.05
     inp = make_inputs(B, T, d, f, seed=7)
     ref = oracle.forward(inp, eta, C, pad_mode=pad_mode, want_vhat=True)
-    got = run(to_device(inp, cuda_device), eta, C, pad_mode=pad_mode, intermediates=True)
+    got = run(to_device(inp, cuda_device), eta, C, pad_mode=pad_mode, intermediates=True,
+              fused_conv=fused_conv)
     assert_parity(host(got["vhat_buf"]), eta * ref["Vhat"], "eta * Vhat")
     assert_parity(host(got["O"]), ref["O"], "O")
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", SHAPES[:4])
+def test_fused_and_split_conv_agree_bitwise(cuda_device, B, T, d, f, C, eta):
+    """Both convolution variants round the same fp32 taps once: identical
+    eta * Vhat and O."""
+    g = to_device(make_inputs(B, T, d, f, seed=300 + d), cuda_device)
+    a = run(g, eta, C, intermediates=True)
+    b = run(g, eta, C, intermediates=True, fused_conv=True)
+    assert torch.equal(a["vhat_buf"], b["vhat_buf"])
+    assert torch.equal(a["O"], b["O"])
 
 
 def test_fp32_output_and_fp32_initial_weight(cuda_device):
