@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fused-conv", action="store_true",
                     help="compute the convolution inside the target GEMM")
+    ap.add_argument("--dual", action="store_true",
+                    help="dual form (scores Z Z^T) instead of the fast-weight walk")
     return ap.parse_args()
 
 
@@ -106,8 +108,10 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def phase_model(B, T, d, f, C):
-    """Algorithmic work per phase: ('tensor', FLOPs) or ('hbm', bytes)."""
+def phase_model(B, T, d, f, C, dual=False):
+    """Algorithmic work per phase: ('tensor', FLOPs) or ('hbm', bytes).  The
+    dual form's extra work (scores Z Z^T, S Vhat) is charged at the primal
+    form's FLOPs, the work the layer needs."""
     n = T // C
     return {
         "conv": ("hbm", 2.0 * B * T * d * 2 + d * 3 * 4),
@@ -231,7 +235,7 @@ def main():
 
     def step(events=None):
         ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, stream=stream, events=events,
-                     fused_conv=args.fused_conv)
+                     fused_conv=args.fused_conv, dual=args.dual)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -261,7 +265,7 @@ def main():
     value = tokens / (elapsed_ms / 1e3)
 
     # Per-phase device durations from the events between launches.
-    model = phase_model(B, T, d, f, C)
+    model = phase_model(B, T, d, f, C, args.dual)
     phases = {}
     for p, name in enumerate(ittt.PHASES):
         ms = sum(ev[k][2 * p].elapsed_time(ev[k][2 * p + 1]) for k in range(args.steps)) / args.steps
@@ -326,7 +330,7 @@ def main():
                 if k >= 2:
                     stream.wait_event(downloaded[j])  # O_j read back before reuse
                 ittt.forward(Hs[j], X0s[j], Wg, Wu, W0, Wt, cw, eta, C, Os[j], stream=stream,
-                             fused_conv=args.fused_conv)
+                             fused_conv=args.fused_conv, dual=args.dual)
                 computed[j].record(stream)
                 down.wait_event(computed[j])
                 with torch.cuda.stream(down):
@@ -362,6 +366,7 @@ def main():
             "config": {"workload": cfg["name"], "B": B, "T": T, "d": d, "f": f, "C": C,
                        "eta": eta, "chunks": T // C, "parallelism": f"batch x{world} (replicas)",
                        "conv": "fused into target GEMM" if args.fused_conv else "own kernel",
+                       "schedule": "dual (scores Z Z^T)" if args.dual else "primal walk",
                        "l2": "inputs larger than L2: H+X0 and Z are several GB per step"},
             "layer_tflops": round(layer_tflops, 1),
             "layer_frac_of_peak": {

@@ -170,7 +170,7 @@ ittt_status check_sizes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chun
 
 // --------------------------------------------------------------- workspace
 struct Layout {
-  size_t z = 0, vhat = 0, xc = 0, snap = 0, total = 0;
+  size_t z = 0, vhat = 0, xc = 0, snap = 0, scores = 0, w0b = 0, total = 0;
 };
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -235,9 +235,13 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if (opts) o = *opts;
   if (o.pad_mode != ITTT_PAD_CHUNK && o.pad_mode != ITTT_PAD_SEQUENCE)
     return fail(ITTT_ERR_INVALID_ARG, "pad_mode %d", int(o.pad_mode));
-  if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV))
+  if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV | ITTT_FLAG_DUAL))
     return fail(ITTT_ERR_INVALID_ARG, "unknown flags 0x%x", unsigned(o.flags));
   const bool fused = (o.flags & ITTT_FLAG_FUSED_CONV) != 0;
+  const bool dual = (o.flags & ITTT_FLAG_DUAL) != 0;
+  if (dual && (o.state_out || o.snap_buf))
+    return fail(ITTT_ERR_UNSUPPORTED,
+                "the dual form forms no fast-weight state: no state_out or snap_buf");
   if (H == nullptr || H->ndim != 3)
     return fail(ITTT_ERR_INVALID_ARG, "H: expected a [B,T,d] descriptor");
   const int64_t B = H->shape[0], T = H->shape[1], d = H->shape[2];
@@ -285,8 +289,19 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if ((s = device_state(&ds))) return s;
 
   // Scratch.
-  const Layout L = plan_workspace(B, T, d, f, chunk, o.z_buf == nullptr, o.vhat_buf == nullptr,
-                                  !fused, o.snap_buf == nullptr);
+  // The dual form needs the scores and, unless W_0 is one bf16 matrix
+  // already, a bf16 copy of each sequence's W_0 instead of the snapshots.
+  const bool w0_is_bf16 = !o.state_in && W_down0->dtype == ITTT_BF16;
+  Layout L = plan_workspace(B, T, d, f, chunk, o.z_buf == nullptr, o.vhat_buf == nullptr, !fused,
+                            !dual && o.snap_buf == nullptr);
+  if (dual) {
+    L.scores = L.total;
+    L.total += round_up(size_t(B) * T * T * 2);
+    if (!w0_is_bf16) {
+      L.w0b = L.total;
+      L.total += round_up(size_t(o.state_in ? B : 1) * d * f * 2);
+    }
+  }
   ScratchGuard guard;
   uint8_t* ws = nullptr;
   if (o.workspace) {
@@ -327,7 +342,17 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if ((s = make_map(&tm_vmn, vhat, d, M, 64, 64, "Vhat"))) return s;
   if ((s = make_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
   if ((s = make_map(&tm_zk, z, f, M, 64, 128, "Z (apply)"))) return s;
-  if ((s = make_map(&tm_snap, snap, f, uint64_t(B * n * d), 64, 256, "snapshots"))) return s;
+  CUtensorMap tm_zs, tm_w0b, tm_sc;
+  auto* scores = reinterpret_cast<__nv_bfloat16*>(ws + L.scores);
+  const void* w0b = w0_is_bf16 ? W_down0->data : static_cast<const void*>(ws + L.w0b);
+  if (dual) {
+    if ((s = make_map(&tm_zs, z, f, M, 64, 256, "Z (scores)"))) return s;
+    if ((s = make_map(&tm_w0b, w0b, f, uint64_t((o.state_in ? B : 1) * d), 64, 256, "bf16 W_0")))
+      return s;
+    if ((s = make_map(&tm_sc, scores, uint64_t(T), M, 64, 128, "scores"))) return s;
+  } else if ((s = make_map(&tm_snap, snap, f, uint64_t(B * n * d), 64, 256, "snapshots"))) {
+    return s;
+  }
 
   const ittt::LaunchEnv env{stream, ds->num_sms, ds->status};
   const void* w0 = o.state_in ? o.state_in->data : W_down0->data;
@@ -361,31 +386,51 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
             "gate/up launch");
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_SNAPSHOT0, stream), "event record");
-  ITTT_STEP(ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride, snap, int(B), int(n), int(d),
-                                   int(f)),
-            "snapshot launch");
+  if (!dual) {
+    ITTT_STEP(ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride, snap, int(B), int(n), int(d),
+                                     int(f)),
+              "snapshot launch");
+  } else if (!w0_is_bf16) {
+    ITTT_STEP(ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride,
+                                     static_cast<__nv_bfloat16*>(const_cast<void*>(w0b)),
+                                     int(o.state_in ? B : 1), 1, int(d), int(f)),
+              "W_0 copy launch");
+  }
   ITTT_STEP(rec(2 * ITTT_PHASE_SNAPSHOT0 + 1, stream), "event record");
-  ittt::UpdateArgs ua;
-  ua.B = int(B);
-  ua.T = int(T);
-  ua.d = int(d);
-  ua.f = int(f);
-  ua.C = int(chunk);
-  ua.n = int(n);
-  ua.n_upd = o.state_out ? int(n) : int(n - 1);
-  ua.w0 = w0;
-  ua.w0_fp32 = w0_fp32;
-  ua.w0_bstride = w0_bstride;
-  ua.snap = snap;
-  ua.state_out = o.state_out ? static_cast<float*>(o.state_out->data) : nullptr;
-  ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");
-  ITTT_STEP(ittt::launch_update(env, tm_vmn, tm_zmn, ua), "update launch");
-  ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
-  ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
-  ITTT_STEP(ittt::launch_apply(env, tm_zk, tm_snap, out->data, out->dtype == ITTT_FP32, int(B),
-                               int(T), int(d), int(f), int(chunk)),
-            "apply launch");
-  ITTT_STEP(rec(2 * ITTT_PHASE_APPLY + 1, stream), "event record");
+  if (!dual) {
+    ittt::UpdateArgs ua;
+    ua.B = int(B);
+    ua.T = int(T);
+    ua.d = int(d);
+    ua.f = int(f);
+    ua.C = int(chunk);
+    ua.n = int(n);
+    ua.n_upd = o.state_out ? int(n) : int(n - 1);
+    ua.w0 = w0;
+    ua.w0_fp32 = w0_fp32;
+    ua.w0_bstride = w0_bstride;
+    ua.snap = snap;
+    ua.state_out = o.state_out ? static_cast<float*>(o.state_out->data) : nullptr;
+    ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");
+    ITTT_STEP(ittt::launch_update(env, tm_vmn, tm_zmn, ua), "update launch");
+    ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
+    ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
+    ITTT_STEP(ittt::launch_apply(env, tm_zk, tm_snap, out->data, out->dtype == ITTT_FP32,
+                                 int(B), int(T), int(d), int(f), int(chunk)),
+              "apply launch");
+    ITTT_STEP(rec(2 * ITTT_PHASE_APPLY + 1, stream), "event record");
+  } else {
+    ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");
+    ITTT_STEP(ittt::launch_scores(env, tm_zk, tm_zs, scores, int(B), int(T), int(f), int(chunk)),
+              "scores launch");
+    ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
+    ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
+    ITTT_STEP(ittt::launch_dual_apply(env, tm_zk, tm_w0b, tm_sc, tm_vmn, o.state_in != nullptr,
+                                      out->data, out->dtype == ITTT_FP32, int(B), int(T), int(d),
+                                      int(f), int(chunk)),
+              "dual apply launch");
+    ITTT_STEP(rec(2 * ITTT_PHASE_APPLY + 1, stream), "event record");
+  }
 #undef ITTT_STEP
   if (what != nullptr) return cuda_fail(e, what);
   return ITTT_OK;

@@ -1,0 +1,271 @@
+// k_dual.cu -- the dual (attention-like) form of the chunk-wise apply:
+//   O_[i] = Z_[i] W_0^T + eta * sum_{j<i} (Z_[i] Z_[j]^T) Vhat_[j]
+// i.e. the apply step with W_i = W_0 + eta * sum_{j<i} Vhat_[j]^T Z_[j]
+// ("[논문리뷰] In-Place Test-Time Training", Method §1 eq. (3), §2 eq. (6);
+// the block-causal mask view of apply/update orderings in "[논문리뷰]
+// Test-Time Training Done Right", "Apply 연산과 Update 연산의 실행 순서").
+//
+// Two tcgen05 kernels:
+//   scores: S[t, s] = Z_t . Z_s for every token s of an earlier chunk than t
+//           (a 128 x 256 tile per unit, K = d_ff), rounded once to bf16 into
+//           a [B, T, T] buffer whose strictly block-lower part is the only
+//           part ever written or read;
+//   apply:  one accumulator per 128 x 256 output tile takes first
+//           Z_[i] W_0^T (K = d_ff, both operands K-major) and then
+//           S_[i] (eta Vhat) over the tokens of chunks 0..i-1 (S K-major,
+//           eta*Vhat read MN-major), so the instruction and shared-memory
+//           descriptors change inside the accumulation.
+// The dual form does no state update at all, and its work grows with the
+// square of the context: per chunk i it costs 2*C*d*f + i*2*C^2*(d + f)
+// FLOPs against 4*C*d*f for the primal apply and update, so the primal walk
+// is the default schedule.
+#include "kernels.h"
+#include "pipeline.cuh"
+
+namespace ittt {
+namespace {
+
+constexpr uint32_t kMnBox = 64 * 64 * 2;  // one {64 cols, 64 tokens} box
+
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int k) {
+  return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
+}
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int k) {
+  return sdesc_sw128(base + uint32_t(k) * 2048u, kMnBox, 1024u);
+}
+
+struct ScoresParams {
+  CUtensorMap tm_zq;    // Z [B*T, f] box {64, 128}  (rows t)
+  CUtensorMap tm_zk;    // Z [B*T, f] box {64, 256}  (rows s)
+  __nv_bfloat16* s;     // [B, T, T]
+  int B, T, C, n, mtpc, nt_max, kblocks;
+};
+
+struct ScoresSched : SchedDefaults {
+  using Params = ScoresParams;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, false);
+
+  const Params& p;
+  int arow0 = 0, brow0 = 0, rows_valid = 0, cols_valid = 0, acc = 0, b = 0, t0 = 0, s0 = 0;
+  bool live = false;
+
+  __device__ explicit ScoresSched(const Params& pp) : p(pp) {}
+  __device__ int num_units() const { return p.B * (p.n - 1) * p.mtpc * p.nt_max; }
+  __device__ void begin_unit(int u, int local) {
+    const int nt = u % p.nt_max;
+    int r = u / p.nt_max;
+    const int mt = r % p.mtpc;
+    r /= p.mtpc;
+    const int i = 1 + r % (p.n - 1);
+    b = r / (p.n - 1);
+    t0 = i * p.C + mt * kBM;
+    s0 = nt * kBN;
+    live = s0 < i * p.C;  // only tokens of earlier chunks
+    arow0 = b * p.T + t0;
+    brow0 = b * p.T + s0;
+    rows_valid = min(kBM, p.C - mt * kBM);
+    cols_valid = min(kBN, i * p.C - s0);
+    acc = local & 1;
+  }
+  __device__ int num_segments() const { return live ? 1 : 0; }
+  __device__ int seg_acc(int) const { return acc; }
+  __device__ int seg_kblocks(int) const { return p.kblocks; }
+  __device__ bool seg_fresh(int) const { return true; }
+  __device__ void load(int, int kb, uint8_t* stage, uint64_t* bar) const {
+    const int k = kb * kBK;
+    tma_load_2d(stage, &p.tm_zq, bar, k, arow0);
+    tma_load_2d(stage + kATileBytes, &p.tm_zk, bar, k, brow0);
+  }
+  static __device__ uint64_t a_desc(uint32_t base, int k) { return kmajor_desc(base, k); }
+  static __device__ uint64_t b_desc(uint32_t base, int k) { return kmajor_desc(base, k); }
+
+  __device__ void epilogue(int, int row, uint32_t trow) const {
+    const bool row_ok = row < rows_valid;
+    __nv_bfloat16* srow = p.s + (size_t(b) * p.T + size_t(t0 + (row_ok ? row : 0))) * size_t(p.T);
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 32) {
+      uint32_t v[32];
+      tmem_ld_32cols(trow + uint32_t(c), v);
+      tmem_wait_ld();
+      pin_regs(v);
+      if (!row_ok) continue;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int cc = c + 8 * q;
+        if (cc < cols_valid) {
+          *reinterpret_cast<uint4*>(srow + s0 + cc) = make_uint4(
+              pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+              pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+              pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+              pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+        }
+      }
+    }
+  }
+};
+
+struct DualParams {
+  CUtensorMap tm_z;   // Z        [B*T, f]   box {64, 128}
+  CUtensorMap tm_w0;  // bf16 W_0 [Bw*d, f]  box {64, 256}
+  CUtensorMap tm_s;   // scores   [B*T, T]   box {64, 128}
+  CUtensorMap tm_v;   // eta*Vhat [B*T, d]   box {64, 64} (read MN-major)
+  void* out;
+  int out_fp32;
+  int w0_per_seq;
+  int B, T, d, C, n, mtpc, nt, kf;
+};
+
+struct DualSched : SchedDefaults {
+  using Params = DualParams;
+  static constexpr bool kMixedOperands = true;
+  static constexpr uint32_t kIdescKK = idesc_bf16_f32(kBM, kBN, false, false);
+  static constexpr uint32_t kIdescKM = idesc_bf16_f32(kBM, kBN, false, true);
+  static constexpr uint32_t kIdesc = kIdescKK;
+
+  const Params& p;
+  int b = 0, i = 0, arow0 = 0, n0 = 0, rows_valid = 0, acc = 0, wrow0 = 0;
+
+  __device__ explicit DualSched(const Params& pp) : p(pp) {}
+  __device__ int num_units() const { return p.B * p.n * p.mtpc * p.nt; }
+  // Latest chunks (longest K) first.
+  __device__ void begin_unit(int u, int local) {
+    const int nt = u % p.nt;
+    int r = u / p.nt;
+    const int mt = r % p.mtpc;
+    r /= p.mtpc;
+    i = p.n - 1 - (r % p.n);
+    b = r / p.n;
+    arow0 = b * p.T + i * p.C + mt * kBM;
+    n0 = nt * kBN;
+    rows_valid = min(kBM, p.C - mt * kBM);
+    wrow0 = (p.w0_per_seq ? b * p.d : 0) + n0;
+    acc = local & 1;
+  }
+  __device__ int num_segments() const { return 1; }
+  __device__ int seg_acc(int) const { return acc; }
+  __device__ int seg_kblocks(int) const { return p.kf + i * p.C / kBK; }
+  __device__ bool seg_fresh(int) const { return true; }
+
+  __device__ void load(int, int kb, uint8_t* stage, uint64_t* bar) const {
+    if (kb < p.kf) {
+      const int k = kb * kBK;
+      tma_load_2d(stage, &p.tm_z, bar, k, arow0);
+      tma_load_2d(stage + kATileBytes, &p.tm_w0, bar, k, wrow0);
+    } else {
+      const int s0 = (kb - p.kf) * kBK;  // token of an earlier chunk
+      tma_load_2d(stage, &p.tm_s, bar, s0, arow0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        tma_load_2d(stage + kATileBytes + q * kMnBox, &p.tm_v, bar, n0 + 64 * q, b * p.T + s0);
+    }
+  }
+  __device__ uint32_t idesc(int, int kb) const { return kb < p.kf ? kIdescKK : kIdescKM; }
+  __device__ uint64_t a_desc(int, int, uint32_t base, int k) const { return kmajor_desc(base, k); }
+  __device__ uint64_t b_desc(int, int kb, uint32_t base, int k) const {
+    return kb < p.kf ? kmajor_desc(base, k) : mnmajor_desc(base, k);
+  }
+
+  __device__ void epilogue(int, int row, uint32_t trow) const {
+    const bool row_ok = row < rows_valid;
+    const size_t grow = size_t(arow0 + (row_ok ? row : 0));
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 32) {
+      uint32_t v[32];
+      tmem_ld_32cols(trow + uint32_t(c), v);
+      tmem_wait_ld();
+      pin_regs(v);
+      if (!row_ok) continue;
+      if (p.out_fp32) {
+        float* orow = static_cast<float*>(p.out) + grow * size_t(p.d);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int col = n0 + c + 4 * q;
+          if (col < p.d)
+            *reinterpret_cast<uint4*>(orow + col) =
+                make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      } else {
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * size_t(p.d);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int col = n0 + c + 8 * q;
+          if (col < p.d)
+            *reinterpret_cast<uint4*>(orow + col) = make_uint4(
+                pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+        }
+      }
+    }
+  }
+};
+
+__global__ void __launch_bounds__(PipeShape<ScoresSched>::kThreads, 1)
+    scores_kernel(const __grid_constant__ ScoresParams p, unsigned int* status) {
+  run_pipeline<ScoresSched>(p, status);
+}
+
+__global__ void __launch_bounds__(PipeShape<DualSched>::kThreads, 1)
+    dual_apply_kernel(const __grid_constant__ DualParams p, unsigned int* status) {
+  run_pipeline<DualSched>(p, status);
+}
+
+}  // namespace
+
+cudaError_t launch_scores(const LaunchEnv& env, const CUtensorMap& tm_zq, const CUtensorMap& tm_zk,
+                          __nv_bfloat16* s, int B, int T, int f, int C) {
+  ScoresParams p;
+  p.tm_zq = tm_zq;
+  p.tm_zk = tm_zk;
+  p.s = s;
+  p.B = B;
+  p.T = T;
+  p.C = C;
+  p.n = T / C;
+  p.mtpc = (C + kBM - 1) / kBM;
+  p.nt_max = ((p.n - 1) * C + kBN - 1) / kBN;
+  p.kblocks = (f + kBK - 1) / kBK;
+  if (p.n < 2) return cudaSuccess;
+  const int64_t units = int64_t(B) * (p.n - 1) * p.mtpc * p.nt_max;
+  cudaError_t e = cudaFuncSetAttribute(scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(pipe_smem_bytes<ScoresSched>()));
+  if (e != cudaSuccess) return e;
+  const int grid = units < env.num_sms ? int(units) : env.num_sms;
+  scores_kernel<<<grid, PipeShape<ScoresSched>::kThreads, pipe_smem_bytes<ScoresSched>(),
+                  env.stream>>>(p, env.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dual_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
+                              const CUtensorMap& tm_w0, const CUtensorMap& tm_s,
+                              const CUtensorMap& tm_v, bool w0_per_seq, void* out, bool out_fp32,
+                              int B, int T, int d, int f, int C) {
+  DualParams p;
+  p.tm_z = tm_z;
+  p.tm_w0 = tm_w0;
+  p.tm_s = tm_s;
+  p.tm_v = tm_v;
+  p.out = out;
+  p.out_fp32 = out_fp32 ? 1 : 0;
+  p.w0_per_seq = w0_per_seq ? 1 : 0;
+  p.B = B;
+  p.T = T;
+  p.d = d;
+  p.C = C;
+  p.n = T / C;
+  p.mtpc = (C + kBM - 1) / kBM;
+  p.nt = (d + kBN - 1) / kBN;
+  p.kf = (f + kBK - 1) / kBK;
+  const int64_t units = int64_t(B) * p.n * p.mtpc * p.nt;
+  cudaError_t e = cudaFuncSetAttribute(dual_apply_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(pipe_smem_bytes<DualSched>()));
+  if (e != cudaSuccess) return e;
+  const int grid = units < env.num_sms ? int(units) : env.num_sms;
+  dual_apply_kernel<<<grid, PipeShape<DualSched>::kThreads, pipe_smem_bytes<DualSched>(),
+                      env.stream>>>(p, env.status);
+  return cudaGetLastError();
+}
+
+}  // namespace ittt

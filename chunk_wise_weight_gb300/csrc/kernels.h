@@ -67,6 +67,22 @@ cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
                          const CUtensorMap& tm_snap, void* out, bool out_fp32, int B, int T,
                          int d, int f, int C);
 
+// Dual form, scores: S[b, t, s] = Z_t . Z_s (bf16) for every token t of chunk
+// i >= 1 and every token s < i*C of the same sequence.  Tensor maps: Z
+// [B*T, f] with box {64,128} (tm_zq) and box {64,256} (tm_zk).
+cudaError_t launch_scores(const LaunchEnv& env, const CUtensorMap& tm_zq,
+                          const CUtensorMap& tm_zk, __nv_bfloat16* s, int B, int T, int f,
+                          int C);
+
+// Dual form, apply: O_[i] = Z_[i] W_0^T + S_[i, <iC] (eta Vhat)_[<iC].  Tensor
+// maps: Z [B*T, f] box {64,128}; bf16 W_0 [Bw*d, f] box {64,256} (Bw = B
+// when w0_per_seq, else 1); S [B*T, T] box {64,128}; eta*Vhat [B*T, d] box
+// {64,64}.
+cudaError_t launch_dual_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
+                              const CUtensorMap& tm_w0, const CUtensorMap& tm_s,
+                              const CUtensorMap& tm_v, bool w0_per_seq, void* out, bool out_fp32,
+                              int B, int T, int d, int f, int C);
+
 // Defined in ittt_api.cu, for entry points in other translation units.
 cudaError_t status_word_address(unsigned int** out);
 void set_last_error(const char* msg);

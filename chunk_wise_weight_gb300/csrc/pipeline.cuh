@@ -69,6 +69,12 @@ struct SchedDefaults {
   static constexpr uint32_t kExtraStageBytes = 0;
   static constexpr int kBuilderWarps = 0;
   static constexpr bool kPreload = false;
+  // With kMixedOperands the MMA asks the schedule for each K block's
+  // instruction and shared-memory descriptors (operand major-ness may change
+  // inside one accumulation):
+  //   uint32_t idesc(int s, int kb); uint64_t a_desc(int s, int kb, uint32_t
+  //   base, int k16); uint64_t b_desc(int s, int kb, uint32_t base, int k16)
+  static constexpr bool kMixedOperands = false;
   // Transaction bytes the producer's copies deliver into a stage.
   __device__ uint32_t tma_bytes(int, int) const { return kStageBytes; }
 };
@@ -207,10 +213,19 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
             tc_fence_after_sync();
             const uint32_t a_base = smem_u32(smem + size_t(stage) * kStride);
             const uint32_t b_base = a_base + kATileBytes;
+            if constexpr (S::kMixedOperands) {
+              const uint32_t id = sched.idesc(s, kb);
 #pragma unroll
-            for (int k = 0; k < kBK / kUmmaK; ++k) {
-              mma_bf16(d_tmem, S::a_desc(a_base, k), S::b_desc(b_base, k), S::kIdesc,
-                       (fresh && kb == 0 && k == 0) ? 0u : 1u);
+              for (int k = 0; k < kBK / kUmmaK; ++k) {
+                mma_bf16(d_tmem, sched.a_desc(s, kb, a_base, k), sched.b_desc(s, kb, b_base, k),
+                         id, (fresh && kb == 0 && k == 0) ? 0u : 1u);
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < kBK / kUmmaK; ++k) {
+                mma_bf16(d_tmem, S::a_desc(a_base, k), S::b_desc(b_base, k), S::kIdesc,
+                         (fresh && kb == 0 && k == 0) ? 0u : 1u);
+              }
             }
             mma_commit(&sync->empty[stage]);
             if (++stage == NS) {

@@ -23,6 +23,7 @@ BF16, FP32 = 0, 1
 PAD_CHUNK, PAD_SEQUENCE = 0, 1
 PHASES = ("conv", "target", "gateup", "snapshot0", "update", "apply")
 FLAG_FUSED_CONV = 1
+FLAG_DUAL = 2
 
 _DTYPES = {torch.bfloat16: BF16, torch.float32: FP32}
 
@@ -132,7 +133,7 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
             out: torch.Tensor | None = None, *, out_dtype=torch.bfloat16, stream=None,
             pad_mode: int = PAD_CHUNK, state_in=None, state_out=None, z_buf=None,
             vhat_buf=None, snap_buf=None, workspace=None, events=None,
-            fused_conv: bool = False) -> torch.Tensor:
+            fused_conv: bool = False, dual: bool = False) -> torch.Tensor:
     """Enqueue one layer forward on `stream` (default: current stream) and
     return `out` [B,T,d].  Extra keyword buffers map to ittt_opts; `events`
     is a list of 2 * len(PHASES) torch.cuda.Event(enable_timing=True): a
@@ -143,7 +144,7 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
     keep = [describe(x) for x in (H, X0, W_gate, W_up, W_down0, W_target, conv_w, out)]
     opts = Opts()
     opts.pad_mode = int(pad_mode)
-    opts.flags = FLAG_FUSED_CONV if fused_conv else 0
+    opts.flags = (FLAG_FUSED_CONV if fused_conv else 0) | (FLAG_DUAL if dual else 0)
     extra = {}
     for name, t in (("state_in", state_in), ("state_out", state_out), ("z_buf", z_buf),
                     ("vhat_buf", vhat_buf), ("snap_buf", snap_buf)):

@@ -130,6 +130,13 @@ typedef struct {
  * Same results; slower on GB300, where the fused convolution is repeated for
  * every 256-column output tile. */
 #define ITTT_FLAG_FUSED_CONV 1
+/* Compute O with the dual form O_[i] = Z_[i] W_0^T + eta sum_{j<i}
+ * (Z_[i] Z_[j]^T) Vhat_[j] instead of walking the fast-weight state: a
+ * scores kernel writes the block-lower part of Z Z^T (bf16, B*T*T*2 bytes of
+ * scratch) and one GEMM accumulates both terms.  Same layer, different
+ * rounding; more work than the primal walk on every workload measured, so
+ * it is never the default.  Not combinable with state_out or snap_buf. */
+#define ITTT_FLAG_DUAL 2
 
 /* Kernel phases of one forward call, in launch order. */
 typedef enum {
@@ -138,8 +145,10 @@ typedef enum {
   ITTT_PHASE_TARGET = 1,    /* eta*Vhat = eta * Xc W_target^T (tensor cores) */
   ITTT_PHASE_GATEUP = 2,    /* Z = SiLU(H W_gate^T) * (H W_up^T) (tensor cores) */
   ITTT_PHASE_SNAPSHOT0 = 3, /* bf16 copy of the initial fast weight */
-  ITTT_PHASE_UPDATE = 4,    /* prefix walk of Vhat^T Z, snapshots W_1..W_{n-1} */
-  ITTT_PHASE_APPLY = 5      /* O_[i] = Z_[i] W_i^T (tensor cores) */
+  ITTT_PHASE_UPDATE = 4,    /* prefix walk of Vhat^T Z, snapshots W_1..W_{n-1}
+                               (dual form: the scores Z Z^T) */
+  ITTT_PHASE_APPLY = 5      /* O_[i] = Z_[i] W_i^T (tensor cores; dual form:
+                               Z_[i] W_0^T + S_[i] eta Vhat) */
 } ittt_phase;
 #define ITTT_NUM_PHASES 6
 
@@ -197,8 +206,9 @@ ITTT_API ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_tenso
                                           ittt_tensor* out, ittt_stream_t stream);
 
 /*
- * Bytes of device scratch one call needs for these sizes when the caller
- * supplies no z_buf / vhat_buf / snap_buf (0 if the sizes are unsupported).
+ * Bytes of device scratch one call needs for these sizes with default flags
+ * when the caller supplies no z_buf / vhat_buf / snap_buf (0 if the sizes
+ * are unsupported).
  */
 ITTT_API size_t ittt_workspace_bytes(int64_t B, int64_t T, int64_t d, int64_t f,
                             int64_t chunk);

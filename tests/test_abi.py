@@ -108,9 +108,15 @@ def test_rejects_bad_options(lib):
     o.pad_mode = 7
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     o = ittt.Opts()
-    o.flags = 6
+    o.flags = 4
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     assert "flags" in ittt.last_error()
+    o = ittt.Opts()
+    o.flags = ittt.FLAG_DUAL
+    st = _desc([1, 64, 256], ittt.FP32, data=FAKE * 9 * 1024)
+    o.state_out = ctypes.pointer(st)
+    assert _call(lib, a, opts=o) == ittt.ERR_UNSUPPORTED
+    assert "dual" in ittt.last_error()
     o = ittt.Opts()
     bad = _desc([1, 64, 256], ittt.BF16, data=FAKE * 9 * 1024)   # state_out wrong dtype/shape
     o.state_out = ctypes.pointer(bad)

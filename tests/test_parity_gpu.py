@@ -49,7 +49,7 @@ def to_device(inp, dev, w0_dtype=torch.bfloat16):
 
 
 def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
-        state_in=None, want_state=False, fused_conv=False):
+        state_in=None, want_state=False, fused_conv=False, dual=False):
     B, T, d = g["H"].shape
     f = g["W_gate"].shape[0]
     dev = g["H"].device
@@ -57,7 +57,8 @@ def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
     if intermediates:
         kw["z_buf"] = torch.empty(B, T, f, dtype=torch.bfloat16, device=dev)
         kw["vhat_buf"] = torch.empty(B, T, d, dtype=torch.bfloat16, device=dev)
-        kw["snap_buf"] = torch.empty(B, T // C, d, f, dtype=torch.bfloat16, device=dev)
+        if not dual:
+            kw["snap_buf"] = torch.empty(B, T // C, d, f, dtype=torch.bfloat16, device=dev)
     if want_state:
         kw["state_out"] = torch.empty(B, d, f, dtype=torch.float32, device=dev)
     if state_in is not None:
@@ -65,7 +66,7 @@ def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
     out = ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"],
                        None if state_in is not None else g["W_down0"], g["W_target"],
                        g["conv_w"], eta, C, out_dtype=out_dtype, pad_mode=pad_mode,
-                       fused_conv=fused_conv, **kw)
+                       fused_conv=fused_conv, dual=dual, **kw)
     ittt.stream_status()
     res = {"O": out}
     res.update(kw)
@@ -170,6 +171,43 @@ def test_state_out_and_streaming_continuation(cuda_device):
 
 
 # --------------------------------------------------------------------------
+# The dual schedule (scores Z Z^T instead of the fast-weight walk)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", SHAPES)
+def test_dual_form_parity(cuda_device, B, T, d, f, C, eta):
+    inp = make_inputs(B, T, d, f, seed=500 + T + d)
+    ref = oracle.forward(inp, eta, C)
+    got = run(to_device(inp, cuda_device), eta, C, dual=True)
+    assert_parity(host(got["O"]), ref["O"], "O (dual)")
+
+
+def test_dual_form_variants(cuda_device):
+    """fp32 output, fp32 W_0, per-sequence initial state, fused conv."""
+    B, T, d, f, C, eta = 2, 512, 192, 320, 128, 0.05
+    inp = make_inputs(B, T, d, f, seed=17)
+    ref = oracle.forward(inp, eta, C)
+    g = to_device(inp, cuda_device, w0_dtype=torch.float32)
+    got = run(g, eta, C, dual=True, out_dtype=torch.float32, fused_conv=True)
+    assert_parity(host(got["O"]), ref["O"], "O (dual, fp32 out, fp32 W_0, fused conv)")
+    st = torch.stack([g["W_down0"], -g["W_down0"]]).contiguous()
+    binp = dict(inp)
+    binp["W_down0"] = torch.stack([inp["W_down0"], -inp["W_down0"]])
+    ref2 = oracle.forward(binp, eta, C)
+    got2 = run(g, eta, C, dual=True, state_in=st)
+    assert_parity(host(got2["O"]), ref2["O"], "O (dual, per-sequence W_0)")
+    got3 = run(g, eta, C, state_in=st)
+    assert_parity(host(got3["O"]), ref2["O"], "O (primal, per-sequence W_0)")
+
+
+def test_dual_form_rejects_state_outputs(cuda_device):
+    g = to_device(make_inputs(1, 256, 64, 256, seed=18), cuda_device)
+    with pytest.raises(ittt.IttError) as e:
+        run(g, 0.1, 64, dual=True, want_state=True)
+    assert e.value.status == ittt.ERR_UNSUPPORTED
+
+
+# --------------------------------------------------------------------------
 # Structural properties, bit-exact on the GPU path
 # --------------------------------------------------------------------------
 
@@ -231,7 +269,7 @@ def test_status_and_argument_errors_on_device(cuda_device):
 # Full-size named workloads: sampled entries against the oracle
 # --------------------------------------------------------------------------
 
-def _sampled_checks(index, device, n_state_pairs=24, n_rows=6):
+def _sampled_checks(index, device, n_state_pairs=24, n_rows=6, dual=False):
     cfg, inp = config_inputs(index)
     B, T, d, f, C, eta = cfg["B"], cfg["T"], cfg["d"], cfg["f"], cfg["C"], cfg["eta"]
     n = T // C
