@@ -201,6 +201,22 @@ Layout plan_workspace(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
 }
 
 // ------------------------------------------------------------- tensor maps
+// 3-D bf16 map {inner, mid, outer} of a dense tensor, 128-byte swizzle.
+ittt_status make_map_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid,
+                   uint64_t outer, uint32_t box_inner, uint32_t box_mid, const char* what) {
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
+  cuuint32_t box[3] = {box_inner, box_mid, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ITTT_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, int(r));
+  return ITTT_OK;
+}
+
 ittt_status make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                      uint32_t box_inner, uint32_t box_outer, const char* what) {
   cuuint64_t dims[2] = {inner, outer};
@@ -339,6 +355,14 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     return s;
   }
   if ((s = make_map(&tm_wt, W_target->data, d, d, 64, 256, "W_target"))) return s;
+  // Output maps for the epilogues' TMA stores (Z's is tm_zk).
+  CUtensorMap tm_vs, tm_ss, tm_os;
+  memset(&tm_ss, 0, sizeof(tm_ss));
+  memset(&tm_os, 0, sizeof(tm_os));
+  if ((s = make_map(&tm_vs, vhat, d, M, 64, 128, "Vhat (store)"))) return s;
+  if (out->dtype == ITTT_BF16 &&
+      (s = make_map_3d(&tm_os, out->data, d, chunk, uint64_t(B * n), 64, 128, "O (store)")))
+    return s;
   if ((s = make_map(&tm_vmn, vhat, d, M, 64, 64, "Vhat"))) return s;
   if ((s = make_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
   if ((s = make_map(&tm_zk, z, f, M, 64, 128, "Z (apply)"))) return s;
@@ -350,8 +374,10 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     if ((s = make_map(&tm_w0b, w0b, f, uint64_t((o.state_in ? B : 1) * d), 64, 256, "bf16 W_0")))
       return s;
     if ((s = make_map(&tm_sc, scores, uint64_t(T), M, 64, 128, "scores"))) return s;
-  } else if ((s = make_map(&tm_snap, snap, f, uint64_t(B * n * d), 64, 256, "snapshots"))) {
-    return s;
+  } else {
+    if ((s = make_map(&tm_snap, snap, f, uint64_t(B * n * d), 64, 256, "snapshots"))) return s;
+    if ((s = make_map_3d(&tm_ss, snap, f, d, uint64_t(B * n), 64, 128, "snapshots (store)")))
+      return s;
   }
 
   const ittt::LaunchEnv env{stream, ds->num_sms, ds->status};
@@ -377,12 +403,12 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   }
   ITTT_STEP(rec(2 * ITTT_PHASE_CONV + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_TARGET, stream), "event record");
-  ITTT_STEP(ittt::launch_target(env, tm_a, tm_wt, cw, vhat, eta, int(M), int(T), int(d),
+  ITTT_STEP(ittt::launch_target(env, tm_a, tm_wt, tm_vs, cw, vhat, eta, int(M), int(T), int(d),
                                 int(chunk), int(o.pad_mode), fused),
             "target launch");
   ITTT_STEP(rec(2 * ITTT_PHASE_TARGET + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP, stream), "event record");
-  ITTT_STEP(ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, z, int(M), int(f), int(d)),
+  ITTT_STEP(ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d)),
             "gate/up launch");
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_SNAPSHOT0, stream), "event record");
@@ -412,11 +438,12 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     ua.snap = snap;
     ua.state_out = o.state_out ? static_cast<float*>(o.state_out->data) : nullptr;
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");
-    ITTT_STEP(ittt::launch_update(env, tm_vmn, tm_zmn, ua), "update launch");
+    ITTT_STEP(ittt::launch_update(env, tm_vmn, tm_zmn, tm_ss, ua), "update launch");
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
-    ITTT_STEP(ittt::launch_apply(env, tm_zk, tm_snap, out->data, out->dtype == ITTT_FP32,
-                                 int(B), int(T), int(d), int(f), int(chunk)),
+    ITTT_STEP(ittt::launch_apply(env, tm_zk, tm_snap, tm_os, out->data,
+                                 out->dtype == ITTT_FP32, int(B), int(T), int(d), int(f),
+                                 int(chunk)),
               "apply launch");
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY + 1, stream), "event record");
   } else {

@@ -144,6 +144,22 @@ size_t na_bytes(const ittt_tensor* t) {
 
 size_t na_round(size_t x) { return (x + 255) & ~size_t(255); }
 
+// 3-D bf16 map {inner, mid, outer} of a dense tensor, 128-byte swizzle.
+ittt_status na_map_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid,
+                   uint64_t outer, uint32_t box_inner, uint32_t box_mid, const char* what) {
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
+  cuuint32_t box[3] = {box_inner, box_mid, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_na_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return na_fail(ITTT_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, int(r));
+  return ITTT_OK;
+}
+
 ittt_status na_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                    uint32_t box_inner, uint32_t box_outer, const char* what) {
   cuuint64_t dims[2] = {inner, outer};
@@ -228,6 +244,14 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   if ((s = na_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
   if ((s = na_map(&tm_zk, z, f, M, 64, 128, "Z (apply)"))) return s;
   if ((s = na_map(&tm_snap, snap, f, uint64_t(B * n * d), 64, 256, "snapshots"))) return s;
+  CUtensorMap tm_vs, tm_ss, tm_os;
+  memset(&tm_os, 0, sizeof(tm_os));
+  if ((s = na_map(&tm_vs, vhat, d, M, 64, 128, "Vhat (store)"))) return s;
+  if ((s = na_map_3d(&tm_ss, snap, f, d, uint64_t(B * n), 64, 128, "snapshots (store)")))
+    return s;
+  if (out->dtype == ITTT_BF16 &&
+      (s = na_map_3d(&tm_os, out->data, d, chunk, uint64_t(B * n), 64, 128, "O (store)")))
+    return s;
 
   const ittt::LaunchEnv env{stream, nd->num_sms, nd->status};
   const bool w0_fp32 = W_down0->dtype == ITTT_FP32;
@@ -237,11 +261,12 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
                              static_cast<const float*>(conv_w->data), xc, int64_t(M), int(T),
                              int(d), int(chunk), ITTT_PAD_CHUNK)) != cudaSuccess) {
     what = "conv";
-  } else if ((e = ittt::launch_target(env, tm_xc, tm_wt, static_cast<const float*>(conv_w->data),
-                                      vhat, eta, int(M), int(T), int(d), int(chunk),
-                                      ITTT_PAD_CHUNK, false)) != cudaSuccess) {
+  } else if ((e = ittt::launch_target(env, tm_xc, tm_wt, tm_vs,
+                                      static_cast<const float*>(conv_w->data), vhat, eta, int(M),
+                                      int(T), int(d), int(chunk), ITTT_PAD_CHUNK, false)) !=
+             cudaSuccess) {
     what = "target";
-  } else if ((e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, z, int(M), int(f), int(d))) !=
+  } else if ((e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d))) !=
              cudaSuccess) {
     what = "gate/up";
   } else if ((e = ittt::launch_snapshot0(env, W_down0->data, w0_fp32, 0, snap, int(B), int(n),
@@ -261,11 +286,11 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
     ua.w0_bstride = 0;
     ua.snap = snap;
     ua.state_out = nullptr;
-    if ((e = ittt::launch_update(env, tm_vmn, tm_zmn, ua)) != cudaSuccess) {
+    if ((e = ittt::launch_update(env, tm_vmn, tm_zmn, tm_ss, ua)) != cudaSuccess) {
       what = "update";
-    } else if ((e = ittt::launch_apply(env, tm_zk, tm_snap, out->data, out->dtype == ITTT_FP32,
-                                       int(B), int(T), int(d), int(f), int(chunk))) !=
-               cudaSuccess) {
+    } else if ((e = ittt::launch_apply(env, tm_zk, tm_snap, tm_os, out->data,
+                                       out->dtype == ITTT_FP32, int(B), int(T), int(d), int(f),
+                                       int(chunk))) != cudaSuccess) {
       what = "apply";
     }
   }

@@ -16,6 +16,7 @@ namespace {
 struct ApplyParams {
   CUtensorMap tm_z;     // Z          [B*T, f]    box {64, 128}
   CUtensorMap tm_snap;  // snapshots  [B*n*d, f]  box {64, 256}
+  CUtensorMap tm_os;    // bf16 O as [B*n chunks][C rows][d cols], box {64, 128, 1} (store)
   void* out;            // O [B*T, d], bf16 or fp32
   int out_fp32;
   int B, T, d, f, C, n;
@@ -25,9 +26,10 @@ struct ApplyParams {
 struct ApplySched : SchedDefaults {
   using Params = ApplyParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, false);
+  static constexpr bool kStagedStores = true;
 
   const Params& p;
-  int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0;
+  int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0, chunk_id = 0, crow0 = 0;
 
   __device__ explicit ApplySched(const Params& pp) : p(pp) {}
   __device__ int num_units() const { return p.B * p.n * p.mt_per_chunk * p.nt; }
@@ -42,6 +44,8 @@ struct ApplySched : SchedDefaults {
     brow0 = (b * p.n + i) * p.d + nt * kBN;
     rows_valid = min(kBM, p.C - mt * kBM);
     n0 = nt * kBN;
+    chunk_id = b * p.n + i;
+    crow0 = mt * kBM;
     acc = local & 1;
   }
   __device__ int num_segments() const { return 1; }
@@ -61,7 +65,35 @@ struct ApplySched : SchedDefaults {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
   }
 
-  __device__ void epilogue(int, int row, uint32_t trow) const {
+  // bf16 O: four 64-column TMA stores through the chunk-bounded 3-D map
+  // (rows past the chunk and columns >= d are not written).  fp32 O: direct
+  // 16-byte stores.
+  __device__ void epilogue(int, int row, uint32_t trow, EpiStager& st) const {
+    if (!p.out_fp32) {
+#pragma unroll 1
+      for (int g = 0; g < kBN / 64; ++g) {
+        uint8_t* buf = st.acquire();
+#pragma unroll 1
+        for (int hc = 0; hc < 2; ++hc) {
+          uint32_t v[32];
+          tmem_ld_32cols(trow + uint32_t(g * 64 + hc * 32), v);
+          tmem_wait_ld();
+          pin_regs(v);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st.put(buf, hc * 4 + q,
+                   make_uint4(
+                       pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]))));
+        }
+        st.commit(buf, [&](uint8_t* src) {
+          tma_store_3d(&p.tm_os, src, n0 + g * 64, crow0, chunk_id);
+        });
+      }
+      return;
+    }
     const bool row_ok = row < rows_valid;
     const size_t grow = size_t(arow0 + (row_ok ? row : 0));
 #pragma unroll 1
@@ -106,10 +138,12 @@ __global__ void __launch_bounds__(PipeShape<ApplySched>::kThreads, 1)
 }  // namespace
 
 cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z, const CUtensorMap& tm_snap,
-                         void* out, bool out_fp32, int B, int T, int d, int f, int C) {
+                         const CUtensorMap& tm_os, void* out, bool out_fp32, int B, int T, int d,
+                         int f, int C) {
   ApplyParams p;
   p.tm_z = tm_z;
   p.tm_snap = tm_snap;
+  p.tm_os = tm_os;
   p.out = out;
   p.out_fp32 = out_fp32 ? 1 : 0;
   p.B = B;

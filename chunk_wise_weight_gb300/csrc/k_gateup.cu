@@ -20,7 +20,7 @@ struct GateUpParams {
   CUtensorMap tm_h;   // H      [M, K]  box {64, 128}
   CUtensorMap tm_wg;  // W_gate [f, K]  box {64, 128}
   CUtensorMap tm_wu;  // W_up   [f, K]  box {64, 128}
-  __nv_bfloat16* z;   // Z      [M, f]
+  CUtensorMap tm_zs;  // Z      [M, f]  box {64, 128}  (TMA store)
   int M, f;
   int m_tiles, n_tiles, kblocks, raster;
 };
@@ -28,6 +28,7 @@ struct GateUpParams {
 struct GateUpSched : SchedDefaults {
   using Params = GateUpParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false, false);
+  static constexpr bool kStagedStores = true;
 
   const Params& p;
   int m0 = 0, n0 = 0, acc = 0;
@@ -61,37 +62,35 @@ struct GateUpSched : SchedDefaults {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
   }
 
-  __device__ void epilogue(int, int row, uint32_t trow) const {
-    const int gm = m0 + row;
-    const bool row_ok = gm < p.M;
-    __nv_bfloat16* zrow = p.z + size_t(row_ok ? gm : 0) * size_t(p.f);
+  // 128 Z columns as two 64-column TMA stores; rows >= M and columns >= f
+  // fall outside the tensor map and are not written.
+  __device__ void epilogue(int, int, uint32_t trow, EpiStager& st) const {
 #pragma unroll 1
-    for (int c = 0; c < kGateUpTileN; c += 32) {
-      uint32_t g[32], u[32];
-      tmem_ld_32cols(trow + uint32_t(c), g);
-      tmem_ld_32cols(trow + uint32_t(kGateUpTileN + c), u);
-      tmem_wait_ld();
-      pin_regs(g);
-      pin_regs(u);
-      uint32_t pk[16];
+    for (int g = 0; g < kGateUpTileN / 64; ++g) {
+      uint8_t* buf = st.acquire();
+#pragma unroll 1
+      for (int hc = 0; hc < 2; ++hc) {
+        const int c = g * 64 + hc * 32;
+        uint32_t gv[32], uv[32];
+        tmem_ld_32cols(trow + uint32_t(c), gv);
+        tmem_ld_32cols(trow + uint32_t(kGateUpTileN + c), uv);
+        tmem_wait_ld();
+        pin_regs(gv);
+        pin_regs(uv);
+        uint32_t pk[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
-        const float u0 = __uint_as_float(u[2 * j]), u1 = __uint_as_float(u[2 * j + 1]);
-        const float z0 = g0 / (1.0f + __expf(-g0)) * u0;
-        const float z1 = g1 / (1.0f + __expf(-g1)) * u1;
-        pk[j] = pack_bf16x2(z0, z1);
-      }
-      if (row_ok) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int col = n0 + c + 8 * q;
-          if (col < p.f) {
-            *reinterpret_cast<uint4*>(zrow + col) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          }
+        for (int j = 0; j < 16; ++j) {
+          const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
+          const float u0 = __uint_as_float(uv[2 * j]), u1 = __uint_as_float(uv[2 * j + 1]);
+          const float z0 = g0 / (1.0f + __expf(-g0)) * u0;
+          const float z1 = g1 / (1.0f + __expf(-g1)) * u1;
+          pk[j] = pack_bf16x2(z0, z1);
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st.put(buf, hc * 4 + q, make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
       }
+      st.commit(buf, [&](uint8_t* src) { tma_store_2d(&p.tm_zs, src, n0 + g * 64, m0); });
     }
   }
 };
@@ -104,12 +103,12 @@ __global__ void __launch_bounds__(PipeShape<GateUpSched>::kThreads, 1)
 }  // namespace
 
 cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h, const CUtensorMap& tm_wg,
-                          const CUtensorMap& tm_wu, __nv_bfloat16* z, int M, int f, int K) {
+                          const CUtensorMap& tm_wu, const CUtensorMap& tm_zs, int M, int f, int K) {
   GateUpParams p;
   p.tm_h = tm_h;
   p.tm_wg = tm_wg;
   p.tm_wu = tm_wu;
-  p.z = z;
+  p.tm_zs = tm_zs;
   p.M = M;
   p.f = f;
   p.m_tiles = (M + kBM - 1) / kBM;

@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(256)
 struct TargetParams {
   CUtensorMap tm_a;      // split: Xc [M, d] box {64, 128}; fused: X0 [M, d] box {64, 130}
   CUtensorMap tm_wt;     // W_target [d, d]  box {64, 256}
+  CUtensorMap tm_vs;     // eta*Vhat [M, d]  box {64, 128}  (TMA store, split variant)
   const float* conv_w;   // [d, 3]
   __nv_bfloat16* vhat;   // eta * Vhat [M, d]
   float eta;
@@ -132,6 +133,7 @@ struct TargetSched : SchedDefaults {
   static constexpr int kNumStages = kFused ? 3 : 4;
   static constexpr uint32_t kExtraStageBytes = kFused ? kX0StageBytes : 0;
   static constexpr int kBuilderWarps = kFused ? 8 : 0;
+  static constexpr bool kStagedStores = !kFused;  // the fused stage leaves no room
   static_assert(kX0StageBytes % 1024 == 0, "stage alignment");
 
   const Params& p;
@@ -253,6 +255,35 @@ struct TargetSched : SchedDefaults {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
   }
 
+  // Split variant: 256 columns as four 64-column TMA stores (rows >= M and
+  // columns >= d are not written).
+  __device__ void epilogue(int, int, uint32_t trow, EpiStager& st) const {
+#pragma unroll 1
+    for (int g = 0; g < kBN / 64; ++g) {
+      uint8_t* buf = st.acquire();
+#pragma unroll 1
+      for (int hc = 0; hc < 2; ++hc) {
+        uint32_t v[32];
+        tmem_ld_32cols(trow + uint32_t(g * 64 + hc * 32), v);
+        tmem_wait_ld();
+        pin_regs(v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st.put(buf, hc * 4 + q,
+                 make_uint4(pack_bf16x2(p.eta * __uint_as_float(v[8 * q]),
+                                        p.eta * __uint_as_float(v[8 * q + 1])),
+                            pack_bf16x2(p.eta * __uint_as_float(v[8 * q + 2]),
+                                        p.eta * __uint_as_float(v[8 * q + 3])),
+                            pack_bf16x2(p.eta * __uint_as_float(v[8 * q + 4]),
+                                        p.eta * __uint_as_float(v[8 * q + 5])),
+                            pack_bf16x2(p.eta * __uint_as_float(v[8 * q + 6]),
+                                        p.eta * __uint_as_float(v[8 * q + 7]))));
+      }
+      st.commit(buf, [&](uint8_t* src) { tma_store_2d(&p.tm_vs, src, n0 + g * 64, m0); });
+    }
+  }
+
+  // Fused variant: direct 16-byte stores.
   __device__ void epilogue(int, int row, uint32_t trow) const {
     const int gm = m0 + row;
     const bool row_ok = gm < p.M;
@@ -314,11 +345,12 @@ cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const flo
 }
 
 cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a, const CUtensorMap& tm_wt,
-                          const float* conv_w, __nv_bfloat16* vhat, float eta, int M, int T, int d,
-                          int C, int pad_mode, bool fused) {
+                          const CUtensorMap& tm_vs, const float* conv_w, __nv_bfloat16* vhat,
+                          float eta, int M, int T, int d, int C, int pad_mode, bool fused) {
   TargetParams p;
   p.tm_a = tm_a;
   p.tm_wt = tm_wt;
+  p.tm_vs = tm_vs;
   p.conv_w = conv_w;
   p.vhat = vhat;
   p.eta = eta;

@@ -30,6 +30,7 @@ constexpr uint32_t kMnBoxBytes = 64 * 64 * 2;  // one {64 cols, 64 tokens} box
 struct UpdateParams {
   CUtensorMap tm_v;  // eta*Vhat [B*T, d]  box {64, 64}
   CUtensorMap tm_z;  // Z        [B*T, f]  box {64, 64}
+  CUtensorMap tm_ss; // snapshots as [B*n slots][d rows][f cols], box {64, 128, 1} (store)
   const void* w0;
   int w0_fp32;
   int64_t w0_bstride;
@@ -43,29 +44,32 @@ struct UpdateSched : SchedDefaults {
   using Params = UpdateParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true, true);
   static constexpr bool kPreload = true;
+  static constexpr bool kStagedStores = true;
 
   const Params& p;
   int b = 0, m0 = 0, nbase = 0, halves = 1;
 
   __device__ explicit UpdateSched(const Params& pp) : p(pp) {}
   __device__ int num_units() const { return p.B * p.mt * p.np; }
+  // d_model blocks vary fastest: the CTAs of one wave share each Z column
+  // block, so Z streams from DRAM about once per sequence.
   __device__ void begin_unit(int u, int) {
-    const int np = u % p.np;
-    const int r = u / p.np;
-    const int mt = r % p.mt;
-    b = r / p.mt;
+    const int mt = u % p.mt;
+    const int r = u / p.mt;
+    const int np = r % p.np;
+    b = r / p.np;
     m0 = mt * kBM;
     nbase = np * (2 * kBN);
     halves = (nbase + kBN < p.f) ? 2 : 1;
   }
   __device__ int num_segments() const { return p.n_upd * halves; }
   __device__ int unit_accs() const { return halves; }
-  __device__ int seg_acc(int s) const { return s % halves; }
+  __device__ int seg_acc(int s) const { return halves == 2 ? (s & 1) : 0; }
   __device__ int seg_kblocks(int) const { return p.kb_per_chunk; }
   __device__ bool seg_fresh(int) const { return false; }  // starts from the preloaded W_0
 
   __device__ void load(int s, int kb, uint8_t* stage, uint64_t* bar) const {
-    const int i = s / halves;
+    const int i = halves == 2 ? (s >> 1) : s;
     const int h = s - i * halves;
     const int tok = b * p.T + i * p.C + kb * kBK;
     uint8_t* sa = stage;
@@ -124,10 +128,12 @@ struct UpdateSched : SchedDefaults {
     }
   }
 
-  // State after chunk i of this half: snapshot W_{i+1} (bf16) and, after
-  // the last update, the fp32 state when the caller wants it.
-  __device__ void epilogue(int s, int row, uint32_t trow) const {
-    const int i = s / halves;
+  // State after chunk i of this half: snapshot W_{i+1} (bf16, four 64-column
+  // TMA stores through the slot-bounded 3-D map, so rows >= d and columns
+  // >= f are not written) and, after the last update, the fp32 state when
+  // the caller wants it (direct stores).
+  __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& stg) const {
+    const int i = halves == 2 ? (s >> 1) : s;
     const int h = s - i * halves;
     const int m = m0 + row;
     const bool row_ok = m < p.d;
@@ -136,33 +142,41 @@ struct UpdateSched : SchedDefaults {
     float* st = (p.state_out != nullptr && (i + 1) == p.n_upd)
                     ? p.state_out + (size_t(b) * p.d + size_t(row_ok ? m : 0)) * size_t(p.f)
                     : nullptr;
-    __nv_bfloat16* snap_row =
-        p.snap + ((size_t(b) * p.n + size_t(write_snap ? i + 1 : 0)) * p.d +
-                  size_t(row_ok ? m : 0)) * size_t(p.f);
+    const int slot = b * p.n + i + 1;
 #pragma unroll 1
-    for (int c = 0; c < kBN; c += 32) {
-      uint32_t v[32];
-      tmem_ld_32cols(trow + uint32_t(c), v);
-      tmem_wait_ld();
-      pin_regs(v);
-      if (!row_ok) continue;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int col = n0 + c + 8 * q;
-        if (col >= p.f) continue;
+    for (int g = 0; g < kBN / 64; ++g) {
+      uint8_t* buf = write_snap ? stg.acquire() : nullptr;
+#pragma unroll 1
+      for (int hc = 0; hc < 2; ++hc) {
+        const int c = g * 64 + hc * 32;
+        uint32_t v[32];
+        tmem_ld_32cols(trow + uint32_t(c), v);
+        tmem_wait_ld();
+        pin_regs(v);
         if (write_snap) {
-          *reinterpret_cast<uint4*>(snap_row + col) = make_uint4(
-              pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-              pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-              pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-              pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            stg.put(buf, hc * 4 + q,
+                    make_uint4(
+                        pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]))));
         }
-        if (st != nullptr) {
-          uint4* dst = reinterpret_cast<uint4*>(st + col);
-          dst[0] = make_uint4(v[8 * q], v[8 * q + 1], v[8 * q + 2], v[8 * q + 3]);
-          dst[1] = make_uint4(v[8 * q + 4], v[8 * q + 5], v[8 * q + 6], v[8 * q + 7]);
+        if (st != nullptr && row_ok) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int col = n0 + c + 8 * q;
+            if (col < p.f) {
+              uint4* dst = reinterpret_cast<uint4*>(st + col);
+              dst[0] = make_uint4(v[8 * q], v[8 * q + 1], v[8 * q + 2], v[8 * q + 3]);
+              dst[1] = make_uint4(v[8 * q + 4], v[8 * q + 5], v[8 * q + 6], v[8 * q + 7]);
+            }
+          }
         }
       }
+      if (write_snap)
+        stg.commit(buf, [&](uint8_t* src) { tma_store_3d(&p.tm_ss, src, n0 + g * 64, m0, slot); });
     }
   }
 };
@@ -214,11 +228,12 @@ cudaError_t launch_snapshot0(const LaunchEnv& env, const void* w0, bool w0_fp32,
 }
 
 cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, const CUtensorMap& tm_z,
-                          const UpdateArgs& a) {
+                          const CUtensorMap& tm_snap_store, const UpdateArgs& a) {
   if (a.n_upd <= 0) return cudaSuccess;
   UpdateParams p;
   p.tm_v = tm_vhat;
   p.tm_z = tm_z;
+  p.tm_ss = tm_snap_store;
   p.w0 = a.w0;
   p.w0_fp32 = a.w0_fp32 ? 1 : 0;
   p.w0_bstride = a.w0_bstride;

@@ -18,10 +18,11 @@ struct LaunchEnv {
 };
 
 // Z[M, f] = SiLU(H W_gate^T) * (H W_up^T).  Tensor maps: H [M, K] box
-// {64,128}; W_gate, W_up [f, K] box {64,128}.  All bf16, K = d_model.
+// {64,128}; W_gate, W_up [f, K] box {64,128}; Z [M, f] box {64,128} for the
+// TMA stores.  All bf16, K = d_model.
 cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h,
                           const CUtensorMap& tm_wg, const CUtensorMap& tm_wu,
-                          __nv_bfloat16* z, int M, int f, int K);
+                          const CUtensorMap& tm_zs, int M, int f, int K);
 
 // Xc = three-tap depthwise conv of X0 (zero padding at chunk edges, or only
 // at sequence edges when pad_mode = 1), rounded to bf16.  x0, xc: [B*T, d].
@@ -29,12 +30,14 @@ cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const flo
                         __nv_bfloat16* xc, int64_t rows, int T, int d, int C, int pad_mode);
 
 // vhat[M, d] = eta * (Conv1D(X0) W_target^T), rounded once to bf16.
-// Split (fused = false): tm_a maps Xc [M, d] with box {64,128}.
-// Fused: tm_a maps X0 [M, d] with box {64,130} and the kernel computes the
-// conv itself.  tm_wt: W_target [d, d] box {64,256}.
+// Split (fused = false): tm_a maps Xc [M, d] with box {64,128} and the
+// output goes out through tm_vs (vhat [M, d], box {64,128}).
+// Fused: tm_a maps X0 [M, d] with box {64,130}, the kernel computes the conv
+// itself and stores vhat directly.  tm_wt: W_target [d, d] box {64,256}.
 cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a,
-                          const CUtensorMap& tm_wt, const float* conv_w, __nv_bfloat16* vhat,
-                          float eta, int M, int T, int d, int C, int pad_mode, bool fused);
+                          const CUtensorMap& tm_wt, const CUtensorMap& tm_vs,
+                          const float* conv_w, __nv_bfloat16* vhat, float eta, int M, int T,
+                          int d, int C, int pad_mode, bool fused);
 
 // snap[b, 0] = bf16(W_0 of sequence b) for every b.  w0 is bf16 or fp32,
 // [d, f] shared (w0_bstride = 0) or [B, d, f].
@@ -57,15 +60,18 @@ struct UpdateArgs {
 // fp32 state starts at W_0 in TMEM and the per-chunk deltas
 // (eta Vhat_[i])^T Z_[i] accumulate onto it; after chunk i the epilogue
 // writes bf16(W_{i+1}) as snapshot i+1.  Tensor maps: eta*Vhat [B*T, d] box
-// {64,64}; Z [B*T, f] box {64,64} (both read MN-major).
+// {64,64}; Z [B*T, f] box {64,64} (both read MN-major); snapshots as
+// [B*n][d][f] with box {64,128,1} for the TMA stores.
 cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
-                          const CUtensorMap& tm_z, const UpdateArgs& a);
+                          const CUtensorMap& tm_z, const CUtensorMap& tm_snap_store,
+                          const UpdateArgs& a);
 
 // O_[i] = Z_[i] snap[b, i]^T for every (sequence, chunk).  Tensor maps:
-// Z [B*T, f] box {64,128}; snapshots [B*n*d, f] box {64,256}.
+// Z [B*T, f] box {64,128}; snapshots [B*n*d, f] box {64,256}; bf16 O as
+// [B*n][C][d] with box {64,128,1} for the TMA stores (unused for fp32 O).
 cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
-                         const CUtensorMap& tm_snap, void* out, bool out_fp32, int B, int T,
-                         int d, int f, int C);
+                         const CUtensorMap& tm_snap, const CUtensorMap& tm_os, void* out,
+                         bool out_fp32, int B, int T, int d, int f, int C);
 
 // Dual form, scores: S[b, t, s] = Z_t . Z_s (bf16) for every token t of chunk
 // i >= 1 and every token s < i*C of the same sequence.  Tensor maps: Z

@@ -38,8 +38,10 @@
 //   void preload(int acc, int row, uint32_t tmem_row_base)   (per thread)
 // Each MMA use of an accumulator then waits for exactly one epilogue arrival:
 // the release after the previous segment's read inside a unit, or the
-// preload at a unit's start (the last read of a unit is not released; the
-// next unit's preload stands for it).
+// preload for a unit's first use (the last read of a unit is not released;
+// the next unit's preload stands for it).  The epilogue preloads accumulator
+// h for the CTA's next unit as soon as it has read h's last value in the
+// current one, so the MMA rolls from one unit into the next without waiting.
 //
 // With kBuilderWarps > 0 the producer's copies complete on a `loaded`
 // barrier (tma_bytes(s, kb) per stage); the builder warps wait for it, call
@@ -64,11 +66,54 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kBaseThreads = 192;
 constexpr int kEpilogueThreads = 128;
 
+// Epilogue output staging for TMA stores: two 128-row x 128-byte tiles.
+constexpr uint32_t kStagingTileBytes = kBM * 128;
+constexpr uint32_t kStagingBytes = 2 * kStagingTileBytes;
+
+// Helper the epilogue threads use to write a 128 x 64 bf16 output tile
+// through shared memory: every thread fills its row (8 x 16 bytes, 128-byte
+// swizzle), then one thread issues the TMA store.  Two staging buffers
+// alternate; a buffer is refilled only after the store that read it two
+// tiles ago has finished reading shared memory.
+struct EpiStager {
+  uint8_t* buf;
+  int tid;  // 0..127 = tile row
+  uint32_t issued;
+
+  // Next buffer to fill (every epilogue thread must call this).
+  __device__ __forceinline__ uint8_t* acquire() {
+    if (tid == 0 && issued >= 2) bulk_wait_group_read<1>();
+    epilogue_bar();
+    return buf + (issued & 1u) * kStagingTileBytes;
+  }
+  // Writes 16-byte chunk c (0..7) of this thread's row.
+  __device__ __forceinline__ void put(uint8_t* b, int c, uint4 v) const {
+    *reinterpret_cast<uint4*>(b + tid * 128 + ((c ^ (tid & 7)) << 4)) = v;
+  }
+  // Publishes the buffer; `store(buf)` runs on one thread and issues the TMA.
+  template <class F>
+  __device__ __forceinline__ void commit(uint8_t* b, F&& store) {
+    fence_proxy_async_smem();
+    epilogue_bar();
+    if (tid == 0) {
+      store(b);
+      bulk_commit_group();
+    }
+    ++issued;
+  }
+  __device__ __forceinline__ void finish() const {
+    if (tid == 0) bulk_wait_group_all();
+  }
+};
+
 struct SchedDefaults {
   static constexpr int kNumStages = 4;
   static constexpr uint32_t kExtraStageBytes = 0;
   static constexpr int kBuilderWarps = 0;
   static constexpr bool kPreload = false;
+  // Epilogue writes bf16 tiles through EpiStager (TMA stores); then
+  //   void epilogue(int s, int row, uint32_t tmem_row_base, EpiStager& st)
+  static constexpr bool kStagedStores = false;
   // With kMixedOperands the MMA asks the schedule for each K block's
   // instruction and shared-memory descriptors (operand major-ness may change
   // inside one accumulation):
@@ -96,11 +141,18 @@ struct __align__(8) PipeSync {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int vote[4];  // epilogue warps' go/unwind votes (staged-store kernels)
 };
 
 template <class S>
-constexpr size_t pipe_smem_bytes() {
-  return 1024 + size_t(S::kNumStages) * PipeShape<S>::kStageStride + sizeof(PipeSync);
+__host__ __device__ constexpr size_t pipe_staging_bytes() {
+  return S::kStagedStores ? kStagingBytes : 0;
+}
+
+template <class S>
+__host__ __device__ constexpr size_t pipe_smem_bytes() {
+  return 1024 + size_t(S::kNumStages) * PipeShape<S>::kStageStride + pipe_staging_bytes<S>() +
+         sizeof(PipeSync);
 }
 
 template <class S>
@@ -111,7 +163,8 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  PipeSync* sync = reinterpret_cast<PipeSync*>(smem + size_t(NS) * kStride);
+  uint8_t* staging = smem + size_t(NS) * kStride;  // 1 KiB aligned
+  PipeSync* sync = reinterpret_cast<PipeSync*>(staging + pipe_staging_bytes<S>());
   volatile int* abort_flag = &sync->abort_flag;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -246,9 +299,13 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
   } else if (warp < 6) {
     // ------------------------------------------------------------- epilogue
     S sched(p);
+    S next(p);  // lookahead for the preload of the CTA's next unit
     const int quad = warp & 3;  // TMEM lanes this warp may touch: 32*quad..+31
     const int row = quad * 32 + lane;
+    EpiStager stager{staging, row, 0u};
+    const uint32_t tlane = tmem + (uint32_t(quad * 32) << 16);
     uint32_t acc_use[2] = {0u, 0u};
+    bool preloaded[2] = {false, false};
     const int nunits = sched.num_units();
     int local = 0;
     bool ok = true;
@@ -257,28 +314,56 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
       const int nseg = sched.num_segments();
       if constexpr (S::kPreload) {
         for (int h = 0; h < sched.unit_accs(); ++h) {
-          sched.preload(h, row, tmem + (uint32_t(quad * 32) << 16) + uint32_t(h * kBN));
-          tmem_wait_st();
-          tc_fence_before_sync();
-          mbar_arrive(&sync->acc_empty[h]);
+          if (!preloaded[h]) {
+            sched.preload(h, row, tlane + uint32_t(h * kBN));
+            tmem_wait_st();
+            tc_fence_before_sync();
+            mbar_arrive(&sync->acc_empty[h]);
+          }
         }
+        preloaded[0] = preloaded[1] = false;
       }
       for (int s = 0; s < nseg; ++s) {
         const int h = sched.seg_acc(s);
         // The TMEM loads below are warp-collective: the whole warp proceeds
-        // or the whole warp unwinds.
-        const bool got = __all_sync(0xffffffffu, mbar_wait(&sync->acc_full[h], acc_use[h] & 1u,
-                                                           abort_flag));
+        // or the whole warp unwinds.  Staged stores also synchronise the four
+        // epilogue warps with a named barrier, so there the four warps vote
+        // and proceed or unwind together.
+        bool got = __all_sync(0xffffffffu, mbar_wait(&sync->acc_full[h], acc_use[h] & 1u,
+                                                     abort_flag));
+        if constexpr (S::kStagedStores) {
+          if (lane == 0) sync->vote[quad] = got ? 1 : 0;
+          epilogue_bar();
+          got = (sync->vote[0] & sync->vote[1] & sync->vote[2] & sync->vote[3]) != 0;
+          epilogue_bar();
+        }
         if (!got) {
           raise_abort(abort_flag, status, kStatusTimeout);
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t trow = tmem + (uint32_t(quad * 32) << 16) + uint32_t(h * kBN);
-        sched.epilogue(s, row, trow);
+        const uint32_t trow = tlane + uint32_t(h * kBN);
+        if constexpr (S::kStagedStores) {
+          sched.epilogue(s, row, trow, stager);
+        } else {
+          sched.epilogue(s, row, trow);
+        }
         bool release = true;
-        if constexpr (S::kPreload) release = s < nseg - sched.unit_accs();
+        if constexpr (S::kPreload) {
+          release = s < nseg - sched.unit_accs();
+          const int un = u + int(gridDim.x);
+          if (!release && un < nunits) {
+            next.begin_unit(un, local + 1);
+            if (h < next.unit_accs()) {
+              next.preload(h, row, trow);
+              tmem_wait_st();
+              tc_fence_before_sync();
+              mbar_arrive(&sync->acc_empty[h]);
+              preloaded[h] = true;
+            }
+          }
+        }
         if (release) {
           tc_fence_before_sync();
           mbar_arrive(&sync->acc_empty[h]);
@@ -286,6 +371,8 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
         ++acc_use[h];
       }
     }
+    // Shared memory must outlive the TMA stores that read it.
+    if constexpr (S::kStagedStores) stager.finish();
   } else if constexpr (kBuild) {
     // ------------------------------------------------------- A-tile builders
     S sched(p);
