@@ -32,9 +32,34 @@ sys.path.insert(0, ROOT)
 
 METRIC = "TTT-MLP tokens/s per layer (d2560/ff9728, 32k ctx); % of GB300 bf16 peak"
 DEFAULT_CONFIG = 2
-# DRAM bytes (read + write) per launch of a kernel, from one ncu capture of
-# that kernel at that workload (profiles/); None once the kernel changes.
-TRAFFIC_BYTES: dict = {}
+# DRAM bytes (read + write) per launch of a kernel at a named workload, from
+# one ncu capture (profiles/traffic_qwen3-4b-layer-B2-T32k-C2048.md), with the
+# hash of the kernel's sources at capture time: once the sources change the
+# figure no longer describes the kernel and `traffic` is reported as null.
+TRAFFIC_BYTES = {
+    (2, "gateup"): (3027029760, "e279823aeef60a84"),
+}
+KERNEL_SOURCES = {
+    "gateup": ["k_gateup.cu"], "target": ["k_target.cu"], "update": ["k_update.cu"],
+    "apply": ["k_apply.cu"], "conv": ["k_target.cu"], "snapshot0": ["k_update.cu"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    import hashlib
+    csrc = os.path.join(ROOT, "chunk_wise_weight_gb300", "csrc")
+    m = hashlib.sha1()
+    for f in KERNEL_SOURCES[kernel] + ["pipeline.cuh", "sm103.cuh"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
+def recorded_traffic(config: int, kernel: str, shape_override: bool):
+    entry = TRAFFIC_BYTES.get((config, kernel))
+    if entry is None or shape_override or entry[1] != kernel_source_hash(kernel):
+        return None
+    return entry[0]
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -287,7 +312,7 @@ def main():
         peak = float(peaks["bf16_tflops"])
         roof = {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
                 "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "traffic": TRAFFIC_BYTES.get((args.config, dominant)),
+                "traffic": recorded_traffic(args.config, dominant, bool(args.shape)),
                 "peak_kind": f"bf16_tflops burst ({peak_src})",
                 "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4),
                 "flops_per_launch": work}
