@@ -66,19 +66,19 @@ def _load():
         lib.oracle_value_target.argtypes = [_i64, _i64, _i64, _int, _fp, _fp, _fp, _dp]
         lib.oracle_forward_sequential.argtypes = [
             _i64, _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp,
-            _i64, _fp, _fp, _dp, _dp, _dp, _dp]
+            _i64, _fp, _fp, _fp, _dp, _dp, _dp, _dp]
         lib.oracle_forward_prefix.argtypes = [
             _i64, _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp,
-            _i64, _fp, _fp, _dp, _dp]
+            _i64, _fp, _fp, _fp, _dp, _dp]
         lib.oracle_forward_dual.argtypes = [
             _i64, _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp,
-            _i64, _fp, _fp, _dp]
+            _i64, _fp, _fp, _fp, _dp]
         lib.oracle_z_entries.argtypes = [_i64, _fp, _fp, _fp, _i64, _ip, _ip, _dp]
         lib.oracle_vhat_entries.argtypes = [_i64, _i64, _i64, _int, _fp, _fp, _fp,
                                             _i64, _ip, _ip, _dp]
         lib.oracle_state_entries.argtypes = [
             _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp, _fp,
-            _fp, _i64, _ip, _ip, _dp]
+            _fp, _fp, _i64, _ip, _ip, _dp]
         lib.oracle_first_chunk_rows.argtypes = [_i64, _i64, _fp, _fp, _fp, _fp,
                                                 _i64, _ip, _dp]
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -93,8 +93,8 @@ def _f32(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.float32)
 
 
-def _fptr(a: np.ndarray):
-    return a.ctypes.data_as(_fp)
+def _fptr(a):
+    return None if a is None else a.ctypes.data_as(_fp)
 
 
 def _dptr(a):
@@ -128,25 +128,39 @@ def _unpack(inp):
     return H, X0, Wg, Wu, W0, Wt, cw, B, T, d, f, w0_stride
 
 
+def _eta_tok(eta_tok, B, T):
+    if eta_tok is None:
+        return None
+    e = _f32(eta_tok).reshape(B, T)
+    return np.ascontiguousarray(e)
+
+
+def _chunks(T: int, chunk: int) -> int:
+    """Chunk count; the last chunk is the remainder when chunk does not divide T."""
+    if chunk <= 0:
+        raise ValueError("chunk must be positive")
+    return -(-T // chunk)
+
+
 def forward(inp, eta: float, chunk: int, pad_mode: int = PAD_CHUNK,
             want_z: bool = False, want_vhat: bool = False,
-            want_states: bool = False) -> dict:
+            want_states: bool = False, eta_tok=None) -> dict:
     """Sequential apply-then-update loop over chunks (the defining form).
 
     Returns {"O": [B,T,d]} plus optional "Z" [B,T,f], "Vhat" [B,T,d] and
-    "states" [B,n+1,d,f] (W^(0)..W^(n)), all float64.
+    "states" [B,n+1,d,f] (W^(0)..W^(n)), all float64.  eta_tok: optional
+    per-token learning-rate weights [B,T].
     """
     H, X0, Wg, Wu, W0, Wt, cw, B, T, d, f, w0s = _unpack(inp)
-    if chunk <= 0 or T % chunk:
-        raise ValueError("chunk must divide T")
-    n = T // chunk
+    n = _chunks(T, chunk)
+    et = _eta_tok(eta_tok, B, T)
     O = np.zeros((B, T, d), np.float64)
     Z = np.zeros((B, T, f), np.float64) if want_z else None
     V = np.zeros((B, T, d), np.float64) if want_vhat else None
     S = np.zeros((B, n + 1, d, f), np.float64) if want_states else None
     _load().oracle_forward_sequential(
         B, T, d, f, chunk, float(eta), pad_mode, _fptr(H), _fptr(X0), _fptr(Wg),
-        _fptr(Wu), _fptr(W0), w0s, _fptr(Wt), _fptr(cw), _dptr(O), _dptr(Z),
+        _fptr(Wu), _fptr(W0), w0s, _fptr(Wt), _fptr(cw), _fptr(et), _dptr(O), _dptr(Z),
         _dptr(V), _dptr(S))
     out = {"O": O}
     if want_z:
@@ -159,32 +173,32 @@ def forward(inp, eta: float, chunk: int, pad_mode: int = PAD_CHUNK,
 
 
 def forward_prefix(inp, eta: float, chunk: int, pad_mode: int = PAD_CHUNK,
-                   want_states: bool = False) -> dict:
+                   want_states: bool = False, eta_tok=None) -> dict:
     """Three-stage form: per-chunk deltas, exclusive prefix sum, apply."""
     H, X0, Wg, Wu, W0, Wt, cw, B, T, d, f, w0s = _unpack(inp)
-    if chunk <= 0 or T % chunk:
-        raise ValueError("chunk must divide T")
-    n = T // chunk
+    n = _chunks(T, chunk)
+    et = _eta_tok(eta_tok, B, T)
     O = np.zeros((B, T, d), np.float64)
     S = np.zeros((B, n + 1, d, f), np.float64) if want_states else None
     _load().oracle_forward_prefix(
         B, T, d, f, chunk, float(eta), pad_mode, _fptr(H), _fptr(X0), _fptr(Wg),
-        _fptr(Wu), _fptr(W0), w0s, _fptr(Wt), _fptr(cw), _dptr(O), _dptr(S))
+        _fptr(Wu), _fptr(W0), w0s, _fptr(Wt), _fptr(cw), _fptr(et), _dptr(O), _dptr(S))
     out = {"O": O}
     if want_states:
         out["states"] = S
     return out
 
 
-def forward_dual(inp, eta: float, chunk: int, pad_mode: int = PAD_CHUNK) -> dict:
+def forward_dual(inp, eta: float, chunk: int, pad_mode: int = PAD_CHUNK,
+                 eta_tok=None) -> dict:
     """Dual form O_[i] = Z_[i] W0^T + eta * sum_{j<i} (Z_[i] Z_[j]^T) Vhat_[j]."""
     H, X0, Wg, Wu, W0, Wt, cw, B, T, d, f, w0s = _unpack(inp)
-    if chunk <= 0 or T % chunk:
-        raise ValueError("chunk must divide T")
+    _chunks(T, chunk)
+    et = _eta_tok(eta_tok, B, T)
     O = np.zeros((B, T, d), np.float64)
     _load().oracle_forward_dual(
         B, T, d, f, chunk, float(eta), pad_mode, _fptr(H), _fptr(X0), _fptr(Wg),
-        _fptr(Wu), _fptr(W0), w0s, _fptr(Wt), _fptr(cw), _dptr(O))
+        _fptr(Wu), _fptr(W0), w0s, _fptr(Wt), _fptr(cw), _fptr(et), _dptr(O))
     return {"O": O}
 
 
@@ -245,21 +259,23 @@ def vhat_entries(X0, conv_w, W_target, chunk: int, t_idx, m_idx,
 
 
 def state_entries(H, X0, W_gate, W_up, w0, W_target, conv_w, eta: float,
-                  chunk: int, m_idx, j_idx, pad_mode: int = PAD_CHUNK) -> np.ndarray:
+                  chunk: int, m_idx, j_idx, pad_mode: int = PAD_CHUNK,
+                  eta_tok=None) -> np.ndarray:
     """W^(i)[m, j] for i = 0..n at each (m, j) pair: returns [count, n+1]."""
     H, X0 = _f32(H), _f32(X0)
     Wg, Wu, w0 = _f32(W_gate), _f32(W_up), _f32(w0)
     Wt, cw = _f32(W_target), _f32(conv_w)
     T, d = H.shape
     f = Wg.shape[0]
-    n = T // chunk
+    n = _chunks(T, chunk)
+    et = None if eta_tok is None else np.ascontiguousarray(_f32(eta_tok).reshape(T))
     m = np.ascontiguousarray(m_idx, np.int64)
     j = np.ascontiguousarray(j_idx, np.int64)
     out = np.zeros((len(m), n + 1), np.float64)
     _load().oracle_state_entries(T, d, f, chunk, float(eta), pad_mode, _fptr(H),
                                  _fptr(X0), _fptr(Wg), _fptr(Wu), _fptr(w0),
-                                 _fptr(Wt), _fptr(cw), len(m), _iptr(m), _iptr(j),
-                                 _dptr(out))
+                                 _fptr(Wt), _fptr(cw), _fptr(et), len(m), _iptr(m),
+                                 _iptr(j), _dptr(out))
     return out
 
 

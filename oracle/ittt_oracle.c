@@ -16,7 +16,8 @@
  *        sections "整体框架" (apply / update) and "实现细节" (prefix sum).
  *
  * Notation: B batch, T tokens per sequence, d = d_model, f = d_ff, C chunk,
- * n = T / C chunks.  Weights use the [out, in] row-major layout:
+ * n = ceil(T / C) chunks; chunk i holds tokens [iC, min((i+1)C, T)).
+ * Weights use the [out, in] row-major layout:
  *   W_gate, W_up : [f, d]      W_down (fast weight) : [d, f]
  *   W_target     : [d, d]      conv_w               : [d, 3]
  * Activations are [B, T, ...] row-major.  Inputs arrive as float (they hold
@@ -35,6 +36,15 @@
  *     chunks 0..i-1 exactly (exclusive prefix, [P3] 实现细节).
  *   - The update is W <- W + eta * Vhat_[i]^T Z_[i] ([P1] eq. (6)): the
  *     gradient step on L = -<Z W^T, Vhat>_F, with no 1/C averaging.
+ *   - Per-token learning rate (optional): with eta_tok given, token t's term
+ *     of the chunk gradient is weighted by eta_tok[t], i.e. the step uses
+ *     grad sum_t eta_tok[t] L_t as in the large-chunk update of [P2]
+ *     ("[논문리뷰] Test-Time Training Done Right", Large-Chunk TTT Layer,
+ *     per-token eta_i); eta_tok == 1 is the plain update.
+ *   - When C does not divide T the last chunk is the shorter remainder
+ *     (the pages only use equal chunks; a stream whose length is not a
+ *     multiple of C ends with a partial chunk).  Chunk-edge padding then
+ *     also pads at T.
  *
  * Parity pins: every function below is checked by tests/test_oracle_pins.py
  * against library routines, closed forms, invariants and finite differences.
@@ -87,7 +97,7 @@ void oracle_conv1d(int64_t T, int64_t d, int64_t C, int pad_mode,
       hi = T;
     } else {
       lo = (t / C) * C;
-      hi = lo + C;
+      hi = lo + C < T ? lo + C : T;
     }
     for (int64_t c = 0; c < d; ++c) {
       double acc = 0.0;
@@ -135,19 +145,33 @@ static void apply_chunk(int64_t t0, int64_t Cn, int64_t d, int64_t f,
   }
 }
 
+/* Per-token weight of the chunk gradient ([P2] per-token eta_i): 1 when no
+ * per-token rates are given. */
+static double token_rate(const float* eta_tok, int64_t t) {
+  return eta_tok ? (double)eta_tok[t] : 1.0;
+}
+
 /* Per-chunk delta, [P1] eq. (6) and Method §3 stage 1:
- *   dW = Vhat_[i]^T Z_[i]   ([d, f]) over the Cn rows starting at row t0. */
+ *   dW = sum_t eta_tok[t] Vhat_t^T Z_t   ([d, f]) over the Cn rows starting
+ * at row t0 (eta_tok == NULL: all weights 1, dW = Vhat_[i]^T Z_[i]). */
 static void chunk_delta(int64_t t0, int64_t Cn, int64_t d, int64_t f,
-                        const double* Vhat, const double* Z, double* dW) {
+                        const double* Vhat, const double* Z, const float* eta_tok,
+                        double* dW) {
 #pragma omp parallel for schedule(static)
   for (int64_t m = 0; m < d; ++m) {
     for (int64_t j = 0; j < f; ++j) {
       double acc = 0.0;
       for (int64_t t = t0; t < t0 + Cn; ++t)
-        acc += Vhat[t * d + m] * Z[t * f + j];
+        acc += token_rate(eta_tok, t) * Vhat[t * d + m] * Z[t * f + j];
       dW[m * f + j] = acc;
     }
   }
+}
+
+/* Number of chunks and the length of chunk i. */
+static int64_t num_chunks(int64_t T, int64_t C) { return (T + C - 1) / C; }
+static int64_t chunk_len(int64_t T, int64_t C, int64_t i) {
+  return (i + 1) * C <= T ? C : T - i * C;
 }
 
 /* Per-sequence intermediates shared by the three forms below. */
@@ -173,7 +197,8 @@ static void sequence_intermediates(int64_t T, int64_t d, int64_t f, int64_t C,
  *
  * Inputs (float, row-major): H, X0 [B,T,d]; W_gate, W_up [f,d];
  * W_down0 [d,f] if w0_batch_stride == 0, else [B,d,f] with that stride
- * (per-sequence initial state); W_target [d,d]; conv_w [d,3].
+ * (per-sequence initial state); W_target [d,d]; conv_w [d,3]; eta_tok
+ * [B,T] per-token rates or NULL.
  * Outputs (double): O [B,T,d].  Optional (may be NULL): Z [B,T,f],
  * Vhat [B,T,d], states [B, n+1, d, f] holding W^(0) .. W^(n).
  */
@@ -183,9 +208,9 @@ void oracle_forward_sequential(int64_t B, int64_t T, int64_t d, int64_t f,
                                const float* W_gate, const float* W_up,
                                const float* W_down0, int64_t w0_batch_stride,
                                const float* W_target, const float* conv_w,
-                               double* O, double* Z_out, double* Vhat_out,
-                               double* states_out) {
-  const int64_t n = T / C;
+                               const float* eta_tok, double* O, double* Z_out,
+                               double* Vhat_out, double* states_out) {
+  const int64_t n = num_chunks(T, C);
   double* Z = (double*)malloc((size_t)(T * f) * sizeof(double));
   double* Vhat = (double*)malloc((size_t)(T * d) * sizeof(double));
   double* W = (double*)malloc((size_t)(d * f) * sizeof(double));
@@ -194,13 +219,15 @@ void oracle_forward_sequential(int64_t B, int64_t T, int64_t d, int64_t f,
     sequence_intermediates(T, d, f, C, pad_mode, H + b * T * d, X0 + b * T * d,
                            W_gate, W_up, W_target, conv_w, Z, Vhat);
     const float* W0 = W_down0 + b * w0_batch_stride;
+    const float* et = eta_tok ? eta_tok + b * T : NULL;
     for (int64_t e = 0; e < d * f; ++e) W[e] = (double)W0[e];
     if (states_out)
       memcpy(states_out + (b * (n + 1)) * d * f, W,
              (size_t)(d * f) * sizeof(double));
     for (int64_t i = 0; i < n; ++i) {
-      apply_chunk(i * C, C, d, f, Z, W, O + b * T * d);          /* apply  */
-      chunk_delta(i * C, C, d, f, Vhat, Z, dW);                  /* update */
+      const int64_t Cn = chunk_len(T, C, i);
+      apply_chunk(i * C, Cn, d, f, Z, W, O + b * T * d);         /* apply  */
+      chunk_delta(i * C, Cn, d, f, Vhat, Z, et, dW);             /* update */
       for (int64_t e = 0; e < d * f; ++e) W[e] += eta * dW[e];
       if (states_out)
         memcpy(states_out + (b * (n + 1) + i + 1) * d * f, W,
@@ -230,9 +257,9 @@ void oracle_forward_prefix(int64_t B, int64_t T, int64_t d, int64_t f,
                            const float* X0, const float* W_gate,
                            const float* W_up, const float* W_down0,
                            int64_t w0_batch_stride, const float* W_target,
-                           const float* conv_w, double* O,
+                           const float* conv_w, const float* eta_tok, double* O,
                            double* states_out) {
-  const int64_t n = T / C;
+  const int64_t n = num_chunks(T, C);
   const int64_t df = d * f;
   double* Z = (double*)malloc((size_t)(T * f) * sizeof(double));
   double* Vhat = (double*)malloc((size_t)(T * d) * sizeof(double));
@@ -242,8 +269,10 @@ void oracle_forward_prefix(int64_t B, int64_t T, int64_t d, int64_t f,
   for (int64_t b = 0; b < B; ++b) {
     sequence_intermediates(T, d, f, C, pad_mode, H + b * T * d, X0 + b * T * d,
                            W_gate, W_up, W_target, conv_w, Z, Vhat);
+    const float* et = eta_tok ? eta_tok + b * T : NULL;
     /* stage 1 */
-    for (int64_t i = 0; i < n; ++i) chunk_delta(i * C, C, d, f, Vhat, Z, dWs + i * df);
+    for (int64_t i = 0; i < n; ++i)
+      chunk_delta(i * C, chunk_len(T, C, i), d, f, Vhat, Z, et, dWs + i * df);
     /* stage 2: exclusive scan, S_0 = 0 */
     for (int64_t e = 0; e < df; ++e) S[e] = 0.0;
     for (int64_t i = 1; i <= n; ++i)
@@ -253,7 +282,7 @@ void oracle_forward_prefix(int64_t B, int64_t T, int64_t d, int64_t f,
     const float* W0 = W_down0 + b * w0_batch_stride;
     for (int64_t i = 0; i <= n; ++i) {
       for (int64_t e = 0; e < df; ++e) W[e] = (double)W0[e] + eta * S[i * df + e];
-      if (i < n) apply_chunk(i * C, C, d, f, Z, W, O + b * T * d);
+      if (i < n) apply_chunk(i * C, chunk_len(T, C, i), d, f, Z, W, O + b * T * d);
       if (states_out)
         memcpy(states_out + (b * (n + 1) + i) * df, W, (size_t)df * sizeof(double));
     }
@@ -267,7 +296,8 @@ void oracle_forward_prefix(int64_t B, int64_t T, int64_t d, int64_t f,
 
 /*
  * The dual (attention-like) form obtained by expanding W^(i) in the apply:
- *   O_[i] = Z_[i] W_down0^T + eta * sum_{j<i} (Z_[i] Z_[j]^T) Vhat_[j].
+ *   O_[i] = Z_[i] W_down0^T + eta * sum_{j<i} (Z_[i] Z_[j]^T) Vhat_[j]
+ * (per-token rates weight each token s of the earlier chunks).
  * ([P1] eq. (3) with W^(i) = W_down0 + eta * sum_{j<i} Vhat_[j]^T Z_[j].)
  * Output O [B,T,d] only.
  */
@@ -276,8 +306,8 @@ void oracle_forward_dual(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C,
                          const float* X0, const float* W_gate,
                          const float* W_up, const float* W_down0,
                          int64_t w0_batch_stride, const float* W_target,
-                         const float* conv_w, double* O) {
-  const int64_t n = T / C;
+                         const float* conv_w, const float* eta_tok, double* O) {
+  const int64_t n = num_chunks(T, C);
   double* Z = (double*)malloc((size_t)(T * f) * sizeof(double));
   double* Vhat = (double*)malloc((size_t)(T * d) * sizeof(double));
   double* W0d = (double*)malloc((size_t)(d * f) * sizeof(double));
@@ -285,16 +315,19 @@ void oracle_forward_dual(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C,
     sequence_intermediates(T, d, f, C, pad_mode, H + b * T * d, X0 + b * T * d,
                            W_gate, W_up, W_target, conv_w, Z, Vhat);
     const float* W0 = W_down0 + b * w0_batch_stride;
+    const float* et = eta_tok ? eta_tok + b * T : NULL;
     for (int64_t e = 0; e < d * f; ++e) W0d[e] = (double)W0[e];
     double* Ob = O + b * T * d;
     for (int64_t i = 0; i < n; ++i) {
-      apply_chunk(i * C, C, d, f, Z, W0d, Ob); /* Z_[i] W_down0^T */
+      const int64_t Cn = chunk_len(T, C, i);
+      apply_chunk(i * C, Cn, d, f, Z, W0d, Ob); /* Z_[i] W_down0^T */
 #pragma omp parallel for schedule(static)
-      for (int64_t t = i * C; t < (i + 1) * C; ++t) {
+      for (int64_t t = i * C; t < i * C + Cn; ++t) {
         for (int64_t s = 0; s < i * C; ++s) { /* every token of chunks j < i */
           double a = 0.0;                     /* (Z_[i] Z_[j]^T)[t, s] */
           for (int64_t k = 0; k < f; ++k) a += Z[t * f + k] * Z[s * f + k];
-          for (int64_t m = 0; m < d; ++m) Ob[t * d + m] += eta * a * Vhat[s * d + m];
+          const double w = eta * token_rate(et, s) * a;
+          for (int64_t m = 0; m < d; ++m) Ob[t * d + m] += w * Vhat[s * d + m];
         }
       }
     }
@@ -333,7 +366,7 @@ static double vhat_entry(int64_t T, int64_t d, int64_t C, int pad_mode,
   int64_t lo = 0, hi = T;
   if (pad_mode != ORACLE_PAD_SEQUENCE) {
     lo = (t / C) * C;
-    hi = lo + C;
+    hi = lo + C < T ? lo + C : T;
   }
   double acc = 0.0;
   for (int64_t c = 0; c < d; ++c) {
@@ -363,31 +396,33 @@ void oracle_vhat_entries(int64_t T, int64_t d, int64_t C, int pad_mode,
 /*
  * Fast-weight state entries W^(i)[m, j] for i = 0..n of one sequence, for
  * `count` (m, j) pairs ([P1] eq. (6) summed over chunks; [P3] 实现细节).
- * W^(i)[m, j] = W_down0[m, j] + eta * sum_{s < iC} Vhat[s, m] Z[s, j].
- * out: [count, n+1].  w0 is this sequence's initial state [d, f].
+ * W^(i)[m, j] = W_down0[m, j] + eta * sum_{s < iC} eta_tok[s] Vhat[s, m] Z[s, j]
+ * (eta_tok NULL: weights 1).  out: [count, n+1].  w0 is this sequence's
+ * initial state [d, f].
  */
 void oracle_state_entries(int64_t T, int64_t d, int64_t f, int64_t C,
                           double eta, int pad_mode, const float* H,
                           const float* X0, const float* W_gate,
                           const float* W_up, const float* w0,
                           const float* W_target, const float* conv_w,
-                          int64_t count, const int64_t* m_idx,
-                          const int64_t* j_idx, double* out) {
-  const int64_t n = T / C;
+                          const float* eta_tok, int64_t count,
+                          const int64_t* m_idx, const int64_t* j_idx,
+                          double* out) {
+  const int64_t n = num_chunks(T, C);
 #pragma omp parallel for schedule(dynamic)
   for (int64_t q = 0; q < count; ++q) {
     const int64_t m = m_idx[q], j = j_idx[q];
     double sum = 0.0;
     out[q * (n + 1)] = (double)w0[m * f + j];
     for (int64_t i = 0; i < n; ++i) {
-      for (int64_t s = i * C; s < (i + 1) * C; ++s) {
+      for (int64_t s = i * C; s < i * C + chunk_len(T, C, i); ++s) {
         double g = 0.0, u = 0.0;
         for (int64_t k = 0; k < d; ++k) {
           g += (double)H[s * d + k] * (double)W_gate[j * d + k];
           u += (double)H[s * d + k] * (double)W_up[j * d + k];
         }
-        sum += vhat_entry(T, d, C, pad_mode, X0, conv_w, W_target, s, m) *
-               (silu(g) * u);
+        sum += token_rate(eta_tok, s) *
+               vhat_entry(T, d, C, pad_mode, X0, conv_w, W_target, s, m) * (silu(g) * u);
       }
       out[q * (n + 1) + i + 1] = (double)w0[m * f + j] + eta * sum;
     }

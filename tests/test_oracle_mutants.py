@@ -19,25 +19,29 @@ MUTANTS = [
     ("conv_taps_flipped",
      "acc += (double)conv_w[c * 3 + (k + 1)] * (double)X0[s * d + c];",
      "acc += (double)conv_w[c * 3 + (1 - k)] * (double)X0[s * d + c];"),
-    ("conv_ignores_chunk_edges", "lo = (t / C) * C;\n      hi = lo + C;", "lo = 0;\n      hi = T;"),
+    ("conv_ignores_chunk_edges", "lo = (t / C) * C;\n      hi = lo + C < T ? lo + C : T;",
+     "lo = 0;\n      hi = T;"),
     ("target_not_transposed",
      "acc += Xc[t * d + c] * (double)W_target[m * d + c];",
      "acc += Xc[t * d + c] * (double)W_target[c * d + m];"),
     ("update_sign_flipped", "for (int64_t e = 0; e < d * f; ++e) W[e] += eta * dW[e];",
      "for (int64_t e = 0; e < d * f; ++e) W[e] -= eta * dW[e];"),
     ("update_before_apply",
-     "      apply_chunk(i * C, C, d, f, Z, W, O + b * T * d);          /* apply  */\n"
-     "      chunk_delta(i * C, C, d, f, Vhat, Z, dW);                  /* update */\n"
+     "      apply_chunk(i * C, Cn, d, f, Z, W, O + b * T * d);         /* apply  */\n"
+     "      chunk_delta(i * C, Cn, d, f, Vhat, Z, et, dW);             /* update */\n"
      "      for (int64_t e = 0; e < d * f; ++e) W[e] += eta * dW[e];",
-     "      chunk_delta(i * C, C, d, f, Vhat, Z, dW);\n"
+     "      chunk_delta(i * C, Cn, d, f, Vhat, Z, et, dW);\n"
      "      for (int64_t e = 0; e < d * f; ++e) W[e] += eta * dW[e];\n"
-     "      apply_chunk(i * C, C, d, f, Z, W, O + b * T * d);"),
+     "      apply_chunk(i * C, Cn, d, f, Z, W, O + b * T * d);"),
     ("initial_weight_dropped", "for (int64_t e = 0; e < d * f; ++e) W[e] = (double)W0[e];",
      "for (int64_t e = 0; e < d * f; ++e) W[e] = 0.0;"),
-    ("delta_reads_next_chunk", "for (int64_t t = t0; t < t0 + Cn; ++t)\n        acc += Vhat",
-     "for (int64_t t = t0 + 1; t < t0 + Cn + 1 && t < t0 + Cn; ++t)\n        acc += Vhat"),
-    ("delta_uses_Z_for_both_operands", "acc += Vhat[t * d + m] * Z[t * f + j];",
-     "acc += Z[t * f + m] * Z[t * f + j];"),
+    ("delta_drops_first_token", "for (int64_t t = t0; t < t0 + Cn; ++t)\n        acc += token_rate",
+     "for (int64_t t = t0 + 1; t < t0 + Cn; ++t)\n        acc += token_rate"),
+    ("delta_uses_Z_for_both_operands", "Vhat[t * d + m] * Z[t * f + j];",
+     "Z[t * f + m] * Z[t * f + j];"),
+    ("token_rate_ignored", "return eta_tok ? (double)eta_tok[t] : 1.0;", "return 1.0;"),
+    ("partial_chunk_dropped", "static int64_t num_chunks(int64_t T, int64_t C) { return (T + C - 1) / C; }",
+     "static int64_t num_chunks(int64_t T, int64_t C) { return T / C; }"),
     ("prefix_scan_inclusive",
      "S[i * df + e] = S[(i - 1) * df + e] + dWs[(i - 1) * df + e];",
      "S[i * df + e] = S[(i - 1) * df + e] + dWs[(i < n ? i : n - 1) * df + e];"),

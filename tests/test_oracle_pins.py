@@ -87,7 +87,7 @@ def test_z_matches_library():
 
 
 @pytest.mark.parametrize("pad_mode", [oracle.PAD_CHUNK, oracle.PAD_SEQUENCE])
-@pytest.mark.parametrize("T,C", [(12, 4), (12, 12), (10, 1), (9, 3)])
+@pytest.mark.parametrize("T,C", [(12, 4), (12, 12), (10, 1), (9, 3), (10, 4), (7, 3), (5, 8)])
 def test_value_target_matches_library(pad_mode, T, C):
     """Method §2 eq. (5): Vhat = Conv1D(X0) W_target^T, depthwise 3-tap conv,
     zero padded at chunk edges (chunk mode) or at sequence ends."""
@@ -105,21 +105,30 @@ def test_value_target_matches_library(pad_mode, T, C):
 # The update is the gradient step of the stated loss (brute force)
 # --------------------------------------------------------------------------
 
-def test_update_is_gradient_of_inner_product_loss():
+@pytest.mark.parametrize("T,C,per_token", [(6, 3, False), (7, 3, False), (7, 3, True)])
+def test_update_is_gradient_of_inner_product_loss(T, C, per_token):
     """Method §2: with L(W) = -<Z_[i] W^T, Vhat_[i]>_F the step
     W <- W - eta grad L is W + eta Vhat_[i]^T Z_[i] (eq. (6)).  Central finite
     differences of L over every entry of W (L is linear in W, so they are
-    exact up to rounding) must equal -(W^(i+1) - W^(i)) / eta for each chunk."""
-    d, f, T, C, eta = 4, 8, 6, 3, 0.37
+    exact up to rounding) must equal -(W^(i+1) - W^(i)) / eta for each chunk,
+    the partial last chunk included.  With per-token rates the loss is
+    sum_t eta_t L_t (the large-chunk update of "Test-Time Training Done
+    Right", per-token eta_i)."""
+    d, f, eta = 4, 8, 0.37
     inp = _inputs(1, T, d, f, seed=21)
-    out = oracle.forward(inp, eta=eta, chunk=C, want_z=True, want_vhat=True, want_states=True)
+    rates = (torch.rand(1, T, generator=torch.Generator().manual_seed(5)) + 0.25
+             if per_token else None)
+    out = oracle.forward(inp, eta=eta, chunk=C, want_z=True, want_vhat=True, want_states=True,
+                         eta_tok=rates)
     Z, V, S = out["Z"][0], out["Vhat"][0], out["states"][0]
+    wt = np.ones(T) if rates is None else rates[0].double().numpy()
     h = 1e-3
-    for i in range(T // C):
+    for i in range(-(-T // C)):
         Zi, Vi = Z[i * C:(i + 1) * C], V[i * C:(i + 1) * C]
+        wi = wt[i * C:(i + 1) * C, None]
 
         def loss(W):
-            return -np.sum((Zi @ W.T) * Vi)
+            return -np.sum(wi * (Zi @ W.T) * Vi)
 
         W = S[i].copy()
         grad = np.zeros_like(W)
@@ -344,7 +353,88 @@ def test_entrywise_evaluators_agree_with_forward(pad_mode):
         full["O"][b][rows], rtol=1e-12, atol=1e-14)
 
 
-def test_rejects_chunk_not_dividing_T():
-    inp = _inputs(1, 10, 3, 4, seed=1)
-    with pytest.raises(ValueError):
-        oracle.forward(inp, 0.1, 3)
+# --------------------------------------------------------------------------
+# Partial last chunk (streams whose length is not a multiple of C)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,C", [(10, 4), (7, 3), (13, 5)])
+def test_partial_last_chunk_extends_the_full_chunks(T, C):
+    """The chunks before the partial one are exactly the run on the first
+    floor(T/C) chunks (causality of the chunk order), and the partial chunk
+    is applied with the state that run ends with."""
+    inp = _inputs(2, T, 4, 6, seed=71)
+    full = oracle.forward(inp, 0.4, C, want_states=True, want_z=True)
+    Tk = (T // C) * C
+    head = dict(inp)
+    head["H"], head["X0"] = inp["H"][:, :Tk], inp["X0"][:, :Tk]
+    part = oracle.forward(head, 0.4, C, want_states=True)
+    np.testing.assert_array_equal(full["O"][:, :Tk], part["O"])
+    np.testing.assert_array_equal(full["states"][:, :T // C + 1], part["states"])
+    Wl = full["states"][:, T // C]
+    for b in range(2):
+        np.testing.assert_allclose(full["O"][b, Tk:], full["Z"][b, Tk:] @ Wl[b].T,
+                                   rtol=1e-12, atol=1e-13)
+
+
+def test_chunk_longer_than_sequence_is_one_partial_chunk():
+    inp = _inputs(1, 5, 3, 4, seed=73)
+    got = oracle.forward(inp, 0.9, 8)["O"]
+    ref = F.linear(_lib_gated_mlp_z(inp["H"], inp["W_gate"], inp["W_up"]), _t64(inp["W_down0"]))
+    np.testing.assert_allclose(got, ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("T,C", [(10, 4), (13, 5)])
+def test_forms_agree_with_partial_last_chunk(T, C):
+    inp = _inputs(2, T, 4, 5, seed=75)
+    seq = oracle.forward(inp, 0.3, C, want_states=True)
+    pre = oracle.forward_prefix(inp, 0.3, C, want_states=True)
+    dual = oracle.forward_dual(inp, 0.3, C)
+    np.testing.assert_allclose(pre["O"], seq["O"], rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(pre["states"], seq["states"], rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(dual["O"], seq["O"], rtol=1e-11, atol=1e-11)
+
+
+# --------------------------------------------------------------------------
+# Per-token learning rates ("Test-Time Training Done Right", per-token eta_i)
+# --------------------------------------------------------------------------
+
+def test_unit_token_rates_are_the_plain_update():
+    inp = _inputs(2, 12, 4, 6, seed=81)
+    plain = oracle.forward(inp, 0.3, 4, want_states=True)
+    ones = oracle.forward(inp, 0.3, 4, want_states=True, eta_tok=torch.ones(2, 12))
+    np.testing.assert_array_equal(ones["O"], plain["O"])
+    np.testing.assert_array_equal(ones["states"], plain["states"])
+
+
+def test_constant_token_rate_scales_eta():
+    inp = _inputs(2, 12, 4, 6, seed=83)
+    a = oracle.forward(inp, 0.3 * 0.25, 4, want_states=True)
+    b = oracle.forward(inp, 0.3, 4, want_states=True, eta_tok=torch.full((2, 12), 0.25))
+    np.testing.assert_allclose(b["O"], a["O"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(b["states"], a["states"], rtol=1e-12, atol=1e-13)
+
+
+def test_zero_token_rates_freeze_the_state():
+    """Rate 0 on every token of chunk 1 leaves the state unchanged by it."""
+    inp = _inputs(1, 12, 4, 6, seed=85)
+    rates = torch.ones(1, 12)
+    rates[0, 4:8] = 0.0
+    out = oracle.forward(inp, 0.3, 4, want_states=True, eta_tok=rates)
+    np.testing.assert_array_equal(out["states"][0, 2], out["states"][0, 1])
+    assert np.abs(out["states"][0, 3] - out["states"][0, 2]).max() > 1e-6
+
+
+def test_forms_agree_with_token_rates():
+    inp = _inputs(2, 13, 4, 5, seed=87)
+    rates = torch.rand(2, 13, generator=torch.Generator().manual_seed(9))
+    seq = oracle.forward(inp, 0.3, 4, want_states=True, eta_tok=rates)
+    pre = oracle.forward_prefix(inp, 0.3, 4, want_states=True, eta_tok=rates)
+    dual = oracle.forward_dual(inp, 0.3, 4, eta_tok=rates)
+    np.testing.assert_allclose(pre["O"], seq["O"], rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(pre["states"], seq["states"], rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(dual["O"], seq["O"], rtol=1e-11, atol=1e-11)
+    m, j = np.array([0, 3, 1]), np.array([4, 0, 2])
+    st = oracle.state_entries(inp["H"][1], inp["X0"][1], inp["W_gate"], inp["W_up"],
+                              inp["W_down0"], inp["W_target"], inp["conv_w"], 0.3, 4, m, j,
+                              eta_tok=rates[1])
+    np.testing.assert_allclose(st, seq["states"][1][:, m, j].T, rtol=1e-12, atol=1e-13)
