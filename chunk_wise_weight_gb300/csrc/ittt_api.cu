@@ -154,15 +154,14 @@ ittt_status check_sizes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chun
   if (B <= 0 || T <= 0 || d <= 0 || f <= 0)
     return fail(ITTT_ERR_INVALID_ARG, "sizes must be positive (B=%lld T=%lld d=%lld f=%lld)",
                 (long long)B, (long long)T, (long long)d, (long long)f);
-  if (chunk <= 0 || T % chunk != 0)
-    return fail(ITTT_ERR_INVALID_ARG, "chunk %lld must be positive and divide T=%lld",
+  if (chunk <= 0) return fail(ITTT_ERR_INVALID_ARG, "chunk %lld must be positive", (long long)chunk);
+  if (chunk % 64 != 0 || T % 64 != 0)
+    return fail(ITTT_ERR_UNSUPPORTED, "chunk %lld and T %lld must be multiples of 64",
                 (long long)chunk, (long long)T);
-  if (chunk % 64 != 0)
-    return fail(ITTT_ERR_UNSUPPORTED, "chunk %lld is not a multiple of 64", (long long)chunk);
   if (d % 8 != 0 || f % 8 != 0)
     return fail(ITTT_ERR_UNSUPPORTED, "d_model=%lld and d_ff=%lld must be multiples of 8",
                 (long long)d, (long long)f);
-  const int64_t n = T / chunk;
+  const int64_t n = (T + chunk - 1) / chunk;
   if (B * T >= (int64_t(1) << 31) || B * n * d >= (int64_t(1) << 31) || d * f >= (int64_t(1) << 40))
     return fail(ITTT_ERR_UNSUPPORTED, "sizes exceed 32-bit tile coordinates");
   return ITTT_OK;
@@ -178,7 +177,7 @@ size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
 Layout plan_workspace(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk, bool need_z,
                       bool need_vhat, bool need_xc, bool need_snap) {
   Layout L;
-  const int64_t n = T / chunk;
+  const int64_t n = (T + chunk - 1) / chunk;
   size_t off = 0;
   if (need_z) {
     L.z = off;
@@ -267,7 +266,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   ittt_status s = check_sizes(B, T, d, f, chunk);
   if (s != ITTT_OK) return s;
   if (!std::isfinite(eta)) return fail(ITTT_ERR_INVALID_ARG, "eta is not finite");
-  const int64_t n = T / chunk;
+  const int64_t n = (T + chunk - 1) / chunk;  // the last chunk may be partial
+  if (dual && T % chunk != 0)
+    return fail(ITTT_ERR_UNSUPPORTED, "the dual form needs chunk to divide T");
 
   const int64_t sh_btd[3] = {B, T, d}, sh_fd[2] = {f, d}, sh_df[2] = {d, f}, sh_dd[2] = {d, d},
                 sh_d3[2] = {d, 3}, sh_bdf[3] = {B, d, f}, sh_btf[3] = {B, T, f},
@@ -288,9 +289,11 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if (o.z_buf && (s = check_tensor(o.z_buf, "z_buf", 3, sh_btf, true, false))) return s;
   if (o.vhat_buf && (s = check_tensor(o.vhat_buf, "vhat_buf", 3, sh_btd, true, false))) return s;
   if (o.snap_buf && (s = check_tensor(o.snap_buf, "snap_buf", 4, sh_bndf, true, false))) return s;
+  const int64_t sh_bt[2] = {B, T};
+  if (o.eta_tok && (s = check_tensor(o.eta_tok, "eta_tok", 2, sh_bt, false, true))) return s;
 
-  const ittt_tensor* inputs[] = {H, X0, W_gate, W_up, o.state_in ? o.state_in : W_down0,
-                                 W_target, conv_w};
+  const ittt_tensor* inputs[] = {H,        X0,     W_gate,   W_up, o.state_in ? o.state_in : W_down0,
+                                 W_target, conv_w, o.eta_tok};
   const ittt_tensor* writes[] = {out, o.state_out, o.z_buf, o.vhat_buf, o.snap_buf};
   for (const ittt_tensor* w : writes) {
     for (const ittt_tensor* in : inputs)
@@ -361,7 +364,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   memset(&tm_os, 0, sizeof(tm_os));
   if ((s = make_map(&tm_vs, vhat, d, M, 64, 128, "Vhat (store)"))) return s;
   if (out->dtype == ITTT_BF16 &&
-      (s = make_map_3d(&tm_os, out->data, d, chunk, uint64_t(B * n), 64, 128, "O (store)")))
+      (s = make_map_3d(&tm_os, out->data, d, T, uint64_t(B), 64, 64, "O (store)")))
     return s;
   if ((s = make_map(&tm_vmn, vhat, d, M, 64, 64, "Vhat"))) return s;
   if ((s = make_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
@@ -403,8 +406,10 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   }
   ITTT_STEP(rec(2 * ITTT_PHASE_CONV + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_TARGET, stream), "event record");
-  ITTT_STEP(ittt::launch_target(env, tm_a, tm_wt, tm_vs, cw, vhat, eta, int(M), int(T), int(d),
-                                int(chunk), int(o.pad_mode), fused),
+  ITTT_STEP(ittt::launch_target(env, tm_a, tm_wt, tm_vs, cw,
+                                o.eta_tok ? static_cast<const float*>(o.eta_tok->data) : nullptr,
+                                vhat, eta, int(M), int(T), int(d), int(chunk), int(o.pad_mode),
+                                fused),
             "target launch");
   ITTT_STEP(rec(2 * ITTT_PHASE_TARGET + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP, stream), "event record");

@@ -190,14 +190,12 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   const int64_t B = H->shape[0], T = H->shape[1], d = H->shape[2], f = W_gate->shape[0];
   if (B <= 0 || T <= 0 || d <= 0 || f <= 0)
     return na_fail(ITTT_ERR_INVALID_ARG, "sizes must be positive");
-  if (chunk <= 0 || T % chunk != 0)
-    return na_fail(ITTT_ERR_INVALID_ARG, "chunk %lld must be positive and divide T=%lld",
-                   (long long)chunk, (long long)T);
-  if (chunk % 64 != 0 || d % 8 != 0 || f % 8 != 0)
+  if (chunk <= 0) return na_fail(ITTT_ERR_INVALID_ARG, "chunk must be positive");
+  if (chunk % 64 != 0 || T % 64 != 0 || d % 8 != 0 || f % 8 != 0)
     return na_fail(ITTT_ERR_UNSUPPORTED,
-                   "chunk must be a multiple of 64, d_model and d_ff multiples of 8");
+                   "chunk and T must be multiples of 64, d_model and d_ff multiples of 8");
   if (!std::isfinite(eta)) return na_fail(ITTT_ERR_INVALID_ARG, "eta is not finite");
-  const int64_t n = T / chunk;
+  const int64_t n = (T + chunk - 1) / chunk;  // the last chunk may be partial
   const int64_t sh_btd[3] = {B, T, d}, sh_fd[2] = {f, d}, sh_df[2] = {d, f}, sh_dd[2] = {d, d},
                 sh_d3[2] = {d, 3};
   ittt_status s;
@@ -250,7 +248,7 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   if ((s = na_map_3d(&tm_ss, snap, f, d, uint64_t(B * n), 64, 128, "snapshots (store)")))
     return s;
   if (out->dtype == ITTT_BF16 &&
-      (s = na_map_3d(&tm_os, out->data, d, chunk, uint64_t(B * n), 64, 128, "O (store)")))
+      (s = na_map_3d(&tm_os, out->data, d, T, uint64_t(B), 64, 64, "O (store)")))
     return s;
 
   const ittt::LaunchEnv env{stream, nd->num_sms, nd->status};
@@ -262,9 +260,9 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
                              int(d), int(chunk), ITTT_PAD_CHUNK)) != cudaSuccess) {
     what = "conv";
   } else if ((e = ittt::launch_target(env, tm_xc, tm_wt, tm_vs,
-                                      static_cast<const float*>(conv_w->data), vhat, eta, int(M),
-                                      int(T), int(d), int(chunk), ITTT_PAD_CHUNK, false)) !=
-             cudaSuccess) {
+                                      static_cast<const float*>(conv_w->data), nullptr, vhat, eta,
+                                      int(M), int(T), int(d), int(chunk), ITTT_PAD_CHUNK,
+                                      false)) != cudaSuccess) {
     what = "target";
   } else if ((e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d))) !=
              cudaSuccess) {

@@ -6,7 +6,8 @@
 // W_i is the bf16 snapshot the update kernel wrote (slot 0 holds W_0).  A
 // work unit is (sequence b, chunk i, 128-row tile of the chunk, 256-column
 // tile of d_model); rows past the chunk's end belong to another chunk and are
-// computed but not stored, so any chunk size that is a multiple of 64 works.
+// computed but not stored, so any chunk size that is a multiple of 64 works,
+// and the last chunk may be the shorter remainder of the sequence.
 #include "kernels.h"
 #include "pipeline.cuh"
 
@@ -16,7 +17,7 @@ namespace {
 struct ApplyParams {
   CUtensorMap tm_z;     // Z          [B*T, f]    box {64, 128}
   CUtensorMap tm_snap;  // snapshots  [B*n*d, f]  box {64, 256}
-  CUtensorMap tm_os;    // bf16 O as [B*n chunks][C rows][d cols], box {64, 128, 1} (store)
+  CUtensorMap tm_os;    // bf16 O as [B][T rows][d cols], box {64, 64, 1} (store)
   void* out;            // O [B*T, d], bf16 or fp32
   int out_fp32;
   int B, T, d, f, C, n;
@@ -29,7 +30,7 @@ struct ApplySched : SchedDefaults {
   static constexpr bool kStagedStores = true;
 
   const Params& p;
-  int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0, chunk_id = 0, crow0 = 0;
+  int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0, seq = 0, srow0 = 0;
 
   __device__ explicit ApplySched(const Params& pp) : p(pp) {}
   __device__ int num_units() const { return p.B * p.n * p.mt_per_chunk * p.nt; }
@@ -42,13 +43,14 @@ struct ApplySched : SchedDefaults {
     const int b = r / p.n;
     arow0 = b * p.T + i * p.C + mt * kBM;
     brow0 = (b * p.n + i) * p.d + nt * kBN;
-    rows_valid = min(kBM, p.C - mt * kBM);
+    rows_valid = min(kBM, min(p.C, p.T - i * p.C) - mt * kBM);
     n0 = nt * kBN;
-    chunk_id = b * p.n + i;
-    crow0 = mt * kBM;
+    seq = b;
+    srow0 = i * p.C + mt * kBM;
     acc = local & 1;
   }
-  __device__ int num_segments() const { return 1; }
+  // Row tiles past the end of a partial last chunk have nothing to do.
+  __device__ int num_segments() const { return rows_valid > 0 ? 1 : 0; }
   __device__ int seg_acc(int) const { return acc; }
   __device__ int seg_kblocks(int) const { return p.kblocks; }
   __device__ bool seg_fresh(int) const { return true; }
@@ -65,9 +67,10 @@ struct ApplySched : SchedDefaults {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
   }
 
-  // bf16 O: four 64-column TMA stores through the chunk-bounded 3-D map
-  // (rows past the chunk and columns >= d are not written).  fp32 O: direct
-  // 16-byte stores.
+  // bf16 O: 64-column TMA stores of 64-row halves through a [B][T][d] map:
+  // the second half is stored only when the chunk reaches it (chunk lengths
+  // are multiples of 64), rows >= T and columns >= d are clipped.  fp32 O:
+  // direct 16-byte stores.
   __device__ void epilogue(int, int row, uint32_t trow, EpiStager& st) const {
     if (!p.out_fp32) {
 #pragma unroll 1
@@ -89,7 +92,8 @@ struct ApplySched : SchedDefaults {
                        pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]))));
         }
         st.commit(buf, [&](uint8_t* src) {
-          tma_store_3d(&p.tm_os, src, n0 + g * 64, crow0, chunk_id);
+          tma_store_3d(&p.tm_os, src, n0 + g * 64, srow0, seq);
+          if (rows_valid > 64) tma_store_3d(&p.tm_os, src + 64 * 128, n0 + g * 64, srow0 + 64, seq);
         });
       }
       return;
@@ -151,7 +155,7 @@ cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z, const CU
   p.d = d;
   p.f = f;
   p.C = C;
-  p.n = T / C;
+  p.n = (T + C - 1) / C;
   p.mt_per_chunk = (C + kBM - 1) / kBM;
   p.nt = (d + kBN - 1) / kBN;
   p.kblocks = (f + kBK - 1) / kBK;

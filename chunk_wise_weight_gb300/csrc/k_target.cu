@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256)
     int lo = 0, hi = T;
     if (pad_mode == 0) {
       lo = (t / C) * C;
-      hi = lo + C;
+      hi = min(lo + C, T);  // a partial last chunk ends at T
     }
     const size_t base = size_t(r) * size_t(d) + size_t(g) * 8;
     const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
@@ -120,6 +120,7 @@ struct TargetParams {
   CUtensorMap tm_wt;     // W_target [d, d]  box {64, 256}
   CUtensorMap tm_vs;     // eta*Vhat [M, d]  box {64, 128}  (TMA store, split variant)
   const float* conv_w;   // [d, 3]
+  const float* eta_tok;  // [M] per-token rate weights or nullptr
   __nv_bfloat16* vhat;   // eta * Vhat [M, d]
   float eta;
   int M, T, d, C, pad_mode;
@@ -224,7 +225,7 @@ struct TargetSched : SchedDefaults {
     if (p.pad_mode == 0) {
       const int pc = t0 % p.C;
       prev_ok = pc > 0;
-      next_ok = pc + 4 < p.C;
+      next_ok = pc + 4 < min(p.C, p.T - (t0 - pc));  // a partial last chunk ends at T
     } else {
       prev_ok = t0 > 0;
       next_ok = t0 + 4 < p.T;
@@ -255,9 +256,15 @@ struct TargetSched : SchedDefaults {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
   }
 
+  // The update's rate for token row gm: eta, times its per-token weight.
+  __device__ float row_rate(int gm) const {
+    return p.eta_tok == nullptr ? p.eta : (gm < p.M ? p.eta * __ldg(p.eta_tok + gm) : 0.0f);
+  }
+
   // Split variant: 256 columns as four 64-column TMA stores (rows >= M and
   // columns >= d are not written).
-  __device__ void epilogue(int, int, uint32_t trow, EpiStager& st) const {
+  __device__ void epilogue(int, int row, uint32_t trow, EpiStager& st) const {
+    const float scale = row_rate(m0 + row);
 #pragma unroll 1
     for (int g = 0; g < kBN / 64; ++g) {
       uint8_t* buf = st.acquire();
@@ -270,14 +277,14 @@ struct TargetSched : SchedDefaults {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           st.put(buf, hc * 4 + q,
-                 make_uint4(pack_bf16x2(p.eta * __uint_as_float(v[8 * q]),
-                                        p.eta * __uint_as_float(v[8 * q + 1])),
-                            pack_bf16x2(p.eta * __uint_as_float(v[8 * q + 2]),
-                                        p.eta * __uint_as_float(v[8 * q + 3])),
-                            pack_bf16x2(p.eta * __uint_as_float(v[8 * q + 4]),
-                                        p.eta * __uint_as_float(v[8 * q + 5])),
-                            pack_bf16x2(p.eta * __uint_as_float(v[8 * q + 6]),
-                                        p.eta * __uint_as_float(v[8 * q + 7]))));
+                 make_uint4(pack_bf16x2(scale * __uint_as_float(v[8 * q]),
+                                        scale * __uint_as_float(v[8 * q + 1])),
+                            pack_bf16x2(scale * __uint_as_float(v[8 * q + 2]),
+                                        scale * __uint_as_float(v[8 * q + 3])),
+                            pack_bf16x2(scale * __uint_as_float(v[8 * q + 4]),
+                                        scale * __uint_as_float(v[8 * q + 5])),
+                            pack_bf16x2(scale * __uint_as_float(v[8 * q + 6]),
+                                        scale * __uint_as_float(v[8 * q + 7]))));
       }
       st.commit(buf, [&](uint8_t* src) { tma_store_2d(&p.tm_vs, src, n0 + g * 64, m0); });
     }
@@ -287,6 +294,7 @@ struct TargetSched : SchedDefaults {
   __device__ void epilogue(int, int row, uint32_t trow) const {
     const int gm = m0 + row;
     const bool row_ok = gm < p.M;
+    const float scale = row_rate(gm);
     __nv_bfloat16* vrow = p.vhat + size_t(row_ok ? gm : 0) * size_t(p.d);
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 32) {
@@ -297,8 +305,8 @@ struct TargetSched : SchedDefaults {
       uint32_t pk[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        pk[j] = pack_bf16x2(p.eta * __uint_as_float(v[2 * j]),
-                            p.eta * __uint_as_float(v[2 * j + 1]));
+        pk[j] = pack_bf16x2(scale * __uint_as_float(v[2 * j]),
+                            scale * __uint_as_float(v[2 * j + 1]));
       if (row_ok) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -345,9 +353,11 @@ cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const flo
 }
 
 cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a, const CUtensorMap& tm_wt,
-                          const CUtensorMap& tm_vs, const float* conv_w, __nv_bfloat16* vhat,
-                          float eta, int M, int T, int d, int C, int pad_mode, bool fused) {
+                          const CUtensorMap& tm_vs, const float* conv_w, const float* eta_tok,
+                          __nv_bfloat16* vhat, float eta, int M, int T, int d, int C, int pad_mode,
+                          bool fused) {
   TargetParams p;
+  p.eta_tok = eta_tok;
   p.tm_a = tm_a;
   p.tm_wt = tm_wt;
   p.tm_vs = tm_vs;

@@ -37,7 +37,7 @@ struct UpdateParams {
   __nv_bfloat16* snap;  // [B, n, d, f]
   float* state_out;     // [B, d, f] or nullptr
   int B, T, d, f, C, n, n_upd;
-  int mt, np, kb_per_chunk;
+  int mt, np, kb_per_chunk, kb_last;  // K blocks of a full chunk / of chunk n-1
 };
 
 struct UpdateSched : SchedDefaults {
@@ -65,7 +65,10 @@ struct UpdateSched : SchedDefaults {
   __device__ int num_segments() const { return p.n_upd * halves; }
   __device__ int unit_accs() const { return halves; }
   __device__ int seg_acc(int s) const { return halves == 2 ? (s & 1) : 0; }
-  __device__ int seg_kblocks(int) const { return p.kb_per_chunk; }
+  __device__ int seg_kblocks(int s) const {
+    const int i = halves == 2 ? (s >> 1) : s;
+    return i == p.n - 1 ? p.kb_last : p.kb_per_chunk;
+  }
   __device__ bool seg_fresh(int) const { return false; }  // starts from the preloaded W_0
 
   __device__ void load(int s, int kb, uint8_t* stage, uint64_t* bar) const {
@@ -249,6 +252,7 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
   p.mt = (a.d + kBM - 1) / kBM;
   p.np = (a.f + 2 * kBN - 1) / (2 * kBN);
   p.kb_per_chunk = a.C / kBK;
+  p.kb_last = (a.T - (a.n - 1) * a.C) / kBK;
   const int units = p.B * p.mt * p.np;
   cudaError_t e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(pipe_smem_bytes<UpdateSched>()));

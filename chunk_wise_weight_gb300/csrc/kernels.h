@@ -29,15 +29,16 @@ cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h,
 cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const float* conv_w,
                         __nv_bfloat16* xc, int64_t rows, int T, int d, int C, int pad_mode);
 
-// vhat[M, d] = eta * (Conv1D(X0) W_target^T), rounded once to bf16.
+// vhat[M, d] = eta * eta_tok[row] * (Conv1D(X0) W_target^T), rounded once to
+// bf16 (eta_tok may be null: weight 1).
 // Split (fused = false): tm_a maps Xc [M, d] with box {64,128} and the
 // output goes out through tm_vs (vhat [M, d], box {64,128}).
 // Fused: tm_a maps X0 [M, d] with box {64,130}, the kernel computes the conv
 // itself and stores vhat directly.  tm_wt: W_target [d, d] box {64,256}.
 cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a,
                           const CUtensorMap& tm_wt, const CUtensorMap& tm_vs,
-                          const float* conv_w, __nv_bfloat16* vhat, float eta, int M, int T,
-                          int d, int C, int pad_mode, bool fused);
+                          const float* conv_w, const float* eta_tok, __nv_bfloat16* vhat,
+                          float eta, int M, int T, int d, int C, int pad_mode, bool fused);
 
 // snap[b, 0] = bf16(W_0 of sequence b) for every b.  w0 is bf16 or fp32,
 // [d, f] shared (w0_bstride = 0) or [B, d, f].
@@ -68,7 +69,8 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
 
 // O_[i] = Z_[i] snap[b, i]^T for every (sequence, chunk).  Tensor maps:
 // Z [B*T, f] box {64,128}; snapshots [B*n*d, f] box {64,256}; bf16 O as
-// [B*n][C][d] with box {64,128,1} for the TMA stores (unused for fp32 O).
+// [B][T][d] with box {64,64,1} for the TMA stores (unused for fp32 O).  The
+// last chunk may be shorter than C (n = ceil(T / C)).
 cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
                          const CUtensorMap& tm_snap, const CUtensorMap& tm_os, void* out,
                          bool out_fp32, int B, int T, int d, int f, int C);

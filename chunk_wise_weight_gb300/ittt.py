@@ -44,7 +44,8 @@ class Opts(ctypes.Structure):
                 ("state_in", ctypes.POINTER(Tensor)), ("state_out", ctypes.POINTER(Tensor)),
                 ("z_buf", ctypes.POINTER(Tensor)), ("vhat_buf", ctypes.POINTER(Tensor)),
                 ("snap_buf", ctypes.POINTER(Tensor)), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t), ("events", ctypes.POINTER(ctypes.c_void_p))]
+                ("workspace_bytes", ctypes.c_size_t), ("events", ctypes.POINTER(ctypes.c_void_p)),
+                ("eta_tok", ctypes.POINTER(Tensor))]
 
 
 _TP = ctypes.POINTER(Tensor)
@@ -133,7 +134,7 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
             out: torch.Tensor | None = None, *, out_dtype=torch.bfloat16, stream=None,
             pad_mode: int = PAD_CHUNK, state_in=None, state_out=None, z_buf=None,
             vhat_buf=None, snap_buf=None, workspace=None, events=None,
-            fused_conv: bool = False, dual: bool = False) -> torch.Tensor:
+            fused_conv: bool = False, dual: bool = False, eta_tok=None) -> torch.Tensor:
     """Enqueue one layer forward on `stream` (default: current stream) and
     return `out` [B,T,d].  Extra keyword buffers map to ittt_opts; `events`
     is a list of 2 * len(PHASES) torch.cuda.Event(enable_timing=True): a
@@ -147,7 +148,7 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
     opts.flags = (FLAG_FUSED_CONV if fused_conv else 0) | (FLAG_DUAL if dual else 0)
     extra = {}
     for name, t in (("state_in", state_in), ("state_out", state_out), ("z_buf", z_buf),
-                    ("vhat_buf", vhat_buf), ("snap_buf", snap_buf)):
+                    ("vhat_buf", vhat_buf), ("snap_buf", snap_buf), ("eta_tok", eta_tok)):
         if t is not None:
             extra[name] = describe(t)
             setattr(opts, name, ctypes.pointer(extra[name]))

@@ -28,8 +28,10 @@
  *     bf16 or fp32; W_target [d,d] bf16; conv_w [d,3] fp32; out [B,T,d]
  *     bf16 or fp32.  Weights use the [out_features, in_features] layout.
  *   - Supported sizes: d and f multiples of 8 (16-byte rows), chunk > 0 a
- *     multiple of 64 that divides T, B*T < 2^31.  Anything else returns
- *     ITTT_ERR_UNSUPPORTED or ITTT_ERR_INVALID_ARG before any launch.
+ *     multiple of 64, T a multiple of 64, B*T < 2^31.  When chunk does not
+ *     divide T the last chunk is the shorter remainder (a stream that ends
+ *     mid-chunk).  Anything else returns ITTT_ERR_UNSUPPORTED or
+ *     ITTT_ERR_INVALID_ARG before any launch.
  *   - Ownership: the caller owns every buffer; the library keeps no pointer
  *     after a call returns.  `out` must not overlap any input.
  *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL is the
@@ -104,6 +106,10 @@ typedef struct {
  *              W_0 .. W_{n-1} that the apply step reads.
  *   workspace  device scratch of workspace_bytes >= ittt_workspace_bytes(...)
  *              (256-byte aligned); when given, nothing is allocated.
+ *   eta_tok    fp32 [B,T]: per-token learning-rate weights; token t's term
+ *              of the chunk update is scaled by eta * eta_tok[b,t] (the
+ *              large-chunk update with a rate per token of "Test-Time
+ *              Training Done Right").  NULL: every weight is 1.
  *   events     profiling: NULL, or 2 * ITTT_NUM_PHASES cudaEvent_t handles.
  *              events[2k] and events[2k+1] are recorded right before and
  *              right after phase k (ittt_phase order) on `stream`, so each
@@ -122,6 +128,7 @@ typedef struct {
   void* workspace;
   size_t workspace_bytes;
   void* const* events;
+  const ittt_tensor* eta_tok;
 } ittt_opts;
 
 /* ittt_opts.flags */
@@ -135,7 +142,8 @@ typedef struct {
  * scores kernel writes the block-lower part of Z Z^T (bf16, B*T*T*2 bytes of
  * scratch) and one GEMM accumulates both terms.  Same layer, different
  * rounding; more work than the primal walk on every workload measured, so
- * it is never the default.  Not combinable with state_out or snap_buf. */
+ * it is never the default.  Not combinable with state_out or snap_buf, and
+ * chunk must divide T. */
 #define ITTT_FLAG_DUAL 2
 
 /* Kernel phases of one forward call, in launch order. */
@@ -189,7 +197,8 @@ ITTT_API ittt_status ittt_forward_ex(const ittt_tensor* H, const ittt_tensor* X0
  * It calls no allocating routine.  Its scratch lives in one library-wide
  * device array of ITTT_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU which
  * loads the library holds until the process exits; a call that needs more
- * (B*T*(f + 2d)*2 + B*n*d*f*2 bytes, each part rounded up to 256) returns
+ * (B*T*(f + 2d)*2 + B*n*d*f*2 bytes with n = ceil(T/chunk), each part
+ * rounded up to 256) returns
  * ITTT_ERR_UNSUPPORTED before anything is enqueued.  All calls share that
  * array, so calls that overlap on the GPU (other streams, other threads)
  * race: serialise them on one stream.  The first call on a device does a

@@ -93,9 +93,12 @@ def test_rejects_bad_descriptors(lib, mutate, status, msg):
 
 
 def test_rejects_bad_sizes(lib):
-    assert _call(lib, _args(), chunk=100) == ittt.ERR_INVALID_ARG   # does not divide T
-    assert "divide" in ittt.last_error()
-    assert _call(lib, _args(T=96), chunk=32) == ittt.ERR_UNSUPPORTED  # not a multiple of 64
+    assert _call(lib, _args(), chunk=0) == ittt.ERR_INVALID_ARG
+    assert "positive" in ittt.last_error()
+    assert _call(lib, _args(), chunk=100) == ittt.ERR_UNSUPPORTED   # not a multiple of 64
+    assert "multiples of 64" in ittt.last_error()
+    assert _call(lib, _args(T=96), chunk=32) == ittt.ERR_UNSUPPORTED
+    assert _call(lib, _args(T=200), chunk=64) == ittt.ERR_UNSUPPORTED  # T not a multiple of 64
     assert _call(lib, _args(d=60), chunk=64) == ittt.ERR_UNSUPPORTED
     assert _call(lib, _args(f=100), chunk=64) == ittt.ERR_UNSUPPORTED
     assert _call(lib, _args(), eta=math.nan) == ittt.ERR_INVALID_ARG
@@ -123,6 +126,14 @@ def test_rejects_bad_options(lib):
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     assert "state_out" in ittt.last_error()
     o = ittt.Opts()
+    o.flags = ittt.FLAG_DUAL
+    assert _call(lib, _args(T=320), chunk=128, opts=o) == ittt.ERR_UNSUPPORTED  # partial chunk
+    o = ittt.Opts()
+    et = _desc([1, 256], ittt.BF16, data=FAKE * 9 * 1024)           # eta_tok must be fp32
+    o.eta_tok = ctypes.pointer(et)
+    assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
+    assert "eta_tok" in ittt.last_error()
+    o = ittt.Opts()
     zb = _desc([1, 256, 256], ittt.BF16, data=a["X0"].data)      # z_buf aliases X0
     o.z_buf = ctypes.pointer(zb)
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
@@ -135,6 +146,8 @@ def test_workspace_bytes_and_launch_count(lib):
     n = T // C
     want = r(B * T * f * 2) + 2 * r(B * T * d * 2) + r(B * n * d * f * 2)
     assert ittt.workspace_bytes(B, T, d, f, C) == want
+    want3 = r(B * T * f * 2) + 2 * r(B * T * d * 2) + r(B * 3 * d * f * 2)   # 1024 = 2*384+256
+    assert ittt.workspace_bytes(B, T, d, f, 384) == want3
     assert ittt.workspace_bytes(B, T, d, f, 100) == 0
     assert ittt.launch_count(B, T, d, f, C) == 6
     assert ittt.launch_count(B, T, d, f, T) == 5

@@ -49,7 +49,7 @@ def to_device(inp, dev, w0_dtype=torch.bfloat16):
 
 
 def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
-        state_in=None, want_state=False, fused_conv=False, dual=False):
+        state_in=None, want_state=False, fused_conv=False, dual=False, eta_tok=None):
     B, T, d = g["H"].shape
     f = g["W_gate"].shape[0]
     dev = g["H"].device
@@ -58,7 +58,7 @@ def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
         kw["z_buf"] = torch.empty(B, T, f, dtype=torch.bfloat16, device=dev)
         kw["vhat_buf"] = torch.empty(B, T, d, dtype=torch.bfloat16, device=dev)
         if not dual:
-            kw["snap_buf"] = torch.empty(B, T // C, d, f, dtype=torch.bfloat16, device=dev)
+            kw["snap_buf"] = torch.empty(B, -(-T // C), d, f, dtype=torch.bfloat16, device=dev)
     if want_state:
         kw["state_out"] = torch.empty(B, d, f, dtype=torch.float32, device=dev)
     if state_in is not None:
@@ -66,7 +66,7 @@ def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
     out = ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"],
                        None if state_in is not None else g["W_down0"], g["W_target"],
                        g["conv_w"], eta, C, out_dtype=out_dtype, pad_mode=pad_mode,
-                       fused_conv=fused_conv, dual=dual, **kw)
+                       fused_conv=fused_conv, dual=dual, eta_tok=eta_tok, **kw)
     ittt.stream_status()
     res = {"O": out}
     res.update(kw)
@@ -171,6 +171,47 @@ def test_state_out_and_streaming_continuation(cuda_device):
 
 
 # --------------------------------------------------------------------------
+# Partial last chunk and per-token learning rates
+# --------------------------------------------------------------------------
+
+PARTIAL = [
+    # B, T, d, f, C, eta: the last chunk is the remainder T - (n-1) C
+    (1, 640, 200, 584, 256, 0.05),   # chunks 256, 256, 128
+    (2, 448, 136, 264, 192, 0.1),    # 192, 192, 64 (row tiles straddle chunks)
+    (1, 192, 64, 256, 128, 0.2),     # 128, 64
+    (2, 128, 72, 136, 256, 0.3),     # one partial chunk shorter than C
+]
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", PARTIAL)
+def test_partial_last_chunk(cuda_device, B, T, d, f, C, eta):
+    inp = make_inputs(B, T, d, f, seed=700 + T + d)
+    ref = oracle.forward(inp, eta, C, want_z=True, want_vhat=True, want_states=True)
+    got = run(to_device(inp, cuda_device), eta, C, intermediates=True, want_state=True)
+    n = -(-T // C)
+    assert_parity(host(got["vhat_buf"]), eta * ref["Vhat"], "eta * Vhat")
+    assert_parity(host(got["snap_buf"]), ref["states"][:, :n], "snapshots")
+    assert_parity(host(got["state_out"]), ref["states"][:, n], "state after the partial chunk")
+    assert_parity(host(got["O"]), ref["O"], "O")
+
+
+@pytest.mark.parametrize("fused_conv,dual", [(False, False), (True, False), (False, True)])
+def test_per_token_rates(cuda_device, fused_conv, dual):
+    B, T, d, f, C, eta = 2, 512, 200, 384, 128, 0.1
+    inp = make_inputs(B, T, d, f, seed=801)
+    rates = torch.rand(B, T, generator=torch.Generator().manual_seed(4)) + 0.25
+    rates[0, 130:200] = 0.0
+    ref = oracle.forward(inp, eta, C, want_vhat=True, want_states=True, eta_tok=rates)
+    got = run(to_device(inp, cuda_device), eta, C, intermediates=True, fused_conv=fused_conv,
+              dual=dual, eta_tok=rates.to(cuda_device))
+    scaled = eta * rates.double().numpy()[:, :, None] * ref["Vhat"]
+    assert_parity(host(got["vhat_buf"]), scaled, "eta * eta_tok * Vhat")
+    if not dual:
+        assert_parity(host(got["snap_buf"]), ref["states"][:, :T // C], "snapshots")
+    assert_parity(host(got["O"]), ref["O"], "O")
+
+
+# --------------------------------------------------------------------------
 # The dual schedule (scores Z Z^T instead of the fast-weight walk)
 # --------------------------------------------------------------------------
 
@@ -260,8 +301,12 @@ def test_status_and_argument_errors_on_device(cuda_device):
     g = to_device(make_inputs(1, 256, 64, 256, seed=14), cuda_device)
     with pytest.raises(ittt.IttError) as e:
         ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
-                     g["conv_w"], 0.1, 100)
+                     g["conv_w"], 0.1, 0)
     assert e.value.status == ittt.ERR_INVALID_ARG
+    with pytest.raises(ittt.IttError) as e:
+        ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                     g["conv_w"], 0.1, 100)
+    assert e.value.status == ittt.ERR_UNSUPPORTED
     ittt.stream_status()  # nothing recorded
 
 
