@@ -83,6 +83,8 @@ def parse_args():
                     help="compute the convolution inside the target GEMM")
     ap.add_argument("--dual", action="store_true",
                     help="dual form (scores Z Z^T) instead of the fast-weight walk")
+    ap.add_argument("--eta-tok", action="store_true",
+                    help="per-token learning-rate weights (seeded uniform [0.5, 1.5))")
     return ap.parse_args()
 
 
@@ -137,13 +139,13 @@ def phase_model(B, T, d, f, C, dual=False):
     """Algorithmic work per phase: ('tensor', FLOPs) or ('hbm', bytes).  The
     dual form's extra work (scores Z Z^T, S Vhat) is charged at the primal
     form's FLOPs, the work the layer needs."""
-    n = T // C
+    n = -(-T // C)
     return {
         "conv": ("hbm", 2.0 * B * T * d * 2 + d * 3 * 4),
         "target": ("tensor", 2.0 * B * T * d * d),
         "gateup": ("tensor", 4.0 * B * T * d * f),
         "snapshot0": ("hbm", 1.0 * d * f * 2 + B * d * f * 2),
-        "update": ("tensor", 2.0 * B * (T - C) * d * f),
+        "update": ("tensor", 2.0 * B * (T - (T - (n - 1) * C)) * d * f),
         "apply": ("tensor", 2.0 * B * T * d * f),
         "_n": n,
     }
@@ -257,10 +259,14 @@ def main():
     cw = inp["conv_w"].to(dev, torch.float32)
     out = torch.empty(B, T, d, dtype=bf, device=dev)
     stream = torch.cuda.current_stream(dev)
+    rates = None
+    if args.eta_tok:
+        g_rates = torch.Generator().manual_seed(4321 + first)
+        rates = (torch.rand(B, T, generator=g_rates) + 0.5).to(dev)
 
     def step(events=None):
         ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, stream=stream, events=events,
-                     fused_conv=args.fused_conv, dual=args.dual)
+                     fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -355,7 +361,7 @@ def main():
                 if k >= 2:
                     stream.wait_event(downloaded[j])  # O_j read back before reuse
                 ittt.forward(Hs[j], X0s[j], Wg, Wu, W0, Wt, cw, eta, C, Os[j], stream=stream,
-                             fused_conv=args.fused_conv, dual=args.dual)
+                             fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates)
                 computed[j].record(stream)
                 down.wait_event(computed[j])
                 with torch.cuda.stream(down):
@@ -392,6 +398,7 @@ def main():
                        "eta": eta, "chunks": T // C, "parallelism": f"batch x{world} (replicas)",
                        "conv": "fused into target GEMM" if args.fused_conv else "own kernel",
                        "schedule": "dual (scores Z Z^T)" if args.dual else "primal walk",
+                       "eta_tok": "per-token rates" if args.eta_tok else None,
                        "l2": "inputs larger than L2: H+X0 and Z are several GB per step"},
             "layer_tflops": round(layer_tflops, 1),
             "layer_frac_of_peak": {

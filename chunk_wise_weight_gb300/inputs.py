@@ -77,6 +77,8 @@ def config_inputs(index: int, round_bf16: bool = True) -> tuple[dict, dict]:
 def counted_flops(B: int, T: int, d: int, f: int, C: int) -> float:
     """Tensor-core FLOPs a call must do: gate/up (4df per token), target
     (2d^2), apply (2df) and the update of every chunk but the last (2df per
-    token of chunks 0..n-2).  Convolution and elementwise work are not
-    counted."""
-    return float(B) * (T * (4 * d * f + 2 * d * d + 2 * d * f) + (T - C) * 2 * d * f)
+    token of chunks 0..n-2; the last chunk may be the partial remainder).
+    Convolution and elementwise work are not counted."""
+    n = -(-T // C)
+    last = T - (n - 1) * C
+    return float(B) * (T * (4 * d * f + 2 * d * d + 2 * d * f) + (T - last) * 2 * d * f)

@@ -38,6 +38,7 @@ def max_ratio(got, ref):
 
 def assert_parity(got, ref, what):
     rf, mr = rel_fro(got, ref), max_ratio(got, ref)
+    print(f"parity {what}: rel_fro={rf:.3e} max_ratio={mr:.3e}")
     assert rf <= REL_FRO and mr <= MAX_RATIO, f"{what}: rel_fro={rf:.3e} max_ratio={mr:.3e}"
 
 
