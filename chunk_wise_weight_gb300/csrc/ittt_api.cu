@@ -17,8 +17,11 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <string>
+#include <utility>
+#include <vector>
 
 #include "ittt.h"
 #include "kernels.h"
@@ -54,11 +57,24 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Pinned host buffers that packed-document tables are uploaded from.  A
+// buffer is rewritten only after the copy that last read it has finished,
+// so several calls can be in flight on the device.
+constexpr int kStagingSlots = 4;
+struct StagingSlot {
+  void* host = nullptr;
+  size_t bytes = 0;
+  cudaEvent_t done = nullptr;
+  bool pending = false;
+};
+
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   unsigned int* status = nullptr;
   cudaMemPool_t pool = nullptr;
+  StagingSlot staging[kStagingSlots];
+  int next_slot = 0;
 };
 
 std::mutex g_mutex;
@@ -111,6 +127,41 @@ ittt_status device_state(DeviceState** out) {
   return ITTT_OK;
 }
 
+// Copies `bytes` of host data to device `dst` in stream order through the
+// device's pinned staging ring.
+ittt_status upload(DeviceState* ds, void* dst, const void* src, size_t bytes,
+                   cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  StagingSlot& sl = ds->staging[ds->next_slot];
+  ds->next_slot = (ds->next_slot + 1) % kStagingSlots;
+  cudaError_t e = cudaSuccess;
+  if (sl.pending) {
+    e = cudaEventSynchronize(sl.done);
+    if (e != cudaSuccess) return cuda_fail(e, "waiting for a staging buffer");
+    sl.pending = false;
+  }
+  if (sl.done == nullptr) {
+    e = cudaEventCreateWithFlags(&sl.done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+  }
+  if (sl.bytes < bytes) {
+    if (sl.host) cudaFreeHost(sl.host);
+    sl.host = nullptr;
+    sl.bytes = 0;
+    const size_t want = std::max(bytes, size_t(64) << 10);
+    e = cudaHostAlloc(&sl.host, want, cudaHostAllocDefault);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc (staging)");
+    sl.bytes = want;
+  }
+  memcpy(sl.host, src, bytes);
+  e = cudaMemcpyAsync(dst, sl.host, bytes, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "document table upload");
+  e = cudaEventRecord(sl.done, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord (staging)");
+  sl.pending = true;
+  return ITTT_OK;
+}
+
 // ---------------------------------------------------------------- validation
 size_t dtype_size(int32_t dt) { return dt == ITTT_FP32 ? 4 : 2; }
 
@@ -155,48 +206,154 @@ ittt_status check_sizes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chun
     return fail(ITTT_ERR_INVALID_ARG, "sizes must be positive (B=%lld T=%lld d=%lld f=%lld)",
                 (long long)B, (long long)T, (long long)d, (long long)f);
   if (chunk <= 0) return fail(ITTT_ERR_INVALID_ARG, "chunk %lld must be positive", (long long)chunk);
-  if (chunk % 64 != 0 || T % 64 != 0)
-    return fail(ITTT_ERR_UNSUPPORTED, "chunk %lld and T %lld must be multiples of 64",
-                (long long)chunk, (long long)T);
   if (d % 8 != 0 || f % 8 != 0)
     return fail(ITTT_ERR_UNSUPPORTED, "d_model=%lld and d_ff=%lld must be multiples of 8",
                 (long long)d, (long long)f);
-  const int64_t n = (T + chunk - 1) / chunk;
-  if (B * T >= (int64_t(1) << 31) || B * n * d >= (int64_t(1) << 31) || d * f >= (int64_t(1) << 40))
+  if (B * T >= (int64_t(1) << 31) || d * f >= (int64_t(1) << 40))
     return fail(ITTT_ERR_UNSUPPORTED, "sizes exceed 32-bit tile coordinates");
   return ITTT_OK;
 }
 
-// --------------------------------------------------------------- workspace
+// --------------------------------------------------------------- planning
 struct Layout {
-  size_t z = 0, vhat = 0, xc = 0, snap = 0, scores = 0, w0b = 0, total = 0;
+  size_t z = 0, vhat = 0, xc = 0, snap = 0, scores = 0, w0b = 0, table = 0, total = 0;
 };
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
 
-Layout plan_workspace(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk, bool need_z,
-                      bool need_vhat, bool need_xc, bool need_snap) {
+// Everything a call needs to know before it touches the device: documents,
+// snapshot slots, the packed-document table and the scratch layout.
+struct Plan {
+  int64_t B = 0, T = 0, d = 0, f = 0, C = 0, M = 0;
+  bool fused = false, dual = false, packed = false;
+  int64_t ndocs = 0;   // documents: B, or the packed count
+  int64_t nslots = 0;  // snapshot slots = chunks over all documents
+  int64_t n = 0;       // chunks per sequence (regular)
+  bool final_update = false;
+  int n_udocs = 0;     // documents that run at least one update
+  // Packed: starts[ndocs+1] | chunk_base[ndocs+1] | chunk_doc[nslots] |
+  // upd_docs[n_udocs], uploaded into the scratch at L.table.
+  std::vector<int> table;
   Layout L;
-  const int64_t n = (T + chunk - 1) / chunk;
+};
+
+// w0_bf16: W_down0 is one bf16 matrix (the dual form then needs no bf16
+// copy of it; pass false when unknown, which plans the larger scratch).
+ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
+                      const ittt_opts& o, bool w0_bf16, Plan* P) {
+  ittt_status s = check_sizes(B, T, d, f, chunk);
+  if (s != ITTT_OK) return s;
+  if (o.pad_mode != ITTT_PAD_CHUNK && o.pad_mode != ITTT_PAD_SEQUENCE)
+    return fail(ITTT_ERR_INVALID_ARG, "pad_mode %d", int(o.pad_mode));
+  if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV | ITTT_FLAG_DUAL))
+    return fail(ITTT_ERR_INVALID_ARG, "unknown flags 0x%x", unsigned(o.flags));
+  P->B = B;
+  P->T = T;
+  P->d = d;
+  P->f = f;
+  P->C = chunk;
+  P->M = B * T;
+  P->fused = (o.flags & ITTT_FLAG_FUSED_CONV) != 0;
+  P->dual = (o.flags & ITTT_FLAG_DUAL) != 0;
+  P->packed = o.cu_seqlens != nullptr;
+  P->final_update = o.state_out != nullptr;
+  if (P->dual && (o.state_out || o.snap_buf))
+    return fail(ITTT_ERR_UNSUPPORTED,
+                "the dual form forms no fast-weight state: no state_out or snap_buf");
+  if (!P->packed && o.num_docs != 0)
+    return fail(ITTT_ERR_INVALID_ARG, "num_docs is set but cu_seqlens is NULL");
+  if (P->packed) {
+    if (P->fused || P->dual)
+      return fail(ITTT_ERR_UNSUPPORTED,
+                  "packed documents run with the split convolution and the primal form only");
+    if (B != 1)
+      return fail(ITTT_ERR_INVALID_ARG, "packed documents need B = 1 (got %lld)", (long long)B);
+    const int64_t nd = o.num_docs;
+    const int64_t* cu = o.cu_seqlens;
+    if (nd < 1) return fail(ITTT_ERR_INVALID_ARG, "num_docs %lld must be >= 1", (long long)nd);
+    if (nd >= (int64_t(1) << 30))
+      return fail(ITTT_ERR_UNSUPPORTED, "num_docs %lld is too large", (long long)nd);
+    if (cu[0] != 0) return fail(ITTT_ERR_INVALID_ARG, "cu_seqlens[0] must be 0");
+    if (cu[nd] != T)
+      return fail(ITTT_ERR_INVALID_ARG, "cu_seqlens[num_docs] = %lld, expected T = %lld",
+                  (long long)cu[nd], (long long)T);
+    int64_t slots = 0;
+    for (int64_t k = 0; k < nd; ++k) {
+      if (cu[k + 1] <= cu[k])
+        return fail(ITTT_ERR_INVALID_ARG,
+                    "cu_seqlens must increase strictly (document %lld is empty or negative)",
+                    (long long)k);
+      slots += (cu[k + 1] - cu[k] + chunk - 1) / chunk;
+    }
+    P->ndocs = nd;
+    P->nslots = slots;
+    // Documents that update, most updates first (the update kernel walks
+    // them in this order, so the longest walks start first).
+    std::vector<std::pair<int64_t, int>> upd;
+    for (int64_t k = 0; k < nd; ++k) {
+      const int64_t nk = (cu[k + 1] - cu[k] + chunk - 1) / chunk;
+      const int64_t nu = P->final_update ? nk : nk - 1;
+      if (nu > 0) upd.push_back({-nu, int(k)});
+    }
+    std::stable_sort(upd.begin(), upd.end(),
+                     [](const std::pair<int64_t, int>& a, const std::pair<int64_t, int>& b) {
+                       return a.first < b.first;
+                     });
+    P->n_udocs = int(upd.size());
+    std::vector<int>& t = P->table;
+    t.resize(size_t(2 * (nd + 1) + slots + P->n_udocs));
+    int* starts = t.data();
+    int* base = starts + (nd + 1);
+    int* cdoc = base + (nd + 1);
+    int* ud = cdoc + slots;
+    int64_t g = 0;
+    for (int64_t k = 0; k <= nd; ++k) {
+      starts[k] = int(cu[k]);
+      base[k] = int(g);
+      if (k < nd) {
+        const int64_t nk = (cu[k + 1] - cu[k] + chunk - 1) / chunk;
+        for (int64_t j = 0; j < nk; ++j) cdoc[g++] = int(k);
+      }
+    }
+    for (int q = 0; q < P->n_udocs; ++q) ud[q] = upd[size_t(q)].second;
+  } else {
+    P->ndocs = B;
+    P->n = (T + chunk - 1) / chunk;  // the last chunk may be partial
+    P->nslots = B * P->n;
+    P->n_udocs = (P->final_update || P->n > 1) ? int(B) : 0;
+  }
+  // The fused convolution forms its A tile from 4-row groups inside one
+  // chunk; the dual form's scores are blocked by 64-token chunks.
+  if (P->fused && (chunk % 64 != 0 || T % 64 != 0))
+    return fail(ITTT_ERR_UNSUPPORTED, "the fused convolution needs chunk and T multiples of 64");
+  if (P->dual && (chunk % 64 != 0 || T % chunk != 0))
+    return fail(ITTT_ERR_UNSUPPORTED,
+                "the dual form needs chunk a multiple of 64 that divides T");
+  const int64_t apply_units = P->nslots * ((chunk + 127) / 128) * ((d + 255) / 256);
+  if (P->nslots * d >= (int64_t(1) << 31) || apply_units >= (int64_t(1) << 31))
+    return fail(ITTT_ERR_UNSUPPORTED, "too many chunks for 32-bit tile coordinates");
+
+  // Scratch.  The dual form needs the scores and, unless W_0 is one bf16
+  // matrix already, a bf16 copy of each sequence's W_0 instead of the
+  // snapshots.
+  Layout& L = P->L;
   size_t off = 0;
-  if (need_z) {
-    L.z = off;
-    off += round_up(size_t(B) * T * f * 2);
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += round_up(bytes);
+    return at;
+  };
+  if (o.z_buf == nullptr) L.z = take(size_t(P->M) * f * 2);
+  if (o.vhat_buf == nullptr) L.vhat = take(size_t(P->M) * d * 2);
+  if (!P->fused) L.xc = take(size_t(P->M) * d * 2);
+  if (!P->dual && o.snap_buf == nullptr) L.snap = take(size_t(P->nslots) * d * f * 2);
+  if (P->dual) {
+    L.scores = take(size_t(B) * T * T * 2);
+    if (o.state_in || !w0_bf16) L.w0b = take(size_t(o.state_in ? B : 1) * d * f * 2);
   }
-  if (need_vhat) {
-    L.vhat = off;
-    off += round_up(size_t(B) * T * d * 2);
-  }
-  if (need_xc) {
-    L.xc = off;
-    off += round_up(size_t(B) * T * d * 2);
-  }
-  if (need_snap) {
-    L.snap = off;
-    off += round_up(size_t(B) * n * d * f * 2);
-  }
+  if (P->packed) L.table = take(P->table.size() * sizeof(int));
   L.total = off;
-  return L;
+  return ITTT_OK;
 }
 
 // ------------------------------------------------------------- tensor maps
@@ -248,47 +405,39 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   ittt_opts o;
   memset(&o, 0, sizeof(o));
   if (opts) o = *opts;
-  if (o.pad_mode != ITTT_PAD_CHUNK && o.pad_mode != ITTT_PAD_SEQUENCE)
-    return fail(ITTT_ERR_INVALID_ARG, "pad_mode %d", int(o.pad_mode));
-  if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV | ITTT_FLAG_DUAL))
-    return fail(ITTT_ERR_INVALID_ARG, "unknown flags 0x%x", unsigned(o.flags));
-  const bool fused = (o.flags & ITTT_FLAG_FUSED_CONV) != 0;
-  const bool dual = (o.flags & ITTT_FLAG_DUAL) != 0;
-  if (dual && (o.state_out || o.snap_buf))
-    return fail(ITTT_ERR_UNSUPPORTED,
-                "the dual form forms no fast-weight state: no state_out or snap_buf");
   if (H == nullptr || H->ndim != 3)
     return fail(ITTT_ERR_INVALID_ARG, "H: expected a [B,T,d] descriptor");
   const int64_t B = H->shape[0], T = H->shape[1], d = H->shape[2];
   if (W_gate == nullptr || W_gate->ndim != 2)
     return fail(ITTT_ERR_INVALID_ARG, "W_gate: expected a [f,d] descriptor");
   const int64_t f = W_gate->shape[0];
-  ittt_status s = check_sizes(B, T, d, f, chunk);
-  if (s != ITTT_OK) return s;
   if (!std::isfinite(eta)) return fail(ITTT_ERR_INVALID_ARG, "eta is not finite");
-  const int64_t n = (T + chunk - 1) / chunk;  // the last chunk may be partial
-  if (dual && T % chunk != 0)
-    return fail(ITTT_ERR_UNSUPPORTED, "the dual form needs chunk to divide T");
+  const bool w0_bf16 = W_down0 != nullptr && W_down0->dtype == ITTT_BF16;
+  Plan P;
+  ittt_status s = make_plan(B, T, d, f, chunk, o, w0_bf16, &P);
+  if (s != ITTT_OK) return s;
+  const bool fused = P.fused, dual = P.dual;
+  const int64_t S = P.ndocs;  // per-document state count
 
   const int64_t sh_btd[3] = {B, T, d}, sh_fd[2] = {f, d}, sh_df[2] = {d, f}, sh_dd[2] = {d, d},
-                sh_d3[2] = {d, 3}, sh_bdf[3] = {B, d, f}, sh_btf[3] = {B, T, f},
-                sh_bndf[4] = {B, n, d, f};
+                sh_d3[2] = {d, 3}, sh_sdf[3] = {S, d, f}, sh_btf[3] = {B, T, f},
+                sh_snap[4] = {B, P.nslots / B, d, f};
   if ((s = check_tensor(H, "H", 3, sh_btd, true, false))) return s;
   if ((s = check_tensor(X0, "X0", 3, sh_btd, true, false))) return s;
   if ((s = check_tensor(W_gate, "W_gate", 2, sh_fd, true, false))) return s;
   if ((s = check_tensor(W_up, "W_up", 2, sh_fd, true, false))) return s;
   if (o.state_in) {
-    if ((s = check_tensor(o.state_in, "state_in", 3, sh_bdf, false, true))) return s;
+    if ((s = check_tensor(o.state_in, "state_in", 3, sh_sdf, false, true))) return s;
   } else if ((s = check_tensor(W_down0, "W_down0", 2, sh_df, true, true))) {
     return s;
   }
   if ((s = check_tensor(W_target, "W_target", 2, sh_dd, true, false))) return s;
   if ((s = check_tensor(conv_w, "conv_w", 2, sh_d3, false, true))) return s;
   if ((s = check_tensor(out, "out", 3, sh_btd, true, true))) return s;
-  if (o.state_out && (s = check_tensor(o.state_out, "state_out", 3, sh_bdf, false, true))) return s;
+  if (o.state_out && (s = check_tensor(o.state_out, "state_out", 3, sh_sdf, false, true))) return s;
   if (o.z_buf && (s = check_tensor(o.z_buf, "z_buf", 3, sh_btf, true, false))) return s;
   if (o.vhat_buf && (s = check_tensor(o.vhat_buf, "vhat_buf", 3, sh_btd, true, false))) return s;
-  if (o.snap_buf && (s = check_tensor(o.snap_buf, "snap_buf", 4, sh_bndf, true, false))) return s;
+  if (o.snap_buf && (s = check_tensor(o.snap_buf, "snap_buf", 4, sh_snap, true, false))) return s;
   const int64_t sh_bt[2] = {B, T};
   if (o.eta_tok && (s = check_tensor(o.eta_tok, "eta_tok", 2, sh_bt, false, true))) return s;
 
@@ -307,20 +456,8 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   DeviceState* ds = nullptr;
   if ((s = device_state(&ds))) return s;
 
-  // Scratch.
-  // The dual form needs the scores and, unless W_0 is one bf16 matrix
-  // already, a bf16 copy of each sequence's W_0 instead of the snapshots.
-  const bool w0_is_bf16 = !o.state_in && W_down0->dtype == ITTT_BF16;
-  Layout L = plan_workspace(B, T, d, f, chunk, o.z_buf == nullptr, o.vhat_buf == nullptr, !fused,
-                            !dual && o.snap_buf == nullptr);
-  if (dual) {
-    L.scores = L.total;
-    L.total += round_up(size_t(B) * T * T * 2);
-    if (!w0_is_bf16) {
-      L.w0b = L.total;
-      L.total += round_up(size_t(o.state_in ? B : 1) * d * f * 2);
-    }
-  }
+  const Layout& L = P.L;
+  const bool w0_is_bf16 = !o.state_in && w0_bf16;
   ScratchGuard guard;
   uint8_t* ws = nullptr;
   if (o.workspace) {
@@ -330,7 +467,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     if (reinterpret_cast<uintptr_t>(o.workspace) % 256 != 0)
       return fail(ITTT_ERR_INVALID_ARG, "workspace not 256-byte aligned");
     ws = static_cast<uint8_t*>(o.workspace);
-  } else {
+  } else if (L.total > 0) {
     void* p = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&p, L.total, ds->pool, stream);
     if (e != cudaSuccess) return cuda_fail(e, "scratch allocation");
@@ -346,8 +483,26 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   auto* snap = o.snap_buf ? static_cast<__nv_bfloat16*>(o.snap_buf->data)
                           : reinterpret_cast<__nv_bfloat16*>(ws + L.snap);
 
+  // Documents.
+  ittt::DocMap docs;
+  memset(&docs, 0, sizeof(docs));
+  docs.ndocs = int(P.ndocs);
+  docs.nchunks = int(P.nslots);
+  docs.T = int(T);
+  docs.n = int(P.n);
+  docs.C = int(chunk);
+  const int* upd_docs = nullptr;
+  if (P.packed) {
+    int* tab = reinterpret_cast<int*>(ws + L.table);
+    if ((s = upload(ds, tab, P.table.data(), P.table.size() * sizeof(int), stream))) return s;
+    docs.starts = tab;
+    docs.chunk_base = tab + (P.ndocs + 1);
+    docs.chunk_doc = tab + 2 * (P.ndocs + 1);
+    upd_docs = docs.chunk_doc + P.nslots;
+  }
+
   // Tensor maps.
-  const uint64_t M = uint64_t(B * T);
+  const uint64_t M = uint64_t(P.M);
   CUtensorMap tm_h, tm_wg, tm_wu, tm_a, tm_wt, tm_vmn, tm_zmn, tm_zk, tm_snap;
   if ((s = make_map(&tm_h, H->data, d, M, 64, 128, "H"))) return s;
   if ((s = make_map(&tm_wg, W_gate->data, d, f, 64, 128, "W_gate"))) return s;
@@ -363,8 +518,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   memset(&tm_ss, 0, sizeof(tm_ss));
   memset(&tm_os, 0, sizeof(tm_os));
   if ((s = make_map(&tm_vs, vhat, d, M, 64, 128, "Vhat (store)"))) return s;
-  if (out->dtype == ITTT_BF16 &&
-      (s = make_map_3d(&tm_os, out->data, d, T, uint64_t(B), 64, 64, "O (store)")))
+  if (out->dtype == ITTT_BF16 && (s = make_map(&tm_os, out->data, d, M, 64, 64, "O (store)")))
     return s;
   if ((s = make_map(&tm_vmn, vhat, d, M, 64, 64, "Vhat"))) return s;
   if ((s = make_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
@@ -378,8 +532,8 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
       return s;
     if ((s = make_map(&tm_sc, scores, uint64_t(T), M, 64, 128, "scores"))) return s;
   } else {
-    if ((s = make_map(&tm_snap, snap, f, uint64_t(B * n * d), 64, 256, "snapshots"))) return s;
-    if ((s = make_map_3d(&tm_ss, snap, f, d, uint64_t(B * n), 64, 128, "snapshots (store)")))
+    if ((s = make_map(&tm_snap, snap, f, uint64_t(P.nslots * d), 64, 256, "snapshots"))) return s;
+    if ((s = make_map_3d(&tm_ss, snap, f, d, uint64_t(P.nslots), 64, 128, "snapshots (store)")))
       return s;
   }
 
@@ -401,7 +555,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   ITTT_STEP(rec(2 * ITTT_PHASE_CONV, stream), "event record");
   if (!fused) {
     ITTT_STEP(ittt::launch_conv(env, static_cast<const __nv_bfloat16*>(X0->data), cw, xc,
-                                int64_t(M), int(T), int(d), int(chunk), int(o.pad_mode)),
+                                int64_t(M), docs, int(d), int(o.pad_mode)),
               "conv launch");
   }
   ITTT_STEP(rec(2 * ITTT_PHASE_CONV + 1, stream), "event record");
@@ -418,37 +572,40 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_SNAPSHOT0, stream), "event record");
   if (!dual) {
-    ITTT_STEP(ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride, snap, int(B), int(n), int(d),
-                                     int(f)),
+    ITTT_STEP(ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride, snap, docs, int(d), int(f)),
               "snapshot launch");
   } else if (!w0_is_bf16) {
+    ittt::DocMap w0docs;
+    memset(&w0docs, 0, sizeof(w0docs));
+    w0docs.ndocs = int(o.state_in ? B : 1);
+    w0docs.nchunks = w0docs.ndocs;
+    w0docs.T = 1;
+    w0docs.n = 1;
+    w0docs.C = 1;
     ITTT_STEP(ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride,
-                                     static_cast<__nv_bfloat16*>(const_cast<void*>(w0b)),
-                                     int(o.state_in ? B : 1), 1, int(d), int(f)),
+                                     static_cast<__nv_bfloat16*>(const_cast<void*>(w0b)), w0docs,
+                                     int(d), int(f)),
               "W_0 copy launch");
   }
   ITTT_STEP(rec(2 * ITTT_PHASE_SNAPSHOT0 + 1, stream), "event record");
   if (!dual) {
     ittt::UpdateArgs ua;
-    ua.B = int(B);
-    ua.T = int(T);
+    ua.docs = docs;
+    ua.upd_docs = upd_docs;
+    ua.n_udocs = P.n_udocs;
+    ua.final_update = P.final_update;
     ua.d = int(d);
     ua.f = int(f);
-    ua.C = int(chunk);
-    ua.n = int(n);
-    ua.n_upd = o.state_out ? int(n) : int(n - 1);
     ua.w0 = w0;
     ua.w0_fp32 = w0_fp32;
     ua.w0_bstride = w0_bstride;
-    ua.snap = snap;
     ua.state_out = o.state_out ? static_cast<float*>(o.state_out->data) : nullptr;
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");
     ITTT_STEP(ittt::launch_update(env, tm_vmn, tm_zmn, tm_ss, ua), "update launch");
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
     ITTT_STEP(ittt::launch_apply(env, tm_zk, tm_snap, tm_os, out->data,
-                                 out->dtype == ITTT_FP32, int(B), int(T), int(d), int(f),
-                                 int(chunk)),
+                                 out->dtype == ITTT_FP32, docs, int(d), int(f)),
               "apply launch");
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY + 1, stream), "event record");
   } else {
@@ -506,12 +663,21 @@ ittt_status ittt_forward_ex(const ittt_tensor* H, const ittt_tensor* X0,
 }
 
 size_t ittt_workspace_bytes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk) {
+  return ittt_workspace_bytes_ex(B, T, d, f, chunk, nullptr);
+}
+
+size_t ittt_workspace_bytes_ex(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
+                               const ittt_opts* opts) {
   const std::string saved = g_last_error;
-  if (check_sizes(B, T, d, f, chunk) != ITTT_OK) {
+  ittt_opts o;
+  memset(&o, 0, sizeof(o));
+  if (opts) o = *opts;
+  Plan P;
+  if (make_plan(B, T, d, f, chunk, o, false, &P) != ITTT_OK) {
     g_last_error = saved;
     return 0;
   }
-  return plan_workspace(B, T, d, f, chunk, true, true, true, true).total;
+  return P.L.total;
 }
 
 ittt_status ittt_stream_status(ittt_stream_t stream) {
@@ -547,7 +713,7 @@ int32_t ittt_launch_count(int64_t B, int64_t T, int64_t d, int64_t f, int64_t ch
     return 0;
   }
   // conv, target, gate/up, snapshot 0, update (when a chunk updates), apply
-  return (T / chunk > 1) ? 6 : 5;
+  return ((T + chunk - 1) / chunk > 1) ? 6 : 5;
 }
 
 }  // extern "C"

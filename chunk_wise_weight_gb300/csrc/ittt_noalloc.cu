@@ -191,9 +191,10 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   if (B <= 0 || T <= 0 || d <= 0 || f <= 0)
     return na_fail(ITTT_ERR_INVALID_ARG, "sizes must be positive");
   if (chunk <= 0) return na_fail(ITTT_ERR_INVALID_ARG, "chunk must be positive");
-  if (chunk % 64 != 0 || T % 64 != 0 || d % 8 != 0 || f % 8 != 0)
-    return na_fail(ITTT_ERR_UNSUPPORTED,
-                   "chunk and T must be multiples of 64, d_model and d_ff multiples of 8");
+  if (d % 8 != 0 || f % 8 != 0)
+    return na_fail(ITTT_ERR_UNSUPPORTED, "d_model and d_ff must be multiples of 8");
+  if (B * T >= (int64_t(1) << 31))
+    return na_fail(ITTT_ERR_UNSUPPORTED, "B*T exceeds 32-bit token coordinates");
   if (!std::isfinite(eta)) return na_fail(ITTT_ERR_INVALID_ARG, "eta is not finite");
   const int64_t n = (T + chunk - 1) / chunk;  // the last chunk may be partial
   const int64_t sh_btd[3] = {B, T, d}, sh_fd[2] = {f, d}, sh_df[2] = {d, f}, sh_dd[2] = {d, d},
@@ -247,17 +248,23 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   if ((s = na_map(&tm_vs, vhat, d, M, 64, 128, "Vhat (store)"))) return s;
   if ((s = na_map_3d(&tm_ss, snap, f, d, uint64_t(B * n), 64, 128, "snapshots (store)")))
     return s;
-  if (out->dtype == ITTT_BF16 &&
-      (s = na_map_3d(&tm_os, out->data, d, T, uint64_t(B), 64, 64, "O (store)")))
+  if (out->dtype == ITTT_BF16 && (s = na_map(&tm_os, out->data, d, M, 64, 64, "O (store)")))
     return s;
 
   const ittt::LaunchEnv env{stream, nd->num_sms, nd->status};
+  ittt::DocMap docs;
+  memset(&docs, 0, sizeof(docs));
+  docs.ndocs = int(B);
+  docs.nchunks = int(B * n);
+  docs.T = int(T);
+  docs.n = int(n);
+  docs.C = int(chunk);
   const bool w0_fp32 = W_down0->dtype == ITTT_FP32;
   cudaError_t e;
   const char* what = nullptr;
   if ((e = ittt::launch_conv(env, static_cast<const __nv_bfloat16*>(X0->data),
-                             static_cast<const float*>(conv_w->data), xc, int64_t(M), int(T),
-                             int(d), int(chunk), ITTT_PAD_CHUNK)) != cudaSuccess) {
+                             static_cast<const float*>(conv_w->data), xc, int64_t(M), docs,
+                             int(d), ITTT_PAD_CHUNK)) != cudaSuccess) {
     what = "conv";
   } else if ((e = ittt::launch_target(env, tm_xc, tm_wt, tm_vs,
                                       static_cast<const float*>(conv_w->data), nullptr, vhat, eta,
@@ -267,28 +274,26 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   } else if ((e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d))) !=
              cudaSuccess) {
     what = "gate/up";
-  } else if ((e = ittt::launch_snapshot0(env, W_down0->data, w0_fp32, 0, snap, int(B), int(n),
-                                         int(d), int(f))) != cudaSuccess) {
+  } else if ((e = ittt::launch_snapshot0(env, W_down0->data, w0_fp32, 0, snap, docs, int(d),
+                                         int(f))) != cudaSuccess) {
     what = "snapshot";
   } else {
     ittt::UpdateArgs ua;
-    ua.B = int(B);
-    ua.T = int(T);
+    ua.docs = docs;
+    ua.upd_docs = nullptr;
+    ua.n_udocs = n > 1 ? int(B) : 0;
+    ua.final_update = false;
     ua.d = int(d);
     ua.f = int(f);
-    ua.C = int(chunk);
-    ua.n = int(n);
-    ua.n_upd = int(n - 1);
     ua.w0 = W_down0->data;
     ua.w0_fp32 = w0_fp32;
     ua.w0_bstride = 0;
-    ua.snap = snap;
     ua.state_out = nullptr;
     if ((e = ittt::launch_update(env, tm_vmn, tm_zmn, tm_ss, ua)) != cudaSuccess) {
       what = "update";
     } else if ((e = ittt::launch_apply(env, tm_zk, tm_snap, tm_os, out->data,
-                                       out->dtype == ITTT_FP32, int(B), int(T), int(d), int(f),
-                                       int(chunk))) != cudaSuccess) {
+                                       out->dtype == ITTT_FP32, docs, int(d), int(f))) !=
+               cudaSuccess) {
       what = "apply";
     }
   }

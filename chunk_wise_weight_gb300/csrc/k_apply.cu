@@ -1,13 +1,15 @@
-// k_apply.cu -- apply step for every chunk of every sequence in one launch:
+// k_apply.cu -- apply step for every chunk of every document in one launch:
 //   O_[i] = Z_[i] W_i^T
 // ("[논문리뷰] In-Place Test-Time Training", Method §1 eq. (3); all chunks in
 // parallel as in Method §3 stage 3).
 //
-// W_i is the bf16 snapshot the update kernel wrote (slot 0 holds W_0).  A
-// work unit is (sequence b, chunk i, 128-row tile of the chunk, 256-column
-// tile of d_model); rows past the chunk's end belong to another chunk and are
-// computed but not stored, so any chunk size that is a multiple of 64 works,
-// and the last chunk may be the shorter remainder of the sequence.
+// W_i is the bf16 snapshot the update kernel wrote into the chunk's slot
+// (a document's first slot holds W_0).  A work unit is (snapshot slot g,
+// 128-row tile of the chunk, 256-column tile of d_model).  Rows past the
+// chunk's end belong to another chunk: they are computed but not stored.
+// Full tiles and 64-row halves leave through TMA stores; a tile that ends
+// elsewhere (a chunk or document length that is not a multiple of 64) is
+// written row by row with masked 16-byte stores.
 #include "kernels.h"
 #include "pipeline.cuh"
 
@@ -15,12 +17,13 @@ namespace ittt {
 namespace {
 
 struct ApplyParams {
-  CUtensorMap tm_z;     // Z          [B*T, f]    box {64, 128}
-  CUtensorMap tm_snap;  // snapshots  [B*n*d, f]  box {64, 256}
-  CUtensorMap tm_os;    // bf16 O as [B][T rows][d cols], box {64, 64, 1} (store)
-  void* out;            // O [B*T, d], bf16 or fp32
+  CUtensorMap tm_z;     // Z          [M, f]        box {64, 128}
+  CUtensorMap tm_snap;  // snapshots  [slots*d, f]  box {64, 256}
+  CUtensorMap tm_os;    // bf16 O     [M, d]        box {64, 64} (store)
+  void* out;            // O [M, d], bf16 or fp32
   int out_fp32;
-  int B, T, d, f, C, n;
+  DocMap docs;
+  int d, f;
   int mt_per_chunk, nt, kblocks;
 };
 
@@ -30,26 +33,25 @@ struct ApplySched : SchedDefaults {
   static constexpr bool kStagedStores = true;
 
   const Params& p;
-  int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0, seq = 0, srow0 = 0;
+  int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0;
 
   __device__ explicit ApplySched(const Params& pp) : p(pp) {}
-  __device__ int num_units() const { return p.B * p.n * p.mt_per_chunk * p.nt; }
+  __device__ int num_units() const { return p.docs.nchunks * p.mt_per_chunk * p.nt; }
   __device__ void begin_unit(int u, int local) {
     const int nt = u % p.nt;
-    int r = u / p.nt;
+    const int r = u / p.nt;
     const int mt = r % p.mt_per_chunk;
-    r /= p.mt_per_chunk;
-    const int i = r % p.n;
-    const int b = r / p.n;
-    arow0 = b * p.T + i * p.C + mt * kBM;
-    brow0 = (b * p.n + i) * p.d + nt * kBN;
-    rows_valid = min(kBM, min(p.C, p.T - i * p.C) - mt * kBM);
+    const int g = r / p.mt_per_chunk;
+    const int k = p.docs.doc_of_chunk(g);
+    const int i = g - p.docs.first_chunk(k);
+    const int len = p.docs.len(k);
+    arow0 = p.docs.start(k) + i * p.docs.C + mt * kBM;
+    brow0 = g * p.d + nt * kBN;
+    rows_valid = min(kBM, min(p.docs.C, len - i * p.docs.C) - mt * kBM);
     n0 = nt * kBN;
-    seq = b;
-    srow0 = i * p.C + mt * kBM;
     acc = local & 1;
   }
-  // Row tiles past the end of a partial last chunk have nothing to do.
+  // Row tiles past the end of a short chunk have nothing to do.
   __device__ int num_segments() const { return rows_valid > 0 ? 1 : 0; }
   __device__ int seg_acc(int) const { return acc; }
   __device__ int seg_kblocks(int) const { return p.kblocks; }
@@ -67,12 +69,11 @@ struct ApplySched : SchedDefaults {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
   }
 
-  // bf16 O: 64-column TMA stores of 64-row halves through a [B][T][d] map:
-  // the second half is stored only when the chunk reaches it (chunk lengths
-  // are multiples of 64), rows >= T and columns >= d are clipped.  fp32 O:
-  // direct 16-byte stores.
+  // bf16 O in whole 64-row halves: 64-column TMA stores (columns >= d are
+  // clipped).  Otherwise (fp32 O, or a tile that ends inside a 64-row half):
+  // direct 16-byte stores of the valid rows.
   __device__ void epilogue(int, int row, uint32_t trow, EpiStager& st) const {
-    if (!p.out_fp32) {
+    if (!p.out_fp32 && (rows_valid == kBM || rows_valid == 64)) {
 #pragma unroll 1
       for (int g = 0; g < kBN / 64; ++g) {
         uint8_t* buf = st.acquire();
@@ -92,8 +93,8 @@ struct ApplySched : SchedDefaults {
                        pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]))));
         }
         st.commit(buf, [&](uint8_t* src) {
-          tma_store_3d(&p.tm_os, src, n0 + g * 64, srow0, seq);
-          if (rows_valid > 64) tma_store_3d(&p.tm_os, src + 64 * 128, n0 + g * 64, srow0 + 64, seq);
+          tma_store_2d(&p.tm_os, src, n0 + g * 64, arow0);
+          if (rows_valid > 64) tma_store_2d(&p.tm_os, src + 64 * 128, n0 + g * 64, arow0 + 64);
         });
       }
       return;
@@ -142,24 +143,21 @@ __global__ void __launch_bounds__(PipeShape<ApplySched>::kThreads, 1)
 }  // namespace
 
 cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z, const CUtensorMap& tm_snap,
-                         const CUtensorMap& tm_os, void* out, bool out_fp32, int B, int T, int d,
-                         int f, int C) {
+                         const CUtensorMap& tm_os, void* out, bool out_fp32, const DocMap& docs,
+                         int d, int f) {
   ApplyParams p;
   p.tm_z = tm_z;
   p.tm_snap = tm_snap;
   p.tm_os = tm_os;
   p.out = out;
   p.out_fp32 = out_fp32 ? 1 : 0;
-  p.B = B;
-  p.T = T;
+  p.docs = docs;
   p.d = d;
   p.f = f;
-  p.C = C;
-  p.n = (T + C - 1) / C;
-  p.mt_per_chunk = (C + kBM - 1) / kBM;
+  p.mt_per_chunk = (docs.C + kBM - 1) / kBM;
   p.nt = (d + kBN - 1) / kBN;
   p.kblocks = (f + kBK - 1) / kBK;
-  const int64_t units = int64_t(B) * p.n * p.mt_per_chunk * p.nt;
+  const int64_t units = int64_t(docs.nchunks) * p.mt_per_chunk * p.nt;
   if (units == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(pipe_smem_bytes<ApplySched>()));

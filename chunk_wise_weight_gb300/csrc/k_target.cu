@@ -64,7 +64,7 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(uint64_t v) {
 
 __global__ void __launch_bounds__(256)
     conv3_kernel(const __nv_bfloat16* __restrict__ x0, const float* __restrict__ conv_w,
-                 __nv_bfloat16* __restrict__ xc, int64_t rows, int T, int d, int C,
+                 __nv_bfloat16* __restrict__ xc, int64_t rows, DocMap docs, int d,
                  int pad_mode) {
   const int groups = d >> 3;
   const int64_t total = rows * groups;
@@ -72,11 +72,16 @@ __global__ void __launch_bounds__(256)
        idx += int64_t(gridDim.x) * blockDim.x) {
     const int64_t r = idx / groups;
     const int g = int(idx - r * groups);
-    const int t = int(r % T);
-    int lo = 0, hi = T;
+    // Taps stay inside the token's document and, with chunk padding, inside
+    // its chunk (chunks start at the document's first token; the last one
+    // ends with the document).
+    const int t = int(r);
+    const int k = docs.doc_of_token(t);
+    int lo = docs.start(k);
+    int hi = lo + docs.len(k);
     if (pad_mode == 0) {
-      lo = (t / C) * C;
-      hi = min(lo + C, T);  // a partial last chunk ends at T
+      lo += ((t - lo) / docs.C) * docs.C;
+      hi = min(lo + docs.C, hi);
     }
     const size_t base = size_t(r) * size_t(d) + size_t(g) * 8;
     const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
@@ -342,13 +347,14 @@ cudaError_t launch_target_variant(const LaunchEnv& env, const TargetParams& p, i
 }  // namespace
 
 cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const float* conv_w,
-                        __nv_bfloat16* xc, int64_t rows, int T, int d, int C, int pad_mode) {
+                        __nv_bfloat16* xc, int64_t rows, const DocMap& docs, int d,
+                        int pad_mode) {
   const int64_t total = rows * (d / 8);
   if (total == 0) return cudaSuccess;
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = int64_t(env.num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  conv3_kernel<<<int(blocks), 256, 0, env.stream>>>(x0, conv_w, xc, rows, T, d, C, pad_mode);
+  conv3_kernel<<<int(blocks), 256, 0, env.stream>>>(x0, conv_w, xc, rows, docs, d, pad_mode);
   return cudaGetLastError();
 }
 

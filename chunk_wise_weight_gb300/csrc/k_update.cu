@@ -6,7 +6,7 @@
 // The per-chunk deltas do not depend on W (the loss is linear in it), so
 // the state after chunk i is W_0 plus one long contraction over the tokens
 // of chunks 0..i.  A work unit owns a 128 (d_model) x 512 (d_ff) block of
-// one sequence's state, split into two 128 x 256 halves.  Each half's fp32
+// one document's state, split into two 128 x 256 halves.  Each half's fp32
 // state lives in one TMEM accumulator for the whole walk: the epilogue
 // warps load W_0 into it (tcgen05.st) and the MMAs accumulate
 // (eta Vhat_[i])^T Z_[i] on top, eta having been folded into Vhat by the
@@ -18,7 +18,10 @@
 //
 // Both operands are read MN-major: the contraction index (token) is the row
 // index of Vhat [T, d] and of Z [T, f].  A 64-token stage holds, per operand,
-// 64-column TMA boxes of 64 token lines x 128 bytes each.
+// 64-column TMA boxes of 64 token lines x 128 bytes each.  A chunk whose
+// length is not a multiple of 64 ends inside a stage: the MMA thread zeroes
+// the token lines past its end (within the last 16-token slice it issues)
+// and skips the slices after them.
 #include "kernels.h"
 #include "pipeline.cuh"
 
@@ -28,16 +31,18 @@ namespace {
 constexpr uint32_t kMnBoxBytes = 64 * 64 * 2;  // one {64 cols, 64 tokens} box
 
 struct UpdateParams {
-  CUtensorMap tm_v;  // eta*Vhat [B*T, d]  box {64, 64}
-  CUtensorMap tm_z;  // Z        [B*T, f]  box {64, 64}
-  CUtensorMap tm_ss; // snapshots as [B*n slots][d rows][f cols], box {64, 128, 1} (store)
+  CUtensorMap tm_v;  // eta*Vhat [M, d]  box {64, 64}
+  CUtensorMap tm_z;  // Z        [M, f]  box {64, 64}
+  CUtensorMap tm_ss; // snapshots as [slots][d rows][f cols], box {64, 128, 1} (store)
   const void* w0;
   int w0_fp32;
-  int64_t w0_bstride;
-  __nv_bfloat16* snap;  // [B, n, d, f]
-  float* state_out;     // [B, d, f] or nullptr
-  int B, T, d, f, C, n, n_upd;
-  int mt, np, kb_per_chunk, kb_last;  // K blocks of a full chunk / of chunk n-1
+  int64_t w0_bstride;   // elements between documents' initial states (0: shared)
+  float* state_out;     // [documents, d, f] or nullptr
+  DocMap docs;
+  const int* upd_docs;  // documents that update, longest first; nullptr: all
+  int n_udocs;
+  int final_update;     // also update with the last chunk (for state_out)
+  int d, f, mt, np;
 };
 
 struct UpdateSched : SchedDefaults {
@@ -45,36 +50,46 @@ struct UpdateSched : SchedDefaults {
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true, true);
   static constexpr bool kPreload = true;
   static constexpr bool kStagedStores = true;
+  static constexpr bool kRaggedK = true;
 
   const Params& p;
-  int b = 0, m0 = 0, nbase = 0, halves = 1;
+  int doc = 0, tok0 = 0, len = 0, nch = 0, nupd = 0, slot0 = 0, m0 = 0, nbase = 0, halves = 1;
 
   __device__ explicit UpdateSched(const Params& pp) : p(pp) {}
-  __device__ int num_units() const { return p.B * p.mt * p.np; }
+  __device__ int num_units() const { return p.n_udocs * p.mt * p.np; }
   // d_model blocks vary fastest: the CTAs of one wave share each Z column
-  // block, so Z streams from DRAM about once per sequence.
+  // block, so Z streams from DRAM about once per document.
   __device__ void begin_unit(int u, int) {
     const int mt = u % p.mt;
     const int r = u / p.mt;
     const int np = r % p.np;
-    b = r / p.np;
+    const int q = r / p.np;
+    doc = p.upd_docs ? __ldg(p.upd_docs + q) : q;
+    tok0 = p.docs.start(doc);
+    len = p.docs.len(doc);
+    nch = p.docs.num_chunks(doc);
+    slot0 = p.docs.first_chunk(doc);
+    nupd = p.final_update ? nch : nch - 1;
     m0 = mt * kBM;
     nbase = np * (2 * kBN);
     halves = (nbase + kBN < p.f) ? 2 : 1;
   }
-  __device__ int num_segments() const { return p.n_upd * halves; }
-  __device__ int unit_accs() const { return halves; }
+  __device__ int num_segments() const { return nupd * halves; }
+  __device__ int unit_accs() const { return nupd > 0 ? halves : 0; }
   __device__ int seg_acc(int s) const { return halves == 2 ? (s & 1) : 0; }
-  __device__ int seg_kblocks(int s) const {
-    const int i = halves == 2 ? (s >> 1) : s;
-    return i == p.n - 1 ? p.kb_last : p.kb_per_chunk;
+  __device__ int seg_chunk(int s) const { return halves == 2 ? (s >> 1) : s; }
+  // Tokens of chunk i of the document (the last chunk may be shorter).
+  __device__ int chunk_len(int i) const { return min(p.docs.C, len - i * p.docs.C); }
+  __device__ int seg_kblocks(int s) const { return (chunk_len(seg_chunk(s)) + kBK - 1) / kBK; }
+  __device__ int k_valid(int s, int kb) const {
+    return min(kBK, chunk_len(seg_chunk(s)) - kb * kBK);
   }
   __device__ bool seg_fresh(int) const { return false; }  // starts from the preloaded W_0
 
   __device__ void load(int s, int kb, uint8_t* stage, uint64_t* bar) const {
-    const int i = halves == 2 ? (s >> 1) : s;
+    const int i = seg_chunk(s);
     const int h = s - i * halves;
-    const int tok = b * p.T + i * p.C + kb * kBK;
+    const int tok = tok0 + i * p.docs.C + kb * kBK;
     uint8_t* sa = stage;
     uint8_t* sb = stage + kATileBytes;
     tma_load_2d(sa, &p.tm_v, bar, m0, tok);
@@ -82,6 +97,20 @@ struct UpdateSched : SchedDefaults {
     const int n0 = nbase + h * kBN;
 #pragma unroll
     for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kMnBoxBytes, &p.tm_z, bar, n0 + 64 * q, tok);
+  }
+  // Token lines [from, to) of both operands' boxes read zero: tokens past
+  // the chunk's end (another chunk's) must not enter its sum.  A whole
+  // 128-byte line is one token, so the swizzle does not matter here.
+  __device__ void clear_k(uint8_t* stage, int from, int to) const {
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+    for (int box = 0; box < 6; ++box) {
+      uint4* line = reinterpret_cast<uint4*>(stage + box * kMnBoxBytes);
+#pragma unroll 1
+      for (int t = from; t < to; ++t)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) line[t * 8 + c] = zero;
+    }
   }
   // MN-major, 128-byte swizzle: a 16-token slice is 16 lines of 128 B; the
   // 64-column groups of the tile are one box (lbo) apart.
@@ -97,7 +126,7 @@ struct UpdateSched : SchedDefaults {
     const int m = m0 + row;
     const bool row_ok = m < p.d;
     const int n0 = nbase + h * kBN;
-    const size_t off = size_t(b) * size_t(p.w0_bstride) + size_t(row_ok ? m : 0) * size_t(p.f);
+    const size_t off = size_t(doc) * size_t(p.w0_bstride) + size_t(row_ok ? m : 0) * size_t(p.f);
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 32) {
       uint32_t v[32];
@@ -136,16 +165,16 @@ struct UpdateSched : SchedDefaults {
   // >= f are not written) and, after the last update, the fp32 state when
   // the caller wants it (direct stores).
   __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& stg) const {
-    const int i = halves == 2 ? (s >> 1) : s;
+    const int i = seg_chunk(s);
     const int h = s - i * halves;
     const int m = m0 + row;
     const bool row_ok = m < p.d;
     const int n0 = nbase + h * kBN;
-    const bool write_snap = (i + 1) < p.n;
-    float* st = (p.state_out != nullptr && (i + 1) == p.n_upd)
-                    ? p.state_out + (size_t(b) * p.d + size_t(row_ok ? m : 0)) * size_t(p.f)
+    const bool write_snap = (i + 1) < nch;
+    float* st = (p.state_out != nullptr && (i + 1) == nupd)
+                    ? p.state_out + (size_t(doc) * p.d + size_t(row_ok ? m : 0)) * size_t(p.f)
                     : nullptr;
-    const int slot = b * p.n + i + 1;
+    const int slot = slot0 + i + 1;
 #pragma unroll 1
     for (int g = 0; g < kBN / 64; ++g) {
       uint8_t* buf = write_snap ? stg.acquire() : nullptr;
@@ -189,12 +218,12 @@ __global__ void __launch_bounds__(PipeShape<UpdateSched>::kThreads, 1)
   run_pipeline<UpdateSched>(p, status);
 }
 
-// snap[b, 0] = bf16(W_0 of sequence b): the state the first chunk applies.
+// Snapshot slot of each document's first chunk = bf16(W_0 of that document).
 __global__ void __launch_bounds__(256)
     snapshot0_kernel(const void* __restrict__ w0, int w0_fp32, int64_t w0_bstride,
-                     __nv_bfloat16* __restrict__ snap, int B, int n, int64_t df) {
+                     __nv_bfloat16* __restrict__ snap, DocMap docs, int64_t df) {
   const int64_t per = df >> 3;
-  const int64_t total = int64_t(B) * per;
+  const int64_t total = int64_t(docs.ndocs) * per;
   for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += int64_t(gridDim.x) * blockDim.x) {
     const int64_t b = idx / per;
@@ -210,29 +239,29 @@ __global__ void __launch_bounds__(256)
       out = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(w0) +
                                                  b * w0_bstride + e));
     }
-    *reinterpret_cast<uint4*>(snap + b * int64_t(n) * df + e) = out;
+    *reinterpret_cast<uint4*>(snap + int64_t(docs.first_chunk(int(b))) * df + e) = out;
   }
 }
 
 }  // namespace
 
 cudaError_t launch_snapshot0(const LaunchEnv& env, const void* w0, bool w0_fp32,
-                             int64_t w0_bstride, __nv_bfloat16* snap, int B, int n, int d,
+                             int64_t w0_bstride, __nv_bfloat16* snap, const DocMap& docs, int d,
                              int f) {
   const int64_t df = int64_t(d) * f;
-  const int64_t total = int64_t(B) * (df / 8);
+  const int64_t total = int64_t(docs.ndocs) * (df / 8);
   if (total == 0) return cudaSuccess;
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = int64_t(env.num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  snapshot0_kernel<<<int(blocks), 256, 0, env.stream>>>(w0, w0_fp32 ? 1 : 0, w0_bstride, snap, B,
-                                                        n, df);
+  snapshot0_kernel<<<int(blocks), 256, 0, env.stream>>>(w0, w0_fp32 ? 1 : 0, w0_bstride, snap,
+                                                        docs, df);
   return cudaGetLastError();
 }
 
 cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, const CUtensorMap& tm_z,
                           const CUtensorMap& tm_snap_store, const UpdateArgs& a) {
-  if (a.n_upd <= 0) return cudaSuccess;
+  if (a.n_udocs <= 0) return cudaSuccess;
   UpdateParams p;
   p.tm_v = tm_vhat;
   p.tm_z = tm_z;
@@ -240,24 +269,20 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
   p.w0 = a.w0;
   p.w0_fp32 = a.w0_fp32 ? 1 : 0;
   p.w0_bstride = a.w0_bstride;
-  p.snap = a.snap;
   p.state_out = a.state_out;
-  p.B = a.B;
-  p.T = a.T;
+  p.docs = a.docs;
+  p.upd_docs = a.upd_docs;
+  p.n_udocs = a.n_udocs;
+  p.final_update = a.final_update ? 1 : 0;
   p.d = a.d;
   p.f = a.f;
-  p.C = a.C;
-  p.n = a.n;
-  p.n_upd = a.n_upd;
   p.mt = (a.d + kBM - 1) / kBM;
   p.np = (a.f + 2 * kBN - 1) / (2 * kBN);
-  p.kb_per_chunk = a.C / kBK;
-  p.kb_last = (a.T - (a.n - 1) * a.C) / kBK;
-  const int units = p.B * p.mt * p.np;
+  const int64_t units = int64_t(p.n_udocs) * p.mt * p.np;
   cudaError_t e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(pipe_smem_bytes<UpdateSched>()));
   if (e != cudaSuccess) return e;
-  const int grid = units < env.num_sms ? units : env.num_sms;
+  const int grid = units < env.num_sms ? int(units) : env.num_sms;
   update_kernel<<<grid, PipeShape<UpdateSched>::kThreads, pipe_smem_bytes<UpdateSched>(), env.stream>>>(p, env.status);
   return cudaGetLastError();
 }

@@ -1,7 +1,7 @@
 // kernels.h -- internal launchers of libittt.so (host side, C++).  The C-ABI
 // in ittt_api.cu validates arguments, builds the TMA tensor maps and calls
-// these in data-flow order: conv (beside gate/up) -> target, gate/up ->
-// snapshot 0 -> update -> apply.
+// these in data-flow order: conv -> target -> gate/up -> snapshot 0 ->
+// update -> apply (or, in the dual form, scores -> dual apply).
 #pragma once
 
 #include <cuda.h>
@@ -17,6 +17,52 @@ struct LaunchEnv {
   unsigned int* status;  // device status word (kStatusTimeout bits)
 };
 
+// The documents along the packed token axis, each with its own fast-weight
+// state that starts from W_0 (the state is reset at document boundaries:
+// "[논문리뷰] In-Place Test-Time Training", Method §3, causality and boundary
+// handling).  Either B sequences of T tokens (starts == nullptr), or a table
+// uploaded by the host: document k covers tokens [starts[k], starts[k+1])
+// and owns snapshot slots [chunk_base[k], chunk_base[k+1]), one per chunk;
+// chunk_doc[g] is the document of slot g.  Chunks start at each document's
+// first token; a document's last chunk may be shorter than C.
+struct DocMap {
+  const int* starts;      // [ndocs + 1] device, or nullptr
+  const int* chunk_base;  // [ndocs + 1] device, or nullptr
+  const int* chunk_doc;   // [nchunks] device, or nullptr
+  int ndocs;              // documents (B when regular)
+  int nchunks;            // snapshot slots over all documents
+  int T;                  // tokens per sequence (regular) / in the pack
+  int n;                  // chunks per sequence (regular)
+  int C;
+
+  __host__ __device__ bool packed() const { return starts != nullptr; }
+#ifdef __CUDACC__
+  __device__ __forceinline__ int start(int k) const { return starts ? __ldg(starts + k) : k * T; }
+  __device__ __forceinline__ int len(int k) const {
+    return starts ? __ldg(starts + k + 1) - __ldg(starts + k) : T;
+  }
+  __device__ __forceinline__ int first_chunk(int k) const {
+    return chunk_base ? __ldg(chunk_base + k) : k * n;
+  }
+  __device__ __forceinline__ int num_chunks(int k) const {
+    return chunk_base ? __ldg(chunk_base + k + 1) - __ldg(chunk_base + k) : n;
+  }
+  __device__ __forceinline__ int doc_of_chunk(int g) const {
+    return chunk_doc ? __ldg(chunk_doc + g) : g / n;
+  }
+  // Document holding token row r (binary search over the starts).
+  __device__ __forceinline__ int doc_of_token(int r) const {
+    if (!starts) return r / T;
+    int lo = 0, hi = ndocs;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(starts + mid) <= r) lo = mid; else hi = mid;
+    }
+    return lo;
+  }
+#endif
+};
+
 // Z[M, f] = SiLU(H W_gate^T) * (H W_up^T).  Tensor maps: H [M, K] box
 // {64,128}; W_gate, W_up [f, K] box {64,128}; Z [M, f] box {64,128} for the
 // TMA stores.  All bf16, K = d_model.
@@ -25,9 +71,10 @@ cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h,
                           const CUtensorMap& tm_zs, int M, int f, int K);
 
 // Xc = three-tap depthwise conv of X0 (zero padding at chunk edges, or only
-// at sequence edges when pad_mode = 1), rounded to bf16.  x0, xc: [B*T, d].
+// at document edges when pad_mode = 1), rounded to bf16.  x0, xc: [rows, d].
 cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const float* conv_w,
-                        __nv_bfloat16* xc, int64_t rows, int T, int d, int C, int pad_mode);
+                        __nv_bfloat16* xc, int64_t rows, const DocMap& docs, int d,
+                        int pad_mode);
 
 // vhat[M, d] = eta * eta_tok[row] * (Conv1D(X0) W_target^T), rounded once to
 // bf16 (eta_tok may be null: weight 1).
@@ -40,40 +87,41 @@ cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a,
                           const float* conv_w, const float* eta_tok, __nv_bfloat16* vhat,
                           float eta, int M, int T, int d, int C, int pad_mode, bool fused);
 
-// snap[b, 0] = bf16(W_0 of sequence b) for every b.  w0 is bf16 or fp32,
-// [d, f] shared (w0_bstride = 0) or [B, d, f].
+// Slot docs.first_chunk(k) of snap = bf16(W_0 of document k) for every k.
+// w0 is bf16 or fp32, [d, f] shared (w0_bstride = 0) or one per document.
 cudaError_t launch_snapshot0(const LaunchEnv& env, const void* w0, bool w0_fp32,
-                             int64_t w0_bstride, __nv_bfloat16* snap, int B, int n, int d,
+                             int64_t w0_bstride, __nv_bfloat16* snap, const DocMap& docs, int d,
                              int f);
 
 struct UpdateArgs {
-  int B, T, d, f, C;
-  int n;          // chunks per sequence
-  int n_upd;      // updates to run: n-1, or n when the final state is wanted
-  const void* w0; // bf16 or fp32 initial state
+  DocMap docs;
+  const int* upd_docs;  // device list of the documents that update, or nullptr (all)
+  int n_udocs;          // documents that update (0: no launch)
+  bool final_update;    // also the last chunk's update (the caller wants the state)
+  int d, f;
+  const void* w0;       // bf16 or fp32 initial state
   bool w0_fp32;
   int64_t w0_bstride;
-  __nv_bfloat16* snap;  // [B, n, d, f]: slots 1..n-1 written here
-  float* state_out;     // [B, d, f] fp32 or nullptr
+  float* state_out;     // [documents, d, f] fp32 or nullptr
 };
 
-// Fast-weight update walk: for each (sequence, 128 x 512 state tile) the
+// Fast-weight update walk: for each (document, 128 x 512 state tile) the
 // fp32 state starts at W_0 in TMEM and the per-chunk deltas
 // (eta Vhat_[i])^T Z_[i] accumulate onto it; after chunk i the epilogue
-// writes bf16(W_{i+1}) as snapshot i+1.  Tensor maps: eta*Vhat [B*T, d] box
-// {64,64}; Z [B*T, f] box {64,64} (both read MN-major); snapshots as
-// [B*n][d][f] with box {64,128,1} for the TMA stores.
+// writes bf16(W_{i+1}) into the document's snapshot slot i+1.  Tensor maps:
+// eta*Vhat [M, d] box {64,64}; Z [M, f] box {64,64} (both read MN-major);
+// snapshots as [slots][d][f] with box {64,128,1} for the TMA stores.
 cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
                           const CUtensorMap& tm_z, const CUtensorMap& tm_snap_store,
                           const UpdateArgs& a);
 
-// O_[i] = Z_[i] snap[b, i]^T for every (sequence, chunk).  Tensor maps:
-// Z [B*T, f] box {64,128}; snapshots [B*n*d, f] box {64,256}; bf16 O as
-// [B][T][d] with box {64,64,1} for the TMA stores (unused for fp32 O).  The
-// last chunk may be shorter than C (n = ceil(T / C)).
+// O_[i] = Z_[i] snap[slot of chunk i]^T for every chunk of every document.
+// Tensor maps: Z [M, f] box {64,128}; snapshots [slots*d, f] box {64,256};
+// bf16 O [M, d] with box {64,64} for the TMA stores (unused for fp32 O).
+// Chunks of any length; a document's last chunk may be shorter than C.
 cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
                          const CUtensorMap& tm_snap, const CUtensorMap& tm_os, void* out,
-                         bool out_fp32, int B, int T, int d, int f, int C);
+                         bool out_fp32, const DocMap& docs, int d, int f);
 
 // Dual form, scores: S[b, t, s] = Z_t . Z_s (bf16) for every token t of chunk
 // i >= 1 and every token s < i*C of the same sequence.  Tensor maps: Z

@@ -120,6 +120,13 @@ struct SchedDefaults {
   //   uint32_t idesc(int s, int kb); uint64_t a_desc(int s, int kb, uint32_t
   //   base, int k16); uint64_t b_desc(int s, int kb, uint32_t base, int k16)
   static constexpr bool kMixedOperands = false;
+  // With kRaggedK a K block may hold fewer than 64 valid K indices (the end
+  // of a chunk that is not a multiple of 64 tokens long).  The MMA thread
+  // then zeroes the operand lines of the invalid K indices inside the last
+  // 16-wide slice it issues and skips the slices after it:
+  //   int  k_valid(int s, int kb)                       1..64
+  //   void clear_k(uint8_t* stage, int from, int to)    (generic stores)
+  static constexpr bool kRaggedK = false;
   // Transaction bytes the producer's copies deliver into a stage.
   __device__ uint32_t tma_bytes(int, int) const { return kStageBytes; }
 };
@@ -266,6 +273,28 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
             tc_fence_after_sync();
             const uint32_t a_base = smem_u32(smem + size_t(stage) * kStride);
             const uint32_t b_base = a_base + kATileBytes;
+            if constexpr (S::kRaggedK) {
+              const int kv = sched.k_valid(s, kb);
+              if (kv < kBK) {
+                const int kv16 = (kv + kUmmaK - 1) / kUmmaK * kUmmaK;
+                if (kv < kv16) {
+                  sched.clear_k(smem + size_t(stage) * kStride, kv, kv16);
+                  fence_proxy_async_smem();  // generic stores -> tensor core
+                }
+#pragma unroll
+                for (int k = 0; k < kBK / kUmmaK; ++k) {
+                  if (k * kUmmaK < kv)
+                    mma_bf16(d_tmem, S::a_desc(a_base, k), S::b_desc(b_base, k), S::kIdesc,
+                             (fresh && kb == 0 && k == 0) ? 0u : 1u);
+                }
+                mma_commit(&sync->empty[stage]);
+                if (++stage == NS) {
+                  stage = 0;
+                  phase ^= 1u;
+                }
+                continue;
+              }
+            }
             if constexpr (S::kMixedOperands) {
               const uint32_t id = sched.idesc(s, kb);
 #pragma unroll

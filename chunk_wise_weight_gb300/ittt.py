@@ -45,7 +45,8 @@ class Opts(ctypes.Structure):
                 ("z_buf", ctypes.POINTER(Tensor)), ("vhat_buf", ctypes.POINTER(Tensor)),
                 ("snap_buf", ctypes.POINTER(Tensor)), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t), ("events", ctypes.POINTER(ctypes.c_void_p)),
-                ("eta_tok", ctypes.POINTER(Tensor))]
+                ("eta_tok", ctypes.POINTER(Tensor)), ("cu_seqlens", ctypes.POINTER(ctypes.c_int64)),
+                ("num_docs", ctypes.c_int64)]
 
 
 _TP = ctypes.POINTER(Tensor)
@@ -74,6 +75,8 @@ def load(path: str | None = None):
     lib.ittt_forward_ex.restype = ctypes.c_int
     lib.ittt_workspace_bytes.argtypes = [ctypes.c_int64] * 5
     lib.ittt_workspace_bytes.restype = ctypes.c_size_t
+    lib.ittt_workspace_bytes_ex.argtypes = [ctypes.c_int64] * 5 + [ctypes.POINTER(Opts)]
+    lib.ittt_workspace_bytes_ex.restype = ctypes.c_size_t
     lib.ittt_stream_status.argtypes = [ctypes.c_void_p]
     lib.ittt_stream_status.restype = ctypes.c_int
     lib.ittt_last_error.argtypes = []
@@ -130,28 +133,50 @@ def _check(status: int):
         raise IttError(status, last_error())
 
 
+def _seqlens(cu_seqlens):
+    """int64 ctypes array of host token offsets (list, tuple or CPU tensor)."""
+    if cu_seqlens is None:
+        return None
+    vals = [int(v) for v in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist")
+                             else cu_seqlens)]
+    return (ctypes.c_int64 * len(vals))(*vals)
+
+
+def _opts(pad_mode, fused_conv, dual, cu_seqlens, keep: dict, **tensors) -> Opts:
+    opts = Opts()
+    opts.pad_mode = int(pad_mode)
+    opts.flags = (FLAG_FUSED_CONV if fused_conv else 0) | (FLAG_DUAL if dual else 0)
+    for name, t in tensors.items():
+        if t is not None:
+            keep[name] = describe(t)
+            setattr(opts, name, ctypes.pointer(keep[name]))
+    arr = _seqlens(cu_seqlens)
+    if arr is not None:
+        keep["cu_seqlens"] = arr
+        opts.cu_seqlens = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64))
+        opts.num_docs = len(arr) - 1
+    return opts
+
+
 def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: int,
             out: torch.Tensor | None = None, *, out_dtype=torch.bfloat16, stream=None,
             pad_mode: int = PAD_CHUNK, state_in=None, state_out=None, z_buf=None,
             vhat_buf=None, snap_buf=None, workspace=None, events=None,
-            fused_conv: bool = False, dual: bool = False, eta_tok=None) -> torch.Tensor:
+            fused_conv: bool = False, dual: bool = False, eta_tok=None,
+            cu_seqlens=None) -> torch.Tensor:
     """Enqueue one layer forward on `stream` (default: current stream) and
     return `out` [B,T,d].  Extra keyword buffers map to ittt_opts; `events`
     is a list of 2 * len(PHASES) torch.cuda.Event(enable_timing=True): a
-    (start, end) pair per phase."""
+    (start, end) pair per phase.  `cu_seqlens` (host ints, num_docs + 1
+    offsets) packs documents into the one row of H [1,T,d]."""
     lib = load()
     if out is None:
         out = torch.empty(H.shape, dtype=out_dtype, device=H.device)
     keep = [describe(x) for x in (H, X0, W_gate, W_up, W_down0, W_target, conv_w, out)]
-    opts = Opts()
-    opts.pad_mode = int(pad_mode)
-    opts.flags = (FLAG_FUSED_CONV if fused_conv else 0) | (FLAG_DUAL if dual else 0)
     extra = {}
-    for name, t in (("state_in", state_in), ("state_out", state_out), ("z_buf", z_buf),
-                    ("vhat_buf", vhat_buf), ("snap_buf", snap_buf), ("eta_tok", eta_tok)):
-        if t is not None:
-            extra[name] = describe(t)
-            setattr(opts, name, ctypes.pointer(extra[name]))
+    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, extra, state_in=state_in,
+                 state_out=state_out, z_buf=z_buf, vhat_buf=vhat_buf, snap_buf=snap_buf,
+                 eta_tok=eta_tok)
     if workspace is not None:
         opts.workspace = workspace.data_ptr()
         opts.workspace_bytes = workspace.numel() * workspace.element_size()
@@ -190,6 +215,18 @@ def stream_status(stream=None, device=None) -> None:
 
 def workspace_bytes(B: int, T: int, d: int, f: int, chunk: int) -> int:
     return int(load().ittt_workspace_bytes(B, T, d, f, chunk))
+
+
+def workspace_bytes_ex(B: int, T: int, d: int, f: int, chunk: int, *, pad_mode: int = PAD_CHUNK,
+                       fused_conv: bool = False, dual: bool = False, cu_seqlens=None,
+                       **buffers) -> int:
+    """ittt_workspace_bytes_ex: scratch for a forward call with these
+    options; `buffers` name the ittt_opts tensors the call passes (state_in,
+    state_out, z_buf, vhat_buf, snap_buf, eta_tok) -- only whether each is
+    given matters."""
+    keep = {}
+    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, keep, **buffers)
+    return int(load().ittt_workspace_bytes_ex(B, T, d, f, chunk, ctypes.byref(opts)))
 
 
 def launch_count(B: int, T: int, d: int, f: int, chunk: int) -> int:

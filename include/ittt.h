@@ -7,7 +7,7 @@
  *
  *   Z     = SiLU(H W_gate^T) (.) (H W_up^T)                  (eq. 2)
  *   Vhat  = Conv1D(X0) W_target^T                             (eq. 5)
- *   W_0   = W_down0                    (reset per sequence, Method §3)
+ *   W_0   = W_down0          (reset per sequence / document, Method §3)
  *   for each chunk i of C tokens, in order:
  *     O_[i]   = Z_[i] W_i^T                                   (eq. 3, apply)
  *     W_{i+1} = W_i + eta * Vhat_[i]^T Z_[i]                  (eq. 6, update)
@@ -27,11 +27,14 @@
  *   - Shapes: H, X0 [B,T,d] bf16; W_gate, W_up [f,d] bf16; W_down0 [d,f]
  *     bf16 or fp32; W_target [d,d] bf16; conv_w [d,3] fp32; out [B,T,d]
  *     bf16 or fp32.  Weights use the [out_features, in_features] layout.
- *   - Supported sizes: d and f multiples of 8 (16-byte rows), chunk > 0 a
- *     multiple of 64, T a multiple of 64, B*T < 2^31.  When chunk does not
- *     divide T the last chunk is the shorter remainder (a stream that ends
- *     mid-chunk).  Anything else returns ITTT_ERR_UNSUPPORTED or
- *     ITTT_ERR_INVALID_ARG before any launch.
+ *   - Supported sizes: d and f multiples of 8 (16-byte rows), any chunk
+ *     >= 1, any T >= 1, B*T < 2^31.  When chunk does not divide T the last
+ *     chunk is the shorter remainder (a stream that ends mid-chunk).  Chunks
+ *     that are multiples of 64 tokens run at full speed; other lengths are
+ *     exact but pay for masking at every chunk end.  (ITTT_FLAG_FUSED_CONV
+ *     and ITTT_FLAG_DUAL have narrower limits, stated with each.)  Anything
+ *     else returns ITTT_ERR_UNSUPPORTED or ITTT_ERR_INVALID_ARG before any
+ *     launch.
  *   - Ownership: the caller owns every buffer; the library keeps no pointer
  *     after a call returns.  `out` must not overlap any input.
  *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL is the
@@ -93,19 +96,39 @@ typedef struct {
  * pointer may be NULL.
  *
  *   pad_mode   ittt_pad_mode for the convolution boundary.
- *   state_in   fp32 [B,d,f]: per-sequence initial fast weight.  Replaces
- *              W_down0 (which may then be NULL) -- continues a stream of
- *              chunks from a state returned by an earlier call.
- *   state_out  fp32 [B,d,f]: receives W_n, the fast weight after the LAST
- *              chunk's update (an update the output itself never needs).
+ *   cu_seqlens HOST array of num_docs + 1 token offsets: packed documents.
+ *              H, X0, out (and eta_tok, z_buf, vhat_buf) then hold B = 1
+ *              row of T tokens in which document k is the token range
+ *              [cu_seqlens[k], cu_seqlens[k+1]); cu_seqlens[0] = 0,
+ *              cu_seqlens[num_docs] = T, and every document has at least one
+ *              token.  Each document runs like a sequence of its own: its
+ *              fast weight starts from W_0 (or its state_in) -- the state is
+ *              reset at document boundaries (Method §3, causality and
+ *              boundary handling) -- its chunks start at its first token,
+ *              its last chunk may be shorter, and no convolution tap crosses
+ *              into another document.  Read during the call only (the
+ *              derived tables go to the device through a pinned staging
+ *              buffer, so such a call cannot be captured into a CUDA graph).
+ *              Not combinable with ITTT_FLAG_FUSED_CONV or ITTT_FLAG_DUAL.
+ *   num_docs   number of packed documents (0 when cu_seqlens is NULL).
+ *   state_in   fp32 [S,d,f]: per-sequence (S = B) or per-document
+ *              (S = num_docs) initial fast weight.  Replaces W_down0 (which
+ *              may then be NULL) -- continues a stream of chunks from a
+ *              state returned by an earlier call.
+ *   state_out  fp32 [S,d,f]: receives each sequence's or document's fast
+ *              weight after its LAST chunk's update (an update the output
+ *              itself never needs).
  *   z_buf      bf16 [B,T,f]: caller buffer used as the Z scratch; after the
  *              call it holds Z.  Lets tests inspect the intermediate.
  *   vhat_buf   bf16 [B,T,d]: same for the update's left operand, which the
  *              library stores with eta folded in: it holds eta * Vhat.
- *   snap_buf   bf16 [B,n,d,f] (n = T/chunk): same for the bf16 snapshots
- *              W_0 .. W_{n-1} that the apply step reads.
- *   workspace  device scratch of workspace_bytes >= ittt_workspace_bytes(...)
- *              (256-byte aligned); when given, nothing is allocated.
+ *   snap_buf   bf16 [B,n,d,f] (n = ceil(T/chunk)): same for the bf16
+ *              snapshots W_0 .. W_{n-1} that the apply step reads.  Packed
+ *              documents: [1,N,d,f] with N the chunks of all documents,
+ *              document k's W_0 at slot sum_{j<k} ceil(len_j / chunk).
+ *   workspace  device scratch of workspace_bytes >= ittt_workspace_bytes_ex
+ *              (...) for the same options (256-byte aligned); when given,
+ *              nothing is allocated.
  *   eta_tok    fp32 [B,T]: per-token learning-rate weights; token t's term
  *              of the chunk update is scaled by eta * eta_tok[b,t] (the
  *              large-chunk update with a rate per token of "Test-Time
@@ -129,21 +152,23 @@ typedef struct {
   size_t workspace_bytes;
   void* const* events;
   const ittt_tensor* eta_tok;
+  const int64_t* cu_seqlens;
+  int64_t num_docs;
 } ittt_opts;
 
 /* ittt_opts.flags */
 /* Compute the convolution inside the W_target GEMM (extra warps build each
  * A tile from raw X0 rows in shared memory) instead of in its own kernel.
  * Same results; slower on GB300, where the fused convolution is repeated for
- * every 256-column output tile. */
+ * every 256-column output tile.  Needs chunk and T multiples of 64. */
 #define ITTT_FLAG_FUSED_CONV 1
 /* Compute O with the dual form O_[i] = Z_[i] W_0^T + eta sum_{j<i}
  * (Z_[i] Z_[j]^T) Vhat_[j] instead of walking the fast-weight state: a
  * scores kernel writes the block-lower part of Z Z^T (bf16, B*T*T*2 bytes of
  * scratch) and one GEMM accumulates both terms.  Same layer, different
  * rounding; more work than the primal walk on every workload measured, so
- * it is never the default.  Not combinable with state_out or snap_buf, and
- * chunk must divide T. */
+ * it is never the default.  Not combinable with state_out or snap_buf; chunk
+ * must be a multiple of 64 that divides T. */
 #define ITTT_FLAG_DUAL 2
 
 /* Kernel phases of one forward call, in launch order. */
@@ -203,8 +228,8 @@ ITTT_API ittt_status ittt_forward_ex(const ittt_tensor* H, const ittt_tensor* X0
  * array, so calls that overlap on the GPU (other streams, other threads)
  * race: serialise them on one stream.  The first call on a device does a
  * one-time set-up (it looks up the array's device address); make that first
- * call before any stream capture.  Pad mode is ITTT_PAD_CHUNK.  Device-side
- * failures are reported by ittt_stream_status().
+ * call before any stream capture.  Pad mode is ITTT_PAD_CHUNK; sizes as for
+ * ittt_forward.  Device-side failures are reported by ittt_stream_status().
  */
 #define ITTT_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 ITTT_API ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_tensor* X0,
@@ -221,6 +246,15 @@ ITTT_API ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_tenso
  */
 ITTT_API size_t ittt_workspace_bytes(int64_t B, int64_t T, int64_t d, int64_t f,
                             int64_t chunk);
+
+/*
+ * Bytes of device scratch an ittt_forward_ex call with these options needs
+ * (0 if the call would be rejected).  Reads opts->flags, pad_mode,
+ * cu_seqlens / num_docs, and which of state_in, state_out, z_buf, vhat_buf
+ * and snap_buf are non-NULL (not their contents).  opts may be NULL.
+ */
+ITTT_API size_t ittt_workspace_bytes_ex(int64_t B, int64_t T, int64_t d, int64_t f,
+                                        int64_t chunk, const ittt_opts* opts);
 
 /*
  * Synchronises `stream`, then reports any device-side failure recorded by

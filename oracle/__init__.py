@@ -289,3 +289,59 @@ def first_chunk_rows(H, W_gate, W_up, w0, rows) -> np.ndarray:
     _load().oracle_first_chunk_rows(d, f, _fptr(H), _fptr(Wg), _fptr(Wu),
                                     _fptr(w0), len(r), _iptr(r), _dptr(out))
     return out
+
+
+# --------------------------------------------------------------------------
+# Packed documents
+# --------------------------------------------------------------------------
+
+def forward_packed(inp, cu_seqlens, eta: float, chunk: int, pad_mode: int = PAD_CHUNK,
+                   want_z: bool = False, want_vhat: bool = False, want_states: bool = False,
+                   eta_tok=None) -> dict:
+    """Documents packed along one token axis, the fast weight reset to W_0 at
+    every document boundary ("[논문리뷰] In-Place Test-Time Training",
+    Method §3, causality and boundary handling): document k, the tokens
+    [cu_seqlens[k], cu_seqlens[k+1]), is run as a sequence of its own -- its
+    chunks start at its first token and no convolution tap crosses into a
+    neighbour.
+
+    inp["H"], inp["X0"]: [T, d] or [1, T, d]; inp["W_down0"]: [d, f] shared
+    or [num_docs, d, f] per document; eta_tok: [T] or [1, T].  Returns "O"
+    [T, d] (and "Z" [T, f], "Vhat" [T, d] when asked), plus "states": a list
+    with document k's W^(0)..W^(n_k) as [n_k + 1, d, f].
+    """
+    cu = [int(v) for v in cu_seqlens]
+    H = _f32(inp["H"]).reshape(-1, _f32(inp["H"]).shape[-1])
+    X0 = _f32(inp["X0"]).reshape(H.shape)
+    W0 = _f32(inp["W_down0"])
+    T, d = H.shape
+    if cu[0] != 0 or cu[-1] != T or any(b <= a for a, b in zip(cu, cu[1:])):
+        raise ValueError("cu_seqlens must rise strictly from 0 to T")
+    et = None if eta_tok is None else _f32(eta_tok).reshape(T)
+    f = _f32(inp["W_gate"]).shape[0]
+    O = np.zeros((T, d), np.float64)
+    Z = np.zeros((T, f), np.float64) if want_z else None
+    V = np.zeros((T, d), np.float64) if want_vhat else None
+    states = []
+    for k in range(len(cu) - 1):
+        a, b = cu[k], cu[k + 1]
+        doc = dict(inp)
+        doc["H"], doc["X0"] = H[a:b][None], X0[a:b][None]
+        doc["W_down0"] = W0[k] if W0.ndim == 3 else W0
+        r = forward(doc, eta, chunk, pad_mode, want_z=want_z, want_vhat=want_vhat,
+                    want_states=want_states, eta_tok=None if et is None else et[a:b][None])
+        O[a:b] = r["O"][0]
+        if want_z:
+            Z[a:b] = r["Z"][0]
+        if want_vhat:
+            V[a:b] = r["Vhat"][0]
+        if want_states:
+            states.append(r["states"][0])
+    out = {"O": O}
+    if want_z:
+        out["Z"] = Z
+    if want_vhat:
+        out["Vhat"] = V
+    if want_states:
+        out["states"] = states
+    return out

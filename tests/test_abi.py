@@ -5,6 +5,7 @@ import ctypes
 import math
 
 import pytest
+import torch
 
 from chunk_wise_weight_gb300 import build, ittt
 
@@ -95,14 +96,23 @@ def test_rejects_bad_descriptors(lib, mutate, status, msg):
 def test_rejects_bad_sizes(lib):
     assert _call(lib, _args(), chunk=0) == ittt.ERR_INVALID_ARG
     assert "positive" in ittt.last_error()
-    assert _call(lib, _args(), chunk=100) == ittt.ERR_UNSUPPORTED   # not a multiple of 64
-    assert "multiples of 64" in ittt.last_error()
-    assert _call(lib, _args(T=96), chunk=32) == ittt.ERR_UNSUPPORTED
-    assert _call(lib, _args(T=200), chunk=64) == ittt.ERR_UNSUPPORTED  # T not a multiple of 64
+    assert _call(lib, _args(), chunk=-64) == ittt.ERR_INVALID_ARG
     assert _call(lib, _args(d=60), chunk=64) == ittt.ERR_UNSUPPORTED
     assert _call(lib, _args(f=100), chunk=64) == ittt.ERR_UNSUPPORTED
     assert _call(lib, _args(), eta=math.nan) == ittt.ERR_INVALID_ARG
     assert _call(lib, _args(), eta=math.inf) == ittt.ERR_INVALID_ARG
+
+
+def test_any_chunk_and_length_plan():
+    """Chunks and lengths that are not multiples of 64 are planned (no call
+    with fake pointers gets past validation here: only the planner runs)."""
+    for T, C in ((256, 100), (96, 32), (200, 64), (257, 1), (5, 7)):
+        assert ittt.workspace_bytes(1, T, 64, 256, C) > 0, (T, C)
+    # narrower limits of the two options
+    assert ittt.workspace_bytes_ex(1, 256, 64, 256, 100, fused_conv=True) == 0
+    assert ittt.workspace_bytes_ex(1, 200, 64, 256, 64, fused_conv=True) == 0
+    assert ittt.workspace_bytes_ex(1, 320, 64, 256, 128, dual=True) == 0
+    assert ittt.workspace_bytes_ex(1, 256, 64, 256, 128, dual=True) > 0
 
 
 def test_rejects_bad_options(lib):
@@ -129,6 +139,9 @@ def test_rejects_bad_options(lib):
     o.flags = ittt.FLAG_DUAL
     assert _call(lib, _args(T=320), chunk=128, opts=o) == ittt.ERR_UNSUPPORTED  # partial chunk
     o = ittt.Opts()
+    o.flags = ittt.FLAG_FUSED_CONV
+    assert _call(lib, _args(), chunk=100, opts=o) == ittt.ERR_UNSUPPORTED
+    o = ittt.Opts()
     et = _desc([1, 256], ittt.BF16, data=FAKE * 9 * 1024)           # eta_tok must be fp32
     o.eta_tok = ctypes.pointer(et)
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
@@ -146,12 +159,72 @@ def test_workspace_bytes_and_launch_count(lib):
     n = T // C
     want = r(B * T * f * 2) + 2 * r(B * T * d * 2) + r(B * n * d * f * 2)
     assert ittt.workspace_bytes(B, T, d, f, C) == want
+    assert ittt.workspace_bytes_ex(B, T, d, f, C) == want
     want3 = r(B * T * f * 2) + 2 * r(B * T * d * 2) + r(B * 3 * d * f * 2)   # 1024 = 2*384+256
     assert ittt.workspace_bytes(B, T, d, f, 384) == want3
-    assert ittt.workspace_bytes(B, T, d, f, 100) == 0
+    assert ittt.workspace_bytes(B, T, d, f, 0) == 0
+    assert ittt.workspace_bytes(B, T, 60, f, C) == 0
+    # caller buffers and the fused convolution take parts out of the scratch
+    assert ittt.workspace_bytes_ex(B, T, d, f, C, fused_conv=True) == want - r(B * T * d * 2)
+    fake_z = torch.empty(0)
+    assert (ittt.workspace_bytes_ex(B, T, d, f, C, z_buf=fake_z) == want - r(B * T * f * 2))
+    # the dual form: scores [B,T,T] bf16, no snapshots (W_0 dtype unknown:
+    # a bf16 copy of it is planned)
+    want_dual = r(B * T * f * 2) + 2 * r(B * T * d * 2) + r(B * T * T * 2) + r(d * f * 2)
+    assert ittt.workspace_bytes_ex(B, T, d, f, C, dual=True) == want_dual
+    # packed documents 300 + 724 tokens: ceil(300/256) + ceil(724/256) = 2 + 3
+    # slots, and a table of 2*(2+1) + 5 + 2 ints (both documents update)
+    cu = [0, 300, 1024]
+    want_packed = (r(T * f * 2) + 2 * r(T * d * 2) + r(5 * d * f * 2) + r((6 + 5 + 2) * 4))
+    assert ittt.workspace_bytes_ex(1, T, d, f, C, cu_seqlens=cu) == want_packed
     assert ittt.launch_count(B, T, d, f, C) == 6
     assert ittt.launch_count(B, T, d, f, T) == 5
-    assert ittt.launch_count(B, T, d, f, 100) == 0
+    assert ittt.launch_count(B, 1000, d, f, 512) == 6   # two chunks, the last partial
+    assert ittt.launch_count(B, T, d, f, 0) == 0
+
+
+def _packed_opts(cu, **kw):
+    o = ittt.Opts()
+    arr = (ctypes.c_int64 * len(cu))(*cu)
+    o.cu_seqlens = ctypes.cast(arr, ctypes.POINTER(ctypes.c_int64))
+    o.num_docs = len(cu) - 1
+    for k, v in kw.items():
+        setattr(o, k, v)
+    return o, arr
+
+
+@pytest.mark.parametrize("cu,msg", [
+    ([1, 100, 256], "cu_seqlens[0]"),
+    ([0, 100, 250], "cu_seqlens[num_docs]"),
+    ([0, 100, 100, 256], "strictly"),
+    ([0, 150, 100, 256], "strictly"),
+    ([0], "num_docs"),
+])
+def test_rejects_bad_document_offsets(lib, cu, msg):
+    o, _arr = _packed_opts(cu)
+    assert _call(lib, _args(), opts=o) == ittt.ERR_INVALID_ARG
+    assert msg in ittt.last_error()
+
+
+def test_rejects_bad_packed_options(lib):
+    o, _arr = _packed_opts([0, 100, 256])
+    assert _call(lib, _args(B=2), opts=o) == ittt.ERR_INVALID_ARG      # packed needs B = 1
+    assert "B = 1" in ittt.last_error()
+    for flag in (ittt.FLAG_FUSED_CONV, ittt.FLAG_DUAL):
+        o, _arr = _packed_opts([0, 128, 256], flags=flag)
+        assert _call(lib, _args(), opts=o) == ittt.ERR_UNSUPPORTED
+    o = ittt.Opts()
+    o.num_docs = 2                                                     # count without offsets
+    assert _call(lib, _args(), opts=o) == ittt.ERR_INVALID_ARG
+    # per-document states are [num_docs, d, f]; snapshots [1, slots, d, f]
+    st = _desc([1, 64, 256], ittt.FP32, data=FAKE * 9 * 1024)
+    o, _arr = _packed_opts([0, 100, 256], state_out=ctypes.pointer(st))
+    assert _call(lib, _args(), opts=o) == ittt.ERR_INVALID_ARG
+    assert "state_out" in ittt.last_error()
+    sb = _desc([1, 4, 64, 256], ittt.BF16, data=FAKE * 9 * 1024)       # 2 + 3 slots at C=64
+    o, _arr = _packed_opts([0, 100, 256], snap_buf=ctypes.pointer(sb))
+    assert _call(lib, _args(), opts=o) == ittt.ERR_INVALID_ARG
+    assert "snap_buf" in ittt.last_error()
 
 
 def test_python_binding_has_no_compute_fallback():

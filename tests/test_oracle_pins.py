@@ -438,3 +438,116 @@ def test_forms_agree_with_token_rates():
                               inp["W_down0"], inp["W_target"], inp["conv_w"], 0.3, 4, m, j,
                               eta_tok=rates[1])
     np.testing.assert_allclose(st, seq["states"][1][:, m, j].T, rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# Packed documents: the fast weight is reset at every document boundary
+# (Method §3, causality and boundary handling)
+# --------------------------------------------------------------------------
+
+def test_packed_equal_documents_are_the_batch():
+    """Documents of equal length packed in one row give the same outputs and
+    states as the same documents run as a batch."""
+    B, L, d, f, C = 3, 10, 4, 6, 4
+    inp = _inputs(B, L, d, f, seed=91)
+    batch = oracle.forward(inp, 0.4, C, want_z=True, want_vhat=True, want_states=True)
+    packed = dict(inp)
+    packed["H"], packed["X0"] = inp["H"].reshape(1, B * L, d), inp["X0"].reshape(1, B * L, d)
+    cu = [0, L, 2 * L, 3 * L]
+    got = oracle.forward_packed(packed, cu, 0.4, C, want_z=True, want_vhat=True,
+                                want_states=True)
+    np.testing.assert_array_equal(got["O"], batch["O"].reshape(B * L, d))
+    np.testing.assert_array_equal(got["Z"], batch["Z"].reshape(B * L, f))
+    np.testing.assert_array_equal(got["Vhat"], batch["Vhat"].reshape(B * L, d))
+    for k in range(B):
+        np.testing.assert_array_equal(got["states"][k], batch["states"][k])
+
+
+@pytest.mark.parametrize("cu", [[0, 3, 7, 11, 12], [0, 4, 8, 12], [0, 12]])
+def test_packed_short_documents_are_the_plain_mlp(cu):
+    """Documents no longer than a chunk are one chunk each, applied with the
+    reset weight before any update: O = Z W0_k^T per document (torch fp64),
+    whatever eta is.  Without the reset, documents after the first chunk
+    boundary of the packed row would see updates."""
+    T, d, f, C = 12, 5, 7, 4 if len(cu) > 2 else 12
+    inp = _inputs(1, T, d, f, seed=93)
+    nd = len(cu) - 1
+    w0 = torch.stack([inp["W_down0"] * (1.0 + 0.5 * k) for k in range(nd)])
+    pk = dict(inp)
+    pk["W_down0"] = w0
+    got = oracle.forward_packed(pk, cu, 0.8, C)["O"]
+    Z = _lib_gated_mlp_z(inp["H"][0], inp["W_gate"], inp["W_up"])
+    for k in range(nd):
+        ref = F.linear(Z[cu[k]:cu[k + 1]], _t64(w0[k]))
+        np.testing.assert_allclose(got[cu[k]:cu[k + 1]], ref.numpy(), rtol=1e-12, atol=1e-13)
+    if nd > 1:
+        # the same row with no reset (one long sequence) differs
+        whole = dict(inp)
+        noreset = oracle.forward(whole, 0.8, C)["O"][0]
+        assert np.abs(noreset - got).max() > 1e-3
+
+
+@pytest.mark.parametrize("pad_mode", [oracle.PAD_CHUNK, oracle.PAD_SEQUENCE])
+@pytest.mark.parametrize("which", ["H", "X0"])
+def test_packed_documents_do_not_leak(pad_mode, which):
+    """Perturbing one document's tokens leaves every other document's
+    output exactly unchanged (no state and no convolution tap crosses a
+    boundary), in both padding modes."""
+    cu = [0, 5, 13, 20]
+    inp = _inputs(1, 20, 4, 6, seed=95)
+    base = oracle.forward_packed(inp, cu, 0.5, 3, pad_mode=pad_mode)["O"]
+    for k in range(3):
+        pert = dict(inp)
+        x = inp[which].clone()
+        x[0, cu[k]:cu[k + 1]] += 1.0
+        pert[which] = x
+        got = oracle.forward_packed(pert, cu, 0.5, 3, pad_mode=pad_mode)["O"]
+        for j in range(3):
+            seg = slice(cu[j], cu[j + 1])
+            if j == k:
+                assert np.abs(got[seg] - base[seg]).max() > 1e-6
+            else:
+                np.testing.assert_array_equal(got[seg], base[seg])
+
+
+def test_packed_chunks_restart_at_each_document():
+    """Next-token target (W_target = I, taps (0, 0, 1)): inside document k
+    the chunks start at its first token, so Vhat_t = X0_{t+1} unless t is
+    the last token of its chunk or of its document, and each chunk's update
+    is the closed-form sum over its own tokens."""
+    cu, C, d, f = [0, 7, 17], 4, 3, 5
+    T = cu[-1]
+    inp = _inputs(1, T, d, f, seed=97)
+    inp["W_target"] = torch.eye(d)
+    inp["conv_w"] = torch.tensor([[0.0, 0.0, 1.0]] * d)
+    out = oracle.forward_packed(inp, cu, 0.5, C, want_z=True, want_vhat=True, want_states=True)
+    X0 = inp["X0"][0].double().numpy()
+    Z = out["Z"]
+    for k in range(2):
+        a, b = cu[k], cu[k + 1]
+        for t in range(a, b):
+            last = (t - a + 1) % C == 0 or t + 1 == b
+            np.testing.assert_array_equal(out["Vhat"][t], np.zeros(d) if last else X0[t + 1])
+        S = out["states"][k]
+        n = -(-(b - a) // C)
+        assert S.shape[0] == n + 1
+        for i in range(n):
+            lo, hi = a + i * C, min(a + (i + 1) * C, b)
+            dW = sum((np.outer(X0[t + 1], Z[t]) for t in range(lo, hi - 1)), np.zeros((d, f)))
+            np.testing.assert_allclose(S[i + 1] - S[i], 0.5 * dW, rtol=1e-12, atol=1e-12)
+
+
+def test_packed_token_rates_follow_their_document():
+    """Zero per-token rates over one document freeze its state; the other
+    documents are as with unit rates."""
+    cu = [0, 9, 16]
+    inp = _inputs(1, 16, 4, 5, seed=99)
+    ones = torch.ones(1, 16)
+    rates = ones.clone()
+    rates[0, 9:] = 0.0
+    ref = oracle.forward_packed(inp, cu, 0.3, 4, want_states=True, eta_tok=ones)
+    got = oracle.forward_packed(inp, cu, 0.3, 4, want_states=True, eta_tok=rates)
+    np.testing.assert_array_equal(got["O"][:9], ref["O"][:9])
+    np.testing.assert_array_equal(got["states"][0], ref["states"][0])
+    for s in got["states"][1]:
+        np.testing.assert_array_equal(s, got["states"][1][0])

@@ -49,25 +49,40 @@ def to_device(inp, dev, w0_dtype=torch.bfloat16):
     return g
 
 
+def packed_slots(cu, C):
+    """Snapshot slot of each packed document's first chunk, and the total."""
+    base, g = [], 0
+    for a, b in zip(cu, cu[1:]):
+        base.append(g)
+        g += -(-(b - a) // C)
+    return base, g
+
+
 def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
-        state_in=None, want_state=False, fused_conv=False, dual=False, eta_tok=None):
+        state_in=None, want_state=False, fused_conv=False, dual=False, eta_tok=None,
+        cu_seqlens=None):
     B, T, d = g["H"].shape
     f = g["W_gate"].shape[0]
     dev = g["H"].device
+    if cu_seqlens is None:
+        states, slots = B, -(-T // C)
+    else:
+        states, slots = len(cu_seqlens) - 1, packed_slots(cu_seqlens, C)[1]
     kw = {}
     if intermediates:
         kw["z_buf"] = torch.empty(B, T, f, dtype=torch.bfloat16, device=dev)
         kw["vhat_buf"] = torch.empty(B, T, d, dtype=torch.bfloat16, device=dev)
         if not dual:
-            kw["snap_buf"] = torch.empty(B, -(-T // C), d, f, dtype=torch.bfloat16, device=dev)
+            kw["snap_buf"] = torch.empty(B, slots, d, f, dtype=torch.bfloat16, device=dev)
     if want_state:
-        kw["state_out"] = torch.empty(B, d, f, dtype=torch.float32, device=dev)
+        kw["state_out"] = torch.empty(states, d, f, dtype=torch.float32, device=dev)
     if state_in is not None:
         kw["state_in"] = state_in
     out = ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"],
                        None if state_in is not None else g["W_down0"], g["W_target"],
                        g["conv_w"], eta, C, out_dtype=out_dtype, pad_mode=pad_mode,
-                       fused_conv=fused_conv, dual=dual, eta_tok=eta_tok, **kw)
+                       fused_conv=fused_conv, dual=dual, eta_tok=eta_tok,
+                       cu_seqlens=cu_seqlens, **kw)
     ittt.stream_status()
     res = {"O": out}
     res.update(kw)
@@ -213,6 +228,104 @@ def test_per_token_rates(cuda_device, fused_conv, dual):
 
 
 # --------------------------------------------------------------------------
+# Chunks and lengths that are not multiples of 64: the update masks the
+# token lines past a chunk's end, the apply stores ragged tiles row by row
+# --------------------------------------------------------------------------
+
+RAGGED = [
+    # B, T, d, f, C, eta
+    (1, 250, 64, 256, 100, 0.05),    # chunks 100, 100, 50; T not a multiple of 64
+    (2, 200, 72, 136, 48, 0.07),     # every chunk ends inside a 64-token stage
+    (1, 77, 200, 584, 13, 0.03),     # 13-token chunks (one 16-token slice each)
+    (2, 70, 64, 128, 1, 0.02),       # one token per chunk: per-token updates
+    (1, 333, 136, 264, 160, 0.1),    # chunks 160, 160, 13
+]
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", RAGGED)
+def test_ragged_chunks(cuda_device, B, T, d, f, C, eta):
+    inp = make_inputs(B, T, d, f, seed=900 + T + C)
+    ref = oracle.forward(inp, eta, C, want_z=True, want_vhat=True, want_states=True)
+    got = run(to_device(inp, cuda_device), eta, C, intermediates=True, want_state=True)
+    n = -(-T // C)
+    assert_parity(host(got["z_buf"]), ref["Z"], "Z")
+    assert_parity(host(got["vhat_buf"]), eta * ref["Vhat"], "eta * Vhat")
+    assert_parity(host(got["snap_buf"]), ref["states"][:, :n], "snapshots")
+    assert_parity(host(got["state_out"]), ref["states"][:, n], "final state")
+    assert_parity(host(got["O"]), ref["O"], "O")
+    o32 = run(to_device(inp, cuda_device), eta, C, out_dtype=torch.float32)["O"]
+    assert_parity(host(o32), ref["O"], "O (fp32 out)")
+
+
+# --------------------------------------------------------------------------
+# Packed documents (state reset at each document boundary)
+# --------------------------------------------------------------------------
+
+PACKED = [
+    # cu_seqlens, d, f, C, eta
+    ([0, 100, 356, 600], 72, 136, 64, 0.05),
+    ([0, 1, 65, 130, 400], 200, 584, 128, 0.05),
+    ([0, 37, 300, 301, 555, 700, 948, 1000, 1200, 1290], 64, 256, 96, 0.03),
+    ([0, 512, 1024], 128, 256, 256, 0.03),   # whole chunks only
+]
+
+
+def _packed_inputs(cu, d, f, seed):
+    inp = make_inputs(1, cu[-1], d, f, seed=seed)
+    return inp
+
+
+@pytest.mark.parametrize("cu,d,f,C,eta", PACKED)
+def test_packed_documents(cuda_device, cu, d, f, C, eta):
+    inp = _packed_inputs(cu, d, f, seed=950 + len(cu) + d)
+    ref = oracle.forward_packed(inp, cu, eta, C, want_z=True, want_vhat=True, want_states=True)
+    got = run(to_device(inp, cuda_device), eta, C, intermediates=True, want_state=True,
+              cu_seqlens=cu)
+    assert_parity(host(got["z_buf"])[0], ref["Z"], "Z")
+    assert_parity(host(got["vhat_buf"])[0], eta * ref["Vhat"], "eta * Vhat")
+    base, slots = packed_slots(cu, C)
+    snap = host(got["snap_buf"])[0]
+    want = np.concatenate([s[:-1] for s in ref["states"]])      # W_0..W_{n_k - 1} per document
+    assert snap.shape[0] == slots == want.shape[0]
+    assert_parity(snap, want, "snapshots")
+    assert_parity(host(got["state_out"]), np.stack([s[-1] for s in ref["states"]]),
+                  "final states")
+    assert_parity(host(got["O"])[0], ref["O"], "O")
+
+
+def test_packed_document_options(cuda_device):
+    """Per-document initial states, per-token rates, sequence padding and
+    fp32 output together."""
+    cu, d, f, C, eta = [0, 150, 151, 420, 640], 128, 256, 128, 0.05
+    inp = _packed_inputs(cu, d, f, seed=977)
+    nd = len(cu) - 1
+    w0 = torch.stack([inp["W_down0"] * (1.0 - 0.3 * k) for k in range(nd)])
+    rates = torch.rand(1, cu[-1], generator=torch.Generator().manual_seed(5)) + 0.5
+    pk = dict(inp)
+    pk["W_down0"] = w0
+    ref = oracle.forward_packed(pk, cu, eta, C, pad_mode=oracle.PAD_SEQUENCE, want_states=True,
+                                eta_tok=rates)
+    g = to_device(inp, cuda_device)
+    got = run(g, eta, C, pad_mode=ittt.PAD_SEQUENCE, out_dtype=torch.float32,
+              state_in=w0.to(cuda_device).contiguous(), want_state=True,
+              eta_tok=rates.to(cuda_device), cu_seqlens=cu)
+    assert_parity(host(got["O"])[0], ref["O"], "O")
+    assert_parity(host(got["state_out"]), np.stack([s[-1] for s in ref["states"]]),
+                  "final states")
+
+
+def test_packed_equals_separate_calls_bitwise(cuda_device):
+    """Each packed document gives bit for bit what a call on that document
+    alone gives (same kernels, same per-row reduction order)."""
+    cu, d, f, C, eta = [0, 200, 264, 700], 128, 256, 128, 0.05
+    g = to_device(_packed_inputs(cu, d, f, seed=978), cuda_device)
+    full = run(g, eta, C, cu_seqlens=cu)["O"]
+    for a, b in zip(cu, cu[1:]):
+        one = {k: (v[:, a:b].contiguous() if k in ("H", "X0") else v) for k, v in g.items()}
+        assert torch.equal(run(one, eta, C)["O"][0], full[0, a:b])
+
+
+# --------------------------------------------------------------------------
 # The dual schedule (scores Z Z^T instead of the fast-weight walk)
 # --------------------------------------------------------------------------
 
@@ -304,9 +417,9 @@ def test_status_and_argument_errors_on_device(cuda_device):
         ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
                      g["conv_w"], 0.1, 0)
     assert e.value.status == ittt.ERR_INVALID_ARG
-    with pytest.raises(ittt.IttError) as e:
+    with pytest.raises(ittt.IttError) as e:   # the fused conv needs 64-token multiples
         ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
-                     g["conv_w"], 0.1, 100)
+                     g["conv_w"], 0.1, 100, fused_conv=True)
     assert e.value.status == ittt.ERR_UNSUPPORTED
     ittt.stream_status()  # nothing recorded
 
