@@ -83,6 +83,9 @@ def parse_args():
                     help="compute the convolution inside the target GEMM")
     ap.add_argument("--dual", action="store_true",
                     help="dual form (scores Z Z^T) instead of the fast-weight walk")
+    ap.add_argument("--packed", action="store_true",
+                    help="pack the workload's B*T tokens into one row of documents with "
+                         "log-uniform lengths in [512, 16384] (state reset per document)")
     ap.add_argument("--eta-tok", action="store_true",
                     help="per-token learning-rate weights (seeded uniform [0.5, 1.5))")
     return ap.parse_args()
@@ -135,19 +138,21 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def phase_model(B, T, d, f, C, dual=False):
+def phase_model(B, T, d, f, C, dual=False, cu=None):
     """Algorithmic work per phase: ('tensor', FLOPs) or ('hbm', bytes).  The
     dual form's extra work (scores Z Z^T, S Vhat) is charged at the primal
-    form's FLOPs, the work the layer needs."""
-    n = -(-T // C)
+    form's FLOPs, the work the layer needs.  With packed documents (cu) B is
+    1, every document is chunked on its own and only the tokens before each
+    document's last chunk update."""
+    lens = [b - a for a, b in zip(cu, cu[1:])] if cu else [T] * B
+    upd_tokens = sum(L - (L - (-(-L // C) - 1) * C) for L in lens)
     return {
         "conv": ("hbm", 2.0 * B * T * d * 2 + d * 3 * 4),
         "target": ("tensor", 2.0 * B * T * d * d),
         "gateup": ("tensor", 4.0 * B * T * d * f),
-        "snapshot0": ("hbm", 1.0 * d * f * 2 + B * d * f * 2),
-        "update": ("tensor", 2.0 * B * (T - (T - (n - 1) * C)) * d * f),
+        "snapshot0": ("hbm", 1.0 * d * f * 2 + len(lens) * d * f * 2),
+        "update": ("tensor", 2.0 * upd_tokens * d * f),
         "apply": ("tensor", 2.0 * B * T * d * f),
-        "_n": n,
     }
 
 
@@ -217,6 +222,7 @@ def main():
     import torch.distributed as dist
 
     from chunk_wise_weight_gb300 import CONFIGS, counted_flops, ittt, make_inputs
+    from chunk_wise_weight_gb300.inputs import counted_flops_packed, packed_offsets
     from chunk_wise_weight_gb300 import build as lib_build
     from chunk_wise_weight_gb300.shard import barrier, max_over_ranks, shard_range
 
@@ -251,6 +257,13 @@ def main():
         g = torch.Generator().manual_seed(1234 + args.config + 1000 * first)
         inp["H"] = torch.randn(B, T, d, generator=g).to(torch.bfloat16).float()
         inp["X0"] = torch.randn(B, T, d, generator=g).to(torch.bfloat16).float()
+    cu = None
+    if args.packed:
+        # The same tokens as one packed row of documents.
+        cu = packed_offsets(B * T, seed=2468 + first)
+        inp["H"] = inp["H"].reshape(1, B * T, d)
+        inp["X0"] = inp["X0"].reshape(1, B * T, d)
+        B, T = 1, B * T
     bf = torch.bfloat16
     H = inp["H"].to(dev, bf)
     X0 = inp["X0"].to(dev, bf)
@@ -266,7 +279,7 @@ def main():
 
     def step(events=None):
         ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, stream=stream, events=events,
-                     fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates)
+                     fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates, cu_seqlens=cu)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -296,7 +309,7 @@ def main():
     value = tokens / (elapsed_ms / 1e3)
 
     # Per-phase device durations from the events between launches.
-    model = phase_model(B, T, d, f, C, args.dual)
+    model = phase_model(B, T, d, f, C, args.dual, cu)
     phases = {}
     for p, name in enumerate(ittt.PHASES):
         ms = sum(ev[k][2 * p].elapsed_time(ev[k][2 * p + 1]) for k in range(args.steps)) / args.steps
@@ -328,7 +341,7 @@ def main():
         roof = {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
                 "peak_kind": f"hbm_gbs ({peak_src})", "bytes_per_launch": work}
-    F = counted_flops(B, T, d, f, C)
+    F = counted_flops_packed(cu, d, f, C) if cu else counted_flops(B, T, d, f, C)
     layer_tflops = F / (ms_per_step * 1e-3) / 1e12
 
     # End to end through the public API with host buffers: every step copies
@@ -361,7 +374,8 @@ def main():
                 if k >= 2:
                     stream.wait_event(downloaded[j])  # O_j read back before reuse
                 ittt.forward(Hs[j], X0s[j], Wg, Wu, W0, Wt, cw, eta, C, Os[j], stream=stream,
-                             fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates)
+                             fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates,
+                             cu_seqlens=cu)
                 computed[j].record(stream)
                 down.wait_event(computed[j])
                 with torch.cuda.stream(down):
@@ -395,7 +409,11 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": cfg["name"], "B": B, "T": T, "d": d, "f": f, "C": C,
-                       "eta": eta, "chunks": T // C, "parallelism": f"batch x{world} (replicas)",
+                       "eta": eta, "chunks": -(-T // C) if cu is None else None,
+                       "parallelism": f"batch x{world} (replicas)",
+                       "packed_docs": None if cu is None else {
+                           "count": len(cu) - 1, "lengths": [b - a for a, b in zip(cu, cu[1:])],
+                           "mix": "log-uniform in [512, 16384] tokens, seeded"},
                        "conv": "fused into target GEMM" if args.fused_conv else "own kernel",
                        "schedule": "dual (scores Z Z^T)" if args.dual else "primal walk",
                        "eta_tok": "per-token rates" if args.eta_tok else None,
@@ -412,7 +430,8 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": ittt.launch_count(B, T, d, f, C) * args.steps,
+            # packed documents add the document-table staging kernel
+            "gpu_launches": (ittt.launch_count(B, T, d, f, C) + (1 if cu else 0)) * args.steps,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -57,16 +57,26 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// Pinned host buffers that packed-document tables are uploaded from.  A
-// buffer is rewritten only after the copy that last read it has finished,
-// so several calls can be in flight on the device.
+// Pinned, device-mapped host buffers that packed-document tables are staged
+// from.  A small kernel on the caller's stream copies a table into device
+// scratch: unlike a host-to-device memcpy it never queues behind the
+// caller's bulk uploads on the copy engines.  A buffer is rewritten only
+// after the kernel that last read it has finished, so several calls can be
+// in flight on the device.
 constexpr int kStagingSlots = 4;
 struct StagingSlot {
   void* host = nullptr;
+  int* dev = nullptr;  // device address of `host`
   size_t bytes = 0;
   cudaEvent_t done = nullptr;
   bool pending = false;
 };
+
+__global__ void __launch_bounds__(256)
+    stage_table_kernel(const int* __restrict__ src, int* __restrict__ dst, int count) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
 
 struct DeviceState {
   bool ready = false;
@@ -127,10 +137,11 @@ ittt_status device_state(DeviceState** out) {
   return ITTT_OK;
 }
 
-// Copies `bytes` of host data to device `dst` in stream order through the
-// device's pinned staging ring.
-ittt_status upload(DeviceState* ds, void* dst, const void* src, size_t bytes,
-                   cudaStream_t stream) {
+// Copies `count` ints of host data to device `dst` in stream order: into a
+// pinned staging buffer on the host, then by stage_table_kernel.
+ittt_status stage_table(DeviceState* ds, int* dst, const int* src, size_t count,
+                        cudaStream_t stream) {
+  const size_t bytes = count * sizeof(int);
   std::lock_guard<std::mutex> lock(g_mutex);
   StagingSlot& sl = ds->staging[ds->next_slot];
   ds->next_slot = (ds->next_slot + 1) % kStagingSlots;
@@ -147,15 +158,22 @@ ittt_status upload(DeviceState* ds, void* dst, const void* src, size_t bytes,
   if (sl.bytes < bytes) {
     if (sl.host) cudaFreeHost(sl.host);
     sl.host = nullptr;
+    sl.dev = nullptr;
     sl.bytes = 0;
     const size_t want = std::max(bytes, size_t(64) << 10);
-    e = cudaHostAlloc(&sl.host, want, cudaHostAllocDefault);
+    e = cudaHostAlloc(&sl.host, want, cudaHostAllocMapped | cudaHostAllocPortable);
     if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc (staging)");
+    void* dp = nullptr;
+    e = cudaHostGetDevicePointer(&dp, sl.host, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostGetDevicePointer (staging)");
+    sl.dev = static_cast<int*>(dp);
     sl.bytes = want;
   }
   memcpy(sl.host, src, bytes);
-  e = cudaMemcpyAsync(dst, sl.host, bytes, cudaMemcpyHostToDevice, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "document table upload");
+  const int blocks = int(std::min<size_t>((count + 255) / 256, 64));
+  stage_table_kernel<<<blocks, 256, 0, stream>>>(sl.dev, dst, int(count));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "document table staging");
   e = cudaEventRecord(sl.done, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord (staging)");
   sl.pending = true;
@@ -231,8 +249,10 @@ struct Plan {
   int64_t n = 0;       // chunks per sequence (regular)
   bool final_update = false;
   int n_udocs = 0;     // documents that run at least one update
+  int64_t ntiles = 0;  // 128-row tiles over all chunks (the apply's row units)
   // Packed: starts[ndocs+1] | chunk_base[ndocs+1] | chunk_doc[nslots] |
-  // upd_docs[n_udocs], uploaded into the scratch at L.table.
+  // tile_base[nslots+1] | upd_docs[n_udocs], staged into the scratch at
+  // L.table.
   std::vector<int> table;
   Layout L;
 };
@@ -301,26 +321,37 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
                      });
     P->n_udocs = int(upd.size());
     std::vector<int>& t = P->table;
-    t.resize(size_t(2 * (nd + 1) + slots + P->n_udocs));
+    t.resize(size_t(2 * (nd + 1) + 2 * slots + 1 + P->n_udocs));
     int* starts = t.data();
     int* base = starts + (nd + 1);
     int* cdoc = base + (nd + 1);
-    int* ud = cdoc + slots;
-    int64_t g = 0;
+    int* tbase = cdoc + slots;
+    int* ud = tbase + slots + 1;
+    int64_t g = 0, tiles = 0;
     for (int64_t k = 0; k <= nd; ++k) {
       starts[k] = int(cu[k]);
       base[k] = int(g);
       if (k < nd) {
-        const int64_t nk = (cu[k + 1] - cu[k] + chunk - 1) / chunk;
-        for (int64_t j = 0; j < nk; ++j) cdoc[g++] = int(k);
+        const int64_t L = cu[k + 1] - cu[k];
+        const int64_t nk = (L + chunk - 1) / chunk;
+        for (int64_t j = 0; j < nk; ++j) {
+          const int64_t len = std::min<int64_t>(chunk, L - j * chunk);
+          tbase[g] = int(tiles);
+          tiles += (len + 127) / 128;
+          cdoc[g++] = int(k);
+        }
       }
     }
+    tbase[slots] = int(tiles);
+    P->ntiles = tiles;
     for (int q = 0; q < P->n_udocs; ++q) ud[q] = upd[size_t(q)].second;
   } else {
     P->ndocs = B;
     P->n = (T + chunk - 1) / chunk;  // the last chunk may be partial
     P->nslots = B * P->n;
     P->n_udocs = (P->final_update || P->n > 1) ? int(B) : 0;
+    const int64_t last = T - (P->n - 1) * chunk;
+    P->ntiles = B * ((P->n - 1) * ((chunk + 127) / 128) + (last + 127) / 128);
   }
   // The fused convolution forms its A tile from 4-row groups inside one
   // chunk; the dual form's scores are blocked by 64-token chunks.
@@ -329,7 +360,7 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   if (P->dual && (chunk % 64 != 0 || T % chunk != 0))
     return fail(ITTT_ERR_UNSUPPORTED,
                 "the dual form needs chunk a multiple of 64 that divides T");
-  const int64_t apply_units = P->nslots * ((chunk + 127) / 128) * ((d + 255) / 256);
+  const int64_t apply_units = P->ntiles * ((d + 255) / 256);
   if (P->nslots * d >= (int64_t(1) << 31) || apply_units >= (int64_t(1) << 31))
     return fail(ITTT_ERR_UNSUPPORTED, "too many chunks for 32-bit tile coordinates");
 
@@ -483,22 +514,25 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   auto* snap = o.snap_buf ? static_cast<__nv_bfloat16*>(o.snap_buf->data)
                           : reinterpret_cast<__nv_bfloat16*>(ws + L.snap);
 
-  // Documents.
+  // Documents (the packed tables are staged at the start of the conv phase).
   ittt::DocMap docs;
   memset(&docs, 0, sizeof(docs));
   docs.ndocs = int(P.ndocs);
   docs.nchunks = int(P.nslots);
+  docs.ntiles = int(P.ntiles);
   docs.T = int(T);
   docs.n = int(P.n);
   docs.C = int(chunk);
+  docs.mtc = int((chunk + 127) / 128);
+  if (!P.packed) docs.tiles_per_seq = int(P.ntiles / B);
   const int* upd_docs = nullptr;
+  int* tab = reinterpret_cast<int*>(ws + L.table);
   if (P.packed) {
-    int* tab = reinterpret_cast<int*>(ws + L.table);
-    if ((s = upload(ds, tab, P.table.data(), P.table.size() * sizeof(int), stream))) return s;
     docs.starts = tab;
     docs.chunk_base = tab + (P.ndocs + 1);
     docs.chunk_doc = tab + 2 * (P.ndocs + 1);
-    upd_docs = docs.chunk_doc + P.nslots;
+    docs.tile_base = docs.chunk_doc + P.nslots;
+    upd_docs = docs.tile_base + P.nslots + 1;
   }
 
   // Tensor maps.
@@ -553,6 +587,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
 #define ITTT_STEP(call, name) \
   if (what == nullptr && (e = (call)) != cudaSuccess) what = name
   ITTT_STEP(rec(2 * ITTT_PHASE_CONV, stream), "event record");
+  if (what == nullptr && P.packed &&
+      (s = stage_table(ds, tab, P.table.data(), P.table.size(), stream)) != ITTT_OK)
+    return s;
   if (!fused) {
     ITTT_STEP(ittt::launch_conv(env, static_cast<const __nv_bfloat16*>(X0->data), cw, xc,
                                 int64_t(M), docs, int(d), int(o.pad_mode)),

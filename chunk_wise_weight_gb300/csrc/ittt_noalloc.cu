@@ -259,6 +259,9 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   docs.T = int(T);
   docs.n = int(n);
   docs.C = int(chunk);
+  docs.mtc = int((chunk + 127) / 128);
+  docs.tiles_per_seq = int((n - 1) * docs.mtc + (T - (n - 1) * chunk + 127) / 128);
+  docs.ntiles = int(B) * docs.tiles_per_seq;
   const bool w0_fp32 = W_down0->dtype == ITTT_FP32;
   cudaError_t e;
   const char* what = nullptr;

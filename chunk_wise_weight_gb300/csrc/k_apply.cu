@@ -4,9 +4,11 @@
 // parallel as in Method §3 stage 3).
 //
 // W_i is the bf16 snapshot the update kernel wrote into the chunk's slot
-// (a document's first slot holds W_0).  A work unit is (snapshot slot g,
-// 128-row tile of the chunk, 256-column tile of d_model).  Rows past the
-// chunk's end belong to another chunk: they are computed but not stored.
+// (a document's first slot holds W_0).  A work unit is (128-row tile of a
+// chunk, 256-column tile of d_model); only tiles that hold rows of their
+// chunk are enumerated (slot order), so short chunks leave no idle units in
+// the persistent schedule.  Rows past the chunk's end belong to another
+// chunk: they are computed but not stored.
 // Full tiles and 64-row halves leave through TMA stores; a tile that ends
 // elsewhere (a chunk or document length that is not a multiple of 64) is
 // written row by row with masked 16-byte stores.
@@ -24,7 +26,7 @@ struct ApplyParams {
   int out_fp32;
   DocMap docs;
   int d, f;
-  int mt_per_chunk, nt, kblocks;
+  int nt, kblocks;
 };
 
 struct ApplySched : SchedDefaults {
@@ -36,12 +38,11 @@ struct ApplySched : SchedDefaults {
   int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0;
 
   __device__ explicit ApplySched(const Params& pp) : p(pp) {}
-  __device__ int num_units() const { return p.docs.nchunks * p.mt_per_chunk * p.nt; }
+  __device__ int num_units() const { return p.docs.ntiles * p.nt; }
   __device__ void begin_unit(int u, int local) {
     const int nt = u % p.nt;
-    const int r = u / p.nt;
-    const int mt = r % p.mt_per_chunk;
-    const int g = r / p.mt_per_chunk;
+    int mt = 0;
+    const int g = p.docs.slot_of_tile(u / p.nt, &mt);
     const int k = p.docs.doc_of_chunk(g);
     const int i = g - p.docs.first_chunk(k);
     const int len = p.docs.len(k);
@@ -51,7 +52,6 @@ struct ApplySched : SchedDefaults {
     n0 = nt * kBN;
     acc = local & 1;
   }
-  // Row tiles past the end of a short chunk have nothing to do.
   __device__ int num_segments() const { return rows_valid > 0 ? 1 : 0; }
   __device__ int seg_acc(int) const { return acc; }
   __device__ int seg_kblocks(int) const { return p.kblocks; }
@@ -154,10 +154,9 @@ cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z, const CU
   p.docs = docs;
   p.d = d;
   p.f = f;
-  p.mt_per_chunk = (docs.C + kBM - 1) / kBM;
   p.nt = (d + kBN - 1) / kBN;
   p.kblocks = (f + kBK - 1) / kBK;
-  const int64_t units = int64_t(docs.nchunks) * p.mt_per_chunk * p.nt;
+  const int64_t units = int64_t(docs.ntiles) * p.nt;
   if (units == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(pipe_smem_bytes<ApplySched>()));

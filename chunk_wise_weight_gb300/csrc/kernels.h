@@ -29,11 +29,15 @@ struct DocMap {
   const int* starts;      // [ndocs + 1] device, or nullptr
   const int* chunk_base;  // [ndocs + 1] device, or nullptr
   const int* chunk_doc;   // [nchunks] device, or nullptr
+  const int* tile_base;   // [nchunks + 1] device: 128-row tiles before slot g, or nullptr
   int ndocs;              // documents (B when regular)
   int nchunks;            // snapshot slots over all documents
+  int ntiles;             // 128-row tiles over all chunks
   int T;                  // tokens per sequence (regular) / in the pack
   int n;                  // chunks per sequence (regular)
   int C;
+  int mtc;                // 128-row tiles of a full chunk (regular)
+  int tiles_per_seq;      // 128-row tiles of a sequence (regular)
 
   __host__ __device__ bool packed() const { return starts != nullptr; }
 #ifdef __CUDACC__
@@ -49,6 +53,24 @@ struct DocMap {
   }
   __device__ __forceinline__ int doc_of_chunk(int g) const {
     return chunk_doc ? __ldg(chunk_doc + g) : g / n;
+  }
+  // Snapshot slot g and row tile mt (of 128 rows within the chunk) of the
+  // t-th non-empty row tile, over all chunks in slot order.
+  __device__ __forceinline__ int slot_of_tile(int t, int* mt) const {
+    if (!tile_base) {
+      const int b = t / tiles_per_seq;
+      const int r = t - b * tiles_per_seq;
+      const int i = min(r / mtc, n - 1);
+      *mt = r - i * mtc;
+      return b * n + i;
+    }
+    int lo = 0, hi = nchunks;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(tile_base + mid) <= t) lo = mid; else hi = mid;
+    }
+    *mt = t - __ldg(tile_base + lo);
+    return lo;
   }
   // Document holding token row r (binary search over the starts).
   __device__ __forceinline__ int doc_of_token(int r) const {

@@ -18,6 +18,8 @@ so that the GPU path (bf16 in) and the oracle (fp64) see identical values.
 """
 from __future__ import annotations
 
+import math
+
 import torch
 
 # Named workloads: (batch, tokens, d_model, d_ff, chunk, eta, input dtype).
@@ -82,3 +84,26 @@ def counted_flops(B: int, T: int, d: int, f: int, C: int) -> float:
     n = -(-T // C)
     last = T - (n - 1) * C
     return float(B) * (T * (4 * d * f + 2 * d * d + 2 * d * f) + (T - last) * 2 * d * f)
+
+
+def packed_offsets(total: int, seed: int, lo: int = 512, hi: int = 16384) -> list[int]:
+    """Document offsets (cu_seqlens) for `total` tokens packed in one row.
+
+    Lengths are drawn log-uniformly in [lo, hi] tokens (torch CPU generator,
+    this seed) until the row is full; the last document takes the remainder.
+    The pages give no document-length mix; this spreads lengths over the
+    chunk sizes they use (a few hundred to many thousand tokens).
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    cu = [0]
+    while cu[-1] < total:
+        u = float(torch.rand((), generator=g))
+        n = int(round(math.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))))
+        cu.append(min(total, cu[-1] + max(1, n)))
+    return cu
+
+
+def counted_flops_packed(cu_seqlens, d: int, f: int, C: int) -> float:
+    """counted_flops summed over packed documents (each chunked on its own)."""
+    return sum(counted_flops(1, b - a, d, f, C) for a, b in zip(cu_seqlens, cu_seqlens[1:]))

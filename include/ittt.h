@@ -106,10 +106,11 @@ typedef struct {
  *              reset at document boundaries (Method §3, causality and
  *              boundary handling) -- its chunks start at its first token,
  *              its last chunk may be shorter, and no convolution tap crosses
- *              into another document.  Read during the call only (the
- *              derived tables go to the device through a pinned staging
- *              buffer, so such a call cannot be captured into a CUDA graph).
- *              Not combinable with ITTT_FLAG_FUSED_CONV or ITTT_FLAG_DUAL.
+ *              into another document.  Read during the call only: the
+ *              derived tables are written to a pinned, device-mapped host
+ *              buffer that one extra kernel copies into device scratch, so
+ *              such a call cannot be captured into a CUDA graph.  Not
+ *              combinable with ITTT_FLAG_FUSED_CONV or ITTT_FLAG_DUAL.
  *   num_docs   number of packed documents (0 when cu_seqlens is NULL).
  *   state_in   fp32 [S,d,f]: per-sequence (S = B) or per-document
  *              (S = num_docs) initial fast weight.  Replaces W_down0 (which
@@ -274,6 +275,7 @@ ITTT_API int32_t ittt_version(void);
 /*
  * Kernel launches one ittt_forward / ittt_forward_ex call makes for these
  * sizes with default options (for launch accounting; 0 if unsupported).
+ * Packed documents add one (the table staging kernel).
  */
 ITTT_API int32_t ittt_launch_count(int64_t B, int64_t T, int64_t d, int64_t f,
                           int64_t chunk);
