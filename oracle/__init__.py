@@ -70,6 +70,9 @@ def _load():
         lib.oracle_forward_prefix.argtypes = [
             _i64, _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp,
             _i64, _fp, _fp, _fp, _dp, _dp]
+        lib.oracle_forward_l2norm.argtypes = [
+            _i64, _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp,
+            _i64, _fp, _fp, _fp, _dp, _dp]
         lib.oracle_forward_dual.argtypes = [
             _i64, _i64, _i64, _i64, _i64, _dbl, _int, _fp, _fp, _fp, _fp, _fp,
             _i64, _fp, _fp, _fp, _dp]
@@ -144,16 +147,30 @@ def _chunks(T: int, chunk: int) -> int:
 
 def forward(inp, eta: float, chunk: int, pad_mode: int = PAD_CHUNK,
             want_z: bool = False, want_vhat: bool = False,
-            want_states: bool = False, eta_tok=None) -> dict:
+            want_states: bool = False, eta_tok=None, l2norm: bool = False) -> dict:
     """Sequential apply-then-update loop over chunks (the defining form).
 
     Returns {"O": [B,T,d]} plus optional "Z" [B,T,f], "Vhat" [B,T,d] and
     "states" [B,n+1,d,f] (W^(0)..W^(n)), all float64.  eta_tok: optional
-    per-token learning-rate weights [B,T].
+    per-token learning-rate weights [B,T].  l2norm: normalise every updated
+    state row by row (the normalised update rule; Z and Vhat are then not
+    returned).
     """
     H, X0, Wg, Wu, W0, Wt, cw, B, T, d, f, w0s = _unpack(inp)
     n = _chunks(T, chunk)
     et = _eta_tok(eta_tok, B, T)
+    if l2norm:
+        if want_z or want_vhat:
+            raise ValueError("the normalised form returns O and the states only")
+        O = np.zeros((B, T, d), np.float64)
+        S = np.zeros((B, n + 1, d, f), np.float64) if want_states else None
+        _load().oracle_forward_l2norm(
+            B, T, d, f, chunk, float(eta), pad_mode, _fptr(H), _fptr(X0), _fptr(Wg),
+            _fptr(Wu), _fptr(W0), w0s, _fptr(Wt), _fptr(cw), _fptr(et), _dptr(O), _dptr(S))
+        out = {"O": O}
+        if want_states:
+            out["states"] = S
+        return out
     O = np.zeros((B, T, d), np.float64)
     Z = np.zeros((B, T, f), np.float64) if want_z else None
     V = np.zeros((B, T, d), np.float64) if want_vhat else None
@@ -297,7 +314,7 @@ def first_chunk_rows(H, W_gate, W_up, w0, rows) -> np.ndarray:
 
 def forward_packed(inp, cu_seqlens, eta: float, chunk: int, pad_mode: int = PAD_CHUNK,
                    want_z: bool = False, want_vhat: bool = False, want_states: bool = False,
-                   eta_tok=None) -> dict:
+                   eta_tok=None, l2norm: bool = False) -> dict:
     """Documents packed along one token axis, the fast weight reset to W_0 at
     every document boundary ("[논문리뷰] In-Place Test-Time Training",
     Method §3, causality and boundary handling): document k, the tokens
@@ -329,7 +346,8 @@ def forward_packed(inp, cu_seqlens, eta: float, chunk: int, pad_mode: int = PAD_
         doc["H"], doc["X0"] = H[a:b][None], X0[a:b][None]
         doc["W_down0"] = W0[k] if W0.ndim == 3 else W0
         r = forward(doc, eta, chunk, pad_mode, want_z=want_z, want_vhat=want_vhat,
-                    want_states=want_states, eta_tok=None if et is None else et[a:b][None])
+                    want_states=want_states, eta_tok=None if et is None else et[a:b][None],
+                    l2norm=l2norm)
         O[a:b] = r["O"][0]
         if want_z:
             Z[a:b] = r["Z"][0]

@@ -41,6 +41,10 @@
  *     grad sum_t eta_tok[t] L_t as in the large-chunk update of [P2]
  *     ("[논문리뷰] Test-Time Training Done Right", Large-Chunk TTT Layer,
  *     per-token eta_i); eta_tok == 1 is the plain update.
+ *   - Fast-weight L2 normalisation (optional, oracle_forward_l2norm): the
+ *     normalised update of [P2] (Non-Linear Update of Fast-Weight),
+ *     W <- L2-Normalize(W + eta * dW), each row of W_down divided by its
+ *     norm over the f inputs (floor 1e-12); W_down0 itself is used as given.
  *   - When C does not divide T the last chunk is the shorter remainder
  *     (the pages only use equal chunks; a stream whose length is not a
  *     multiple of C ends with a partial chunk).  Chunk-edge padding then
@@ -236,6 +240,70 @@ void oracle_forward_sequential(int64_t B, int64_t T, int64_t d, int64_t f,
     if (Z_out) memcpy(Z_out + b * T * f, Z, (size_t)(T * f) * sizeof(double));
     if (Vhat_out)
       memcpy(Vhat_out + b * T * d, Vhat, (size_t)(T * d) * sizeof(double));
+  }
+  free(Z);
+  free(Vhat);
+  free(W);
+  free(dW);
+}
+
+/*
+ * Fast-weight L2 normalisation ([P2] "[논문리뷰] Test-Time Training Done
+ * Right", Non-Linear Update of Fast-Weight, fast-weight normalisation:
+ * weight-update(W, g) = L2-Normalize(W - g), taken along the weight's input
+ * dimension).  W_down maps the f-dimensional Z to the d-dimensional output,
+ * so its input dimension is f: each row m is divided by its L2 norm over
+ * the f inputs.  A zero row is divided by 1e-12 instead (the usual floor).
+ */
+static void l2_normalize_rows(int64_t d, int64_t f, double* W) {
+  for (int64_t m = 0; m < d; ++m) {
+    double ss = 0.0;
+    for (int64_t j = 0; j < f; ++j) ss += W[m * f + j] * W[m * f + j];
+    double norm = sqrt(ss);
+    if (norm < 1e-12) norm = 1e-12;
+    for (int64_t j = 0; j < f; ++j) W[m * f + j] /= norm;
+  }
+}
+
+/*
+ * The sequential layer with the normalised update rule of [P2] applied to
+ * In-Place TTT's fast weight: every updated state is normalised row by row,
+ *     W^(0)   = W_down0                      (used as given)
+ *     O_[i]   = Z_[i] (W^(i))^T
+ *     W^(i+1) = L2-Normalize(W^(i) + eta * Vhat_[i]^T Z_[i]).
+ * The gradient step inside is the one of oracle_forward_sequential (the
+ * pages' L2-Normalize(W - g) with g the gradient of L = -<Z W^T, Vhat>_F).
+ * The normalisation makes the update non-additive: there is no prefix or
+ * dual form.  Same arguments as oracle_forward_sequential, without the Z
+ * and Vhat outputs.
+ */
+void oracle_forward_l2norm(int64_t B, int64_t T, int64_t d, int64_t f, int64_t C,
+                           double eta, int pad_mode, const float* H, const float* X0,
+                           const float* W_gate, const float* W_up, const float* W_down0,
+                           int64_t w0_batch_stride, const float* W_target,
+                           const float* conv_w, const float* eta_tok, double* O,
+                           double* states_out) {
+  const int64_t n = num_chunks(T, C);
+  const int64_t df = d * f;
+  double* Z = (double*)malloc((size_t)(T * f) * sizeof(double));
+  double* Vhat = (double*)malloc((size_t)(T * d) * sizeof(double));
+  double* W = (double*)malloc((size_t)df * sizeof(double));
+  double* dW = (double*)malloc((size_t)df * sizeof(double));
+  for (int64_t b = 0; b < B; ++b) {
+    sequence_intermediates(T, d, f, C, pad_mode, H + b * T * d, X0 + b * T * d,
+                           W_gate, W_up, W_target, conv_w, Z, Vhat);
+    const float* et = eta_tok ? eta_tok + b * T : NULL;
+    for (int64_t e = 0; e < df; ++e) W[e] = (double)W_down0[b * w0_batch_stride + e];
+    if (states_out) memcpy(states_out + (b * (n + 1)) * df, W, (size_t)df * sizeof(double));
+    for (int64_t i = 0; i < n; ++i) {
+      const int64_t Cn = chunk_len(T, C, i);
+      apply_chunk(i * C, Cn, d, f, Z, W, O + b * T * d);
+      chunk_delta(i * C, Cn, d, f, Vhat, Z, et, dW);
+      for (int64_t e = 0; e < df; ++e) W[e] = W[e] + eta * dW[e];
+      l2_normalize_rows(d, f, W);
+      if (states_out)
+        memcpy(states_out + (b * (n + 1) + i + 1) * df, W, (size_t)df * sizeof(double));
+    }
   }
   free(Z);
   free(Vhat);

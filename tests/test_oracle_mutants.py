@@ -47,6 +47,14 @@ MUTANTS = [
      "S[i * df + e] = S[(i - 1) * df + e] + dWs[(i < n ? i : n - 1) * df + e];"),
     ("dual_includes_current_chunk", "for (int64_t s = 0; s < i * C; ++s) { /* every token",
      "for (int64_t s = 0; s < (i + 1) * C; ++s) { /* every token"),
+    ("l2norm_skipped", "      l2_normalize_rows(d, f, W);\n", "\n"),
+    ("l2norm_over_columns",
+     "    for (int64_t j = 0; j < f; ++j) ss += W[m * f + j] * W[m * f + j];",
+     "    for (int64_t j = 0; j < d; ++j) ss += W[j * f + (m % f)] * W[j * f + (m % f)];"),
+    ("l2norm_applied_to_initial_weight",
+     "    if (states_out) memcpy(states_out + (b * (n + 1)) * df, W, (size_t)df * sizeof(double));",
+     "    l2_normalize_rows(d, f, W);\n"
+     "    if (states_out) memcpy(states_out + (b * (n + 1)) * df, W, (size_t)df * sizeof(double));"),
     ("state_entries_skip_eta",
      "out[q * (n + 1) + i + 1] = (double)w0[m * f + j] + eta * sum;",
      "out[q * (n + 1) + i + 1] = (double)w0[m * f + j] + sum;"),

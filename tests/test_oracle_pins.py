@@ -551,3 +551,90 @@ def test_packed_token_rates_follow_their_document():
     np.testing.assert_array_equal(got["states"][0], ref["states"][0])
     for s in got["states"][1]:
         np.testing.assert_array_equal(s, got["states"][1][0])
+
+
+# --------------------------------------------------------------------------
+# Fast-weight L2 normalisation ("[논문리뷰] Test-Time Training Done Right",
+# Non-Linear Update of Fast-Weight): W <- L2-Normalize(W + eta dW), rows of
+# W_down normalised over their f inputs
+# --------------------------------------------------------------------------
+
+def test_l2norm_first_update_matches_library():
+    """The first update, from library pieces: torch F.normalize (dim=1, the
+    input dimension of W_down [d, f]) of W_0 + eta Vhat_[0]^T Z_[0], with
+    Z and Vhat from torch's silu/linear/conv1d."""
+    T, C, d, f, eta = 12, 4, 5, 7, 0.6
+    inp = _inputs(1, T, d, f, seed=101)
+    out = oracle.forward(inp, eta, C, want_states=True, l2norm=True)
+    Z = _lib_gated_mlp_z(inp["H"][0], inp["W_gate"], inp["W_up"])
+    V = _lib_conv_target(inp["X0"][0], inp["conv_w"], inp["W_target"], C, oracle.PAD_CHUNK)
+    W1 = F.normalize(_t64(inp["W_down0"]) + eta * V[:C].T @ Z[:C], dim=1)
+    np.testing.assert_allclose(out["states"][0, 1], W1.numpy(), rtol=1e-12, atol=1e-13)
+    # the first chunk is applied with W_0 as given
+    np.testing.assert_allclose(out["O"][0, :C], (Z[:C] @ _t64(inp["W_down0"]).T).numpy(),
+                               rtol=1e-12, atol=1e-13)
+
+
+def test_l2norm_rows_of_every_updated_state_are_unit():
+    inp = _inputs(2, 13, 4, 9, seed=103)
+    S = oracle.forward(inp, 0.2, 4, want_states=True, l2norm=True)["states"]
+    norms = np.linalg.norm(S[:, 1:], axis=3)
+    np.testing.assert_allclose(norms, np.ones_like(norms), rtol=1e-13)
+    assert abs(np.linalg.norm(S[0, 0], axis=1) - 1.0).max() > 1e-3   # W_0 is not normalised
+
+
+def test_l2norm_eta_zero_applies_the_normalised_initial_weight():
+    """eta = 0: every update just normalises, and normalising twice changes
+    nothing, so chunks after the first see F.normalize(W_0, dim=1)."""
+    T, C, d, f = 12, 4, 5, 6
+    inp = _inputs(1, T, d, f, seed=105)
+    got = oracle.forward(inp, 0.0, C, l2norm=True)["O"][0]
+    Z = _lib_gated_mlp_z(inp["H"][0], inp["W_gate"], inp["W_up"])
+    W0 = _t64(inp["W_down0"])
+    ref = torch.cat([Z[:C] @ W0.T, Z[C:] @ F.normalize(W0, dim=1).T])
+    np.testing.assert_allclose(got, ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_l2norm_first_update_is_scale_invariant():
+    """Scaling W_0 and eta by the same a > 0 scales the first update's
+    argument by a, which the row normalisation removes: W^(1) and the
+    output of chunk 1 are unchanged, chunk 0's output scales by a, and the
+    later states (whose steps start from a unit-row W^(1) with a step a
+    times larger) change."""
+    T, C, a = 12, 4, 4.0   # a power of two: a * W_0 is exact in float32
+    inp = _inputs(1, T, 4, 6, seed=107)
+    ref = oracle.forward(inp, 0.3, C, want_states=True, l2norm=True)
+    sc = dict(inp)
+    sc["W_down0"] = inp["W_down0"] * a
+    got = oracle.forward(sc, 0.3 * a, C, want_states=True, l2norm=True)
+    np.testing.assert_allclose(got["states"][:, 1], ref["states"][:, 1], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(got["O"][:, C:2 * C], ref["O"][:, C:2 * C], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(got["O"][:, :C], a * ref["O"][:, :C], rtol=1e-12, atol=1e-12)
+    assert np.abs(got["states"][:, 2] - ref["states"][:, 2]).max() > 1e-3
+
+
+def test_l2norm_differs_from_the_plain_update_and_keeps_causality():
+    inp = _inputs(1, 16, 4, 6, seed=109)
+    plain = oracle.forward(inp, 0.5, 4)["O"]
+    norm = oracle.forward(inp, 0.5, 4, l2norm=True)["O"]
+    np.testing.assert_array_equal(norm[:, :4], plain[:, :4])
+    assert np.abs(norm[:, 4:] - plain[:, 4:]).max() > 1e-3
+    for which in ("H", "X0"):
+        pert = dict(inp)
+        x = inp[which].clone()
+        x[0, 9] += 1.0
+        pert[which] = x
+        got = oracle.forward(pert, 0.5, 4, l2norm=True)["O"]
+        np.testing.assert_array_equal(got[:, :9], norm[:, :9])
+
+
+def test_l2norm_packed_equal_documents_are_the_batch():
+    B, L, d, f, C = 2, 10, 4, 6, 4
+    inp = _inputs(B, L, d, f, seed=111)
+    batch = oracle.forward(inp, 0.4, C, want_states=True, l2norm=True)
+    packed = dict(inp)
+    packed["H"], packed["X0"] = inp["H"].reshape(1, B * L, d), inp["X0"].reshape(1, B * L, d)
+    got = oracle.forward_packed(packed, [0, L, 2 * L], 0.4, C, want_states=True, l2norm=True)
+    np.testing.assert_array_equal(got["O"], batch["O"].reshape(B * L, d))
+    for k in range(B):
+        np.testing.assert_array_equal(got["states"][k], batch["states"][k])
