@@ -86,6 +86,8 @@ def parse_args():
     ap.add_argument("--packed", action="store_true",
                     help="pack the workload's B*T tokens into one row of documents with "
                          "log-uniform lengths in [512, 16384] (state reset per document)")
+    ap.add_argument("--l2norm", action="store_true",
+                    help="normalise every updated fast weight row by row (one launch per chunk)")
     ap.add_argument("--eta-tok", action="store_true",
                     help="per-token learning-rate weights (seeded uniform [0.5, 1.5))")
     return ap.parse_args()
@@ -154,6 +156,17 @@ def phase_model(B, T, d, f, C, dual=False, cu=None):
         "update": ("tensor", 2.0 * upd_tokens * d * f),
         "apply": ("tensor", 2.0 * B * T * d * f),
     }
+
+
+def launches_per_step(B, T, C, cu, l2norm):
+    """Kernel launches of one forward: conv, target, gate/up, snapshot 0, the
+    update walk (one launch, or with L2 normalisation one per chunk that
+    updates plus a finalising launch), apply; packed documents add the
+    table-staging kernel."""
+    lens = [b - a for a, b in zip(cu, cu[1:])] if cu else [T] * B
+    steps = max(-(-L // C) - 1 for L in lens)
+    walk = (steps + 1 if l2norm else 1) if steps > 0 else 0
+    return 5 + walk + (1 if cu else 0)
 
 
 def init_dist(args):
@@ -279,7 +292,8 @@ def main():
 
     def step(events=None):
         ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, stream=stream, events=events,
-                     fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates, cu_seqlens=cu)
+                     fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates, cu_seqlens=cu,
+                     l2norm=args.l2norm)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -375,7 +389,7 @@ def main():
                     stream.wait_event(downloaded[j])  # O_j read back before reuse
                 ittt.forward(Hs[j], X0s[j], Wg, Wu, W0, Wt, cw, eta, C, Os[j], stream=stream,
                              fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates,
-                             cu_seqlens=cu)
+                             cu_seqlens=cu, l2norm=args.l2norm)
                 computed[j].record(stream)
                 down.wait_event(computed[j])
                 with torch.cuda.stream(down):
@@ -417,6 +431,7 @@ def main():
                        "conv": "fused into target GEMM" if args.fused_conv else "own kernel",
                        "schedule": "dual (scores Z Z^T)" if args.dual else "primal walk",
                        "eta_tok": "per-token rates" if args.eta_tok else None,
+                       "update_rule": "L2-normalised rows" if args.l2norm else "additive",
                        "l2": "inputs larger than L2: H+X0 and Z are several GB per step"},
             "layer_tflops": round(layer_tflops, 1),
             "layer_frac_of_peak": {
@@ -430,8 +445,7 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clocks,
             "e2e": e2e,
-            # packed documents add the document-table staging kernel
-            "gpu_launches": (ittt.launch_count(B, T, d, f, C) + (1 if cu else 0)) * args.steps,
+            "gpu_launches": launches_per_step(B, T, C, cu, args.l2norm) * args.steps,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -234,7 +234,8 @@ ittt_status check_sizes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chun
 
 // --------------------------------------------------------------- planning
 struct Layout {
-  size_t z = 0, vhat = 0, xc = 0, snap = 0, scores = 0, w0b = 0, table = 0, total = 0;
+  size_t z = 0, vhat = 0, xc = 0, snap = 0, scores = 0, w0b = 0, table = 0, state = 0,
+         partial = 0, total = 0;
 };
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -243,13 +244,16 @@ size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
 // snapshot slots, the packed-document table and the scratch layout.
 struct Plan {
   int64_t B = 0, T = 0, d = 0, f = 0, C = 0, M = 0;
-  bool fused = false, dual = false, packed = false;
+  bool fused = false, dual = false, packed = false, l2norm = false;
   int64_t ndocs = 0;   // documents: B, or the packed count
   int64_t nslots = 0;  // snapshot slots = chunks over all documents
   int64_t n = 0;       // chunks per sequence (regular)
   bool final_update = false;
   int n_udocs = 0;     // documents that run at least one update
   int64_t ntiles = 0;  // 128-row tiles over all chunks (the apply's row units)
+  // L2 normalisation: launches of the walk, and how many documents are
+  // still updating at each (documents sorted by update count).
+  std::vector<int> active;
   // Packed: starts[ndocs+1] | chunk_base[ndocs+1] | chunk_doc[nslots] |
   // tile_base[nslots+1] | upd_docs[n_udocs], staged into the scratch at
   // L.table.
@@ -265,7 +269,7 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   if (s != ITTT_OK) return s;
   if (o.pad_mode != ITTT_PAD_CHUNK && o.pad_mode != ITTT_PAD_SEQUENCE)
     return fail(ITTT_ERR_INVALID_ARG, "pad_mode %d", int(o.pad_mode));
-  if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV | ITTT_FLAG_DUAL))
+  if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV | ITTT_FLAG_DUAL | ITTT_FLAG_L2_NORM))
     return fail(ITTT_ERR_INVALID_ARG, "unknown flags 0x%x", unsigned(o.flags));
   P->B = B;
   P->T = T;
@@ -276,6 +280,10 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   P->fused = (o.flags & ITTT_FLAG_FUSED_CONV) != 0;
   P->dual = (o.flags & ITTT_FLAG_DUAL) != 0;
   P->packed = o.cu_seqlens != nullptr;
+  P->l2norm = (o.flags & ITTT_FLAG_L2_NORM) != 0;
+  if (P->l2norm && P->dual)
+    return fail(ITTT_ERR_UNSUPPORTED,
+                "the normalised update has no dual form (the update is not additive)");
   P->final_update = o.state_out != nullptr;
   if (P->dual && (o.state_out || o.snap_buf))
     return fail(ITTT_ERR_UNSUPPORTED,
@@ -320,6 +328,11 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
                        return a.first < b.first;
                      });
     P->n_udocs = int(upd.size());
+    if (P->l2norm && !upd.empty()) {
+      P->active.assign(size_t(-upd[0].first), 0);
+      for (const auto& u : upd)
+        for (int64_t i = 0; i < -u.first; ++i) ++P->active[size_t(i)];
+    }
     std::vector<int>& t = P->table;
     t.resize(size_t(2 * (nd + 1) + 2 * slots + 1 + P->n_udocs));
     int* starts = t.data();
@@ -350,6 +363,8 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
     P->n = (T + chunk - 1) / chunk;  // the last chunk may be partial
     P->nslots = B * P->n;
     P->n_udocs = (P->final_update || P->n > 1) ? int(B) : 0;
+    if (P->l2norm && P->n_udocs > 0)
+      P->active.assign(size_t(P->final_update ? P->n : P->n - 1), int(B));
     const int64_t last = T - (P->n - 1) * chunk;
     P->ntiles = B * ((P->n - 1) * ((chunk + 127) / 128) + (last + 127) / 128);
   }
@@ -383,6 +398,10 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
     if (o.state_in || !w0_bf16) L.w0b = take(size_t(o.state_in ? B : 1) * d * f * 2);
   }
   if (P->packed) L.table = take(P->table.size() * sizeof(int));
+  if (P->l2norm && P->n_udocs > 0) {
+    L.state = take(size_t(P->ndocs) * d * f * 4);
+    L.partial = take(size_t(2) * P->ndocs * ((f + 511) / 512) * d * 4);
+  }
   L.total = off;
   return ITTT_OK;
 }
@@ -638,7 +657,26 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     ua.w0_bstride = w0_bstride;
     ua.state_out = o.state_out ? static_cast<float*>(o.state_out->data) : nullptr;
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");
-    ITTT_STEP(ittt::launch_update(env, tm_vmn, tm_zmn, tm_ss, ua), "update launch");
+    if (P.l2norm) {
+      ittt::NormUpdateArgs na;
+      na.docs = docs;
+      na.upd_docs = upd_docs;
+      na.n_udocs = P.n_udocs;
+      na.n_steps = int(P.active.size());
+      na.active = P.active.data();
+      na.d = int(d);
+      na.f = int(f);
+      na.w0 = w0;
+      na.w0_fp32 = w0_fp32;
+      na.w0_bstride = w0_bstride;
+      na.state = reinterpret_cast<float*>(ws + L.state);
+      na.partial = reinterpret_cast<float*>(ws + L.partial);
+      na.snap = snap;
+      na.state_out = ua.state_out;
+      ITTT_STEP(ittt::launch_norm_update(env, tm_vmn, tm_zmn, na), "normalised update launch");
+    } else {
+      ITTT_STEP(ittt::launch_update(env, tm_vmn, tm_zmn, tm_ss, ua), "update launch");
+    }
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
     ITTT_STEP(ittt::launch_apply(env, tm_zk, tm_snap, tm_os, out->data,

@@ -30,6 +30,64 @@ namespace {
 
 constexpr uint32_t kMnBoxBytes = 64 * 64 * 2;  // one {64 cols, 64 tokens} box
 
+// One 64-token stage of the update: eta*Vhat^T rows m0..m0+127 (A, two
+// boxes) and Z columns n0..n0+255 (B, four boxes) of tokens tok..tok+63.
+__device__ __forceinline__ void load_update_stage(const CUtensorMap& tm_v, const CUtensorMap& tm_z,
+                                                  uint8_t* stage, uint64_t* bar, int m0, int n0,
+                                                  int tok) {
+  uint8_t* sb = stage + kATileBytes;
+  tma_load_2d(stage, &tm_v, bar, m0, tok);
+  tma_load_2d(stage + kMnBoxBytes, &tm_v, bar, m0 + 64, tok);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kMnBoxBytes, &tm_z, bar, n0 + 64 * q, tok);
+}
+
+// Token lines [from, to) of both operands' boxes read zero: tokens past the
+// chunk's end (another chunk's) must not enter its sum.  A whole 128-byte
+// line is one token, so the swizzle does not matter here.
+__device__ __forceinline__ void clear_token_lines(uint8_t* stage, int from, int to) {
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+  for (int box = 0; box < 6; ++box) {
+    uint4* line = reinterpret_cast<uint4*>(stage + box * kMnBoxBytes);
+#pragma unroll 1
+    for (int t = from; t < to; ++t)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) line[t * 8 + c] = zero;
+  }
+}
+
+// MN-major, 128-byte swizzle: a 16-token slice is 16 lines of 128 B; the
+// 64-column groups of the tile are one box (lbo) apart.
+__device__ __forceinline__ uint64_t mn_desc(uint32_t base, int k) {
+  return sdesc_sw128(base + uint32_t(k) * 2048u, kMnBoxBytes, 1024u);
+}
+
+// Eight fp32 values of the initial state W_0 (bf16 or fp32 source; zeros
+// outside the [d, f] state).
+__device__ __forceinline__ void load_w0_8(const void* w0, bool fp32, size_t off, bool ok,
+                                          float* w) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w[j] = 0.f;
+  if (!ok) return;
+  if (fp32) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(w0) + off);
+    const float4 lo = __ldg(src), hi = __ldg(src + 1);
+    w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
+    w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
+  } else {
+    const uint4 raw =
+        __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(w0) + off));
+    const uint32_t r4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f2 = unpack_bf16x2(r4[j]);
+      w[2 * j] = f2.x;
+      w[2 * j + 1] = f2.y;
+    }
+  }
+}
+
 struct UpdateParams {
   CUtensorMap tm_v;  // eta*Vhat [M, d]  box {64, 64}
   CUtensorMap tm_z;  // Z        [M, f]  box {64, 64}
@@ -89,37 +147,14 @@ struct UpdateSched : SchedDefaults {
   __device__ void load(int s, int kb, uint8_t* stage, uint64_t* bar) const {
     const int i = seg_chunk(s);
     const int h = s - i * halves;
-    const int tok = tok0 + i * p.docs.C + kb * kBK;
-    uint8_t* sa = stage;
-    uint8_t* sb = stage + kATileBytes;
-    tma_load_2d(sa, &p.tm_v, bar, m0, tok);
-    tma_load_2d(sa + kMnBoxBytes, &p.tm_v, bar, m0 + 64, tok);
-    const int n0 = nbase + h * kBN;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kMnBoxBytes, &p.tm_z, bar, n0 + 64 * q, tok);
+    load_update_stage(p.tm_v, p.tm_z, stage, bar, m0, nbase + h * kBN,
+                      tok0 + i * p.docs.C + kb * kBK);
   }
-  // Token lines [from, to) of both operands' boxes read zero: tokens past
-  // the chunk's end (another chunk's) must not enter its sum.  A whole
-  // 128-byte line is one token, so the swizzle does not matter here.
   __device__ void clear_k(uint8_t* stage, int from, int to) const {
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 1
-    for (int box = 0; box < 6; ++box) {
-      uint4* line = reinterpret_cast<uint4*>(stage + box * kMnBoxBytes);
-#pragma unroll 1
-      for (int t = from; t < to; ++t)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) line[t * 8 + c] = zero;
-    }
+    clear_token_lines(stage, from, to);
   }
-  // MN-major, 128-byte swizzle: a 16-token slice is 16 lines of 128 B; the
-  // 64-column groups of the tile are one box (lbo) apart.
-  static __device__ uint64_t a_desc(uint32_t base, int k) {
-    return sdesc_sw128(base + uint32_t(k) * 2048u, kMnBoxBytes, 1024u);
-  }
-  static __device__ uint64_t b_desc(uint32_t base, int k) {
-    return sdesc_sw128(base + uint32_t(k) * 2048u, kMnBoxBytes, 1024u);
-  }
+  static __device__ uint64_t a_desc(uint32_t base, int k) { return mn_desc(base, k); }
+  static __device__ uint64_t b_desc(uint32_t base, int k) { return mn_desc(base, k); }
 
   // W_0 rows of this half into its accumulator (zeros outside the state).
   __device__ void preload(int h, int row, uint32_t trow) const {
@@ -133,26 +168,8 @@ struct UpdateSched : SchedDefaults {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int col = n0 + c + 8 * q;
-        float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (row_ok && col < p.f) {
-          if (p.w0_fp32) {
-            const float4* src =
-                reinterpret_cast<const float4*>(static_cast<const float*>(p.w0) + off + col);
-            const float4 lo = __ldg(src), hi = __ldg(src + 1);
-            w[0] = lo.x; w[1] = lo.y; w[2] = lo.z; w[3] = lo.w;
-            w[4] = hi.x; w[5] = hi.y; w[6] = hi.z; w[7] = hi.w;
-          } else {
-            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-                static_cast<const __nv_bfloat16*>(p.w0) + off + col));
-            const uint32_t r4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 f2 = unpack_bf16x2(r4[j]);
-              w[2 * j] = f2.x;
-              w[2 * j + 1] = f2.y;
-            }
-          }
-        }
+        float w[8];
+        load_w0_8(p.w0, p.w0_fp32 != 0, off + col, row_ok && col < p.f, w);
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[8 * q + j] = __float_as_uint(w[j]);
       }
@@ -216,6 +233,244 @@ struct UpdateSched : SchedDefaults {
 __global__ void __launch_bounds__(PipeShape<UpdateSched>::kThreads, 1)
     update_kernel(const __grid_constant__ UpdateParams p, unsigned int* status) {
   run_pipeline<UpdateSched>(p, status);
+}
+
+// ----------------------------------------------------------------------------
+// Fast-weight L2 normalisation ("[논문리뷰] Test-Time Training Done Right",
+// Non-Linear Update of Fast-Weight): W_{i+1} = L2-Normalize(W_i + eta dW_i),
+// each row of the state divided by its norm over the d_ff inputs.  The row
+// norm couples every column block of a row, which live in different CTAs,
+// so the walk runs one launch per chunk i:
+//   preload  W_i = c_i S_i into TMEM (i = 0: W_0 as given), where S_i is the
+//            unnormalised fp32 state in HBM and c_i = 1 / ||row of S_i||
+//            from the previous launch's per-block partial sums; the bf16
+//            snapshot W_i goes out from the same registers;
+//   MMA      accumulate (eta Vhat_[i])^T Z_[i];
+//   epilogue store S_{i+1} in place of S_i (a unit reads its block before it
+//            writes it, and no other unit touches that block) and its row
+//            sums of squares per 512-column unit into partial[(i+1) & 1].
+// A final kernel normalises the last state into the last snapshot or into
+// state_out.
+// ----------------------------------------------------------------------------
+
+// Sum of a row's per-block partial sums of squares, four independent
+// accumulators (the loads overlap).  The update kernel's preload and the
+// finalising kernel both call it, so they agree bit for bit.
+__device__ __forceinline__ float sum_partials(const float* base, size_t stride, int nblk) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int b = 0;
+  for (; b + 4 <= nblk; b += 4) {
+    a0 += __ldcg(base + size_t(b) * stride);
+    a1 += __ldcg(base + size_t(b + 1) * stride);
+    a2 += __ldcg(base + size_t(b + 2) * stride);
+    a3 += __ldcg(base + size_t(b + 3) * stride);
+  }
+  for (; b < nblk; ++b) a0 += __ldcg(base + size_t(b) * stride);
+  return (a0 + a1) + (a2 + a3);
+}
+
+__device__ __forceinline__ float row_scale_of(float ss) { return 1.0f / fmaxf(sqrtf(ss), 1e-12f); }
+
+struct NormUpdateParams {
+  CUtensorMap tm_v;      // eta*Vhat [M, d]  box {64, 64}
+  CUtensorMap tm_z;      // Z        [M, f]  box {64, 64}
+  const void* w0;
+  int w0_fp32;
+  int64_t w0_bstride;
+  float* state;          // S, [documents, d, f] fp32
+  float* partial;        // [2][documents][np][d] row sums of squares per 512-column unit
+  __nv_bfloat16* snap;   // [slots, d, f]
+  DocMap docs;
+  const int* upd_docs;   // updating documents, most updates first; nullptr: all
+  int n_active;          // documents with an update at chunk i
+  int i;                 // the chunk this launch updates with
+  int d, f, mt, np;
+};
+
+struct NormUpdateSched : SchedDefaults {
+  using Params = NormUpdateParams;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true, true);
+  static constexpr bool kPreload = true;
+  static constexpr bool kRaggedK = true;
+
+  const Params& p;
+  int doc = 0, tok = 0, clen = 0, slot = 0, m0 = 0, nbase = 0, npi = 0, halves = 1;
+  mutable float ss_carry = 0.f;  // this thread's row sum of squares over the unit's halves
+
+  __device__ explicit NormUpdateSched(const Params& pp) : p(pp) {}
+  __device__ int num_units() const { return p.n_active * p.mt * p.np; }
+  __device__ void begin_unit(int u, int) {
+    const int mt = u % p.mt;
+    const int r = u / p.mt;
+    const int np = r % p.np;
+    const int q = r / p.np;
+    doc = p.upd_docs ? __ldg(p.upd_docs + q) : q;
+    tok = p.docs.start(doc) + p.i * p.docs.C;
+    clen = min(p.docs.C, p.docs.len(doc) - p.i * p.docs.C);
+    slot = p.docs.first_chunk(doc) + p.i;
+    m0 = mt * kBM;
+    npi = np;
+    nbase = np * (2 * kBN);
+    halves = (nbase + kBN < p.f) ? 2 : 1;
+  }
+  __device__ int num_segments() const { return halves; }
+  __device__ int unit_accs() const { return halves; }
+  __device__ int seg_acc(int s) const { return s; }
+  __device__ int seg_kblocks(int) const { return (clen + kBK - 1) / kBK; }
+  __device__ int k_valid(int, int kb) const { return min(kBK, clen - kb * kBK); }
+  __device__ bool seg_fresh(int) const { return false; }
+  __device__ void load(int s, int kb, uint8_t* stage, uint64_t* bar) const {
+    load_update_stage(p.tm_v, p.tm_z, stage, bar, m0, nbase + s * kBN, tok + kb * kBK);
+  }
+  __device__ void clear_k(uint8_t* stage, int from, int to) const {
+    clear_token_lines(stage, from, to);
+  }
+  static __device__ uint64_t a_desc(uint32_t base, int k) { return mn_desc(base, k); }
+  static __device__ uint64_t b_desc(uint32_t base, int k) { return mn_desc(base, k); }
+
+  __device__ size_t partial_at(int par, int blk, int m) const {
+    return ((size_t(par) * p.docs.ndocs + doc) * p.np + blk) * size_t(p.d) + m;
+  }
+
+  // W_i of this half into its accumulator, and out as snapshot slot i.
+  __device__ void preload(int h, int row, uint32_t trow) const {
+    const int m = m0 + row;
+    const bool row_ok = m < p.d;
+    const int n0 = nbase + h * kBN;
+    const size_t rowoff = size_t(row_ok ? m : 0) * size_t(p.f);
+    if (p.i == 0) {
+      const size_t off = size_t(doc) * size_t(p.w0_bstride) + rowoff;
+#pragma unroll 1
+      for (int c = 0; c < kBN; c += 32) {
+        uint32_t v[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int col = n0 + c + 8 * q;
+          float w[8];
+          load_w0_8(p.w0, p.w0_fp32 != 0, off + col, row_ok && col < p.f, w);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[8 * q + j] = __float_as_uint(w[j]);
+        }
+        tmem_st_32cols(trow + uint32_t(c), v);
+      }
+      return;
+    }
+    const float scale =
+        row_ok ? row_scale_of(sum_partials(p.partial + partial_at(p.i & 1, 0, m), p.d, p.np))
+               : 0.f;
+    const float* srow = p.state + size_t(doc) * size_t(p.d) * size_t(p.f) + rowoff;
+    __nv_bfloat16* wrow = p.snap + size_t(slot) * size_t(p.d) * size_t(p.f) + rowoff;
+    // 64 columns per step: sixteen independent 16-byte loads in flight.
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 64) {
+      float w[64];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int col = n0 + c + 8 * q;
+        if (row_ok && col < p.f) {
+          const float4* src = reinterpret_cast<const float4*>(srow + col);
+          const float4 lo = __ldcg(src), hi = __ldcg(src + 1);
+          w[8 * q] = lo.x; w[8 * q + 1] = lo.y; w[8 * q + 2] = lo.z; w[8 * q + 3] = lo.w;
+          w[8 * q + 4] = hi.x; w[8 * q + 5] = hi.y; w[8 * q + 6] = hi.z; w[8 * q + 7] = hi.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) w[8 * q + j] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 64; ++j) w[j] *= scale;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int col = n0 + c + 8 * q;
+        if (row_ok && col < p.f)
+          *reinterpret_cast<uint4*>(wrow + col) = make_uint4(
+              pack_bf16x2(w[8 * q], w[8 * q + 1]), pack_bf16x2(w[8 * q + 2], w[8 * q + 3]),
+              pack_bf16x2(w[8 * q + 4], w[8 * q + 5]), pack_bf16x2(w[8 * q + 6], w[8 * q + 7]));
+      }
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        uint32_t v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(w[32 * hc + j]);
+        tmem_st_32cols(trow + uint32_t(c + 32 * hc), v);
+      }
+    }
+  }
+
+  // S_{i+1} of this half back to HBM, and its row sum of squares.
+  __device__ void epilogue(int s, int row, uint32_t trow) const {
+    const int m = m0 + row;
+    const bool row_ok = m < p.d;
+    const int n0 = nbase + s * kBN;
+    float* srow = p.state + (size_t(doc) * size_t(p.d) + size_t(row_ok ? m : 0)) * size_t(p.f);
+    float ss = s == 0 ? 0.f : ss_carry;
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 32) {
+      uint32_t v[32];
+      tmem_ld_32cols(trow + uint32_t(c), v);
+      tmem_wait_ld();
+      pin_regs(v);
+      if (!row_ok) continue;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int col = n0 + c + 8 * q;
+        if (col < p.f) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float x = __uint_as_float(v[8 * q + j]);
+            ss = fmaf(x, x, ss);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(srow + col);
+          __stcg(dst, make_uint4(v[8 * q], v[8 * q + 1], v[8 * q + 2], v[8 * q + 3]));
+          __stcg(dst + 1, make_uint4(v[8 * q + 4], v[8 * q + 5], v[8 * q + 6], v[8 * q + 7]));
+        }
+      }
+    }
+    ss_carry = ss;
+    if (row_ok && s == halves - 1) __stcg(p.partial + partial_at((p.i + 1) & 1, npi, m), ss);
+  }
+};
+
+__global__ void __launch_bounds__(PipeShape<NormUpdateSched>::kThreads, 1)
+    norm_update_kernel(const __grid_constant__ NormUpdateParams p, unsigned int* status) {
+  run_pipeline<NormUpdateSched>(p, status);
+}
+
+// The last state of each updating document, normalised: into state_out
+// (fp32, when the last chunk also updated) or into the document's last
+// snapshot slot (bf16).  One block per (row m, document).
+__global__ void __launch_bounds__(256)
+    norm_finalize_kernel(const float* __restrict__ state, const float* __restrict__ partial,
+                         __nv_bfloat16* __restrict__ snap, float* __restrict__ state_out,
+                         DocMap docs, const int* __restrict__ upd_docs, int final_update, int d,
+                         int f, int np) {
+  __shared__ float row_scale;
+  const int m = blockIdx.x;
+  const int doc = upd_docs ? __ldg(upd_docs + blockIdx.y) : int(blockIdx.y);
+  const int nch = docs.num_chunks(doc);
+  const int j = final_update ? nch : nch - 1;  // state index after the last update
+  if (threadIdx.x == 0)
+    row_scale = row_scale_of(
+        sum_partials(partial + (size_t(j & 1) * docs.ndocs + doc) * np * size_t(d) + m, d, np));
+  __syncthreads();
+  const float scale = row_scale;
+  const size_t row = (size_t(doc) * d + m) * size_t(f);
+  for (int c = threadIdx.x * 8; c < f; c += blockDim.x * 8) {
+    const float4 lo = *reinterpret_cast<const float4*>(state + row + c);
+    const float4 hi = *reinterpret_cast<const float4*>(state + row + c + 4);
+    const float w[8] = {lo.x * scale, lo.y * scale, lo.z * scale, lo.w * scale,
+                        hi.x * scale, hi.y * scale, hi.z * scale, hi.w * scale};
+    if (final_update) {
+      float4* dst = reinterpret_cast<float4*>(state_out + row + c);
+      dst[0] = make_float4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_float4(w[4], w[5], w[6], w[7]);
+    } else {
+      const size_t at = (size_t(docs.first_chunk(doc) + nch - 1) * d + m) * size_t(f) + c;
+      *reinterpret_cast<uint4*>(snap + at) =
+          make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                     pack_bf16x2(w[6], w[7]));
+    }
+  }
 }
 
 // Snapshot slot of each document's first chunk = bf16(W_0 of that document).
@@ -284,6 +539,46 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? int(units) : env.num_sms;
   update_kernel<<<grid, PipeShape<UpdateSched>::kThreads, pipe_smem_bytes<UpdateSched>(), env.stream>>>(p, env.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
+                               const CUtensorMap& tm_z, const NormUpdateArgs& a) {
+  if (a.n_udocs <= 0) return cudaSuccess;
+  NormUpdateParams p;
+  p.tm_v = tm_vhat;
+  p.tm_z = tm_z;
+  p.w0 = a.w0;
+  p.w0_fp32 = a.w0_fp32 ? 1 : 0;
+  p.w0_bstride = a.w0_bstride;
+  p.state = a.state;
+  p.partial = a.partial;
+  p.snap = a.snap;
+  p.docs = a.docs;
+  p.upd_docs = a.upd_docs;
+  p.d = a.d;
+  p.f = a.f;
+  p.mt = (a.d + kBM - 1) / kBM;
+  p.np = (a.f + 2 * kBN - 1) / (2 * kBN);
+  cudaError_t e = cudaFuncSetAttribute(norm_update_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(pipe_smem_bytes<NormUpdateSched>()));
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < a.n_steps; ++i) {
+    p.i = i;
+    p.n_active = a.active[i];
+    const int64_t units = int64_t(p.n_active) * p.mt * p.np;
+    if (units == 0) continue;
+    const int grid = units < env.num_sms ? int(units) : env.num_sms;
+    norm_update_kernel<<<grid, PipeShape<NormUpdateSched>::kThreads,
+                         pipe_smem_bytes<NormUpdateSched>(), env.stream>>>(p, env.status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 fin(unsigned(a.d), unsigned(a.n_udocs));
+  norm_finalize_kernel<<<fin, 256, 0, env.stream>>>(a.state, a.partial, a.snap, a.state_out,
+                                                    a.docs, a.upd_docs, a.state_out ? 1 : 0,
+                                                    a.d, a.f, p.np);
   return cudaGetLastError();
 }
 

@@ -137,6 +137,28 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
                           const CUtensorMap& tm_z, const CUtensorMap& tm_snap_store,
                           const UpdateArgs& a);
 
+struct NormUpdateArgs {
+  DocMap docs;
+  const int* upd_docs;  // updating documents, most updates first (nullptr: all)
+  int n_udocs;          // updating documents (0: no launch)
+  int n_steps;          // launches: the largest number of updates of a document
+  const int* active;    // host [n_steps]: documents still updating at chunk i
+  int d, f;
+  const void* w0;
+  bool w0_fp32;
+  int64_t w0_bstride;
+  float* state;         // scratch [documents, d, f] fp32
+  float* partial;       // scratch [2][documents][ceil(f/512)][d] fp32
+  __nv_bfloat16* snap;  // [slots, d, f]: slots 1..n-1 of each document written
+  float* state_out;     // [documents, d, f] fp32 or nullptr
+};
+
+// The fast-weight walk with L2 normalisation of every updated state, rows
+// over d_ff (one launch per chunk, then one finalising launch).  Tensor maps
+// as for launch_update.
+cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
+                               const CUtensorMap& tm_z, const NormUpdateArgs& a);
+
 // O_[i] = Z_[i] snap[slot of chunk i]^T for every chunk of every document.
 // Tensor maps: Z [M, f] box {64,128}; snapshots [slots*d, f] box {64,256};
 // bf16 O [M, d] with box {64,64} for the TMA stores (unused for fp32 O).

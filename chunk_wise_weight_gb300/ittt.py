@@ -24,6 +24,7 @@ PAD_CHUNK, PAD_SEQUENCE = 0, 1
 PHASES = ("conv", "target", "gateup", "snapshot0", "update", "apply")
 FLAG_FUSED_CONV = 1
 FLAG_DUAL = 2
+FLAG_L2_NORM = 4
 
 _DTYPES = {torch.bfloat16: BF16, torch.float32: FP32}
 
@@ -142,10 +143,12 @@ def _seqlens(cu_seqlens):
     return (ctypes.c_int64 * len(vals))(*vals)
 
 
-def _opts(pad_mode, fused_conv, dual, cu_seqlens, keep: dict, **tensors) -> Opts:
+def _opts(pad_mode, fused_conv, dual, cu_seqlens, keep: dict, l2norm=False,
+          **tensors) -> Opts:
     opts = Opts()
     opts.pad_mode = int(pad_mode)
-    opts.flags = (FLAG_FUSED_CONV if fused_conv else 0) | (FLAG_DUAL if dual else 0)
+    opts.flags = ((FLAG_FUSED_CONV if fused_conv else 0) | (FLAG_DUAL if dual else 0)
+                  | (FLAG_L2_NORM if l2norm else 0))
     for name, t in tensors.items():
         if t is not None:
             keep[name] = describe(t)
@@ -163,7 +166,7 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
             pad_mode: int = PAD_CHUNK, state_in=None, state_out=None, z_buf=None,
             vhat_buf=None, snap_buf=None, workspace=None, events=None,
             fused_conv: bool = False, dual: bool = False, eta_tok=None,
-            cu_seqlens=None) -> torch.Tensor:
+            cu_seqlens=None, l2norm: bool = False) -> torch.Tensor:
     """Enqueue one layer forward on `stream` (default: current stream) and
     return `out` [B,T,d].  Extra keyword buffers map to ittt_opts; `events`
     is a list of 2 * len(PHASES) torch.cuda.Event(enable_timing=True): a
@@ -174,7 +177,7 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
         out = torch.empty(H.shape, dtype=out_dtype, device=H.device)
     keep = [describe(x) for x in (H, X0, W_gate, W_up, W_down0, W_target, conv_w, out)]
     extra = {}
-    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, extra, state_in=state_in,
+    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, extra, l2norm=l2norm, state_in=state_in,
                  state_out=state_out, z_buf=z_buf, vhat_buf=vhat_buf, snap_buf=snap_buf,
                  eta_tok=eta_tok)
     if workspace is not None:
@@ -219,13 +222,13 @@ def workspace_bytes(B: int, T: int, d: int, f: int, chunk: int) -> int:
 
 def workspace_bytes_ex(B: int, T: int, d: int, f: int, chunk: int, *, pad_mode: int = PAD_CHUNK,
                        fused_conv: bool = False, dual: bool = False, cu_seqlens=None,
-                       **buffers) -> int:
+                       l2norm: bool = False, **buffers) -> int:
     """ittt_workspace_bytes_ex: scratch for a forward call with these
     options; `buffers` name the ittt_opts tensors the call passes (state_in,
     state_out, z_buf, vhat_buf, snap_buf, eta_tok) -- only whether each is
     given matters."""
     keep = {}
-    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, keep, **buffers)
+    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, keep, l2norm=l2norm, **buffers)
     return int(load().ittt_workspace_bytes_ex(B, T, d, f, chunk, ctypes.byref(opts)))
 
 

@@ -171,6 +171,15 @@ typedef struct {
  * it is never the default.  Not combinable with state_out or snap_buf; chunk
  * must be a multiple of 64 that divides T. */
 #define ITTT_FLAG_DUAL 2
+/* Normalise the fast weight after every update, row by row over its d_ff
+ * inputs: W_{i+1} = L2-Normalize(W_i + eta Vhat_[i]^T Z_[i]) with
+ * L2-Normalize(W)[m,:] = W[m,:] / max(||W[m,:]||_2, 1e-12) (the normalised
+ * update rule of "[논문리뷰] Test-Time Training Done Right", Non-Linear
+ * Update of Fast-Weight; W_down0 is applied as given).  The update is then
+ * not additive: the walk runs one launch per chunk with the fp32 state in
+ * device scratch ([S,d,f] fp32 more scratch).  Snapshots and state_out hold
+ * normalised states.  Not combinable with ITTT_FLAG_DUAL. */
+#define ITTT_FLAG_L2_NORM 4
 
 /* Kernel phases of one forward call, in launch order. */
 typedef enum {

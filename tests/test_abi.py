@@ -121,7 +121,7 @@ def test_rejects_bad_options(lib):
     o.pad_mode = 7
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     o = ittt.Opts()
-    o.flags = 4
+    o.flags = 8
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     assert "flags" in ittt.last_error()
     o = ittt.Opts()
@@ -141,6 +141,10 @@ def test_rejects_bad_options(lib):
     o = ittt.Opts()
     o.flags = ittt.FLAG_FUSED_CONV
     assert _call(lib, _args(), chunk=100, opts=o) == ittt.ERR_UNSUPPORTED
+    o = ittt.Opts()
+    o.flags = ittt.FLAG_L2_NORM | ittt.FLAG_DUAL
+    assert _call(lib, a, opts=o) == ittt.ERR_UNSUPPORTED
+    assert "dual" in ittt.last_error()
     o = ittt.Opts()
     et = _desc([1, 256], ittt.BF16, data=FAKE * 9 * 1024)           # eta_tok must be fp32
     o.eta_tok = ctypes.pointer(et)
@@ -178,6 +182,11 @@ def test_workspace_bytes_and_launch_count(lib):
     cu = [0, 300, 1024]
     want_packed = (r(T * f * 2) + 2 * r(T * d * 2) + r(5 * d * f * 2) + r((6 + 5 + 6 + 2) * 4))
     assert ittt.workspace_bytes_ex(1, T, d, f, C, cu_seqlens=cu) == want_packed
+    # the normalised walk keeps an fp32 state and row partial sums
+    nblk = -(-f // 512)
+    assert (ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True)
+            == want + r(B * d * f * 4) + r(2 * B * nblk * d * 4))
+    assert ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True, dual=True) == 0
     assert ittt.launch_count(B, T, d, f, C) == 6
     assert ittt.launch_count(B, T, d, f, T) == 5
     assert ittt.launch_count(B, 1000, d, f, 512) == 6   # two chunks, the last partial

@@ -60,7 +60,7 @@ def packed_slots(cu, C):
 
 def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
         state_in=None, want_state=False, fused_conv=False, dual=False, eta_tok=None,
-        cu_seqlens=None):
+        cu_seqlens=None, l2norm=False):
     B, T, d = g["H"].shape
     f = g["W_gate"].shape[0]
     dev = g["H"].device
@@ -82,7 +82,7 @@ def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
                        None if state_in is not None else g["W_down0"], g["W_target"],
                        g["conv_w"], eta, C, out_dtype=out_dtype, pad_mode=pad_mode,
                        fused_conv=fused_conv, dual=dual, eta_tok=eta_tok,
-                       cu_seqlens=cu_seqlens, **kw)
+                       cu_seqlens=cu_seqlens, l2norm=l2norm, **kw)
     ittt.stream_status()
     res = {"O": out}
     res.update(kw)
@@ -323,6 +323,85 @@ def test_packed_equals_separate_calls_bitwise(cuda_device):
     for a, b in zip(cu, cu[1:]):
         one = {k: (v[:, a:b].contiguous() if k in ("H", "X0") else v) for k, v in g.items()}
         assert torch.equal(run(one, eta, C)["O"][0], full[0, a:b])
+
+
+# --------------------------------------------------------------------------
+# Fast-weight L2 normalisation (one launch per chunk)
+# --------------------------------------------------------------------------
+
+L2 = [
+    # B, T, d, f, C, eta
+    (1, 512, 64, 256, 128, 0.05),
+    (2, 640, 200, 584, 256, 0.05),     # ragged d, odd 256-column blocks, partial chunk
+    (1, 333, 136, 264, 100, 0.1),      # chunks that end inside a stage
+    (3, 384, 136, 1000, 192, 0.02),
+]
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", L2)
+def test_l2norm_parity(cuda_device, B, T, d, f, C, eta):
+    inp = make_inputs(B, T, d, f, seed=1100 + T + d)
+    ref = oracle.forward(inp, eta, C, want_states=True, l2norm=True)
+    got = run(to_device(inp, cuda_device), eta, C, intermediates=True, want_state=True,
+              l2norm=True)
+    n = -(-T // C)
+    assert_parity(host(got["snap_buf"]), ref["states"][:, :n], "normalised snapshots")
+    assert_parity(host(got["state_out"]), ref["states"][:, n], "normalised final state")
+    assert_parity(host(got["O"]), ref["O"], "O")
+    # without state_out the last snapshot comes from the finalising kernel
+    got2 = run(to_device(inp, cuda_device), eta, C, intermediates=True, l2norm=True)
+    assert torch.equal(got2["snap_buf"], got["snap_buf"])
+    assert torch.equal(got2["O"], got["O"])
+
+
+def test_l2norm_packed_with_options(cuda_device):
+    """Packed documents, per-document initial states (fp32), per-token
+    rates and fp32 output with the normalised walk."""
+    cu, d, f, C, eta = [0, 150, 151, 420, 700], 128, 256, 128, 0.05
+    inp = _packed_inputs(cu, d, f, seed=1177)
+    nd = len(cu) - 1
+    w0 = torch.stack([inp["W_down0"] * (1.0 + 0.5 * k) for k in range(nd)])
+    rates = torch.rand(1, cu[-1], generator=torch.Generator().manual_seed(6)) + 0.5
+    pk = dict(inp)
+    pk["W_down0"] = w0
+    ref = oracle.forward_packed(pk, cu, eta, C, want_states=True, eta_tok=rates, l2norm=True)
+    g = to_device(inp, cuda_device)
+    got = run(g, eta, C, out_dtype=torch.float32, state_in=w0.to(cuda_device).contiguous(),
+              want_state=True, eta_tok=rates.to(cuda_device), cu_seqlens=cu, l2norm=True,
+              intermediates=True)
+    snaps = np.concatenate([s[:-1] for s in ref["states"]])
+    assert_parity(host(got["snap_buf"])[0], snaps, "normalised snapshots")
+    assert_parity(host(got["state_out"]), np.stack([s[-1] for s in ref["states"]]),
+                  "normalised final states")
+    assert_parity(host(got["O"])[0], ref["O"], "O")
+
+
+def test_l2norm_named_workload_sampled(cuda_device):
+    """The 8k-token Qwen3-4B-shaped workload with the normalised walk: chunk 0
+    rows exactly from the oracle; every snapshot after W_0 has unit rows;
+    W_1 rows equal L2-Normalize(W_0 + (eta Vhat_[0])^T Z_[0]) on the
+    kernel's own bf16 operands; later rows follow O_[i] = Z_[i] W_i^T."""
+    cfg, inp = config_inputs(1)
+    T, d, f, C, eta = cfg["T"], cfg["d"], cfg["f"], cfg["C"], cfg["eta"]
+    g = to_device(inp, cuda_device)
+    got = run(g, eta, C, intermediates=True, l2norm=True)
+    snap = got["snap_buf"][0].float()
+    norms = snap[1:].norm(dim=2)
+    assert (norms - 1.0).abs().max().item() < 1e-2
+    rows = np.array([0, 5, C - 1])
+    assert_parity(host(got["O"][0][torch.as_tensor(rows)]),
+                  oracle.first_chunk_rows(inp["H"][0], inp["W_gate"], inp["W_up"],
+                                          inp["W_down0"], rows), "O chunk 0")
+    V = host(got["vhat_buf"][0][:C])                     # eta * Vhat, bf16 values
+    Z = host(got["z_buf"][0][:C])
+    W0 = inp["W_down0"].double().numpy()
+    for m in (0, 777, d - 1):
+        u = W0[m] + V[:, m] @ Z
+        assert_parity(host(snap[1, m]), u / np.linalg.norm(u), f"W_1 row {m}")
+    for tok in (C + 3, T // 2, T - 1):
+        i = tok // C
+        assert_parity(host(got["O"][0][tok]), host(snap[i]) @ host(got["z_buf"][0][tok]),
+                      f"O row {tok}")
 
 
 # --------------------------------------------------------------------------
