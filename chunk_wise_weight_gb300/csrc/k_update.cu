@@ -5,15 +5,14 @@
 //
 // The per-chunk deltas do not depend on W (the loss is linear in it), so
 // the state after chunk i is W_0 plus one long contraction over the tokens
-// of chunks 0..i.  A work unit owns a 128 (d_model) x 512 (d_ff) block of
-// one document's state, split into two 128 x 256 halves.  Each half's fp32
-// state lives in one TMEM accumulator for the whole walk: the epilogue
-// warps load W_0 into it (tcgen05.st) and the MMAs accumulate
-// (eta Vhat_[i])^T Z_[i] on top, eta having been folded into Vhat by the
-// target kernel.  The MMAs alternate halves chunk by chunk: while the tensor
-// core accumulates chunk i of one half, the epilogue reads the other half's
-// state at its chunk boundary and writes the bf16 snapshot W_{i+1} that the
-// apply kernel reads.  The fp32 state reaches HBM only when the caller asks
+// of chunks 0..i.  A work unit owns two 128 (d_model) x 256 (d_ff) blocks
+// ("halves") of the state.  Each half's fp32 state lives in one TMEM
+// accumulator for the whole walk: the epilogue warps load W_0 into it
+// (tcgen05.st) and the MMAs accumulate (eta Vhat_[i])^T Z_[i] on top, eta
+// having been folded into Vhat by the target kernel.  The MMAs alternate
+// halves chunk by chunk: while the tensor core accumulates chunk i of one
+// half, the epilogue reads the other half's state at its chunk boundary and
+// writes the bf16 snapshot W_{i+1} that the apply kernel reads.  The fp32 state reaches HBM only when the caller asks
 // for the final state.
 //
 // Both operands are read MN-major: the contraction index (token) is the row
@@ -100,9 +99,21 @@ struct UpdateParams {
   const int* upd_docs;  // documents that update, longest first; nullptr: all
   int n_udocs;
   int final_update;     // also update with the last chunk (for state_out)
-  int d, f, mt, np;
+  int d, f;
+  int MT, NH, NP;       // 128-row blocks of d_model; 256- and 512-column blocks of d_ff
+  int P;                // pairs: documents x MT x NP
+  int RG;               // pairs walked whole: full rounds over the grid
+  int split;            // the last partial round walks its halves one by one
 };
 
+// A unit is a pair of 128 (d_model) x 256 (d_ff) state blocks, (document,
+// 512-column block, 128-row block) listed d_model block fastest: the CTAs
+// of one round over the grid share the same document's chunks and Z column
+// blocks, so those stream from DRAM about once.  The MMAs of a pair
+// alternate chunk by chunk, so each chunk-boundary epilogue of one half
+// overlaps the other half's MMAs.  When the pairs do not fill the last round
+// (Q pairs left, 2Q <= CTAs) those pairs are walked as 2Q single halves on
+// as many CTAs, which shortens the longest CTA by one half-walk.
 struct UpdateSched : SchedDefaults {
   using Params = UpdateParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true, true);
@@ -111,31 +122,42 @@ struct UpdateSched : SchedDefaults {
   static constexpr bool kRaggedK = true;
 
   const Params& p;
-  int doc = 0, tok0 = 0, len = 0, nch = 0, nupd = 0, slot0 = 0, m0 = 0, nbase = 0, halves = 1;
+  int nh = 0;                 // halves in this unit (0, 1 or 2)
+  int doc = 0, m0 = 0, tok0 = 0, slot0 = 0;
+  int hn0[2] = {0, 0};        // first d_ff column of each half
+  int len = 0, nch = 0, nupd = 0;
 
   __device__ explicit UpdateSched(const Params& pp) : p(pp) {}
-  __device__ int num_units() const { return p.n_udocs * p.mt * p.np; }
-  // d_model blocks vary fastest: the CTAs of one wave share each Z column
-  // block, so Z streams from DRAM about once per document.
+  __device__ int num_units() const {
+    return p.split ? p.RG + 2 * (p.P - p.RG) : p.P;
+  }
   __device__ void begin_unit(int u, int) {
-    const int mt = u % p.mt;
-    const int r = u / p.mt;
-    const int np = r % p.np;
-    const int q = r / p.np;
+    int pi = u, first = 0, want = 2;
+    if (p.split && u >= p.RG) {
+      pi = p.RG + (u - p.RG) / 2;
+      first = (u - p.RG) % 2;
+      want = 1;
+    }
+    const int q = pi / (p.MT * p.NP);
+    const int r = pi - q * p.MT * p.NP;
+    const int np = r / p.MT;
+    const int hb0 = 2 * np + first;
+    nh = min(want, p.NH - hb0);
+    if (nh < 0) nh = 0;
     doc = p.upd_docs ? __ldg(p.upd_docs + q) : q;
+    m0 = (r % p.MT) * kBM;
+    hn0[0] = hb0 * kBN;
+    hn0[1] = (hb0 + 1) * kBN;
     tok0 = p.docs.start(doc);
+    slot0 = p.docs.first_chunk(doc);
     len = p.docs.len(doc);
     nch = p.docs.num_chunks(doc);
-    slot0 = p.docs.first_chunk(doc);
-    nupd = p.final_update ? nch : nch - 1;
-    m0 = mt * kBM;
-    nbase = np * (2 * kBN);
-    halves = (nbase + kBN < p.f) ? 2 : 1;
+    nupd = nh > 0 ? (p.final_update ? nch : nch - 1) : 0;
   }
-  __device__ int num_segments() const { return nupd * halves; }
-  __device__ int unit_accs() const { return nupd > 0 ? halves : 0; }
-  __device__ int seg_acc(int s) const { return halves == 2 ? (s & 1) : 0; }
-  __device__ int seg_chunk(int s) const { return halves == 2 ? (s >> 1) : s; }
+  __device__ int num_segments() const { return nupd * nh; }
+  __device__ int unit_accs() const { return nupd > 0 ? nh : 0; }
+  __device__ int seg_acc(int s) const { return nh == 2 ? (s & 1) : 0; }
+  __device__ int seg_chunk(int s) const { return nh == 2 ? (s >> 1) : s; }
   // Tokens of chunk i of the document (the last chunk may be shorter).
   __device__ int chunk_len(int i) const { return min(p.docs.C, len - i * p.docs.C); }
   __device__ int seg_kblocks(int s) const { return (chunk_len(seg_chunk(s)) + kBK - 1) / kBK; }
@@ -146,8 +168,8 @@ struct UpdateSched : SchedDefaults {
 
   __device__ void load(int s, int kb, uint8_t* stage, uint64_t* bar) const {
     const int i = seg_chunk(s);
-    const int h = s - i * halves;
-    load_update_stage(p.tm_v, p.tm_z, stage, bar, m0, nbase + h * kBN,
+    const int h = s - i * nh;
+    load_update_stage(p.tm_v, p.tm_z, stage, bar, m0, h ? hn0[1] : hn0[0],
                       tok0 + i * p.docs.C + kb * kBK);
   }
   __device__ void clear_k(uint8_t* stage, int from, int to) const {
@@ -156,11 +178,11 @@ struct UpdateSched : SchedDefaults {
   static __device__ uint64_t a_desc(uint32_t base, int k) { return mn_desc(base, k); }
   static __device__ uint64_t b_desc(uint32_t base, int k) { return mn_desc(base, k); }
 
-  // W_0 rows of this half into its accumulator (zeros outside the state).
+  // W_0 rows of half h into its accumulator (zeros outside the state).
   __device__ void preload(int h, int row, uint32_t trow) const {
     const int m = m0 + row;
     const bool row_ok = m < p.d;
-    const int n0 = nbase + h * kBN;
+    const int n0 = h ? hn0[1] : hn0[0];
     const size_t off = size_t(doc) * size_t(p.w0_bstride) + size_t(row_ok ? m : 0) * size_t(p.f);
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 32) {
@@ -183,10 +205,10 @@ struct UpdateSched : SchedDefaults {
   // the caller wants it (direct stores).
   __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& stg) const {
     const int i = seg_chunk(s);
-    const int h = s - i * halves;
+    const int h = s - i * nh;
     const int m = m0 + row;
     const bool row_ok = m < p.d;
-    const int n0 = nbase + h * kBN;
+    const int n0 = h ? hn0[1] : hn0[0];
     const bool write_snap = (i + 1) < nch;
     float* st = (p.state_out != nullptr && (i + 1) == nupd)
                     ? p.state_out + (size_t(doc) * p.d + size_t(row_ok ? m : 0)) * size_t(p.f)
@@ -531,13 +553,19 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
   p.final_update = a.final_update ? 1 : 0;
   p.d = a.d;
   p.f = a.f;
-  p.mt = (a.d + kBM - 1) / kBM;
-  p.np = (a.f + 2 * kBN - 1) / (2 * kBN);
-  const int64_t units = int64_t(p.n_udocs) * p.mt * p.np;
+  p.MT = (a.d + kBM - 1) / kBM;
+  p.NH = (a.f + kBN - 1) / kBN;
+  p.NP = (a.f + 2 * kBN - 1) / (2 * kBN);
+  const int64_t P = int64_t(p.n_udocs) * p.MT * p.NP;
+  const int64_t Q = P % env.num_sms;
+  p.P = int(P);
+  p.RG = int(P - Q);
+  p.split = (Q > 0 && 2 * Q <= env.num_sms) ? 1 : 0;
+  const int64_t units = p.split ? p.RG + 2 * Q : P;
+  const int grid = int(units < env.num_sms ? units : env.num_sms);
   cudaError_t e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(pipe_smem_bytes<UpdateSched>()));
   if (e != cudaSuccess) return e;
-  const int grid = units < env.num_sms ? int(units) : env.num_sms;
   update_kernel<<<grid, PipeShape<UpdateSched>::kThreads, pipe_smem_bytes<UpdateSched>(), env.stream>>>(p, env.status);
   return cudaGetLastError();
 }
