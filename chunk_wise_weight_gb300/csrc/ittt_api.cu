@@ -250,13 +250,14 @@ struct Plan {
   int64_t n = 0;       // chunks per sequence (regular)
   bool final_update = false;
   int n_udocs = 0;     // documents that run at least one update
-  int64_t ntiles = 0;  // 128-row tiles over all chunks (the apply's row units)
+  int64_t ntiles = 0;   // 128-row tiles over all chunks (the apply's row units)
+  int64_t ntiles2 = 0;  // 256-row tiles over all chunks (row units on CTA pairs)
   // L2 normalisation: launches of the walk, and how many documents are
   // still updating at each (documents sorted by update count).
   std::vector<int> active;
   // Packed: starts[ndocs+1] | chunk_base[ndocs+1] | chunk_doc[nslots] |
-  // tile_base[nslots+1] | upd_docs[n_udocs], staged into the scratch at
-  // L.table.
+  // tile_base[nslots+1] | tile_base2[nslots+1] | upd_docs[n_udocs], staged
+  // into the scratch at L.table.
   std::vector<int> table;
   Layout L;
 };
@@ -334,13 +335,14 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
         for (int64_t i = 0; i < -u.first; ++i) ++P->active[size_t(i)];
     }
     std::vector<int>& t = P->table;
-    t.resize(size_t(2 * (nd + 1) + 2 * slots + 1 + P->n_udocs));
+    t.resize(size_t(2 * (nd + 1) + 3 * slots + 2 + P->n_udocs));
     int* starts = t.data();
     int* base = starts + (nd + 1);
     int* cdoc = base + (nd + 1);
     int* tbase = cdoc + slots;
-    int* ud = tbase + slots + 1;
-    int64_t g = 0, tiles = 0;
+    int* tbase2 = tbase + slots + 1;
+    int* ud = tbase2 + slots + 1;
+    int64_t g = 0, tiles = 0, tiles2 = 0;
     for (int64_t k = 0; k <= nd; ++k) {
       starts[k] = int(cu[k]);
       base[k] = int(g);
@@ -350,13 +352,17 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
         for (int64_t j = 0; j < nk; ++j) {
           const int64_t len = std::min<int64_t>(chunk, L - j * chunk);
           tbase[g] = int(tiles);
+          tbase2[g] = int(tiles2);
           tiles += (len + 127) / 128;
+          tiles2 += (len + 255) / 256;
           cdoc[g++] = int(k);
         }
       }
     }
     tbase[slots] = int(tiles);
+    tbase2[slots] = int(tiles2);
     P->ntiles = tiles;
+    P->ntiles2 = tiles2;
     for (int q = 0; q < P->n_udocs; ++q) ud[q] = upd[size_t(q)].second;
   } else {
     P->ndocs = B;
@@ -367,6 +373,7 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
       P->active.assign(size_t(P->final_update ? P->n : P->n - 1), int(B));
     const int64_t last = T - (P->n - 1) * chunk;
     P->ntiles = B * ((P->n - 1) * ((chunk + 127) / 128) + (last + 127) / 128);
+    P->ntiles2 = B * ((P->n - 1) * ((chunk + 255) / 256) + (last + 255) / 256);
   }
   // The fused convolution forms its A tile from 4-row groups inside one
   // chunk; the dual form's scores are blocked by 64-token chunks.
@@ -542,8 +549,13 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   docs.T = int(T);
   docs.n = int(P.n);
   docs.C = int(chunk);
+  docs.ntiles2 = int(P.ntiles2);
   docs.mtc = int((chunk + 127) / 128);
-  if (!P.packed) docs.tiles_per_seq = int(P.ntiles / B);
+  docs.mtc2 = int((chunk + 255) / 256);
+  if (!P.packed) {
+    docs.tiles_per_seq = int(P.ntiles / B);
+    docs.tiles_per_seq2 = int(P.ntiles2 / B);
+  }
   const int* upd_docs = nullptr;
   int* tab = reinterpret_cast<int*>(ws + L.table);
   if (P.packed) {
@@ -551,7 +563,8 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     docs.chunk_base = tab + (P.ndocs + 1);
     docs.chunk_doc = tab + 2 * (P.ndocs + 1);
     docs.tile_base = docs.chunk_doc + P.nslots;
-    upd_docs = docs.tile_base + P.nslots + 1;
+    docs.tile_base2 = docs.tile_base + P.nslots + 1;
+    upd_docs = docs.tile_base2 + P.nslots + 1;
   }
 
   // Tensor maps.
@@ -576,7 +589,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if ((s = make_map(&tm_vmn, vhat, d, M, 64, 64, "Vhat"))) return s;
   if ((s = make_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
   if ((s = make_map(&tm_zk, z, f, M, 64, 128, "Z (apply)"))) return s;
-  CUtensorMap tm_zs, tm_w0b, tm_sc;
+  CUtensorMap tm_zs, tm_w0b, tm_sc, tm_snap_pair;
   auto* scores = reinterpret_cast<__nv_bfloat16*>(ws + L.scores);
   const void* w0b = w0_is_bf16 ? W_down0->data : static_cast<const void*>(ws + L.w0b);
   if (dual) {
@@ -586,6 +599,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     if ((s = make_map(&tm_sc, scores, uint64_t(T), M, 64, 128, "scores"))) return s;
   } else {
     if ((s = make_map(&tm_snap, snap, f, uint64_t(P.nslots * d), 64, 256, "snapshots"))) return s;
+    if ((s = make_map(&tm_snap_pair, snap, f, uint64_t(P.nslots * d), 64, 128,
+                      "snapshots (pair)")))
+      return s;
     if ((s = make_map_3d(&tm_ss, snap, f, d, uint64_t(P.nslots), 64, 128, "snapshots (store)")))
       return s;
   }
@@ -679,9 +695,17 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     }
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
-    ITTT_STEP(ittt::launch_apply(env, tm_zk, tm_snap, tm_os, out->data,
-                                 out->dtype == ITTT_FP32, docs, int(d), int(f)),
-              "apply launch");
+    if (what == nullptr) {
+      // CTA pairs where two can be resident, else one CTA per tile.
+      e = ittt::launch_apply_pair(env, tm_zk, tm_snap_pair, tm_os, out->data,
+                                  out->dtype == ITTT_FP32, docs, int(d), int(f));
+      if (e == cudaErrorNotSupported) {
+        cudaGetLastError();
+        e = ittt::launch_apply(env, tm_zk, tm_snap, tm_os, out->data, out->dtype == ITTT_FP32,
+                               docs, int(d), int(f));
+      }
+      if (e != cudaSuccess) what = "apply launch";
+    }
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY + 1, stream), "event record");
   } else {
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");

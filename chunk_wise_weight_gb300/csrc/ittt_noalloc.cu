@@ -262,6 +262,9 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   docs.mtc = int((chunk + 127) / 128);
   docs.tiles_per_seq = int((n - 1) * docs.mtc + (T - (n - 1) * chunk + 127) / 128);
   docs.ntiles = int(B) * docs.tiles_per_seq;
+  docs.mtc2 = int((chunk + 255) / 256);
+  docs.tiles_per_seq2 = int((n - 1) * docs.mtc2 + (T - (n - 1) * chunk + 255) / 256);
+  docs.ntiles2 = int(B) * docs.tiles_per_seq2;
   const bool w0_fp32 = W_down0->dtype == ITTT_FP32;
   cudaError_t e;
   const char* what = nullptr;

@@ -14,6 +14,7 @@
 // written row by row with masked 16-byte stores.
 #include "kernels.h"
 #include "pipeline.cuh"
+#include "pipeline_pair.cuh"
 
 namespace ittt {
 namespace {
@@ -28,6 +29,72 @@ struct ApplyParams {
   int d, f;
   int nt, kblocks;
 };
+
+// bf16 O in whole 64-row halves: 64-column TMA stores (columns >= d are
+// clipped).  Otherwise (fp32 O, or a tile that ends inside a 64-row half):
+// direct 16-byte stores of the valid rows.
+__device__ __forceinline__ void apply_epilogue(const ApplyParams& p, int arow0, int rows_valid,
+                                             int n0, int row, uint32_t trow, EpiStager& st) {
+  if (!p.out_fp32 && (rows_valid == kBM || rows_valid == 64)) {
+#pragma unroll 1
+    for (int g = 0; g < kBN / 64; ++g) {
+      uint8_t* buf = st.acquire();
+#pragma unroll 1
+      for (int hc = 0; hc < 2; ++hc) {
+        uint32_t v[32];
+        tmem_ld_32cols(trow + uint32_t(g * 64 + hc * 32), v);
+        tmem_wait_ld();
+        pin_regs(v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          st.put(buf, hc * 4 + q,
+                 make_uint4(
+                     pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                     pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                     pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                     pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]))));
+      }
+      st.commit(buf, [&](uint8_t* src) {
+        tma_store_2d(&p.tm_os, src, n0 + g * 64, arow0);
+        if (rows_valid > 64) tma_store_2d(&p.tm_os, src + 64 * 128, n0 + g * 64, arow0 + 64);
+      });
+    }
+    return;
+  }
+  const bool row_ok = row < rows_valid;
+  const size_t grow = size_t(arow0 + (row_ok ? row : 0));
+#pragma unroll 1
+  for (int c = 0; c < kBN; c += 32) {
+    uint32_t v[32];
+    tmem_ld_32cols(trow + uint32_t(c), v);
+    tmem_wait_ld();
+    pin_regs(v);
+    if (!row_ok) continue;
+    if (p.out_fp32) {
+      float* orow = static_cast<float*>(p.out) + grow * size_t(p.d);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int col = n0 + c + 4 * q;
+        if (col < p.d)
+          *reinterpret_cast<uint4*>(orow + col) =
+              make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    } else {
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * size_t(p.d);
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int col = n0 + c + 8 * q;
+        if (col < p.d)
+          *reinterpret_cast<uint4*>(orow + col) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
+    }
+  }
+}
 
 struct ApplySched : SchedDefaults {
   using Params = ApplyParams;
@@ -69,69 +136,8 @@ struct ApplySched : SchedDefaults {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
   }
 
-  // bf16 O in whole 64-row halves: 64-column TMA stores (columns >= d are
-  // clipped).  Otherwise (fp32 O, or a tile that ends inside a 64-row half):
-  // direct 16-byte stores of the valid rows.
   __device__ void epilogue(int, int row, uint32_t trow, EpiStager& st) const {
-    if (!p.out_fp32 && (rows_valid == kBM || rows_valid == 64)) {
-#pragma unroll 1
-      for (int g = 0; g < kBN / 64; ++g) {
-        uint8_t* buf = st.acquire();
-#pragma unroll 1
-        for (int hc = 0; hc < 2; ++hc) {
-          uint32_t v[32];
-          tmem_ld_32cols(trow + uint32_t(g * 64 + hc * 32), v);
-          tmem_wait_ld();
-          pin_regs(v);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            st.put(buf, hc * 4 + q,
-                   make_uint4(
-                       pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                       pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                       pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                       pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]))));
-        }
-        st.commit(buf, [&](uint8_t* src) {
-          tma_store_2d(&p.tm_os, src, n0 + g * 64, arow0);
-          if (rows_valid > 64) tma_store_2d(&p.tm_os, src + 64 * 128, n0 + g * 64, arow0 + 64);
-        });
-      }
-      return;
-    }
-    const bool row_ok = row < rows_valid;
-    const size_t grow = size_t(arow0 + (row_ok ? row : 0));
-#pragma unroll 1
-    for (int c = 0; c < kBN; c += 32) {
-      uint32_t v[32];
-      tmem_ld_32cols(trow + uint32_t(c), v);
-      tmem_wait_ld();
-      pin_regs(v);
-      if (!row_ok) continue;
-      if (p.out_fp32) {
-        float* orow = static_cast<float*>(p.out) + grow * size_t(p.d);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int col = n0 + c + 4 * q;
-          if (col < p.d)
-            *reinterpret_cast<uint4*>(orow + col) =
-                make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
-      } else {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * size_t(p.d);
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int col = n0 + c + 8 * q;
-          if (col < p.d)
-            *reinterpret_cast<uint4*>(orow + col) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        }
-      }
-    }
+    apply_epilogue(p, arow0, rows_valid, n0, row, trow, st);
   }
 };
 
@@ -140,7 +146,92 @@ __global__ void __launch_bounds__(PipeShape<ApplySched>::kThreads, 1)
   run_pipeline<ApplySched>(p, status);
 }
 
+// CTA pairs: a unit is (256-row tile of a chunk, 256-column tile of d);
+// this CTA holds rows [128 rank, 128 rank + 128) of the tile and loads the
+// snapshot rows of its 128 columns.
+struct ApplyPairSched : PairDefaults {
+  using Params = ApplyParams;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, kBN, false, false);
+  static constexpr bool kStagedStores = true;
+
+  const Params& p;
+  const int rank;
+  int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0;
+
+  __device__ ApplyPairSched(const Params& pp, uint32_t r) : p(pp), rank(int(r)) {}
+  __device__ int num_units() const { return p.docs.ntiles2 * p.nt; }
+  __device__ void begin_unit(int u, int local) {
+    const int nt = u % p.nt;
+    int mt = 0;
+    const int g = p.docs.slot_of_tile(u / p.nt, &mt, true);
+    const int k = p.docs.doc_of_chunk(g);
+    const int i = g - p.docs.first_chunk(k);
+    const int len = p.docs.len(k);
+    const int r0 = mt * (2 * kBM) + rank * kBM;  // first row of this CTA's half in the chunk
+    arow0 = p.docs.start(k) + i * p.docs.C + r0;
+    brow0 = g * p.d + nt * kBN + rank * kBM;
+    rows_valid = min(kBM, min(p.docs.C, len - i * p.docs.C) - r0);
+    n0 = nt * kBN;
+    acc = local & 1;
+  }
+  __device__ int num_segments() const { return 1; }
+  __device__ int seg_acc(int) const { return acc; }
+  __device__ int seg_kblocks(int) const { return p.kblocks; }
+  __device__ bool seg_fresh(int) const { return true; }
+  __device__ void load(int, int kb, uint8_t* stage, uint32_t bar) const {
+    const int k = kb * kBK;
+    tma_load_2d_pair(stage, &p.tm_z, bar, k, arow0);
+    tma_load_2d_pair(stage + kPairATileBytes, &p.tm_snap, bar, k, brow0);
+  }
+  static __device__ uint64_t a_desc(uint32_t base, int k) {
+    return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
+  }
+  static __device__ uint64_t b_desc(uint32_t base, int k) {
+    return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
+  }
+  // The second half of a tile may lie past its chunk (rows_valid <= 0):
+  // computed, nothing stored.
+  __device__ void epilogue(int, int row, uint32_t trow, EpiStager& st) const {
+    apply_epilogue(p, arow0, rows_valid, n0, row, trow, st);
+  }
+};
+
+__global__ void __launch_bounds__(kBaseThreads, 1)
+    apply_pair_kernel(const __grid_constant__ ApplyParams p, unsigned int* status) {
+  run_pipeline_pair<ApplyPairSched>(p, status);
+}
+
 }  // namespace
+
+cudaError_t launch_apply_pair(const LaunchEnv& env, const CUtensorMap& tm_z,
+                              const CUtensorMap& tm_snap, const CUtensorMap& tm_os, void* out,
+                              bool out_fp32, const DocMap& docs, int d, int f) {
+  ApplyParams p;
+  p.tm_z = tm_z;
+  p.tm_snap = tm_snap;
+  p.tm_os = tm_os;
+  p.out = out;
+  p.out_fp32 = out_fp32 ? 1 : 0;
+  p.docs = docs;
+  p.d = d;
+  p.f = f;
+  p.nt = (d + kBN - 1) / kBN;
+  p.kblocks = (f + kBK - 1) / kBK;
+  const int64_t units = int64_t(docs.ntiles2) * p.nt;
+  if (units == 0) return cudaSuccess;
+  const size_t smem = pair_smem_bytes<ApplyPairSched>();
+  cudaError_t e = cudaFuncSetAttribute(apply_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  static std::atomic<int> resident{-1};
+  int pairs = 0;
+  if ((e = max_pairs(reinterpret_cast<const void*>(apply_pair_kernel), smem, env, &pairs,
+                     &resident)) != cudaSuccess)
+    return e;
+  if (pairs < 1) return cudaErrorNotSupported;
+  if (units < pairs) pairs = int(units);
+  return launch_on_pairs(reinterpret_cast<const void*>(apply_pair_kernel), pairs, smem, env, &p);
+}
 
 cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z, const CUtensorMap& tm_snap,
                          const CUtensorMap& tm_os, void* out, bool out_fp32, const DocMap& docs,

@@ -30,14 +30,18 @@ struct DocMap {
   const int* chunk_base;  // [ndocs + 1] device, or nullptr
   const int* chunk_doc;   // [nchunks] device, or nullptr
   const int* tile_base;   // [nchunks + 1] device: 128-row tiles before slot g, or nullptr
+  const int* tile_base2;  // [nchunks + 1] device: 256-row tiles before slot g, or nullptr
   int ndocs;              // documents (B when regular)
   int nchunks;            // snapshot slots over all documents
   int ntiles;             // 128-row tiles over all chunks
+  int ntiles2;            // 256-row tiles over all chunks
   int T;                  // tokens per sequence (regular) / in the pack
   int n;                  // chunks per sequence (regular)
   int C;
   int mtc;                // 128-row tiles of a full chunk (regular)
   int tiles_per_seq;      // 128-row tiles of a sequence (regular)
+  int mtc2;               // 256-row tiles of a full chunk (regular)
+  int tiles_per_seq2;     // 256-row tiles of a sequence (regular)
 
   __host__ __device__ bool packed() const { return starts != nullptr; }
 #ifdef __CUDACC__
@@ -54,22 +58,25 @@ struct DocMap {
   __device__ __forceinline__ int doc_of_chunk(int g) const {
     return chunk_doc ? __ldg(chunk_doc + g) : g / n;
   }
-  // Snapshot slot g and row tile mt (of 128 rows within the chunk) of the
-  // t-th non-empty row tile, over all chunks in slot order.
-  __device__ __forceinline__ int slot_of_tile(int t, int* mt) const {
-    if (!tile_base) {
-      const int b = t / tiles_per_seq;
-      const int r = t - b * tiles_per_seq;
-      const int i = min(r / mtc, n - 1);
-      *mt = r - i * mtc;
+  // Snapshot slot g and row tile mt (of 128 rows, or 256 with `wide`, within
+  // the chunk) of the t-th non-empty row tile, over all chunks in slot order.
+  __device__ __forceinline__ int slot_of_tile(int t, int* mt, bool wide = false) const {
+    const int* base = wide ? tile_base2 : tile_base;
+    if (!base) {
+      const int per = wide ? tiles_per_seq2 : tiles_per_seq;
+      const int m = wide ? mtc2 : mtc;
+      const int b = t / per;
+      const int r = t - b * per;
+      const int i = min(r / m, n - 1);
+      *mt = r - i * m;
       return b * n + i;
     }
     int lo = 0, hi = nchunks;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (__ldg(tile_base + mid) <= t) lo = mid; else hi = mid;
+      if (__ldg(base + mid) <= t) lo = mid; else hi = mid;
     }
-    *mt = t - __ldg(tile_base + lo);
+    *mt = t - __ldg(base + lo);
     return lo;
   }
   // Document holding token row r (binary search over the starts).
@@ -166,6 +173,13 @@ cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
 cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
                          const CUtensorMap& tm_snap, const CUtensorMap& tm_os, void* out,
                          bool out_fp32, const DocMap& docs, int d, int f);
+
+// The same on CTA pairs (256-row tiles, tcgen05 cta_group::2): tm_snap has
+// box {64,128} (each CTA loads its 128 of the tile's 256 columns).  Returns
+// cudaErrorNotSupported when no pair can be resident (nothing launched).
+cudaError_t launch_apply_pair(const LaunchEnv& env, const CUtensorMap& tm_z,
+                              const CUtensorMap& tm_snap, const CUtensorMap& tm_os, void* out,
+                              bool out_fp32, const DocMap& docs, int d, int f);
 
 // Dual form, scores: S[b, t, s] = Z_t . Z_s (bf16) for every token t of chunk
 // i >= 1 and every token s < i*C of the same sequence.  Tensor maps: Z

@@ -178,9 +178,11 @@ def test_workspace_bytes_and_launch_count(lib):
     assert ittt.workspace_bytes_ex(B, T, d, f, C, dual=True) == want_dual
     # packed documents 300 + 724 tokens: ceil(300/256) + ceil(724/256) = 2 + 3
     # slots, and a table of starts and slot bases 2*(2+1), the slot-to-
-    # document map 5, the tile bases 5+1 and the updating documents 2 ints
+    # document map 5, the 128- and 256-row tile bases 2*(5+1) and the
+    # updating documents 2 ints
     cu = [0, 300, 1024]
-    want_packed = (r(T * f * 2) + 2 * r(T * d * 2) + r(5 * d * f * 2) + r((6 + 5 + 6 + 2) * 4))
+    want_packed = (r(T * f * 2) + 2 * r(T * d * 2) + r(5 * d * f * 2)
+                   + r((6 + 5 + 12 + 2) * 4))
     assert ittt.workspace_bytes_ex(1, T, d, f, C, cu_seqlens=cu) == want_packed
     # the normalised walk keeps an fp32 state and row partial sums
     nblk = -(-f // 512)
