@@ -569,7 +569,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
 
   // Tensor maps.
   const uint64_t M = uint64_t(P.M);
-  CUtensorMap tm_h, tm_wg, tm_wu, tm_a, tm_wt, tm_vmn, tm_zmn, tm_zk, tm_snap;
+  CUtensorMap tm_h, tm_wg, tm_wu, tm_a, tm_wt, tm_wt128, tm_vmn, tm_zmn, tm_zk, tm_snap;
   if ((s = make_map(&tm_h, H->data, d, M, 64, 128, "H"))) return s;
   if ((s = make_map(&tm_wg, W_gate->data, d, f, 64, 128, "W_gate"))) return s;
   if ((s = make_map(&tm_wu, W_up->data, d, f, 64, 128, "W_up"))) return s;
@@ -579,6 +579,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     return s;
   }
   if ((s = make_map(&tm_wt, W_target->data, d, d, 64, 256, "W_target"))) return s;
+  if ((s = make_map(&tm_wt128, W_target->data, d, d, 64, 128, "W_target (pair)"))) return s;
   // Output maps for the epilogues' TMA stores (Z's is tm_zk).
   CUtensorMap tm_vs, tm_ss, tm_os;
   memset(&tm_ss, 0, sizeof(tm_ss));
@@ -632,15 +633,29 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   }
   ITTT_STEP(rec(2 * ITTT_PHASE_CONV + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_TARGET, stream), "event record");
-  ITTT_STEP(ittt::launch_target(env, tm_a, tm_wt, tm_vs, cw,
-                                o.eta_tok ? static_cast<const float*>(o.eta_tok->data) : nullptr,
-                                vhat, eta, int(M), int(T), int(d), int(chunk), int(o.pad_mode),
-                                fused),
-            "target launch");
+  if (what == nullptr) {
+    const float* et = o.eta_tok ? static_cast<const float*>(o.eta_tok->data) : nullptr;
+    // CTA pairs where two can be resident (split convolution), else one CTA.
+    e = fused ? cudaErrorNotSupported
+              : ittt::launch_target_pair(env, tm_a, tm_wt128, tm_vs, et, vhat, eta, int(M),
+                                         int(d));
+    if (e == cudaErrorNotSupported) {
+      cudaGetLastError();
+      e = ittt::launch_target(env, tm_a, tm_wt, tm_vs, cw, et, vhat, eta, int(M), int(T), int(d),
+                              int(chunk), int(o.pad_mode), fused);
+    }
+    if (e != cudaSuccess) what = "target launch";
+  }
   ITTT_STEP(rec(2 * ITTT_PHASE_TARGET + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP, stream), "event record");
-  ITTT_STEP(ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d)),
-            "gate/up launch");
+  if (what == nullptr) {
+    e = ittt::launch_gateup_pair(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d));
+    if (e == cudaErrorNotSupported) {
+      cudaGetLastError();
+      e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d));
+    }
+    if (e != cudaSuccess) what = "gate/up launch";
+  }
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_SNAPSHOT0, stream), "event record");
   if (!dual) {

@@ -34,7 +34,7 @@ struct ApplyParams {
 // clipped).  Otherwise (fp32 O, or a tile that ends inside a 64-row half):
 // direct 16-byte stores of the valid rows.
 __device__ __forceinline__ void apply_epilogue(const ApplyParams& p, int arow0, int rows_valid,
-                                             int n0, int row, uint32_t trow, EpiStager& st) {
+                                               int n0, int row, uint32_t trow, EpiStager& st) {
   if (!p.out_fp32 && (rows_valid == kBM || rows_valid == 64)) {
 #pragma unroll 1
     for (int g = 0; g < kBN / 64; ++g) {

@@ -8,8 +8,14 @@
 // gate pre-activations in TMEM columns 0..127 and up pre-activations in
 // 128..255.  The epilogue pairs column j with column j + 128 and writes
 // 128 bf16 Z columns.
+//
+// On CTA pairs (the default) a unit is 256 rows: each CTA keeps its 128 H
+// rows, the leader loads the W_gate rows of the f-range and its peer the
+// W_up rows, so the pair MMA leaves [gate | up] in each CTA's TMEM exactly
+// as above.
 #include "kernels.h"
 #include "pipeline.cuh"
+#include "pipeline_pair.cuh"
 
 namespace ittt {
 namespace {
@@ -24,6 +30,39 @@ struct GateUpParams {
   int M, f;
   int m_tiles, n_tiles, kblocks, raster;
 };
+
+// 128 Z columns as two 64-column TMA stores; rows >= M and columns >= f
+// fall outside the tensor map and are not written.
+__device__ __forceinline__ void gateup_epilogue(const GateUpParams& p, int m0, int n0,
+                                                uint32_t trow, EpiStager& st) {
+#pragma unroll 1
+  for (int g = 0; g < kGateUpTileN / 64; ++g) {
+    uint8_t* buf = st.acquire();
+#pragma unroll 1
+    for (int hc = 0; hc < 2; ++hc) {
+      const int c = g * 64 + hc * 32;
+      uint32_t gv[32], uv[32];
+      tmem_ld_32cols(trow + uint32_t(c), gv);
+      tmem_ld_32cols(trow + uint32_t(kGateUpTileN + c), uv);
+      tmem_wait_ld();
+      pin_regs(gv);
+      pin_regs(uv);
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
+        const float u0 = __uint_as_float(uv[2 * j]), u1 = __uint_as_float(uv[2 * j + 1]);
+        const float z0 = g0 / (1.0f + __expf(-g0)) * u0;
+        const float z1 = g1 / (1.0f + __expf(-g1)) * u1;
+        pk[j] = pack_bf16x2(z0, z1);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st.put(buf, hc * 4 + q, make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
+    }
+    st.commit(buf, [&](uint8_t* src) { tma_store_2d(&p.tm_zs, src, n0 + g * 64, m0); });
+  }
+}
 
 struct GateUpSched : SchedDefaults {
   using Params = GateUpParams;
@@ -62,36 +101,8 @@ struct GateUpSched : SchedDefaults {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
   }
 
-  // 128 Z columns as two 64-column TMA stores; rows >= M and columns >= f
-  // fall outside the tensor map and are not written.
   __device__ void epilogue(int, int, uint32_t trow, EpiStager& st) const {
-#pragma unroll 1
-    for (int g = 0; g < kGateUpTileN / 64; ++g) {
-      uint8_t* buf = st.acquire();
-#pragma unroll 1
-      for (int hc = 0; hc < 2; ++hc) {
-        const int c = g * 64 + hc * 32;
-        uint32_t gv[32], uv[32];
-        tmem_ld_32cols(trow + uint32_t(c), gv);
-        tmem_ld_32cols(trow + uint32_t(kGateUpTileN + c), uv);
-        tmem_wait_ld();
-        pin_regs(gv);
-        pin_regs(uv);
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
-          const float u0 = __uint_as_float(uv[2 * j]), u1 = __uint_as_float(uv[2 * j + 1]);
-          const float z0 = g0 / (1.0f + __expf(-g0)) * u0;
-          const float z1 = g1 / (1.0f + __expf(-g1)) * u1;
-          pk[j] = pack_bf16x2(z0, z1);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st.put(buf, hc * 4 + q, make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]));
-      }
-      st.commit(buf, [&](uint8_t* src) { tma_store_2d(&p.tm_zs, src, n0 + g * 64, m0); });
-    }
+    gateup_epilogue(p, m0, n0, trow, st);
   }
 };
 
@@ -100,7 +111,80 @@ __global__ void __launch_bounds__(PipeShape<GateUpSched>::kThreads, 1)
   run_pipeline<GateUpSched>(p, status);
 }
 
+struct GateUpPairSched : PairDefaults {
+  using Params = GateUpParams;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, kBN, false, false);
+  static constexpr bool kStagedStores = true;
+
+  const Params& p;
+  const int rank;
+  int m0 = 0, n0 = 0, acc = 0;
+
+  __device__ GateUpPairSched(const Params& pp, uint32_t r) : p(pp), rank(int(r)) {}
+  __device__ int num_units() const { return p.m_tiles * p.n_tiles; }
+  __device__ void begin_unit(int u, int local) {
+    int m, n;
+    raster_grouped(u, p.m_tiles, p.n_tiles, p.raster, m, n);
+    m0 = m * (2 * kBM) + rank * kBM;
+    n0 = n * kGateUpTileN;
+    acc = local & 1;
+  }
+  __device__ int num_segments() const { return 1; }
+  __device__ int seg_acc(int) const { return acc; }
+  __device__ int seg_kblocks(int) const { return p.kblocks; }
+  __device__ bool seg_fresh(int) const { return true; }
+  __device__ void load(int, int kb, uint8_t* stage, uint32_t bar) const {
+    const int k = kb * kBK;
+    tma_load_2d_pair(stage, &p.tm_h, bar, k, m0);
+    tma_load_2d_pair(stage + kPairATileBytes, rank == 0 ? &p.tm_wg : &p.tm_wu, bar, k, n0);
+  }
+  static __device__ uint64_t a_desc(uint32_t base, int k) {
+    return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
+  }
+  static __device__ uint64_t b_desc(uint32_t base, int k) {
+    return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
+  }
+  __device__ void epilogue(int, int, uint32_t trow, EpiStager& st) const {
+    gateup_epilogue(p, m0, n0, trow, st);
+  }
+};
+
+__global__ void __launch_bounds__(kBaseThreads, 1)
+    gateup_pair_kernel(const __grid_constant__ GateUpParams p, unsigned int* status) {
+  run_pipeline_pair<GateUpPairSched>(p, status);
+}
+
 }  // namespace
+
+cudaError_t launch_gateup_pair(const LaunchEnv& env, const CUtensorMap& tm_h,
+                               const CUtensorMap& tm_wg, const CUtensorMap& tm_wu,
+                               const CUtensorMap& tm_zs, int M, int f, int K) {
+  GateUpParams p;
+  p.tm_h = tm_h;
+  p.tm_wg = tm_wg;
+  p.tm_wu = tm_wu;
+  p.tm_zs = tm_zs;
+  p.M = M;
+  p.f = f;
+  p.m_tiles = (M + 2 * kBM - 1) / (2 * kBM);
+  p.n_tiles = (f + kGateUpTileN - 1) / kGateUpTileN;
+  p.kblocks = (K + kBK - 1) / kBK;
+  p.raster = p.n_tiles < 16 ? p.n_tiles : 16;
+  const int units = p.m_tiles * p.n_tiles;
+  if (units == 0) return cudaSuccess;
+  const size_t smem = pair_smem_bytes<GateUpPairSched>();
+  cudaError_t e = cudaFuncSetAttribute(gateup_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  static std::atomic<int> resident{-1};
+  int pairs = 0;
+  if ((e = max_pairs(reinterpret_cast<const void*>(gateup_pair_kernel), smem, env, &pairs,
+                     &resident)) != cudaSuccess)
+    return e;
+  if (pairs < 1) return cudaErrorNotSupported;
+  if (units < pairs) pairs = units;
+  return launch_on_pairs(reinterpret_cast<const void*>(gateup_pair_kernel), pairs, smem, env, &p);
+}
 
 cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h, const CUtensorMap& tm_wg,
                           const CUtensorMap& tm_wu, const CUtensorMap& tm_zs, int M, int f, int K) {

@@ -28,6 +28,7 @@
 // here with the whole eta on the value side).
 #include "kernels.h"
 #include "pipeline.cuh"
+#include "pipeline_pair.cuh"
 
 namespace ittt {
 namespace {
@@ -131,6 +132,41 @@ struct TargetParams {
   int M, T, d, C, pad_mode;
   int m_tiles, n_tiles, kblocks, raster;
 };
+
+// The update's rate for token row gm: eta, times its per-token weight.
+__device__ __forceinline__ float target_row_rate(const TargetParams& p, int gm) {
+  return p.eta_tok == nullptr ? p.eta : (gm < p.M ? p.eta * __ldg(p.eta_tok + gm) : 0.0f);
+}
+
+// Split variant's epilogue: 256 columns of rows m0.. as four 64-column TMA
+// stores (rows >= M and columns >= d are not written).
+__device__ __forceinline__ void target_epilogue(const TargetParams& p, int m0, int n0, int row,
+                                                uint32_t trow, EpiStager& st) {
+  const float scale = target_row_rate(p, m0 + row);
+#pragma unroll 1
+  for (int g = 0; g < kBN / 64; ++g) {
+    uint8_t* buf = st.acquire();
+#pragma unroll 1
+    for (int hc = 0; hc < 2; ++hc) {
+      uint32_t v[32];
+      tmem_ld_32cols(trow + uint32_t(g * 64 + hc * 32), v);
+      tmem_wait_ld();
+      pin_regs(v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        st.put(buf, hc * 4 + q,
+               make_uint4(pack_bf16x2(scale * __uint_as_float(v[8 * q]),
+                                      scale * __uint_as_float(v[8 * q + 1])),
+                          pack_bf16x2(scale * __uint_as_float(v[8 * q + 2]),
+                                      scale * __uint_as_float(v[8 * q + 3])),
+                          pack_bf16x2(scale * __uint_as_float(v[8 * q + 4]),
+                                      scale * __uint_as_float(v[8 * q + 5])),
+                          pack_bf16x2(scale * __uint_as_float(v[8 * q + 6]),
+                                      scale * __uint_as_float(v[8 * q + 7]))));
+    }
+    st.commit(buf, [&](uint8_t* src) { tma_store_2d(&p.tm_vs, src, n0 + g * 64, m0); });
+  }
+}
 
 template <bool kFused>
 struct TargetSched : SchedDefaults {
@@ -261,38 +297,12 @@ struct TargetSched : SchedDefaults {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
   }
 
-  // The update's rate for token row gm: eta, times its per-token weight.
-  __device__ float row_rate(int gm) const {
-    return p.eta_tok == nullptr ? p.eta : (gm < p.M ? p.eta * __ldg(p.eta_tok + gm) : 0.0f);
-  }
+  __device__ float row_rate(int gm) const { return target_row_rate(p, gm); }
 
   // Split variant: 256 columns as four 64-column TMA stores (rows >= M and
   // columns >= d are not written).
   __device__ void epilogue(int, int row, uint32_t trow, EpiStager& st) const {
-    const float scale = row_rate(m0 + row);
-#pragma unroll 1
-    for (int g = 0; g < kBN / 64; ++g) {
-      uint8_t* buf = st.acquire();
-#pragma unroll 1
-      for (int hc = 0; hc < 2; ++hc) {
-        uint32_t v[32];
-        tmem_ld_32cols(trow + uint32_t(g * 64 + hc * 32), v);
-        tmem_wait_ld();
-        pin_regs(v);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          st.put(buf, hc * 4 + q,
-                 make_uint4(pack_bf16x2(scale * __uint_as_float(v[8 * q]),
-                                        scale * __uint_as_float(v[8 * q + 1])),
-                            pack_bf16x2(scale * __uint_as_float(v[8 * q + 2]),
-                                        scale * __uint_as_float(v[8 * q + 3])),
-                            pack_bf16x2(scale * __uint_as_float(v[8 * q + 4]),
-                                        scale * __uint_as_float(v[8 * q + 5])),
-                            pack_bf16x2(scale * __uint_as_float(v[8 * q + 6]),
-                                        scale * __uint_as_float(v[8 * q + 7]))));
-      }
-      st.commit(buf, [&](uint8_t* src) { tma_store_2d(&p.tm_vs, src, n0 + g * 64, m0); });
-    }
+    target_epilogue(p, m0, n0, row, trow, st);
   }
 
   // Fused variant: direct 16-byte stores.
@@ -331,6 +341,51 @@ __global__ void __launch_bounds__(PipeShape<TargetSched<kFused>>::kThreads, 1)
   run_pipeline<TargetSched<kFused>>(p, status);
 }
 
+// CTA pairs (split convolution only): a unit is a 256-row x 256-column
+// tile; each CTA keeps its 128 Xc rows and 128 of the W_target rows.
+struct TargetPairSched : PairDefaults {
+  using Params = TargetParams;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, kBN, false, false);
+  static constexpr bool kStagedStores = true;
+
+  const Params& p;
+  const int rank;
+  int m0 = 0, n0 = 0, acc = 0;
+
+  __device__ TargetPairSched(const Params& pp, uint32_t r) : p(pp), rank(int(r)) {}
+  __device__ int num_units() const { return p.m_tiles * p.n_tiles; }
+  __device__ void begin_unit(int u, int local) {
+    int m, n;
+    raster_grouped(u, p.m_tiles, p.n_tiles, p.raster, m, n);
+    m0 = m * (2 * kBM) + rank * kBM;
+    n0 = n * kBN;
+    acc = local & 1;
+  }
+  __device__ int num_segments() const { return 1; }
+  __device__ int seg_acc(int) const { return acc; }
+  __device__ int seg_kblocks(int) const { return p.kblocks; }
+  __device__ bool seg_fresh(int) const { return true; }
+  __device__ void load(int, int kb, uint8_t* stage, uint32_t bar) const {
+    const int k = kb * kBK;
+    tma_load_2d_pair(stage, &p.tm_a, bar, k, m0);
+    tma_load_2d_pair(stage + kPairATileBytes, &p.tm_wt, bar, k, n0 + rank * kBM);
+  }
+  static __device__ uint64_t a_desc(uint32_t base, int k) {
+    return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
+  }
+  static __device__ uint64_t b_desc(uint32_t base, int k) {
+    return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
+  }
+  __device__ void epilogue(int, int row, uint32_t trow, EpiStager& st) const {
+    target_epilogue(p, m0, n0, row, trow, st);
+  }
+};
+
+__global__ void __launch_bounds__(kBaseThreads, 1)
+    target_pair_kernel(const __grid_constant__ TargetParams p, unsigned int* status) {
+  run_pipeline_pair<TargetPairSched>(p, status);
+}
+
 template <bool kFused>
 cudaError_t launch_target_variant(const LaunchEnv& env, const TargetParams& p, int units) {
   using S = TargetSched<kFused>;
@@ -356,6 +411,40 @@ cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const flo
   if (blocks > cap) blocks = cap;
   conv3_kernel<<<int(blocks), 256, 0, env.stream>>>(x0, conv_w, xc, rows, docs, d, pad_mode);
   return cudaGetLastError();
+}
+
+cudaError_t launch_target_pair(const LaunchEnv& env, const CUtensorMap& tm_xc,
+                               const CUtensorMap& tm_wt, const CUtensorMap& tm_vs,
+                               const float* eta_tok, __nv_bfloat16* vhat, float eta, int M,
+                               int d) {
+  TargetParams p;
+  memset(&p, 0, sizeof(p));
+  p.eta_tok = eta_tok;
+  p.tm_a = tm_xc;
+  p.tm_wt = tm_wt;
+  p.tm_vs = tm_vs;
+  p.vhat = vhat;
+  p.eta = eta;
+  p.M = M;
+  p.d = d;
+  p.m_tiles = (M + 2 * kBM - 1) / (2 * kBM);
+  p.n_tiles = (d + kBN - 1) / kBN;
+  p.kblocks = (d + kBK - 1) / kBK;
+  p.raster = p.n_tiles < 16 ? p.n_tiles : 16;
+  const int units = p.m_tiles * p.n_tiles;
+  if (units == 0) return cudaSuccess;
+  const size_t smem = pair_smem_bytes<TargetPairSched>();
+  cudaError_t e = cudaFuncSetAttribute(target_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  static std::atomic<int> resident{-1};
+  int pairs = 0;
+  if ((e = max_pairs(reinterpret_cast<const void*>(target_pair_kernel), smem, env, &pairs,
+                     &resident)) != cudaSuccess)
+    return e;
+  if (pairs < 1) return cudaErrorNotSupported;
+  if (units < pairs) pairs = units;
+  return launch_on_pairs(reinterpret_cast<const void*>(target_pair_kernel), pairs, smem, env, &p);
 }
 
 cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a, const CUtensorMap& tm_wt,

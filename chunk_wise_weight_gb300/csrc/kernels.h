@@ -99,6 +99,12 @@ cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h,
                           const CUtensorMap& tm_wg, const CUtensorMap& tm_wu,
                           const CUtensorMap& tm_zs, int M, int f, int K);
 
+// The same on CTA pairs (256-row tiles); cudaErrorNotSupported when no pair
+// can be resident (nothing launched).
+cudaError_t launch_gateup_pair(const LaunchEnv& env, const CUtensorMap& tm_h,
+                               const CUtensorMap& tm_wg, const CUtensorMap& tm_wu,
+                               const CUtensorMap& tm_zs, int M, int f, int K);
+
 // Xc = three-tap depthwise conv of X0 (zero padding at chunk edges, or only
 // at document edges when pad_mode = 1), rounded to bf16.  x0, xc: [rows, d].
 cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const float* conv_w,
@@ -115,6 +121,14 @@ cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a,
                           const CUtensorMap& tm_wt, const CUtensorMap& tm_vs,
                           const float* conv_w, const float* eta_tok, __nv_bfloat16* vhat,
                           float eta, int M, int T, int d, int C, int pad_mode, bool fused);
+
+// The split variant on CTA pairs (256-row tiles): tm_xc maps Xc [M, d] box
+// {64,128}, tm_wt maps W_target [d, d] box {64,128}, tm_vs as above.
+// cudaErrorNotSupported when no pair can be resident (nothing launched).
+cudaError_t launch_target_pair(const LaunchEnv& env, const CUtensorMap& tm_xc,
+                               const CUtensorMap& tm_wt, const CUtensorMap& tm_vs,
+                               const float* eta_tok, __nv_bfloat16* vhat, float eta, int M,
+                               int d);
 
 // Slot docs.first_chunk(k) of snap = bf16(W_0 of document k) for every k.
 // w0 is bf16 or fp32, [d, f] shared (w0_bstride = 0) or one per document.
