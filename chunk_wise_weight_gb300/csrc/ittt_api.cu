@@ -249,6 +249,7 @@ struct Plan {
   int64_t nslots = 0;  // snapshot slots = chunks over all documents
   int64_t n = 0;       // chunks per sequence (regular)
   bool final_update = false;
+  bool ragged_walk = false;  // an updated chunk is not a multiple of 64 tokens
   int n_udocs = 0;     // documents that run at least one update
   int64_t ntiles = 0;   // 128-row tiles over all chunks (the apply's row units)
   int64_t ntiles2 = 0;  // 256-row tiles over all chunks (row units on CTA pairs)
@@ -364,6 +365,12 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
     P->ntiles = tiles;
     P->ntiles2 = tiles2;
     for (int q = 0; q < P->n_udocs; ++q) ud[q] = upd[size_t(q)].second;
+    P->ragged_walk = chunk % 64 != 0;
+    if (P->final_update)
+      for (int64_t k = 0; k < nd; ++k) {
+        const int64_t L = cu[k + 1] - cu[k];
+        if ((L - ((L + chunk - 1) / chunk - 1) * chunk) % 64 != 0) P->ragged_walk = true;
+      }
   } else {
     P->ndocs = B;
     P->n = (T + chunk - 1) / chunk;  // the last chunk may be partial
@@ -372,6 +379,7 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
     if (P->l2norm && P->n_udocs > 0)
       P->active.assign(size_t(P->final_update ? P->n : P->n - 1), int(B));
     const int64_t last = T - (P->n - 1) * chunk;
+    P->ragged_walk = chunk % 64 != 0 || (P->final_update && last % 64 != 0);
     P->ntiles = B * ((P->n - 1) * ((chunk + 127) / 128) + (last + 127) / 128);
     P->ntiles2 = B * ((P->n - 1) * ((chunk + 255) / 256) + (last + 255) / 256);
   }
@@ -687,6 +695,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     ua.w0_fp32 = w0_fp32;
     ua.w0_bstride = w0_bstride;
     ua.state_out = o.state_out ? static_cast<float*>(o.state_out->data) : nullptr;
+    ua.allow_pairs = !P.ragged_walk;
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");
     if (P.l2norm) {
       ittt::NormUpdateArgs na;

@@ -295,6 +295,7 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
     ua.w0_fp32 = w0_fp32;
     ua.w0_bstride = 0;
     ua.state_out = nullptr;
+    ua.allow_pairs = false;
     if ((e = ittt::launch_update(env, tm_vmn, tm_zmn, tm_ss, ua)) != cudaSuccess) {
       what = "update";
     } else if ((e = ittt::launch_apply(env, tm_zk, tm_snap, tm_os, out->data,

@@ -21,8 +21,11 @@
 // length is not a multiple of 64 ends inside a stage: the MMA thread zeroes
 // the token lines past its end (within the last 16-token slice it issues)
 // and skips the slices after them.
+#include <type_traits>
+
 #include "kernels.h"
 #include "pipeline.cuh"
+#include "pipeline_pair.cuh"
 
 namespace ittt {
 namespace {
@@ -100,8 +103,9 @@ struct UpdateParams {
   int n_udocs;
   int final_update;     // also update with the last chunk (for state_out)
   int d, f;
-  int MT, NH, NP;       // 128-row blocks of d_model; 256- and 512-column blocks of d_ff
-  int P;                // pairs: documents x MT x NP
+  int MT, NH, NP;       // row blocks of d_model (128 rows, 256 on CTA pairs);
+                        // 256- and 512-column blocks of d_ff
+  int P;                // pairs of halves: documents x MT x NP
   int RG;               // pairs walked whole: full rounds over the grid
   int split;            // the last partial round walks its halves one by one
 };
@@ -114,20 +118,27 @@ struct UpdateParams {
 // overlaps the other half's MMAs.  When the pairs do not fill the last round
 // (Q pairs left, 2Q <= CTAs) those pairs are walked as 2Q single halves on
 // as many CTAs, which shortens the longest CTA by one half-walk.
-struct UpdateSched : SchedDefaults {
+//
+// On CTA pairs (kPair; every chunk a multiple of 64 tokens) a block is 256
+// d_model rows: each CTA keeps its 128 rows of eta*Vhat^T and 128 of the
+// half's 256 Z columns in shared memory, and its 128 state rows of both
+// halves in its own TMEM.
+template <bool kPair>
+struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
   using Params = UpdateParams;
-  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true, true);
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kPair ? 2 * kBM : kBM, kBN, true, true);
   static constexpr bool kPreload = true;
   static constexpr bool kStagedStores = true;
-  static constexpr bool kRaggedK = true;
+  static constexpr bool kRaggedK = !kPair;
 
   const Params& p;
+  const int rank;
   int nh = 0;                 // halves in this unit (0, 1 or 2)
   int doc = 0, m0 = 0, tok0 = 0, slot0 = 0;
   int hn0[2] = {0, 0};        // first d_ff column of each half
   int len = 0, nch = 0, nupd = 0;
 
-  __device__ explicit UpdateSched(const Params& pp) : p(pp) {}
+  __device__ explicit UpdateSchedT(const Params& pp, uint32_t r = 0) : p(pp), rank(int(r)) {}
   __device__ int num_units() const {
     return p.split ? p.RG + 2 * (p.P - p.RG) : p.P;
   }
@@ -145,7 +156,7 @@ struct UpdateSched : SchedDefaults {
     nh = min(want, p.NH - hb0);
     if (nh < 0) nh = 0;
     doc = p.upd_docs ? __ldg(p.upd_docs + q) : q;
-    m0 = (r % p.MT) * kBM;
+    m0 = kPair ? (r % p.MT) * (2 * kBM) + rank * kBM : (r % p.MT) * kBM;
     hn0[0] = hb0 * kBN;
     hn0[1] = (hb0 + 1) * kBN;
     tok0 = p.docs.start(doc);
@@ -171,6 +182,18 @@ struct UpdateSched : SchedDefaults {
     const int h = s - i * nh;
     load_update_stage(p.tm_v, p.tm_z, stage, bar, m0, h ? hn0[1] : hn0[0],
                       tok0 + i * p.docs.C + kb * kBK);
+  }
+  // CTA pairs: this CTA's 128 rows of eta*Vhat^T (two boxes) and its 128 of
+  // the half's Z columns (two boxes).
+  __device__ void load(int s, int kb, uint8_t* stage, uint32_t bar) const {
+    const int i = seg_chunk(s);
+    const int h = s - i * nh;
+    const int tok = tok0 + i * p.docs.C + kb * kBK;
+    const int n0 = (h ? hn0[1] : hn0[0]) + rank * kBM;
+    tma_load_2d_pair(stage, &p.tm_v, bar, m0, tok);
+    tma_load_2d_pair(stage + kMnBoxBytes, &p.tm_v, bar, m0 + 64, tok);
+    tma_load_2d_pair(stage + kPairATileBytes, &p.tm_z, bar, n0, tok);
+    tma_load_2d_pair(stage + kPairATileBytes + kMnBoxBytes, &p.tm_z, bar, n0 + 64, tok);
   }
   __device__ void clear_k(uint8_t* stage, int from, int to) const {
     clear_token_lines(stage, from, to);
@@ -252,9 +275,17 @@ struct UpdateSched : SchedDefaults {
   }
 };
 
+using UpdateSched = UpdateSchedT<false>;
+using UpdatePairSched = UpdateSchedT<true>;
+
 __global__ void __launch_bounds__(PipeShape<UpdateSched>::kThreads, 1)
     update_kernel(const __grid_constant__ UpdateParams p, unsigned int* status) {
   run_pipeline<UpdateSched>(p, status);
+}
+
+__global__ void __launch_bounds__(kBaseThreads, 1)
+    update_pair_kernel(const __grid_constant__ UpdateParams p, unsigned int* status) {
+  run_pipeline_pair<UpdatePairSched>(p, status);
 }
 
 // ----------------------------------------------------------------------------
@@ -553,18 +584,36 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
   p.final_update = a.final_update ? 1 : 0;
   p.d = a.d;
   p.f = a.f;
-  p.MT = (a.d + kBM - 1) / kBM;
   p.NH = (a.f + kBN - 1) / kBN;
   p.NP = (a.f + 2 * kBN - 1) / (2 * kBN);
+  // The grid's width in units: CTA pairs when every updated chunk is a
+  // multiple of 64 tokens and pairs can be resident, else single CTAs.
+  static std::atomic<int> resident{-1};
+  const size_t psmem = pair_smem_bytes<UpdatePairSched>();
+  int pairs = 0;
+  cudaError_t e = cudaSuccess;
+  if (a.allow_pairs) {
+    if ((e = cudaFuncSetAttribute(update_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(psmem))) != cudaSuccess)
+      return e;
+    if ((e = max_pairs(reinterpret_cast<const void*>(update_pair_kernel), psmem, env, &pairs,
+                       &resident)) != cudaSuccess)
+      return e;
+  }
+  const bool use_pairs = pairs >= 1;
+  const int width = use_pairs ? pairs : env.num_sms;
+  p.MT = use_pairs ? (a.d + 2 * kBM - 1) / (2 * kBM) : (a.d + kBM - 1) / kBM;
   const int64_t P = int64_t(p.n_udocs) * p.MT * p.NP;
-  const int64_t Q = P % env.num_sms;
+  const int64_t Q = P % width;
   p.P = int(P);
   p.RG = int(P - Q);
-  p.split = (Q > 0 && 2 * Q <= env.num_sms) ? 1 : 0;
+  p.split = (Q > 0 && 2 * Q <= width) ? 1 : 0;
   const int64_t units = p.split ? p.RG + 2 * Q : P;
-  const int grid = int(units < env.num_sms ? units : env.num_sms);
-  cudaError_t e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(pipe_smem_bytes<UpdateSched>()));
+  const int grid = int(units < width ? units : width);
+  if (use_pairs)
+    return launch_on_pairs(reinterpret_cast<const void*>(update_pair_kernel), grid, psmem, env, &p);
+  e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(pipe_smem_bytes<UpdateSched>()));
   if (e != cudaSuccess) return e;
   update_kernel<<<grid, PipeShape<UpdateSched>::kThreads, pipe_smem_bytes<UpdateSched>(), env.stream>>>(p, env.status);
   return cudaGetLastError();

@@ -146,6 +146,7 @@ struct UpdateArgs {
   bool w0_fp32;
   int64_t w0_bstride;
   float* state_out;     // [documents, d, f] fp32 or nullptr
+  bool allow_pairs;     // every updated chunk is a multiple of 64 tokens
 };
 
 // Fast-weight update walk: for each (document, 128 x 512 state tile) the
