@@ -3,10 +3,10 @@
 // ("[논문리뷰] In-Place Test-Time Training", Method §2 eq. (5); causal
 // padding from Method §3), in two variants with identical results:
 //
-// Split (default): conv3_kernel streams X0 once (one thread per 8 channels
-// of a token row, 128-bit loads of rows t-1, t, t+1, fp32 taps, one bf16
-// rounding) into Xc; the host runs it beside the gate/up GEMM, and the
-// target GEMM then TMA-loads Xc as its A operand.
+// Split (default): conv3_kernel streams X0 once (a thread owns 8 channels of
+// 8 consecutive token rows: 128-bit loads of the 10-row window, fp32 taps,
+// one bf16 rounding) into Xc, and the target GEMM then TMA-loads Xc as its A
+// operand.
 //
 // Fused: the GEMM builds each A tile itself.  Per 64-channel K block the
 // producer loads, besides the W_target tile, a TMA box of the 130 X0 rows
@@ -63,32 +63,33 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(uint64_t v) {
   return pack_bf16x2(__uint_as_float(uint32_t(v)), __uint_as_float(uint32_t(v >> 32)));
 }
 
+// Rows per thread of conv3_kernel: a thread loads kConvRows + 2 rows of its
+// 8 channels once and writes kConvRows (a sliding window instead of three
+// loads per output row).
+constexpr int kConvRows = 8;
+
 __global__ void __launch_bounds__(256)
     conv3_kernel(const __nv_bfloat16* __restrict__ x0, const float* __restrict__ conv_w,
                  __nv_bfloat16* __restrict__ xc, int64_t rows, DocMap docs, int d,
                  int pad_mode) {
   const int groups = d >> 3;
-  const int64_t total = rows * groups;
+  const int64_t blocks = (rows + kConvRows - 1) / kConvRows;
+  const int64_t total = blocks * groups;
   for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = idx / groups;
-    const int g = int(idx - r * groups);
-    // Taps stay inside the token's document and, with chunk padding, inside
-    // its chunk (chunks start at the document's first token; the last one
-    // ends with the document).
-    const int t = int(r);
-    const int k = docs.doc_of_token(t);
-    int lo = docs.start(k);
-    int hi = lo + docs.len(k);
-    if (pad_mode == 0) {
-      lo += ((t - lo) / docs.C) * docs.C;
-      hi = min(lo + docs.C, hi);
-    }
-    const size_t base = size_t(r) * size_t(d) + size_t(g) * 8;
+    const int64_t rb = idx / groups;
+    const int g = int(idx - rb * groups);
+    const int64_t r0 = rb * kConvRows;
+    // Window rows r0-1 .. r0+kConvRows (those inside the tensor).
+    uint4 x[kConvRows + 2];
     const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-    const uint4 xm = (t - 1 >= lo) ? __ldg(reinterpret_cast<const uint4*>(x0 + base - d)) : zero4;
-    const uint4 x = __ldg(reinterpret_cast<const uint4*>(x0 + base));
-    const uint4 xp = (t + 1 < hi) ? __ldg(reinterpret_cast<const uint4*>(x0 + base + d)) : zero4;
+#pragma unroll
+    for (int j = 0; j < kConvRows + 2; ++j) {
+      const int64_t r = r0 - 1 + j;
+      x[j] = (r >= 0 && r < rows)
+                 ? __ldg(reinterpret_cast<const uint4*>(x0 + size_t(r) * size_t(d) + size_t(g) * 8))
+                 : zero4;
+    }
     float w[24];
     const float4* w4 = reinterpret_cast<const float4*>(conv_w + size_t(g) * 24);
 #pragma unroll
@@ -99,25 +100,45 @@ __global__ void __launch_bounds__(256)
       w[4 * q + 2] = v.z;
       w[4 * q + 3] = v.w;
     }
-    const uint32_t am[4] = {xm.x, xm.y, xm.z, xm.w};
-    const uint32_t a0[4] = {x.x, x.y, x.z, x.w};
-    const uint32_t ap[4] = {xp.x, xp.y, xp.z, xp.w};
-    uint32_t o[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 fm = unpack_bf16x2(am[q]);
-      const float2 f0 = unpack_bf16x2(a0[q]);
-      const float2 fp = unpack_bf16x2(ap[q]);
-      const int c0 = 2 * q, c1 = 2 * q + 1;  // channel within the group of 8
-      float y0 = w[3 * c0] * fm.x;
-      y0 = fmaf(w[3 * c0 + 1], f0.x, y0);
-      y0 = fmaf(w[3 * c0 + 2], fp.x, y0);
-      float y1 = w[3 * c1] * fm.y;
-      y1 = fmaf(w[3 * c1 + 1], f0.y, y1);
-      y1 = fmaf(w[3 * c1 + 2], fp.y, y1);
-      o[q] = pack_bf16x2(y0, y1);
+    for (int j = 0; j < kConvRows; ++j) {
+      const int64_t r = r0 + j;
+      if (r >= rows) break;
+      // Taps stay inside the token's document and, with chunk padding,
+      // inside its chunk (chunks start at the document's first token; the
+      // last one ends with the document).
+      const int t = int(r);
+      const int k = docs.doc_of_token(t);
+      int lo = docs.start(k);
+      int hi = lo + docs.len(k);
+      if (pad_mode == 0) {
+        lo += ((t - lo) / docs.C) * docs.C;
+        hi = min(lo + docs.C, hi);
+      }
+      const uint4 xm = t - 1 >= lo ? x[j] : zero4;
+      const uint4 xp = t + 1 < hi ? x[j + 2] : zero4;
+      const uint4 xx = x[j + 1];
+      const uint32_t am[4] = {xm.x, xm.y, xm.z, xm.w};
+      const uint32_t a0[4] = {xx.x, xx.y, xx.z, xx.w};
+      const uint32_t ap[4] = {xp.x, xp.y, xp.z, xp.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 fm = unpack_bf16x2(am[q]);
+        const float2 f0 = unpack_bf16x2(a0[q]);
+        const float2 fp = unpack_bf16x2(ap[q]);
+        const int c0 = 2 * q, c1 = 2 * q + 1;  // channel within the group of 8
+        float y0 = w[3 * c0] * fm.x;
+        y0 = fmaf(w[3 * c0 + 1], f0.x, y0);
+        y0 = fmaf(w[3 * c0 + 2], fp.x, y0);
+        float y1 = w[3 * c1] * fm.y;
+        y1 = fmaf(w[3 * c1 + 1], f0.y, y1);
+        y1 = fmaf(w[3 * c1 + 2], fp.y, y1);
+        o[q] = pack_bf16x2(y0, y1);
+      }
+      *reinterpret_cast<uint4*>(xc + size_t(r) * size_t(d) + size_t(g) * 8) =
+          make_uint4(o[0], o[1], o[2], o[3]);
     }
-    *reinterpret_cast<uint4*>(xc + base) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -404,7 +425,7 @@ cudaError_t launch_target_variant(const LaunchEnv& env, const TargetParams& p, i
 cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const float* conv_w,
                         __nv_bfloat16* xc, int64_t rows, const DocMap& docs, int d,
                         int pad_mode) {
-  const int64_t total = rows * (d / 8);
+  const int64_t total = (rows + kConvRows - 1) / kConvRows * (d / 8);
   if (total == 0) return cudaSuccess;
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = int64_t(env.num_sms) * 8;
