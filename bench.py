@@ -49,7 +49,7 @@ def kernel_source_hash(kernel: str) -> str:
     import hashlib
     csrc = os.path.join(ROOT, "chunk_wise_weight_gb300", "csrc")
     m = hashlib.sha1()
-    for f in KERNEL_SOURCES[kernel] + ["pipeline.cuh", "sm103.cuh"]:
+    for f in KERNEL_SOURCES[kernel] + ["pipeline.cuh", "pipeline_pair.cuh", "sm103.cuh"]:
         with open(os.path.join(csrc, f), "rb") as fh:
             m.update(fh.read())
     return m.hexdigest()[:16]

@@ -4,7 +4,7 @@
 // padding from Method §3), in two variants with identical results:
 //
 // Split (default): conv3_kernel streams X0 once (a thread owns 8 channels of
-// 8 consecutive token rows: 128-bit loads of the 10-row window, fp32 taps,
+// 4 consecutive token rows: 128-bit loads of the 6-row window, fp32 taps,
 // one bf16 rounding) into Xc, and the target GEMM then TMA-loads Xc as its A
 // operand.
 //
@@ -66,7 +66,7 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(uint64_t v) {
 // Rows per thread of conv3_kernel: a thread loads kConvRows + 2 rows of its
 // 8 channels once and writes kConvRows (a sliding window instead of three
 // loads per output row).
-constexpr int kConvRows = 8;
+constexpr int kConvRows = 4;
 
 __global__ void __launch_bounds__(256)
     conv3_kernel(const __nv_bfloat16* __restrict__ x0, const float* __restrict__ conv_w,
