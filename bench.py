@@ -158,15 +158,19 @@ def phase_model(B, T, d, f, C, dual=False, cu=None):
     }
 
 
-def launches_per_step(B, T, C, cu, l2norm):
-    """Kernel launches of one forward: conv, target, gate/up, snapshot 0, the
-    update walk (one launch, or with L2 normalisation one per chunk that
-    updates plus a finalising launch), apply; packed documents add the
-    table-staging kernel."""
+def launches_per_step(B, T, C, cu, l2norm, dual=False):
+    """Kernel launches of one forward with the bench's bf16 W_down0 and no
+    snapshot buffer: conv, target, gate/up, the update walk (one launch, or
+    with L2 normalisation one per chunk that updates plus a finalising
+    launch), apply (the apply reads W_0 itself, so no snapshot-0 copy);
+    packed documents add the table-staging kernel; the dual form runs scores
+    and dual apply instead of walk and apply."""
     lens = [b - a for a, b in zip(cu, cu[1:])] if cu else [T] * B
     steps = max(-(-L // C) - 1 for L in lens)
+    if dual:
+        return 5
     walk = (steps + 1 if l2norm else 1) if steps > 0 else 0
-    return 5 + walk + (1 if cu else 0)
+    return 4 + walk + (1 if cu else 0)
 
 
 def init_dist(args):
@@ -445,7 +449,7 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": launches_per_step(B, T, C, cu, args.l2norm) * args.steps,
+            "gpu_launches": launches_per_step(B, T, C, cu, args.l2norm, args.dual) * args.steps,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -598,7 +598,11 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if ((s = make_map(&tm_vmn, vhat, d, M, 64, 64, "Vhat"))) return s;
   if ((s = make_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
   if ((s = make_map(&tm_zk, z, f, M, 64, 128, "Z (apply)"))) return s;
-  CUtensorMap tm_zs, tm_w0b, tm_sc, tm_snap_pair;
+  CUtensorMap tm_zs, tm_w0b, tm_sc, tm_snap_pair, tm_w0d, tm_w0d_pair;
+  // The apply reads a shared bf16 W_0 itself for first chunks, so slot 0 of
+  // each document need not be copied (unless the caller asked for the
+  // snapshots).
+  const bool w0_direct = !dual && w0_is_bf16 && o.snap_buf == nullptr;
   auto* scores = reinterpret_cast<__nv_bfloat16*>(ws + L.scores);
   const void* w0b = w0_is_bf16 ? W_down0->data : static_cast<const void*>(ws + L.w0b);
   if (dual) {
@@ -611,6 +615,11 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     if ((s = make_map(&tm_snap_pair, snap, f, uint64_t(P.nslots * d), 64, 128,
                       "snapshots (pair)")))
       return s;
+    if (w0_direct) {
+      if ((s = make_map(&tm_w0d, W_down0->data, f, uint64_t(d), 64, 256, "W_0 (apply)"))) return s;
+      if ((s = make_map(&tm_w0d_pair, W_down0->data, f, uint64_t(d), 64, 128, "W_0 (apply, pair)")))
+        return s;
+    }
     if ((s = make_map_3d(&tm_ss, snap, f, d, uint64_t(P.nslots), 64, 128, "snapshots (store)")))
       return s;
   }
@@ -666,7 +675,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   }
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_SNAPSHOT0, stream), "event record");
-  if (!dual) {
+  if (!dual && !w0_direct) {
     ITTT_STEP(ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride, snap, docs, int(d), int(f)),
               "snapshot launch");
   } else if (!w0_is_bf16) {
@@ -721,12 +730,13 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
     if (what == nullptr) {
       // CTA pairs where two can be resident, else one CTA per tile.
-      e = ittt::launch_apply_pair(env, tm_zk, tm_snap_pair, tm_os, out->data,
-                                  out->dtype == ITTT_FP32, docs, int(d), int(f));
+      e = ittt::launch_apply_pair(env, tm_zk, tm_snap_pair, w0_direct ? &tm_w0d_pair : nullptr,
+                                  tm_os, out->data, out->dtype == ITTT_FP32, docs, int(d),
+                                  int(f));
       if (e == cudaErrorNotSupported) {
         cudaGetLastError();
-        e = ittt::launch_apply(env, tm_zk, tm_snap, tm_os, out->data, out->dtype == ITTT_FP32,
-                               docs, int(d), int(f));
+        e = ittt::launch_apply(env, tm_zk, tm_snap, w0_direct ? &tm_w0d : nullptr, tm_os,
+                               out->data, out->dtype == ITTT_FP32, docs, int(d), int(f));
       }
       if (e != cudaSuccess) what = "apply launch";
     }
@@ -835,8 +845,10 @@ int32_t ittt_launch_count(int64_t B, int64_t T, int64_t d, int64_t f, int64_t ch
     g_last_error = saved;
     return 0;
   }
-  // conv, target, gate/up, snapshot 0, update (when a chunk updates), apply
-  return ((T + chunk - 1) / chunk > 1) ? 6 : 5;
+  // conv, target, gate/up, update (when a chunk updates), apply; with a
+  // shared bf16 W_down0 and no snapshot buffer the apply reads W_0 itself,
+  // so no snapshot-0 copy is launched
+  return ((T + chunk - 1) / chunk > 1) ? 5 : 4;
 }
 
 }  // extern "C"

@@ -298,7 +298,7 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
     ua.allow_pairs = false;
     if ((e = ittt::launch_update(env, tm_vmn, tm_zmn, tm_ss, ua)) != cudaSuccess) {
       what = "update";
-    } else if ((e = ittt::launch_apply(env, tm_zk, tm_snap, tm_os, out->data,
+    } else if ((e = ittt::launch_apply(env, tm_zk, tm_snap, nullptr, tm_os, out->data,
                                        out->dtype == ITTT_FP32, docs, int(d), int(f))) !=
                cudaSuccess) {
       what = "apply";

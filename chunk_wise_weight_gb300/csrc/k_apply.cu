@@ -4,7 +4,9 @@
 // parallel as in Method §3 stage 3).
 //
 // W_i is the bf16 snapshot the update kernel wrote into the chunk's slot
-// (a document's first slot holds W_0).  A work unit is (128-row tile of a
+// (a document's first slot holds W_0; when W_0 is one shared bf16 matrix
+// and no caller snapshot buffer is given, first chunks read W_0 itself and
+// that slot is never written).  A work unit is (128-row tile of a
 // chunk, 256-column tile of d_model); only tiles that hold rows of their
 // chunk are enumerated (slot order), so short chunks leave no idle units in
 // the persistent schedule.  Rows past the chunk's end belong to another
@@ -21,11 +23,13 @@ namespace {
 
 struct ApplyParams {
   CUtensorMap tm_z;     // Z          [M, f]        box {64, 128}
-  CUtensorMap tm_snap;  // snapshots  [slots*d, f]  box {64, 256}
+  CUtensorMap tm_snap;  // snapshots  [slots*d, f]  box {64, 256} (pairs: {64, 128})
+  CUtensorMap tm_w0;    // bf16 W_0   [d, f], same box; read for first chunks when w0_direct
   CUtensorMap tm_os;    // bf16 O     [M, d]        box {64, 64} (store)
   void* out;            // O [M, d], bf16 or fp32
   int out_fp32;
   DocMap docs;
+  int w0_direct;        // a document's first chunk reads W_0 itself, not its snapshot slot
   int d, f;
   int nt, kblocks;
 };
@@ -103,6 +107,7 @@ struct ApplySched : SchedDefaults {
 
   const Params& p;
   int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0;
+  const CUtensorMap* bmap = nullptr;
 
   __device__ explicit ApplySched(const Params& pp) : p(pp) {}
   __device__ int num_units() const { return p.docs.ntiles * p.nt; }
@@ -114,7 +119,9 @@ struct ApplySched : SchedDefaults {
     const int i = g - p.docs.first_chunk(k);
     const int len = p.docs.len(k);
     arow0 = p.docs.start(k) + i * p.docs.C + mt * kBM;
-    brow0 = g * p.d + nt * kBN;
+    const bool first = i == 0 && p.w0_direct;
+    bmap = first ? &p.tm_w0 : &p.tm_snap;
+    brow0 = (first ? 0 : g * p.d) + nt * kBN;
     rows_valid = min(kBM, min(p.docs.C, len - i * p.docs.C) - mt * kBM);
     n0 = nt * kBN;
     acc = local & 1;
@@ -127,7 +134,7 @@ struct ApplySched : SchedDefaults {
   __device__ void load(int, int kb, uint8_t* stage, uint64_t* bar) const {
     const int k = kb * kBK;
     tma_load_2d(stage, &p.tm_z, bar, k, arow0);
-    tma_load_2d(stage + kATileBytes, &p.tm_snap, bar, k, brow0);
+    tma_load_2d(stage + kATileBytes, bmap, bar, k, brow0);
   }
   static __device__ uint64_t a_desc(uint32_t base, int k) {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
@@ -157,6 +164,7 @@ struct ApplyPairSched : PairDefaults {
   const Params& p;
   const int rank;
   int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0;
+  const CUtensorMap* bmap = nullptr;
 
   __device__ ApplyPairSched(const Params& pp, uint32_t r) : p(pp), rank(int(r)) {}
   __device__ int num_units() const { return p.docs.ntiles2 * p.nt; }
@@ -169,7 +177,9 @@ struct ApplyPairSched : PairDefaults {
     const int len = p.docs.len(k);
     const int r0 = mt * (2 * kBM) + rank * kBM;  // first row of this CTA's half in the chunk
     arow0 = p.docs.start(k) + i * p.docs.C + r0;
-    brow0 = g * p.d + nt * kBN + rank * kBM;
+    const bool first = i == 0 && p.w0_direct;
+    bmap = first ? &p.tm_w0 : &p.tm_snap;
+    brow0 = (first ? 0 : g * p.d) + nt * kBN + rank * kBM;
     rows_valid = min(kBM, min(p.docs.C, len - i * p.docs.C) - r0);
     n0 = nt * kBN;
     acc = local & 1;
@@ -181,7 +191,7 @@ struct ApplyPairSched : PairDefaults {
   __device__ void load(int, int kb, uint8_t* stage, uint32_t bar) const {
     const int k = kb * kBK;
     tma_load_2d_pair(stage, &p.tm_z, bar, k, arow0);
-    tma_load_2d_pair(stage + kPairATileBytes, &p.tm_snap, bar, k, brow0);
+    tma_load_2d_pair(stage + kPairATileBytes, bmap, bar, k, brow0);
   }
   static __device__ uint64_t a_desc(uint32_t base, int k) {
     return sdesc_sw128(base + uint32_t(k) * 32u, 16u, 1024u);
@@ -204,11 +214,14 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
 }  // namespace
 
 cudaError_t launch_apply_pair(const LaunchEnv& env, const CUtensorMap& tm_z,
-                              const CUtensorMap& tm_snap, const CUtensorMap& tm_os, void* out,
-                              bool out_fp32, const DocMap& docs, int d, int f) {
+                              const CUtensorMap& tm_snap, const CUtensorMap* tm_w0,
+                              const CUtensorMap& tm_os, void* out, bool out_fp32,
+                              const DocMap& docs, int d, int f) {
   ApplyParams p;
   p.tm_z = tm_z;
   p.tm_snap = tm_snap;
+  p.w0_direct = tm_w0 != nullptr ? 1 : 0;
+  p.tm_w0 = tm_w0 != nullptr ? *tm_w0 : tm_snap;
   p.tm_os = tm_os;
   p.out = out;
   p.out_fp32 = out_fp32 ? 1 : 0;
@@ -234,11 +247,13 @@ cudaError_t launch_apply_pair(const LaunchEnv& env, const CUtensorMap& tm_z,
 }
 
 cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z, const CUtensorMap& tm_snap,
-                         const CUtensorMap& tm_os, void* out, bool out_fp32, const DocMap& docs,
-                         int d, int f) {
+                         const CUtensorMap* tm_w0, const CUtensorMap& tm_os, void* out,
+                         bool out_fp32, const DocMap& docs, int d, int f) {
   ApplyParams p;
   p.tm_z = tm_z;
   p.tm_snap = tm_snap;
+  p.w0_direct = tm_w0 != nullptr ? 1 : 0;
+  p.tm_w0 = tm_w0 != nullptr ? *tm_w0 : tm_snap;
   p.tm_os = tm_os;
   p.out = out;
   p.out_fp32 = out_fp32 ? 1 : 0;

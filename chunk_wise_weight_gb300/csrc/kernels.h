@@ -185,16 +185,21 @@ cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
 // Tensor maps: Z [M, f] box {64,128}; snapshots [slots*d, f] box {64,256};
 // bf16 O [M, d] with box {64,64} for the TMA stores (unused for fp32 O).
 // Chunks of any length; a document's last chunk may be shorter than C.
+// tm_w0 (nullptr, or bf16 W_0 [d, f] with tm_snap's box): read instead of a
+// document's first snapshot slot, which is then never read.
 cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
-                         const CUtensorMap& tm_snap, const CUtensorMap& tm_os, void* out,
-                         bool out_fp32, const DocMap& docs, int d, int f);
+                         const CUtensorMap& tm_snap, const CUtensorMap* tm_w0,
+                         const CUtensorMap& tm_os, void* out, bool out_fp32,
+                         const DocMap& docs, int d, int f);
 
-// The same on CTA pairs (256-row tiles, tcgen05 cta_group::2): tm_snap has
-// box {64,128} (each CTA loads its 128 of the tile's 256 columns).  Returns
-// cudaErrorNotSupported when no pair can be resident (nothing launched).
+// The same on CTA pairs (256-row tiles, tcgen05 cta_group::2): tm_snap and
+// tm_w0 have box {64,128} (each CTA loads its 128 of the tile's 256
+// columns).  Returns cudaErrorNotSupported when no pair can be resident
+// (nothing launched).
 cudaError_t launch_apply_pair(const LaunchEnv& env, const CUtensorMap& tm_z,
-                              const CUtensorMap& tm_snap, const CUtensorMap& tm_os, void* out,
-                              bool out_fp32, const DocMap& docs, int d, int f);
+                              const CUtensorMap& tm_snap, const CUtensorMap* tm_w0,
+                              const CUtensorMap& tm_os, void* out, bool out_fp32,
+                              const DocMap& docs, int d, int f);
 
 // Dual form, scores: S[b, t, s] = Z_t . Z_s (bf16) for every token t of chunk
 // i >= 1 and every token s < i*C of the same sequence.  Tensor maps: Z

@@ -283,8 +283,11 @@ ITTT_API int32_t ittt_version(void);
 
 /*
  * Kernel launches one ittt_forward / ittt_forward_ex call makes for these
- * sizes with default options (for launch accounting; 0 if unsupported).
- * Packed documents add one (the table staging kernel).
+ * sizes with default options and a bf16 W_down0 (for launch accounting; 0
+ * if unsupported): conv, target, gate/up, the update walk when a chunk
+ * updates, apply.  An fp32 W_down0, state_in or snap_buf adds the snapshot-0
+ * copy; packed documents add the table staging kernel; ITTT_FLAG_L2_NORM
+ * launches the walk once per updating chunk plus a finalising launch.
  */
 ITTT_API int32_t ittt_launch_count(int64_t B, int64_t T, int64_t d, int64_t f,
                           int64_t chunk);

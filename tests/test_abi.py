@@ -189,9 +189,9 @@ def test_workspace_bytes_and_launch_count(lib):
     assert (ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True)
             == want + r(B * d * f * 4) + r(2 * B * nblk * d * 4))
     assert ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True, dual=True) == 0
-    assert ittt.launch_count(B, T, d, f, C) == 6
-    assert ittt.launch_count(B, T, d, f, T) == 5
-    assert ittt.launch_count(B, 1000, d, f, 512) == 6   # two chunks, the last partial
+    assert ittt.launch_count(B, T, d, f, C) == 5
+    assert ittt.launch_count(B, T, d, f, T) == 4
+    assert ittt.launch_count(B, 1000, d, f, 512) == 5   # two chunks, the last partial
     assert ittt.launch_count(B, T, d, f, 0) == 0
 
 
