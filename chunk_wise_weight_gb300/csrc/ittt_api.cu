@@ -414,7 +414,7 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   }
   if (P->packed) L.table = take(P->table.size() * sizeof(int));
   if (P->l2norm && P->n_udocs > 0) {
-    L.state = take(size_t(P->ndocs) * d * f * 4);
+    L.state = take(size_t(P->ndocs) * ((d + 127) / 128) * ((f + 31) / 32) * 128 * 32 * 4);
     L.partial = take(size_t(2) * P->ndocs * ((f + 511) / 512) * d * 4);
   }
   L.total = off;
@@ -422,14 +422,18 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
 }
 
 // ------------------------------------------------------------- tensor maps
-// 3-D bf16 map {inner, mid, outer} of a dense tensor, 128-byte swizzle.
+// 3-D map {inner, mid, outer} of a dense bf16 (or fp32) tensor, 128-byte
+// swizzle.
 ittt_status make_map_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid,
-                   uint64_t outer, uint32_t box_inner, uint32_t box_mid, const char* what) {
+                        uint64_t outer, uint32_t box_inner, uint32_t box_mid, const char* what,
+                        bool fp32 = false) {
+  const uint64_t es = fp32 ? 4 : 2;
   cuuint64_t dims[3] = {inner, mid, outer};
-  cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
+  cuuint64_t strides[2] = {inner * es, inner * mid * es};
   cuuint32_t box[3] = {box_inner, box_mid, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  CUresult r = g_encode(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -722,7 +726,8 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
       na.partial = reinterpret_cast<float*>(ws + L.partial);
       na.snap = snap;
       na.state_out = ua.state_out;
-      ITTT_STEP(ittt::launch_norm_update(env, tm_vmn, tm_zmn, na), "normalised update launch");
+      ITTT_STEP(ittt::launch_norm_update(env, tm_vmn, tm_zmn, tm_ss, na),
+                "normalised update launch");
     } else {
       ITTT_STEP(ittt::launch_update(env, tm_vmn, tm_zmn, tm_ss, ua), "update launch");
     }

@@ -302,6 +302,13 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
 //   epilogue store S_{i+1} in place of S_i (a unit reads its block before it
 //            writes it, and no other unit touches that block) and its row
 //            sums of squares per 512-column unit into partial[(i+1) & 1].
+// S is kept tiled: 16 KB tiles of 128 rows x 32 fp32 columns, each laid out
+// exactly as a 128-byte-swizzled staging tile (row r at r * 128 bytes, its
+// 16-byte chunk c at position c ^ (r & 7)).  The epilogue writes a tile
+// with one contiguous bulk copy from shared memory and the preload of a
+// warp reads 4 KB of consecutive rows, so the state's round trip through
+// HBM runs in long contiguous bursts instead of 256-byte pieces of
+// 38 KB-strided rows.
 // A final kernel normalises the last state into the last snapshot or into
 // state_out.
 // ----------------------------------------------------------------------------
@@ -327,24 +334,33 @@ __device__ __forceinline__ float row_scale_of(float ss) { return 1.0f / fmaxf(sq
 struct NormUpdateParams {
   CUtensorMap tm_v;      // eta*Vhat [M, d]  box {64, 64}
   CUtensorMap tm_z;      // Z        [M, f]  box {64, 64}
+  CUtensorMap tm_ss;     // snapshots as [slots][d rows][f cols] bf16, box {64, 128, 1} (store)
   const void* w0;
   int w0_fp32;
   int64_t w0_bstride;
-  float* state;          // S, [documents, d, f] fp32
+  float* state;          // S, tiled: [documents][ceil(d/128)][ceil(f/32)] tiles of 4096 fp32
   float* partial;        // [2][documents][np][d] row sums of squares per 512-column unit
   __nv_bfloat16* snap;   // [slots, d, f]
   DocMap docs;
   const int* upd_docs;   // updating documents, most updates first; nullptr: all
   int n_active;          // documents with an update at chunk i
   int i;                 // the chunk this launch updates with
-  int d, f, mt, np;
+  int d, f, mt, np, ncb;  // ncb: 32-column tiles per row block
 };
+
+// First fp32 of S's tile (document, 128-row block, 32-column block).
+__device__ __forceinline__ float* state_tile(float* state, int ncb, int mt_all, int doc, int mt,
+                                             int cb) {
+  return state + ((size_t(doc) * mt_all + mt) * ncb + cb) * size_t(kBM * 32);
+}
 
 struct NormUpdateSched : SchedDefaults {
   using Params = NormUpdateParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true, true);
   static constexpr bool kPreload = true;
   static constexpr bool kRaggedK = true;
+  static constexpr bool kStagedStores = true;
+  static constexpr bool kStagedPreload = true;
 
   const Params& p;
   int doc = 0, tok = 0, clen = 0, slot = 0, m0 = 0, nbase = 0, npi = 0, halves = 1;
@@ -385,14 +401,16 @@ struct NormUpdateSched : SchedDefaults {
     return ((size_t(par) * p.docs.ndocs + doc) * p.np + blk) * size_t(p.d) + m;
   }
 
-  // W_i of this half into its accumulator, and out as snapshot slot i.
-  __device__ void preload(int h, int row, uint32_t trow) const {
+  // W_i of this half into its accumulator, and out as snapshot slot i
+  // (bf16 64-column tiles through the staging buffers, TMA stores clipped at
+  // d and f).
+  __device__ void preload(int h, int row, uint32_t trow, EpiStager& st) const {
     const int m = m0 + row;
     const bool row_ok = m < p.d;
     const int n0 = nbase + h * kBN;
-    const size_t rowoff = size_t(row_ok ? m : 0) * size_t(p.f);
     if (p.i == 0) {
-      const size_t off = size_t(doc) * size_t(p.w0_bstride) + rowoff;
+      const size_t off =
+          size_t(doc) * size_t(p.w0_bstride) + size_t(row_ok ? m : 0) * size_t(p.f);
 #pragma unroll 1
       for (int c = 0; c < kBN; c += 32) {
         uint32_t v[32];
@@ -411,35 +429,37 @@ struct NormUpdateSched : SchedDefaults {
     const float scale =
         row_ok ? row_scale_of(sum_partials(p.partial + partial_at(p.i & 1, 0, m), p.d, p.np))
                : 0.f;
-    const float* srow = p.state + size_t(doc) * size_t(p.d) * size_t(p.f) + rowoff;
-    __nv_bfloat16* wrow = p.snap + size_t(slot) * size_t(p.d) * size_t(p.f) + rowoff;
-    // 64 columns per step: sixteen independent 16-byte loads in flight.
+    // 64 columns (two tiles) per step: sixteen independent 16-byte loads of
+    // this row's two 128-byte tile rows.
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 64) {
       float w[64];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int col = n0 + c + 8 * q;
-        if (row_ok && col < p.f) {
-          const float4* src = reinterpret_cast<const float4*>(srow + col);
-          const float4 lo = __ldcg(src), hi = __ldcg(src + 1);
-          w[8 * q] = lo.x; w[8 * q + 1] = lo.y; w[8 * q + 2] = lo.z; w[8 * q + 3] = lo.w;
-          w[8 * q + 4] = hi.x; w[8 * q + 5] = hi.y; w[8 * q + 6] = hi.z; w[8 * q + 7] = hi.w;
-        } else {
+      for (int t = 0; t < 2; ++t) {
+        const int col0 = n0 + c + 32 * t;
+        const bool tile_ok = col0 < p.f;
+        const float* trowp =
+            state_tile(p.state, p.ncb, p.mt, doc, m0 / kBM, tile_ok ? col0 / 32 : 0) + row * 32;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) w[8 * q + j] = 0.f;
+        for (int q = 0; q < 8; ++q) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (tile_ok) v = __ldcg(reinterpret_cast<const float4*>(trowp) + (q ^ (row & 7)));
+          w[32 * t + 4 * q] = v.x;
+          w[32 * t + 4 * q + 1] = v.y;
+          w[32 * t + 4 * q + 2] = v.z;
+          w[32 * t + 4 * q + 3] = v.w;
         }
       }
 #pragma unroll
       for (int j = 0; j < 64; ++j) w[j] *= scale;
+      uint8_t* buf = st.acquire();
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int col = n0 + c + 8 * q;
-        if (row_ok && col < p.f)
-          *reinterpret_cast<uint4*>(wrow + col) = make_uint4(
-              pack_bf16x2(w[8 * q], w[8 * q + 1]), pack_bf16x2(w[8 * q + 2], w[8 * q + 3]),
-              pack_bf16x2(w[8 * q + 4], w[8 * q + 5]), pack_bf16x2(w[8 * q + 6], w[8 * q + 7]));
-      }
+      for (int q = 0; q < 8; ++q)
+        st.put(buf, q,
+               make_uint4(pack_bf16x2(w[8 * q], w[8 * q + 1]), pack_bf16x2(w[8 * q + 2], w[8 * q + 3]),
+                          pack_bf16x2(w[8 * q + 4], w[8 * q + 5]),
+                          pack_bf16x2(w[8 * q + 6], w[8 * q + 7])));
+      st.commit(buf, [&](uint8_t* src) { tma_store_3d(&p.tm_ss, src, n0 + c, m0, slot); });
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         uint32_t v[32];
@@ -450,12 +470,12 @@ struct NormUpdateSched : SchedDefaults {
     }
   }
 
-  // S_{i+1} of this half back to HBM, and its row sum of squares.
-  __device__ void epilogue(int s, int row, uint32_t trow) const {
+  // S_{i+1} of this half back to HBM (its 32-column tiles through the
+  // staging buffers, one bulk copy each), and its row sum of squares.
+  __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& st) const {
     const int m = m0 + row;
     const bool row_ok = m < p.d;
     const int n0 = nbase + s * kBN;
-    float* srow = p.state + (size_t(doc) * size_t(p.d) + size_t(row_ok ? m : 0)) * size_t(p.f);
     float ss = s == 0 ? 0.f : ss_carry;
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 32) {
@@ -463,19 +483,23 @@ struct NormUpdateSched : SchedDefaults {
       tmem_ld_32cols(trow + uint32_t(c), v);
       tmem_wait_ld();
       pin_regs(v);
-      if (!row_ok) continue;
+      if (n0 + c < p.f) {  // the same for every epilogue thread
+        uint8_t* buf = st.acquire();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int col = n0 + c + 8 * q;
-        if (col < p.f) {
+        for (int q = 0; q < 8; ++q)
+          st.put(buf, q, make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        st.commit(buf, [&](uint8_t* src) {
+          bulk_store(state_tile(p.state, p.ncb, p.mt, doc, m0 / kBM, (n0 + c) / 32), src,
+                     kStagingTileBytes);
+        });
+      }
+      if (row_ok) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float x = __uint_as_float(v[8 * q + j]);
+        for (int j = 0; j < 32; ++j) {
+          if (n0 + c + j < p.f) {
+            const float x = __uint_as_float(v[j]);
             ss = fmaf(x, x, ss);
           }
-          uint4* dst = reinterpret_cast<uint4*>(srow + col);
-          __stcg(dst, make_uint4(v[8 * q], v[8 * q + 1], v[8 * q + 2], v[8 * q + 3]));
-          __stcg(dst + 1, make_uint4(v[8 * q + 4], v[8 * q + 5], v[8 * q + 6], v[8 * q + 7]));
         }
       }
     }
@@ -508,9 +532,15 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   const float scale = row_scale;
   const size_t row = (size_t(doc) * d + m) * size_t(f);
+  const int mt_all = (d + kBM - 1) / kBM;
+  const int ncb = (f + 31) / 32;
+  const int r = m % kBM;
   for (int c = threadIdx.x * 8; c < f; c += blockDim.x * 8) {
-    const float4 lo = *reinterpret_cast<const float4*>(state + row + c);
-    const float4 hi = *reinterpret_cast<const float4*>(state + row + c + 4);
+    // chunks c/4 and c/4 + 1 of row r in the tile of column block c / 32
+    const float* tile = state_tile(const_cast<float*>(state), ncb, mt_all, doc, m / kBM, c / 32);
+    const int q = (c % 32) / 4;
+    const float4 lo = reinterpret_cast<const float4*>(tile + r * 32)[q ^ (r & 7)];
+    const float4 hi = reinterpret_cast<const float4*>(tile + r * 32)[(q + 1) ^ (r & 7)];
     const float w[8] = {lo.x * scale, lo.y * scale, lo.z * scale, lo.w * scale,
                         hi.x * scale, hi.y * scale, hi.z * scale, hi.w * scale};
     if (final_update) {
@@ -620,11 +650,13 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
 }
 
 cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
-                               const CUtensorMap& tm_z, const NormUpdateArgs& a) {
+                               const CUtensorMap& tm_z, const CUtensorMap& tm_snap_store,
+                               const NormUpdateArgs& a) {
   if (a.n_udocs <= 0) return cudaSuccess;
   NormUpdateParams p;
   p.tm_v = tm_vhat;
   p.tm_z = tm_z;
+  p.tm_ss = tm_snap_store;
   p.w0 = a.w0;
   p.w0_fp32 = a.w0_fp32 ? 1 : 0;
   p.w0_bstride = a.w0_bstride;
@@ -637,6 +669,7 @@ cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
   p.f = a.f;
   p.mt = (a.d + kBM - 1) / kBM;
   p.np = (a.f + 2 * kBN - 1) / (2 * kBN);
+  p.ncb = (a.f + 31) / 32;
   cudaError_t e = cudaFuncSetAttribute(norm_update_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(pipe_smem_bytes<NormUpdateSched>()));

@@ -169,17 +169,19 @@ struct NormUpdateArgs {
   const void* w0;
   bool w0_fp32;
   int64_t w0_bstride;
-  float* state;         // scratch [documents, d, f] fp32
+  float* state;         // scratch: documents x ceil(d/128) x ceil(f/32) tiles of 16 KB
   float* partial;       // scratch [2][documents][ceil(f/512)][d] fp32
   __nv_bfloat16* snap;  // [slots, d, f]: slots 1..n-1 of each document written
   float* state_out;     // [documents, d, f] fp32 or nullptr
 };
 
 // The fast-weight walk with L2 normalisation of every updated state, rows
-// over d_ff (one launch per chunk, then one finalising launch).  Tensor maps
-// as for launch_update.
+// over d_ff (one launch per chunk, then one finalising launch).  Tensor maps:
+// eta*Vhat and Z as for launch_update; the snapshots as [slots][d][f] with
+// box {64,128,1} for TMA stores.
 cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
-                               const CUtensorMap& tm_z, const NormUpdateArgs& a);
+                               const CUtensorMap& tm_z, const CUtensorMap& tm_snap_store,
+                               const NormUpdateArgs& a);
 
 // O_[i] = Z_[i] snap[slot of chunk i]^T for every chunk of every document.
 // Tensor maps: Z [M, f] box {64,128}; snapshots [slots*d, f] box {64,256};

@@ -114,6 +114,10 @@ struct SchedDefaults {
   // Epilogue writes bf16 tiles through EpiStager (TMA stores); then
   //   void epilogue(int s, int row, uint32_t tmem_row_base, EpiStager& st)
   static constexpr bool kStagedStores = false;
+  // With kStagedPreload (needs kStagedStores) the preload may store through
+  // the staging tiles too:
+  //   void preload(int acc, int row, uint32_t tmem_row_base, EpiStager& st)
+  static constexpr bool kStagedPreload = false;
   // With kMixedOperands the MMA asks the schedule for each K block's
   // instruction and shared-memory descriptors (operand major-ness may change
   // inside one accumulation):
@@ -344,7 +348,11 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
       if constexpr (S::kPreload) {
         for (int h = 0; h < sched.unit_accs(); ++h) {
           if (!preloaded[h]) {
-            sched.preload(h, row, tlane + uint32_t(h * kBN));
+            if constexpr (S::kStagedPreload) {
+              sched.preload(h, row, tlane + uint32_t(h * kBN), stager);
+            } else {
+              sched.preload(h, row, tlane + uint32_t(h * kBN));
+            }
             tmem_wait_st();
             tc_fence_before_sync();
             mbar_arrive(&sync->acc_empty[h]);
@@ -385,7 +393,11 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
           if (!release && un < nunits) {
             next.begin_unit(un, local + 1);
             if (h < next.unit_accs()) {
-              next.preload(h, row, trow);
+              if constexpr (S::kStagedPreload) {
+                next.preload(h, row, trow, stager);
+              } else {
+                next.preload(h, row, trow);
+              }
               tmem_wait_st();
               tc_fence_before_sync();
               mbar_arrive(&sync->acc_empty[h]);

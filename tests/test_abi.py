@@ -186,8 +186,9 @@ def test_workspace_bytes_and_launch_count(lib):
     assert ittt.workspace_bytes_ex(1, T, d, f, C, cu_seqlens=cu) == want_packed
     # the normalised walk keeps an fp32 state and row partial sums
     nblk = -(-f // 512)
+    tiles = -(-d // 128) * -(-f // 32)      # the fp32 state in 128 x 32 tiles
     assert (ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True)
-            == want + r(B * d * f * 4) + r(2 * B * nblk * d * 4))
+            == want + r(B * tiles * 128 * 32 * 4) + r(2 * B * nblk * d * 4))
     assert ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True, dual=True) == 0
     assert ittt.launch_count(B, T, d, f, C) == 5
     assert ittt.launch_count(B, T, d, f, T) == 4
