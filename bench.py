@@ -180,6 +180,23 @@ def init_dist(args):
     return world, rank, local
 
 
+def arm_config(cfg, args, world, cu=None):
+    """The `config` object of a bench line (both arms report the same one)."""
+    T = cfg["T"] if cu is None else cu[-1]
+    return {"workload": cfg["name"], "B": cfg["B"] if cu is None else 1, "T": T,
+            "d": cfg["d"], "f": cfg["f"], "C": cfg["C"], "eta": cfg["eta"],
+            "chunks": -(-T // cfg["C"]) if cu is None else None,
+            "parallelism": f"batch x{world} (replicas)",
+            "packed_docs": None if cu is None else {
+                "count": len(cu) - 1, "lengths": [b - a for a, b in zip(cu, cu[1:])],
+                "mix": "log-uniform in [512, 16384] tokens, seeded"},
+            "conv": "fused into target GEMM" if args.fused_conv else "own kernel",
+            "schedule": "dual (scores Z Z^T)" if args.dual else "primal walk",
+            "eta_tok": "per-token rates" if args.eta_tok else None,
+            "update_rule": "L2-normalised rows" if args.l2norm else "additive",
+            "l2": "inputs larger than L2: H+X0 and Z are several GB per step"}
+
+
 def run_reference(args):
     world, rank, _ = init_dist(args)
     if rank != 0:
@@ -190,7 +207,8 @@ def run_reference(args):
     S = max(128, min(256, cfg["T"]))
     Cs = S // 2
     inp = make_inputs(1, S, cfg["d"], cfg["f"], seed=1234 + args.config)
-    for _ in range(args.warmup):
+    warmup = max(3, args.warmup)
+    for _ in range(warmup):
         oracle.forward(inp, cfg["eta"], Cs)
     t0 = time.perf_counter()
     for _ in range(args.steps):
@@ -202,11 +220,10 @@ def run_reference(args):
               f"d={cfg['d']}, d_ff={cfg['f']} per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": warmup,
         "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg["name"], "B": cfg["B"], "T": cfg["T"], "d": cfg["d"],
-                   "f": cfg["f"], "C": cfg["C"], "eta": cfg["eta"]},
+        "config": arm_config(cfg, args, world),
         "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -426,17 +443,7 @@ def main():
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": cfg["name"], "B": B, "T": T, "d": d, "f": f, "C": C,
-                       "eta": eta, "chunks": -(-T // C) if cu is None else None,
-                       "parallelism": f"batch x{world} (replicas)",
-                       "packed_docs": None if cu is None else {
-                           "count": len(cu) - 1, "lengths": [b - a for a, b in zip(cu, cu[1:])],
-                           "mix": "log-uniform in [512, 16384] tokens, seeded"},
-                       "conv": "fused into target GEMM" if args.fused_conv else "own kernel",
-                       "schedule": "dual (scores Z Z^T)" if args.dual else "primal walk",
-                       "eta_tok": "per-token rates" if args.eta_tok else None,
-                       "update_rule": "L2-normalised rows" if args.l2norm else "additive",
-                       "l2": "inputs larger than L2: H+X0 and Z are several GB per step"},
+            "config": arm_config(cfg, args, world, cu),
             "layer_tflops": round(layer_tflops, 1),
             "layer_frac_of_peak": {
                 "bf16_tflops": round(layer_tflops / float(peaks["bf16_tflops"]), 4),
