@@ -257,6 +257,47 @@ def test_ragged_chunks(cuda_device, B, T, d, f, C, eta):
     assert_parity(host(o32), ref["O"], "O (fp32 out)")
 
 
+EDGE = [
+    # B, T, d, f, C, eta
+    (1, 100, 8, 8, 7, 0.1),        # smallest widths: every TMA box exceeds its tensor
+    (2, 33, 16, 24, 64, 0.2),      # chunk longer than the sequence: one partial chunk
+    (3, 1, 64, 128, 1, 0.3),       # one token per sequence
+    (1, 130, 24, 40, 2, 0.05),     # two-token chunks, widths below one 64-column box
+]
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", EDGE)
+def test_edge_shapes(cuda_device, B, T, d, f, C, eta):
+    inp = make_inputs(B, T, d, f, seed=1300 + T + d)
+    ref = oracle.forward(inp, eta, C, want_states=True)
+    got = run(to_device(inp, cuda_device), eta, C, want_state=True, intermediates=True)
+    n = -(-T // C)
+    assert_parity(host(got["snap_buf"]), ref["states"][:, :n], "snapshots")
+    assert_parity(host(got["state_out"]), ref["states"][:, n], "final state")
+    assert_parity(host(got["O"]), ref["O"], "O")
+    # the default call (no snapshot buffer: W_0 read directly for chunk 0)
+    plain = run(to_device(inp, cuda_device), eta, C)["O"]
+    assert_parity(host(plain), ref["O"], "O (default call)")
+
+
+def test_long_chunk_single_sequence(cuda_device):
+    """A 2^17-token chunk: one chunk, O = Z W_0^T; the final state from one
+    long contraction (sampled entries against the oracle)."""
+    T, d, f, eta = 1 << 17, 64, 128, 1e-4
+    inp = make_inputs(1, T, d, f, seed=1400)
+    g = to_device(inp, cuda_device)
+    got = run(g, eta, T, want_state=True, intermediates=True)
+    rows = np.array([0, 1, T // 2, T - 1])
+    assert_parity(host(got["O"][0][torch.as_tensor(rows)]),
+                  oracle.first_chunk_rows(inp["H"][0], inp["W_gate"], inp["W_up"],
+                                          inp["W_down0"], rows), "O rows")
+    m, j = np.array([0, 5, d - 1]), np.array([0, 77, f - 1])
+    ws = oracle.state_entries(inp["H"][0], inp["X0"][0], inp["W_gate"], inp["W_up"],
+                              inp["W_down0"], inp["W_target"], inp["conv_w"], eta, T, m, j)
+    assert_parity(host(got["state_out"][0][torch.as_tensor(m), torch.as_tensor(j)]), ws[:, 1],
+                  "final state entries")
+
+
 # --------------------------------------------------------------------------
 # Packed documents (state reset at each document boundary)
 # --------------------------------------------------------------------------
