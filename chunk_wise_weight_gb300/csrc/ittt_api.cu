@@ -1,15 +1,23 @@
 // ittt_api.cu -- the C-ABI of libittt.so (declared in include/ittt.h).
 //
-// Validates every descriptor before anything is enqueued, takes the scratch
-// it needs (stream-ordered, from a library-private memory pool, or from a
-// caller workspace), encodes the TMA tensor maps and launches the kernels in
+// Validates every descriptor before anything is enqueued, plans the call
+// (documents, snapshot slots, scratch), takes the scratch it needs
+// (stream-ordered, from a library-private memory pool, or from a caller
+// workspace), encodes the TMA tensor maps and launches the kernels in
 // data-flow order on the caller's stream:
-//   conv3 (Xc) ; target GEMM (eta*Vhat) ; gate/up GEMM (Z) ; snapshot 0 ;
-//   update walk (snapshots W_1..W_{n-1}) ; apply GEMM (O).
-// With ITTT_FLAG_FUSED_CONV the target GEMM computes the conv itself.  (Run
-// beside the gate/up GEMM on a second stream, the conv slowed that GEMM by
-// more than its own 0.2 ms at the 32k-token workload, so it runs in line.)
-// No host synchronisation happens inside a forward call.
+//   [packed documents: table staging] ; conv3 (Xc) ; target GEMM (eta*Vhat) ;
+//   gate/up GEMM (Z) ; [snapshot 0, when W_0 is not one shared bf16 matrix or
+//   the caller wants the snapshots] ; update walk (snapshots W_1..W_{n-1}) ;
+//   apply GEMM (O).
+// The GEMMs run on CTA pairs where two can be resident (and the update walk
+// when every updated chunk is a multiple of 64 tokens), else on single CTAs.
+// With ITTT_FLAG_FUSED_CONV the target GEMM computes the conv itself; with
+// ITTT_FLAG_DUAL scores Z Z^T and the dual apply replace walk and apply; with
+// ITTT_FLAG_L2_NORM the walk runs one launch per chunk.  (Run beside the
+// gate/up GEMM on a second stream, the conv slowed that GEMM by more than its
+// own 0.2 ms at the 32k-token workload, so it runs in line.)  No host
+// synchronisation happens inside a forward call; the packed-document staging
+// waits only for a staging buffer's previous copy.
 #include <cuda.h>
 #include <cuda_runtime.h>
 

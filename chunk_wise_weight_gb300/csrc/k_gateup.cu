@@ -2,17 +2,15 @@
 //   Z = SiLU(H W_gate^T) (.) (H W_up^T)
 // ("[논문리뷰] In-Place Test-Time Training", Method §1 eq. (2), phi = SiLU).
 //
-// Each 128 x 256 MMA tile computes 128 gate columns and the matching 128 up
-// columns for the same f-range: the producer stacks the W_gate rows and the
-// W_up rows of that range into one 256-row B tile, so the accumulator holds
-// gate pre-activations in TMEM columns 0..127 and up pre-activations in
-// 128..255.  The epilogue pairs column j with column j + 128 and writes
-// 128 bf16 Z columns.
+// Each MMA tile computes 128 gate columns and the matching 128 up columns
+// for the same f-range, so the accumulator holds gate pre-activations in
+// TMEM columns 0..127 and up pre-activations in 128..255; the epilogue pairs
+// column j with column j + 128 and writes 128 bf16 Z columns.
 //
 // On CTA pairs (the default) a unit is 256 rows: each CTA keeps its 128 H
-// rows, the leader loads the W_gate rows of the f-range and its peer the
-// W_up rows, so the pair MMA leaves [gate | up] in each CTA's TMEM exactly
-// as above.
+// rows, the leader loads the 128 W_gate rows of the f-range and its peer the
+// 128 W_up rows (the pair MMA's two B halves).  On a single CTA (fallback)
+// the producer stacks both into one 256-row B tile of a 128-row unit.
 #include "kernels.h"
 #include "pipeline.cuh"
 #include "pipeline_pair.cuh"

@@ -92,9 +92,9 @@ struct DocMap {
 #endif
 };
 
-// Z[M, f] = SiLU(H W_gate^T) * (H W_up^T).  Tensor maps: H [M, K] box
-// {64,128}; W_gate, W_up [f, K] box {64,128}; Z [M, f] box {64,128} for the
-// TMA stores.  All bf16, K = d_model.
+// Z[M, f] = SiLU(H W_gate^T) * (H W_up^T) on single CTAs (fallback).  Tensor
+// maps: H [M, K] box {64,128}; W_gate, W_up [f, K] box {64,128}; Z [M, f] box
+// {64,128} for the TMA stores.  All bf16, K = d_model.
 cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h,
                           const CUtensorMap& tm_wg, const CUtensorMap& tm_wu,
                           const CUtensorMap& tm_zs, int M, int f, int K);
@@ -183,7 +183,8 @@ cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
                                const CUtensorMap& tm_z, const CUtensorMap& tm_snap_store,
                                const NormUpdateArgs& a);
 
-// O_[i] = Z_[i] snap[slot of chunk i]^T for every chunk of every document.
+// O_[i] = Z_[i] snap[slot of chunk i]^T for every chunk of every document,
+// one CTA per 128-row tile (fallback when no CTA pair can be resident).
 // Tensor maps: Z [M, f] box {64,128}; snapshots [slots*d, f] box {64,256};
 // bf16 O [M, d] with box {64,64} for the TMA stores (unused for fp32 O).
 // Chunks of any length; a document's last chunk may be shorter than C.
