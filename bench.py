@@ -45,13 +45,39 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C++ source with comments and runs of white space removed (string
+    literals kept)."""
+    import re
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of the code (not the comments) a kernel is built from: recorded
+    DRAM traffic is reported only while it matches."""
     import hashlib
     csrc = os.path.join(ROOT, "chunk_wise_weight_gb300", "csrc")
     m = hashlib.sha1()
     for f in KERNEL_SOURCES[kernel] + ["pipeline.cuh", "pipeline_pair.cuh", "sm103.cuh"]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            m.update(fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            m.update(_code_only(fh.read()).encode())
     return m.hexdigest()[:16]
 
 
