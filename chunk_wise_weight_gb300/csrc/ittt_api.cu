@@ -279,7 +279,8 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   if (s != ITTT_OK) return s;
   if (o.pad_mode != ITTT_PAD_CHUNK && o.pad_mode != ITTT_PAD_SEQUENCE)
     return fail(ITTT_ERR_INVALID_ARG, "pad_mode %d", int(o.pad_mode));
-  if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV | ITTT_FLAG_DUAL | ITTT_FLAG_L2_NORM))
+  if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV | ITTT_FLAG_DUAL | ITTT_FLAG_L2_NORM |
+                          ITTT_FLAG_SINGLE_CTA))
     return fail(ITTT_ERR_INVALID_ARG, "unknown flags 0x%x", unsigned(o.flags));
   P->B = B;
   P->T = T;
@@ -494,6 +495,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   ittt_status s = make_plan(B, T, d, f, chunk, o, w0_bf16, &P);
   if (s != ITTT_OK) return s;
   const bool fused = P.fused, dual = P.dual;
+  const bool single = (o.flags & ITTT_FLAG_SINGLE_CTA) != 0;
   const int64_t S = P.ndocs;  // per-document state count
 
   const int64_t sh_btd[3] = {B, T, d}, sh_fd[2] = {f, d}, sh_df[2] = {d, f}, sh_dd[2] = {d, d},
@@ -665,9 +667,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if (what == nullptr) {
     const float* et = o.eta_tok ? static_cast<const float*>(o.eta_tok->data) : nullptr;
     // CTA pairs where two can be resident (split convolution), else one CTA.
-    e = fused ? cudaErrorNotSupported
-              : ittt::launch_target_pair(env, tm_a, tm_wt128, tm_vs, et, vhat, eta, int(M),
-                                         int(d));
+    e = fused || single ? cudaErrorNotSupported
+                        : ittt::launch_target_pair(env, tm_a, tm_wt128, tm_vs, et, vhat, eta,
+                                                   int(M), int(d));
     if (e == cudaErrorNotSupported) {
       cudaGetLastError();
       e = ittt::launch_target(env, tm_a, tm_wt, tm_vs, cw, et, vhat, eta, int(M), int(T), int(d),
@@ -678,7 +680,8 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   ITTT_STEP(rec(2 * ITTT_PHASE_TARGET + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP, stream), "event record");
   if (what == nullptr) {
-    e = ittt::launch_gateup_pair(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d));
+    e = single ? cudaErrorNotSupported
+               : ittt::launch_gateup_pair(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d));
     if (e == cudaErrorNotSupported) {
       cudaGetLastError();
       e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d));
@@ -716,7 +719,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     ua.w0_fp32 = w0_fp32;
     ua.w0_bstride = w0_bstride;
     ua.state_out = o.state_out ? static_cast<float*>(o.state_out->data) : nullptr;
-    ua.allow_pairs = !P.ragged_walk;
+    ua.allow_pairs = !P.ragged_walk && !single;
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");
     if (P.l2norm) {
       ittt::NormUpdateArgs na;
@@ -743,9 +746,10 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
     if (what == nullptr) {
       // CTA pairs where two can be resident, else one CTA per tile.
-      e = ittt::launch_apply_pair(env, tm_zk, tm_snap_pair, w0_direct ? &tm_w0d_pair : nullptr,
-                                  tm_os, out->data, out->dtype == ITTT_FP32, docs, int(d),
-                                  int(f));
+      e = single ? cudaErrorNotSupported
+                 : ittt::launch_apply_pair(env, tm_zk, tm_snap_pair,
+                                           w0_direct ? &tm_w0d_pair : nullptr, tm_os, out->data,
+                                           out->dtype == ITTT_FP32, docs, int(d), int(f));
       if (e == cudaErrorNotSupported) {
         cudaGetLastError();
         e = ittt::launch_apply(env, tm_zk, tm_snap, w0_direct ? &tm_w0d : nullptr, tm_os,

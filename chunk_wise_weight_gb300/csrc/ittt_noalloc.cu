@@ -175,6 +175,27 @@ ittt_status na_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
   return ITTT_OK;
 }
 
+// The target and gate/up GEMMs on CTA pairs where two can be resident.
+cudaError_t target_pair_or_single(const ittt::LaunchEnv& env, const CUtensorMap& tm_xc,
+                                  const CUtensorMap& tm_wt, const CUtensorMap& tm_wt128,
+                                  const CUtensorMap& tm_vs, const float* conv_w,
+                                  __nv_bfloat16* vhat, float eta, int M, int T, int d, int C) {
+  cudaError_t e = ittt::launch_target_pair(env, tm_xc, tm_wt128, tm_vs, nullptr, vhat, eta, M, d);
+  if (e != cudaErrorNotSupported) return e;
+  cudaGetLastError();
+  return ittt::launch_target(env, tm_xc, tm_wt, tm_vs, conv_w, nullptr, vhat, eta, M, T, d, C,
+                             ITTT_PAD_CHUNK, false);
+}
+
+cudaError_t gateup_pair_or_single(const ittt::LaunchEnv& env, const CUtensorMap& tm_h,
+                                  const CUtensorMap& tm_wg, const CUtensorMap& tm_wu,
+                                  const CUtensorMap& tm_zk, int M, int f, int d) {
+  cudaError_t e = ittt::launch_gateup_pair(env, tm_h, tm_wg, tm_wu, tm_zk, M, f, d);
+  if (e != cudaErrorNotSupported) return e;
+  cudaGetLastError();
+  return ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, M, f, d);
+}
+
 }  // namespace
 
 extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_tensor* X0,
@@ -233,16 +254,28 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   auto* snap = reinterpret_cast<__nv_bfloat16*>(nd->scratch + z_bytes + 2 * act_bytes);
 
   const uint64_t M = uint64_t(B * T);
-  CUtensorMap tm_h, tm_wg, tm_wu, tm_xc, tm_wt, tm_vmn, tm_zmn, tm_zk, tm_snap;
+  CUtensorMap tm_h, tm_wg, tm_wu, tm_xc, tm_wt, tm_wt128, tm_vmn, tm_zmn, tm_zk, tm_snap,
+      tm_snap_pair, tm_w0d, tm_w0d_pair;
+  // As in ittt_forward: a bf16 W_0 is read by the apply itself (no slot-0
+  // copy), the GEMMs run on CTA pairs where two can be resident.
+  const bool w0_direct = W_down0->dtype == ITTT_BF16;
   if ((s = na_map(&tm_h, H->data, d, M, 64, 128, "H"))) return s;
   if ((s = na_map(&tm_wg, W_gate->data, d, f, 64, 128, "W_gate"))) return s;
   if ((s = na_map(&tm_wu, W_up->data, d, f, 64, 128, "W_up"))) return s;
   if ((s = na_map(&tm_xc, xc, d, M, 64, 128, "Xc"))) return s;
   if ((s = na_map(&tm_wt, W_target->data, d, d, 64, 256, "W_target"))) return s;
+  if ((s = na_map(&tm_wt128, W_target->data, d, d, 64, 128, "W_target (pair)"))) return s;
   if ((s = na_map(&tm_vmn, vhat, d, M, 64, 64, "Vhat"))) return s;
   if ((s = na_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
   if ((s = na_map(&tm_zk, z, f, M, 64, 128, "Z (apply)"))) return s;
   if ((s = na_map(&tm_snap, snap, f, uint64_t(B * n * d), 64, 256, "snapshots"))) return s;
+  if ((s = na_map(&tm_snap_pair, snap, f, uint64_t(B * n * d), 64, 128, "snapshots (pair)")))
+    return s;
+  if (w0_direct) {
+    if ((s = na_map(&tm_w0d, W_down0->data, f, uint64_t(d), 64, 256, "W_0"))) return s;
+    if ((s = na_map(&tm_w0d_pair, W_down0->data, f, uint64_t(d), 64, 128, "W_0 (pair)")))
+      return s;
+  }
   CUtensorMap tm_vs, tm_ss, tm_os;
   memset(&tm_os, 0, sizeof(tm_os));
   if ((s = na_map(&tm_vs, vhat, d, M, 64, 128, "Vhat (store)"))) return s;
@@ -272,16 +305,15 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
                              static_cast<const float*>(conv_w->data), xc, int64_t(M), docs,
                              int(d), ITTT_PAD_CHUNK)) != cudaSuccess) {
     what = "conv";
-  } else if ((e = ittt::launch_target(env, tm_xc, tm_wt, tm_vs,
-                                      static_cast<const float*>(conv_w->data), nullptr, vhat, eta,
-                                      int(M), int(T), int(d), int(chunk), ITTT_PAD_CHUNK,
-                                      false)) != cudaSuccess) {
+  } else if ((e = target_pair_or_single(env, tm_xc, tm_wt, tm_wt128, tm_vs,
+                                         static_cast<const float*>(conv_w->data), vhat, eta,
+                                         int(M), int(T), int(d), int(chunk))) != cudaSuccess) {
     what = "target";
-  } else if ((e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d))) !=
-             cudaSuccess) {
+  } else if ((e = gateup_pair_or_single(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f),
+                                        int(d))) != cudaSuccess) {
     what = "gate/up";
-  } else if ((e = ittt::launch_snapshot0(env, W_down0->data, w0_fp32, 0, snap, docs, int(d),
-                                         int(f))) != cudaSuccess) {
+  } else if (!w0_direct && (e = ittt::launch_snapshot0(env, W_down0->data, w0_fp32, 0, snap, docs,
+                                                       int(d), int(f))) != cudaSuccess) {
     what = "snapshot";
   } else {
     ittt::UpdateArgs ua;
@@ -295,13 +327,18 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
     ua.w0_fp32 = w0_fp32;
     ua.w0_bstride = 0;
     ua.state_out = nullptr;
-    ua.allow_pairs = false;
+    ua.allow_pairs = chunk % 64 == 0;  // every updated chunk is a whole chunk
     if ((e = ittt::launch_update(env, tm_vmn, tm_zmn, tm_ss, ua)) != cudaSuccess) {
       what = "update";
-    } else if ((e = ittt::launch_apply(env, tm_zk, tm_snap, nullptr, tm_os, out->data,
-                                       out->dtype == ITTT_FP32, docs, int(d), int(f))) !=
-               cudaSuccess) {
-      what = "apply";
+    } else {
+      e = ittt::launch_apply_pair(env, tm_zk, tm_snap_pair, w0_direct ? &tm_w0d_pair : nullptr,
+                                  tm_os, out->data, out->dtype == ITTT_FP32, docs, int(d), int(f));
+      if (e == cudaErrorNotSupported) {
+        cudaGetLastError();
+        e = ittt::launch_apply(env, tm_zk, tm_snap, w0_direct ? &tm_w0d : nullptr, tm_os,
+                               out->data, out->dtype == ITTT_FP32, docs, int(d), int(f));
+      }
+      if (e != cudaSuccess) what = "apply";
     }
   }
   if (what != nullptr)

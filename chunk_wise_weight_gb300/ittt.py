@@ -25,6 +25,7 @@ PHASES = ("conv", "target", "gateup", "snapshot0", "update", "apply")
 FLAG_FUSED_CONV = 1
 FLAG_DUAL = 2
 FLAG_L2_NORM = 4
+FLAG_SINGLE_CTA = 8
 
 _DTYPES = {torch.bfloat16: BF16, torch.float32: FP32}
 
@@ -144,11 +145,11 @@ def _seqlens(cu_seqlens):
 
 
 def _opts(pad_mode, fused_conv, dual, cu_seqlens, keep: dict, l2norm=False,
-          **tensors) -> Opts:
+          single_cta=False, **tensors) -> Opts:
     opts = Opts()
     opts.pad_mode = int(pad_mode)
     opts.flags = ((FLAG_FUSED_CONV if fused_conv else 0) | (FLAG_DUAL if dual else 0)
-                  | (FLAG_L2_NORM if l2norm else 0))
+                  | (FLAG_L2_NORM if l2norm else 0) | (FLAG_SINGLE_CTA if single_cta else 0))
     for name, t in tensors.items():
         if t is not None:
             keep[name] = describe(t)
@@ -166,7 +167,7 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
             pad_mode: int = PAD_CHUNK, state_in=None, state_out=None, z_buf=None,
             vhat_buf=None, snap_buf=None, workspace=None, events=None,
             fused_conv: bool = False, dual: bool = False, eta_tok=None,
-            cu_seqlens=None, l2norm: bool = False) -> torch.Tensor:
+            cu_seqlens=None, l2norm: bool = False, single_cta: bool = False) -> torch.Tensor:
     """Enqueue one layer forward on `stream` (default: current stream) and
     return `out` [B,T,d].  Extra keyword buffers map to ittt_opts; `events`
     is a list of 2 * len(PHASES) torch.cuda.Event(enable_timing=True): a
@@ -177,7 +178,8 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
         out = torch.empty(H.shape, dtype=out_dtype, device=H.device)
     keep = [describe(x) for x in (H, X0, W_gate, W_up, W_down0, W_target, conv_w, out)]
     extra = {}
-    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, extra, l2norm=l2norm, state_in=state_in,
+    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, extra, l2norm=l2norm,
+                 single_cta=single_cta, state_in=state_in,
                  state_out=state_out, z_buf=z_buf, vhat_buf=vhat_buf, snap_buf=snap_buf,
                  eta_tok=eta_tok)
     if workspace is not None:

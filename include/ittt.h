@@ -180,6 +180,11 @@ typedef struct {
  * device scratch ([S,d,f] fp32 more scratch).  Snapshots and state_out hold
  * normalised states.  Not combinable with ITTT_FLAG_DUAL. */
 #define ITTT_FLAG_L2_NORM 4
+/* Run every GEMM on single CTAs (128-row tiles) instead of CTA pairs
+ * (tcgen05 cta_group::2 on 2-CTA clusters, the default wherever a pair can be
+ * resident).  Same results; for systems where 2-CTA clusters cannot be
+ * scheduled and for comparing the two. */
+#define ITTT_FLAG_SINGLE_CTA 8
 
 /* Kernel phases of one forward call, in launch order. */
 typedef enum {

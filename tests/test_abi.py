@@ -69,6 +69,10 @@ def _args(B=1, T=256, d=64, f=256, out_dtype=ittt.BF16):
 
 
 def _call(lib, a, eta=0.1, chunk=64, opts=None):
+    # The descriptors hold fake device addresses: a call that passed
+    # validation on a machine with a GPU would launch kernels on them.
+    if torch.cuda.is_available():
+        pytest.skip("argument checks with fake device pointers run on hosts without a GPU")
     r = lambda x: None if x is None else ctypes.byref(x)  # noqa: E731
     return lib.ittt_forward_ex(r(a["H"]), r(a["X0"]), r(a["Wg"]), r(a["Wu"]), r(a["W0"]),
                                r(a["Wt"]), r(a["cw"]), ctypes.c_float(eta), ctypes.c_int64(chunk),
@@ -121,7 +125,7 @@ def test_rejects_bad_options(lib):
     o.pad_mode = 7
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     o = ittt.Opts()
-    o.flags = 8
+    o.flags = 16
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     assert "flags" in ittt.last_error()
     o = ittt.Opts()

@@ -60,7 +60,7 @@ def packed_slots(cu, C):
 
 def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
         state_in=None, want_state=False, fused_conv=False, dual=False, eta_tok=None,
-        cu_seqlens=None, l2norm=False):
+        cu_seqlens=None, l2norm=False, single_cta=False):
     B, T, d = g["H"].shape
     f = g["W_gate"].shape[0]
     dev = g["H"].device
@@ -82,7 +82,7 @@ def run(g, eta, C, *, pad_mode=0, out_dtype=torch.bfloat16, intermediates=False,
                        None if state_in is not None else g["W_down0"], g["W_target"],
                        g["conv_w"], eta, C, out_dtype=out_dtype, pad_mode=pad_mode,
                        fused_conv=fused_conv, dual=dual, eta_tok=eta_tok,
-                       cu_seqlens=cu_seqlens, l2norm=l2norm, **kw)
+                       cu_seqlens=cu_seqlens, l2norm=l2norm, single_cta=single_cta, **kw)
     ittt.stream_status()
     res = {"O": out}
     res.update(kw)
@@ -225,6 +225,22 @@ def test_per_token_rates(cuda_device, fused_conv, dual):
     if not dual:
         assert_parity(host(got["snap_buf"]), ref["states"][:, :T // C], "snapshots")
     assert_parity(host(got["O"]), ref["O"], "O")
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", SHAPES[:4])
+def test_single_cta_kernels(cuda_device, B, T, d, f, C, eta):
+    """The single-CTA GEMMs (the fallback where CTA pairs cannot be resident)
+    against the oracle, and against the default CTA-pair path."""
+    inp = make_inputs(B, T, d, f, seed=1500 + T + d)
+    ref = oracle.forward(inp, eta, C, want_states=True)
+    g = to_device(inp, cuda_device)
+    one = run(g, eta, C, intermediates=True, single_cta=True)
+    assert_parity(host(one["snap_buf"]), ref["states"][:, :T // C], "snapshots (single CTA)")
+    assert_parity(host(one["O"]), ref["O"], "O (single CTA)")
+    # Same K order and fp32 accumulation: the two paths agree bit for bit.
+    pair = run(g, eta, C, intermediates=True)
+    for k in ("z_buf", "vhat_buf", "snap_buf", "O"):
+        assert torch.equal(one[k], pair[k]), k
 
 
 # --------------------------------------------------------------------------
