@@ -167,7 +167,13 @@ cudaError_t launch_gateup_pair(const LaunchEnv& env, const CUtensorMap& tm_h,
   p.m_tiles = (M + 2 * kBM - 1) / (2 * kBM);
   p.n_tiles = (f + kGateUpTileN - 1) / kGateUpTileN;
   p.kblocks = (K + kBK - 1) / kBK;
-  p.raster = p.n_tiles < 16 ? p.n_tiles : 16;
+  // Column tiles in the fewest even bands of at most 40 (each band re-reads
+  // H once; 76 tiles -> 2 x 38: a same-box sweep gave 3.67 ms at 38, 3.70 at
+  // 16 and 4.16 at 76, where the band's weights no longer stay in L2).
+  {
+    const int bands = (p.n_tiles + 39) / 40;
+    p.raster = (p.n_tiles + bands - 1) / bands;
+  }
   const int units = p.m_tiles * p.n_tiles;
   if (units == 0) return cudaSuccess;
   const size_t smem = pair_smem_bytes<GateUpPairSched>();
