@@ -37,7 +37,7 @@ DEFAULT_CONFIG = 2
 # hash of the kernel's sources at capture time: once the sources change the
 # figure no longer describes the kernel and `traffic` is reported as null.
 TRAFFIC_BYTES = {
-    (2, "gateup"): (4036667136, "92df0a1f1d53e139"),
+    (2, "gateup"): (2789991321, "d38d124caee580c8"),
 }
 KERNEL_SOURCES = {
     "gateup": ["k_gateup.cu"], "target": ["k_target.cu"], "update": ["k_update.cu"],
@@ -116,6 +116,9 @@ def parse_args():
                     help="normalise every updated fast weight row by row (one launch per chunk)")
     ap.add_argument("--eta-tok", action="store_true",
                     help="per-token learning-rate weights (seeded uniform [0.5, 1.5))")
+    ap.add_argument("--seq-shards", type=int, default=0,
+                    help="run the sequence-sharded schedule with this many spans, the spans "
+                         "run in turn on this GPU (fold, exclusive prefix, apply); one rank only")
     return ap.parse_args()
 
 
@@ -197,6 +200,108 @@ def launches_per_step(B, T, C, cu, l2norm, dual=False):
         return 5
     walk = (steps + 1 if l2norm else 1) if steps > 0 else 0
     return 4 + walk + (1 if cu else 0)
+
+
+def run_seq_shards(args, cfg, tensors, stream, dev, peaks, peak_src, rates, local, cpu):
+    """--seq-shards R: every span's work of the sequence-sharded schedule on
+    this one GPU, span after span: fold each span into its delta
+    (ITTT_FLAG_UPDATE_ONLY, from zero), take each span's exclusive prefix
+    (ittt_state_prefix), then walk and apply each span from its prefix
+    reusing Z and eta * Vhat.  ms_per_step is the time one GPU needs for all
+    spans; on R GPUs each would run one span and all-gather the deltas."""
+    import torch
+    from chunk_wise_weight_gb300 import counted_flops, ittt
+    from chunk_wise_weight_gb300.shard import sequence_span
+
+    H, X0, Wg, Wu, W0, Wt, cw = tensors
+    B, T, d = H.shape
+    f = Wg.shape[0]
+    C, eta, R = cfg["C"], cfg["eta"], args.seq_shards
+    spans = [sequence_span(T, C, R, r) for r in range(R)]
+    spans = [(a, b) for a, b in spans if b > a]
+    n_sp = len(spans)
+    bf, f32 = torch.bfloat16, torch.float32
+    Hs = [H[:, a:b].contiguous() for a, b in spans]
+    X0s = [X0[:, a:b].contiguous() for a, b in spans]
+    ets = [None if rates is None else rates[:, a:b].contiguous() for a, b in spans]
+    zs = [torch.empty(B, b - a, f, dtype=bf, device=dev) for a, b in spans]
+    vs = [torch.empty(B, b - a, d, dtype=bf, device=dev) for a, b in spans]
+    outs = [torch.empty(B, b - a, d, dtype=bf, device=dev) for a, b in spans]
+    deltas = torch.empty(n_sp, B, d, f, dtype=f32, device=dev)
+    states = [torch.empty(B, d, f, dtype=f32, device=dev) for _ in spans]
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        for k in range(n_sp):
+            ittt.forward(Hs[k], X0s[k], Wg, Wu, None, Wt, cw, eta, C, stream=stream,
+                         update_only=True, state_out=deltas[k], z_buf=zs[k], vhat_buf=vs[k],
+                         eta_tok=ets[k])
+        if ev:
+            ev[1].record(stream)
+        for k in range(n_sp):
+            ittt.state_prefix(W0, deltas, k, states[k], stream=stream)
+        if ev:
+            ev[2].record(stream)
+        for k in range(n_sp):
+            ittt.forward(Hs[k], X0s[k], Wg, Wu, None, Wt, cw, eta, C, outs[k], stream=stream,
+                         state_in=states[k], reuse_zv=True, z_buf=zs[k], vhat_buf=vs[k])
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    ittt.stream_status(stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    for k in range(args.steps):
+        step(ev[k])
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    ittt.stream_status(stream)
+    ms_per_step = sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps
+    part = [sum(e[p].elapsed_time(e[p + 1]) for e in ev) / args.steps for p in range(3)]
+    # Algorithmic work: the fold is gate/up, target and one 2*d*f-FLOP
+    # contraction per token; the prefix of span k reads k deltas and W_0 and
+    # writes one state; the apply phase is the walk and the apply.
+    fold_flops = B * T * (4 * d * f + 2 * d * d + 2 * d * f)
+    prefix_bytes = sum(k * B * d * f * 4 + d * f * 2 + B * d * f * 4 for k in range(n_sp))
+    F = counted_flops(B, T, d, f, C)
+    phases = {
+        "fold": {"ms": round(part[0], 4), "share": round(part[0] / ms_per_step, 4),
+                 "tflops": round(fold_flops / (part[0] * 1e-3) / 1e12, 1)},
+        "prefix": {"ms": round(part[1], 4), "share": round(part[1] / ms_per_step, 4),
+                   "gbs": round(prefix_bytes / (part[1] * 1e-3) / 1e9, 1)},
+        "apply": {"ms": round(part[2], 4), "share": round(part[2] / ms_per_step, 4)},
+    }
+    peak = float(peaks["bf16_tflops"])
+    achieved = fold_flops / (part[0] * 1e-3) / 1e12
+    launches = 0
+    for a, b in spans:
+        n_k = -(-(b - a) // C)
+        launches += 4 + 1 + 2 + (1 if n_k > 1 else 0)
+    conf = arm_config(cfg, args, 1)
+    conf["parallelism"] = f"sequence x{R} (spans run in turn on one GPU)"
+    conf["spans"] = [b - a for a, b in spans]
+    line = {
+        "metric": METRIC, "value": B * T / (ms_per_step * 1e-3), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": conf,
+        "layer_tflops": round(F / (ms_per_step * 1e-3) / 1e12, 1),
+        "counted_tflop_per_step": round(F / 1e12, 4),
+        "roofline": {"bound": "tensor", "kernel": "fold (conv, target, gate/up, update)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_kind": f"bf16_tflops burst ({peak_src})"},
+        "phases": phases, "cpu_baseline": cpu, "clocks": clocks, "e2e": None,
+        "gpu_launches": launches * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
 
 
 def init_dist(args):
@@ -337,6 +442,14 @@ def main():
         g_rates = torch.Generator().manual_seed(4321 + first)
         rates = (torch.rand(B, T, generator=g_rates) + 0.5).to(dev)
 
+    if args.seq_shards:
+        if world > 1:
+            raise SystemExit("--seq-shards runs its spans in turn on one GPU: one rank only")
+        if args.packed or args.l2norm or args.dual:
+            raise SystemExit("--seq-shards needs regular sequences and the additive update")
+        return run_seq_shards(args, cfg, (H, X0, Wg, Wu, W0, Wt, cw), stream, dev, peaks,
+                              peak_src, rates, local, cpu)
+
     def step(events=None):
         ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, stream=stream, events=events,
                      fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates, cu_seqlens=cu,
@@ -356,21 +469,17 @@ def main():
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)  # let the sampler take its first reading
+    # The library records each phase's start and end events on the launching
+    # stream, so the per-kernel durations come from the timed steps themselves.
     t_start.record(stream)
     for k in range(args.steps):
-        step()
+        step(ev[k])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     barrier(dev)
     ittt.stream_status(stream)
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
-    # Per-phase times from a second pass of the same length, with the
-    # library's phase events on (kept out of the timed region above).
-    for k in range(args.steps):
-        step(ev[k])
-    torch.cuda.synchronize(dev)
-    ittt.stream_status(stream)
     ms_per_step = elapsed_ms / args.steps
     tokens = B * T * world * args.steps
     value = tokens / (elapsed_ms / 1e3)

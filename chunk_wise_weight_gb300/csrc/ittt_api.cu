@@ -253,6 +253,8 @@ size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
 struct Plan {
   int64_t B = 0, T = 0, d = 0, f = 0, C = 0, M = 0;
   bool fused = false, dual = false, packed = false, l2norm = false;
+  bool update_only = false;  // fold every chunk into state_out, no apply
+  bool reuse = false;        // Z and eta*Vhat come in through z_buf / vhat_buf
   int64_t ndocs = 0;   // documents: B, or the packed count
   int64_t nslots = 0;  // snapshot slots = chunks over all documents
   int64_t n = 0;       // chunks per sequence (regular)
@@ -280,7 +282,7 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   if (o.pad_mode != ITTT_PAD_CHUNK && o.pad_mode != ITTT_PAD_SEQUENCE)
     return fail(ITTT_ERR_INVALID_ARG, "pad_mode %d", int(o.pad_mode));
   if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV | ITTT_FLAG_DUAL | ITTT_FLAG_L2_NORM |
-                          ITTT_FLAG_SINGLE_CTA))
+                          ITTT_FLAG_SINGLE_CTA | ITTT_FLAG_UPDATE_ONLY | ITTT_FLAG_REUSE_ZV))
     return fail(ITTT_ERR_INVALID_ARG, "unknown flags 0x%x", unsigned(o.flags));
   P->B = B;
   P->T = T;
@@ -295,6 +297,19 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   if (P->l2norm && P->dual)
     return fail(ITTT_ERR_UNSUPPORTED,
                 "the normalised update has no dual form (the update is not additive)");
+  P->update_only = (o.flags & ITTT_FLAG_UPDATE_ONLY) != 0;
+  P->reuse = (o.flags & ITTT_FLAG_REUSE_ZV) != 0;
+  if (P->update_only) {
+    if (o.state_out == nullptr)
+      return fail(ITTT_ERR_INVALID_ARG, "ITTT_FLAG_UPDATE_ONLY needs state_out");
+    if (o.snap_buf != nullptr)
+      return fail(ITTT_ERR_INVALID_ARG, "ITTT_FLAG_UPDATE_ONLY forms no snapshots: no snap_buf");
+    if (P->dual || P->l2norm)
+      return fail(ITTT_ERR_UNSUPPORTED,
+                  "ITTT_FLAG_UPDATE_ONLY needs the additive primal update (no dual, no L2 norm)");
+  }
+  if (P->reuse && (o.z_buf == nullptr || o.vhat_buf == nullptr))
+    return fail(ITTT_ERR_INVALID_ARG, "ITTT_FLAG_REUSE_ZV needs z_buf and vhat_buf");
   P->final_update = o.state_out != nullptr;
   if (P->dual && (o.state_out || o.snap_buf))
     return fail(ITTT_ERR_UNSUPPORTED,
@@ -375,7 +390,13 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
     P->ntiles2 = tiles2;
     for (int q = 0; q < P->n_udocs; ++q) ud[q] = upd[size_t(q)].second;
     P->ragged_walk = chunk % 64 != 0;
-    if (P->final_update)
+    if (P->update_only) {
+      // One contraction over each document's tokens.
+      P->n_udocs = int(nd);
+      P->ragged_walk = false;
+      for (int64_t k = 0; k < nd; ++k)
+        if ((cu[k + 1] - cu[k]) % 64 != 0) P->ragged_walk = true;
+    } else if (P->final_update)
       for (int64_t k = 0; k < nd; ++k) {
         const int64_t L = cu[k + 1] - cu[k];
         if ((L - ((L + chunk - 1) / chunk - 1) * chunk) % 64 != 0) P->ragged_walk = true;
@@ -389,6 +410,7 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
       P->active.assign(size_t(P->final_update ? P->n : P->n - 1), int(B));
     const int64_t last = T - (P->n - 1) * chunk;
     P->ragged_walk = chunk % 64 != 0 || (P->final_update && last % 64 != 0);
+    if (P->update_only) P->ragged_walk = T % 64 != 0;  // one contraction over T tokens
     P->ntiles = B * ((P->n - 1) * ((chunk + 127) / 128) + (last + 127) / 128);
     P->ntiles2 = B * ((P->n - 1) * ((chunk + 255) / 256) + (last + 255) / 256);
   }
@@ -415,8 +437,9 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   };
   if (o.z_buf == nullptr) L.z = take(size_t(P->M) * f * 2);
   if (o.vhat_buf == nullptr) L.vhat = take(size_t(P->M) * d * 2);
-  if (!P->fused) L.xc = take(size_t(P->M) * d * 2);
-  if (!P->dual && o.snap_buf == nullptr) L.snap = take(size_t(P->nslots) * d * f * 2);
+  if (!P->fused && !P->reuse) L.xc = take(size_t(P->M) * d * 2);
+  if (!P->dual && !P->update_only && o.snap_buf == nullptr)
+    L.snap = take(size_t(P->nslots) * d * f * 2);
   if (P->dual) {
     L.scores = take(size_t(B) * T * T * 2);
     if (o.state_in || !w0_bf16) L.w0b = take(size_t(o.state_in ? B : 1) * d * f * 2);
@@ -496,6 +519,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if (s != ITTT_OK) return s;
   const bool fused = P.fused, dual = P.dual;
   const bool single = (o.flags & ITTT_FLAG_SINGLE_CTA) != 0;
+  const bool update_only = P.update_only, reuse = P.reuse;
   const int64_t S = P.ndocs;  // per-document state count
 
   const int64_t sh_btd[3] = {B, T, d}, sh_fd[2] = {f, d}, sh_df[2] = {d, f}, sh_dd[2] = {d, d},
@@ -505,14 +529,18 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if ((s = check_tensor(X0, "X0", 3, sh_btd, true, false))) return s;
   if ((s = check_tensor(W_gate, "W_gate", 2, sh_fd, true, false))) return s;
   if ((s = check_tensor(W_up, "W_up", 2, sh_fd, true, false))) return s;
+  // Folding chunks only, with neither state_in nor W_down0, starts from zero.
+  const bool zero_start = update_only && o.state_in == nullptr && W_down0 == nullptr;
   if (o.state_in) {
     if ((s = check_tensor(o.state_in, "state_in", 3, sh_sdf, false, true))) return s;
-  } else if ((s = check_tensor(W_down0, "W_down0", 2, sh_df, true, true))) {
+  } else if (!zero_start && (s = check_tensor(W_down0, "W_down0", 2, sh_df, true, true))) {
     return s;
   }
   if ((s = check_tensor(W_target, "W_target", 2, sh_dd, true, false))) return s;
   if ((s = check_tensor(conv_w, "conv_w", 2, sh_d3, false, true))) return s;
-  if ((s = check_tensor(out, "out", 3, sh_btd, true, true))) return s;
+  // Nothing is applied when folding chunks only: out is ignored.
+  if (update_only) out = nullptr;
+  if (!update_only && (s = check_tensor(out, "out", 3, sh_btd, true, true))) return s;
   if (o.state_out && (s = check_tensor(o.state_out, "state_out", 3, sh_sdf, false, true))) return s;
   if (o.z_buf && (s = check_tensor(o.z_buf, "z_buf", 3, sh_btf, true, false))) return s;
   if (o.vhat_buf && (s = check_tensor(o.vhat_buf, "vhat_buf", 3, sh_btd, true, false))) return s;
@@ -527,6 +555,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     for (const ittt_tensor* in : inputs)
       if (overlaps(w, in)) return fail(ITTT_ERR_INVALID_ARG, "an output overlaps an input");
   }
+  // Reused Z and eta*Vhat are read by the walk and the apply: no written
+  // buffer may overlap them (the check above covers out, state_out and
+  // snap_buf against each other and against z_buf / vhat_buf).
   for (int a = 0; a < 5; ++a)
     for (int b = a + 1; b < 5; ++b)
       if (overlaps(writes[a], writes[b]))
@@ -592,22 +623,25 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   // Tensor maps.
   const uint64_t M = uint64_t(P.M);
   CUtensorMap tm_h, tm_wg, tm_wu, tm_a, tm_wt, tm_wt128, tm_vmn, tm_zmn, tm_zk, tm_snap;
-  if ((s = make_map(&tm_h, H->data, d, M, 64, 128, "H"))) return s;
-  if ((s = make_map(&tm_wg, W_gate->data, d, f, 64, 128, "W_gate"))) return s;
-  if ((s = make_map(&tm_wu, W_up->data, d, f, 64, 128, "W_up"))) return s;
-  if (fused) {
-    if ((s = make_map(&tm_a, X0->data, d, M, 64, 130, "X0"))) return s;
-  } else if ((s = make_map(&tm_a, xc, d, M, 64, 128, "Xc"))) {
-    return s;
-  }
-  if ((s = make_map(&tm_wt, W_target->data, d, d, 64, 256, "W_target"))) return s;
-  if ((s = make_map(&tm_wt128, W_target->data, d, d, 64, 128, "W_target (pair)"))) return s;
   // Output maps for the epilogues' TMA stores (Z's is tm_zk).
   CUtensorMap tm_vs, tm_ss, tm_os;
   memset(&tm_ss, 0, sizeof(tm_ss));
   memset(&tm_os, 0, sizeof(tm_os));
-  if ((s = make_map(&tm_vs, vhat, d, M, 64, 128, "Vhat (store)"))) return s;
-  if (out->dtype == ITTT_BF16 && (s = make_map(&tm_os, out->data, d, M, 64, 64, "O (store)")))
+  if (!reuse) {  // the producers of Z and eta*Vhat
+    if ((s = make_map(&tm_h, H->data, d, M, 64, 128, "H"))) return s;
+    if ((s = make_map(&tm_wg, W_gate->data, d, f, 64, 128, "W_gate"))) return s;
+    if ((s = make_map(&tm_wu, W_up->data, d, f, 64, 128, "W_up"))) return s;
+    if (fused) {
+      if ((s = make_map(&tm_a, X0->data, d, M, 64, 130, "X0"))) return s;
+    } else if ((s = make_map(&tm_a, xc, d, M, 64, 128, "Xc"))) {
+      return s;
+    }
+    if ((s = make_map(&tm_wt, W_target->data, d, d, 64, 256, "W_target"))) return s;
+    if ((s = make_map(&tm_wt128, W_target->data, d, d, 64, 128, "W_target (pair)"))) return s;
+    if ((s = make_map(&tm_vs, vhat, d, M, 64, 128, "Vhat (store)"))) return s;
+  }
+  if (out && out->dtype == ITTT_BF16 &&
+      (s = make_map(&tm_os, out->data, d, M, 64, 64, "O (store)")))
     return s;
   if ((s = make_map(&tm_vmn, vhat, d, M, 64, 64, "Vhat"))) return s;
   if ((s = make_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
@@ -624,6 +658,10 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     if ((s = make_map(&tm_w0b, w0b, f, uint64_t((o.state_in ? B : 1) * d), 64, 256, "bf16 W_0")))
       return s;
     if ((s = make_map(&tm_sc, scores, uint64_t(T), M, 64, 128, "scores"))) return s;
+  } else if (update_only) {
+    // No snapshot is formed; the walk's store map only needs valid memory.
+    if ((s = make_map_3d(&tm_ss, o.state_out->data, f, d, 1, 64, 128, "snapshots (unused)")))
+      return s;
   } else {
     if ((s = make_map(&tm_snap, snap, f, uint64_t(P.nslots * d), 64, 256, "snapshots"))) return s;
     if ((s = make_map(&tm_snap_pair, snap, f, uint64_t(P.nslots * d), 64, 128,
@@ -639,8 +677,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   }
 
   const ittt::LaunchEnv env{stream, ds->num_sms, ds->status};
-  const void* w0 = o.state_in ? o.state_in->data : W_down0->data;
-  const bool w0_fp32 = o.state_in ? true : (W_down0->dtype == ITTT_FP32);
+  // w0 == nullptr: the walk starts from zero (folding chunks only).
+  const void* w0 = o.state_in ? o.state_in->data : (zero_start ? nullptr : W_down0->data);
+  const bool w0_fp32 = o.state_in ? true : (!zero_start && W_down0->dtype == ITTT_FP32);
   const int64_t w0_bstride = o.state_in ? d * f : 0;
 
   cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(o.events);
@@ -657,14 +696,14 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if (what == nullptr && P.packed &&
       (s = stage_table(ds, tab, P.table.data(), P.table.size(), stream)) != ITTT_OK)
     return s;
-  if (!fused) {
+  if (!fused && !reuse) {
     ITTT_STEP(ittt::launch_conv(env, static_cast<const __nv_bfloat16*>(X0->data), cw, xc,
                                 int64_t(M), docs, int(d), int(o.pad_mode)),
               "conv launch");
   }
   ITTT_STEP(rec(2 * ITTT_PHASE_CONV + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_TARGET, stream), "event record");
-  if (what == nullptr) {
+  if (what == nullptr && !reuse) {
     const float* et = o.eta_tok ? static_cast<const float*>(o.eta_tok->data) : nullptr;
     // CTA pairs where two can be resident (split convolution), else one CTA.
     e = fused || single ? cudaErrorNotSupported
@@ -679,7 +718,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   }
   ITTT_STEP(rec(2 * ITTT_PHASE_TARGET + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP, stream), "event record");
-  if (what == nullptr) {
+  if (what == nullptr && !reuse) {
     e = single ? cudaErrorNotSupported
                : ittt::launch_gateup_pair(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d));
     if (e == cudaErrorNotSupported) {
@@ -690,10 +729,14 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   }
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP + 1, stream), "event record");
   ITTT_STEP(rec(2 * ITTT_PHASE_SNAPSHOT0, stream), "event record");
-  if (!dual && !w0_direct) {
-    ITTT_STEP(ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride, snap, docs, int(d), int(f)),
-              "snapshot launch");
+  if (!dual) {
+    // Slot 0 of each document, unless the apply reads a shared bf16 W_0
+    // itself or nothing is applied.
+    if (!w0_direct && !update_only)
+      ITTT_STEP(ittt::launch_snapshot0(env, w0, w0_fp32, w0_bstride, snap, docs, int(d), int(f)),
+                "snapshot launch");
   } else if (!w0_is_bf16) {
+    // The dual form's bf16 copy of each W_0.
     ittt::DocMap w0docs;
     memset(&w0docs, 0, sizeof(w0docs));
     w0docs.ndocs = int(o.state_in ? B : 1);
@@ -710,6 +753,16 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if (!dual) {
     ittt::UpdateArgs ua;
     ua.docs = docs;
+    if (update_only) {
+      // The update is additive, so folding every chunk is one contraction
+      // over each document's tokens: walk with a single chunk of T tokens
+      // (no boundary, so no snapshot) and keep the final state.
+      ua.docs.C = int(T);
+      ua.docs.n = 1;
+      ua.docs.nchunks = int(P.ndocs);
+      ua.docs.chunk_base = nullptr;
+      ua.docs.chunk_doc = nullptr;
+    }
     ua.upd_docs = upd_docs;
     ua.n_udocs = P.n_udocs;
     ua.final_update = P.final_update;
@@ -744,7 +797,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     }
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
-    if (what == nullptr) {
+    if (what == nullptr && !update_only) {
       // CTA pairs where two can be resident, else one CTA per tile.
       e = single ? cudaErrorNotSupported
                  : ittt::launch_apply_pair(env, tm_zk, tm_snap_pair,
@@ -810,6 +863,46 @@ ittt_status ittt_forward_ex(const ittt_tensor* H, const ittt_tensor* X0,
                             ittt_tensor* out, ittt_stream_t stream, const ittt_opts* opts) {
   return forward_impl(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta, chunk, out,
                       reinterpret_cast<cudaStream_t>(stream), opts);
+}
+
+ittt_status ittt_state_prefix(const ittt_tensor* W_start, const ittt_tensor* deltas,
+                              int32_t count, ittt_tensor* state, ittt_stream_t stream) {
+  g_last_error.clear();
+  if (deltas == nullptr || deltas->ndim != 4)
+    return fail(ITTT_ERR_INVALID_ARG, "deltas: expected an [R,S,d,f] descriptor");
+  const int64_t R = deltas->shape[0], S = deltas->shape[1], d = deltas->shape[2],
+                f = deltas->shape[3];
+  if (R <= 0 || S <= 0 || d <= 0 || f <= 0)
+    return fail(ITTT_ERR_INVALID_ARG, "deltas: sizes must be positive");
+  if (d % 8 != 0 || f % 8 != 0)
+    return fail(ITTT_ERR_UNSUPPORTED, "d_model=%lld and d_ff=%lld must be multiples of 8",
+                (long long)d, (long long)f);
+  if (count < 0 || count > R)
+    return fail(ITTT_ERR_INVALID_ARG, "count %d outside 0..%lld", int(count), (long long)R);
+  const int64_t sh_r[4] = {R, S, d, f}, sh_s[3] = {S, d, f}, sh_df[2] = {d, f};
+  ittt_status s;
+  if ((s = check_tensor(deltas, "deltas", 4, sh_r, false, true))) return s;
+  if ((s = check_tensor(state, "state", 3, sh_s, false, true))) return s;
+  int kind = 0;
+  if (W_start != nullptr) {
+    if (W_start->ndim == 2) {
+      if ((s = check_tensor(W_start, "W_start", 2, sh_df, true, true))) return s;
+      kind = W_start->dtype == ITTT_BF16 ? 1 : 2;
+    } else {
+      if ((s = check_tensor(W_start, "W_start", 3, sh_s, false, true))) return s;
+      kind = 3;
+    }
+  }
+  if (overlaps(state, deltas) || overlaps(state, W_start))
+    return fail(ITTT_ERR_INVALID_ARG, "state overlaps an input");
+  DeviceState* ds = nullptr;
+  if ((s = device_state(&ds))) return s;
+  const ittt::LaunchEnv env{reinterpret_cast<cudaStream_t>(stream), ds->num_sms, ds->status};
+  const cudaError_t e = ittt::launch_state_prefix(
+      env, W_start ? W_start->data : nullptr, kind, static_cast<const float*>(deltas->data),
+      int(count), static_cast<float*>(state->data), S, d * f);
+  if (e != cudaSuccess) return cuda_fail(e, "state prefix launch");
+  return ITTT_OK;
 }
 
 size_t ittt_workspace_bytes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk) {

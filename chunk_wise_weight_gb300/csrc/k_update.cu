@@ -66,12 +66,12 @@ __device__ __forceinline__ uint64_t mn_desc(uint32_t base, int k) {
 }
 
 // Eight fp32 values of the initial state W_0 (bf16 or fp32 source; zeros
-// outside the [d, f] state).
+// outside the [d, f] state, and everywhere when w0 is null: a zero start).
 __device__ __forceinline__ void load_w0_8(const void* w0, bool fp32, size_t off, bool ok,
                                           float* w) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) w[j] = 0.f;
-  if (!ok) return;
+  if (!ok || w0 == nullptr) return;
   if (fp32) {
     const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(w0) + off);
     const float4 lo = __ldg(src), hi = __ldg(src + 1);
@@ -594,6 +594,53 @@ cudaError_t launch_snapshot0(const LaunchEnv& env, const void* w0, bool w0_fp32,
   if (blocks > cap) blocks = cap;
   snapshot0_kernel<<<int(blocks), 256, 0, env.stream>>>(w0, w0_fp32 ? 1 : 0, w0_bstride, snap,
                                                         docs, df);
+  return cudaGetLastError();
+}
+
+// state[s] = W_start[s] + deltas[0, s] + ... + deltas[count-1, s], four fp32
+// elements a thread-step, added in that order.  w0_kind: 0 zero start, 1 a
+// shared bf16 [d, f], 2 a shared fp32 [d, f], 3 fp32 [S, d, f].  df = d * f
+// is a multiple of 64, so a group of four never straddles two states.
+__global__ void __launch_bounds__(256)
+    state_prefix_kernel(const void* __restrict__ w0, int w0_kind, const float* __restrict__ deltas,
+                        int64_t per_delta, int count, float* __restrict__ state, int64_t df,
+                        int64_t groups) {
+  for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+       g += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t e = g * 4;
+    const int64_t r = e % df;  // element within its state
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (w0_kind == 1) {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(w0) + r));
+      const float2 lo = unpack_bf16x2(raw.x), hi = unpack_bf16x2(raw.y);
+      acc = make_float4(lo.x, lo.y, hi.x, hi.y);
+    } else if (w0_kind == 2 || w0_kind == 3) {
+      acc = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(w0) +
+                                                  (w0_kind == 3 ? e : r)));
+    }
+#pragma unroll 1
+    for (int k = 0; k < count; ++k) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(deltas + int64_t(k) * per_delta + e));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(state + e) = acc;
+  }
+}
+
+cudaError_t launch_state_prefix(const LaunchEnv& env, const void* w0, int w0_kind,
+                                const float* deltas, int count, float* state, int64_t S,
+                                int64_t df) {
+  const int64_t groups = S * df / 4;
+  if (groups == 0) return cudaSuccess;
+  // Grid-stride over a few blocks per SM: the kernel streams HBM.
+  const int64_t want = (groups + 255) / 256;
+  const int64_t cap = int64_t(env.num_sms) * 8;
+  const int grid = int(want < cap ? want : cap);
+  state_prefix_kernel<<<grid, 256, 0, env.stream>>>(w0, w0_kind, deltas, S * df, count, state, df,
+                                                    groups);
   return cudaGetLastError();
 }
 

@@ -92,6 +92,14 @@ struct DocMap {
 #endif
 };
 
+// state[s] = W_start[s] + sum_{k < count} deltas[k, s] over S states of
+// df = d * f fp32 elements (df a multiple of 64), added in that order.
+// w0_kind: 0 zero start, 1 shared bf16 [d, f], 2 shared fp32 [d, f],
+// 3 fp32 [S, d, f].  deltas: [count.., S, d, f] fp32.
+cudaError_t launch_state_prefix(const LaunchEnv& env, const void* w0, int w0_kind,
+                                const float* deltas, int count, float* state, int64_t S,
+                                int64_t df);
+
 // Z[M, f] = SiLU(H W_gate^T) * (H W_up^T) on single CTAs (fallback).  Tensor
 // maps: H [M, K] box {64,128}; W_gate, W_up [f, K] box {64,128}; Z [M, f] box
 // {64,128} for the TMA stores.  All bf16, K = d_model.

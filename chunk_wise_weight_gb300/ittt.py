@@ -26,6 +26,8 @@ FLAG_FUSED_CONV = 1
 FLAG_DUAL = 2
 FLAG_L2_NORM = 4
 FLAG_SINGLE_CTA = 8
+FLAG_UPDATE_ONLY = 16
+FLAG_REUSE_ZV = 32
 
 _DTYPES = {torch.bfloat16: BF16, torch.float32: FP32}
 
@@ -87,6 +89,8 @@ def load(path: str | None = None):
     lib.ittt_version.restype = ctypes.c_int32
     lib.ittt_launch_count.argtypes = [ctypes.c_int64] * 5
     lib.ittt_launch_count.restype = ctypes.c_int32
+    lib.ittt_state_prefix.argtypes = [_TP, _TP, ctypes.c_int32, _TP, ctypes.c_void_p]
+    lib.ittt_state_prefix.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -145,11 +149,13 @@ def _seqlens(cu_seqlens):
 
 
 def _opts(pad_mode, fused_conv, dual, cu_seqlens, keep: dict, l2norm=False,
-          single_cta=False, **tensors) -> Opts:
+          single_cta=False, update_only=False, reuse_zv=False, **tensors) -> Opts:
     opts = Opts()
     opts.pad_mode = int(pad_mode)
     opts.flags = ((FLAG_FUSED_CONV if fused_conv else 0) | (FLAG_DUAL if dual else 0)
-                  | (FLAG_L2_NORM if l2norm else 0) | (FLAG_SINGLE_CTA if single_cta else 0))
+                  | (FLAG_L2_NORM if l2norm else 0) | (FLAG_SINGLE_CTA if single_cta else 0)
+                  | (FLAG_UPDATE_ONLY if update_only else 0)
+                  | (FLAG_REUSE_ZV if reuse_zv else 0))
     for name, t in tensors.items():
         if t is not None:
             keep[name] = describe(t)
@@ -167,19 +173,26 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
             pad_mode: int = PAD_CHUNK, state_in=None, state_out=None, z_buf=None,
             vhat_buf=None, snap_buf=None, workspace=None, events=None,
             fused_conv: bool = False, dual: bool = False, eta_tok=None,
-            cu_seqlens=None, l2norm: bool = False, single_cta: bool = False) -> torch.Tensor:
+            cu_seqlens=None, l2norm: bool = False, single_cta: bool = False,
+            update_only: bool = False, reuse_zv: bool = False):
     """Enqueue one layer forward on `stream` (default: current stream) and
     return `out` [B,T,d].  Extra keyword buffers map to ittt_opts; `events`
     is a list of 2 * len(PHASES) torch.cuda.Event(enable_timing=True): a
     (start, end) pair per phase.  `cu_seqlens` (host ints, num_docs + 1
-    offsets) packs documents into the one row of H [1,T,d]."""
+    offsets) packs documents into the one row of H [1,T,d].
+    `update_only` folds every chunk into `state_out` and applies nothing
+    (returns None; W_down0 None starts from zero); `reuse_zv` takes Z and
+    eta * Vhat from `z_buf` / `vhat_buf` instead of computing them."""
     lib = load()
-    if out is None:
+    if update_only:
+        out = None
+    elif out is None:
         out = torch.empty(H.shape, dtype=out_dtype, device=H.device)
     keep = [describe(x) for x in (H, X0, W_gate, W_up, W_down0, W_target, conv_w, out)]
     extra = {}
     opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, extra, l2norm=l2norm,
-                 single_cta=single_cta, state_in=state_in,
+                 single_cta=single_cta, update_only=update_only, reuse_zv=reuse_zv,
+                 state_in=state_in,
                  state_out=state_out, z_buf=z_buf, vhat_buf=vhat_buf, snap_buf=snap_buf,
                  eta_tok=eta_tok)
     if workspace is not None:
@@ -213,6 +226,22 @@ def forward_plain(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, ch
     return out
 
 
+def state_prefix(W_start, deltas: torch.Tensor, count: int, state: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """ittt_state_prefix: state = W_start + deltas[0] + ... + deltas[count-1]
+    (fp32, in that order).  W_start: [d,f] bf16/fp32 shared by every state,
+    [S,d,f] fp32, or None (zero); deltas: fp32 [R,S,d,f]; returns `state`
+    [S,d,f] fp32."""
+    lib = load()
+    if state is None:
+        state = torch.empty(deltas.shape[1:], dtype=torch.float32, device=deltas.device)
+    keep = [describe(W_start), describe(deltas), describe(state)]
+    s = _stream_handle(stream, deltas.device)
+    _check(lib.ittt_state_prefix(_ref(keep[0]), _ref(keep[1]), ctypes.c_int32(count),
+                                 _ref(keep[2]), ctypes.c_void_p(s)))
+    return state
+
+
 def stream_status(stream=None, device=None) -> None:
     """Synchronise and raise IttError if a kernel recorded a failure."""
     _check(load().ittt_stream_status(ctypes.c_void_p(_stream_handle(stream, device))))
@@ -224,13 +253,15 @@ def workspace_bytes(B: int, T: int, d: int, f: int, chunk: int) -> int:
 
 def workspace_bytes_ex(B: int, T: int, d: int, f: int, chunk: int, *, pad_mode: int = PAD_CHUNK,
                        fused_conv: bool = False, dual: bool = False, cu_seqlens=None,
-                       l2norm: bool = False, **buffers) -> int:
+                       l2norm: bool = False, update_only: bool = False, reuse_zv: bool = False,
+                       **buffers) -> int:
     """ittt_workspace_bytes_ex: scratch for a forward call with these
     options; `buffers` name the ittt_opts tensors the call passes (state_in,
     state_out, z_buf, vhat_buf, snap_buf, eta_tok) -- only whether each is
     given matters."""
     keep = {}
-    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, keep, l2norm=l2norm, **buffers)
+    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, keep, l2norm=l2norm,
+                 update_only=update_only, reuse_zv=reuse_zv, **buffers)
     return int(load().ittt_workspace_bytes_ex(B, T, d, f, chunk, ctypes.byref(opts)))
 
 

@@ -1,11 +1,26 @@
-"""Batch sharding across ranks (one process per GPU).
+"""Sharding the layer across ranks (one process per GPU).
 
-Each sequence carries its own fast-weight state that starts from W_down0
-(reset at document boundaries, "[논문리뷰] In-Place Test-Time Training",
-Method §3), so sequences are independent units: a rank runs the layer on its
-contiguous share of the batch and no tensor crosses ranks.  The only
-cross-rank traffic is host-side bookkeeping: barriers and the max of the
-ranks' timings.
+Batch sharding.  Each sequence carries its own fast-weight state that starts
+from W_down0 (reset at document boundaries, "[논문리뷰] In-Place Test-Time
+Training", Method §3), so sequences are independent units: a rank runs the
+layer on its contiguous share of the batch and no tensor crosses ranks.  The
+only cross-rank traffic is host-side bookkeeping: barriers and the max of
+the ranks' timings.
+
+Sequence sharding (context parallelism, Method §3 "Implementation Details":
+per-chunk deltas in parallel, one prefix sum, then the apply).  Rank r owns
+a contiguous span of whole chunks of every sequence.  The update is additive
+and each chunk's delta depends on that chunk's tokens alone (the convolution
+is zero-padded at chunk edges), so
+
+  1. every rank folds its span into D_r = eta * sum_{i in span r}
+     Vhat_[i]^T Z_[i] from a zero start, keeping Z and eta * Vhat;
+  2. the ranks all-gather the D_r (one [B, d, f] fp32 tensor each);
+  3. rank r starts from W_down0 + D_0 + ... + D_{r-1} (an exclusive prefix)
+     and runs the usual walk and apply over its span, reusing Z and eta*Vhat.
+
+The all-gather is the one data-path collective.  The work per token is the
+single-GPU work plus one extra 2*d*f-FLOP contraction (step 1's fold).
 """
 from __future__ import annotations
 
@@ -21,6 +36,18 @@ def shard_range(total: int, world: int, rank: int) -> tuple[int, int]:
     base, extra = divmod(total, world)
     start = rank * base + min(rank, extra)
     return start, start + base + (1 if rank < extra else 0)
+
+
+def sequence_span(T: int, chunk: int, world: int, rank: int) -> tuple[int, int]:
+    """Token span [start, stop) of `rank` when the chunks of a T-token
+    sequence are shared out in contiguous runs: spans start on chunk
+    boundaries, only the last non-empty span may end in a partial chunk, and
+    ranks beyond the chunk count get an empty span."""
+    if chunk <= 0 or T < 0:
+        raise ValueError("bad T/chunk")
+    n = -(-T // chunk)
+    a, b = shard_range(n, world, rank)
+    return min(a * chunk, T), min(b * chunk, T)
 
 
 def max_over_ranks(value: float, device: torch.device | None = None) -> float:
@@ -39,3 +66,80 @@ def barrier(device: torch.device | None = None) -> None:
             dist.barrier(device_ids=[device.index])
         else:
             dist.barrier()
+
+
+class CudaEngine:
+    """The three per-rank steps of sequence sharding on the library's kernels."""
+
+    def __init__(self, stream=None):
+        from . import ittt
+        self.ittt = ittt
+        self.stream = stream
+
+    def fold(self, H, X0, W_gate, W_up, W_target, conv_w, eta, chunk, eta_tok=None):
+        """D = eta * sum_i Vhat_[i]^T Z_[i] over the span's chunks (zero
+        start); returns (D [B,d,f] fp32, (Z, eta * Vhat))."""
+        B, T, d = H.shape
+        f = W_gate.shape[0]
+        z = torch.empty(B, T, f, dtype=torch.bfloat16, device=H.device)
+        vhat = torch.empty(B, T, d, dtype=torch.bfloat16, device=H.device)
+        delta = torch.empty(B, d, f, dtype=torch.float32, device=H.device)
+        self.ittt.forward(H, X0, W_gate, W_up, None, W_target, conv_w, eta, chunk,
+                          stream=self.stream, update_only=True, state_out=delta, z_buf=z,
+                          vhat_buf=vhat, eta_tok=eta_tok)
+        return delta, (z, vhat)
+
+    def zeros(self, B, d, f, device):
+        return torch.zeros(B, d, f, dtype=torch.float32, device=device)
+
+    def prefix(self, W_down0, deltas, count):
+        """W_down0 + deltas[0] + ... + deltas[count-1] (fp32 [B,d,f])."""
+        return self.ittt.state_prefix(W_down0, deltas, count, stream=self.stream)
+
+    def apply(self, H, X0, W_gate, W_up, W_target, conv_w, eta, chunk, zv, state_in,
+              out=None):
+        z, vhat = zv
+        return self.ittt.forward(H, X0, W_gate, W_up, None, W_target, conv_w, eta, chunk, out,
+                                 stream=self.stream, state_in=state_in, reuse_zv=True, z_buf=z,
+                                 vhat_buf=vhat)
+
+
+def sequence_parallel_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float,
+                              chunk: int, *, eta_tok=None, group=None, engine=None,
+                              want_state: bool = False):
+    """This rank's part of a sequence-sharded forward.
+
+    H, X0 [B, T_r, d] (and eta_tok [B, T_r]) hold this rank's span of every
+    sequence, as `sequence_span` assigns it: a multiple of `chunk` tokens
+    except on the last non-empty span, possibly empty.  Every rank of
+    `group` must call this together (the deltas are all-gathered).  Returns
+    O [B, T_r, d] for the span and, with `want_state`, the fast weight after
+    the span (on the last rank: after the whole sequence).  The convolution
+    is zero-padded at chunk edges (the default pad mode), so no token crosses
+    a span boundary.
+    """
+    engine = engine or CudaEngine()
+    if dist.is_available() and dist.is_initialized():
+        world, rank = dist.get_world_size(group), dist.get_rank(group)
+    else:
+        world, rank = 1, 0
+    B, T_r, d = H.shape
+    f = W_gate.shape[0]
+    if T_r > 0:
+        delta, zv = engine.fold(H, X0, W_gate, W_up, W_target, conv_w, eta, chunk,
+                                eta_tok=eta_tok)
+    else:
+        delta, zv = engine.zeros(B, d, f, H.device), None
+    if world > 1:
+        deltas = delta.new_empty((world,) + tuple(delta.shape))
+        dist.all_gather(list(deltas.unbind(0)), delta, group=group)
+    else:
+        deltas = delta.unsqueeze(0)
+    state_in = engine.prefix(W_down0, deltas, rank)
+    if T_r > 0:
+        O = engine.apply(H, X0, W_gate, W_up, W_target, conv_w, eta, chunk, zv, state_in)
+    else:
+        O = H.new_empty((B, 0, d))
+    if want_state:
+        return O, engine.prefix(W_down0, deltas, rank + 1)
+    return O

@@ -115,7 +115,9 @@ typedef struct {
  *   state_in   fp32 [S,d,f]: per-sequence (S = B) or per-document
  *              (S = num_docs) initial fast weight.  Replaces W_down0 (which
  *              may then be NULL) -- continues a stream of chunks from a
- *              state returned by an earlier call.
+ *              state returned by an earlier call, or starts a span of a
+ *              sequence from the prefix of the spans before it
+ *              (ittt_state_prefix).
  *   state_out  fp32 [S,d,f]: receives each sequence's or document's fast
  *              weight after its LAST chunk's update (an update the output
  *              itself never needs).
@@ -185,6 +187,23 @@ typedef struct {
  * resident).  Same results; for systems where 2-CTA clusters cannot be
  * scheduled and for comparing the two. */
 #define ITTT_FLAG_SINGLE_CTA 8
+/* Fold the call's chunks into the fast weight without applying it:
+ * state_out (required) receives W_start + eta sum_i Vhat_[i]^T Z_[i] over
+ * every chunk of each sequence or document, W_start being state_in, else
+ * W_down0, else (both NULL) zero -- with a zero start it is the sum of the
+ * call's per-chunk deltas, the quantity the parallel form of Method §3 sums
+ * ahead of the apply ("Implementation Details", context parallelism).  The
+ * update is additive, so the whole sequence is one contraction over its
+ * tokens: no snapshots are formed and nothing is applied (out may be NULL;
+ * snap_buf must be NULL).  Not combinable with ITTT_FLAG_DUAL or
+ * ITTT_FLAG_L2_NORM. */
+#define ITTT_FLAG_UPDATE_ONLY 16
+/* z_buf and vhat_buf are INPUTS: they already hold Z and eta * Vhat for
+ * these tokens (from an earlier call with the same H, X0, weights, eta,
+ * eta_tok, chunk and pad mode, e.g. an ITTT_FLAG_UPDATE_ONLY call), so the
+ * conv, target and gate/up phases are skipped.  H, X0, W_gate, W_up,
+ * W_target and conv_w are checked for shape but not read. */
+#define ITTT_FLAG_REUSE_ZV 32
 
 /* Kernel phases of one forward call, in launch order. */
 typedef enum {
@@ -253,6 +272,25 @@ ITTT_API ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_tenso
                                           const ittt_tensor* W_target,
                                           const ittt_tensor* conv_w, float eta, int64_t chunk,
                                           ittt_tensor* out, ittt_stream_t stream);
+
+/*
+ * state[s] = W_start[s] + sum_{k < count} deltas[k, s] for each of the S
+ * fast-weight states, summed in fp32 in that order (W_start first, then
+ * deltas[0], deltas[1], ...).  This is the exclusive prefix of the parallel
+ * form ("[논문리뷰] In-Place Test-Time Training", Method §3 "Implementation
+ * Details": per-chunk deltas computed in parallel, one prefix sum, then the
+ * apply): when span k of a sequence has folded its chunks into deltas[k]
+ * (ITTT_FLAG_UPDATE_ONLY from a zero start), span r starts from the prefix
+ * with count = r.
+ *   W_start  W_down0 [d,f] bf16 or fp32 (shared by every state), an fp32
+ *            [S,d,f] per-state start, or NULL (zero).
+ *   deltas   fp32 [R,S,d,f] device tensor; count in 0..R.
+ *   state    fp32 [S,d,f] device tensor; must not overlap the inputs.
+ * Enqueued on `stream` like ittt_forward; argument errors are reported
+ * before anything is enqueued.
+ */
+ITTT_API ittt_status ittt_state_prefix(const ittt_tensor* W_start, const ittt_tensor* deltas,
+                                       int32_t count, ittt_tensor* state, ittt_stream_t stream);
 
 /*
  * Bytes of device scratch one call needs for these sizes with default flags

@@ -125,7 +125,7 @@ def test_rejects_bad_options(lib):
     o.pad_mode = 7
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     o = ittt.Opts()
-    o.flags = 16
+    o.flags = 64
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     assert "flags" in ittt.last_error()
     o = ittt.Opts()
@@ -252,3 +252,75 @@ def test_python_binding_has_no_compute_fallback():
     assert "oracle" not in src.replace("no fallback", "")
     for op in ("torch.matmul", "F.linear", "silu", "conv1d", "einsum", "@"):
         assert op not in src
+
+
+def test_update_only_and_reuse_options(lib):
+    a = _args()
+    st = _desc([1, 64, 256], ittt.FP32, data=FAKE * 9 * 1024)
+    sb = _desc([1, 4, 64, 256], ittt.BF16, data=FAKE * 10 * 1024)
+    o = ittt.Opts()
+    o.flags = ittt.FLAG_UPDATE_ONLY                                     # nowhere to put the state
+    assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
+    assert "state_out" in ittt.last_error()
+    o.state_out = ctypes.pointer(st)
+    o.snap_buf = ctypes.pointer(sb)                                     # no snapshots are formed
+    assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
+    assert "snap_buf" in ittt.last_error()
+    for extra in (ittt.FLAG_DUAL, ittt.FLAG_L2_NORM):
+        o = ittt.Opts()
+        o.flags = ittt.FLAG_UPDATE_ONLY | extra
+        o.state_out = ctypes.pointer(st)
+        assert _call(lib, a, opts=o) == ittt.ERR_UNSUPPORTED
+    o = ittt.Opts()
+    o.flags = ittt.FLAG_REUSE_ZV                                        # nothing to reuse
+    assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
+    assert "z_buf" in ittt.last_error()
+
+
+def test_update_only_and_reuse_scratch():
+    def r(x):
+        return (x + 255) // 256 * 256
+    B, T, d, f, C = 2, 1024, 320, 1000, 256
+    n = T // C
+    z, vh, xc, snap = r(B * T * f * 2), r(B * T * d * 2), r(B * T * d * 2), r(B * n * d * f * 2)
+    fake = torch.empty(0)
+    # folding chunks only forms no snapshots
+    assert (ittt.workspace_bytes_ex(B, T, d, f, C, update_only=True, state_out=fake)
+            == z + vh + xc)
+    assert ittt.workspace_bytes_ex(B, T, d, f, C, update_only=True) == 0   # needs state_out
+    # reusing Z and eta*Vhat needs neither the producers' scratch nor Xc
+    assert (ittt.workspace_bytes_ex(B, T, d, f, C, reuse_zv=True, z_buf=fake, vhat_buf=fake)
+            == snap)
+    assert ittt.workspace_bytes_ex(B, T, d, f, C, reuse_zv=True, z_buf=fake) == 0
+    assert ittt.workspace_bytes_ex(B, T, d, f, C, update_only=True, reuse_zv=True,
+                                   state_out=fake, z_buf=fake, vhat_buf=fake) == 0
+
+
+def _prefix_call(lib, W_start, deltas, count, state):
+    if torch.cuda.is_available():
+        pytest.skip("argument checks with fake device pointers run on hosts without a GPU")
+    r = lambda x: None if x is None else ctypes.byref(x)  # noqa: E731
+    return lib.ittt_state_prefix(r(W_start), r(deltas), ctypes.c_int32(count), r(state), None)
+
+
+def test_state_prefix_rejects_bad_arguments(lib):
+    R, S, d, f = 3, 2, 64, 256
+    dl = _desc([R, S, d, f], ittt.FP32, data=FAKE)
+    st = _desc([S, d, f], ittt.FP32, data=FAKE * 1024)
+    w0 = _desc([d, f], ittt.BF16, data=FAKE * 2048)
+    assert _prefix_call(lib, w0, _desc([S, d, f], ittt.FP32), 1, st) == ittt.ERR_INVALID_ARG
+    assert _prefix_call(lib, w0, dl, R + 1, st) == ittt.ERR_INVALID_ARG
+    assert "count" in ittt.last_error()
+    assert _prefix_call(lib, w0, dl, -1, st) == ittt.ERR_INVALID_ARG
+    assert _prefix_call(lib, w0, dl, 1, _desc([S, d, f], ittt.BF16, data=FAKE * 1024)) \
+        == ittt.ERR_INVALID_ARG
+    assert _prefix_call(lib, _desc([d, f + 8], ittt.BF16, data=FAKE * 2048), dl, 1, st) \
+        == ittt.ERR_INVALID_ARG
+    assert _prefix_call(lib, _desc([S, d, f], ittt.BF16, data=FAKE * 2048), dl, 1, st) \
+        == ittt.ERR_INVALID_ARG                                         # per-state starts are fp32
+    assert _prefix_call(lib, w0, dl, 1, _desc([S, d, f], ittt.FP32, data=FAKE + 4096)) \
+        == ittt.ERR_INVALID_ARG                                         # state inside the deltas
+    assert "overlaps" in ittt.last_error()
+    odd = _desc([R, S, 60, f], ittt.FP32, data=FAKE)
+    assert _prefix_call(lib, None, odd, 1, _desc([S, 60, f], ittt.FP32, data=FAKE * 1024)) \
+        == ittt.ERR_UNSUPPORTED

@@ -564,8 +564,13 @@ def test_status_and_argument_errors_on_device(cuda_device):
 # Full-size named workloads: sampled entries against the oracle
 # --------------------------------------------------------------------------
 
-def _sampled_checks(index, device, n_state_pairs=24, n_rows=6, dual=False):
-    cfg, inp = config_inputs(index)
+def _sampled_checks(index, device, n_state_pairs=24, n_rows=6, dual=False, shape=None):
+    if shape is None:
+        cfg, inp = config_inputs(index)
+    else:
+        B, T, d, f, C, eta = shape
+        cfg = dict(B=B, T=T, d=d, f=f, C=C, eta=eta)
+        inp = make_inputs(B, T, d, f, seed=index)
     B, T, d, f, C, eta = cfg["B"], cfg["T"], cfg["d"], cfg["f"], cfg["C"], cfg["eta"]
     n = T // C
     g = to_device(inp, device)
@@ -614,3 +619,196 @@ def test_named_workload_sampled(cuda_device, index):
 @pytest.mark.parametrize("index", [3, 4])
 def test_named_workload_sampled_large(cuda_device, index):
     _sampled_checks(index, cuda_device, n_state_pairs=12)
+
+
+def test_longest_sequence_sampled(cuda_device):
+    """262,144 tokens in one sequence (64 chunks of 4096; Z alone is 5 GB and
+    T * d_ff exceeds 2^31 elements): the same sampled checks."""
+    _sampled_checks(1700, cuda_device, n_state_pairs=6, shape=(1, 262144, 2560, 9728, 4096, 0.005))
+
+
+# --------------------------------------------------------------------------
+# Sequence sharding: folding a span (ITTT_FLAG_UPDATE_ONLY), the exclusive
+# prefix of the spans' deltas (ittt_state_prefix), and the apply that reuses
+# Z and eta * Vhat (ITTT_FLAG_REUSE_ZV); ranks emulated one after another
+# on this GPU (no kernel waits on another)
+# --------------------------------------------------------------------------
+
+FOLD = [
+    # B, T, d, f, C, eta
+    (2, 512, 200, 584, 128, 0.05),   # CTA pairs: T a multiple of 64
+    (1, 333, 136, 264, 160, 0.1),    # ragged T: single-CTA walk with masked K tail
+    (3, 384, 64, 256, 384, 0.2),     # one chunk
+]
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", FOLD)
+def test_update_only_folds_every_chunk(cuda_device, B, T, d, f, C, eta):
+    inp = make_inputs(B, T, d, f, seed=1800 + T)
+    g = to_device(inp, cuda_device)
+    rates = torch.rand(B, T, generator=torch.Generator().manual_seed(6)) + 0.5
+    ref = oracle.forward(inp, eta, C, want_states=True, eta_tok=rates)
+    zero = dict(inp, W_down0=torch.zeros(d, f))
+    delta_ref = oracle.forward(zero, eta, C, want_states=True, eta_tok=rates)["states"][:, -1]
+    start = torch.randn(B, d, f, generator=torch.Generator().manual_seed(7)) * 0.02
+    start_ref = oracle.forward(dict(inp, W_down0=start), eta, C, want_states=True,
+                               eta_tok=rates)["states"][:, -1]
+    et = rates.to(cuda_device)
+    plain = run(g, eta, C, intermediates=True, eta_tok=et)
+    for w0, state_in, want in ((None, None, delta_ref), (g["W_down0"], None, ref["states"][:, -1]),
+                               (None, start.to(cuda_device), start_ref)):
+        st = torch.empty(B, d, f, dtype=torch.float32, device=cuda_device)
+        z = torch.empty_like(plain["z_buf"])
+        vh = torch.empty_like(plain["vhat_buf"])
+        res = ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], w0, g["W_target"],
+                           g["conv_w"], eta, C, update_only=True, state_in=state_in,
+                           state_out=st, z_buf=z, vhat_buf=vh, eta_tok=et)
+        ittt.stream_status()
+        assert res is None
+        assert_parity(host(st), want, "folded state")
+        # the producers are the forward's own: identical Z and eta * Vhat
+        assert torch.equal(z, plain["z_buf"]) and torch.equal(vh, plain["vhat_buf"])
+
+
+def test_update_only_packed_documents(cuda_device):
+    cu = [0, 100, 356, 512]
+    d, f, C, eta = 136, 264, 64, 0.05
+    inp = make_inputs(1, 512, d, f, seed=1810)
+    zero = dict(inp, W_down0=torch.zeros(d, f))
+    ref = oracle.forward_packed(zero, cu, eta, C, want_states=True)
+    g = to_device(inp, cuda_device)
+    st = torch.empty(3, d, f, dtype=torch.float32, device=cuda_device)
+    ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], None, g["W_target"], g["conv_w"],
+                 eta, C, update_only=True, state_out=st, cu_seqlens=cu)
+    ittt.stream_status()
+    for k in range(3):
+        assert_parity(host(st[k]), ref["states"][k][-1], f"document {k} folded")
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", SHAPES[:4] + [RAGGED[0]])
+def test_reuse_zv_is_bitwise_the_forward(cuda_device, B, T, d, f, C, eta):
+    """Given the Z and eta * Vhat a forward produced, the reusing call walks
+    and applies the same operands: identical snapshots and output."""
+    g = to_device(make_inputs(B, T, d, f, seed=1820 + T), cuda_device)
+    a = run(g, eta, C, intermediates=True, want_state=True)
+    snap = torch.empty_like(a["snap_buf"])
+    st = torch.empty_like(a["state_out"])
+    # the reusing call must not read H, X0 or the producer weights: poison them
+    poisoned = {k: (torch.full_like(v, float("nan")) if k in ("H", "X0", "W_gate", "W_up",
+                                                               "W_target", "conv_w") else v)
+                for k, v in g.items()}
+    O = ittt.forward(poisoned["H"], poisoned["X0"], poisoned["W_gate"], poisoned["W_up"],
+                     g["W_down0"], poisoned["W_target"], poisoned["conv_w"], eta, C,
+                     reuse_zv=True, z_buf=a["z_buf"], vhat_buf=a["vhat_buf"], snap_buf=snap,
+                     state_out=st)
+    ittt.stream_status()
+    assert torch.equal(snap, a["snap_buf"])
+    assert torch.equal(st, a["state_out"])
+    assert torch.equal(O, a["O"])
+
+
+@pytest.mark.parametrize("start", ["none", "bf16", "fp32", "per_state"])
+def test_state_prefix_sums_in_order(cuda_device, start):
+    """fp32 W_start + deltas[0] + ... + deltas[count-1], added in that order:
+    bit for bit what numpy's sequential fp32 adds give."""
+    R, S, d, f = 4, 3, 72, 136
+    gen = torch.Generator().manual_seed(11)
+    deltas = torch.randn(R, S, d, f, generator=gen) * torch.logspace(-3, 1, R)[:, None, None, None]
+    w = {"none": None, "bf16": torch.randn(d, f, generator=gen).bfloat16(),
+         "fp32": torch.randn(d, f, generator=gen), "per_state": torch.randn(S, d, f, generator=gen)}[start]
+    dd = deltas.to(cuda_device)
+    wd = None if w is None else w.to(cuda_device)
+    for count in range(R + 1):
+        got = ittt.state_prefix(wd, dd, count)
+        ittt.stream_status()
+        want = np.zeros((S, d, f), np.float32) if w is None else np.broadcast_to(
+            w.float().numpy(), (S, d, f)).astype(np.float32)
+        for k in range(count):
+            want = want + deltas[k].numpy()
+        assert np.array_equal(got.cpu().numpy(), want), count
+
+
+SEQ_SHARDS = [
+    # B, T, d, f, C, eta, ranks
+    (2, 512, 200, 584, 128, 0.05, 2),
+    (1, 1000, 136, 264, 128, 0.1, 3),   # 8 chunks, the last partial: spans 3, 3, 2
+    (2, 384, 64, 256, 128, 0.2, 5),     # 3 chunks over 5 ranks: two empty spans
+]
+
+
+def _emulate_ranks(g, eta, C, ranks, eta_tok=None):
+    """The sequence-sharded schedule with every rank's kernels run in turn on
+    this GPU: fold each span, take the exclusive prefixes, apply each span."""
+    from chunk_wise_weight_gb300.shard import CudaEngine, sequence_span
+    eng = CudaEngine()
+    B, T, d = g["H"].shape
+    f = g["W_gate"].shape[0]
+    spans = [sequence_span(T, C, ranks, r) for r in range(ranks)]
+    deltas = torch.zeros(ranks, B, d, f, dtype=torch.float32, device=g["H"].device)
+    keep = []
+    for r, (a, b) in enumerate(spans):
+        if b == a:
+            keep.append(None)
+            continue
+        et = None if eta_tok is None else eta_tok[:, a:b].contiguous()
+        delta, zv = eng.fold(g["H"][:, a:b].contiguous(), g["X0"][:, a:b].contiguous(),
+                             g["W_gate"], g["W_up"], g["W_target"], g["conv_w"], eta, C,
+                             eta_tok=et)
+        deltas[r].copy_(delta)
+        keep.append(zv)
+    outs = []
+    for r, (a, b) in enumerate(spans):
+        if b == a:
+            continue
+        state_in = eng.prefix(g["W_down0"], deltas, r)
+        outs.append(eng.apply(g["H"][:, a:b].contiguous(), g["X0"][:, a:b].contiguous(),
+                              g["W_gate"], g["W_up"], g["W_target"], g["conv_w"], eta, C,
+                              keep[r], state_in))
+    final = eng.prefix(g["W_down0"], deltas, ranks)
+    ittt.stream_status()
+    return torch.cat(outs, dim=1), final
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta,ranks", SEQ_SHARDS)
+def test_sequence_sharded_matches_oracle(cuda_device, B, T, d, f, C, eta, ranks):
+    inp = make_inputs(B, T, d, f, seed=1830 + T)
+    rates = torch.rand(B, T, generator=torch.Generator().manual_seed(8)) + 0.5
+    ref = oracle.forward(inp, eta, C, want_states=True, eta_tok=rates)
+    g = to_device(inp, cuda_device)
+    O, final = _emulate_ranks(g, eta, C, ranks, eta_tok=rates.to(cuda_device))
+    assert_parity(host(O), ref["O"], f"O over {ranks} spans")
+    assert_parity(host(final), ref["states"][:, -1], "state after the last span")
+
+
+def test_sequence_parallel_forward_single_rank(cuda_device):
+    """With no process group the sharded entry runs the whole sequence."""
+    from chunk_wise_weight_gb300.shard import sequence_parallel_forward
+    B, T, d, f, C, eta = 2, 512, 200, 584, 128, 0.05
+    inp = make_inputs(B, T, d, f, seed=1840)
+    ref = oracle.forward(inp, eta, C, want_states=True)
+    g = to_device(inp, cuda_device)
+    O, st = sequence_parallel_forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"],
+                                      g["W_target"], g["conv_w"], eta, C, want_state=True)
+    ittt.stream_status()
+    assert_parity(host(O), ref["O"], "O")
+    assert_parity(host(st), ref["states"][:, -1], "final state")
+
+
+def test_sequence_sharded_full_size(cuda_device):
+    """The 2 x 32k-token workload (d 2560, d_ff 9728, chunks of 2048) split
+    into 4 spans of 4 chunks: the same output as the unsharded call up to
+    the bf16 rounding of the snapshots (the deltas are summed in another
+    order), and sampled states against the oracle."""
+    cfg, inp = config_inputs(2)
+    B, T, d, f, C, eta = cfg["B"], cfg["T"], cfg["d"], cfg["f"], cfg["C"], cfg["eta"]
+    g = to_device(inp, cuda_device)
+    whole = run(g, eta, C, want_state=True)
+    O, final = _emulate_ranks(g, eta, C, 4)
+    assert_parity(host(O), host(whole["O"]), "O, 4 spans vs one call")
+    assert_parity(host(final), host(whole["state_out"]), "final state, 4 spans vs one call")
+    rng = np.random.default_rng(1850)
+    m, j = rng.integers(0, d, 12), rng.integers(0, f, 12)
+    ws = oracle.state_entries(inp["H"][0], inp["X0"][0], inp["W_gate"], inp["W_up"],
+                              inp["W_down0"], inp["W_target"], inp["conv_w"], eta, C, m, j)
+    got = host(final[0][torch.as_tensor(m), torch.as_tensor(j)])
+    assert_parity(got, ws[:, -1], "final state entries vs the oracle")

@@ -62,3 +62,98 @@ def test_two_gloo_ranks_reproduce_the_batch(tmp_path):
 
 def test_max_over_ranks_without_group():
     assert max_over_ranks(3.5) == 3.5
+
+
+# --------------------------------------------------------------------------
+# Sequence sharding: spans of whole chunks, fold, all-gather, prefix, apply
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,chunk,world", [(10, 3, 4), (4, 2, 3), (64, 16, 2), (70, 16, 3),
+                                           (5, 8, 2), (96, 16, 6)])
+def test_sequence_spans_are_whole_chunks(T, chunk, world):
+    from chunk_wise_weight_gb300.shard import sequence_span
+    spans = [sequence_span(T, chunk, world, r) for r in range(world)]
+    assert spans[0][0] == 0 and spans[-1][1] == T
+    for (a, b), (c, _) in zip(spans, spans[1:]):
+        assert b == c                                   # contiguous, in rank order
+    nonempty = [(a, b) for a, b in spans if b > a]
+    for a, b in nonempty:
+        assert a % chunk == 0
+    for a, b in nonempty[:-1]:
+        assert (b - a) % chunk == 0                     # only the last may end mid-chunk
+    n = -(-T // chunk)
+    assert len(nonempty) == min(n, world)
+
+
+class OracleEngine:
+    """The three per-rank steps evaluated by the fp64 oracle (stands in for
+    the GPU kernels on CPU ranks)."""
+
+    def __init__(self, pad_mode=0):
+        import oracle
+        self.oracle = oracle
+
+    def _span(self, H, X0, Wg, Wu, W0, Wt, cw):
+        return dict(H=H, X0=X0, W_gate=Wg, W_up=Wu, W_down0=W0, W_target=Wt, conv_w=cw)
+
+    def fold(self, H, X0, Wg, Wu, Wt, cw, eta, chunk, eta_tok=None):
+        d, f = H.shape[2], Wg.shape[0]
+        zero = torch.zeros(d, f)
+        ref = self.oracle.forward(self._span(H, X0, Wg, Wu, zero, Wt, cw), eta, chunk,
+                                  want_states=True, eta_tok=eta_tok)
+        # what the kernels keep between the passes (Z and eta * Vhat) the
+        # oracle recomputes: it keeps the span's per-token rates
+        return torch.from_numpy(ref["states"][:, -1]), eta_tok
+
+    def zeros(self, B, d, f, device):
+        return torch.zeros(B, d, f, dtype=torch.float64)
+
+    def prefix(self, W0, deltas, count):
+        return W0.double() + deltas[:count].sum(0)
+
+    def apply(self, H, X0, Wg, Wu, Wt, cw, eta, chunk, zv, state_in, out=None):
+        return torch.from_numpy(self.oracle.forward(
+            self._span(H, X0, Wg, Wu, state_in.float(), Wt, cw), eta, chunk, eta_tok=zv)["O"])
+
+
+def _seq_worker(rank, world, port, result_dir, T, chunk):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from chunk_wise_weight_gb300 import make_inputs
+        from chunk_wise_weight_gb300.shard import sequence_parallel_forward, sequence_span
+        B, d, f, eta = 2, 6, 10, 0.3
+        inp = make_inputs(B, T, d, f, seed=91)
+        rates = torch.rand(B, T, generator=torch.Generator().manual_seed(5)) + 0.5
+        a, b = sequence_span(T, chunk, world, rank)
+        O, state = sequence_parallel_forward(
+            inp["H"][:, a:b], inp["X0"][:, a:b], inp["W_gate"], inp["W_up"], inp["W_down0"],
+            inp["W_target"], inp["conv_w"], eta, chunk, eta_tok=rates[:, a:b],
+            engine=OracleEngine(), want_state=True)
+        np.save(os.path.join(result_dir, f"O{rank}.npy"), O.double().numpy())
+        np.save(os.path.join(result_dir, f"S{rank}.npy"), state.double().numpy())
+        if rank == 0:
+            import oracle
+            ref = oracle.forward(inp, eta, chunk, want_states=True, eta_tok=rates)
+            np.save(os.path.join(result_dir, "full.npy"), ref["O"])
+            np.save(os.path.join(result_dir, "final.npy"), ref["states"][:, -1])
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,T,chunk", [(2, 24, 4), (3, 26, 4), (3, 8, 4)])
+def test_gloo_ranks_shard_one_sequence(tmp_path, world, T, chunk):
+    """Each rank folds its span, the deltas are all-gathered, each rank
+    applies from the exclusive prefix: the spans' outputs concatenated equal
+    the unsharded sequence, and the last rank's state is the final state.
+    (26 tokens in chunks of 4 leave a partial last chunk; 8 tokens over
+    three ranks leave the third with nothing.)"""
+    mp.spawn(_seq_worker, args=(world, _free_port(), str(tmp_path), T, chunk), nprocs=world,
+             join=True)
+    O = np.concatenate([np.load(tmp_path / f"O{r}.npy") for r in range(world)], axis=1)
+    full = np.load(tmp_path / "full.npy")
+    assert O.shape == full.shape
+    # the oracle takes fp32 starting states: agreement to fp32 rounding
+    np.testing.assert_allclose(O, full, rtol=1e-5, atol=1e-5 * np.abs(full).max())
+    np.testing.assert_allclose(np.load(tmp_path / f"S{world - 1}.npy"),
+                               np.load(tmp_path / "final.npy"), rtol=1e-5, atol=1e-6)
