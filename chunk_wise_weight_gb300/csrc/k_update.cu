@@ -302,13 +302,14 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
 //   epilogue store S_{i+1} in place of S_i (a unit reads its block before it
 //            writes it, and no other unit touches that block) and its row
 //            sums of squares per 512-column unit into partial[(i+1) & 1].
-// S is kept tiled: 16 KB tiles of 128 rows x 32 fp32 columns, each laid out
-// exactly as a 128-byte-swizzled staging tile (row r at r * 128 bytes, its
-// 16-byte chunk c at position c ^ (r & 7)).  The epilogue writes a tile
-// with one contiguous bulk copy from shared memory and the preload of a
-// warp reads 4 KB of consecutive rows, so the state's round trip through
-// HBM runs in long contiguous bursts instead of 256-byte pieces of
-// 38 KB-strided rows.
+// S is kept tiled: 16 KB tiles of 128 rows x 32 fp32 columns, chunk-major:
+// 16-byte chunk c (columns 4c..4c+3) of row r at byte (c * 128 + r) * 16.
+// The epilogue writes a tile with one contiguous bulk copy from a staging
+// buffer of the same layout (a warp's 32 rows of one chunk are 512
+// consecutive bytes, so its shared-memory stores are conflict-free), and a
+// warp of the preload reads one chunk of its 32 rows as 512 consecutive
+// bytes of the tile (coalesced), so the state's round trip through HBM runs
+// in long contiguous bursts.
 // A final kernel normalises the last state into the last snapshot or into
 // state_out.
 // ----------------------------------------------------------------------------
@@ -349,6 +350,7 @@ struct NormUpdateParams {
 };
 
 // First fp32 of S's tile (document, 128-row block, 32-column block).
+// Chunk c of row r of a tile: float4 index c * kBM + r.
 __device__ __forceinline__ float* state_tile(float* state, int ncb, int mt_all, int doc, int mt,
                                              int cb) {
   return state + ((size_t(doc) * mt_all + mt) * ncb + cb) * size_t(kBM * 32);
@@ -438,12 +440,12 @@ struct NormUpdateSched : SchedDefaults {
       for (int t = 0; t < 2; ++t) {
         const int col0 = n0 + c + 32 * t;
         const bool tile_ok = col0 < p.f;
-        const float* trowp =
-            state_tile(p.state, p.ncb, p.mt, doc, m0 / kBM, tile_ok ? col0 / 32 : 0) + row * 32;
+        const float4* tile = reinterpret_cast<const float4*>(
+            state_tile(p.state, p.ncb, p.mt, doc, m0 / kBM, tile_ok ? col0 / 32 : 0));
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (tile_ok) v = __ldcg(reinterpret_cast<const float4*>(trowp) + (q ^ (row & 7)));
+          if (tile_ok) v = __ldcg(tile + q * kBM + row);
           w[32 * t + 4 * q] = v.x;
           w[32 * t + 4 * q + 1] = v.y;
           w[32 * t + 4 * q + 2] = v.z;
@@ -486,8 +488,9 @@ struct NormUpdateSched : SchedDefaults {
       if (n0 + c < p.f) {  // the same for every epilogue thread
         uint8_t* buf = st.acquire();
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st.put(buf, q, make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+        for (int q = 0; q < 8; ++q)  // chunk-major, as the tile is in HBM
+          *reinterpret_cast<uint4*>(buf + (q * kBM + row) * 16) =
+              make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         st.commit(buf, [&](uint8_t* src) {
           bulk_store(state_tile(p.state, p.ncb, p.mt, doc, m0 / kBM, (n0 + c) / 32), src,
                      kStagingTileBytes);
@@ -537,10 +540,11 @@ __global__ void __launch_bounds__(256)
   const int r = m % kBM;
   for (int c = threadIdx.x * 8; c < f; c += blockDim.x * 8) {
     // chunks c/4 and c/4 + 1 of row r in the tile of column block c / 32
-    const float* tile = state_tile(const_cast<float*>(state), ncb, mt_all, doc, m / kBM, c / 32);
+    const float4* tile = reinterpret_cast<const float4*>(
+        state_tile(const_cast<float*>(state), ncb, mt_all, doc, m / kBM, c / 32));
     const int q = (c % 32) / 4;
-    const float4 lo = reinterpret_cast<const float4*>(tile + r * 32)[q ^ (r & 7)];
-    const float4 hi = reinterpret_cast<const float4*>(tile + r * 32)[(q + 1) ^ (r & 7)];
+    const float4 lo = tile[q * kBM + r];
+    const float4 hi = tile[(q + 1) * kBM + r];
     const float w[8] = {lo.x * scale, lo.y * scale, lo.z * scale, lo.w * scale,
                         hi.x * scale, hi.y * scale, hi.z * scale, hi.w * scale};
     if (final_update) {
