@@ -790,6 +790,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
       na.partial = reinterpret_cast<float*>(ws + L.partial);
       na.snap = snap;
       na.state_out = ua.state_out;
+      na.allow_pairs = !P.ragged_walk && !single && d % 256 == 0;
       ITTT_STEP(ittt::launch_norm_update(env, tm_vmn, tm_zmn, tm_ss, na),
                 "normalised update launch");
     } else {

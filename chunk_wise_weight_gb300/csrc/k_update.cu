@@ -346,7 +346,9 @@ struct NormUpdateParams {
   const int* upd_docs;   // updating documents, most updates first; nullptr: all
   int n_active;          // documents with an update at chunk i
   int i;                 // the chunk this launch updates with
-  int d, f, mt, np, ncb;  // ncb: 32-column tiles per row block
+  int d, f, mt, np, ncb;  // mt: row blocks of a unit (128 rows, 256 on CTA pairs);
+                          // ncb: 32-column tiles per 128-row block
+  int mtb;                // 128-row blocks of the state (its tile layout)
 };
 
 // First fp32 of S's tile (document, 128-row block, 32-column block).
@@ -356,19 +358,25 @@ __device__ __forceinline__ float* state_tile(float* state, int ncb, int mt_all, 
   return state + ((size_t(doc) * mt_all + mt) * ncb + cb) * size_t(kBM * 32);
 }
 
-struct NormUpdateSched : SchedDefaults {
+// On CTA pairs (kPair; every chunk a multiple of 64 tokens and d a multiple
+// of 256) a unit's row block is 256 rows: each CTA loads its 128 rows of
+// eta*Vhat^T and 128 of each half's Z columns, and preloads, stores and sums
+// the state of its own 128 rows.
+template <bool kPair>
+struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
   using Params = NormUpdateParams;
-  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, true, true);
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kPair ? 2 * kBM : kBM, kBN, true, true);
   static constexpr bool kPreload = true;
-  static constexpr bool kRaggedK = true;
+  static constexpr bool kRaggedK = !kPair;
   static constexpr bool kStagedStores = true;
   static constexpr bool kStagedPreload = true;
 
   const Params& p;
+  const int rank;
   int doc = 0, tok = 0, clen = 0, slot = 0, m0 = 0, nbase = 0, npi = 0, halves = 1;
   mutable float ss_carry = 0.f;  // this thread's row sum of squares over the unit's halves
 
-  __device__ explicit NormUpdateSched(const Params& pp) : p(pp) {}
+  __device__ explicit NormUpdateSchedT(const Params& pp, uint32_t r = 0) : p(pp), rank(int(r)) {}
   __device__ int num_units() const { return p.n_active * p.mt * p.np; }
   __device__ void begin_unit(int u, int) {
     const int mt = u % p.mt;
@@ -379,7 +387,7 @@ struct NormUpdateSched : SchedDefaults {
     tok = p.docs.start(doc) + p.i * p.docs.C;
     clen = min(p.docs.C, p.docs.len(doc) - p.i * p.docs.C);
     slot = p.docs.first_chunk(doc) + p.i;
-    m0 = mt * kBM;
+    m0 = kPair ? mt * (2 * kBM) + rank * kBM : mt * kBM;
     npi = np;
     nbase = np * (2 * kBN);
     halves = (nbase + kBN < p.f) ? 2 : 1;
@@ -392,6 +400,16 @@ struct NormUpdateSched : SchedDefaults {
   __device__ bool seg_fresh(int) const { return false; }
   __device__ void load(int s, int kb, uint8_t* stage, uint64_t* bar) const {
     load_update_stage(p.tm_v, p.tm_z, stage, bar, m0, nbase + s * kBN, tok + kb * kBK);
+  }
+  // CTA pairs: this CTA's 128 rows of eta*Vhat^T and its 128 of the half's
+  // Z columns (two 64-wide boxes each).
+  __device__ void load(int s, int kb, uint8_t* stage, uint32_t bar) const {
+    const int t = tok + kb * kBK;
+    const int n0 = nbase + s * kBN + rank * kBM;
+    tma_load_2d_pair(stage, &p.tm_v, bar, m0, t);
+    tma_load_2d_pair(stage + kMnBoxBytes, &p.tm_v, bar, m0 + 64, t);
+    tma_load_2d_pair(stage + kPairATileBytes, &p.tm_z, bar, n0, t);
+    tma_load_2d_pair(stage + kPairATileBytes + kMnBoxBytes, &p.tm_z, bar, n0 + 64, t);
   }
   __device__ void clear_k(uint8_t* stage, int from, int to) const {
     clear_token_lines(stage, from, to);
@@ -441,7 +459,7 @@ struct NormUpdateSched : SchedDefaults {
         const int col0 = n0 + c + 32 * t;
         const bool tile_ok = col0 < p.f;
         const float4* tile = reinterpret_cast<const float4*>(
-            state_tile(p.state, p.ncb, p.mt, doc, m0 / kBM, tile_ok ? col0 / 32 : 0));
+            state_tile(p.state, p.ncb, p.mtb, doc, m0 / kBM, tile_ok ? col0 / 32 : 0));
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -492,7 +510,7 @@ struct NormUpdateSched : SchedDefaults {
           *reinterpret_cast<uint4*>(buf + (q * kBM + row) * 16) =
               make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         st.commit(buf, [&](uint8_t* src) {
-          bulk_store(state_tile(p.state, p.ncb, p.mt, doc, m0 / kBM, (n0 + c) / 32), src,
+          bulk_store(state_tile(p.state, p.ncb, p.mtb, doc, m0 / kBM, (n0 + c) / 32), src,
                      kStagingTileBytes);
         });
       }
@@ -511,9 +529,17 @@ struct NormUpdateSched : SchedDefaults {
   }
 };
 
+using NormUpdateSched = NormUpdateSchedT<false>;
+using NormUpdatePairSched = NormUpdateSchedT<true>;
+
 __global__ void __launch_bounds__(PipeShape<NormUpdateSched>::kThreads, 1)
     norm_update_kernel(const __grid_constant__ NormUpdateParams p, unsigned int* status) {
   run_pipeline<NormUpdateSched>(p, status);
+}
+
+__global__ void __launch_bounds__(kBaseThreads, 1)
+    norm_update_pair_kernel(const __grid_constant__ NormUpdateParams p, unsigned int* status) {
+  run_pipeline_pair<NormUpdatePairSched>(p, status);
 }
 
 // The last state of each updating document, normalised: into state_out
@@ -718,22 +744,44 @@ cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
   p.upd_docs = a.upd_docs;
   p.d = a.d;
   p.f = a.f;
-  p.mt = (a.d + kBM - 1) / kBM;
+  p.mtb = (a.d + kBM - 1) / kBM;
   p.np = (a.f + 2 * kBN - 1) / (2 * kBN);
   p.ncb = (a.f + 31) / 32;
-  cudaError_t e = cudaFuncSetAttribute(norm_update_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(pipe_smem_bytes<NormUpdateSched>()));
-  if (e != cudaSuccess) return e;
+  // CTA pairs where allowed and two can be resident: each SM then reads a
+  // third less operand data per FLOP.
+  static std::atomic<int> resident{-1};
+  const size_t psmem = pair_smem_bytes<NormUpdatePairSched>();
+  int pairs = 0;
+  cudaError_t e = cudaSuccess;
+  if (a.allow_pairs) {
+    if ((e = cudaFuncSetAttribute(norm_update_pair_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(psmem))) !=
+        cudaSuccess)
+      return e;
+    if ((e = max_pairs(reinterpret_cast<const void*>(norm_update_pair_kernel), psmem, env, &pairs,
+                       &resident)) != cudaSuccess)
+      return e;
+  }
+  const bool use_pairs = pairs >= 1;
+  p.mt = use_pairs ? (a.d + 2 * kBM - 1) / (2 * kBM) : p.mtb;
+  if (!use_pairs &&
+      (e = cudaFuncSetAttribute(norm_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(pipe_smem_bytes<NormUpdateSched>()))) != cudaSuccess)
+    return e;
   for (int i = 0; i < a.n_steps; ++i) {
     p.i = i;
     p.n_active = a.active[i];
     const int64_t units = int64_t(p.n_active) * p.mt * p.np;
     if (units == 0) continue;
-    const int grid = units < env.num_sms ? int(units) : env.num_sms;
-    norm_update_kernel<<<grid, PipeShape<NormUpdateSched>::kThreads,
-                         pipe_smem_bytes<NormUpdateSched>(), env.stream>>>(p, env.status);
-    e = cudaGetLastError();
+    if (use_pairs) {
+      e = launch_on_pairs(reinterpret_cast<const void*>(norm_update_pair_kernel),
+                          int(units < pairs ? units : pairs), psmem, env, &p);
+    } else {
+      const int grid = units < env.num_sms ? int(units) : env.num_sms;
+      norm_update_kernel<<<grid, PipeShape<NormUpdateSched>::kThreads,
+                           pipe_smem_bytes<NormUpdateSched>(), env.stream>>>(p, env.status);
+      e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
   }
   const dim3 fin(unsigned(a.d), unsigned(a.n_udocs));

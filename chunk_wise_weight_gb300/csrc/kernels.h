@@ -181,12 +181,14 @@ struct NormUpdateArgs {
   float* partial;       // scratch [2][documents][ceil(f/512)][d] fp32
   __nv_bfloat16* snap;  // [slots, d, f]: slots 1..n-1 of each document written
   float* state_out;     // [documents, d, f] fp32 or nullptr
+  bool allow_pairs;     // every updated chunk a multiple of 64 tokens and d of 256
 };
 
 // The fast-weight walk with L2 normalisation of every updated state, rows
 // over d_ff (one launch per chunk, then one finalising launch).  Tensor maps:
 // eta*Vhat and Z as for launch_update; the snapshots as [slots][d][f] with
-// box {64,128,1} for TMA stores.
+// box {64,128,1} for TMA stores.  Runs on CTA pairs when allowed and two can
+// be resident, else on single CTAs.
 cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
                                const CUtensorMap& tm_z, const CUtensorMap& tm_snap_store,
                                const NormUpdateArgs& a);

@@ -228,7 +228,11 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
       if constexpr (S::kPreload) {
         for (int h = 0; h < sched.unit_accs(); ++h) {
           if (!preloaded[h]) {
-            sched.preload(h, row, tlane + uint32_t(h * kBN));
+            if constexpr (S::kStagedPreload) {
+              sched.preload(h, row, tlane + uint32_t(h * kBN), stager);
+            } else {
+              sched.preload(h, row, tlane + uint32_t(h * kBN));
+            }
             tmem_wait_st();
             tc_fence_before_sync();
             mbar_arrive_cluster(acc_empty_leader[h]);
@@ -265,7 +269,11 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
           if (!release && un < nunits) {
             next.begin_unit(un, local + 1);
             if (h < next.unit_accs()) {
-              next.preload(h, row, trow);
+              if constexpr (S::kStagedPreload) {
+                next.preload(h, row, trow, stager);
+              } else {
+                next.preload(h, row, trow);
+              }
               tmem_wait_st();
               tc_fence_before_sync();
               mbar_arrive_cluster(acc_empty_leader[h]);

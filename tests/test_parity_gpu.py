@@ -395,6 +395,29 @@ L2 = [
 ]
 
 
+L2_PAIRS = [
+    # d a multiple of 256 and every chunk a multiple of 64 tokens: the walk
+    # runs on CTA pairs
+    (2, 640, 256, 584, 128, 0.05),     # odd 256-column halves, chunks 128 x 5
+    (1, 512, 512, 1000, 256, 0.02),    # two 256-row blocks, ragged d_ff
+]
+
+
+@pytest.mark.parametrize("B,T,d,f,C,eta", L2_PAIRS)
+def test_l2norm_pairs_parity_and_single_cta_bitwise(cuda_device, B, T, d, f, C, eta):
+    inp = make_inputs(B, T, d, f, seed=1150 + T + d)
+    ref = oracle.forward(inp, eta, C, want_states=True, l2norm=True)
+    g = to_device(inp, cuda_device)
+    got = run(g, eta, C, intermediates=True, want_state=True, l2norm=True)
+    n = -(-T // C)
+    assert_parity(host(got["snap_buf"]), ref["states"][:, :n], "normalised snapshots")
+    assert_parity(host(got["state_out"]), ref["states"][:, n], "normalised final state")
+    assert_parity(host(got["O"]), ref["O"], "O")
+    one = run(g, eta, C, intermediates=True, want_state=True, l2norm=True, single_cta=True)
+    for k in ("snap_buf", "state_out", "O"):
+        assert torch.equal(one[k], got[k]), k
+
+
 @pytest.mark.parametrize("B,T,d,f,C,eta", L2)
 def test_l2norm_parity(cuda_device, B, T, d, f, C, eta):
     inp = make_inputs(B, T, d, f, seed=1100 + T + d)
