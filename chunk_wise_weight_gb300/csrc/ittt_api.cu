@@ -447,7 +447,8 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   if (P->packed) L.table = take(P->table.size() * sizeof(int));
   if (P->l2norm && P->n_udocs > 0) {
     L.state = take(size_t(P->ndocs) * ((d + 127) / 128) * ((f + 31) / 32) * 128 * 32 * 4);
-    L.partial = take(size_t(2) * P->ndocs * ((f + 511) / 512) * d * 4);
+    // row partial sums per 512-column block, in two 128-column parts of its halves
+    L.partial = take(size_t(2) * P->ndocs * 2 * ((f + 511) / 512) * d * 4);
   }
   L.total = off;
   return ITTT_OK;

@@ -340,7 +340,8 @@ struct NormUpdateParams {
   int w0_fp32;
   int64_t w0_bstride;
   float* state;          // S, tiled: [documents][ceil(d/128)][ceil(f/32)] tiles of 4096 fp32
-  float* partial;        // [2][documents][np][d] row sums of squares per 512-column unit
+  float* partial;        // [2][documents][2 * np][d] row sums of squares per 512-column
+                         // unit and 128-column part of its halves
   __nv_bfloat16* snap;   // [slots, d, f]
   DocMap docs;
   const int* upd_docs;   // updating documents, most updates first; nullptr: all
@@ -349,6 +350,7 @@ struct NormUpdateParams {
   int d, f, mt, np, ncb;  // mt: row blocks of a unit (128 rows, 256 on CTA pairs);
                           // ncb: 32-column tiles per 128-row block
   int mtb;                // 128-row blocks of the state (its tile layout)
+  int nparts;             // partial sums per row: 2 * np
 };
 
 // First fp32 of S's tile (document, 128-row block, 32-column block).
@@ -361,7 +363,10 @@ __device__ __forceinline__ float* state_tile(float* state, int ncb, int mt_all, 
 // On CTA pairs (kPair; every chunk a multiple of 64 tokens and d a multiple
 // of 256) a unit's row block is 256 rows: each CTA loads its 128 rows of
 // eta*Vhat^T and 128 of each half's Z columns, and preloads, stores and sums
-// the state of its own 128 rows.
+// the state of its own 128 rows.  There two groups of four epilogue warps
+// share the work, each on 128 of every half's 256 columns (five operand
+// stages leave room for the second group's staging buffers): the preloads and
+// epilogues, not the MMAs, bound this walk.
 template <bool kPair>
 struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
   using Params = NormUpdateParams;
@@ -370,11 +375,19 @@ struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults>
   static constexpr bool kRaggedK = !kPair;
   static constexpr bool kStagedStores = true;
   static constexpr bool kStagedPreload = true;
+  static constexpr int kEpilogueGroups = kPair ? 2 : 1;
+  static constexpr int kNumStages = kPair ? 5 : 4;
+  static constexpr int kGroupCols = kBN / kEpilogueGroups;  // columns of a half per group
+  // A row's sum of squares is kept per 512-column unit in two parts (columns
+  // 0-127 and 128-255 of each half): the two epilogue groups on pairs each
+  // own one part, a single CTA sums both in the same order, so both walks
+  // round alike.
+  static constexpr int kPartCols = 128;
 
   const Params& p;
   const int rank;
   int doc = 0, tok = 0, clen = 0, slot = 0, m0 = 0, nbase = 0, npi = 0, halves = 1;
-  mutable float ss_carry = 0.f;  // this thread's row sum of squares over the unit's halves
+  mutable float ss_carry[2] = {0.f, 0.f};  // this row's sums of squares per part, over halves
 
   __device__ explicit NormUpdateSchedT(const Params& pp, uint32_t r = 0) : p(pp), rank(int(r)) {}
   __device__ int num_units() const { return p.n_active * p.mt * p.np; }
@@ -418,7 +431,7 @@ struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults>
   static __device__ uint64_t b_desc(uint32_t base, int k) { return mn_desc(base, k); }
 
   __device__ size_t partial_at(int par, int blk, int m) const {
-    return ((size_t(par) * p.docs.ndocs + doc) * p.np + blk) * size_t(p.d) + m;
+    return ((size_t(par) * p.docs.ndocs + doc) * p.nparts + blk) * size_t(p.d) + m;
   }
 
   // W_i of this half into its accumulator, and out as snapshot slot i
@@ -428,11 +441,12 @@ struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults>
     const int m = m0 + row;
     const bool row_ok = m < p.d;
     const int n0 = nbase + h * kBN;
+    const int c_begin = st.group * kGroupCols, c_end = c_begin + kGroupCols;
     if (p.i == 0) {
       const size_t off =
           size_t(doc) * size_t(p.w0_bstride) + size_t(row_ok ? m : 0) * size_t(p.f);
 #pragma unroll 1
-      for (int c = 0; c < kBN; c += 32) {
+      for (int c = c_begin; c < c_end; c += 32) {
         uint32_t v[32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -447,12 +461,12 @@ struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults>
       return;
     }
     const float scale =
-        row_ok ? row_scale_of(sum_partials(p.partial + partial_at(p.i & 1, 0, m), p.d, p.np))
+        row_ok ? row_scale_of(sum_partials(p.partial + partial_at(p.i & 1, 0, m), p.d, p.nparts))
                : 0.f;
     // 64 columns (two tiles) per step: sixteen independent 16-byte loads of
     // this row's two 128-byte tile rows.
 #pragma unroll 1
-    for (int c = 0; c < kBN; c += 64) {
+    for (int c = c_begin; c < c_end; c += 64) {
       float w[64];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
@@ -496,9 +510,10 @@ struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults>
     const int m = m0 + row;
     const bool row_ok = m < p.d;
     const int n0 = nbase + s * kBN;
-    float ss = s == 0 ? 0.f : ss_carry;
+    const int c_begin = st.group * kGroupCols, c_end = c_begin + kGroupCols;
+    float ss0 = s == 0 ? 0.f : ss_carry[0], ss1 = s == 0 ? 0.f : ss_carry[1];
 #pragma unroll 1
-    for (int c = 0; c < kBN; c += 32) {
+    for (int c = c_begin; c < c_end; c += 32) {
       uint32_t v[32];
       tmem_ld_32cols(trow + uint32_t(c), v);
       tmem_wait_ld();
@@ -515,17 +530,24 @@ struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults>
         });
       }
       if (row_ok) {
+        const bool first = c < kPartCols;
+        float a = first ? ss0 : ss1;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if (n0 + c + j < p.f) {
             const float x = __uint_as_float(v[j]);
-            ss = fmaf(x, x, ss);
+            a = fmaf(x, x, a);
           }
         }
+        if (first) ss0 = a; else ss1 = a;
       }
     }
-    ss_carry = ss;
-    if (row_ok && s == halves - 1) __stcg(p.partial + partial_at((p.i + 1) & 1, npi, m), ss);
+    ss_carry[0] = ss0;
+    ss_carry[1] = ss1;
+    if (row_ok && s == halves - 1) {
+      if (c_begin < kPartCols) __stcg(p.partial + partial_at((p.i + 1) & 1, npi * 2, m), ss0);
+      if (c_end > kPartCols) __stcg(p.partial + partial_at((p.i + 1) & 1, npi * 2 + 1, m), ss1);
+    }
   }
 };
 
@@ -537,7 +559,7 @@ __global__ void __launch_bounds__(PipeShape<NormUpdateSched>::kThreads, 1)
   run_pipeline<NormUpdateSched>(p, status);
 }
 
-__global__ void __launch_bounds__(kBaseThreads, 1)
+__global__ void __launch_bounds__(pair_threads<NormUpdatePairSched>(), 1)
     norm_update_pair_kernel(const __grid_constant__ NormUpdateParams p, unsigned int* status) {
   run_pipeline_pair<NormUpdatePairSched>(p, status);
 }
@@ -549,7 +571,7 @@ __global__ void __launch_bounds__(256)
     norm_finalize_kernel(const float* __restrict__ state, const float* __restrict__ partial,
                          __nv_bfloat16* __restrict__ snap, float* __restrict__ state_out,
                          DocMap docs, const int* __restrict__ upd_docs, int final_update, int d,
-                         int f, int np) {
+                         int f, int nparts) {
   __shared__ float row_scale;
   const int m = blockIdx.x;
   const int doc = upd_docs ? __ldg(upd_docs + blockIdx.y) : int(blockIdx.y);
@@ -557,7 +579,8 @@ __global__ void __launch_bounds__(256)
   const int j = final_update ? nch : nch - 1;  // state index after the last update
   if (threadIdx.x == 0)
     row_scale = row_scale_of(
-        sum_partials(partial + (size_t(j & 1) * docs.ndocs + doc) * np * size_t(d) + m, d, np));
+        sum_partials(partial + (size_t(j & 1) * docs.ndocs + doc) * nparts * size_t(d) + m, d,
+                     nparts));
   __syncthreads();
   const float scale = row_scale;
   const size_t row = (size_t(doc) * d + m) * size_t(f);
@@ -759,11 +782,12 @@ cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
         cudaSuccess)
       return e;
     if ((e = max_pairs(reinterpret_cast<const void*>(norm_update_pair_kernel), psmem, env, &pairs,
-                       &resident)) != cudaSuccess)
+                       &resident, pair_threads<NormUpdatePairSched>())) != cudaSuccess)
       return e;
   }
   const bool use_pairs = pairs >= 1;
   p.mt = use_pairs ? (a.d + 2 * kBM - 1) / (2 * kBM) : p.mtb;
+  p.nparts = 2 * p.np;
   if (!use_pairs &&
       (e = cudaFuncSetAttribute(norm_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 int(pipe_smem_bytes<NormUpdateSched>()))) != cudaSuccess)
@@ -775,7 +799,8 @@ cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
     if (units == 0) continue;
     if (use_pairs) {
       e = launch_on_pairs(reinterpret_cast<const void*>(norm_update_pair_kernel),
-                          int(units < pairs ? units : pairs), psmem, env, &p);
+                          int(units < pairs ? units : pairs), psmem, env, &p,
+                          pair_threads<NormUpdatePairSched>());
     } else {
       const int grid = units < env.num_sms ? int(units) : env.num_sms;
       norm_update_kernel<<<grid, PipeShape<NormUpdateSched>::kThreads,
@@ -787,7 +812,7 @@ cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
   const dim3 fin(unsigned(a.d), unsigned(a.n_udocs));
   norm_finalize_kernel<<<fin, 256, 0, env.stream>>>(a.state, a.partial, a.snap, a.state_out,
                                                     a.docs, a.upd_docs, a.state_out ? 1 : 0,
-                                                    a.d, a.f, p.np);
+                                                    a.d, a.f, p.nparts);
   return cudaGetLastError();
 }
 

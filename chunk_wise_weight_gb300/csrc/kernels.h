@@ -178,7 +178,7 @@ struct NormUpdateArgs {
   bool w0_fp32;
   int64_t w0_bstride;
   float* state;         // scratch: documents x ceil(d/128) x ceil(f/32) tiles of 16 KB
-  float* partial;       // scratch [2][documents][ceil(f/512)][d] fp32
+  float* partial;       // scratch [2][documents][2 * ceil(f/512)][d] fp32
   __nv_bfloat16* snap;  // [slots, d, f]: slots 1..n-1 of each document written
   float* state_out;     // [documents, d, f] fp32 or nullptr
   bool allow_pairs;     // every updated chunk a multiple of 64 tokens and d of 256

@@ -74,16 +74,19 @@ constexpr uint32_t kStagingBytes = 2 * kStagingTileBytes;
 // through shared memory: every thread fills its row (8 x 16 bytes, 128-byte
 // swizzle), then one thread issues the TMA store.  Two staging buffers
 // alternate; a buffer is refilled only after the store that read it two
-// tiles ago has finished reading shared memory.
+// tiles ago has finished reading shared memory.  With two epilogue groups
+// (kEpilogueGroups) each group has its own pair of buffers and its own
+// named barrier.
 struct EpiStager {
   uint8_t* buf;
   int tid;  // 0..127 = tile row
   uint32_t issued;
+  int group = 0;  // epilogue group (named barrier 1 + group)
 
-  // Next buffer to fill (every epilogue thread must call this).
+  // Next buffer to fill (every thread of the group must call this).
   __device__ __forceinline__ uint8_t* acquire() {
     if (tid == 0 && issued >= 2) bulk_wait_group_read<1>();
-    epilogue_bar();
+    epilogue_group_bar(group);
     return buf + (issued & 1u) * kStagingTileBytes;
   }
   // Writes 16-byte chunk c (0..7) of this thread's row.
@@ -94,7 +97,7 @@ struct EpiStager {
   template <class F>
   __device__ __forceinline__ void commit(uint8_t* b, F&& store) {
     fence_proxy_async_smem();
-    epilogue_bar();
+    epilogue_group_bar(group);
     if (tid == 0) {
       store(b);
       bulk_commit_group();
@@ -131,6 +134,10 @@ struct SchedDefaults {
   //   int  k_valid(int s, int kb)                       1..64
   //   void clear_k(uint8_t* stage, int from, int to)    (generic stores)
   static constexpr bool kRaggedK = false;
+  // Groups of four epilogue warps (CTA-pair pipeline only): each group runs
+  // the epilogue and preload on the same accumulator lanes, on its share of
+  // the columns (EpiStager::group tells the schedule which).
+  static constexpr int kEpilogueGroups = 1;
   // Transaction bytes the producer's copies deliver into a stage.
   __device__ uint32_t tma_bytes(int, int) const { return kStageBytes; }
 };
@@ -139,6 +146,7 @@ template <class S>
 struct PipeShape {
   static_assert(S::kNumStages >= 2 && S::kNumStages <= kMaxStages, "stage count");
   static_assert((kStageBytes + S::kExtraStageBytes) % 1024 == 0, "stages stay 1 KiB aligned");
+  static_assert(S::kEpilogueGroups == 1, "one epilogue group on single CTAs");
   static constexpr uint32_t kStageStride = kStageBytes + S::kExtraStageBytes;
   static constexpr int kThreads = kBaseThreads + 32 * S::kBuilderWarps;
 };
@@ -157,7 +165,7 @@ struct __align__(8) PipeSync {
 
 template <class S>
 __host__ __device__ constexpr size_t pipe_staging_bytes() {
-  return S::kStagedStores ? kStagingBytes : 0;
+  return S::kStagedStores ? kStagingBytes * S::kEpilogueGroups : 0;
 }
 
 template <class S>

@@ -16,7 +16,8 @@
 //   warp 1         : TMEM allocation for the pair; in the leader, lane 0
 //                    issues the pair MMAs and commits them to the barriers
 //                    of both CTAs (multicast).
-//   warps 2..5     : epilogue on this CTA's accumulator rows; a release
+//   warps 2..5     : epilogue on this CTA's accumulator rows (with two epilogue
+//   (and 6..9)       groups, each group on its share of the columns); a release
 //                    arrives on the leader's acc_empty barrier.
 // Both CTAs walk the same units in the same order.  Every wait is bounded
 // (kWaitLimitNs); a CTA that gives up records kStatusTimeout and unwinds,
@@ -53,6 +54,13 @@ struct PairDefaults : SchedDefaults {
   static constexpr int kNumStages = 6;
 };
 
+// Threads of a CTA: producer, MMA and one or two groups of epilogue warps.
+template <class S>
+__host__ __device__ constexpr int pair_threads() {
+  static_assert(S::kEpilogueGroups == 1 || S::kEpilogueGroups == 2, "epilogue groups");
+  return kBaseThreads + kEpilogueThreads * (S::kEpilogueGroups - 1);
+}
+
 struct __align__(8) PairSync {
   uint64_t full[kMaxPairStages];   // leader: both CTAs' operand bytes landed
   uint64_t empty[kMaxPairStages];  // both: the pair MMAs reading the stage are done
@@ -61,7 +69,7 @@ struct __align__(8) PairSync {
   uint64_t drain;                  // leader: every pair MMA is done
   uint32_t tmem_base;
   int abort_flag;
-  int vote[4];
+  int vote[8];                     // epilogue warps' go/unwind votes, four per group
 };
 
 template <class S>
@@ -96,7 +104,7 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&sync->acc_full[h], 1);
-      mbar_init(&sync->acc_empty[h], 2 * kEpilogueThreads);
+      mbar_init(&sync->acc_empty[h], 2 * kEpilogueThreads * S::kEpilogueGroups);
     }
     mbar_init(&sync->drain, 1);
     sync->abort_flag = 0;
@@ -207,13 +215,14 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
       const int zero = 0;
       if (!mbar_wait(&sync->drain, 0u, &zero)) atomicOr(status, kStatusTimeout);
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + 4 * S::kEpilogueGroups) {
     // ------------------------------------------------------------- epilogue
     S sched(p, rank);
     S next(p, rank);
+    const int group = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    EpiStager stager{staging, row, 0u};
+    EpiStager stager{staging + size_t(group) * kStagingBytes, row, 0u, group};
     const uint32_t tlane = tmem + (uint32_t(quad * 32) << 16);
     const uint32_t acc_empty_leader[2] = {mapa_shared(smem_u32(&sync->acc_empty[0]), 0),
                                           mapa_shared(smem_u32(&sync->acc_empty[1]), 0)};
@@ -245,10 +254,11 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
         bool got = __all_sync(0xffffffffu, mbar_wait(&sync->acc_full[h], acc_use[h] & 1u,
                                                      abort_flag));
         if constexpr (S::kStagedStores) {
-          if (lane == 0) sync->vote[quad] = got ? 1 : 0;
-          epilogue_bar();
-          got = (sync->vote[0] & sync->vote[1] & sync->vote[2] & sync->vote[3]) != 0;
-          epilogue_bar();
+          volatile int* vote = sync->vote + 4 * group;
+          if (lane == 0) vote[quad] = got ? 1 : 0;
+          epilogue_group_bar(group);
+          got = (vote[0] & vote[1] & vote[2] & vote[3]) != 0;
+          epilogue_group_bar(group);
         }
         if (!got) {
           raise_abort(abort_flag, status, kStatusTimeout);
@@ -303,11 +313,12 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
 
 // ------------------------------------------------------------------ host side
 inline cudaLaunchConfig_t pair_launch_config(int pairs, size_t smem, const LaunchEnv& env,
-                                             cudaLaunchAttribute* attr) {
+                                             cudaLaunchAttribute* attr,
+                                             int threads = kBaseThreads) {
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(unsigned(2 * pairs), 1, 1);
-  cfg.blockDim = dim3(kBaseThreads, 1, 1);
+  cfg.blockDim = dim3(unsigned(threads), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = env.stream;
   attr->id = cudaLaunchAttributeClusterDimension;
@@ -322,11 +333,11 @@ inline cudaLaunchConfig_t pair_launch_config(int pairs, size_t smem, const Launc
 // Number of CTA pairs of `kernel` that can be resident at once (0: none).
 // Asked once per kernel and device configuration, then remembered.
 inline cudaError_t max_pairs(const void* kernel, size_t smem, const LaunchEnv& env, int* out,
-                             std::atomic<int>* cache) {
+                             std::atomic<int>* cache, int threads = kBaseThreads) {
   int n = cache->load();
   if (n < 0) {
     cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = pair_launch_config(env.num_sms / 2, smem, env, &attr);
+    cudaLaunchConfig_t cfg = pair_launch_config(env.num_sms / 2, smem, env, &attr, threads);
     cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
     if (e != cudaSuccess) return e;
     cache->store(n);
@@ -337,9 +348,10 @@ inline cudaError_t max_pairs(const void* kernel, size_t smem, const LaunchEnv& e
 
 template <class P>
 inline cudaError_t launch_on_pairs(const void* kernel, int pairs, size_t smem,
-                                   const LaunchEnv& env, const P* params) {
+                                   const LaunchEnv& env, const P* params,
+                                   int threads = kBaseThreads) {
   cudaLaunchAttribute attr;
-  cudaLaunchConfig_t cfg = pair_launch_config(pairs, smem, env, &attr);
+  cudaLaunchConfig_t cfg = pair_launch_config(pairs, smem, env, &attr, threads);
   unsigned int* status = env.status;
   void* args[] = {const_cast<P*>(params), &status};
   return cudaLaunchKernelExC(&cfg, kernel, args);

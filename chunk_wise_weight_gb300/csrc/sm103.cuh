@@ -156,6 +156,11 @@ __device__ __forceinline__ void bulk_wait_group_all() {
 }
 
 // Barrier among the 128 epilogue threads only (id 1; __syncthreads uses 0).
+// Barrier among the 128 threads of epilogue group g (named barrier 1 + g).
+__device__ __forceinline__ void epilogue_group_bar(int g) {
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
+}
+
 __device__ __forceinline__ void epilogue_bar() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }

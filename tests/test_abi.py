@@ -192,7 +192,7 @@ def test_workspace_bytes_and_launch_count(lib):
     nblk = -(-f // 512)
     tiles = -(-d // 128) * -(-f // 32)      # the fp32 state in 128 x 32 tiles
     assert (ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True)
-            == want + r(B * tiles * 128 * 32 * 4) + r(2 * B * nblk * d * 4))
+            == want + r(B * tiles * 128 * 32 * 4) + r(2 * B * 2 * nblk * d * 4))
     assert ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True, dual=True) == 0
     assert ittt.launch_count(B, T, d, f, C) == 5
     assert ittt.launch_count(B, T, d, f, T) == 4
