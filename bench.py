@@ -116,6 +116,9 @@ def parse_args():
                     help="normalise every updated fast weight row by row (one launch per chunk)")
     ap.add_argument("--eta-tok", action="store_true",
                     help="per-token learning-rate weights (seeded uniform [0.5, 1.5))")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step (with a caller workspace) into a CUDA graph and time "
+                         "its replays; per-kernel phases then come from an eager pass")
     ap.add_argument("--seq-shards", type=int, default=0,
                     help="run the sequence-sharded schedule with this many spans, the spans "
                          "run in turn on this GPU (fold, exclusive prefix, apply); one rank only")
@@ -325,7 +328,25 @@ def arm_config(cfg, args, world, cu=None):
             "schedule": "dual (scores Z Z^T)" if args.dual else "primal walk",
             "eta_tok": "per-token rates" if args.eta_tok else None,
             "update_rule": "L2-normalised rows" if args.l2norm else "additive",
-            "l2": "inputs larger than L2: H+X0 and Z are several GB per step"}
+            "launch": "CUDA graph replay" if getattr(args, "graph", False) else "eager",
+            "l2": l2_note(cfg, T)}
+
+
+def l2_note(cfg, T):
+    """Whether one step's tensors outrun the 126 MB L2 (no flush is then
+    needed between timed steps): H and X0, Z, and the weight snapshots the
+    walk writes and the apply reads."""
+    B = cfg["B"] if T == cfg["T"] else 1
+    n = -(-T // cfg["C"])
+    z_bytes = B * T * cfg["f"] * 2
+    act_bytes = 2 * B * T * cfg["d"] * 2
+    snap_bytes = B * max(n - 1, 0) * cfg["d"] * cfg["f"] * 2
+    total = z_bytes + act_bytes + snap_bytes
+    if total > 2 * 126e6:
+        return (f"inputs larger than L2: H+X0 {act_bytes / 1e9:.2f} GB, Z "
+                f"{z_bytes / 1e9:.2f} GB and snapshots {snap_bytes / 1e9:.2f} GB per step")
+    return (f"small workload: {total / 1e6:.0f} MB of activations and snapshots per step, "
+            "not flushed from L2 between steps")
 
 
 def run_reference(args):
@@ -450,14 +471,35 @@ def main():
         return run_seq_shards(args, cfg, (H, X0, Wg, Wu, W0, Wt, cw), stream, dev, peaks,
                               peak_src, rates, local, cpu)
 
+    workspace = None
+    if args.graph:
+        if cu is not None:
+            raise SystemExit("--graph: packed documents stage host tables and cannot be captured")
+        ws_bytes = ittt.workspace_bytes_ex(B, T, d, f, C, fused_conv=args.fused_conv,
+                                           dual=args.dual, l2norm=args.l2norm,
+                                           eta_tok=rates)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
     def step(events=None):
         ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, stream=stream, events=events,
                      fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates, cu_seqlens=cu,
-                     l2norm=args.l2norm)
+                     l2norm=args.l2norm, workspace=workspace)
 
     for _ in range(max(3, args.warmup)):
         step()
     ittt.stream_status(stream)
+    graph = None
+    if args.graph:
+        # One step captured once; the timed loop replays it.  Capture runs on
+        # a side stream, as CUDA graph capture requires.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, fused_conv=args.fused_conv,
+                         dual=args.dual, eta_tok=rates, l2norm=args.l2norm, workspace=workspace)
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        ittt.stream_status(stream)
 
     nph = len(ittt.PHASES)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nph)]
@@ -473,11 +515,19 @@ def main():
     # stream, so the per-kernel durations come from the timed steps themselves.
     t_start.record(stream)
     for k in range(args.steps):
-        step(ev[k])
+        if graph is not None:
+            graph.replay()
+        else:
+            step(ev[k])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     barrier(dev)
+    if graph is not None:
+        # Per-kernel phases from an eager pass of the same length.
+        for k in range(args.steps):
+            step(ev[k])
+        torch.cuda.synchronize(dev)
     ittt.stream_status(stream)
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     ms_per_step = elapsed_ms / args.steps

@@ -835,3 +835,50 @@ def test_sequence_sharded_full_size(cuda_device):
                               inp["W_down0"], inp["W_target"], inp["conv_w"], eta, C, m, j)
     got = host(final[0][torch.as_tensor(m), torch.as_tensor(j)])
     assert_parity(got, ws[:, -1], "final state entries vs the oracle")
+
+
+# --------------------------------------------------------------------------
+# CUDA graphs: a forward with a caller workspace allocates nothing and
+# synchronises nothing, so it can be captured once and replayed
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", ["default", "l2norm", "fused_conv", "dual"])
+def test_forward_captured_in_cuda_graph(cuda_device, variant):
+    B, T, d, f, C, eta = 2, 512, 256, 584, 128, 0.05
+    kw = {"l2norm": variant == "l2norm", "fused_conv": variant == "fused_conv",
+          "dual": variant == "dual"}
+    g = to_device(make_inputs(B, T, d, f, seed=1900), cuda_device)
+    ws_bytes = ittt.workspace_bytes_ex(B, T, d, f, C, **kw)
+    assert ws_bytes > 0
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=cuda_device)
+    out = torch.empty(B, T, d, dtype=torch.bfloat16, device=cuda_device)
+
+    def call():
+        ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                     g["conv_w"], eta, C, out, workspace=ws, **kw)
+
+    side = torch.cuda.Stream(cuda_device)
+    side.wait_stream(torch.cuda.current_stream(cuda_device))
+    with torch.cuda.stream(side):
+        call()  # first call on the device: one-time set-up outside the capture
+    torch.cuda.current_stream(cuda_device).wait_stream(side)
+    ittt.stream_status()
+    eager = out.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    out.zero_()
+    for _ in range(3):
+        graph.replay()
+    ittt.stream_status()
+    assert torch.equal(out, eager)
+    # the graph reads the same buffers: new input values, new output
+    g["H"].copy_(torch.flip(g["H"], dims=[1]))
+    graph.replay()
+    ittt.stream_status()
+    want = torch.empty_like(out)
+    ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                 g["conv_w"], eta, C, want, workspace=ws, **kw)
+    ittt.stream_status()
+    assert torch.equal(out, want)
+    assert not torch.equal(out, eager)
