@@ -26,10 +26,13 @@
 #include <cstdio>
 #include <cstring>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <utility>
 #include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "ittt.h"
 #include "kernels.h"
@@ -40,6 +43,40 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 thread_local std::string g_last_error;
+
+// Scratch bytes one call may allocate (0: no cap); ittt_set_scratch_limit.
+std::atomic<size_t> g_scratch_limit{0};
+
+// An NVTX range for the lifetime of the object: the host side of each phase
+// shows up by name on a profiler's timeline (no cost without a tool).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// One NVTX range per phase of a forward call (opened at the phase's start
+// event, closed at its end); ranges still open when the call returns early
+// are closed then.
+struct PhaseRanges {
+  int open = 0;
+  void mark(int slot) {
+    static const char* const kNames[ITTT_NUM_PHASES] = {
+        "ittt conv", "ittt target", "ittt gate/up", "ittt snapshot 0", "ittt update",
+        "ittt apply"};
+    if (slot % 2 == 0) {
+      nvtxRangePushA(kNames[slot / 2]);
+      ++open;
+    } else if (open > 0) {
+      nvtxRangePop();
+      --open;
+    }
+  }
+  ~PhaseRanges() {
+    for (; open > 0; --open) nvtxRangePop();
+  }
+};
 
 ittt_status fail(ittt_status s, const char* fmt, ...) {
   char buf[512];
@@ -564,10 +601,15 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
       if (overlaps(writes[a], writes[b]))
         return fail(ITTT_ERR_INVALID_ARG, "two output buffers overlap");
 
+  const Layout& L = P.L;
+  const size_t cap = g_scratch_limit.load();
+  if (o.workspace == nullptr && cap != 0 && L.total > cap)
+    return fail(ITTT_ERR_OOM, "the call needs %zu bytes of scratch, over the limit of %zu",
+                L.total, cap);
+
   DeviceState* ds = nullptr;
   if ((s = device_state(&ds))) return s;
 
-  const Layout& L = P.L;
   const bool w0_is_bf16 = !o.state_in && w0_bf16;
   ScratchGuard guard;
   uint8_t* ws = nullptr;
@@ -684,7 +726,10 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   const int64_t w0_bstride = o.state_in ? d * f : 0;
 
   cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(o.events);
+  NvtxRange call_range("ittt_forward");
+  PhaseRanges ranges;
   auto rec = [&](int slot, cudaStream_t st) -> cudaError_t {
+    ranges.mark(slot);
     return ev ? cudaEventRecord(ev[slot], st) : cudaSuccess;
   };
   const float* cw = static_cast<const float*>(conv_w->data);
@@ -906,6 +951,8 @@ ittt_status ittt_state_prefix(const ittt_tensor* W_start, const ittt_tensor* del
   if (e != cudaSuccess) return cuda_fail(e, "state prefix launch");
   return ITTT_OK;
 }
+
+void ittt_set_scratch_limit(size_t bytes) { g_scratch_limit.store(bytes); }
 
 size_t ittt_workspace_bytes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk) {
   return ittt_workspace_bytes_ex(B, T, d, f, chunk, nullptr);

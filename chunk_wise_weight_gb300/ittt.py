@@ -91,6 +91,8 @@ def load(path: str | None = None):
     lib.ittt_launch_count.restype = ctypes.c_int32
     lib.ittt_state_prefix.argtypes = [_TP, _TP, ctypes.c_int32, _TP, ctypes.c_void_p]
     lib.ittt_state_prefix.restype = ctypes.c_int
+    lib.ittt_set_scratch_limit.argtypes = [ctypes.c_size_t]
+    lib.ittt_set_scratch_limit.restype = None
     _lib = lib
     return lib
 
@@ -240,6 +242,12 @@ def state_prefix(W_start, deltas: torch.Tensor, count: int, state: torch.Tensor 
     _check(lib.ittt_state_prefix(_ref(keep[0]), _ref(keep[1]), ctypes.c_int32(count),
                                  _ref(keep[2]), ctypes.c_void_p(s)))
     return state
+
+
+def set_scratch_limit(nbytes: int) -> None:
+    """ittt_set_scratch_limit: cap on the scratch one call may allocate (0:
+    none); a call over it raises IttError(ERR_OOM) before anything runs."""
+    load().ittt_set_scratch_limit(ctypes.c_size_t(int(nbytes)))
 
 
 def stream_status(stream=None, device=None) -> None:

@@ -310,6 +310,16 @@ ITTT_API size_t ittt_workspace_bytes_ex(int64_t B, int64_t T, int64_t d, int64_t
                                         int64_t chunk, const ittt_opts* opts);
 
 /*
+ * Caps the device scratch one call may allocate (bytes; 0, the default,
+ * means no cap) for every later call in this process: a call that would
+ * allocate more returns ITTT_ERR_OOM before anything is enqueued.  Calls
+ * given a caller workspace allocate nothing and are not affected.  Lets a
+ * process keep the library inside a memory budget, and lets tests take the
+ * out-of-memory path without exhausting the device.
+ */
+ITTT_API void ittt_set_scratch_limit(size_t bytes);
+
+/*
  * Synchronises `stream`, then reports any device-side failure recorded by
  * this library's kernels on the current device since the previous call
  * (ITTT_ERR_TIMEOUT when a bounded wait ran out) or a pending CUDA error

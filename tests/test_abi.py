@@ -324,3 +324,20 @@ def test_state_prefix_rejects_bad_arguments(lib):
     odd = _desc([R, S, 60, f], ittt.FP32, data=FAKE)
     assert _prefix_call(lib, None, odd, 1, _desc([S, 60, f], ittt.FP32, data=FAKE * 1024)) \
         == ittt.ERR_UNSUPPORTED
+
+
+def test_scratch_limit_fails_before_any_work(lib):
+    """Over the scratch cap a call returns ITTT_ERR_OOM before it touches the
+    device (fake pointers: nothing may run); a caller workspace is exempt."""
+    a = _args()
+    need = ittt.workspace_bytes(1, 256, 64, 256, 64)
+    try:
+        ittt.set_scratch_limit(need - 1)
+        assert _call(lib, a) == ittt.ERR_OOM
+        assert "limit" in ittt.last_error()
+        o = ittt.Opts()
+        o.workspace = FAKE * 64
+        o.workspace_bytes = need
+        assert _call(lib, a, opts=o) != ittt.ERR_OOM      # no allocation: past the cap check
+    finally:
+        ittt.set_scratch_limit(0)

@@ -882,3 +882,103 @@ def test_forward_captured_in_cuda_graph(cuda_device, variant):
     ittt.stream_status()
     assert torch.equal(out, want)
     assert not torch.equal(out, eager)
+
+
+# --------------------------------------------------------------------------
+# Canaries: every buffer the library writes sits inside a larger allocation
+# whose guard bytes before and after hold a sentinel; after the call the
+# guards must be untouched (out-of-bounds writes on ragged shapes would show)
+# --------------------------------------------------------------------------
+
+GUARD = 4096  # bytes on each side (a multiple of 256: the views stay aligned)
+
+
+def guarded(shape, dtype, device):
+    """A tensor of `shape` inside a byte buffer with GUARD sentinel bytes on
+    both sides; returns (view, check) where check() is True while the guards
+    hold."""
+    elem = torch.tensor([], dtype=dtype).element_size()
+    n = int(np.prod(shape)) * elem
+    raw = torch.full((n + 2 * GUARD,), 0xA5, dtype=torch.uint8, device=device)
+    view = raw[GUARD:GUARD + n].view(dtype).view(shape)
+
+    def check():
+        return bool((raw[:GUARD] == 0xA5).all()) and bool((raw[GUARD + n:] == 0xA5).all())
+    return view, check
+
+
+CANARY = [
+    # B, T, d, f, C, options
+    (2, 333, 136, 264, 100, {}),                          # ragged chunks, single-CTA walk
+    (1, 250, 200, 584, 128, {"want_state": True}),        # partial last chunk with state_out
+    (2, 640, 72, 136, 320, {"out_dtype": torch.float32}), # fp32 output, masked stores
+    (1, 512, 256, 584, 128, {"l2norm": True, "want_state": True}),
+    (1, 600, 64, 256, 64, {"cu_seqlens": [0, 1, 130, 387, 600]}),
+    (2, 256, 64, 256, 64, {"dual": True}),
+]
+
+
+@pytest.mark.parametrize("B,T,d,f,C,opts", CANARY)
+def test_no_writes_outside_buffers(cuda_device, B, T, d, f, C, opts):
+    opts = dict(opts)
+    g = to_device(make_inputs(B, T, d, f, seed=2000 + T), cuda_device)
+    cu = opts.pop("cu_seqlens", None)
+    want_state = opts.pop("want_state", False)
+    out_dtype = opts.pop("out_dtype", torch.bfloat16)
+    states = B if cu is None else len(cu) - 1
+    slots = -(-T // C) if cu is None else packed_slots(cu, C)[1]
+    checks = []
+    out, c = guarded((B, T, d), out_dtype, cuda_device)
+    checks.append(("out", c))
+    kw = {}
+    kw["z_buf"], c = guarded((B, T, f), torch.bfloat16, cuda_device)
+    checks.append(("z_buf", c))
+    kw["vhat_buf"], c = guarded((B, T, d), torch.bfloat16, cuda_device)
+    checks.append(("vhat_buf", c))
+    if not opts.get("dual"):
+        kw["snap_buf"], c = guarded((B, slots, d, f), torch.bfloat16, cuda_device)
+        checks.append(("snap_buf", c))
+    if want_state:
+        kw["state_out"], c = guarded((states, d, f), torch.float32, cuda_device)
+        checks.append(("state_out", c))
+    ws_bytes = ittt.workspace_bytes_ex(B, T, d, f, C, cu_seqlens=cu, **opts, **kw)
+    assert ws_bytes > 0
+    kw["workspace"], c = guarded((ws_bytes,), torch.uint8, cuda_device)
+    checks.append(("workspace", c))
+    ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                 g["conv_w"], 0.05, C, out, cu_seqlens=cu, **opts, **kw)
+    ittt.stream_status()
+    for name, check in checks:
+        assert check(), f"a kernel wrote outside {name}"
+    # and the call did what it should: the output matches a plain call
+    ref = torch.empty_like(out)
+    ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                 g["conv_w"], 0.05, C, ref, cu_seqlens=cu, **opts)
+    ittt.stream_status()
+    assert torch.equal(out, ref)
+
+
+def test_scratch_limit_on_device(cuda_device):
+    B, T, d, f, C, eta = 1, 256, 64, 256, 64, 0.05
+    g = to_device(make_inputs(B, T, d, f, seed=2100), cuda_device)
+    need = ittt.workspace_bytes(B, T, d, f, C)
+    out = torch.full((B, T, d), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    args = (g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"], g["conv_w"],
+            eta, C, out)
+    try:
+        ittt.set_scratch_limit(need - 1)
+        with pytest.raises(ittt.IttError) as err:
+            ittt.forward(*args)
+        assert err.value.status == ittt.ERR_OOM
+        ittt.stream_status()
+        assert bool((out == 7.0).all())                    # nothing ran
+        ws = torch.empty(need, dtype=torch.uint8, device=cuda_device)
+        ittt.forward(*args, workspace=ws)                  # caller scratch: not capped
+        ittt.stream_status()
+        first = out.clone()
+        ittt.set_scratch_limit(need)                       # exactly enough
+        ittt.forward(*args)
+        ittt.stream_status()
+        assert torch.equal(out, first)
+    finally:
+        ittt.set_scratch_limit(0)
