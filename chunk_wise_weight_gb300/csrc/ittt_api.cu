@@ -119,6 +119,8 @@ struct StagingSlot {
 
 __global__ void __launch_bounds__(256)
     stage_table_kernel(const int* __restrict__ src, int* __restrict__ dst, int count) {
+  ittt::griddep_wait();  // programmatic launch: the previous grid is done
+  ittt::griddep_launch_dependents();
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += gridDim.x * blockDim.x)
     dst[i] = src[i];
 }
@@ -216,8 +218,8 @@ ittt_status stage_table(DeviceState* ds, int* dst, const int* src, size_t count,
   }
   memcpy(sl.host, src, bytes);
   const int blocks = int(std::min<size_t>((count + 255) / 256, 64));
-  stage_table_kernel<<<blocks, 256, 0, stream>>>(sl.dev, dst, int(count));
-  e = cudaGetLastError();
+  e = ittt::launch_pdl(stage_table_kernel, dim3(blocks), dim3(256), 0, stream,
+                       static_cast<const int*>(sl.dev), dst, int(count));
   if (e != cudaSuccess) return cuda_fail(e, "document table staging");
   e = cudaEventRecord(sl.done, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord (staging)");

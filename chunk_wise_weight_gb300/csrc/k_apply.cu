@@ -268,8 +268,8 @@ cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z, const CU
                                        int(pipe_smem_bytes<ApplySched>()));
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? int(units) : env.num_sms;
-  apply_kernel<<<grid, PipeShape<ApplySched>::kThreads, pipe_smem_bytes<ApplySched>(), env.stream>>>(p, env.status);
-  return cudaGetLastError();
+  return launch_pdl(apply_kernel, dim3(grid), dim3(PipeShape<ApplySched>::kThreads),
+                    pipe_smem_bytes<ApplySched>(), env.stream, p, env.status);
 }
 
 }  // namespace ittt

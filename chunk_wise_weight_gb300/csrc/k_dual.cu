@@ -232,9 +232,8 @@ cudaError_t launch_scores(const LaunchEnv& env, const CUtensorMap& tm_zq, const 
                                        int(pipe_smem_bytes<ScoresSched>()));
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? int(units) : env.num_sms;
-  scores_kernel<<<grid, PipeShape<ScoresSched>::kThreads, pipe_smem_bytes<ScoresSched>(),
-                  env.stream>>>(p, env.status);
-  return cudaGetLastError();
+  return launch_pdl(scores_kernel, dim3(grid), dim3(PipeShape<ScoresSched>::kThreads),
+                    pipe_smem_bytes<ScoresSched>(), env.stream, p, env.status);
 }
 
 cudaError_t launch_dual_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
@@ -263,9 +262,8 @@ cudaError_t launch_dual_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
                                        int(pipe_smem_bytes<DualSched>()));
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? int(units) : env.num_sms;
-  dual_apply_kernel<<<grid, PipeShape<DualSched>::kThreads, pipe_smem_bytes<DualSched>(),
-                      env.stream>>>(p, env.status);
-  return cudaGetLastError();
+  return launch_pdl(dual_apply_kernel, dim3(grid), dim3(PipeShape<DualSched>::kThreads),
+                    pipe_smem_bytes<DualSched>(), env.stream, p, env.status);
 }
 
 }  // namespace ittt

@@ -209,8 +209,8 @@ cudaError_t launch_gateup(const LaunchEnv& env, const CUtensorMap& tm_h, const C
                                        int(pipe_smem_bytes<GateUpSched>()));
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? units : env.num_sms;
-  gateup_kernel<<<grid, PipeShape<GateUpSched>::kThreads, pipe_smem_bytes<GateUpSched>(), env.stream>>>(p, env.status);
-  return cudaGetLastError();
+  return launch_pdl(gateup_kernel, dim3(grid), dim3(PipeShape<GateUpSched>::kThreads),
+                    pipe_smem_bytes<GateUpSched>(), env.stream, p, env.status);
 }
 
 }  // namespace ittt

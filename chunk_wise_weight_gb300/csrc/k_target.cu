@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(256)
     conv3_kernel(const __nv_bfloat16* __restrict__ x0, const float* __restrict__ conv_w,
                  __nv_bfloat16* __restrict__ xc, int64_t rows, DocMap docs, int d,
                  int pad_mode) {
+  griddep_wait();  // programmatic launch: the previous grid is done
+  griddep_launch_dependents();
   const int groups = d >> 3;
   const int64_t blocks = (rows + kConvRows - 1) / kConvRows;
   const int64_t total = blocks * groups;
@@ -415,9 +417,8 @@ cudaError_t launch_target_variant(const LaunchEnv& env, const TargetParams& p, i
                                        int(pipe_smem_bytes<S>()));
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? units : env.num_sms;
-  target_kernel<kFused><<<grid, PipeShape<S>::kThreads, pipe_smem_bytes<S>(), env.stream>>>(
-      p, env.status);
-  return cudaGetLastError();
+  return launch_pdl(target_kernel<kFused>, dim3(grid), dim3(PipeShape<S>::kThreads),
+                    pipe_smem_bytes<S>(), env.stream, p, env.status);
 }
 
 }  // namespace
@@ -430,8 +431,8 @@ cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const flo
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = int64_t(env.num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  conv3_kernel<<<int(blocks), 256, 0, env.stream>>>(x0, conv_w, xc, rows, docs, d, pad_mode);
-  return cudaGetLastError();
+  return launch_pdl(conv3_kernel, dim3(unsigned(blocks)), dim3(256), 0, env.stream, x0, conv_w,
+                    xc, rows, docs, d, pad_mode);
 }
 
 cudaError_t launch_target_pair(const LaunchEnv& env, const CUtensorMap& tm_xc,

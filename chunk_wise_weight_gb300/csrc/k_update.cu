@@ -572,6 +572,8 @@ __global__ void __launch_bounds__(256)
                          __nv_bfloat16* __restrict__ snap, float* __restrict__ state_out,
                          DocMap docs, const int* __restrict__ upd_docs, int final_update, int d,
                          int f, int nparts) {
+  griddep_wait();  // programmatic launch: the previous grid is done
+  griddep_launch_dependents();
   __shared__ float row_scale;
   const int m = blockIdx.x;
   const int doc = upd_docs ? __ldg(upd_docs + blockIdx.y) : int(blockIdx.y);
@@ -613,6 +615,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256)
     snapshot0_kernel(const void* __restrict__ w0, int w0_fp32, int64_t w0_bstride,
                      __nv_bfloat16* __restrict__ snap, DocMap docs, int64_t df) {
+  griddep_wait();  // programmatic launch: the previous grid is done
+  griddep_launch_dependents();
   const int64_t per = df >> 3;
   const int64_t total = int64_t(docs.ndocs) * per;
   for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -645,9 +649,8 @@ cudaError_t launch_snapshot0(const LaunchEnv& env, const void* w0, bool w0_fp32,
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = int64_t(env.num_sms) * 8;
   if (blocks > cap) blocks = cap;
-  snapshot0_kernel<<<int(blocks), 256, 0, env.stream>>>(w0, w0_fp32 ? 1 : 0, w0_bstride, snap,
-                                                        docs, df);
-  return cudaGetLastError();
+  return launch_pdl(snapshot0_kernel, dim3(unsigned(blocks)), dim3(256), 0, env.stream, w0,
+                    w0_fp32 ? 1 : 0, w0_bstride, snap, docs, df);
 }
 
 // state[s] = W_start[s] + deltas[0, s] + ... + deltas[count-1, s], four fp32
@@ -658,6 +661,8 @@ __global__ void __launch_bounds__(256)
     state_prefix_kernel(const void* __restrict__ w0, int w0_kind, const float* __restrict__ deltas,
                         int64_t per_delta, int count, float* __restrict__ state, int64_t df,
                         int64_t groups) {
+  griddep_wait();  // programmatic launch: the previous grid is done
+  griddep_launch_dependents();
   for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
        g += int64_t(gridDim.x) * blockDim.x) {
     const int64_t e = g * 4;
@@ -692,9 +697,8 @@ cudaError_t launch_state_prefix(const LaunchEnv& env, const void* w0, int w0_kin
   const int64_t want = (groups + 255) / 256;
   const int64_t cap = int64_t(env.num_sms) * 8;
   const int grid = int(want < cap ? want : cap);
-  state_prefix_kernel<<<grid, 256, 0, env.stream>>>(w0, w0_kind, deltas, S * df, count, state, df,
-                                                    groups);
-  return cudaGetLastError();
+  return launch_pdl(state_prefix_kernel, dim3(grid), dim3(256), 0, env.stream, w0, w0_kind, deltas,
+                    S * df, count, state, df, groups);
 }
 
 cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, const CUtensorMap& tm_z,
@@ -745,8 +749,8 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
   e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(pipe_smem_bytes<UpdateSched>()));
   if (e != cudaSuccess) return e;
-  update_kernel<<<grid, PipeShape<UpdateSched>::kThreads, pipe_smem_bytes<UpdateSched>(), env.stream>>>(p, env.status);
-  return cudaGetLastError();
+  return launch_pdl(update_kernel, dim3(grid), dim3(PipeShape<UpdateSched>::kThreads),
+                    pipe_smem_bytes<UpdateSched>(), env.stream, p, env.status);
 }
 
 cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
@@ -803,17 +807,16 @@ cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
                           pair_threads<NormUpdatePairSched>());
     } else {
       const int grid = units < env.num_sms ? int(units) : env.num_sms;
-      norm_update_kernel<<<grid, PipeShape<NormUpdateSched>::kThreads,
-                           pipe_smem_bytes<NormUpdateSched>(), env.stream>>>(p, env.status);
-      e = cudaGetLastError();
+      e = launch_pdl(norm_update_kernel, dim3(grid), dim3(PipeShape<NormUpdateSched>::kThreads),
+                     pipe_smem_bytes<NormUpdateSched>(), env.stream, p, env.status);
     }
     if (e != cudaSuccess) return e;
   }
   const dim3 fin(unsigned(a.d), unsigned(a.n_udocs));
-  norm_finalize_kernel<<<fin, 256, 0, env.stream>>>(a.state, a.partial, a.snap, a.state_out,
-                                                    a.docs, a.upd_docs, a.state_out ? 1 : 0,
-                                                    a.d, a.f, p.nparts);
-  return cudaGetLastError();
+  return launch_pdl(norm_finalize_kernel, fin, dim3(256), 0, env.stream,
+                    static_cast<const float*>(a.state), static_cast<const float*>(a.partial),
+                    a.snap, a.state_out, a.docs, a.upd_docs, a.state_out ? 1 : 0, a.d, a.f,
+                    p.nparts);
 }
 
 }  // namespace ittt

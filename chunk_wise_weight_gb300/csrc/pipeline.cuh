@@ -210,6 +210,11 @@ __device__ __forceinline__ void run_pipeline(const typename S::Params& p, unsign
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sync->tmem_base;
+  // Set-up done: only now touch memory the previous grid may still write or
+  // read (launched with programmatic serialization, this grid's set-up
+  // overlapped that grid's last CTAs).
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {

@@ -118,6 +118,10 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
   cluster_sync();  // both CTAs' barriers exist before either reaches across
   tc_fence_after_sync();
   const uint32_t tmem = sync->tmem_base;
+  // Set-up done: only now touch memory the previous grid may still write or
+  // read (see pipeline.cuh).
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -312,21 +316,28 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
 }
 
 // ------------------------------------------------------------------ host side
+// attr: room for two attributes (the cluster shape and, with `pdl`,
+// programmatic stream serialization as in launch_pdl).
 inline cudaLaunchConfig_t pair_launch_config(int pairs, size_t smem, const LaunchEnv& env,
                                              cudaLaunchAttribute* attr,
-                                             int threads = kBaseThreads) {
+                                             int threads = kBaseThreads, bool pdl = false) {
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(unsigned(2 * pairs), 1, 1);
   cfg.blockDim = dim3(unsigned(threads), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = env.stream;
-  attr->id = cudaLaunchAttributeClusterDimension;
-  attr->val.clusterDim.x = 2;
-  attr->val.clusterDim.y = 1;
-  attr->val.clusterDim.z = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (pdl) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
   return cfg;
 }
 
@@ -336,8 +347,8 @@ inline cudaError_t max_pairs(const void* kernel, size_t smem, const LaunchEnv& e
                              std::atomic<int>* cache, int threads = kBaseThreads) {
   int n = cache->load();
   if (n < 0) {
-    cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = pair_launch_config(env.num_sms / 2, smem, env, &attr, threads);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pair_launch_config(env.num_sms / 2, smem, env, attr, threads);
     cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
     if (e != cudaSuccess) return e;
     cache->store(n);
@@ -350,8 +361,8 @@ template <class P>
 inline cudaError_t launch_on_pairs(const void* kernel, int pairs, size_t smem,
                                    const LaunchEnv& env, const P* params,
                                    int threads = kBaseThreads) {
-  cudaLaunchAttribute attr;
-  cudaLaunchConfig_t cfg = pair_launch_config(pairs, smem, env, &attr, threads);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_launch_config(pairs, smem, env, attr, threads, true);
   unsigned int* status = env.status;
   void* args[] = {const_cast<P*>(params), &status};
   return cudaLaunchKernelExC(&cfg, kernel, args);

@@ -140,6 +140,18 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_
                : "memory");
 }
 
+// Programmatic dependent launch.  A grid launched with programmatic stream
+// serialization may start while the previous grid on its stream is still
+// running; griddep_wait() blocks until that grid has completed and its memory
+// operations are visible (a no-op for a grid launched without the attribute),
+// and griddep_launch_dependents() lets the next such grid start its set-up.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
