@@ -501,9 +501,28 @@ def main():
         torch.cuda.synchronize(dev)
         ittt.stream_status(stream)
 
+    # An untimed pass of the same length with every phase's events finds the
+    # dominant kernel and gives the other phases' times; the timed steps then
+    # record only the dominant kernel's two events (an event between two
+    # kernels costs a little and keeps the second from starting early).
     nph = len(ittt.PHASES)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nph)]
-          for _ in range(args.steps)]
+    ev_all = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nph)]
+              for _ in range(args.steps)]
+    for k in range(args.steps):
+        step(ev_all[k])
+    torch.cuda.synchronize(dev)
+    ittt.stream_status(stream)
+    pass_ms = {name: sum(ev_all[k][2 * p].elapsed_time(ev_all[k][2 * p + 1])
+                         for k in range(args.steps)) / args.steps
+               for p, name in enumerate(ittt.PHASES)}
+    dominant = max(ittt.PHASES, key=lambda nm: pass_ms[nm])
+    di = ittt.PHASES.index(dominant)
+    ev_dom = []
+    for _ in range(args.steps):
+        row = [None] * (2 * nph)
+        row[2 * di] = torch.cuda.Event(enable_timing=True)
+        row[2 * di + 1] = torch.cuda.Event(enable_timing=True)
+        ev_dom.append(row)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
@@ -511,42 +530,41 @@ def main():
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)  # let the sampler take its first reading
-    # The library records each phase's start and end events on the launching
-    # stream, so the per-kernel durations come from the timed steps themselves.
     t_start.record(stream)
     for k in range(args.steps):
         if graph is not None:
             graph.replay()
         else:
-            step(ev[k])
+            step(ev_dom[k])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     barrier(dev)
-    if graph is not None:
-        # Per-kernel phases from an eager pass of the same length.
-        for k in range(args.steps):
-            step(ev[k])
-        torch.cuda.synchronize(dev)
     ittt.stream_status(stream)
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     ms_per_step = elapsed_ms / args.steps
     tokens = B * T * world * args.steps
     value = tokens / (elapsed_ms / 1e3)
 
-    # Per-phase device durations from the events between launches.
+    # Per-phase device durations: the dominant kernel's from the timed steps
+    # (a replayed graph records none: then from the untimed pass), the
+    # others' from the untimed pass.
+    live = graph is None
+    if live:
+        pass_ms[dominant] = sum(ev_dom[k][2 * di].elapsed_time(ev_dom[k][2 * di + 1])
+                                for k in range(args.steps)) / args.steps
     model = phase_model(B, T, d, f, C, args.dual, cu)
     phases = {}
-    for p, name in enumerate(ittt.PHASES):
-        ms = sum(ev[k][2 * p].elapsed_time(ev[k][2 * p + 1]) for k in range(args.steps)) / args.steps
+    for name in ittt.PHASES:
+        ms = pass_ms[name]
         kind, work = model[name]
-        entry = {"ms": round(ms, 4), "share": round(ms / ms_per_step, 4)}
+        entry = {"ms": round(ms, 4), "share": round(ms / ms_per_step, 4),
+                 "timed": "timed steps" if (live and name == dominant) else "untimed pass"}
         if kind == "tensor":
             entry["tflops"] = round(work / (ms * 1e-3) / 1e12, 1) if ms > 0 else None
         else:
             entry["gbs"] = round(work / (ms * 1e-3) / 1e9, 1) if ms > 0 else None
         phases[name] = entry
-    dominant = max(ittt.PHASES, key=lambda nm: phases[nm]["ms"])
     kind, work = model[dominant]
     dom_ms = phases[dominant]["ms"]
     if kind == "tensor":
@@ -560,13 +578,15 @@ def main():
                 "traffic": recorded_traffic(args.config, dominant, bool(args.shape)),
                 "peak_kind": f"bf16_tflops burst ({peak_src})",
                 "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4),
-                "flops_per_launch": work}
+                "flops_per_launch": work,
+                "timed": "CUDA events in the timed steps" if live else "untimed eager pass"}
     else:
         achieved = work / (dom_ms * 1e-3) / 1e9
         peak = float(peaks["hbm_gbs"])
         roof = {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
-                "peak_kind": f"hbm_gbs ({peak_src})", "bytes_per_launch": work}
+                "peak_kind": f"hbm_gbs ({peak_src})", "bytes_per_launch": work,
+                "timed": "CUDA events in the timed steps" if live else "untimed eager pass"}
     F = counted_flops_packed(cu, d, f, C) if cu else counted_flops(B, T, d, f, C)
     layer_tflops = F / (ms_per_step * 1e-3) / 1e12
 

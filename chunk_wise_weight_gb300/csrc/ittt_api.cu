@@ -732,7 +732,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   PhaseRanges ranges;
   auto rec = [&](int slot, cudaStream_t st) -> cudaError_t {
     ranges.mark(slot);
-    return ev ? cudaEventRecord(ev[slot], st) : cudaSuccess;
+    return (ev && ev[slot]) ? cudaEventRecord(ev[slot], st) : cudaSuccess;
   };
   const float* cw = static_cast<const float*>(conv_w->data);
 

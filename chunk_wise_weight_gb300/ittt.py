@@ -179,8 +179,8 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
             update_only: bool = False, reuse_zv: bool = False):
     """Enqueue one layer forward on `stream` (default: current stream) and
     return `out` [B,T,d].  Extra keyword buffers map to ittt_opts; `events`
-    is a list of 2 * len(PHASES) torch.cuda.Event(enable_timing=True): a
-    (start, end) pair per phase.  `cu_seqlens` (host ints, num_docs + 1
+    is a list of 2 * len(PHASES) torch.cuda.Event(enable_timing=True) or
+    None entries: a (start, end) pair per phase, None where not wanted.  `cu_seqlens` (host ints, num_docs + 1
     offsets) packs documents into the one row of H [1,T,d].
     `update_only` folds every chunk into `state_out` and applies nothing
     (returns None; W_down0 None starts from zero); `reuse_zv` takes Z and
@@ -205,9 +205,10 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
         if len(events) != 2 * len(PHASES):
             raise ValueError(f"events needs {2 * len(PHASES)} entries")
         for e in events:  # torch creates the CUDA event on its first record
-            if not e.cuda_event:
+            if e is not None and not e.cuda_event:
                 e.record(torch.cuda.current_stream(H.device) if stream is None else stream)
-        ev_arr = (ctypes.c_void_p * len(events))(*[int(e.cuda_event) for e in events])
+        ev_arr = (ctypes.c_void_p * len(events))(
+            *[0 if e is None else int(e.cuda_event) for e in events])
         opts.events = ctypes.cast(ev_arr, ctypes.POINTER(ctypes.c_void_p))
     s = _stream_handle(stream, H.device)
     status = lib.ittt_forward_ex(*[_ref(k) for k in keep[:7]], ctypes.c_float(eta),

@@ -140,7 +140,10 @@ typedef struct {
  *              events[2k] and events[2k+1] are recorded right before and
  *              right after phase k (ittt_phase order) on `stream`, so each
  *              pair brackets one phase on the device timeline.  A phase with
- *              nothing to do records both.
+ *              nothing to do records both.  A NULL entry is not recorded
+ *              (time only the phases you need: an event between two kernels
+ *              costs a little and keeps the second from starting its set-up
+ *              early).
  *   flags      ITTT_FLAG_* bits.
  */
 typedef struct {

@@ -982,3 +982,23 @@ def test_scratch_limit_on_device(cuda_device):
         assert torch.equal(out, first)
     finally:
         ittt.set_scratch_limit(0)
+
+
+def test_phase_events_may_be_partial(cuda_device):
+    """NULL entries of the events array are skipped; the others bracket their
+    phase."""
+    B, T, d, f, C, eta = 1, 512, 256, 584, 128, 0.05
+    g = to_device(make_inputs(B, T, d, f, seed=2200), cuda_device)
+    n = len(ittt.PHASES)
+    gi = ittt.PHASES.index("gateup")
+    events = [None] * (2 * n)
+    events[2 * gi] = torch.cuda.Event(enable_timing=True)
+    events[2 * gi + 1] = torch.cuda.Event(enable_timing=True)
+    out = ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                       g["conv_w"], eta, C, events=events)
+    ittt.stream_status()
+    assert events[2 * gi].elapsed_time(events[2 * gi + 1]) > 0.0
+    ref = ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                       g["conv_w"], eta, C)
+    ittt.stream_status()
+    assert torch.equal(out, ref)
