@@ -37,7 +37,7 @@ DEFAULT_CONFIG = 2
 # hash of the kernel's sources at capture time: once the sources change the
 # figure no longer describes the kernel and `traffic` is reported as null.
 TRAFFIC_BYTES = {
-    (2, "gateup"): (2789991321, "d38d124caee580c8"),
+    (2, "gateup"): (3042022765, "34275b50d60d5cd6"),
 }
 KERNEL_SOURCES = {
     "gateup": ["k_gateup.cu"], "target": ["k_target.cu"], "update": ["k_update.cu"],
@@ -134,6 +134,78 @@ def load_peaks():
     return dict(PEAK_FALLBACK), "fallback"
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (libnvidia-ml, via
+    ctypes) every 10 ms on a host thread, so even a timed region of a few
+    tens of milliseconds gets several samples.  Read-only: it sets nothing.
+    Falls back to nvidia-smi (ClockSampler) where NVML cannot be loaded."""
+
+    # NVML clock-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, device=None):
+        import ctypes
+        import threading
+        self.ctypes, self.threading = ctypes, threading
+        self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nvml.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        found = False
+        if device is not None:  # match the CUDA device by its PCI address
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(device)
+                bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+                found = self.nvml.nvmlDeviceGetHandleByPciBusId_v2(
+                    bus.encode(), ctypes.byref(self.handle)) == 0
+            except (AttributeError, RuntimeError):
+                found = False
+        if not found and self.nvml.nvmlDeviceGetHandleByIndex_v2(
+                ctypes.c_uint(index), ctypes.byref(self.handle)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) \
+            or self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+
+    def _run(self):
+        ctypes = self.ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            if (self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0 and
+                    self.reasons_fn(self.handle, ctypes.byref(rs)) == 0):
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(0.01)
+
+    def start(self):
+        self.thread = self.threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self) -> dict | None:
+        self.stop_flag.set()
+        self.thread.join()
+        if not self.samples:
+            return None
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items()
+                          if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(self.samples), "source": "NVML every 10 ms in the timed region"}
+
+
+def clock_sampler(index: int, device=None):
+    try:
+        return NvmlClockSampler(index, device)
+    except (OSError, AttributeError):
+        return ClockSampler(index)
+
+
 class ClockSampler:
     """nvidia-smi samples every 200 ms while the timed region runs."""
 
@@ -169,7 +241,7 @@ class ClockSampler:
                           if r[5 + k].strip().lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "source": "nvidia-smi every 200 ms"}
 
 
 def phase_model(B, T, d, f, C, dual=False, cu=None):
@@ -256,10 +328,11 @@ def run_seq_shards(args, cfg, tensors, stream, dev, peaks, peak_src, rates, loca
         step()
     ittt.stream_status(stream)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    sampler = ClockSampler(local)
+    sampler = clock_sampler(local, dev)
     torch.cuda.synchronize(dev)
     sampler.start()
-    time.sleep(0.3)
+    if isinstance(sampler, ClockSampler):
+        time.sleep(0.3)  # let nvidia-smi take its first reading
     for k in range(args.steps):
         step(ev[k])
     torch.cuda.synchronize(dev)
@@ -525,11 +598,14 @@ def main():
         ev_dom.append(row)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local)
+    sampler = clock_sampler(local, dev)
     barrier(dev)
     torch.cuda.synchronize(dev)
-    sampler.start()
-    time.sleep(0.3)  # let the sampler take its first reading
+    if isinstance(sampler, ClockSampler):
+        sampler.start()
+        time.sleep(0.3)  # let nvidia-smi take its first reading
+    else:
+        sampler.start()
     t_start.record(stream)
     for k in range(args.steps):
         if graph is not None:
