@@ -644,6 +644,17 @@ def test_named_workload_sampled_large(cuda_device, index):
     _sampled_checks(index, cuda_device, n_state_pairs=12)
 
 
+@pytest.mark.parametrize("shape", [
+    (1, 8192, 4096, 14336, 2048, 0.01),   # Llama-3-8B-sized MLP
+    (2, 4096, 5120, 13824, 1024, 0.01),   # Qwen2.5-14B-sized MLP
+    (2, 4096, 1024, 3072, 512, 0.02),     # Qwen3-0.6B-sized MLP
+])
+def test_other_layer_widths_sampled(cuda_device, shape):
+    """Layer widths of other model sizes, full size, sampled like the named
+    workloads."""
+    _sampled_checks(1600 + shape[2], cuda_device, n_state_pairs=12, shape=shape)
+
+
 def test_longest_sequence_sampled(cuda_device):
     """262,144 tokens in one sequence (64 chunks of 4096; Z alone is 5 GB and
     T * d_ff exceeds 2^31 elements): the same sampled checks."""
