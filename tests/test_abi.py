@@ -3,6 +3,7 @@ exports every entry point include/ittt.h declares, and rejects bad
 arguments with the documented status before touching any memory."""
 import ctypes
 import math
+import os
 
 import pytest
 import torch
@@ -341,3 +342,27 @@ def test_scratch_limit_fails_before_any_work(lib):
         assert _call(lib, a, opts=o) != ittt.ERR_OOM      # no allocation: past the cap check
     finally:
         ittt.set_scratch_limit(0)
+
+
+C_PROGRAM = os.path.join(os.path.dirname(os.path.abspath(__file__)), "c_abi", "forward_from_c.c")
+
+
+def build_c_program(out_path):
+    """gcc, C99, against include/ittt.h, libittt.so and the CUDA runtime."""
+    import subprocess
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    libdir = os.path.dirname(build.LIB_PATH)
+    cmd = ["gcc", "-std=c99", "-O2", "-Wall", "-Werror", "-o", out_path, C_PROGRAM,
+           "-I", build.INCLUDE, "-I", os.path.join(cuda, "include"),
+           "-L", libdir, "-Wl,-rpath," + libdir, "-l:" + os.path.basename(build.LIB_PATH),
+           "-L", os.path.join(cuda, "lib64"), "-Wl,-rpath," + os.path.join(cuda, "lib64"),
+           "-lcudart"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    return out_path
+
+
+def test_header_and_a_c_caller_build_as_c99(lib, tmp_path):
+    """The boundary is plain C: a C99 program using only ittt.h and the CUDA
+    runtime compiles (-Wall -Werror) and links against libittt.so."""
+    exe = build_c_program(str(tmp_path / "forward_from_c"))
+    assert os.path.exists(exe)

@@ -1013,3 +1013,26 @@ def test_phase_events_may_be_partial(cuda_device):
                        g["conv_w"], eta, C)
     ittt.stream_status()
     assert torch.equal(out, ref)
+
+
+def test_forward_called_from_c(cuda_device, tmp_path):
+    """A plain C99 program (tests/c_abi/forward_from_c.c) calls ittt_forward
+    through the C-ABI on its own device buffers: its O equals, bit for bit,
+    the same call made from Python."""
+    import subprocess
+    from test_abi import build_c_program
+    exe = build_c_program(str(tmp_path / "forward_from_c"))
+    B, T, d, f, C, eta = 2, 512, 256, 584, 128, 0.05
+    g = to_device(make_inputs(B, T, d, f, seed=2300), cuda_device)
+    src, dst = tmp_path / "in.bin", tmp_path / "out.bin"
+    with open(src, "wb") as fh:
+        fh.write(np.array([B, T, d, f, C], np.int64).tobytes())
+        fh.write(np.array([eta], np.float32).tobytes())
+        for k in ("H", "X0", "W_gate", "W_up", "W_down0", "W_target"):
+            fh.write(g[k].contiguous().view(torch.int16).cpu().numpy().tobytes())
+        fh.write(g["conv_w"].contiguous().cpu().numpy().astype(np.float32).tobytes())
+    r = subprocess.run([exe, str(src), str(dst)], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    got = torch.from_numpy(np.fromfile(dst, dtype=np.int16).reshape(B, T, d)).view(torch.bfloat16)
+    ref = run(g, eta, C)["O"].cpu()
+    assert torch.equal(got, ref)
