@@ -104,6 +104,24 @@ class CudaEngine:
                                  vhat_buf=vhat)
 
 
+def check_spans(T_r: int, chunk: int, world: int, group, device) -> None:
+    """Every rank's span length, all-gathered: the spans must be whole chunks
+    except the last non-empty one, and no non-empty span may follow an empty
+    one (chunk edges are where the convolution pads and the prefix splits).
+    Raises ValueError on every rank alike."""
+    mine = torch.tensor([T_r], dtype=torch.int64, device=device)
+    lens = [torch.zeros_like(mine) for _ in range(world)]
+    dist.all_gather(lens, mine, group=group)
+    lens = [int(t.item()) for t in lens]
+    nonempty = [r for r, n in enumerate(lens) if n > 0]
+    if nonempty and nonempty != list(range(len(nonempty))):
+        raise ValueError(f"span lengths {lens}: a non-empty span follows an empty one")
+    for r in nonempty[:-1]:
+        if lens[r] % chunk != 0:
+            raise ValueError(f"span lengths {lens}: span {r} is not a whole number of "
+                             f"{chunk}-token chunks")
+
+
 def sequence_parallel_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float,
                               chunk: int, *, eta_tok=None, group=None, engine=None,
                               want_state: bool = False):
@@ -125,6 +143,8 @@ def sequence_parallel_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, et
         world, rank = 1, 0
     B, T_r, d = H.shape
     f = W_gate.shape[0]
+    if world > 1:
+        check_spans(T_r, chunk, world, group, H.device)
     if T_r > 0:
         delta, zv = engine.fold(H, X0, W_gate, W_up, W_target, conv_w, eta, chunk,
                                 eta_tok=eta_tok)

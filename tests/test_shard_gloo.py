@@ -157,3 +157,30 @@ def test_gloo_ranks_shard_one_sequence(tmp_path, world, T, chunk):
     np.testing.assert_allclose(O, full, rtol=1e-5, atol=1e-5 * np.abs(full).max())
     np.testing.assert_allclose(np.load(tmp_path / f"S{world - 1}.npy"),
                                np.load(tmp_path / "final.npy"), rtol=1e-5, atol=1e-6)
+
+
+def _misaligned_worker(rank, world, port, result_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from chunk_wise_weight_gb300 import make_inputs
+        from chunk_wise_weight_gb300.shard import sequence_parallel_forward
+        inp = make_inputs(1, 12, 6, 10, seed=92)
+        a, b = [(0, 6), (6, 12)][rank]        # 6 tokens: not a whole number of 4-token chunks
+        try:
+            sequence_parallel_forward(inp["H"][:, a:b], inp["X0"][:, a:b], inp["W_gate"],
+                                      inp["W_up"], inp["W_down0"], inp["W_target"],
+                                      inp["conv_w"], 0.3, 4, engine=OracleEngine())
+            msg = "no error"
+        except ValueError as e:
+            msg = str(e)
+        with open(os.path.join(result_dir, f"r{rank}.txt"), "w") as fh:
+            fh.write(msg)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_gloo_ranks_reject_spans_off_chunk_edges(tmp_path):
+    mp.spawn(_misaligned_worker, args=(2, _free_port(), str(tmp_path)), nprocs=2, join=True)
+    for r in range(2):
+        assert "not a whole number" in (tmp_path / f"r{r}.txt").read_text()
