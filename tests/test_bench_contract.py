@@ -1,0 +1,42 @@
+"""The bench's reference arm (the fp64 oracle on the host cores) prints the
+one JSON line the contract asks for; runs on the CPU with the tiny workload."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--config", "0",
+                        "--steps", "2", "--warmup", "3"], cwd=ROOT, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference"
+    assert line["steps"] == 2 and line["warmup"] == 3
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "tiny-d64-f256-T256-C64"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_launch_accounting_matches_the_library():
+    """gpu_launches in the bench line counts what the library launches."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunk_wise_weight_gb300 import build, ittt
+    build.build()
+    for B, T, C in ((2, 32768, 2048), (1, 8192, 1024), (1, 256, 256), (1, 1000, 512)):
+        assert bench.launches_per_step(B, T, C, None, False) == ittt.launch_count(B, T, 2560,
+                                                                                 9728, C)
