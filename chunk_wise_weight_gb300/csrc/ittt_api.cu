@@ -591,9 +591,17 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   const ittt_tensor* inputs[] = {H,        X0,     W_gate,   W_up, o.state_in ? o.state_in : W_down0,
                                  W_target, conv_w, o.eta_tok};
   const ittt_tensor* writes[] = {out, o.state_out, o.z_buf, o.vhat_buf, o.snap_buf};
+  // state_out may be state_in itself: every kernel reads a block of the
+  // initial state before that block's final state is written (the walk's
+  // unit preloads the block it later stores; the snapshot-0 copy runs first;
+  // the normalised walk writes state_out after its last launch).
+  const bool in_place = o.state_in && o.state_out && o.state_in->data == o.state_out->data &&
+                        tensor_bytes(o.state_in) == tensor_bytes(o.state_out);
   for (const ittt_tensor* w : writes) {
-    for (const ittt_tensor* in : inputs)
+    for (const ittt_tensor* in : inputs) {
+      if (in_place && w == o.state_out && in == o.state_in) continue;
       if (overlaps(w, in)) return fail(ITTT_ERR_INVALID_ARG, "an output overlaps an input");
+    }
   }
   // Reused Z and eta*Vhat are read by the walk and the apply: no written
   // buffer may overlap them (the check above covers out, state_out and

@@ -120,7 +120,9 @@ typedef struct {
  *              (ittt_state_prefix).
  *   state_out  fp32 [S,d,f]: receives each sequence's or document's fast
  *              weight after its LAST chunk's update (an update the output
- *              itself never needs).
+ *              itself never needs).  May be state_in itself (the same
+ *              buffer, updated in place); any other overlap with an input
+ *              is rejected.
  *   z_buf      bf16 [B,T,f]: caller buffer used as the Z scratch; after the
  *              call it holds Z.  Lets tests inspect the intermediate.
  *   vhat_buf   bf16 [B,T,d]: same for the update's left operand, which the

@@ -366,3 +366,16 @@ def test_header_and_a_c_caller_build_as_c99(lib, tmp_path):
     runtime compiles (-Wall -Werror) and links against libittt.so."""
     exe = build_c_program(str(tmp_path / "forward_from_c"))
     assert os.path.exists(exe)
+
+
+def test_state_in_place_only_as_exact_alias(lib):
+    a = _args()
+    st = _desc([1, 64, 256], ittt.FP32, data=FAKE * 9 * 1024)
+    part = _desc([1, 64, 256], ittt.FP32, data=FAKE * 9 * 1024 + 4096)   # overlaps, not equal
+    o = ittt.Opts()
+    o.state_in = ctypes.pointer(st)
+    o.state_out = ctypes.pointer(part)
+    assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
+    assert "overlaps" in ittt.last_error()
+    o.state_out = ctypes.pointer(st)                                   # the same buffer
+    assert _call(lib, a, opts=o) != ittt.ERR_INVALID_ARG               # past validation

@@ -1036,3 +1036,37 @@ def test_forward_called_from_c(cuda_device, tmp_path):
     got = torch.from_numpy(np.fromfile(dst, dtype=np.int16).reshape(B, T, d)).view(torch.bfloat16)
     ref = run(g, eta, C)["O"].cpu()
     assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("l2norm,update_only,packed", [(False, False, False), (True, False, False),
+                                                       (False, True, False), (False, False, True)])
+def test_state_updated_in_place(cuda_device, l2norm, update_only, packed):
+    """state_out may be state_in itself: a stream of calls continues from one
+    fp32 state buffer, bit-identical to separate in and out buffers."""
+    B, T, d, f, C, eta = 2, 512, 256, 584, 128, 0.05
+    cu = None
+    if packed:
+        B, cu = 1, [0, 200, 384, 512]
+    S = B if cu is None else len(cu) - 1
+    g = to_device(make_inputs(B, T, d, f, seed=2400), cuda_device)
+    start = (torch.randn(S, d, f, generator=torch.Generator().manual_seed(9)) * 0.02).to(cuda_device)
+    kw = dict(l2norm=l2norm, update_only=update_only, cu_seqlens=cu)
+
+    def call(state_in, state_out):
+        return ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], None, g["W_target"],
+                            g["conv_w"], eta, C, state_in=state_in, state_out=state_out, **kw)
+
+    sep_out = torch.empty_like(start)
+    o_sep = call(start.clone(), sep_out)
+    buf = start.clone()
+    o_in = call(buf, buf)
+    ittt.stream_status()
+    assert torch.equal(buf, sep_out)
+    if not update_only:
+        assert torch.equal(o_in, o_sep)
+    # a second step continues from the updated buffer
+    sep2 = torch.empty_like(start)
+    call(sep_out.clone(), sep2)
+    call(buf, buf)
+    ittt.stream_status()
+    assert torch.equal(buf, sep2)
