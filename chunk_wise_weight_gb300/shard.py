@@ -15,11 +15,13 @@ is zero-padded at chunk edges), so
 
   1. every rank folds its span into D_r = eta * sum_{i in span r}
      Vhat_[i]^T Z_[i] from a zero start, keeping Z and eta * Vhat;
-  2. the ranks all-gather the D_r (one [B, d, f] fp32 tensor each);
+  2. the ranks exchange the D_r: an all-gather of one [B, d, f] fp32 tensor
+     per rank, or an exclusive scan by recursive doubling (ceil(log2 R) + 1
+     point-to-point rounds of one tensor each instead of R - 1 received);
   3. rank r starts from W_down0 + D_0 + ... + D_{r-1} (an exclusive prefix)
      and runs the usual walk and apply over its span, reusing Z and eta*Vhat.
 
-The all-gather is the one data-path collective.  The work per token is the
+The exchange is the one data-path communication.  The work per token is the
 single-GPU work plus one extra 2*d*f-FLOP contraction (step 1's fold).
 """
 from __future__ import annotations
@@ -96,6 +98,10 @@ class CudaEngine:
         """W_down0 + deltas[0] + ... + deltas[count-1] (fp32 [B,d,f])."""
         return self.ittt.state_prefix(W_down0, deltas, count, stream=self.stream)
 
+    def add(self, a, b):
+        """a + b for two fp32 [B,d,f] states (a first)."""
+        return self.ittt.state_prefix(a, b.unsqueeze(0), 1, stream=self.stream)
+
     def apply(self, H, X0, W_gate, W_up, W_target, conv_w, eta, chunk, zv, state_in,
               out=None):
         z, vhat = zv
@@ -122,9 +128,41 @@ def check_spans(T_r: int, chunk: int, world: int, group, device) -> None:
                              f"{chunk}-token chunks")
 
 
+def exclusive_scan(delta, engine, world: int, rank: int, group=None):
+    """(sum of the deltas of ranks < rank, sum of ranks <= rank) by recursive
+    doubling: in round k each rank sends its running sum to rank + k and adds
+    the one received from rank - k in front of its own (ranks in order), then
+    one shift turns the inclusive sums into exclusive ones.  None stands for
+    an empty sum (rank 0's exclusive prefix)."""
+    incl = delta.contiguous()
+    k = 1
+    while k < world:
+        ops, recv = [], None
+        if rank + k < world:
+            ops.append(dist.P2POp(dist.isend, incl, rank + k, group))
+        if rank - k >= 0:
+            recv = torch.empty_like(incl)
+            ops.append(dist.P2POp(dist.irecv, recv, rank - k, group))
+        for req in (dist.batch_isend_irecv(ops) if ops else []):
+            req.wait()
+        if recv is not None:
+            incl = engine.add(recv, incl)
+        k *= 2
+    ops, excl = [], None
+    if rank + 1 < world:
+        ops.append(dist.P2POp(dist.isend, incl, rank + 1, group))
+    if rank >= 1:
+        excl = torch.empty_like(incl)
+        ops.append(dist.P2POp(dist.irecv, excl, rank - 1, group))
+    if ops:
+        for req in dist.batch_isend_irecv(ops):
+            req.wait()
+    return excl, incl
+
+
 def sequence_parallel_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float,
                               chunk: int, *, eta_tok=None, group=None, engine=None,
-                              want_state: bool = False):
+                              want_state: bool = False, exchange: str = "allgather"):
     """This rank's part of a sequence-sharded forward.
 
     H, X0 [B, T_r, d] (and eta_tok [B, T_r]) hold this rank's span of every
@@ -134,8 +172,11 @@ def sequence_parallel_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, et
     O [B, T_r, d] for the span and, with `want_state`, the fast weight after
     the span (on the last rank: after the whole sequence).  The convolution
     is zero-padded at chunk edges (the default pad mode), so no token crosses
-    a span boundary.
+    a span boundary.  `exchange`: "allgather" (the prefix adds the deltas in
+    rank order) or "scan" (recursive doubling; the same sum in tree order).
     """
+    if exchange not in ("allgather", "scan"):
+        raise ValueError(f"exchange {exchange!r}")
     engine = engine or CudaEngine()
     if dist.is_available() and dist.is_initialized():
         world, rank = dist.get_world_size(group), dist.get_rank(group)
@@ -150,16 +191,23 @@ def sequence_parallel_forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, et
                                 eta_tok=eta_tok)
     else:
         delta, zv = engine.zeros(B, d, f, H.device), None
-    if world > 1:
-        deltas = delta.new_empty((world,) + tuple(delta.shape))
-        dist.all_gather(list(deltas.unbind(0)), delta, group=group)
+    if world > 1 and exchange == "scan":
+        excl, incl = exclusive_scan(delta, engine, world, rank, group)
+        state_in = (engine.prefix(W_down0, delta.unsqueeze(0), 0) if excl is None
+                    else engine.prefix(W_down0, excl.unsqueeze(0), 1))
+        after = lambda: engine.prefix(W_down0, incl.unsqueeze(0), 1)  # noqa: E731
     else:
-        deltas = delta.unsqueeze(0)
-    state_in = engine.prefix(W_down0, deltas, rank)
+        if world > 1:
+            deltas = delta.new_empty((world,) + tuple(delta.shape))
+            dist.all_gather(list(deltas.unbind(0)), delta, group=group)
+        else:
+            deltas = delta.unsqueeze(0)
+        state_in = engine.prefix(W_down0, deltas, rank)
+        after = lambda: engine.prefix(W_down0, deltas, rank + 1)  # noqa: E731
     if T_r > 0:
         O = engine.apply(H, X0, W_gate, W_up, W_target, conv_w, eta, chunk, zv, state_in)
     else:
         O = H.new_empty((B, 0, d))
     if want_state:
-        return O, engine.prefix(W_down0, deltas, rank + 1)
+        return O, after()
     return O

@@ -111,12 +111,15 @@ class OracleEngine:
     def prefix(self, W0, deltas, count):
         return W0.double() + deltas[:count].sum(0)
 
+    def add(self, a, b):
+        return a + b
+
     def apply(self, H, X0, Wg, Wu, Wt, cw, eta, chunk, zv, state_in, out=None):
         return torch.from_numpy(self.oracle.forward(
             self._span(H, X0, Wg, Wu, state_in.float(), Wt, cw), eta, chunk, eta_tok=zv)["O"])
 
 
-def _seq_worker(rank, world, port, result_dir, T, chunk):
+def _seq_worker(rank, world, port, result_dir, T, chunk, exchange="allgather"):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
@@ -129,7 +132,7 @@ def _seq_worker(rank, world, port, result_dir, T, chunk):
         O, state = sequence_parallel_forward(
             inp["H"][:, a:b], inp["X0"][:, a:b], inp["W_gate"], inp["W_up"], inp["W_down0"],
             inp["W_target"], inp["conv_w"], eta, chunk, eta_tok=rates[:, a:b],
-            engine=OracleEngine(), want_state=True)
+            engine=OracleEngine(), want_state=True, exchange=exchange)
         np.save(os.path.join(result_dir, f"O{rank}.npy"), O.double().numpy())
         np.save(os.path.join(result_dir, f"S{rank}.npy"), state.double().numpy())
         if rank == 0:
@@ -141,15 +144,18 @@ def _seq_worker(rank, world, port, result_dir, T, chunk):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world,T,chunk", [(2, 24, 4), (3, 26, 4), (3, 8, 4)])
-def test_gloo_ranks_shard_one_sequence(tmp_path, world, T, chunk):
+@pytest.mark.parametrize("world,T,chunk,exchange", [
+    (2, 24, 4, "allgather"), (3, 26, 4, "allgather"), (3, 8, 4, "allgather"),
+    (2, 24, 4, "scan"), (3, 26, 4, "scan"), (4, 32, 4, "scan"), (5, 38, 4, "scan"),
+    (5, 12, 4, "scan")])
+def test_gloo_ranks_shard_one_sequence(tmp_path, world, T, chunk, exchange):
     """Each rank folds its span, the deltas are all-gathered, each rank
     applies from the exclusive prefix: the spans' outputs concatenated equal
     the unsharded sequence, and the last rank's state is the final state.
     (26 tokens in chunks of 4 leave a partial last chunk; 8 tokens over
     three ranks leave the third with nothing.)"""
-    mp.spawn(_seq_worker, args=(world, _free_port(), str(tmp_path), T, chunk), nprocs=world,
-             join=True)
+    mp.spawn(_seq_worker, args=(world, _free_port(), str(tmp_path), T, chunk, exchange),
+             nprocs=world, join=True)
     O = np.concatenate([np.load(tmp_path / f"O{r}.npy") for r in range(world)], axis=1)
     full = np.load(tmp_path / "full.npy")
     assert O.shape == full.shape
