@@ -108,7 +108,10 @@ def parse_args():
     ap.add_argument("--fused-conv", action="store_true",
                     help="compute the convolution inside the target GEMM")
     ap.add_argument("--dual", action="store_true",
-                    help="dual form (scores Z Z^T) instead of the fast-weight walk")
+                    help="force the dual form (scores Z Z^T) instead of the fast-weight walk")
+    ap.add_argument("--primal", action="store_true",
+                    help="force the fast-weight walk (the library otherwise picks the dual "
+                         "form for short sequences)")
     ap.add_argument("--packed", action="store_true",
                     help="pack the workload's B*T tokens into one row of documents with "
                          "log-uniform lengths in [512, 16384] (state reset per document)")
@@ -387,6 +390,18 @@ def init_dist(args):
     return world, rank, local
 
 
+def dual_form(cfg, args, cu=None) -> bool:
+    """Whether the call runs the dual form: forced by --dual, else the
+    library's choice for these options (the rule of ittt_plan_form: the dual
+    form where allowed and T < 2 d f / (d + f))."""
+    if args.dual:
+        return True
+    if args.primal or cu is not None or args.l2norm or args.fused_conv:
+        return False
+    T, d, f, C = cfg["T"], cfg["d"], cfg["f"], cfg["C"]
+    return C % 64 == 0 and T % C == 0 and T // C >= 2 and T * (d + f) < 2 * d * f
+
+
 def arm_config(cfg, args, world, cu=None):
     """The `config` object of a bench line (both arms report the same one)."""
     T = cfg["T"] if cu is None else cu[-1]
@@ -398,7 +413,9 @@ def arm_config(cfg, args, world, cu=None):
                 "count": len(cu) - 1, "lengths": [b - a for a, b in zip(cu, cu[1:])],
                 "mix": "log-uniform in [512, 16384] tokens, seeded"},
             "conv": "fused into target GEMM" if args.fused_conv else "own kernel",
-            "schedule": "dual (scores Z Z^T)" if args.dual else "primal walk",
+            "schedule": ("dual (scores Z Z^T), forced" if args.dual else
+                         "dual (scores Z Z^T), chosen for short sequences"
+                         if dual_form(cfg, args, cu) else "primal walk"),
             "eta_tok": "per-token rates" if args.eta_tok else None,
             "update_rule": "L2-normalised rows" if args.l2norm else "additive",
             "launch": "CUDA graph replay" if getattr(args, "graph", False) else "eager",
@@ -539,7 +556,7 @@ def main():
     if args.seq_shards:
         if world > 1:
             raise SystemExit("--seq-shards runs its spans in turn on one GPU: one rank only")
-        if args.packed or args.l2norm or args.dual:
+        if args.packed or args.l2norm or args.dual or dual_form(cfg, args):
             raise SystemExit("--seq-shards needs regular sequences and the additive update")
         return run_seq_shards(args, cfg, (H, X0, Wg, Wu, W0, Wt, cw), stream, dev, peaks,
                               peak_src, rates, local, cpu)
@@ -549,13 +566,15 @@ def main():
         if cu is not None:
             raise SystemExit("--graph: packed documents stage host tables and cannot be captured")
         ws_bytes = ittt.workspace_bytes_ex(B, T, d, f, C, fused_conv=args.fused_conv,
-                                           dual=args.dual, l2norm=args.l2norm,
+                                           dual=args.dual, primal=args.primal,
+                                           l2norm=args.l2norm,
                                            eta_tok=rates)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
     def step(events=None):
         ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, stream=stream, events=events,
-                     fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates, cu_seqlens=cu,
+                     fused_conv=args.fused_conv, dual=args.dual, primal=args.primal,
+                     eta_tok=rates, cu_seqlens=cu,
                      l2norm=args.l2norm, workspace=workspace)
 
     for _ in range(max(3, args.warmup)):
@@ -568,7 +587,8 @@ def main():
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             ittt.forward(H, X0, Wg, Wu, W0, Wt, cw, eta, C, out, fused_conv=args.fused_conv,
-                         dual=args.dual, eta_tok=rates, l2norm=args.l2norm, workspace=workspace)
+                         dual=args.dual, primal=args.primal, eta_tok=rates, l2norm=args.l2norm,
+                         workspace=workspace)
         for _ in range(max(3, args.warmup)):
             graph.replay()
         torch.cuda.synchronize(dev)
@@ -629,7 +649,11 @@ def main():
     if live:
         pass_ms[dominant] = sum(ev_dom[k][2 * di].elapsed_time(ev_dom[k][2 * di + 1])
                                 for k in range(args.steps)) / args.steps
-    model = phase_model(B, T, d, f, C, args.dual, cu)
+    form_dual = dual_form(cfg, args, cu)
+    assert form_dual == (ittt.plan_form(B, T, d, f, C, dual=args.dual, primal=args.primal,
+                                        fused_conv=args.fused_conv, l2norm=args.l2norm,
+                                        cu_seqlens=cu) == ittt.FORM_DUAL)
+    model = phase_model(B, T, d, f, C, form_dual, cu)
     phases = {}
     for name in ittt.PHASES:
         ms = pass_ms[name]
@@ -696,7 +720,8 @@ def main():
                 if k >= 2:
                     stream.wait_event(downloaded[j])  # O_j read back before reuse
                 ittt.forward(Hs[j], X0s[j], Wg, Wu, W0, Wt, cw, eta, C, Os[j], stream=stream,
-                             fused_conv=args.fused_conv, dual=args.dual, eta_tok=rates,
+                             fused_conv=args.fused_conv, dual=args.dual, primal=args.primal,
+                             eta_tok=rates,
                              cu_seqlens=cu, l2norm=args.l2norm)
                 computed[j].record(stream)
                 down.wait_event(computed[j])
@@ -743,7 +768,7 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": launches_per_step(B, T, C, cu, args.l2norm, args.dual) * args.steps,
+            "gpu_launches": launches_per_step(B, T, C, cu, args.l2norm, form_dual) * args.steps,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

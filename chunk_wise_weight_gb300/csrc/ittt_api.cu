@@ -321,8 +321,11 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   if (o.pad_mode != ITTT_PAD_CHUNK && o.pad_mode != ITTT_PAD_SEQUENCE)
     return fail(ITTT_ERR_INVALID_ARG, "pad_mode %d", int(o.pad_mode));
   if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV | ITTT_FLAG_DUAL | ITTT_FLAG_L2_NORM |
-                          ITTT_FLAG_SINGLE_CTA | ITTT_FLAG_UPDATE_ONLY | ITTT_FLAG_REUSE_ZV))
+                          ITTT_FLAG_SINGLE_CTA | ITTT_FLAG_UPDATE_ONLY | ITTT_FLAG_REUSE_ZV |
+                          ITTT_FLAG_PRIMAL))
     return fail(ITTT_ERR_INVALID_ARG, "unknown flags 0x%x", unsigned(o.flags));
+  if ((o.flags & ITTT_FLAG_DUAL) && (o.flags & ITTT_FLAG_PRIMAL))
+    return fail(ITTT_ERR_INVALID_ARG, "ITTT_FLAG_DUAL and ITTT_FLAG_PRIMAL exclude each other");
   P->B = B;
   P->T = T;
   P->d = d;
@@ -333,6 +336,14 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   P->dual = (o.flags & ITTT_FLAG_DUAL) != 0;
   P->packed = o.cu_seqlens != nullptr;
   P->l2norm = (o.flags & ITTT_FLAG_L2_NORM) != 0;
+  // Form choice by measured cost: the dual form for short sequences, where
+  // the walk's per-chunk d x f snapshots cost more than the dual form's
+  // T^2 terms (crossover near T = 2 d f / (d + f) on GB300).
+  if (!P->dual && !(o.flags & ITTT_FLAG_PRIMAL) && !P->fused && !P->packed && !P->l2norm &&
+      o.state_out == nullptr && o.snap_buf == nullptr && !(o.flags & ITTT_FLAG_UPDATE_ONLY) &&
+      chunk % 64 == 0 && T % chunk == 0 && T / chunk >= 2 &&
+      double(T) * double(d + f) < 2.0 * double(d) * double(f))
+    P->dual = true;
   if (P->l2norm && P->dual)
     return fail(ITTT_ERR_UNSUPPORTED,
                 "the normalised update has no dual form (the update is not additive)");
@@ -964,6 +975,20 @@ ittt_status ittt_state_prefix(const ittt_tensor* W_start, const ittt_tensor* del
 
 void ittt_set_scratch_limit(size_t bytes) { g_scratch_limit.store(bytes); }
 
+int32_t ittt_plan_form(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
+                       const ittt_opts* opts) {
+  const std::string saved = g_last_error;
+  ittt_opts o;
+  memset(&o, 0, sizeof(o));
+  if (opts) o = *opts;
+  Plan P;
+  if (make_plan(B, T, d, f, chunk, o, false, &P) != ITTT_OK) {
+    g_last_error = saved;
+    return -1;
+  }
+  return P.dual ? ITTT_FORM_DUAL : ITTT_FORM_PRIMAL;
+}
+
 size_t ittt_workspace_bytes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk) {
   return ittt_workspace_bytes_ex(B, T, d, f, chunk, nullptr);
 }
@@ -1014,9 +1039,10 @@ int32_t ittt_launch_count(int64_t B, int64_t T, int64_t d, int64_t f, int64_t ch
     g_last_error = saved;
     return 0;
   }
-  // conv, target, gate/up, update (when a chunk updates), apply; with a
-  // shared bf16 W_down0 and no snapshot buffer the apply reads W_0 itself,
-  // so no snapshot-0 copy is launched
+  // conv, target, gate/up, update (when a chunk updates), apply -- or, in
+  // the dual form (which needs two chunks or more), conv, target, gate/up,
+  // scores, dual apply; with a shared bf16 W_down0 and no snapshot buffer
+  // neither form copies W_0
   return ((T + chunk - 1) / chunk > 1) ? 5 : 4;
 }
 

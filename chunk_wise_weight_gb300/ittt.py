@@ -28,6 +28,8 @@ FLAG_L2_NORM = 4
 FLAG_SINGLE_CTA = 8
 FLAG_UPDATE_ONLY = 16
 FLAG_REUSE_ZV = 32
+FLAG_PRIMAL = 64
+FORM_PRIMAL, FORM_DUAL = 0, 1
 
 _DTYPES = {torch.bfloat16: BF16, torch.float32: FP32}
 
@@ -93,6 +95,8 @@ def load(path: str | None = None):
     lib.ittt_state_prefix.restype = ctypes.c_int
     lib.ittt_set_scratch_limit.argtypes = [ctypes.c_size_t]
     lib.ittt_set_scratch_limit.restype = None
+    lib.ittt_plan_form.argtypes = [ctypes.c_int64] * 5 + [ctypes.POINTER(Opts)]
+    lib.ittt_plan_form.restype = ctypes.c_int32
     _lib = lib
     return lib
 
@@ -151,13 +155,14 @@ def _seqlens(cu_seqlens):
 
 
 def _opts(pad_mode, fused_conv, dual, cu_seqlens, keep: dict, l2norm=False,
-          single_cta=False, update_only=False, reuse_zv=False, **tensors) -> Opts:
+          single_cta=False, update_only=False, reuse_zv=False, primal=False,
+          **tensors) -> Opts:
     opts = Opts()
     opts.pad_mode = int(pad_mode)
     opts.flags = ((FLAG_FUSED_CONV if fused_conv else 0) | (FLAG_DUAL if dual else 0)
                   | (FLAG_L2_NORM if l2norm else 0) | (FLAG_SINGLE_CTA if single_cta else 0)
                   | (FLAG_UPDATE_ONLY if update_only else 0)
-                  | (FLAG_REUSE_ZV if reuse_zv else 0))
+                  | (FLAG_REUSE_ZV if reuse_zv else 0) | (FLAG_PRIMAL if primal else 0))
     for name, t in tensors.items():
         if t is not None:
             keep[name] = describe(t)
@@ -176,7 +181,7 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
             vhat_buf=None, snap_buf=None, workspace=None, events=None,
             fused_conv: bool = False, dual: bool = False, eta_tok=None,
             cu_seqlens=None, l2norm: bool = False, single_cta: bool = False,
-            update_only: bool = False, reuse_zv: bool = False):
+            update_only: bool = False, reuse_zv: bool = False, primal: bool = False):
     """Enqueue one layer forward on `stream` (default: current stream) and
     return `out` [B,T,d].  Extra keyword buffers map to ittt_opts; `events`
     is a list of 2 * len(PHASES) torch.cuda.Event(enable_timing=True) or
@@ -184,7 +189,9 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
     offsets) packs documents into the one row of H [1,T,d].
     `update_only` folds every chunk into `state_out` and applies nothing
     (returns None; W_down0 None starts from zero); `reuse_zv` takes Z and
-    eta * Vhat from `z_buf` / `vhat_buf` instead of computing them."""
+    eta * Vhat from `z_buf` / `vhat_buf` instead of computing them.  The
+    library picks the primal or dual form by measured cost (plan_form);
+    `dual` / `primal` force one."""
     lib = load()
     if update_only:
         out = None
@@ -194,7 +201,7 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
     extra = {}
     opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, extra, l2norm=l2norm,
                  single_cta=single_cta, update_only=update_only, reuse_zv=reuse_zv,
-                 state_in=state_in,
+                 primal=primal, state_in=state_in,
                  state_out=state_out, z_buf=z_buf, vhat_buf=vhat_buf, snap_buf=snap_buf,
                  eta_tok=eta_tok)
     if workspace is not None:
@@ -263,15 +270,27 @@ def workspace_bytes(B: int, T: int, d: int, f: int, chunk: int) -> int:
 def workspace_bytes_ex(B: int, T: int, d: int, f: int, chunk: int, *, pad_mode: int = PAD_CHUNK,
                        fused_conv: bool = False, dual: bool = False, cu_seqlens=None,
                        l2norm: bool = False, update_only: bool = False, reuse_zv: bool = False,
-                       **buffers) -> int:
+                       primal: bool = False, **buffers) -> int:
     """ittt_workspace_bytes_ex: scratch for a forward call with these
     options; `buffers` name the ittt_opts tensors the call passes (state_in,
     state_out, z_buf, vhat_buf, snap_buf, eta_tok) -- only whether each is
     given matters."""
     keep = {}
     opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, keep, l2norm=l2norm,
-                 update_only=update_only, reuse_zv=reuse_zv, **buffers)
+                 update_only=update_only, reuse_zv=reuse_zv, primal=primal, **buffers)
     return int(load().ittt_workspace_bytes_ex(B, T, d, f, chunk, ctypes.byref(opts)))
+
+
+def plan_form(B: int, T: int, d: int, f: int, chunk: int, *, pad_mode: int = PAD_CHUNK,
+              fused_conv: bool = False, dual: bool = False, cu_seqlens=None,
+              l2norm: bool = False, update_only: bool = False, reuse_zv: bool = False,
+              primal: bool = False, **buffers) -> int:
+    """ittt_plan_form: FORM_PRIMAL or FORM_DUAL for a call with these sizes
+    and options (-1 if it would be rejected)."""
+    keep = {}
+    opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, keep, l2norm=l2norm,
+                 update_only=update_only, reuse_zv=reuse_zv, primal=primal, **buffers)
+    return int(load().ittt_plan_form(B, T, d, f, chunk, ctypes.byref(opts)))
 
 
 def launch_count(B: int, T: int, d: int, f: int, chunk: int) -> int:

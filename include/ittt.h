@@ -209,6 +209,22 @@ typedef struct {
  * conv, target and gate/up phases are skipped.  H, X0, W_gate, W_up,
  * W_target and conv_w are checked for shape but not read. */
 #define ITTT_FLAG_REUSE_ZV 32
+/* Never use the dual form (see "Form choice" below). */
+#define ITTT_FLAG_PRIMAL 64
+
+/*
+ * Form choice.  Without ITTT_FLAG_DUAL or ITTT_FLAG_PRIMAL a call uses the
+ * dual form when it can (regular sequences, chunk a multiple of 64 dividing
+ * T, at least two chunks, no state_out, snap_buf, packed documents,
+ * ITTT_FLAG_L2_NORM or ITTT_FLAG_FUSED_CONV) and its sequences are short:
+ * T < 2 d f / (d + f) tokens.  The primal walk writes and re-reads one d x f
+ * weight snapshot per chunk whatever the chunk's length, while the dual
+ * form's extra work grows with T^2; measured on GB300 the dual form was
+ * faster below that length (4.3x at 64 x 256 tokens, 1.2x at 8 x 2048 for
+ * d 2560, f 9728) and slower above it (6x at 2 x 32768).  Both forms compute
+ * the same layer; they round differently.  ittt_plan_form says which form a
+ * call would use.
+ */
 
 /* Kernel phases of one forward call, in launch order. */
 typedef enum {
@@ -314,6 +330,13 @@ ITTT_API size_t ittt_workspace_bytes(int64_t B, int64_t T, int64_t d, int64_t f,
 ITTT_API size_t ittt_workspace_bytes_ex(int64_t B, int64_t T, int64_t d, int64_t f,
                                         int64_t chunk, const ittt_opts* opts);
 
+/* Form a call with these sizes and options would run: ITTT_FORM_PRIMAL or
+ * ITTT_FORM_DUAL, or -1 if the call would be rejected.  opts may be NULL. */
+#define ITTT_FORM_PRIMAL 0
+#define ITTT_FORM_DUAL 1
+ITTT_API int32_t ittt_plan_form(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
+                                const ittt_opts* opts);
+
 /*
  * Caps the device scratch one call may allocate (bytes; 0, the default,
  * means no cap) for every later call in this process: a call that would
@@ -343,7 +366,8 @@ ITTT_API int32_t ittt_version(void);
  * Kernel launches one ittt_forward / ittt_forward_ex call makes for these
  * sizes with default options and a bf16 W_down0 (for launch accounting; 0
  * if unsupported): conv, target, gate/up, the update walk when a chunk
- * updates, apply.  An fp32 W_down0, state_in or snap_buf adds the snapshot-0
+ * updates, apply (the dual form's scores and dual apply in their place when
+ * the call chooses it: the same count).  An fp32 W_down0, state_in or snap_buf adds the snapshot-0
  * copy; packed documents add the table staging kernel; ITTT_FLAG_L2_NORM
  * launches the walk once per updating chunk plus a finalising launch.
  */

@@ -126,7 +126,7 @@ def test_rejects_bad_options(lib):
     o.pad_mode = 7
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     o = ittt.Opts()
-    o.flags = 64
+    o.flags = 128
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     assert "flags" in ittt.last_error()
     o = ittt.Opts()
@@ -379,3 +379,36 @@ def test_state_in_place_only_as_exact_alias(lib):
     assert "overlaps" in ittt.last_error()
     o.state_out = ctypes.pointer(st)                                   # the same buffer
     assert _call(lib, a, opts=o) != ittt.ERR_INVALID_ARG               # past validation
+
+
+def test_form_choice_by_sequence_length():
+    """The dual form for short sequences (T < 2 d f / (d + f)) where it is
+    allowed, the primal walk otherwise; DUAL / PRIMAL force one."""
+    P, D = ittt.FORM_PRIMAL, ittt.FORM_DUAL
+    cases = [
+        ((8, 2048, 2560, 9728, 512), D),      # 2048 < 4054
+        ((64, 256, 2560, 9728, 64), D),
+        ((4, 4096, 2560, 9728, 1024), P),     # 4096 > 4054
+        ((2, 32768, 2560, 9728, 2048), P),    # the bench workload
+        ((8, 1024, 1024, 3072, 256), D),      # 1024 < 1536
+        ((4, 2048, 1024, 3072, 512), P),
+        ((1, 256, 64, 256, 64), P),           # 256 > 102
+        ((8, 2048, 2560, 9728, 2048), P),     # one chunk: nothing to update
+        ((8, 2000, 2560, 9728, 500), P),      # chunk not a multiple of 64
+        ((8, 2048, 2560, 9728, 768), P),      # chunk does not divide T
+    ]
+    for args, want in cases:
+        assert ittt.plan_form(*args) == want, args
+        assert ittt.plan_form(*args, primal=True) == P
+        assert ittt.plan_form(*args, dual=True, primal=True) == -1
+    short = (8, 2048, 2560, 9728, 512)
+    fake = torch.empty(0)
+    for kw in ({"state_out": fake}, {"snap_buf": fake}, {"l2norm": True}, {"fused_conv": True},
+               {"cu_seqlens": [0, 8192, 16384]}):
+        if "cu_seqlens" in kw:
+            assert ittt.plan_form(1, 16384, 2560, 9728, 512, **kw) == P
+        else:
+            assert ittt.plan_form(*short, **kw) == P, kw
+    # the plan's scratch is the dual form's: no snapshots, the scores instead
+    assert ittt.workspace_bytes(*short) == ittt.workspace_bytes_ex(*short, dual=True)
+    assert ittt.workspace_bytes(*short) != ittt.workspace_bytes_ex(*short, primal=True)

@@ -40,3 +40,29 @@ def test_launch_accounting_matches_the_library():
     for B, T, C in ((2, 32768, 2048), (1, 8192, 1024), (1, 256, 256), (1, 1000, 512)):
         assert bench.launches_per_step(B, T, C, None, False) == ittt.launch_count(B, T, 2560,
                                                                                  9728, C)
+
+
+def test_bench_form_rule_matches_the_library():
+    """The bench names the form a call runs from its own copy of the rule
+    (the reference arm never loads the CUDA library): it must agree with
+    ittt_plan_form."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    from chunk_wise_weight_gb300 import build, ittt
+    build.build()
+    for B, T, d, f, C in ((8, 2048, 2560, 9728, 512), (4, 4096, 2560, 9728, 1024),
+                          (2, 32768, 2560, 9728, 2048), (64, 256, 2560, 9728, 64),
+                          (8, 1024, 1024, 3072, 256), (4, 2048, 1024, 3072, 512),
+                          (1, 256, 64, 256, 64), (8, 2000, 2560, 9728, 500),
+                          (8, 2048, 2560, 9728, 2048), (4, 512, 512, 1024, 128)):
+        cfg = dict(B=B, T=T, d=d, f=f, C=C)
+        for flags in ({}, {"dual": True}, {"primal": True}, {"l2norm": True},
+                      {"fused_conv": True}):
+            args = argparse.Namespace(dual=False, primal=False, l2norm=False, fused_conv=False)
+            for k, v in flags.items():
+                setattr(args, k, v)
+            form = ittt.plan_form(B, T, d, f, C, **flags)
+            if form < 0:
+                continue  # the library rejects the call (e.g. a forced dual form)
+            assert bench.dual_form(cfg, args) == (form == ittt.FORM_DUAL), (cfg, flags)

@@ -602,7 +602,25 @@ def _sampled_checks(index, device, n_state_pairs=24, n_rows=6, dual=False, shape
     ittt.forward_plain(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
                        g["conv_w"], eta, C, plain)
     ittt.stream_status()
-    assert torch.equal(plain, got["O"]), "bench launch path differs from the checked one"
+    if ittt.plan_form(B, T, d, f, C) == ittt.FORM_PRIMAL:
+        assert torch.equal(plain, got["O"]), "bench launch path differs from the checked one"
+    else:
+        # Short sequences: the plain call runs the dual form (the checks
+        # below follow the walk, which the snapshot buffer selects).  It is
+        # the forced dual form bit for bit, its first-chunk rows match the
+        # oracle, and it agrees with the walk within twice the bar (the two
+        # forms round differently, each within the bar of the exact result).
+        dual = ittt.forward(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"],
+                            g["W_target"], g["conv_w"], eta, C, dual=True)
+        ittt.stream_status()
+        assert torch.equal(plain, dual)
+        assert rel_fro(host(plain), host(got["O"])) <= 2 * REL_FRO
+        for b in sorted({0, B - 1}):
+            rows = np.array([0, 1, C // 2, C - 1])
+            assert_parity(host(plain[b][torch.as_tensor(rows)]),
+                          oracle.first_chunk_rows(inp["H"][b], inp["W_gate"], inp["W_up"],
+                                                  inp["W_down0"], rows),
+                          f"dual-form O chunk 0 [b={b}]")
     rng = np.random.default_rng(1000 + index)
     for b in sorted({0, B - 1}):
         H, X0 = inp["H"][b], inp["X0"][b]
@@ -1070,3 +1088,25 @@ def test_state_updated_in_place(cuda_device, l2norm, update_only, packed):
     call(buf, buf)
     ittt.stream_status()
     assert torch.equal(buf, sep2)
+
+
+def test_form_chosen_by_sequence_length(cuda_device):
+    """Short sequences take the dual form by default (d 512, f 1024: below
+    T = 683 tokens); both forms match the oracle, the default is the dual
+    form bit for bit, and forcing the primal form gives the walk."""
+    B, T, d, f, C, eta = 4, 512, 512, 1024, 128, 0.05
+    assert ittt.plan_form(B, T, d, f, C) == ittt.FORM_DUAL
+    inp = make_inputs(B, T, d, f, seed=2500)
+    ref = oracle.forward(inp, eta, C)
+    g = to_device(inp, cuda_device)
+    args = (g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"], g["conv_w"],
+            eta, C)
+    auto = ittt.forward(*args)
+    dual = ittt.forward(*args, dual=True)
+    primal = ittt.forward(*args, primal=True)
+    ittt.stream_status()
+    assert torch.equal(auto, dual)
+    assert_parity(host(auto), ref["O"], "O (dual form, chosen)")
+    assert_parity(host(primal), ref["O"], "O (primal form, forced)")
+    walk = run(g, eta, C, intermediates=True)["O"]   # snapshots requested: the walk
+    assert torch.equal(primal, walk)
