@@ -11,9 +11,11 @@
 //   apply GEMM (O).
 // The GEMMs run on CTA pairs where two can be resident (and the update walk
 // when every updated chunk is a multiple of 64 tokens), else on single CTAs.
-// With ITTT_FLAG_FUSED_CONV the target GEMM computes the conv itself; with
-// ITTT_FLAG_DUAL scores Z Z^T and the dual apply replace walk and apply; with
-// ITTT_FLAG_L2_NORM the walk runs one launch per chunk.  (Run beside the
+// With ITTT_FLAG_FUSED_CONV the target GEMM computes the conv itself; in the
+// dual form (forced by ITTT_FLAG_DUAL, or chosen by the planner for short
+// sequences, T < 2 d f / (d + f), where it measured faster) scores Z Z^T and
+// the dual apply replace walk and apply; with ITTT_FLAG_L2_NORM the walk runs
+// one launch per chunk.  (Run beside the
 // gate/up GEMM on a second stream, the conv slowed that GEMM by more than its
 // own 0.2 ms at the 32k-token workload, so it runs in line.)  No host
 // synchronisation happens inside a forward call; the packed-document staging
