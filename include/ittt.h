@@ -272,7 +272,9 @@ ITTT_API ittt_status ittt_forward_ex(const ittt_tensor* H, const ittt_tensor* X0
  * process whose device memory belongs to another framework's caching
  * allocator, a real-time path that forbids allocation after start-up.
  * The pages have no counterpart: this is a deployment variant of
- * ittt_forward with the same arguments, kernels and results.
+ * ittt_forward with the same arguments and kernels, always in the primal form
+ * (ittt_forward picks the dual form for short sequences; the two round
+ * differently).
  *
  * It calls no allocating routine.  Its scratch lives in one library-wide
  * device array of ITTT_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU which
