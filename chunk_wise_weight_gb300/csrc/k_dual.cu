@@ -17,8 +17,10 @@
 //           descriptors change inside the accumulation.
 // The dual form does no state update at all, and its work grows with the
 // square of the context: per chunk i it costs 2*C*d*f + i*2*C^2*(d + f)
-// FLOPs against 4*C*d*f for the primal apply and update, so the primal walk
-// is the default schedule.
+// FLOPs against 4*C*d*f for the primal apply and update -- but it writes no
+// d x f snapshot per chunk, so it wins on short sequences (the planner picks
+// it below T = 2 d f / (d + f)).  Units are 128-row tiles of one chunk: with
+// 64-token chunks half of each tile's rows are computed and dropped.
 #include "kernels.h"
 #include "pipeline.cuh"
 

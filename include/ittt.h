@@ -174,9 +174,9 @@ typedef struct {
  * (Z_[i] Z_[j]^T) Vhat_[j] instead of walking the fast-weight state: a
  * scores kernel writes the block-lower part of Z Z^T (bf16, B*T*T*2 bytes of
  * scratch) and one GEMM accumulates both terms.  Same layer, different
- * rounding; more work than the primal walk on every workload measured, so
- * it is never the default.  Not combinable with state_out or snap_buf; chunk
- * must be a multiple of 64 that divides T. */
+ * rounding.  Forces the form a call would otherwise choose by sequence
+ * length (see "Form choice" below).  Not combinable with state_out or
+ * snap_buf; chunk must be a multiple of 64 that divides T. */
 #define ITTT_FLAG_DUAL 2
 /* Normalise the fast weight after every update, row by row over its d_ff
  * inputs: W_{i+1} = L2-Normalize(W_i + eta Vhat_[i]^T Z_[i]) with
