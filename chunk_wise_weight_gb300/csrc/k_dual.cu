@@ -5,22 +5,25 @@
 // the block-causal mask view of apply/update orderings in "[논문리뷰]
 // Test-Time Training Done Right", "Apply 연산과 Update 연산의 실행 순서").
 //
-// Two tcgen05 kernels:
-//   scores: S[t, s] = Z_t . Z_s for every token s of an earlier chunk than t
-//           (a 128 x 256 tile per unit, K = d_ff), rounded once to bf16 into
-//           a [B, T, T] buffer whose strictly block-lower part is the only
-//           part ever written or read;
+// Both kernels tile the token axis in 128-row tiles that may span chunk
+// edges (chunks are multiples of 64 tokens).  A tile's rows read the scores
+// of every token before the first token of its LAST row's chunk, s_end:
+//   scores: S[t, s] = Z_t . Z_s for s < s_end of t's tile, where s lies in
+//           an earlier chunk than t, and 0 where it does not (t's own chunk
+//           inside the tile's range), in a 128 x 256 tile per unit (K =
+//           d_ff), rounded once to bf16 into a [B, T, T] buffer of which
+//           only those entries are ever written or read;
 //   apply:  one accumulator per 128 x 256 output tile takes first
-//           Z_[i] W_0^T (K = d_ff, both operands K-major) and then
-//           S_[i] (eta Vhat) over the tokens of chunks 0..i-1 (S K-major,
-//           eta*Vhat read MN-major), so the instruction and shared-memory
-//           descriptors change inside the accumulation.
+//           Z W_0^T (K = d_ff, both operands K-major) and then S (eta Vhat)
+//           over the tokens s < s_end (S K-major, eta*Vhat read MN-major),
+//           so the instruction and shared-memory descriptors change inside
+//           the accumulation; the zero scores add nothing to a row whose
+//           chunk starts before s_end.
 // The dual form does no state update at all, and its work grows with the
 // square of the context: per chunk i it costs 2*C*d*f + i*2*C^2*(d + f)
 // FLOPs against 4*C*d*f for the primal apply and update -- but it writes no
 // d x f snapshot per chunk, so it wins on short sequences (the planner picks
-// it below T = 2 d f / (d + f)).  Units are 128-row tiles of one chunk: with
-// 64-token chunks half of each tile's rows are computed and dropped.
+// it below T = 2 d f / (d + f)).
 #include "kernels.h"
 #include "pipeline.cuh"
 
@@ -40,8 +43,15 @@ struct ScoresParams {
   CUtensorMap tm_zq;    // Z [B*T, f] box {64, 128}  (rows t)
   CUtensorMap tm_zk;    // Z [B*T, f] box {64, 256}  (rows s)
   __nv_bfloat16* s;     // [B, T, T]
-  int B, T, C, n, mtpc, nt_max, kblocks;
+  int B, T, C, n, mts, nt_max, kblocks;  // mts: 128-row tiles of a sequence
 };
+
+// First token of the chunk of a 128-row tile's last row: the scores the
+// tile's rows read are those of tokens s < tile_s_end.
+__device__ __forceinline__ int tile_s_end(int t0, int T, int C) {
+  const int last = min(t0 + kBM, T) - 1;
+  return (last / C) * C;
+}
 
 struct ScoresSched : SchedDefaults {
   using Params = ScoresParams;
@@ -52,21 +62,20 @@ struct ScoresSched : SchedDefaults {
   bool live = false;
 
   __device__ explicit ScoresSched(const Params& pp) : p(pp) {}
-  __device__ int num_units() const { return p.B * (p.n - 1) * p.mtpc * p.nt_max; }
+  __device__ int num_units() const { return p.B * p.mts * p.nt_max; }
   __device__ void begin_unit(int u, int local) {
     const int nt = u % p.nt_max;
-    int r = u / p.nt_max;
-    const int mt = r % p.mtpc;
-    r /= p.mtpc;
-    const int i = 1 + r % (p.n - 1);
-    b = r / (p.n - 1);
-    t0 = i * p.C + mt * kBM;
+    const int r = u / p.nt_max;
+    const int mt = r % p.mts;
+    b = r / p.mts;
+    t0 = mt * kBM;
     s0 = nt * kBN;
-    live = s0 < i * p.C;  // only tokens of earlier chunks
+    const int s_end = tile_s_end(t0, p.T, p.C);
+    live = s0 < s_end;  // only tokens before the tile's last chunk
     arow0 = b * p.T + t0;
     brow0 = b * p.T + s0;
-    rows_valid = min(kBM, p.C - mt * kBM);
-    cols_valid = min(kBN, i * p.C - s0);
+    rows_valid = min(kBM, p.T - t0);
+    cols_valid = min(kBN, s_end - s0);
     acc = local & 1;
   }
   __device__ int num_segments() const { return live ? 1 : 0; }
@@ -81,9 +90,15 @@ struct ScoresSched : SchedDefaults {
   static __device__ uint64_t a_desc(uint32_t base, int k) { return kmajor_desc(base, k); }
   static __device__ uint64_t b_desc(uint32_t base, int k) { return kmajor_desc(base, k); }
 
+  // Row t keeps the scores of tokens before its own chunk; the rest of the
+  // tile's range (t's chunk, when a later chunk's row shares the tile) is
+  // written as zeros.  Chunks are multiples of 64 tokens, so an 8-column
+  // group lies wholly on one side.
   __device__ void epilogue(int, int row, uint32_t trow) const {
     const bool row_ok = row < rows_valid;
-    __nv_bfloat16* srow = p.s + (size_t(b) * p.T + size_t(t0 + (row_ok ? row : 0))) * size_t(p.T);
+    const int t = t0 + (row_ok ? row : 0);
+    const int own = (t / p.C) * p.C;  // first token of t's chunk
+    __nv_bfloat16* srow = p.s + (size_t(b) * p.T + size_t(t)) * size_t(p.T);
 #pragma unroll 1
     for (int c = 0; c < kBN; c += 32) {
       uint32_t v[32];
@@ -95,11 +110,15 @@ struct ScoresSched : SchedDefaults {
       for (int q = 0; q < 4; ++q) {
         const int cc = c + 8 * q;
         if (cc < cols_valid) {
-          *reinterpret_cast<uint4*>(srow + s0 + cc) = make_uint4(
-              pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-              pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-              pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-              pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+          const uint4 val =
+              (s0 + cc < own)
+                  ? make_uint4(
+                        pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                        pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])))
+                  : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(srow + s0 + cc) = val;
         }
       }
     }
@@ -114,7 +133,7 @@ struct DualParams {
   void* out;
   int out_fp32;
   int w0_per_seq;
-  int B, T, d, C, n, mtpc, nt, kf;
+  int B, T, d, C, n, mts, nt, kf;  // mts: 128-row tiles of a sequence
 };
 
 struct DualSched : SchedDefaults {
@@ -125,27 +144,27 @@ struct DualSched : SchedDefaults {
   static constexpr uint32_t kIdesc = kIdescKK;
 
   const Params& p;
-  int b = 0, i = 0, arow0 = 0, n0 = 0, rows_valid = 0, acc = 0, wrow0 = 0;
+  int b = 0, s_end = 0, arow0 = 0, n0 = 0, rows_valid = 0, acc = 0, wrow0 = 0;
 
   __device__ explicit DualSched(const Params& pp) : p(pp) {}
-  __device__ int num_units() const { return p.B * p.n * p.mtpc * p.nt; }
-  // Latest chunks (longest K) first.
+  __device__ int num_units() const { return p.B * p.mts * p.nt; }
+  // Latest tiles (longest K) first.
   __device__ void begin_unit(int u, int local) {
     const int nt = u % p.nt;
-    int r = u / p.nt;
-    const int mt = r % p.mtpc;
-    r /= p.mtpc;
-    i = p.n - 1 - (r % p.n);
-    b = r / p.n;
-    arow0 = b * p.T + i * p.C + mt * kBM;
+    const int r = u / p.nt;
+    const int mt = p.mts - 1 - (r % p.mts);
+    b = r / p.mts;
+    const int t0 = mt * kBM;
+    s_end = tile_s_end(t0, p.T, p.C);
+    arow0 = b * p.T + t0;
     n0 = nt * kBN;
-    rows_valid = min(kBM, p.C - mt * kBM);
+    rows_valid = min(kBM, p.T - t0);
     wrow0 = (p.w0_per_seq ? b * p.d : 0) + n0;
     acc = local & 1;
   }
   __device__ int num_segments() const { return 1; }
   __device__ int seg_acc(int) const { return acc; }
-  __device__ int seg_kblocks(int) const { return p.kf + i * p.C / kBK; }
+  __device__ int seg_kblocks(int) const { return p.kf + s_end / kBK; }
   __device__ bool seg_fresh(int) const { return true; }
 
   __device__ void load(int, int kb, uint8_t* stage, uint64_t* bar) const {
@@ -225,11 +244,11 @@ cudaError_t launch_scores(const LaunchEnv& env, const CUtensorMap& tm_zq, const 
   p.T = T;
   p.C = C;
   p.n = T / C;
-  p.mtpc = (C + kBM - 1) / kBM;
+  p.mts = (T + kBM - 1) / kBM;
   p.nt_max = ((p.n - 1) * C + kBN - 1) / kBN;
   p.kblocks = (f + kBK - 1) / kBK;
   if (p.n < 2) return cudaSuccess;
-  const int64_t units = int64_t(B) * (p.n - 1) * p.mtpc * p.nt_max;
+  const int64_t units = int64_t(B) * p.mts * p.nt_max;
   cudaError_t e = cudaFuncSetAttribute(scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(pipe_smem_bytes<ScoresSched>()));
   if (e != cudaSuccess) return e;
@@ -255,10 +274,10 @@ cudaError_t launch_dual_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
   p.d = d;
   p.C = C;
   p.n = T / C;
-  p.mtpc = (C + kBM - 1) / kBM;
+  p.mts = (T + kBM - 1) / kBM;
   p.nt = (d + kBN - 1) / kBN;
   p.kf = (f + kBK - 1) / kBK;
-  const int64_t units = int64_t(B) * p.n * p.mtpc * p.nt;
+  const int64_t units = int64_t(B) * p.mts * p.nt;
   cudaError_t e = cudaFuncSetAttribute(dual_apply_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        int(pipe_smem_bytes<DualSched>()));
