@@ -293,15 +293,29 @@ def test_next_token_target_closed_form():
 # Hand-derived worked examples (tests/golden)
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["scalar_two_chunks.json", "next_token_d2_f1.json"])
+@pytest.mark.parametrize("name", ["scalar_two_chunks.json", "next_token_d2_f1.json",
+                                  "l2norm_d1_f2.json", "packed_two_documents.json"])
 def test_golden_worked_example(name):
     """Worked examples derived by hand from Method §1 eq. (2)-(3), §2 eq.
-    (5)-(6); each fixture carries its derivation and citation."""
+    (5)-(6) (and, where the fixture says so, the normalised update and
+    packed documents with the reset at document boundaries); each fixture
+    carries its derivation and citation."""
     with open(os.path.join(GOLDEN, name)) as fh:
         g = json.load(fh)
     inp = {k: torch.tensor(v, dtype=torch.float32) for k, v in g["inputs"].items()}
-    out = oracle.forward(inp, g["eta"], g["chunk"], g.get("pad_mode", 0),
-                         want_states=True, want_vhat=True)
+    l2 = g.get("l2norm", False)
+    if "cu_seqlens" in g:
+        out = oracle.forward_packed(inp, g["cu_seqlens"], g["eta"], g["chunk"],
+                                    g.get("pad_mode", 0), want_states=True, want_vhat=not l2,
+                                    l2norm=l2)
+        O, V = out["O"], out.get("Vhat")
+        states = out["states"]          # per document: [n_k + 1, d, f]
+    else:
+        out = oracle.forward(inp, g["eta"], g["chunk"], g.get("pad_mode", 0),
+                             want_states=True, want_vhat=not l2, l2norm=l2)
+        O, V = out["O"][0], out.get("Vhat")
+        V = None if V is None else V[0]
+        states = [out["states"][0]]
     env = {"math": math}
     for name_, expr in g.get("let", {}).items():
         env[name_] = _ev(expr, env)
@@ -310,10 +324,14 @@ def test_golden_worked_example(name):
         return np.array([[_ev(e, env) for e in row] for row in rows], dtype=np.float64)
 
     if "Vhat" in g["expected"]:
-        np.testing.assert_allclose(out["Vhat"][0], mat(g["expected"]["Vhat"]), rtol=1e-14, atol=0)
-    np.testing.assert_allclose(out["O"][0], mat(g["expected"]["O"]), rtol=1e-13, atol=1e-15)
-    for i, st in enumerate(g["expected"]["states"]):
-        np.testing.assert_allclose(out["states"][0, i], mat(st), rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(V, mat(g["expected"]["Vhat"]), rtol=1e-14, atol=0)
+    np.testing.assert_allclose(O, mat(g["expected"]["O"]), rtol=1e-13, atol=1e-15)
+    exp_states = g["expected"]["states"]
+    if "cu_seqlens" not in g:
+        exp_states = [exp_states]
+    for k, doc in enumerate(exp_states):
+        for i, st in enumerate(doc):
+            np.testing.assert_allclose(states[k][i], mat(st), rtol=1e-13, atol=1e-15)
 
 
 def _ev(e, env):
