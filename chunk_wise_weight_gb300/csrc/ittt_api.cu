@@ -712,7 +712,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if ((s = make_map(&tm_vmn, vhat, d, M, 64, 64, "Vhat"))) return s;
   if ((s = make_map(&tm_zmn, z, f, M, 64, 64, "Z (update)"))) return s;
   if ((s = make_map(&tm_zk, z, f, M, 64, 128, "Z (apply)"))) return s;
-  CUtensorMap tm_zs, tm_w0b, tm_sc, tm_snap_pair, tm_w0d, tm_w0d_pair;
+  CUtensorMap tm_zs, tm_w0b, tm_w0b_pair, tm_sc, tm_snap_pair, tm_w0d, tm_w0d_pair;
   // The apply reads a shared bf16 W_0 itself for first chunks, so slot 0 of
   // each document need not be copied (unless the caller asked for the
   // snapshots).
@@ -722,6 +722,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if (dual) {
     if ((s = make_map(&tm_zs, z, f, M, 64, 256, "Z (scores)"))) return s;
     if ((s = make_map(&tm_w0b, w0b, f, uint64_t((o.state_in ? B : 1) * d), 64, 256, "bf16 W_0")))
+      return s;
+    if ((s = make_map(&tm_w0b_pair, w0b, f, uint64_t((o.state_in ? B : 1) * d), 64, 128,
+                      "bf16 W_0 (pair)")))
       return s;
     if ((s = make_map(&tm_sc, scores, uint64_t(T), M, 64, 128, "scores"))) return s;
   } else if (update_only) {
@@ -887,9 +890,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
               "scores launch");
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");
-    ITTT_STEP(ittt::launch_dual_apply(env, tm_zk, tm_w0b, tm_sc, tm_vmn, o.state_in != nullptr,
-                                      out->data, out->dtype == ITTT_FP32, int(B), int(T), int(d),
-                                      int(f), int(chunk)),
+    ITTT_STEP(ittt::launch_dual_apply(env, tm_zk, tm_w0b, tm_w0b_pair, tm_sc, tm_vmn,
+                                      o.state_in != nullptr, out->data, out->dtype == ITTT_FP32,
+                                      int(B), int(T), int(d), int(f), int(chunk), !single),
               "dual apply launch");
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY + 1, stream), "event record");
   }

@@ -5,20 +5,23 @@
 // the block-causal mask view of apply/update orderings in "[논문리뷰]
 // Test-Time Training Done Right", "Apply 연산과 Update 연산의 실행 순서").
 //
-// Both kernels tile the token axis in 128-row tiles that may span chunk
-// edges (chunks are multiples of 64 tokens).  A tile's rows read the scores
-// of every token before the first token of its LAST row's chunk, s_end:
-//   scores: S[t, s] = Z_t . Z_s for s < s_end of t's tile, where s lies in
+// Both kernels tile the token axis in tiles that may span chunk edges
+// (chunks are multiples of 64 tokens).  The rows of a 256-row group read the
+// scores of every token before the first token of the group's LAST row's
+// chunk, s_end:
+//   scores: S[t, s] = Z_t . Z_s for s < s_end of t's group, where s lies in
 //           an earlier chunk than t, and 0 where it does not (t's own chunk
-//           inside the tile's range), in a 128 x 256 tile per unit (K =
+//           inside the group's range), in a 128 x 256 tile per unit (K =
 //           d_ff), rounded once to bf16 into a [B, T, T] buffer of which
 //           only those entries are ever written or read;
-//   apply:  one accumulator per 128 x 256 output tile takes first
-//           Z W_0^T (K = d_ff, both operands K-major) and then S (eta Vhat)
-//           over the tokens s < s_end (S K-major, eta*Vhat read MN-major),
-//           so the instruction and shared-memory descriptors change inside
-//           the accumulation; the zero scores add nothing to a row whose
-//           chunk starts before s_end.
+//   apply:  one accumulator per 256 x 256 output tile on a CTA pair (each
+//           CTA 128 rows; 128 x 256 tiles on single CTAs where no pair fits)
+//           takes first Z W_0^T (K = d_ff, both operands K-major) and then
+//           S (eta Vhat) over the tokens s < s_end (S K-major, eta*Vhat read
+//           MN-major), so the instruction and shared-memory descriptors
+//           change inside the accumulation; the zero scores add nothing to
+//           a row whose chunk starts before s_end, so both tilings give the
+//           same sums.
 // The dual form does no state update at all, and its work grows with the
 // square of the context: per chunk i it costs 2*C*d*f + i*2*C^2*(d + f)
 // FLOPs against 4*C*d*f for the primal apply and update -- but it writes no
@@ -26,6 +29,7 @@
 // it below T = 2 d f / (d + f)).
 #include "kernels.h"
 #include "pipeline.cuh"
+#include "pipeline_pair.cuh"
 
 namespace ittt {
 namespace {
@@ -46,11 +50,18 @@ struct ScoresParams {
   int B, T, C, n, mts, nt_max, kblocks;  // mts: 128-row tiles of a sequence
 };
 
-// First token of the chunk of a 128-row tile's last row: the scores the
-// tile's rows read are those of tokens s < tile_s_end.
-__device__ __forceinline__ int tile_s_end(int t0, int T, int C) {
-  const int last = min(t0 + kBM, T) - 1;
+// First token of the chunk of the last row of the `rows`-row tile at t0:
+// the scores the tile's rows read are those of tokens s < that.
+__device__ __forceinline__ int tile_s_end(int t0, int rows, int T, int C) {
+  const int last = min(t0 + rows, T) - 1;
   return (last / C) * C;
+}
+
+// The scores kernel fills, for every row, the range its 256-row group reads
+// (the CTA-pair apply's tile; a 128-row tile of the single-CTA apply reads a
+// part of it).
+__device__ __forceinline__ int group_s_end(int t0, int T, int C) {
+  return tile_s_end(t0 - t0 % (2 * kBM), 2 * kBM, T, C);
 }
 
 struct ScoresSched : SchedDefaults {
@@ -70,8 +81,8 @@ struct ScoresSched : SchedDefaults {
     b = r / p.mts;
     t0 = mt * kBM;
     s0 = nt * kBN;
-    const int s_end = tile_s_end(t0, p.T, p.C);
-    live = s0 < s_end;  // only tokens before the tile's last chunk
+    const int s_end = group_s_end(t0, p.T, p.C);
+    live = s0 < s_end;  // only tokens before the 256-row group's last chunk
     arow0 = b * p.T + t0;
     brow0 = b * p.T + s0;
     rows_valid = min(kBM, p.T - t0);
@@ -127,14 +138,52 @@ struct ScoresSched : SchedDefaults {
 
 struct DualParams {
   CUtensorMap tm_z;   // Z        [B*T, f]   box {64, 128}
-  CUtensorMap tm_w0;  // bf16 W_0 [Bw*d, f]  box {64, 256}
+  CUtensorMap tm_w0;  // bf16 W_0 [Bw*d, f]  box {64, 256} (CTA pairs: {64, 128})
   CUtensorMap tm_s;   // scores   [B*T, T]   box {64, 128}
   CUtensorMap tm_v;   // eta*Vhat [B*T, d]   box {64, 64} (read MN-major)
   void* out;
   int out_fp32;
   int w0_per_seq;
-  int B, T, d, C, n, mts, nt, kf;  // mts: 128-row tiles of a sequence
+  int B, T, d, C, n, mts, mts2, nt, kf;  // mts, mts2: 128- and 256-row tiles of a sequence
 };
+
+// 256 output columns of row `row` of a tile at token row arow0 (rows past
+// rows_valid and columns past d are not written).
+__device__ __forceinline__ void dual_epilogue(const DualParams& p, int arow0, int rows_valid,
+                                              int n0, int row, uint32_t trow) {
+  const bool row_ok = row < rows_valid;
+  const size_t grow = size_t(arow0 + (row_ok ? row : 0));
+#pragma unroll 1
+  for (int c = 0; c < kBN; c += 32) {
+    uint32_t v[32];
+    tmem_ld_32cols(trow + uint32_t(c), v);
+    tmem_wait_ld();
+    pin_regs(v);
+    if (!row_ok) continue;
+    if (p.out_fp32) {
+      float* orow = static_cast<float*>(p.out) + grow * size_t(p.d);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int col = n0 + c + 4 * q;
+        if (col < p.d)
+          *reinterpret_cast<uint4*>(orow + col) =
+              make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    } else {
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * size_t(p.d);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int col = n0 + c + 8 * q;
+        if (col < p.d)
+          *reinterpret_cast<uint4*>(orow + col) = make_uint4(
+              pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+              pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+              pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+              pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+      }
+    }
+  }
+}
 
 struct DualSched : SchedDefaults {
   using Params = DualParams;
@@ -155,7 +204,7 @@ struct DualSched : SchedDefaults {
     const int mt = p.mts - 1 - (r % p.mts);
     b = r / p.mts;
     const int t0 = mt * kBM;
-    s_end = tile_s_end(t0, p.T, p.C);
+    s_end = tile_s_end(t0, kBM, p.T, p.C);
     arow0 = b * p.T + t0;
     n0 = nt * kBN;
     rows_valid = min(kBM, p.T - t0);
@@ -187,38 +236,66 @@ struct DualSched : SchedDefaults {
   }
 
   __device__ void epilogue(int, int row, uint32_t trow) const {
-    const bool row_ok = row < rows_valid;
-    const size_t grow = size_t(arow0 + (row_ok ? row : 0));
-#pragma unroll 1
-    for (int c = 0; c < kBN; c += 32) {
-      uint32_t v[32];
-      tmem_ld_32cols(trow + uint32_t(c), v);
-      tmem_wait_ld();
-      pin_regs(v);
-      if (!row_ok) continue;
-      if (p.out_fp32) {
-        float* orow = static_cast<float*>(p.out) + grow * size_t(p.d);
+    dual_epilogue(p, arow0, rows_valid, n0, row, trow);
+  }
+};
+
+// The same on CTA pairs: 256-row tiles (each CTA its 128 rows of Z or of the
+// scores, and 128 of the 256 output columns' W_0 rows or eta*Vhat columns),
+// both CTAs' rows sharing one scores range.
+struct DualPairSched : PairDefaults {
+  using Params = DualParams;
+  static constexpr bool kMixedOperands = true;
+  static constexpr uint32_t kIdescKK = idesc_bf16_f32(2 * kBM, kBN, false, false);
+  static constexpr uint32_t kIdescKM = idesc_bf16_f32(2 * kBM, kBN, false, true);
+  static constexpr uint32_t kIdesc = kIdescKK;
+
+  const Params& p;
+  const int rank;
+  int b = 0, s_end = 0, arow0 = 0, n0 = 0, rows_valid = 0, acc = 0, wrow0 = 0;
+
+  __device__ DualPairSched(const Params& pp, uint32_t r) : p(pp), rank(int(r)) {}
+  __device__ int num_units() const { return p.B * p.mts2 * p.nt; }
+  // Latest tiles (longest K) first.
+  __device__ void begin_unit(int u, int local) {
+    const int nt = u % p.nt;
+    const int r = u / p.nt;
+    const int mt = p.mts2 - 1 - (r % p.mts2);
+    b = r / p.mts2;
+    const int t0 = mt * (2 * kBM);
+    s_end = tile_s_end(t0, 2 * kBM, p.T, p.C);
+    const int r0 = t0 + rank * kBM;  // this CTA's first row in the sequence
+    arow0 = b * p.T + r0;
+    n0 = nt * kBN;
+    rows_valid = min(kBM, p.T - r0);  // <= 0: the tile ends in the other half
+    wrow0 = (p.w0_per_seq ? b * p.d : 0) + n0 + rank * kBM;
+    acc = local & 1;
+  }
+  __device__ int num_segments() const { return 1; }
+  __device__ int seg_acc(int) const { return acc; }
+  __device__ int seg_kblocks(int) const { return p.kf + s_end / kBK; }
+  __device__ bool seg_fresh(int) const { return true; }
+  __device__ void load(int, int kb, uint8_t* stage, uint32_t bar) const {
+    if (kb < p.kf) {
+      const int k = kb * kBK;
+      tma_load_2d_pair(stage, &p.tm_z, bar, k, arow0);
+      tma_load_2d_pair(stage + kPairATileBytes, &p.tm_w0, bar, k, wrow0);
+    } else {
+      const int s0 = (kb - p.kf) * kBK;  // token of an earlier chunk
+      tma_load_2d_pair(stage, &p.tm_s, bar, s0, arow0);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int col = n0 + c + 4 * q;
-          if (col < p.d)
-            *reinterpret_cast<uint4*>(orow + col) =
-                make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
-      } else {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * size_t(p.d);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int col = n0 + c + 8 * q;
-          if (col < p.d)
-            *reinterpret_cast<uint4*>(orow + col) = make_uint4(
-                pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
-        }
-      }
+      for (int q = 0; q < 2; ++q)
+        tma_load_2d_pair(stage + kPairATileBytes + q * kMnBox, &p.tm_v, bar,
+                         n0 + rank * kBM + 64 * q, b * p.T + s0);
     }
+  }
+  __device__ uint32_t idesc(int, int kb) const { return kb < p.kf ? kIdescKK : kIdescKM; }
+  __device__ uint64_t a_desc(int, int, uint32_t base, int k) const { return kmajor_desc(base, k); }
+  __device__ uint64_t b_desc(int, int kb, uint32_t base, int k) const {
+    return kb < p.kf ? kmajor_desc(base, k) : mnmajor_desc(base, k);
+  }
+  __device__ void epilogue(int, int row, uint32_t trow) const {
+    dual_epilogue(p, arow0, rows_valid, n0, row, trow);
   }
 };
 
@@ -230,6 +307,11 @@ __global__ void __launch_bounds__(PipeShape<ScoresSched>::kThreads, 1)
 __global__ void __launch_bounds__(PipeShape<DualSched>::kThreads, 1)
     dual_apply_kernel(const __grid_constant__ DualParams p, unsigned int* status) {
   run_pipeline<DualSched>(p, status);
+}
+
+__global__ void __launch_bounds__(kBaseThreads, 1)
+    dual_apply_pair_kernel(const __grid_constant__ DualParams p, unsigned int* status) {
+  run_pipeline_pair<DualPairSched>(p, status);
 }
 
 }  // namespace
@@ -258,9 +340,10 @@ cudaError_t launch_scores(const LaunchEnv& env, const CUtensorMap& tm_zq, const 
 }
 
 cudaError_t launch_dual_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
-                              const CUtensorMap& tm_w0, const CUtensorMap& tm_s,
-                              const CUtensorMap& tm_v, bool w0_per_seq, void* out, bool out_fp32,
-                              int B, int T, int d, int f, int C) {
+                              const CUtensorMap& tm_w0, const CUtensorMap& tm_w0_pair,
+                              const CUtensorMap& tm_s, const CUtensorMap& tm_v, bool w0_per_seq,
+                              void* out, bool out_fp32, int B, int T, int d, int f, int C,
+                              bool allow_pairs) {
   DualParams p;
   p.tm_z = tm_z;
   p.tm_w0 = tm_w0;
@@ -275,12 +358,33 @@ cudaError_t launch_dual_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
   p.C = C;
   p.n = T / C;
   p.mts = (T + kBM - 1) / kBM;
+  p.mts2 = (T + 2 * kBM - 1) / (2 * kBM);
   p.nt = (d + kBN - 1) / kBN;
   p.kf = (f + kBK - 1) / kBK;
+  cudaError_t e = cudaSuccess;
+  if (allow_pairs) {
+    // CTA pairs where two can be resident: 256-row tiles.
+    DualParams q = p;
+    q.tm_w0 = tm_w0_pair;
+    const size_t smem = pair_smem_bytes<DualPairSched>();
+    if ((e = cudaFuncSetAttribute(dual_apply_pair_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) !=
+        cudaSuccess)
+      return e;
+    static std::atomic<int> resident{-1};
+    int pairs = 0;
+    if ((e = max_pairs(reinterpret_cast<const void*>(dual_apply_pair_kernel), smem, env, &pairs,
+                       &resident)) != cudaSuccess)
+      return e;
+    if (pairs >= 1) {
+      const int64_t units = int64_t(B) * q.mts2 * q.nt;
+      return launch_on_pairs(reinterpret_cast<const void*>(dual_apply_pair_kernel),
+                             int(units < pairs ? units : pairs), smem, env, &q);
+    }
+  }
   const int64_t units = int64_t(B) * p.mts * p.nt;
-  cudaError_t e = cudaFuncSetAttribute(dual_apply_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(pipe_smem_bytes<DualSched>()));
+  e = cudaFuncSetAttribute(dual_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(pipe_smem_bytes<DualSched>()));
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? int(units) : env.num_sms;
   return launch_pdl(dual_apply_kernel, dim3(grid), dim3(PipeShape<DualSched>::kThreads),

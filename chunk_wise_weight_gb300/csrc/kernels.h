@@ -244,13 +244,16 @@ cudaError_t launch_scores(const LaunchEnv& env, const CUtensorMap& tm_zq,
                           int C);
 
 // Dual form, apply: O_[i] = Z_[i] W_0^T + S_[i, <iC] (eta Vhat)_[<iC].  Tensor
-// maps: Z [B*T, f] box {64,128}; bf16 W_0 [Bw*d, f] box {64,256} (Bw = B
-// when w0_per_seq, else 1); S [B*T, T] box {64,128}; eta*Vhat [B*T, d] box
-// {64,64}.
+// maps: Z [B*T, f] box {64,128}; bf16 W_0 [Bw*d, f] box {64,256} (tm_w0) and
+// {64,128} (tm_w0_pair) (Bw = B when w0_per_seq, else 1); S [B*T, T] box
+// {64,128}; eta*Vhat [B*T, d] box {64,64}.  With allow_pairs it runs on CTA
+// pairs (256-row tiles) when a pair can be resident, else on single CTAs;
+// both read the same scores entries and give the same result.
 cudaError_t launch_dual_apply(const LaunchEnv& env, const CUtensorMap& tm_z,
-                              const CUtensorMap& tm_w0, const CUtensorMap& tm_s,
-                              const CUtensorMap& tm_v, bool w0_per_seq, void* out, bool out_fp32,
-                              int B, int T, int d, int f, int C);
+                              const CUtensorMap& tm_w0, const CUtensorMap& tm_w0_pair,
+                              const CUtensorMap& tm_s, const CUtensorMap& tm_v, bool w0_per_seq,
+                              void* out, bool out_fp32, int B, int T, int d, int f, int C,
+                              bool allow_pairs);
 
 // Defined in ittt_api.cu, for entry points in other translation units.
 cudaError_t status_word_address(unsigned int** out);

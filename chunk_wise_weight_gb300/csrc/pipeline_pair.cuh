@@ -198,10 +198,20 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
             tc_fence_after_sync();
             const uint32_t a_base = smem_u32(smem + size_t(stage) * kPairStageBytes);
             const uint32_t b_base = a_base + kPairATileBytes;
+            if constexpr (S::kMixedOperands) {
+              const uint32_t id = sched.idesc(s, kb);
 #pragma unroll
-            for (int k = 0; k < kBK / kUmmaK; ++k) {
-              mma_bf16_pair(d_tmem, S::a_desc(a_base, k), S::b_desc(b_base, k), S::kIdesc,
-                            (fresh && kb == 0 && k == 0) ? 0u : 1u);
+              for (int k = 0; k < kBK / kUmmaK; ++k) {
+                mma_bf16_pair(d_tmem, sched.a_desc(s, kb, a_base, k),
+                              sched.b_desc(s, kb, b_base, k), id,
+                              (fresh && kb == 0 && k == 0) ? 0u : 1u);
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < kBK / kUmmaK; ++k) {
+                mma_bf16_pair(d_tmem, S::a_desc(a_base, k), S::b_desc(b_base, k), S::kIdesc,
+                              (fresh && kb == 0 && k == 0) ? 0u : 1u);
+              }
             }
             mma_commit_pair(&sync->empty[stage], kBoth);
             if (++stage == NS) {

@@ -496,6 +496,26 @@ def test_dual_form_parity(cuda_device, B, T, d, f, C, eta):
     assert_parity(host(got["O"]), ref["O"], "O (dual)")
 
 
+@pytest.mark.parametrize("B,T,d,f,C,eta", [
+    (3, 320, 192, 320, 64, 0.05),     # last 256-row tile half past T; d < 256
+    (2, 960, 320, 448, 192, 0.02),    # 256-row tiles straddle 192-token chunk edges
+    (2, 1024, 512, 640, 128, 0.03),
+])
+def test_dual_form_pairs_match_single_cta(cuda_device, B, T, d, f, C, eta):
+    """The dual apply on CTA pairs (256-row tiles sharing one scores range)
+    against the oracle and against the single-CTA kernel: the extra scores
+    a pair tile reads for its earlier rows are zeros, so both sum the same
+    products in the same order."""
+    inp = make_inputs(B, T, d, f, seed=900 + T + d)
+    ref = oracle.forward(inp, eta, C)
+    g = to_device(inp, cuda_device)
+    pair = run(g, eta, C, dual=True)
+    one = run(g, eta, C, dual=True, single_cta=True)
+    assert_parity(host(pair["O"]), ref["O"], "O (dual, CTA pairs)")
+    assert_parity(host(one["O"]), ref["O"], "O (dual, single CTA)")
+    assert torch.equal(pair["O"], one["O"])
+
+
 def test_dual_form_variants(cuda_device):
     """fp32 output, fp32 W_0, per-sequence initial state, fused conv."""
     B, T, d, f, C, eta = 2, 512, 192, 320, 128, 0.05
