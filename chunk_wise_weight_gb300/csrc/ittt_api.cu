@@ -127,6 +127,27 @@ __global__ void __launch_bounds__(256)
     dst[i] = src[i];
 }
 
+// The bounded waits' failure path, on purpose: one CTA of two warps waits
+// on an mbarrier that nothing arrives on.  Warp 0 gives up after limit_ns,
+// records kStatusTimeout and raises the CTA's abort flag; warp 1, allowed
+// four times as long, unwinds as soon as it sees the flag (as the roles of
+// a pipeline do), so the kernel ends after about limit_ns.
+__global__ void __launch_bounds__(64, 1) wait_check_kernel(uint64_t limit_ns,
+                                                           unsigned int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ittt::mbar_init(&bar, 1);
+    abort_flag = 0;
+    ittt::fence_mbar_init();
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  const bool got = ittt::mbar_wait(&bar, 0u, &abort_flag, warp == 0 ? limit_ns : 4 * limit_ns);
+  if (!got && warp == 0 && (threadIdx.x & 31) == 0)
+    ittt::raise_abort(&abort_flag, status, ittt::kStatusTimeout);
+}
+
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
@@ -979,6 +1000,20 @@ ittt_status ittt_state_prefix(const ittt_tensor* W_start, const ittt_tensor* del
 }
 
 void ittt_set_scratch_limit(size_t bytes) { g_scratch_limit.store(bytes); }
+
+ittt_status ittt_check_wait_timeout(uint64_t limit_ns, ittt_stream_t stream) {
+  g_last_error.clear();
+  if (limit_ns < 1000 || limit_ns > 1000000000ull)
+    return fail(ITTT_ERR_INVALID_ARG, "limit_ns %llu outside [1e3, 1e9]",
+                static_cast<unsigned long long>(limit_ns));
+  DeviceState* ds = nullptr;
+  ittt_status s = device_state(&ds);
+  if (s != ITTT_OK) return s;
+  wait_check_kernel<<<1, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns, ds->status);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "wait check launch");
+  return ITTT_OK;
+}
 
 int32_t ittt_plan_form(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
                        const ittt_opts* opts) {

@@ -97,6 +97,8 @@ def load(path: str | None = None):
     lib.ittt_set_scratch_limit.restype = None
     lib.ittt_plan_form.argtypes = [ctypes.c_int64] * 5 + [ctypes.POINTER(Opts)]
     lib.ittt_plan_form.restype = ctypes.c_int32
+    lib.ittt_check_wait_timeout.argtypes = [ctypes.c_uint64, ctypes.c_void_p]
+    lib.ittt_check_wait_timeout.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -256,6 +258,14 @@ def set_scratch_limit(nbytes: int) -> None:
     """ittt_set_scratch_limit: cap on the scratch one call may allocate (0:
     none); a call over it raises IttError(ERR_OOM) before anything runs."""
     load().ittt_set_scratch_limit(ctypes.c_size_t(int(nbytes)))
+
+
+def check_wait_timeout(limit_ns: int, stream=None, device=None) -> None:
+    """ittt_check_wait_timeout: enqueue a kernel whose bounded wait runs out
+    after `limit_ns`; the next stream_status() then raises
+    IttError(ERR_TIMEOUT)."""
+    _check(load().ittt_check_wait_timeout(ctypes.c_uint64(int(limit_ns)),
+                                          ctypes.c_void_p(_stream_handle(stream, device))))
 
 
 def stream_status(stream=None, device=None) -> None:

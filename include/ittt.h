@@ -350,6 +350,20 @@ ITTT_API int32_t ittt_plan_form(int64_t B, int64_t T, int64_t d, int64_t f, int6
 ITTT_API void ittt_set_scratch_limit(size_t bytes);
 
 /*
+ * Exercises the failure path of the kernels' bounded waits without a fault:
+ * enqueues on `stream` one small kernel whose threads wait on a barrier that
+ * nothing completes.  One warp gives up after `limit_ns` (1e3 .. 1e9 ns),
+ * records the timeout in the device status word and raises its block's
+ * abort flag; the other warp, allowed four times as long, unwinds on the
+ * flag, so the kernel ends after about `limit_ns` and the context stays
+ * usable.  The next ittt_stream_status() on that stream then returns
+ * ITTT_ERR_TIMEOUT (and clears the record).  Returns ITTT_ERR_INVALID_ARG
+ * for a limit outside the range (nothing enqueued), ITTT_ERR_CUDA if the
+ * launch fails, else ITTT_OK.
+ */
+ITTT_API ittt_status ittt_check_wait_timeout(uint64_t limit_ns, ittt_stream_t stream);
+
+/*
  * Synchronises `stream`, then reports any device-side failure recorded by
  * this library's kernels on the current device since the previous call
  * (ITTT_ERR_TIMEOUT when a bounded wait ran out) or a pending CUDA error

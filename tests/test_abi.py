@@ -344,6 +344,14 @@ def test_scratch_limit_fails_before_any_work(lib):
         ittt.set_scratch_limit(0)
 
 
+def test_wait_check_rejects_limits_out_of_range(lib):
+    """ittt_check_wait_timeout validates its limit before it enqueues anything
+    (no device needed for these)."""
+    for bad in (0, 999, 10**9 + 1):
+        assert lib.ittt_check_wait_timeout(ctypes.c_uint64(bad), None) == ittt.ERR_INVALID_ARG
+        assert "limit_ns" in ittt.last_error()
+
+
 C_PROGRAM = os.path.join(os.path.dirname(os.path.abspath(__file__)), "c_abi", "forward_from_c.c")
 
 

@@ -603,6 +603,30 @@ def test_status_and_argument_errors_on_device(cuda_device):
     ittt.stream_status()  # nothing recorded
 
 
+def test_bounded_wait_times_out_and_context_survives(cuda_device):
+    """A wait that nothing completes runs out after its limit: the kernel
+    records the timeout, its other warp unwinds on the abort flag (the whole
+    kernel lasts about one limit, not the other warp's four), the host reads
+    ITTT_ERR_TIMEOUT once, and the library keeps working afterwards."""
+    limit_ns = 20_000_000
+    stream = torch.cuda.current_stream(cuda_device)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    ittt.check_wait_timeout(limit_ns, stream)
+    t1.record(stream)
+    with pytest.raises(ittt.IttError) as e:
+        ittt.stream_status(stream)
+    assert e.value.status == ittt.ERR_TIMEOUT
+    assert "bounded wait" in str(e.value)
+    ms = t0.elapsed_time(t1)
+    assert 0.9 * limit_ns / 1e6 <= ms < 2.5 * limit_ns / 1e6, ms
+    ittt.stream_status(stream)  # the record was cleared
+    B, T, d, f, C, eta = 1, 256, 64, 256, 64, 0.05
+    inp = make_inputs(B, T, d, f, seed=19)
+    got = run(to_device(inp, cuda_device), eta, C)
+    assert_parity(host(got["O"]), oracle.forward(inp, eta, C)["O"], "O after a timeout")
+
+
 # --------------------------------------------------------------------------
 # Full-size named workloads: sampled entries against the oracle
 # --------------------------------------------------------------------------
