@@ -907,7 +907,8 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY + 1, stream), "event record");
   } else {
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE, stream), "event record");
-    ITTT_STEP(ittt::launch_scores(env, tm_zk, tm_zs, scores, int(B), int(T), int(f), int(chunk)),
+    ITTT_STEP(ittt::launch_scores(env, tm_zk, tm_zs, scores, int(B), int(T), int(f), int(chunk),
+                                  !single),
               "scores launch");
     ITTT_STEP(rec(2 * ITTT_PHASE_UPDATE + 1, stream), "event record");
     ITTT_STEP(rec(2 * ITTT_PHASE_APPLY, stream), "event record");

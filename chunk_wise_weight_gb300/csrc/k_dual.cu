@@ -47,22 +47,79 @@ struct ScoresParams {
   CUtensorMap tm_zq;    // Z [B*T, f] box {64, 128}  (rows t)
   CUtensorMap tm_zk;    // Z [B*T, f] box {64, 256}  (rows s)
   __nv_bfloat16* s;     // [B, T, T]
-  int B, T, C, n, mts, nt_max, kblocks;  // mts: 128-row tiles of a sequence
+  int B, T, C, n, mts, mts2, kblocks;  // mts, mts2: 128- and 256-row tiles of a sequence
+  int live1, live2;  // units with work per sequence: 128-row and 256-row tiles
 };
 
 // First token of the chunk of the last row of the `rows`-row tile at t0:
 // the scores the tile's rows read are those of tokens s < that.
-__device__ __forceinline__ int tile_s_end(int t0, int rows, int T, int C) {
-  const int last = min(t0 + rows, T) - 1;
+__host__ __device__ __forceinline__ int tile_s_end(int t0, int rows, int T, int C) {
+  const int last = (t0 + rows < T ? t0 + rows : T) - 1;
   return (last / C) * C;
 }
 
 // The scores kernel fills, for every row, the range its 256-row group reads
 // (the CTA-pair apply's tile; a 128-row tile of the single-CTA apply reads a
 // part of it).
-__device__ __forceinline__ int group_s_end(int t0, int T, int C) {
+__host__ __device__ __forceinline__ int group_s_end(int t0, int T, int C) {
   return tile_s_end(t0 - t0 % (2 * kBM), 2 * kBM, T, C);
 }
+
+// Score tiles (kBN tokens s each) the rows of the `rows`-row tile m read.
+__host__ __device__ __forceinline__ int score_tiles(int m, int rows, int T, int C) {
+  return (group_s_end(m * rows, T, C) + kBN - 1) / kBN;
+}
+
+// Only tiles with work are units: the k-th of a sequence is row tile *m and
+// score tile *nt, counting score_tiles(m) units per row tile (a short scan:
+// a sequence has at most a few hundred row tiles).
+__device__ __forceinline__ void live_unit(int k, int rows, int ntiles, int T, int C, int* m,
+                                          int* nt) {
+  int mm = 0;
+  for (; mm < ntiles - 1; ++mm) {
+    const int L = score_tiles(mm, rows, T, C);
+    if (k < L) break;
+    k -= L;
+  }
+  *m = mm;
+  *nt = k;
+}
+
+// Row t (tile row `row` at t0) keeps the scores of tokens before its own
+// chunk; the rest of the tile's range (t's chunk, when a later chunk's row
+// shares the group) is written as zeros.  Chunks are multiples of 64 tokens,
+// so an 8-column group lies wholly on one side.
+__device__ __forceinline__ void scores_epilogue(const ScoresParams& p, int b, int t0, int s0,
+                                              int rows_valid, int cols_valid, int row,
+                                              uint32_t trow) {
+  const bool row_ok = row < rows_valid;
+  const int t = t0 + (row_ok ? row : 0);
+  const int own = (t / p.C) * p.C;  // first token of t's chunk
+  __nv_bfloat16* srow = p.s + (size_t(b) * p.T + size_t(t)) * size_t(p.T);
+#pragma unroll 1
+  for (int c = 0; c < kBN; c += 32) {
+    uint32_t v[32];
+    tmem_ld_32cols(trow + uint32_t(c), v);
+    tmem_wait_ld();
+    pin_regs(v);
+    if (!row_ok) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int cc = c + 8 * q;
+      if (cc < cols_valid) {
+        const uint4 val =
+            (s0 + cc < own)
+                ? make_uint4(
+                      pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                      pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                      pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                      pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])))
+                : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(srow + s0 + cc) = val;
+      }
+    }
+  }
+  }
 
 struct ScoresSched : SchedDefaults {
   using Params = ScoresParams;
@@ -73,12 +130,11 @@ struct ScoresSched : SchedDefaults {
   bool live = false;
 
   __device__ explicit ScoresSched(const Params& pp) : p(pp) {}
-  __device__ int num_units() const { return p.B * p.mts * p.nt_max; }
+  __device__ int num_units() const { return p.B * p.live1; }
   __device__ void begin_unit(int u, int local) {
-    const int nt = u % p.nt_max;
-    const int r = u / p.nt_max;
-    const int mt = r % p.mts;
-    b = r / p.mts;
+    int mt = 0, nt = 0;
+    b = u / p.live1;
+    live_unit(u - b * p.live1, kBM, p.mts, p.T, p.C, &mt, &nt);
     t0 = mt * kBM;
     s0 = nt * kBN;
     const int s_end = group_s_end(t0, p.T, p.C);
@@ -101,38 +157,52 @@ struct ScoresSched : SchedDefaults {
   static __device__ uint64_t a_desc(uint32_t base, int k) { return kmajor_desc(base, k); }
   static __device__ uint64_t b_desc(uint32_t base, int k) { return kmajor_desc(base, k); }
 
-  // Row t keeps the scores of tokens before its own chunk; the rest of the
-  // tile's range (t's chunk, when a later chunk's row shares the tile) is
-  // written as zeros.  Chunks are multiples of 64 tokens, so an 8-column
-  // group lies wholly on one side.
   __device__ void epilogue(int, int row, uint32_t trow) const {
-    const bool row_ok = row < rows_valid;
-    const int t = t0 + (row_ok ? row : 0);
-    const int own = (t / p.C) * p.C;  // first token of t's chunk
-    __nv_bfloat16* srow = p.s + (size_t(b) * p.T + size_t(t)) * size_t(p.T);
-#pragma unroll 1
-    for (int c = 0; c < kBN; c += 32) {
-      uint32_t v[32];
-      tmem_ld_32cols(trow + uint32_t(c), v);
-      tmem_wait_ld();
-      pin_regs(v);
-      if (!row_ok) continue;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int cc = c + 8 * q;
-        if (cc < cols_valid) {
-          const uint4 val =
-              (s0 + cc < own)
-                  ? make_uint4(
-                        pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                        pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                        pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                        pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])))
-                  : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(srow + s0 + cc) = val;
-        }
-      }
-    }
+    scores_epilogue(p, b, t0, s0, rows_valid, cols_valid, row, trow);
+  }
+};
+
+// The scores on CTA pairs: 256 x 256 tiles, each CTA 128 rows t and 128 of
+// the tokens s (both operands Z rows, box {64, 128}).
+struct ScoresPairSched : PairDefaults {
+  using Params = ScoresParams;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, kBN, false, false);
+
+  const Params& p;
+  const int rank;
+  int arow0 = 0, brow0 = 0, rows_valid = 0, cols_valid = 0, acc = 0, b = 0, t0 = 0, s0 = 0;
+  bool live = false;
+
+  __device__ ScoresPairSched(const Params& pp, uint32_t r) : p(pp), rank(int(r)) {}
+  __device__ int num_units() const { return p.B * p.live2; }
+  __device__ void begin_unit(int u, int local) {
+    int mt = 0, nt = 0;
+    b = u / p.live2;
+    live_unit(u - b * p.live2, 2 * kBM, p.mts2, p.T, p.C, &mt, &nt);
+    const int g0 = mt * (2 * kBM);
+    t0 = g0 + rank * kBM;
+    s0 = nt * kBN;
+    const int s_end = tile_s_end(g0, 2 * kBM, p.T, p.C);  // the same for both CTAs
+    live = s0 < s_end;
+    arow0 = b * p.T + t0;
+    brow0 = b * p.T + s0 + rank * kBM;
+    rows_valid = min(kBM, p.T - t0);  // <= 0: the group ends in the other half
+    cols_valid = min(kBN, s_end - s0);
+    acc = local & 1;
+  }
+  __device__ int num_segments() const { return live ? 1 : 0; }
+  __device__ int seg_acc(int) const { return acc; }
+  __device__ int seg_kblocks(int) const { return p.kblocks; }
+  __device__ bool seg_fresh(int) const { return true; }
+  __device__ void load(int, int kb, uint8_t* stage, uint32_t bar) const {
+    const int k = kb * kBK;
+    tma_load_2d_pair(stage, &p.tm_zq, bar, k, arow0);
+    tma_load_2d_pair(stage + kPairATileBytes, &p.tm_zq, bar, k, brow0);
+  }
+  static __device__ uint64_t a_desc(uint32_t base, int k) { return kmajor_desc(base, k); }
+  static __device__ uint64_t b_desc(uint32_t base, int k) { return kmajor_desc(base, k); }
+  __device__ void epilogue(int, int row, uint32_t trow) const {
+    scores_epilogue(p, b, t0, s0, rows_valid, cols_valid, row, trow);
   }
 };
 
@@ -304,6 +374,11 @@ __global__ void __launch_bounds__(PipeShape<ScoresSched>::kThreads, 1)
   run_pipeline<ScoresSched>(p, status);
 }
 
+__global__ void __launch_bounds__(kBaseThreads, 1)
+    scores_pair_kernel(const __grid_constant__ ScoresParams p, unsigned int* status) {
+  run_pipeline_pair<ScoresPairSched>(p, status);
+}
+
 __global__ void __launch_bounds__(PipeShape<DualSched>::kThreads, 1)
     dual_apply_kernel(const __grid_constant__ DualParams p, unsigned int* status) {
   run_pipeline<DualSched>(p, status);
@@ -317,7 +392,7 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
 }  // namespace
 
 cudaError_t launch_scores(const LaunchEnv& env, const CUtensorMap& tm_zq, const CUtensorMap& tm_zk,
-                          __nv_bfloat16* s, int B, int T, int f, int C) {
+                          __nv_bfloat16* s, int B, int T, int f, int C, bool allow_pairs) {
   ScoresParams p;
   p.tm_zq = tm_zq;
   p.tm_zk = tm_zk;
@@ -327,12 +402,32 @@ cudaError_t launch_scores(const LaunchEnv& env, const CUtensorMap& tm_zq, const 
   p.C = C;
   p.n = T / C;
   p.mts = (T + kBM - 1) / kBM;
-  p.nt_max = ((p.n - 1) * C + kBN - 1) / kBN;
+  p.mts2 = (T + 2 * kBM - 1) / (2 * kBM);
   p.kblocks = (f + kBK - 1) / kBK;
-  if (p.n < 2) return cudaSuccess;
-  const int64_t units = int64_t(B) * p.mts * p.nt_max;
-  cudaError_t e = cudaFuncSetAttribute(scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(pipe_smem_bytes<ScoresSched>()));
+  p.live1 = p.live2 = 0;
+  for (int m = 0; m < p.mts; ++m) p.live1 += score_tiles(m, kBM, T, C);
+  for (int m = 0; m < p.mts2; ++m) p.live2 += score_tiles(m, 2 * kBM, T, C);
+  if (p.n < 2 || p.live1 == 0) return cudaSuccess;
+  cudaError_t e = cudaSuccess;
+  if (allow_pairs) {
+    const size_t smem = pair_smem_bytes<ScoresPairSched>();
+    if ((e = cudaFuncSetAttribute(scores_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(smem))) != cudaSuccess)
+      return e;
+    static std::atomic<int> resident{-1};
+    int pairs = 0;
+    if ((e = max_pairs(reinterpret_cast<const void*>(scores_pair_kernel), smem, env, &pairs,
+                       &resident)) != cudaSuccess)
+      return e;
+    if (pairs >= 1) {
+      const int64_t units = int64_t(B) * p.live2;
+      return launch_on_pairs(reinterpret_cast<const void*>(scores_pair_kernel),
+                             int(units < pairs ? units : pairs), smem, env, &p);
+    }
+  }
+  const int64_t units = int64_t(B) * p.live1;
+  e = cudaFuncSetAttribute(scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(pipe_smem_bytes<ScoresSched>()));
   if (e != cudaSuccess) return e;
   const int grid = units < env.num_sms ? int(units) : env.num_sms;
   return launch_pdl(scores_kernel, dim3(grid), dim3(PipeShape<ScoresSched>::kThreads),

@@ -237,11 +237,14 @@ cudaError_t launch_apply_pair(const LaunchEnv& env, const CUtensorMap& tm_z,
                               const DocMap& docs, int d, int f);
 
 // Dual form, scores: S[b, t, s] = Z_t . Z_s (bf16) for every token t of chunk
-// i >= 1 and every token s < i*C of the same sequence.  Tensor maps: Z
-// [B*T, f] with box {64,128} (tm_zq) and box {64,256} (tm_zk).
+// i >= 1 and every token s < i*C of the same sequence (and zeros for the
+// other tokens s before the first token of the last chunk of t's 256-row
+// group).  Tensor maps: Z [B*T, f] with box {64,128} (tm_zq) and box
+// {64,256} (tm_zk).  With allow_pairs it runs on CTA pairs when a pair can
+// be resident, else on single CTAs; both write the same entries.
 cudaError_t launch_scores(const LaunchEnv& env, const CUtensorMap& tm_zq,
                           const CUtensorMap& tm_zk, __nv_bfloat16* s, int B, int T, int f,
-                          int C);
+                          int C, bool allow_pairs);
 
 // Dual form, apply: O_[i] = Z_[i] W_0^T + S_[i, <iC] (eta Vhat)_[<iC].  Tensor
 // maps: Z [B*T, f] box {64,128}; bf16 W_0 [Bw*d, f] box {64,256} (tm_w0) and
