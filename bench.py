@@ -393,13 +393,13 @@ def init_dist(args):
 def dual_form(cfg, args, cu=None) -> bool:
     """Whether the call runs the dual form: forced by --dual, else the
     library's choice for these options (the rule of ittt_plan_form: the dual
-    form where allowed and T < 2 d f / (d + f))."""
+    form where allowed and T < 2.5 d f / (d + f))."""
     if args.dual:
         return True
     if args.primal or cu is not None or args.l2norm or args.fused_conv:
         return False
     T, d, f, C = cfg["T"], cfg["d"], cfg["f"], cfg["C"]
-    return C % 64 == 0 and T % C == 0 and T // C >= 2 and T * (d + f) < 2 * d * f
+    return C % 64 == 0 and T % C == 0 and T // C >= 2 and 2 * T * (d + f) < 5 * d * f
 
 
 def arm_config(cfg, args, world, cu=None):

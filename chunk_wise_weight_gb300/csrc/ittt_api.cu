@@ -13,7 +13,7 @@
 // when every updated chunk is a multiple of 64 tokens), else on single CTAs.
 // With ITTT_FLAG_FUSED_CONV the target GEMM computes the conv itself; in the
 // dual form (forced by ITTT_FLAG_DUAL, or chosen by the planner for short
-// sequences, T < 2 d f / (d + f), where it measured faster) scores Z Z^T and
+// sequences, T < 2.5 d f / (d + f), where it measured faster) scores Z Z^T and
 // the dual apply replace walk and apply; with ITTT_FLAG_L2_NORM the walk runs
 // one launch per chunk.  (Run beside the
 // gate/up GEMM on a second stream, the conv slowed that GEMM by more than its
@@ -361,11 +361,13 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   P->l2norm = (o.flags & ITTT_FLAG_L2_NORM) != 0;
   // Form choice by measured cost: the dual form for short sequences, where
   // the walk's per-chunk d x f snapshots cost more than the dual form's
-  // T^2 terms (crossover near T = 2 d f / (d + f) on GB300).
+  // T^2 terms.  The two forms' FLOPs are equal at T = 2 d f / (d + f); the
+  // walk's snapshot traffic moves the measured crossover on GB300 to
+  // 1.25-1.3 times that length.
   if (!P->dual && !(o.flags & ITTT_FLAG_PRIMAL) && !P->fused && !P->packed && !P->l2norm &&
       o.state_out == nullptr && o.snap_buf == nullptr && !(o.flags & ITTT_FLAG_UPDATE_ONLY) &&
       chunk % 64 == 0 && T % chunk == 0 && T / chunk >= 2 &&
-      double(T) * double(d + f) < 2.0 * double(d) * double(f))
+      double(T) * double(d + f) < 2.5 * double(d) * double(f))
     P->dual = true;
   if (P->l2norm && P->dual)
     return fail(ITTT_ERR_UNSUPPORTED,

@@ -26,7 +26,7 @@
 // square of the context: per chunk i it costs 2*C*d*f + i*2*C^2*(d + f)
 // FLOPs against 4*C*d*f for the primal apply and update -- but it writes no
 // d x f snapshot per chunk, so it wins on short sequences (the planner picks
-// it below T = 2 d f / (d + f)).
+// it below T = 2.5 d f / (d + f)).
 #include "kernels.h"
 #include "pipeline.cuh"
 #include "pipeline_pair.cuh"

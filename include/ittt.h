@@ -217,13 +217,14 @@ typedef struct {
  * dual form when it can (regular sequences, chunk a multiple of 64 dividing
  * T, at least two chunks, no state_out, snap_buf, packed documents,
  * ITTT_FLAG_L2_NORM or ITTT_FLAG_FUSED_CONV) and its sequences are short:
- * T < 2 d f / (d + f) tokens.  The primal walk writes and re-reads one d x f
- * weight snapshot per chunk whatever the chunk's length, while the dual
- * form's extra work grows with T^2; measured on GB300 the dual form was
- * faster below that length (4.3x at 64 x 256 tokens, 1.2x at 8 x 2048 for
- * d 2560, f 9728) and slower above it (6x at 2 x 32768).  Both forms compute
- * the same layer; they round differently.  ittt_plan_form says which form a
- * call would use.
+ * T < 2.5 d f / (d + f) tokens.  The dual form's extra FLOPs grow with T^2
+ * and equal the walk's update FLOPs at T = 2 d f / (d + f); the primal walk
+ * also writes and re-reads one d x f weight snapshot per chunk whatever the
+ * chunk's length, which moves the measured crossover on GB300 to 1.25-1.3
+ * times that length (d 2560, f 9728: the dual form 5.6x faster at 64 x 256
+ * tokens, 1.06x at 4 x 4096, 0.82x at 2 x 8192, 0.3x at 2 x 32768).  Both
+ * forms compute the same layer; they round differently.  ittt_plan_form
+ * says which form a call would use.
  */
 
 /* Kernel phases of one forward call, in launch order. */

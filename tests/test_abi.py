@@ -390,17 +390,20 @@ def test_state_in_place_only_as_exact_alias(lib):
 
 
 def test_form_choice_by_sequence_length():
-    """The dual form for short sequences (T < 2 d f / (d + f)) where it is
+    """The dual form for short sequences (T < 2.5 d f / (d + f)) where it is
     allowed, the primal walk otherwise; DUAL / PRIMAL force one."""
     P, D = ittt.FORM_PRIMAL, ittt.FORM_DUAL
     cases = [
-        ((8, 2048, 2560, 9728, 512), D),      # 2048 < 4054
+        ((8, 2048, 2560, 9728, 512), D),      # 2048 < 5068
         ((64, 256, 2560, 9728, 64), D),
-        ((4, 4096, 2560, 9728, 1024), P),     # 4096 > 4054
+        ((4, 4096, 2560, 9728, 1024), D),     # 4096 < 5068
+        ((2, 8192, 2560, 9728, 2048), P),     # 8192 > 5068
         ((2, 32768, 2560, 9728, 2048), P),    # the bench workload
-        ((8, 1024, 1024, 3072, 256), D),      # 1024 < 1536
-        ((4, 2048, 1024, 3072, 512), P),
-        ((1, 256, 64, 256, 64), P),           # 256 > 102
+        ((4, 4096, 4096, 14336, 1024), D),    # 4096 < 7964
+        ((2, 8192, 4096, 14336, 1024), P),    # 8192 > 7964
+        ((8, 1024, 1024, 3072, 256), D),      # 1024 < 1920
+        ((4, 2048, 1024, 3072, 512), P),      # 2048 > 1920
+        ((1, 256, 64, 256, 64), P),           # 256 > 128
         ((8, 2048, 2560, 9728, 2048), P),     # one chunk: nothing to update
         ((8, 2000, 2560, 9728, 500), P),      # chunk not a multiple of 64
         ((8, 2048, 2560, 9728, 768), P),      # chunk does not divide T

@@ -1136,7 +1136,7 @@ def test_state_updated_in_place(cuda_device, l2norm, update_only, packed):
 
 def test_form_chosen_by_sequence_length(cuda_device):
     """Short sequences take the dual form by default (d 512, f 1024: below
-    T = 683 tokens); both forms match the oracle, the default is the dual
+    T = 853 tokens); both forms match the oracle, the default is the dual
     form bit for bit, and forcing the primal form gives the walk."""
     B, T, d, f, C, eta = 4, 512, 512, 1024, 128, 0.05
     assert ittt.plan_form(B, T, d, f, C) == ittt.FORM_DUAL
