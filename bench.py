@@ -467,7 +467,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": arm_config(cfg, args, world),
         "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -475,18 +475,56 @@ def run_reference(args):
     return 0
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    architecture)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(cfg, index, tokens):
+    """The oracle on a bounded sample of the workload, on every host core;
+    then, single-threaded, on the tiny d 64 / d_ff 256 workload whole."""
     import oracle
-    from chunk_wise_weight_gb300 import make_inputs
+    from chunk_wise_weight_gb300 import CONFIGS, make_inputs
     S = max(128, tokens)
     Cs = S // 2
     inp = make_inputs(1, S, cfg["d"], cfg["f"], seed=1234 + index)
     t0 = time.perf_counter()
     oracle.forward(inp, cfg["eta"], Cs)
     dt = time.perf_counter() - t0
-    return {"value": S / dt, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+    cores = oracle.num_threads()
+    tiny = CONFIGS[0]
+    tin = make_inputs(tiny["B"], tiny["T"], tiny["d"], tiny["f"], seed=1234)
+    oracle.set_num_threads(1)
+    try:
+        t1 = time.perf_counter()
+        oracle.forward(tin, tiny["eta"], tiny["C"])
+        dt1 = time.perf_counter() - t1
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": S / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": (f"fp64 oracle on one sequence of {S} tokens in two chunks of {Cs} at "
-                       f"d={cfg['d']}, d_ff={cfg['f']} ({dt:.1f} s)")}
+                       f"d={cfg['d']}, d_ff={cfg['f']} ({dt:.1f} s)"),
+            "cpu_model": cpu_model(),
+            "single_thread": {"workload": tiny["name"], "cores": 1,
+                              "value": tiny["B"] * tiny["T"] / dt1, "unit": "tokens/s",
+                              "seconds": round(dt1, 4)}}
 
 
 def main():

@@ -85,6 +85,8 @@ def _load():
         lib.oracle_first_chunk_rows.argtypes = [_i64, _i64, _fp, _fp, _fp, _fp,
                                                 _i64, _ip, _dp]
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_set_num_threads.restype = None
         _lib = lib
         return lib
 
@@ -110,6 +112,12 @@ def _iptr(a: np.ndarray):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's OpenMP loops use from now on (results do not
+    depend on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _unpack(inp):

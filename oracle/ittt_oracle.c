@@ -535,3 +535,14 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads the OpenMP loops use from now on (n >= 1; a single-threaded timing
+ * of the baseline sets 1, then restores the previous count).  No effect on
+ * any result: every parallel loop writes disjoint outputs. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
