@@ -101,6 +101,11 @@ def test_rejects_bad_descriptors(lib, mutate, status, msg):
 def test_rejects_bad_sizes(lib):
     assert _call(lib, _args(), chunk=0) == ittt.ERR_INVALID_ARG
     assert "positive" in ittt.last_error()
+    # empty inputs (no sequence, no token) are argument errors, before any work
+    for B, T in ((0, 256), (1, 0), (0, 0)):
+        assert _call(lib, _args(B=B, T=T)) == ittt.ERR_INVALID_ARG, (B, T)
+        assert "positive" in ittt.last_error()
+        assert ittt.workspace_bytes(B, T, 64, 256, 64) == 0
     assert _call(lib, _args(), chunk=-64) == ittt.ERR_INVALID_ARG
     assert _call(lib, _args(d=60), chunk=64) == ittt.ERR_UNSUPPORTED
     assert _call(lib, _args(f=100), chunk=64) == ittt.ERR_UNSUPPORTED
