@@ -137,7 +137,9 @@ typedef struct {
  *   eta_tok    fp32 [B,T]: per-token learning-rate weights; token t's term
  *              of the chunk update is scaled by eta * eta_tok[b,t] (the
  *              large-chunk update with a rate per token of "Test-Time
- *              Training Done Right").  NULL: every weight is 1.
+ *              Training Done Right").  NULL: every weight is 1.  The update
+ *              averaged over its chunk (eta times the chunk's mean of
+ *              Vhat_t^T Z_t) is eta_tok[b,t] = 1 / (length of t's chunk).
  *   events     profiling: NULL, or 2 * ITTT_NUM_PHASES cudaEvent_t handles.
  *              events[2k] and events[2k+1] are recorded right before and
  *              right after phase k (ittt_phase order) on `stream`, so each

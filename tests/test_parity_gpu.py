@@ -227,6 +227,27 @@ def test_per_token_rates(cuda_device, fused_conv, dual):
     assert_parity(host(got["O"]), ref["O"], "O")
 
 
+def test_chunk_mean_update_through_token_rates(cuda_device):
+    """The 1/C-scaled update (eta times the chunk's mean of Vhat_t^T Z_t, a
+    variant the pages mention beside per-token rates) is the per-token rate
+    1 / (length of t's chunk): the last, shorter chunk is averaged over its
+    own length.  Against the oracle with the same rates, and with full
+    chunks against the plain update at eta / C."""
+    B, T, d, f, C, eta = 2, 456, 128, 320, 128, 0.5     # chunks 128, 128, 128, 72
+    inp = make_inputs(B, T, d, f, seed=802)
+    t = torch.arange(T)
+    start = (t // C) * C
+    length = torch.clamp(T - start, max=C).float()
+    rates = (1.0 / length).expand(B, T).contiguous()
+    ref = oracle.forward(inp, eta, C, want_states=True, eta_tok=rates)
+    got = run(to_device(inp, cuda_device), eta, C, want_state=True, eta_tok=rates.to(cuda_device))
+    assert_parity(host(got["O"]), ref["O"], "O (chunk-mean update)")
+    assert_parity(host(got["state_out"]), ref["states"][:, -1], "final state (chunk-mean update)")
+    full = oracle.forward(inp, eta / C, C, want_states=True)
+    np.testing.assert_allclose(ref["states"][:, T // C], full["states"][:, T // C],
+                               rtol=1e-6, atol=1e-9)
+
+
 @pytest.mark.parametrize("B,T,d,f,C,eta", SHAPES[:4])
 def test_single_cta_kernels(cuda_device, B, T, d, f, C, eta):
     """The single-CTA GEMMs (the fallback where CTA pairs cannot be resident)
