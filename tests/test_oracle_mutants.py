@@ -2,7 +2,9 @@
 
 Each case plants one mistake in a copy of oracle/ittt_oracle.c (on the CPU,
 in a temporary directory), builds it, and runs the pin suite against that
-copy: the suite has to fail.  The committed oracle is never modified.
+copy: the suite has to fail.  The same is done for the chunk-by-chunk oracle
+(oracle/chunked.py) and its own pins.  The committed oracle is never
+modified.
 """
 import os
 import subprocess
@@ -12,6 +14,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ittt_oracle.c")
+SRC_CHUNKED = os.path.join(ROOT, "oracle", "chunked.py")
 
 # (name, exact text in the oracle, replacement)
 MUTANTS = [
@@ -73,5 +76,43 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new):
     env = dict(os.environ, ITTT_ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
+
+
+# (name, exact text in oracle/chunked.py, replacement)
+CHUNKED_MUTANTS = [
+    ("silu_drops_sigmoid", "return x / (1.0 + np.exp(-x))", "return x"),
+    ("conv_taps_flipped", "pad[:-2] * w[:, 0] + pad[1:-1] * w[:, 1] + pad[2:] * w[:, 2]",
+     "pad[:-2] * w[:, 2] + pad[1:-1] * w[:, 1] + pad[2:] * w[:, 0]"),
+    ("conv_ignores_chunk_edges",
+     "        seg = (lo, hi) if pad_mode == PAD_CHUNK else (0, T)\n        V = conv_rows(X0, conv_w, lo, hi, *seg) @ Wt.T\n        O = Z @ W.T",
+     "        seg = (0, T)\n        V = conv_rows(X0, conv_w, lo, hi, *seg) @ Wt.T\n        O = Z @ W.T"),
+    ("target_not_transposed", "V = conv_rows(X0, conv_w, lo, hi, *seg) @ Wt.T\n        O = Z @ W.T",
+     "V = conv_rows(X0, conv_w, lo, hi, *seg) @ Wt\n        O = Z @ W.T"),
+    ("update_sign_flipped", "W_next = W + eta * (Vr.T @ Z)", "W_next = W - eta * (Vr.T @ Z)"),
+    ("update_before_apply", "        O = Z @ W.T\n        out = {",
+     "        O = Z @ (W + eta * (V.T @ Z)).T\n        out = {"),
+    ("initial_weight_dropped", "W = _f64(W0).copy()", "W = 0.0 * _f64(W0)"),
+    ("token_rates_ignored", "Vr = V if rates is None else V * rates[lo:hi, None]", "Vr = V"),
+    ("apply_uses_Z_for_output", "O = Z @ W.T", "O = Z[:, :W.shape[0]] * 1.0"),
+    ("l2norm_skipped", "                W_next = _normalise_rows(W_next)\n", "\n"),
+    ("l2norm_over_columns", "norm = np.sqrt((W * W).sum(axis=1))\n    return W / np.maximum(norm, 1e-12)[:, None]",
+     "norm = np.sqrt((W * W).sum(axis=0))\n    return W / np.maximum(norm, 1e-12)[None, :]"),
+    ("state_grid_skips_eta", "out[i + 1] = out[0] + eta * acc", "out[i + 1] = out[0] + acc"),
+    ("state_grid_inclusive", "        acc = acc + V.T @ Z\n        out[i + 1] = out[0] + eta * acc",
+     "        acc = acc + V.T @ Z\n        out[i + 1] = out[0] + eta * (acc + V.T @ Z)"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", CHUNKED_MUTANTS, ids=[m[0] for m in CHUNKED_MUTANTS])
+def test_chunked_pins_catch_planted_mistake(tmp_path, name, old, new):
+    src = open(SRC_CHUNKED).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutated = tmp_path / "chunked_mutant.py"
+    mutated.write_text(src.replace(old, new))
+    env = dict(os.environ, ITTT_CHUNKED_ORACLE=str(mutated), OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_chunked.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
