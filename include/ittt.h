@@ -46,6 +46,12 @@
  *     Argument errors are detected before anything is enqueued.  Device-side
  *     failures (a bounded wait that ran out) are reported by
  *     ittt_stream_status().
+ *   - Per-device state: the first call on a device looks up device addresses
+ *     (the status word, the fixed scratch of ittt_forward_noalloc) and
+ *     creates a memory pool; they are kept for the life of the process.
+ *     Resetting the device (cudaDeviceReset) or destroying its primary
+ *     context after that first call is not supported: later calls would use
+ *     addresses of the destroyed context.
  */
 #ifndef ITTT_H_
 #define ITTT_H_

@@ -4,10 +4,22 @@ memory budget; device memory owned by another framework's caching allocator;
 a real-time path that forbids allocation after start-up).
 
 It keeps its scratch in one fixed 64 MiB device array instead of allocating.
-These tests check that it gives the output of ittt_forward on two calls in a
-row (different inputs each time, so nothing left in the shared scratch by the
-first call can stand in for the second), and that work too large for the
-fixed array is refused before anything runs.
+These tests check, on two calls in a row with different inputs (so nothing
+the first call leaves in the shared scratch can stand in for the second):
+
+  * that each output equals, bit for bit, the output of ittt_forward_ex in
+    the primal form on the same inputs -- the two run the same kernels in
+    the same order -- and matches the fp64 oracle within the layer's bar;
+  * that the second call changes neither the device's free memory nor the
+    memory PyTorch's caching allocator holds (nothing was allocated);
+  * for a bf16 and an fp32 W_down0 (the fp32 one is first copied into the
+    scratch's snapshot slot 0), bf16 and fp32 output, a partial last chunk,
+    and chunks that are not multiples of 64 tokens (the single-CTA walk with
+    masked K blocks);
+
+and that work too large for the fixed array is refused before anything
+runs.  This file is collected last, so a run that stops at the first
+failure has run every other test before it.
 """
 import ctypes
 
@@ -15,6 +27,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from chunk_wise_weight_gb300 import build, ittt, make_inputs
 
 REL_FRO = 5e-3
@@ -39,27 +52,57 @@ def _call(fn, tensors, eta, chunk, out, stream):
               ctypes.c_void_p(stream))
 
 
+CASES = [
+    # W_down0 dtype, out dtype, T, chunk
+    (torch.bfloat16, torch.bfloat16, 1024, 256),
+    (torch.float32, torch.bfloat16, 1024, 256),   # W_0 copied into snapshot slot 0
+    (torch.bfloat16, torch.float32, 1024, 256),   # fp32 output (no TMA store map)
+    (torch.bfloat16, torch.bfloat16, 1000, 192),  # partial last chunk of 40 tokens
+    (torch.bfloat16, torch.bfloat16, 1000, 200),  # chunks not multiples of 64: single-CTA walk
+]
+
+
 @pytest.mark.gpu
-def test_noalloc_matches_forward_on_two_calls_in_a_row(cuda_device):
+@pytest.mark.parametrize("w0_dtype,out_dtype,T,C", CASES)
+def test_noalloc_matches_forward_on_two_calls_in_a_row(cuda_device, w0_dtype, out_dtype, T, C):
     fn = _entry()
-    B, T, d, f, C, eta = 2, 1024, 256, 1024, 256, 0.03
+    B, d, f, eta = 2, 256, 1024, 0.03
     stream = torch.cuda.current_stream(cuda_device)
+    calls = []
     for seed in (21, 22):
-        inp = make_inputs(B, T, d, f, seed=seed)
-        g = [inp[k].to(cuda_device, torch.bfloat16)
-             for k in ("H", "X0", "W_gate", "W_up", "W_down0", "W_target")]
+        inp = make_inputs(B, T, d, f, seed=seed + T + C)
+        g = [inp[k].to(cuda_device, torch.bfloat16) for k in ("H", "X0", "W_gate", "W_up")]
+        g.append(inp["W_down0"].to(cuda_device, w0_dtype))
+        g.append(inp["W_target"].to(cuda_device, torch.bfloat16))
         g.append(inp["conv_w"].to(cuda_device, torch.float32))
-        ref = torch.empty(B, T, d, dtype=torch.bfloat16, device=cuda_device)
-        ittt.forward_plain(*g, eta, C, ref)
-        out = torch.full((B, T, d), float("nan"), dtype=torch.bfloat16, device=cuda_device)
-        status = _call(fn, g, eta, C, out, stream.cuda_stream)
-        assert status == ittt.OK, ittt.last_error()
-        ittt.stream_status()
+        ref = ittt.forward(*g, eta, C, out_dtype=out_dtype, primal=True)
+        out = torch.full((B, T, d), float("nan"), dtype=out_dtype, device=cuda_device)
+        calls.append((inp, g, ref, out))
+    ittt.stream_status()
+    torch.cuda.synchronize(cuda_device)
+
+    # First call (on a fresh device it also does the one-time set-up).
+    inp, g, ref, out = calls[0]
+    assert _call(fn, g, eta, C, out, stream.cuda_stream) == ittt.OK, ittt.last_error()
+    torch.cuda.synchronize(cuda_device)
+    free_before = torch.cuda.mem_get_info(cuda_device)[0]
+    reserved_before = torch.cuda.memory_reserved(cuda_device)
+    # Second call, other inputs, straight after: no allocation anywhere.
+    inp, g, ref, out = calls[1]
+    assert _call(fn, g, eta, C, out, stream.cuda_stream) == ittt.OK, ittt.last_error()
+    torch.cuda.synchronize(cuda_device)
+    assert torch.cuda.mem_get_info(cuda_device)[0] == free_before
+    assert torch.cuda.memory_reserved(cuda_device) == reserved_before
+    ittt.stream_status()
+
+    for k, (inp, g, ref, out) in enumerate(calls):
+        # Same kernels, same order, same operands as the primal ittt_forward_ex.
+        assert torch.equal(out, ref), f"call {k}: differs from ittt_forward_ex (primal)"
+        want = oracle.forward(inp, eta, C)["O"]
         got = out.double().cpu().numpy()
-        want = ref.double().cpu().numpy()
         rel = np.linalg.norm(got - want) / np.linalg.norm(want)
         mx = np.abs(got - want).max() / np.abs(want).max()
-        assert rel <= REL_FRO and mx <= MAX_RATIO, f"seed {seed}: rel={rel:.3e} max={mx:.3e}"
+        assert rel <= REL_FRO and mx <= MAX_RATIO, f"call {k}: rel={rel:.3e} max={mx:.3e}"
 
 
 def test_noalloc_refuses_work_beyond_its_fixed_scratch():
