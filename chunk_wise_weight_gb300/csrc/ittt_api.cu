@@ -551,15 +551,15 @@ ittt_status make_map_3d(CUtensorMap* map, const void* base, uint64_t inner, uint
 }
 
 ittt_status make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                     uint32_t box_inner, uint32_t box_outer, const char* what) {
+                     uint32_t box_inner, uint32_t box_outer, const char* what,
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(ITTT_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, int(r));
   return ITTT_OK;
@@ -792,8 +792,12 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
       (s = stage_table(ds, tab, P.table.data(), P.table.size(), stream)) != ITTT_OK)
     return s;
   if (!fused && !reuse) {
-    ITTT_STEP(ittt::launch_conv(env, static_cast<const __nv_bfloat16*>(X0->data), cw, xc,
-                                int64_t(M), docs, int(d), int(o.pad_mode)),
+    CUtensorMap tm_x0;
+    if (what == nullptr &&
+        (s = make_map(&tm_x0, X0->data, d, M, ittt::kConvMapBoxCols, ittt::kConvMapBoxRows,
+                      "X0 (conv)", CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return s;
+    ITTT_STEP(ittt::launch_conv(env, tm_x0, cw, xc, int64_t(M), docs, int(d), int(o.pad_mode)),
               "conv launch");
   }
   ITTT_STEP(rec(2 * ITTT_PHASE_CONV + 1, stream), "event record");

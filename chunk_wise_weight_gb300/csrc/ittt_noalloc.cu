@@ -161,15 +161,15 @@ ittt_status na_map_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64
 }
 
 ittt_status na_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                   uint32_t box_inner, uint32_t box_outer, const char* what) {
+                   uint32_t box_inner, uint32_t box_outer, const char* what,
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_na_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return na_fail(ITTT_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, int(r));
   return ITTT_OK;
@@ -254,7 +254,7 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   auto* snap = reinterpret_cast<__nv_bfloat16*>(nd->scratch + z_bytes + 2 * act_bytes);
 
   const uint64_t M = uint64_t(B * T);
-  CUtensorMap tm_h, tm_wg, tm_wu, tm_xc, tm_wt, tm_wt128, tm_vmn, tm_zmn, tm_zk, tm_snap,
+  CUtensorMap tm_h, tm_wg, tm_wu, tm_x0, tm_xc, tm_wt, tm_wt128, tm_vmn, tm_zmn, tm_zk, tm_snap,
       tm_snap_pair, tm_w0d, tm_w0d_pair;
   // As in ittt_forward: a bf16 W_0 is read by the apply itself (no slot-0
   // copy), the GEMMs run on CTA pairs where two can be resident.
@@ -262,6 +262,9 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   if ((s = na_map(&tm_h, H->data, d, M, 64, 128, "H"))) return s;
   if ((s = na_map(&tm_wg, W_gate->data, d, f, 64, 128, "W_gate"))) return s;
   if ((s = na_map(&tm_wu, W_up->data, d, f, 64, 128, "W_up"))) return s;
+  if ((s = na_map(&tm_x0, X0->data, d, M, ittt::kConvMapBoxCols, ittt::kConvMapBoxRows,
+                  "X0 (conv)", CU_TENSOR_MAP_SWIZZLE_NONE)))
+    return s;
   if ((s = na_map(&tm_xc, xc, d, M, 64, 128, "Xc"))) return s;
   if ((s = na_map(&tm_wt, W_target->data, d, d, 64, 256, "W_target"))) return s;
   if ((s = na_map(&tm_wt128, W_target->data, d, d, 64, 128, "W_target (pair)"))) return s;
@@ -301,9 +304,8 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   const bool w0_fp32 = W_down0->dtype == ITTT_FP32;
   cudaError_t e;
   const char* what = nullptr;
-  if ((e = ittt::launch_conv(env, static_cast<const __nv_bfloat16*>(X0->data),
-                             static_cast<const float*>(conv_w->data), xc, int64_t(M), docs,
-                             int(d), ITTT_PAD_CHUNK)) != cudaSuccess) {
+  if ((e = ittt::launch_conv(env, tm_x0, static_cast<const float*>(conv_w->data), xc,
+                             int64_t(M), docs, int(d), ITTT_PAD_CHUNK)) != cudaSuccess) {
     what = "conv";
   } else if ((e = target_pair_or_single(env, tm_xc, tm_wt, tm_wt128, tm_vs,
                                          static_cast<const float*>(conv_w->data), vhat, eta,

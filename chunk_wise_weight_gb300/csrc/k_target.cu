@@ -3,10 +3,10 @@
 // ("[논문리뷰] In-Place Test-Time Training", Method §2 eq. (5); causal
 // padding from Method §3), in two variants with identical results:
 //
-// Split (default): conv3_kernel streams X0 once (a thread owns 8 channels of
-// 4 consecutive token rows: 128-bit loads of the 6-row window, fp32 taps,
-// one bf16 rounding) into Xc, and the target GEMM then TMA-loads Xc as its A
-// operand.
+// Split (default): conv3_kernel streams X0 once into Xc (TMA boxes of 66
+// rows x 256 channels through a shared-memory ring; a thread owns 8 channels
+// of 8 consecutive token rows: fp32 taps, one bf16 rounding), and the target
+// GEMM then TMA-loads Xc as its A operand.
 //
 // Fused: the GEMM builds each A tile itself.  Per 64-channel K block the
 // producer loads, besides the W_target tile, a TMA box of the 130 X0 rows
@@ -63,85 +63,192 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(uint64_t v) {
   return pack_bf16x2(__uint_as_float(uint32_t(v)), __uint_as_float(uint32_t(v >> 32)));
 }
 
-// Rows per thread of conv3_kernel: a thread loads kConvRows + 2 rows of its
-// 8 channels once and writes kConvRows (a sliding window instead of three
-// loads per output row).
-constexpr int kConvRows = 4;
+// conv3_kernel: persistent, two CTAs per SM.  A unit is a tile of 64 token
+// rows x 256 channels.  One producer lane TMA-loads the tile's X0 box with
+// one halo row on each side (66 x 256; rows outside [0, rows) and channels
+// past d read zero) into a ring of three 33 KB shared-memory stages, so about
+// 200 KB per SM are in flight however many registers the compute threads
+// use.  Eight compute warps take eight rows each; lane g owns channels
+// 8g..8g+7 (16 bytes): a warp reads one 512-byte box row without bank
+// conflicts and writes 512 contiguous bytes of Xc per row.  (Measured at
+// 2 x 32k tokens, d 2560: 0.110 ms against 0.115 ms with 32-row tiles and six
+// stages and 0.178 ms for a thread-per-window kernel without the ring; a
+// plain device copy of the same bytes takes 0.105 ms.)
+constexpr int kConvCols = int(kConvMapBoxCols);         // 256
+constexpr int kConvBoxRows = int(kConvMapBoxRows);      // 66
+constexpr int kConvTileRows = kConvBoxRows - 2;         // 64
+constexpr uint32_t kConvRowBytes = kConvCols * 2;                    // 512
+constexpr uint32_t kConvBoxBytes = kConvBoxRows * kConvRowBytes;     // 33792
+constexpr int kConvStages = 3;
+constexpr int kConvComputeWarps = 8;
+constexpr int kConvRowsPerWarp = kConvTileRows / kConvComputeWarps;  // 8
+constexpr int kConvThreads = 32 * (kConvComputeWarps + 1);
+constexpr int kConvCtasPerSm = 2;
+static_assert(kConvBoxBytes % 128 == 0, "stages stay 128-byte aligned for TMA");
 
-__global__ void __launch_bounds__(256)
-    conv3_kernel(const __nv_bfloat16* __restrict__ x0, const float* __restrict__ conv_w,
-                 __nv_bfloat16* __restrict__ xc, int64_t rows, DocMap docs, int d,
-                 int pad_mode) {
+struct __align__(8) ConvSync {
+  uint64_t full[kConvStages];
+  uint64_t empty[kConvStages];
+  int abort_flag;
+};
+
+constexpr size_t kConvSmemBytes = 128 + size_t(kConvStages) * kConvBoxBytes + sizeof(ConvSync);
+
+// Tokens [lo, hi) a tap of token t may read: its document and, with chunk
+// padding, its chunk (chunks start at the document's first token; the last
+// one ends with the document).
+struct TapSpan {
+  int lo, hi;
+};
+
+__device__ __forceinline__ TapSpan tap_span(const DocMap& docs, int t, int pad_mode) {
+  const int k = docs.doc_of_token(t);
+  int lo = docs.start(k);
+  int hi = lo + docs.len(k);
+  if (pad_mode == 0) {
+    lo += ((t - lo) / docs.C) * docs.C;
+    hi = min(lo + docs.C, hi);
+  }
+  return {lo, hi};
+}
+
+__global__ void __launch_bounds__(kConvThreads, kConvCtasPerSm)
+    conv3_kernel(const __grid_constant__ CUtensorMap tm_x0, const float* __restrict__ conv_w,
+                 __nv_bfloat16* __restrict__ xc, int rows, DocMap docs, int d, int pad_mode,
+                 unsigned int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  ConvSync* sync = reinterpret_cast<ConvSync*>(smem + size_t(kConvStages) * kConvBoxBytes);
+  volatile int* abort_flag = &sync->abort_flag;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kConvStages; ++s) {
+      mbar_init(&sync->full[s], 1);
+      mbar_init(&sync->empty[s], 32 * kConvComputeWarps);
+    }
+    sync->abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
   griddep_wait();  // programmatic launch: the previous grid is done
   griddep_launch_dependents();
-  const int groups = d >> 3;
-  const int64_t blocks = (rows + kConvRows - 1) / kConvRows;
-  const int64_t total = blocks * groups;
-  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t rb = idx / groups;
-    const int g = int(idx - rb * groups);
-    const int64_t r0 = rb * kConvRows;
-    // Window rows r0-1 .. r0+kConvRows (those inside the tensor).
-    uint4 x[kConvRows + 2];
-    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int j = 0; j < kConvRows + 2; ++j) {
-      const int64_t r = r0 - 1 + j;
-      x[j] = (r >= 0 && r < rows)
-                 ? __ldg(reinterpret_cast<const uint4*>(x0 + size_t(r) * size_t(d) + size_t(g) * 8))
-                 : zero4;
-    }
-    float w[24];
-    const float4* w4 = reinterpret_cast<const float4*>(conv_w + size_t(g) * 24);
-#pragma unroll
-    for (int q = 0; q < 6; ++q) {
-      const float4 v = __ldg(w4 + q);
-      w[4 * q] = v.x;
-      w[4 * q + 1] = v.y;
-      w[4 * q + 2] = v.z;
-      w[4 * q + 3] = v.w;
-    }
-#pragma unroll
-    for (int j = 0; j < kConvRows; ++j) {
-      const int64_t r = r0 + j;
-      if (r >= rows) break;
-      // Taps stay inside the token's document and, with chunk padding,
-      // inside its chunk (chunks start at the document's first token; the
-      // last one ends with the document).
-      const int t = int(r);
-      const int k = docs.doc_of_token(t);
-      int lo = docs.start(k);
-      int hi = lo + docs.len(k);
-      if (pad_mode == 0) {
-        lo += ((t - lo) / docs.C) * docs.C;
-        hi = min(lo + docs.C, hi);
+  const int ctiles = (d + kConvCols - 1) / kConvCols;
+  const int64_t nunits = int64_t((rows + kConvTileRows - 1) / kConvTileRows) * ctiles;
+
+  if (warp == kConvComputeWarps) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      tma_prefetch_desc(&tm_x0);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0;
+      for (int64_t u = blockIdx.x; u < nunits && !*abort_flag; u += gridDim.x) {
+        if (!mbar_wait(&sync->empty[stage], phase ^ 1u, abort_flag)) {
+          raise_abort(abort_flag, status, kStatusTimeout);
+          break;
+        }
+        const int mt = int(u / ctiles);
+        const int ct = int(u - int64_t(mt) * ctiles);
+        mbar_arrive_expect_tx(&sync->full[stage], kConvBoxBytes);
+        tma_load_2d(smem + size_t(stage) * kConvBoxBytes, &tm_x0, &sync->full[stage],
+                    ct * kConvCols, mt * kConvTileRows - 1);
+        ++issued;
+        if (++stage == kConvStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      const uint4 xm = t - 1 >= lo ? x[j] : zero4;
-      const uint4 xp = t + 1 < hi ? x[j + 2] : zero4;
-      const uint4 xx = x[j + 1];
-      const uint32_t am[4] = {xm.x, xm.y, xm.z, xm.w};
-      const uint32_t a0[4] = {xx.x, xx.y, xx.z, xx.w};
-      const uint32_t ap[4] = {xp.x, xp.y, xp.z, xp.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 fm = unpack_bf16x2(am[q]);
-        const float2 f0 = unpack_bf16x2(a0[q]);
-        const float2 fp = unpack_bf16x2(ap[q]);
-        const int c0 = 2 * q, c1 = 2 * q + 1;  // channel within the group of 8
-        float y0 = w[3 * c0] * fm.x;
-        y0 = fmaf(w[3 * c0 + 1], f0.x, y0);
-        y0 = fmaf(w[3 * c0 + 2], fp.x, y0);
-        float y1 = w[3 * c1] * fm.y;
-        y1 = fmaf(w[3 * c1 + 1], f0.y, y1);
-        y1 = fmaf(w[3 * c1 + 2], fp.y, y1);
-        o[q] = pack_bf16x2(y0, y1);
+      // Let every load still in flight land before the CTA can exit.
+      const int zero = 0;
+      const uint32_t tail = issued < uint32_t(kConvStages) ? issued : uint32_t(kConvStages);
+      for (uint32_t q = issued - tail; q < issued; ++q) {
+        if (!mbar_wait(&sync->full[q % kConvStages], (q / kConvStages) & 1u, &zero))
+          atomicOr(status, kStatusTimeout);
       }
-      *reinterpret_cast<uint4*>(xc + size_t(r) * size_t(d) + size_t(g) * 8) =
-          make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ compute warps
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int64_t u = blockIdx.x; u < nunits; u += gridDim.x) {
+    if (!mbar_wait(&sync->full[stage], phase, abort_flag)) {
+      if (lane == 0) raise_abort(abort_flag, status, kStatusTimeout);
+      break;
+    }
+    const int mt = int(u / ctiles);
+    const int ct = int(u - int64_t(mt) * ctiles);
+    const int t0 = mt * kConvTileRows + warp * kConvRowsPerWarp;
+    const int c = ct * kConvCols + lane * 8;
+    const bool active = c < d && t0 < rows;
+    // Box rows warp*8 .. warp*8+9 hold tokens t0-1 .. t0+8.
+    const uint8_t* box = smem + size_t(stage) * kConvBoxBytes +
+                         size_t(warp * kConvRowsPerWarp) * kConvRowBytes + lane * 16;
+    uint4 o[kConvRowsPerWarp];
+    if (active) {
+      uint4 x[kConvRowsPerWarp + 2];
+#pragma unroll
+      for (int j = 0; j < kConvRowsPerWarp + 2; ++j)
+        x[j] = *reinterpret_cast<const uint4*>(box + j * kConvRowBytes);
+      float w[24];
+      const float4* w4 = reinterpret_cast<const float4*>(conv_w + size_t(c) * 3);
+#pragma unroll
+      for (int q = 0; q < 6; ++q) {
+        const float4 v = __ldg(w4 + q);
+        w[4 * q] = v.x;
+        w[4 * q + 1] = v.y;
+        w[4 * q + 2] = v.z;
+        w[4 * q + 3] = v.w;
+      }
+      TapSpan sp = tap_span(docs, t0, pad_mode);
+#pragma unroll
+      for (int j = 0; j < kConvRowsPerWarp; ++j) {
+        const int t = t0 + j;
+        if (t < rows && t >= sp.hi) sp = tap_span(docs, t, pad_mode);  // next chunk or document
+        const uint4 xm = t - 1 >= sp.lo ? x[j] : zero4;
+        const uint4 xp = t + 1 < sp.hi ? x[j + 2] : zero4;
+        const uint4 xx = x[j + 1];
+        const uint32_t am[4] = {xm.x, xm.y, xm.z, xm.w};
+        const uint32_t a0[4] = {xx.x, xx.y, xx.z, xx.w};
+        const uint32_t ap[4] = {xp.x, xp.y, xp.z, xp.w};
+        uint32_t r[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 fm = unpack_bf16x2(am[q]);
+          const float2 f0 = unpack_bf16x2(a0[q]);
+          const float2 fp = unpack_bf16x2(ap[q]);
+          const int c0 = 2 * q, c1 = 2 * q + 1;  // channel within the group of 8
+          float y0 = w[3 * c0] * fm.x;
+          y0 = fmaf(w[3 * c0 + 1], f0.x, y0);
+          y0 = fmaf(w[3 * c0 + 2], fp.x, y0);
+          float y1 = w[3 * c1] * fm.y;
+          y1 = fmaf(w[3 * c1 + 1], f0.y, y1);
+          y1 = fmaf(w[3 * c1 + 2], fp.y, y1);
+          r[q] = pack_bf16x2(y0, y1);
+        }
+        o[j] = make_uint4(r[0], r[1], r[2], r[3]);
+      }
+    }
+    // Every value this lane read from the stage is consumed above.  Order
+    // those reads before the next TMA write into the stage (a different
+    // proxy), then release the stage: each lane arrives for itself.
+    fence_proxy_async_smem();
+    mbar_arrive(&sync->empty[stage]);
+    if (++stage == kConvStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    if (active) {
+#pragma unroll
+      for (int j = 0; j < kConvRowsPerWarp; ++j)
+        if (t0 + j < rows)
+          *reinterpret_cast<uint4*>(xc + size_t(t0 + j) * size_t(d) + size_t(c)) = o[j];
     }
   }
+  fence_proxy_async_global();  // the target GEMM reads Xc through TMA
 }
 
 struct TargetParams {
@@ -423,16 +530,18 @@ cudaError_t launch_target_variant(const LaunchEnv& env, const TargetParams& p, i
 
 }  // namespace
 
-cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const float* conv_w,
+cudaError_t launch_conv(const LaunchEnv& env, const CUtensorMap& tm_x0, const float* conv_w,
                         __nv_bfloat16* xc, int64_t rows, const DocMap& docs, int d,
                         int pad_mode) {
-  const int64_t total = (rows + kConvRows - 1) / kConvRows * (d / 8);
-  if (total == 0) return cudaSuccess;
-  int64_t blocks = (total + 255) / 256;
-  const int64_t cap = int64_t(env.num_sms) * 8;
-  if (blocks > cap) blocks = cap;
-  return launch_pdl(conv3_kernel, dim3(unsigned(blocks)), dim3(256), 0, env.stream, x0, conv_w,
-                    xc, rows, docs, d, pad_mode);
+  const int64_t units = (rows + kConvTileRows - 1) / kConvTileRows * ((d + kConvCols - 1) / kConvCols);
+  if (units == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(conv3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(kConvSmemBytes));
+  if (e != cudaSuccess) return e;
+  int64_t grid = int64_t(env.num_sms) * kConvCtasPerSm;
+  if (grid > units) grid = units;
+  return launch_pdl(conv3_kernel, dim3(unsigned(grid)), dim3(kConvThreads), kConvSmemBytes,
+                    env.stream, tm_x0, conv_w, xc, int(rows), docs, d, pad_mode, env.status);
 }
 
 cudaError_t launch_target_pair(const LaunchEnv& env, const CUtensorMap& tm_xc,

@@ -636,6 +636,7 @@ __global__ void __launch_bounds__(256)
     }
     *reinterpret_cast<uint4*>(snap + int64_t(docs.first_chunk(int(b))) * df + e) = out;
   }
+  fence_proxy_async_global();  // the apply reads the snapshots through TMA
 }
 
 }  // namespace
@@ -686,6 +687,7 @@ __global__ void __launch_bounds__(256)
     }
     *reinterpret_cast<float4*>(state + e) = acc;
   }
+  fence_proxy_async_global();  // a later walk may read the state with bulk copies
 }
 
 cudaError_t launch_state_prefix(const LaunchEnv& env, const void* w0, int w0_kind,

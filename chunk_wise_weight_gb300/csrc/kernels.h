@@ -136,10 +136,14 @@ cudaError_t launch_gateup_pair(const LaunchEnv& env, const CUtensorMap& tm_h,
                                const CUtensorMap& tm_zs, int M, int f, int K);
 
 // Xc = three-tap depthwise conv of X0 (zero padding at chunk edges, or only
-// at document edges when pad_mode = 1), rounded to bf16.  x0, xc: [rows, d].
-cudaError_t launch_conv(const LaunchEnv& env, const __nv_bfloat16* x0, const float* conv_w,
+// at document edges when pad_mode = 1), rounded to bf16.  tm_x0 maps X0
+// [rows, d] bf16 with box {kConvMapBoxCols, kConvMapBoxRows} and no
+// swizzle; xc: [rows, d].
+cudaError_t launch_conv(const LaunchEnv& env, const CUtensorMap& tm_x0, const float* conv_w,
                         __nv_bfloat16* xc, int64_t rows, const DocMap& docs, int d,
                         int pad_mode);
+// The box launch_conv's X0 map must have: {channels, rows}.
+constexpr uint32_t kConvMapBoxCols = 256, kConvMapBoxRows = 66;
 
 // vhat[M, d] = eta * eta_tok[row] * (Conv1D(X0) W_target^T), rounded once to
 // bf16 (eta_tok may be null: weight 1).

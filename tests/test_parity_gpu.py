@@ -631,6 +631,29 @@ def _stratified(size, block, rng):
     return np.array([s + rng.integers(0, min(block, size - s)) for s in starts])
 
 
+def _rows_differing(a, b):
+    rows = (a != b).reshape(-1, a.shape[-1]).any(dim=1).nonzero().flatten()
+    return f"{len(rows)} rows (first {rows[:6].tolist()})"
+
+
+def _report_mismatch(g, eta, C, got, plain):
+    """The plain call and the exporting call must agree bit for bit; when
+    they do not, run both again and say which call and which stage was off
+    before failing."""
+    again = run(g, eta, C, intermediates=True)
+    plain2 = torch.empty_like(plain)
+    ittt.forward_plain(g["H"], g["X0"], g["W_gate"], g["W_up"], g["W_down0"], g["W_target"],
+                       g["conv_w"], eta, C, plain2)
+    ittt.stream_status()
+    lines = [f"O plain vs export: {_rows_differing(plain, got['O'])}",
+             f"O plain vs plain again: {_rows_differing(plain, plain2)}",
+             f"O export vs export again: {_rows_differing(got['O'], again['O'])}",
+             f"O plain again vs export again: {_rows_differing(plain2, again['O'])}"]
+    for k in ("z_buf", "vhat_buf", "snap_buf"):
+        lines.append(f"{k} export vs export again: {_rows_differing(got[k], again[k])}")
+    pytest.fail("plain and exporting calls differ:\n  " + "\n  ".join(lines))
+
+
 def _sampled_checks(index, device, dual=False, shape=None):
     """Sampled checks for sequences too long for a whole-output comparison.
 
@@ -657,7 +680,8 @@ def _sampled_checks(index, device, dual=False, shape=None):
                        g["conv_w"], eta, C, plain)
     ittt.stream_status()
     assert ittt.plan_form(B, T, d, f, C) == ittt.FORM_PRIMAL
-    assert torch.equal(plain, got["O"]), "bench launch path differs from the checked one"
+    if not torch.equal(plain, got["O"]):
+        _report_mismatch(g, eta, C, got, plain)
     rng = np.random.default_rng(1000 + index)
     for b in sorted({0, B - 1}):
         H, X0 = inp["H"][b], inp["X0"][b]
