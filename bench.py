@@ -33,11 +33,13 @@ sys.path.insert(0, ROOT)
 METRIC = "TTT-MLP tokens/s per layer (d2560/ff9728, 32k ctx); % of GB300 bf16 peak"
 DEFAULT_CONFIG = 2
 # DRAM bytes (read + write) per launch of a kernel at a named workload, from
-# one ncu capture (profiles/traffic_qwen3-4b-layer-B2-T32k-C2048.md), with the
-# hash of the kernel's sources at capture time: once the sources change the
-# figure no longer describes the kernel and `traffic` is reported as null.
+# one ncu capture (profiles/traffic_qwen3-4b-layer-B2-T32k-C2048.md: the
+# kernels of one forward over 1 x 32768 tokens, scaled by the token count to
+# the 2 x 32768 launch), with the hash of the kernel's sources at capture
+# time: once the sources change the figure no longer describes the kernel
+# and `traffic` is reported as null.
 TRAFFIC_BYTES = {
-    (2, "gateup"): (2875250505, "22c3d99b538464a7"),
+    (2, "gateup"): (2580674048, "2cc449219b6d1678"),
 }
 KERNEL_SOURCES = {
     "gateup": ["k_gateup.cu"], "target": ["k_target.cu"], "update": ["k_update.cu"],
