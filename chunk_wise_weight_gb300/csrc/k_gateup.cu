@@ -50,8 +50,11 @@ __device__ __forceinline__ void gateup_epilogue(const GateUpParams& p, int m0, i
       for (int j = 0; j < 16; ++j) {
         const float g0 = __uint_as_float(gv[2 * j]), g1 = __uint_as_float(gv[2 * j + 1]);
         const float u0 = __uint_as_float(uv[2 * j]), u1 = __uint_as_float(uv[2 * j + 1]);
-        const float z0 = g0 / (1.0f + __expf(-g0)) * u0;
-        const float z1 = g1 / (1.0f + __expf(-g1)) * u1;
+        // CUDA's full-precision expf: against the fast __expf intrinsic it
+        // measured no slower and the same Z and O error (both dominated by
+        // the bf16 rounding of Z).
+        const float z0 = g0 / (1.0f + expf(-g0)) * u0;
+        const float z1 = g1 / (1.0f + expf(-g1)) * u1;
         pk[j] = pack_bf16x2(z0, z1);
       }
 #pragma unroll
