@@ -809,22 +809,56 @@ def main():
                     up.wait_event(downloaded[j])
                 e_end.record(up)
 
+        def copies_only(count, h2d, d2h):
+            """The same copies with no compute: host-copy rates in this run."""
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            t0.record(up)
+            down.wait_event(t0)
+            for k in range(count):
+                j = k % 2
+                if h2d:
+                    with torch.cuda.stream(up):
+                        Hs[j].copy_(H_h, non_blocking=True)
+                        X0s[j].copy_(X0_h, non_blocking=True)
+                if d2h:
+                    with torch.cuda.stream(down):
+                        O_h[j].copy_(Os[j], non_blocking=True)
+            up.wait_stream(down)
+            t1.record(up)
+            torch.cuda.synchronize(dev)
+            return t0.elapsed_time(t1) / count
+
+        # At least 30 steps: the first upload and the last download of the
+        # region are not overlapped with compute, and over a short region
+        # they weigh on the average.
+        e2e_n = max(args.steps, 30)
         e2e_steps(3)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(dev)
         torch.cuda.synchronize(dev)
-        e2e_steps(args.steps, e0, e1)
+        e2e_steps(e2e_n, e0, e1)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
-        e2e = {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": H_h.numel() * 2 + X0_h.numel() * 2,
-               "d2h_bytes_per_step": O_h[0].numel() * 2,
+        h2d_b = H_h.numel() * 2 + X0_h.numel() * 2
+        d2h_b = O_h[0].numel() * 2
+        ms_up = copies_only(e2e_n, True, False)
+        ms_down = copies_only(e2e_n, False, True)
+        ms_both = copies_only(e2e_n, True, True)
+        e2e = {"value": B * T * world * e2e_n / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
+               "steps": e2e_n,
                "note": "per step: H2D of H and X0 from pinned host memory, ittt_forward, D2H "
                        "of O to pinned host memory; copies overlap compute on two buffer "
                        "sets; weights stay resident",
                "pinned_on": (f"the GPU's NUMA node ({len(near)} CPUs)" if near
-                             else "the allocating thread's node")}
+                             else "the allocating thread's node"),
+               "copies_alone": {"h2d_gbs": round(h2d_b / ms_up / 1e6, 1),
+                                "d2h_gbs": round(d2h_b / ms_down / 1e6, 1),
+                                "both_ms_per_step": round(ms_both, 3),
+                                "both_gbs": round((h2d_b + d2h_b) / ms_both / 1e6, 1),
+                                "note": "the same copies with no compute, same run"}}
         ittt.stream_status(stream)
 
     if rank == 0:
