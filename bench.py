@@ -267,18 +267,22 @@ def phase_model(B, T, d, f, C, dual=False, cu=None):
     }
 
 
-def launches_per_step(B, T, C, cu, l2norm, dual=False):
+def launches_per_step(B, T, C, cu, l2norm, dual=False, d=2560, f=9728, pairs=76):
     """Kernel launches of one forward with the bench's bf16 W_down0 and no
-    snapshot buffer: conv, target, gate/up, the update walk (one launch, or
-    with L2 normalisation one per chunk that updates plus a finalising
-    launch), apply (the apply reads W_0 itself, so no snapshot-0 copy);
-    packed documents add the table-staging kernel; the dual form runs scores
-    and dual apply instead of walk and apply."""
+    snapshot buffer: conv, target, gate/up, the update walk, apply (the
+    apply reads W_0 itself, so no snapshot-0 copy); packed documents add the
+    table-staging kernel; the dual form runs scores and dual apply instead of
+    walk and apply.  The walk is one launch; with L2 normalisation too when
+    the batch is regular, d a multiple of 256, every chunk a multiple of 64
+    tokens and a group of ceil(f/256) CTA pairs fits in the GPU's 76 (the
+    state stays in TMEM), else one launch per chunk that updates plus a
+    finalising launch."""
     lens = [b - a for a, b in zip(cu, cu[1:])] if cu else [T] * B
     steps = max(-(-L // C) - 1 for L in lens)
     if dual:
         return 5
-    walk = (steps + 1 if l2norm else 1) if steps > 0 else 0
+    in_tmem = not cu and d % 256 == 0 and C % 64 == 0 and -(-f // 256) <= pairs
+    walk = (steps + 1 if l2norm and not in_tmem else 1) if steps > 0 else 0
     return 4 + walk + (1 if cu else 0)
 
 
@@ -880,7 +884,7 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": launches_per_step(B, T, C, cu, args.l2norm, form_dual) * args.steps,
+            "gpu_launches": launches_per_step(B, T, C, cu, args.l2norm, form_dual, d, f) * args.steps,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

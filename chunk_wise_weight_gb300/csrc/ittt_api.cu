@@ -305,7 +305,7 @@ ittt_status check_sizes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chun
 // --------------------------------------------------------------- planning
 struct Layout {
   size_t z = 0, vhat = 0, xc = 0, snap = 0, scores = 0, w0b = 0, table = 0, state = 0,
-         partial = 0, total = 0;
+         partial = 0, walk_part = 0, walk_arrive = 0, total = 0;
 };
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -522,8 +522,12 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   if (P->packed) L.table = take(P->table.size() * sizeof(int));
   if (P->l2norm && P->n_udocs > 0) {
     L.state = take(size_t(P->ndocs) * ((d + 127) / 128) * ((f + 31) / 32) * 128 * 32 * 4);
-    // row partial sums per 512-column block, in two 128-column parts of its halves
-    L.partial = take(size_t(2) * P->ndocs * 2 * ((f + 511) / 512) * d * 4);
+    // row partial sums per 256-column block of the state, in two 128-column parts
+    L.partial = take(size_t(2) * P->ndocs * 2 * ((f + 255) / 256) * d * 4);
+    if (!P->packed) {  // the walk with the state in TMEM (used when the pairs fit)
+      L.walk_part = take(ittt::norm_walk_part_bytes(int(f), ittt::kNormWalkMaxPairs));
+      L.walk_arrive = take(ittt::norm_walk_arrive_bytes(ittt::kNormWalkMaxPairs));
+    }
   }
   L.total = off;
   return ITTT_OK;
@@ -887,6 +891,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
       na.w0_bstride = w0_bstride;
       na.state = reinterpret_cast<float*>(ws + L.state);
       na.partial = reinterpret_cast<float*>(ws + L.partial);
+      na.walk_part = P.packed ? nullptr : reinterpret_cast<float*>(ws + L.walk_part);
+      na.walk_arrive = P.packed ? nullptr : reinterpret_cast<unsigned int*>(ws + L.walk_arrive);
+      na.walk_pairs = ittt::kNormWalkMaxPairs;
       na.snap = snap;
       na.state_out = ua.state_out;
       na.allow_pairs = !P.ragged_walk && !single && d % 256 == 0;

@@ -340,8 +340,8 @@ struct NormUpdateParams {
   int w0_fp32;
   int64_t w0_bstride;
   float* state;          // S, tiled: [documents][ceil(d/128)][ceil(f/32)] tiles of 4096 fp32
-  float* partial;        // [2][documents][2 * np][d] row sums of squares per 512-column
-                         // unit and 128-column part of its halves
+  float* partial;        // [2][documents][nparts][d] row sums of squares per 256-column
+                         // block of the state, in two 128-column parts
   __nv_bfloat16* snap;   // [slots, d, f]
   DocMap docs;
   const int* upd_docs;   // updating documents, most updates first; nullptr: all
@@ -350,7 +350,7 @@ struct NormUpdateParams {
   int d, f, mt, np, ncb;  // mt: row blocks of a unit (128 rows, 256 on CTA pairs);
                           // ncb: 32-column tiles per 128-row block
   int mtb;                // 128-row blocks of the state (its tile layout)
-  int nparts;             // partial sums per row: 2 * np
+  int nparts;             // partial sums per row: 2 per 256-column block
 };
 
 // First fp32 of S's tile (document, 128-row block, 32-column block).
@@ -378,16 +378,15 @@ struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults>
   static constexpr int kEpilogueGroups = kPair ? 2 : 1;
   static constexpr int kNumStages = kPair ? 5 : 4;
   static constexpr int kGroupCols = kBN / kEpilogueGroups;  // columns of a half per group
-  // A row's sum of squares is kept per 512-column unit in two parts (columns
-  // 0-127 and 128-255 of each half): the two epilogue groups on pairs each
-  // own one part, a single CTA sums both in the same order, so both walks
-  // round alike.
+  // A row's sum of squares is kept per 256-column block of the state (one
+  // half) in two parts, columns 0-127 and 128-255: the two epilogue groups
+  // on pairs each own one part, a single CTA sums both in the same order,
+  // so both walks round alike.
   static constexpr int kPartCols = 128;
 
   const Params& p;
   const int rank;
   int doc = 0, tok = 0, clen = 0, slot = 0, m0 = 0, nbase = 0, npi = 0, halves = 1;
-  mutable float ss_carry[2] = {0.f, 0.f};  // this row's sums of squares per part, over halves
 
   __device__ explicit NormUpdateSchedT(const Params& pp, uint32_t r = 0) : p(pp), rank(int(r)) {}
   __device__ int num_units() const { return p.n_active * p.mt * p.np; }
@@ -511,7 +510,7 @@ struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults>
     const bool row_ok = m < p.d;
     const int n0 = nbase + s * kBN;
     const int c_begin = st.group * kGroupCols, c_end = c_begin + kGroupCols;
-    float ss0 = s == 0 ? 0.f : ss_carry[0], ss1 = s == 0 ? 0.f : ss_carry[1];
+    float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll 1
     for (int c = c_begin; c < c_end; c += 32) {
       uint32_t v[32];
@@ -542,11 +541,10 @@ struct NormUpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults>
         if (first) ss0 = a; else ss1 = a;
       }
     }
-    ss_carry[0] = ss0;
-    ss_carry[1] = ss1;
-    if (row_ok && s == halves - 1) {
-      if (c_begin < kPartCols) __stcg(p.partial + partial_at((p.i + 1) & 1, npi * 2, m), ss0);
-      if (c_end > kPartCols) __stcg(p.partial + partial_at((p.i + 1) & 1, npi * 2 + 1, m), ss1);
+    if (row_ok) {
+      const int blk = 2 * (2 * npi + s);  // this half's 256-column block, part 0
+      if (c_begin < kPartCols) __stcg(p.partial + partial_at((p.i + 1) & 1, blk, m), ss0);
+      if (c_end > kPartCols) __stcg(p.partial + partial_at((p.i + 1) & 1, blk + 1, m), ss1);
     }
   }
 };
@@ -562,6 +560,266 @@ __global__ void __launch_bounds__(PipeShape<NormUpdateSched>::kThreads, 1)
 __global__ void __launch_bounds__(pair_threads<NormUpdatePairSched>(), 1)
     norm_update_pair_kernel(const __grid_constant__ NormUpdateParams p, unsigned int* status) {
   run_pipeline_pair<NormUpdatePairSched>(p, status);
+}
+
+// ----------------------------------------------------------------------------
+// The normalised walk with the fp32 state resident in TMEM (regular batches on
+// CTA pairs; "[논문리뷰] Test-Time Training Done Right", Non-Linear Update of
+// Fast-Weight, rows normalised over d_ff after every update).
+//
+// The row norm couples every column block of a row, so the CTA pairs that
+// hold one row block's column blocks form a group that exchanges row sums of
+// squares at every chunk boundary; the fp32 state itself never leaves the
+// chip.  With nf = ceil(f / 256) column blocks, G = floor(pairs / nf) groups
+// of nf pairs run at once (f = 9728: 38 blocks, two groups filling 76 pairs).
+// A row task is (sequence b, 256-row block m); round r gives group g's
+// accumulator h the task 2Gr + Gh + g, and pair j of the group its column
+// block j.  Each pair so walks two independent 256 x 256 blocks of the state
+// (one per TMEM accumulator, rows of different tasks), alternating chunk by
+// chunk: while the tensor core adds chunk i's delta to one block, the
+// epilogue normalises the other.
+//
+// At a boundary the epilogue of accumulator h (state S_{i+1} = W_i + eta
+// dW_i in TMEM):
+//   1. sums the squares of its row over its 128 columns (one part per
+//      epilogue group, as the per-launch walk does) and publishes the sum;
+//   2. arrives on its (accumulator, group) counter and waits until every CTA
+//      of the group has published (a bounded spin on the counter);
+//   3. adds the 2 nf partial sums of its row in block order, forms
+//      W_{i+1} = S_{i+1} / ||row||, writes it back into TMEM for the next
+//      chunk and out as the bf16 snapshot (or, after the last update, the
+//      fp32 state_out).
+// The arithmetic (partial sums per 256-column block and 128-column part,
+// their order, the scale, the chunk's delta added onto W_i by the tensor
+// core) is the per-launch walk's, so both give the same bits.  Every CTA of
+// the grid must be resident at once: the launch is exactly G nf pairs, no
+// more than can be resident.
+// ----------------------------------------------------------------------------
+struct NormWalkParams {
+  CUtensorMap tm_v;      // eta*Vhat [M, d]  box {64, 64}
+  CUtensorMap tm_z;      // Z        [M, f]  box {64, 64}
+  CUtensorMap tm_ss;     // snapshots as [slots][d rows][f cols] bf16, box {64, 128, 1} (store)
+  const void* w0;
+  int w0_fp32;
+  int64_t w0_bstride;
+  float* state_out;      // [B, d, f] fp32, or nullptr
+  float* part;           // [2][G][2][nparts][256] row sums of squares
+  unsigned int* arrive;  // [2][G] arrival counters, zero at launch
+  int B, T, C, n, nupd;  // sequences, tokens each, chunk, chunks, updates per sequence
+  int d, f, nd, nf, G, nparts, rounds;
+};
+
+// sum_partials' sum of one row's `n` partial sums, `stride` floats apart:
+// the same four accumulators in the same order, fed by loads issued 64 at a
+// time instead of four.
+__device__ __forceinline__ float sum_partials_batched(const float* base, size_t stride, int n) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  const int full = n & ~3;
+#pragma unroll 1
+  for (int b0 = 0; b0 < full; b0 += 64) {
+    float v[64];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) v[j] = b0 + j < full ? __ldcg(base + size_t(b0 + j) * stride) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 64; j += 4) {
+      if (b0 + j < full) {
+        a0 += v[j];
+        a1 += v[j + 1];
+        a2 += v[j + 2];
+        a3 += v[j + 3];
+      }
+    }
+  }
+  for (int b = full; b < n; ++b) a0 += __ldcg(base + size_t(b) * stride);
+  return (a0 + a1) + (a2 + a3);
+}
+
+struct NormWalkSched : PairDefaults {
+  using Params = NormWalkParams;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, kBN, true, true);
+  static constexpr bool kPreload = true;
+  static constexpr bool kStagedStores = true;
+  static constexpr bool kStagedPreload = true;
+  static constexpr bool kBindsSync = true;
+  static constexpr int kEpilogueGroups = 2;
+  static constexpr int kNumStages = 5;
+  static constexpr int kGroupCols = kBN / kEpilogueGroups;  // 128: one part
+
+  const Params& p;
+  const int rank;
+  int nh = 0, g = 0, fb = 0, rnd = 0;
+  int doc0 = 0, doc1 = 0, m00 = 0, m01 = 0;  // per accumulator: sequence, first row
+  volatile int* abort_flag = nullptr;
+  unsigned int* status = nullptr;
+  mutable bool broken = false;  // a group wait ran out: do not wait again
+
+  __device__ NormWalkSched(const Params& pp, uint32_t r) : p(pp), rank(int(r)) {}
+  __device__ void bind_sync(volatile int* a, unsigned int* st) {
+    abort_flag = a;
+    status = st;
+  }
+  __device__ int num_units() const { return p.rounds * p.G * p.nf; }
+  __device__ void begin_unit(int u, int) {
+    const int per = p.G * p.nf;
+    rnd = u / per;
+    const int pr = u - rnd * per;
+    g = pr / p.nf;
+    fb = pr - g * p.nf;
+    const int t0 = rnd * 2 * p.G + g, t1 = t0 + p.G;
+    const int tasks = p.B * p.nd;
+    nh = t1 < tasks ? 2 : (t0 < tasks ? 1 : 0);
+    doc0 = t0 / p.nd;
+    doc1 = t1 / p.nd;
+    m00 = (t0 - doc0 * p.nd) * (2 * kBM) + rank * kBM;
+    m01 = (t1 - doc1 * p.nd) * (2 * kBM) + rank * kBM;
+  }
+  __device__ int doc_of(int h) const { return h ? doc1 : doc0; }
+  __device__ int row0_of(int h) const { return h ? m01 : m00; }
+  __device__ int num_segments() const { return p.nupd * nh; }
+  __device__ int unit_accs() const { return nh; }
+  __device__ int seg_acc(int s) const { return nh == 2 ? (s & 1) : 0; }
+  __device__ int seg_chunk(int s) const { return nh == 2 ? (s >> 1) : s; }
+  __device__ int seg_kblocks(int s) const {
+    return (min(p.C, p.T - seg_chunk(s) * p.C) + kBK - 1) / kBK;
+  }
+  __device__ bool seg_fresh(int) const { return false; }  // onto W_i in TMEM
+  // This CTA's 128 rows of eta*Vhat^T and its 128 of the block's 256 Z
+  // columns, two 64-wide boxes each.
+  __device__ void load(int s, int kb, uint8_t* stage, uint32_t bar) const {
+    const int h = seg_acc(s);
+    const int tok = doc_of(h) * p.T + seg_chunk(s) * p.C + kb * kBK;
+    const int n0 = fb * kBN + rank * kBM;
+    tma_load_2d_pair(stage, &p.tm_v, bar, row0_of(h), tok);
+    tma_load_2d_pair(stage + kMnBoxBytes, &p.tm_v, bar, row0_of(h) + 64, tok);
+    tma_load_2d_pair(stage + kPairATileBytes, &p.tm_z, bar, n0, tok);
+    tma_load_2d_pair(stage + kPairATileBytes + kMnBoxBytes, &p.tm_z, bar, n0 + 64, tok);
+  }
+  static __device__ uint64_t a_desc(uint32_t base, int k) { return mn_desc(base, k); }
+  static __device__ uint64_t b_desc(uint32_t base, int k) { return mn_desc(base, k); }
+
+  // W_0 (as given, not normalised) into accumulator h: this group's 128
+  // columns of this row.
+  __device__ void preload(int h, int row, uint32_t trow, EpiStager& st) const {
+    const int m = row0_of(h) + row;
+    const int n0 = fb * kBN;
+    const int c_begin = st.group * kGroupCols;
+    const size_t off = size_t(doc_of(h)) * size_t(p.w0_bstride) + size_t(m) * size_t(p.f);
+#pragma unroll 1
+    for (int c = c_begin; c < c_begin + kGroupCols; c += 32) {
+      uint32_t v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int col = n0 + c + 8 * q;
+        float w[8];
+        load_w0_8(p.w0, p.w0_fp32 != 0, off + col, col < p.f, w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[8 * q + j] = __float_as_uint(w[j]);
+      }
+      tmem_st_32cols(trow + uint32_t(c), v);
+    }
+  }
+
+  // Publish, exchange within the group, normalise (see above).
+  __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& st) const {
+    const int h = seg_acc(s);
+    const int i = seg_chunk(s);
+    const int k = rnd * p.nupd + i;  // boundaries this (accumulator, group) passed before
+    const int m = row0_of(h) + row;
+    const int n0 = fb * kBN;
+    const int c_begin = st.group * kGroupCols, c_end = c_begin + kGroupCols;
+    const int prow = rank * kBM + row;  // this row within the 256-row block
+    const float* pbase =
+        p.part + ((size_t(h) * p.G + g) * 2 + (k & 1)) * size_t(p.nparts) * (2 * kBM) + prow;
+    // 1. this part's sum of squares of S_{i+1}
+    float a = 0.f;
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; c += 32) {
+      uint32_t v[32];
+      tmem_ld_32cols(trow + uint32_t(c), v);
+      tmem_wait_ld();
+      pin_regs(v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (n0 + c + j < p.f) {
+          const float x = __uint_as_float(v[j]);
+          a = fmaf(x, x, a);
+        }
+      }
+    }
+    __stcg(const_cast<float*>(pbase) + size_t(2 * fb + st.group) * (2 * kBM), a);
+    // 2. every CTA of the group has published
+    epilogue_all_bar();
+    if (st.group == 0 && row == 0) {
+      unsigned int* ctr = p.arrive + h * p.G + g;
+      __threadfence();
+      atomicAdd(ctr, 1u);
+      if (!broken) {
+        const unsigned int want = 2u * unsigned(p.nf) * unsigned(k + 1);
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(ctr) < want) {
+          if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+            broken = true;
+            atomicOr(status, kStatusTimeout);
+            break;
+          }
+          __nanosleep(128);
+        }
+      }
+    }
+    epilogue_all_bar();
+    // 3. W_{i+1} = S_{i+1} / ||row||: into TMEM, out as snapshot or state_out
+    const float scale = row_scale_of(sum_partials_batched(pbase, 2 * kBM, p.nparts));
+    const bool last = (i + 1) == p.nupd;
+    const bool write_snap = (i + 1) < p.n;
+    float* so = (p.state_out != nullptr && last)
+                    ? p.state_out + (size_t(doc_of(h)) * p.d + m) * size_t(p.f)
+                    : nullptr;
+    const int slot = doc_of(h) * p.n + i + 1;
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; c += 64) {
+      uint8_t* buf = write_snap ? st.acquire() : nullptr;
+#pragma unroll 1
+      for (int hc = 0; hc < 2; ++hc) {
+        const int cc = c + 32 * hc;
+        uint32_t v[32];
+        tmem_ld_32cols(trow + uint32_t(cc), v);
+        tmem_wait_ld();
+        pin_regs(v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * scale);
+        if (!last) tmem_st_32cols(trow + uint32_t(cc), v);
+        if (write_snap) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            st.put(buf, hc * 4 + q,
+                   make_uint4(
+                       pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                       pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]))));
+        }
+        if (so != nullptr) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int col = n0 + cc + 8 * q;
+            if (col < p.f) {
+              uint4* dst = reinterpret_cast<uint4*>(so + col);
+              dst[0] = make_uint4(v[8 * q], v[8 * q + 1], v[8 * q + 2], v[8 * q + 3]);
+              dst[1] = make_uint4(v[8 * q + 4], v[8 * q + 5], v[8 * q + 6], v[8 * q + 7]);
+            }
+          }
+        }
+      }
+      if (write_snap)
+        st.commit(buf, [&](uint8_t* src) { tma_store_3d(&p.tm_ss, src, n0 + c, row0_of(h), slot); });
+    }
+    if (!last) tmem_wait_st();  // the next chunk's MMAs add onto W_{i+1}
+  }
+};
+
+__global__ void __launch_bounds__(pair_threads<NormWalkSched>(), 1)
+    norm_walk_pair_kernel(const __grid_constant__ NormWalkParams p, unsigned int* status) {
+  run_pipeline_pair<NormWalkSched>(p, status);
 }
 
 // The last state of each updating document, normalised: into state_out
@@ -755,10 +1013,80 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
                     pipe_smem_bytes<UpdateSched>(), env.stream, p, env.status);
 }
 
+size_t norm_walk_part_bytes(int f, int pairs) {
+  const int nf = (f + kBN - 1) / kBN;
+  const int groups = pairs / nf > 0 ? pairs / nf : 1;
+  return size_t(2) * groups * 2 * size_t(2 * nf) * (2 * kBM) * sizeof(float);
+}
+
+size_t norm_walk_arrive_bytes(int pairs) { return size_t(2) * pairs * sizeof(unsigned int); }
+
+namespace {
+
+// The walk with the state in TMEM, when the batch is regular, CTA pairs are
+// allowed and at least one group of pairs (one per 256-column block) can be
+// resident.  Returns cudaErrorNotSupported (nothing enqueued) otherwise.
+cudaError_t launch_norm_walk(const LaunchEnv& env, const CUtensorMap& tm_vhat,
+                             const CUtensorMap& tm_z, const CUtensorMap& tm_snap_store,
+                             const NormUpdateArgs& a) {
+  if (!a.allow_pairs || a.docs.packed() || a.walk_part == nullptr || a.walk_arrive == nullptr ||
+      a.upd_docs != nullptr || a.n_udocs != a.docs.ndocs)
+    return cudaErrorNotSupported;
+  const int nf = (a.f + kBN - 1) / kBN;
+  static std::atomic<int> resident{-1};
+  const size_t smem = pair_smem_bytes<NormWalkSched>();
+  cudaError_t e = cudaFuncSetAttribute(norm_walk_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  int pairs = 0;
+  if ((e = max_pairs(reinterpret_cast<const void*>(norm_walk_pair_kernel), smem, env, &pairs,
+                     &resident, pair_threads<NormWalkSched>())) != cudaSuccess)
+    return e;
+  if (pairs > a.walk_pairs) pairs = a.walk_pairs;
+  const int G = pairs / nf;
+  if (G < 1) return cudaErrorNotSupported;
+  NormWalkParams p;
+  memset(&p, 0, sizeof(p));
+  p.tm_v = tm_vhat;
+  p.tm_z = tm_z;
+  p.tm_ss = tm_snap_store;
+  p.w0 = a.w0;
+  p.w0_fp32 = a.w0_fp32 ? 1 : 0;
+  p.w0_bstride = a.w0_bstride;
+  p.state_out = a.state_out;
+  p.part = a.walk_part;
+  p.arrive = a.walk_arrive;
+  p.B = a.docs.ndocs;
+  p.T = a.docs.T;
+  p.C = a.docs.C;
+  p.n = a.docs.n;
+  p.nupd = a.n_steps;
+  p.d = a.d;
+  p.f = a.f;
+  p.nd = a.d / (2 * kBM);
+  p.nf = nf;
+  p.G = G;
+  p.nparts = 2 * nf;
+  const int tasks = p.B * p.nd;
+  p.rounds = (tasks + 2 * G - 1) / (2 * G);
+  if ((e = cudaMemsetAsync(a.walk_arrive, 0, norm_walk_arrive_bytes(G), env.stream)) !=
+      cudaSuccess)
+    return e;
+  return launch_on_pairs(reinterpret_cast<const void*>(norm_walk_pair_kernel), G * nf, smem, env,
+                         &p, pair_threads<NormWalkSched>());
+}
+
+}  // namespace
+
 cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
                                const CUtensorMap& tm_z, const CUtensorMap& tm_snap_store,
                                const NormUpdateArgs& a) {
   if (a.n_udocs <= 0) return cudaSuccess;
+  {
+    const cudaError_t e = launch_norm_walk(env, tm_vhat, tm_z, tm_snap_store, a);
+    if (e != cudaErrorNotSupported) return e;
+    cudaGetLastError();
+  }
   NormUpdateParams p;
   p.tm_v = tm_vhat;
   p.tm_z = tm_z;
@@ -793,7 +1121,7 @@ cudaError_t launch_norm_update(const LaunchEnv& env, const CUtensorMap& tm_vhat,
   }
   const bool use_pairs = pairs >= 1;
   p.mt = use_pairs ? (a.d + 2 * kBM - 1) / (2 * kBM) : p.mtb;
-  p.nparts = 2 * p.np;
+  p.nparts = 2 * ((a.f + kBN - 1) / kBN);
   if (!use_pairs &&
       (e = cudaFuncSetAttribute(norm_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 int(pipe_smem_bytes<NormUpdateSched>()))) != cudaSuccess)

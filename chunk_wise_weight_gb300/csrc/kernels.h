@@ -208,10 +208,24 @@ struct NormUpdateArgs {
   __nv_bfloat16* snap;  // [slots, d, f]: slots 1..n-1 of each document written
   float* state_out;     // [documents, d, f] fp32 or nullptr
   bool allow_pairs;     // every updated chunk a multiple of 64 tokens and d of 256
+  // Scratch of the walk with the state resident in TMEM (regular batches on
+  // CTA pairs; nullptr: not available): row sums of squares for up to
+  // walk_pairs CTA pairs, and 2 x walk_pairs arrival counters.
+  float* walk_part;
+  unsigned int* walk_arrive;
+  int walk_pairs;
 };
 
+// Bytes of that scratch for d_ff = f and up to `pairs` CTA pairs.
+size_t norm_walk_part_bytes(int f, int pairs);
+size_t norm_walk_arrive_bytes(int pairs);
+constexpr int kNormWalkMaxPairs = 128;
+
 // The fast-weight walk with L2 normalisation of every updated state, rows
-// over d_ff (one launch per chunk, then one finalising launch).  Tensor maps:
+// over d_ff.  Regular batches on CTA pairs keep the fp32 state in TMEM for
+// the whole walk (one launch; the pairs holding a row block exchange row sums
+// of squares at every chunk boundary); otherwise one launch per chunk with
+// the state in HBM, then one finalising launch.  Tensor maps:
 // eta*Vhat and Z as for launch_update; the snapshots as [slots][d][f] with
 // box {64,128,1} for TMA stores.  Runs on CTA pairs when allowed and two can
 // be resident, else on single CTAs.

@@ -140,6 +140,11 @@ struct SchedDefaults {
   static constexpr int kEpilogueGroups = 1;
   // Transaction bytes the producer's copies deliver into a stage.
   __device__ uint32_t tma_bytes(int, int) const { return kStageBytes; }
+  // With kBindsSync (CTA-pair pipeline only) the epilogue's schedule gets
+  // the CTA's abort flag and the device status word before its first unit:
+  //   void bind_sync(volatile int* abort_flag, unsigned int* status)
+  // for epilogues that wait on other CTAs.
+  static constexpr bool kBindsSync = false;
 };
 
 template <class S>

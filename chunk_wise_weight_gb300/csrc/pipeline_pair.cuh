@@ -233,6 +233,7 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
     // ------------------------------------------------------------- epilogue
     S sched(p, rank);
     S next(p, rank);
+    if constexpr (S::kBindsSync) sched.bind_sync(abort_flag, status);
     const int group = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
@@ -267,7 +268,16 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
         const int h = sched.seg_acc(s);
         bool got = __all_sync(0xffffffffu, mbar_wait(&sync->acc_full[h], acc_use[h] & 1u,
                                                      abort_flag));
-        if constexpr (S::kStagedStores) {
+        if constexpr (S::kBindsSync) {
+          // One vote over both groups: such an epilogue meets the other
+          // group at CTA-wide barriers, so the groups unwind together.
+          static_assert(S::kEpilogueGroups == 2, "CTA-wide vote over two groups");
+          volatile int* vote = sync->vote;
+          if (lane == 0) vote[warp - 2] = got ? 1 : 0;
+          epilogue_all_bar();
+          got = (vote[0] & vote[1] & vote[2] & vote[3] & vote[4] & vote[5] & vote[6] & vote[7]) != 0;
+          epilogue_all_bar();
+        } else if constexpr (S::kStagedStores) {
           volatile int* vote = sync->vote + 4 * group;
           if (lane == 0) vote[quad] = got ? 1 : 0;
           epilogue_group_bar(group);

@@ -178,6 +178,18 @@ __device__ __forceinline__ void epilogue_bar() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// Barrier among the 256 threads of both epilogue groups (named barrier 3).
+__device__ __forceinline__ void epilogue_all_bar() {
+  asm volatile("bar.sync 3, 256;" ::: "memory");
+}
+
+// Load of a counter that other CTAs increment, acquiring their writes.
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -194,11 +194,16 @@ def test_workspace_bytes_and_launch_count(lib):
     want_packed = (r(T * f * 2) + 2 * r(T * d * 2) + r(5 * d * f * 2)
                    + r((6 + 5 + 12 + 2) * 4))
     assert ittt.workspace_bytes_ex(1, T, d, f, C, cu_seqlens=cu) == want_packed
-    # the normalised walk keeps an fp32 state and row partial sums
-    nblk = -(-f // 512)
+    # the normalised walk keeps an fp32 state and row partial sums per
+    # 256-column block (for the walk with the state in HBM), and, for a
+    # regular batch, the row sums and arrival counters of the walk with the
+    # state in TMEM (groups of ceil(f/256) CTA pairs, up to 128 pairs)
+    nblk = -(-f // 256)
     tiles = -(-d // 128) * -(-f // 32)      # the fp32 state in 128 x 32 tiles
+    groups = max(1, 128 // nblk)
+    walk = r(2 * groups * 2 * (2 * nblk) * 256 * 4) + r(2 * 128 * 4)
     assert (ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True)
-            == want + r(B * tiles * 128 * 32 * 4) + r(2 * B * 2 * nblk * d * 4))
+            == want + r(B * tiles * 128 * 32 * 4) + r(2 * B * 2 * nblk * d * 4) + walk)
     assert ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True, dual=True) == 0
     assert ittt.launch_count(B, T, d, f, C) == 5
     assert ittt.launch_count(B, T, d, f, T) == 4

@@ -418,15 +418,20 @@ L2 = [
 
 
 L2_PAIRS = [
-    # d a multiple of 256 and every chunk a multiple of 64 tokens: the walk
-    # runs on CTA pairs
-    (2, 640, 256, 584, 128, 0.05),     # odd 256-column halves, chunks 128 x 5
+    # d a multiple of 256 and every chunk a multiple of 64 tokens: a regular
+    # batch runs the walk with the state in TMEM on CTA pairs
+    (2, 640, 256, 584, 128, 0.05),     # three 256-column blocks, chunks 128 x 5
     (1, 512, 512, 1000, 256, 0.02),    # two 256-row blocks, ragged d_ff
+    (3, 512, 256, 9728, 128, 0.05),    # 38 column blocks: two groups of 38 pairs, 2 rounds
 ]
 
 
 @pytest.mark.parametrize("B,T,d,f,C,eta", L2_PAIRS)
 def test_l2norm_pairs_parity_and_single_cta_bitwise(cuda_device, B, T, d, f, C, eta):
+    """The walk with the state in TMEM (regular batch on CTA pairs) against
+    the oracle, and bit for bit against the walk with the state in HBM on
+    single CTAs and on CTA pairs (forced by packing the same sequences as
+    documents): all three sum the same partial sums in the same order."""
     inp = make_inputs(B, T, d, f, seed=1150 + T + d)
     ref = oracle.forward(inp, eta, C, want_states=True, l2norm=True)
     g = to_device(inp, cuda_device)
@@ -436,6 +441,13 @@ def test_l2norm_pairs_parity_and_single_cta_bitwise(cuda_device, B, T, d, f, C, 
     assert_parity(host(got["state_out"]), ref["states"][:, n], "normalised final state")
     assert_parity(host(got["O"]), ref["O"], "O")
     one = run(g, eta, C, intermediates=True, want_state=True, l2norm=True, single_cta=True)
+    assert_parity(host(one["O"]), ref["O"], "O (state in HBM, single CTAs)")
+    cu = [b * T for b in range(B + 1)]
+    pk = {k: v.reshape(1, B * T, d) if k in ("H", "X0") else v for k, v in g.items()}
+    packed = run(pk, eta, C, intermediates=True, want_state=True, l2norm=True, cu_seqlens=cu)
+    assert torch.equal(packed["O"].reshape(B, T, d), one["O"])
+    assert torch.equal(packed["state_out"], one["state_out"])
+    assert torch.equal(packed["snap_buf"].reshape(B, n, d, f), one["snap_buf"])
     for k in ("snap_buf", "state_out", "O"):
         assert torch.equal(one[k], got[k]), k
 
