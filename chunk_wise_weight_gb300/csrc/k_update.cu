@@ -641,9 +641,10 @@ struct NormWalkSched : PairDefaults {
   static constexpr bool kStagedStores = true;
   static constexpr bool kStagedPreload = true;
   static constexpr bool kBindsSync = true;
+  static constexpr bool kAccTeams = true;   // epilogue group h owns accumulator h
   static constexpr int kEpilogueGroups = 2;
   static constexpr int kNumStages = 5;
-  static constexpr int kGroupCols = kBN / kEpilogueGroups;  // 128: one part
+  static constexpr int kPartCols = 128;     // a row's sum of squares in two parts
 
   const Params& p;
   const int rank;
@@ -697,15 +698,14 @@ struct NormWalkSched : PairDefaults {
   static __device__ uint64_t a_desc(uint32_t base, int k) { return mn_desc(base, k); }
   static __device__ uint64_t b_desc(uint32_t base, int k) { return mn_desc(base, k); }
 
-  // W_0 (as given, not normalised) into accumulator h: this group's 128
-  // columns of this row.
-  __device__ void preload(int h, int row, uint32_t trow, EpiStager& st) const {
+  // W_0 (as given, not normalised) into accumulator h: this row's 256
+  // columns (the group that owns the accumulator).
+  __device__ void preload(int h, int row, uint32_t trow, EpiStager&) const {
     const int m = row0_of(h) + row;
     const int n0 = fb * kBN;
-    const int c_begin = st.group * kGroupCols;
     const size_t off = size_t(doc_of(h)) * size_t(p.w0_bstride) + size_t(m) * size_t(p.f);
 #pragma unroll 1
-    for (int c = c_begin; c < c_begin + kGroupCols; c += 32) {
+    for (int c = 0; c < kBN; c += 32) {
       uint32_t v[32];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -719,25 +719,26 @@ struct NormWalkSched : PairDefaults {
     }
   }
 
-  // Publish, exchange within the group, normalise (see above).
+  // Publish, exchange within the group, normalise (see above); run by the
+  // epilogue group that owns accumulator h, on all 256 columns of its rows.
   __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& st) const {
     const int h = seg_acc(s);
     const int i = seg_chunk(s);
     const int k = rnd * p.nupd + i;  // boundaries this (accumulator, group) passed before
     const int m = row0_of(h) + row;
     const int n0 = fb * kBN;
-    const int c_begin = st.group * kGroupCols, c_end = c_begin + kGroupCols;
     const int prow = rank * kBM + row;  // this row within the 256-row block
     const float* pbase =
         p.part + ((size_t(h) * p.G + g) * 2 + (k & 1)) * size_t(p.nparts) * (2 * kBM) + prow;
-    // 1. this part's sum of squares of S_{i+1}
-    float a = 0.f;
+    // 1. the two parts' sums of squares of S_{i+1} (columns 0-127, 128-255)
+    float ss[2] = {0.f, 0.f};
 #pragma unroll 1
-    for (int c = c_begin; c < c_end; c += 32) {
+    for (int c = 0; c < kBN; c += 32) {
       uint32_t v[32];
       tmem_ld_32cols(trow + uint32_t(c), v);
       tmem_wait_ld();
       pin_regs(v);
+      float a = c < kPartCols ? ss[0] : ss[1];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         if (n0 + c + j < p.f) {
@@ -745,11 +746,14 @@ struct NormWalkSched : PairDefaults {
           a = fmaf(x, x, a);
         }
       }
+      if (c < kPartCols) ss[0] = a; else ss[1] = a;
     }
-    __stcg(const_cast<float*>(pbase) + size_t(2 * fb + st.group) * (2 * kBM), a);
+    float* pw = const_cast<float*>(pbase) + size_t(2 * fb) * (2 * kBM);
+    __stcg(pw, ss[0]);
+    __stcg(pw + 2 * kBM, ss[1]);
     // 2. every CTA of the group has published
-    epilogue_all_bar();
-    if (st.group == 0 && row == 0) {
+    epilogue_group_bar(st.group);
+    if (row == 0) {
       unsigned int* ctr = p.arrive + h * p.G + g;
       __threadfence();
       atomicAdd(ctr, 1u);
@@ -766,7 +770,7 @@ struct NormWalkSched : PairDefaults {
         }
       }
     }
-    epilogue_all_bar();
+    epilogue_group_bar(st.group);
     // 3. W_{i+1} = S_{i+1} / ||row||: into TMEM, out as snapshot or state_out
     const float scale = row_scale_of(sum_partials_batched(pbase, 2 * kBM, p.nparts));
     const bool last = (i + 1) == p.nupd;
@@ -776,7 +780,7 @@ struct NormWalkSched : PairDefaults {
                     : nullptr;
     const int slot = doc_of(h) * p.n + i + 1;
 #pragma unroll 1
-    for (int c = c_begin; c < c_end; c += 64) {
+    for (int c = 0; c < kBN; c += 64) {
       uint8_t* buf = write_snap ? st.acquire() : nullptr;
 #pragma unroll 1
       for (int hc = 0; hc < 2; ++hc) {

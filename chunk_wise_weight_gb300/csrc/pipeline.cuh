@@ -145,6 +145,11 @@ struct SchedDefaults {
   //   void bind_sync(volatile int* abort_flag, unsigned int* status)
   // for epilogues that wait on other CTAs.
   static constexpr bool kBindsSync = false;
+  // With kAccTeams (CTA-pair pipeline, two epilogue groups) epilogue group g
+  // alone drains, preloads and releases accumulator g, all of its columns:
+  // the two accumulators' epilogues then run side by side instead of in
+  // turn on the same warps.
+  static constexpr bool kAccTeams = false;
 };
 
 template <class S>

@@ -104,7 +104,8 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(&sync->acc_full[h], 1);
-      mbar_init(&sync->acc_empty[h], 2 * kEpilogueThreads * S::kEpilogueGroups);
+      mbar_init(&sync->acc_empty[h],
+                2 * kEpilogueThreads * (S::kAccTeams ? 1 : S::kEpilogueGroups));
     }
     mbar_init(&sync->drain, 1);
     sync->abort_flag = 0;
@@ -251,7 +252,7 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
       const int nseg = sched.num_segments();
       if constexpr (S::kPreload) {
         for (int h = 0; h < sched.unit_accs(); ++h) {
-          if (!preloaded[h]) {
+          if (!preloaded[h] && (!S::kAccTeams || h == group)) {
             if constexpr (S::kStagedPreload) {
               sched.preload(h, row, tlane + uint32_t(h * kBN), stager);
             } else {
@@ -266,9 +267,13 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
       }
       for (int s = 0; s < nseg; ++s) {
         const int h = sched.seg_acc(s);
+        if constexpr (S::kAccTeams) {
+          static_assert(S::kEpilogueGroups == 2, "one epilogue group per accumulator");
+          if (h != group) continue;  // the other group's accumulator
+        }
         bool got = __all_sync(0xffffffffu, mbar_wait(&sync->acc_full[h], acc_use[h] & 1u,
                                                      abort_flag));
-        if constexpr (S::kBindsSync) {
+        if constexpr (S::kBindsSync && !S::kAccTeams) {
           // One vote over both groups: such an epilogue meets the other
           // group at CTA-wide barriers, so the groups unwind together.
           static_assert(S::kEpilogueGroups == 2, "CTA-wide vote over two groups");
