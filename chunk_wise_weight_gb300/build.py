@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libittt.so")
 
 SOURCES = ["ittt_api.cu", "k_gateup.cu", "k_target.cu", "k_update.cu", "k_apply.cu",
-           "k_dual.cu", "ittt_noalloc.cu"]
+           "k_dual.cu", "k_fp32_inputs.cu", "ittt_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

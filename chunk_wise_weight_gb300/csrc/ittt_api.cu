@@ -306,6 +306,8 @@ ittt_status check_sizes(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chun
 struct Layout {
   size_t z = 0, vhat = 0, xc = 0, snap = 0, scores = 0, w0b = 0, table = 0, state = 0,
          partial = 0, walk_part = 0, walk_arrive = 0, total = 0;
+  // fp32 inputs: the bf16 split operands of the gate/up and target GEMMs
+  size_t h3 = 0, wg3 = 0, wu3 = 0, wt3 = 0;
 };
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -317,6 +319,7 @@ struct Plan {
   bool fused = false, dual = false, packed = false, l2norm = false;
   bool update_only = false;  // fold every chunk into state_out, no apply
   bool reuse = false;        // Z and eta*Vhat come in through z_buf / vhat_buf
+  bool fp32_in = false;      // H, X0, W_gate, W_up, W_target are fp32 (hi/lo split)
   int64_t ndocs = 0;   // documents: B, or the packed count
   int64_t nslots = 0;  // snapshot slots = chunks over all documents
   int64_t n = 0;       // chunks per sequence (regular)
@@ -345,7 +348,7 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
     return fail(ITTT_ERR_INVALID_ARG, "pad_mode %d", int(o.pad_mode));
   if (o.flags & ~int32_t(ITTT_FLAG_FUSED_CONV | ITTT_FLAG_DUAL | ITTT_FLAG_L2_NORM |
                           ITTT_FLAG_SINGLE_CTA | ITTT_FLAG_UPDATE_ONLY | ITTT_FLAG_REUSE_ZV |
-                          ITTT_FLAG_PRIMAL))
+                          ITTT_FLAG_PRIMAL | ITTT_FLAG_FP32_INPUTS))
     return fail(ITTT_ERR_INVALID_ARG, "unknown flags 0x%x", unsigned(o.flags));
   if ((o.flags & ITTT_FLAG_DUAL) && (o.flags & ITTT_FLAG_PRIMAL))
     return fail(ITTT_ERR_INVALID_ARG, "ITTT_FLAG_DUAL and ITTT_FLAG_PRIMAL exclude each other");
@@ -359,6 +362,10 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   P->dual = (o.flags & ITTT_FLAG_DUAL) != 0;
   P->packed = o.cu_seqlens != nullptr;
   P->l2norm = (o.flags & ITTT_FLAG_L2_NORM) != 0;
+  P->fp32_in = (o.flags & ITTT_FLAG_FP32_INPUTS) != 0;
+  if (P->fp32_in && P->fused)
+    return fail(ITTT_ERR_UNSUPPORTED,
+                "fp32 inputs run with the split convolution (no ITTT_FLAG_FUSED_CONV)");
   // Form choice by measured cost: the dual form for short sequences, where
   // the walk's per-chunk d x f snapshots cost more than the dual form's
   // T^2 terms.  The two forms' FLOPs are equal at T = 2 d f / (d + f); the
@@ -512,7 +519,13 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   };
   if (o.z_buf == nullptr) L.z = take(size_t(P->M) * f * 2);
   if (o.vhat_buf == nullptr) L.vhat = take(size_t(P->M) * d * 2);
-  if (!P->fused && !P->reuse) L.xc = take(size_t(P->M) * d * 2);
+  if (!P->fused && !P->reuse) L.xc = take(size_t(P->M) * d * 2 * (P->fp32_in ? 3 : 1));
+  if (P->fp32_in && !P->reuse) {
+    L.h3 = take(size_t(P->M) * 3 * d * 2);
+    L.wg3 = take(size_t(f) * 3 * d * 2);
+    L.wu3 = take(size_t(f) * 3 * d * 2);
+    L.wt3 = take(size_t(d) * 3 * d * 2);
+  }
   if (!P->dual && !P->update_only && o.snap_buf == nullptr)
     L.snap = take(size_t(P->nslots) * d * f * 2);
   if (P->dual) {
@@ -593,6 +606,11 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     return fail(ITTT_ERR_INVALID_ARG, "W_gate: expected a [f,d] descriptor");
   const int64_t f = W_gate->shape[0];
   if (!std::isfinite(eta)) return fail(ITTT_ERR_INVALID_ARG, "eta is not finite");
+  // fp32 inputs follow from H's dtype; the flag alone (bf16 H) is an error.
+  const bool fp32_in = H->dtype == ITTT_FP32;
+  if ((o.flags & ITTT_FLAG_FP32_INPUTS) && !fp32_in)
+    return fail(ITTT_ERR_INVALID_ARG, "ITTT_FLAG_FP32_INPUTS is set but H is not fp32");
+  if (fp32_in) o.flags |= ITTT_FLAG_FP32_INPUTS;
   const bool w0_bf16 = W_down0 != nullptr && W_down0->dtype == ITTT_BF16;
   Plan P;
   ittt_status s = make_plan(B, T, d, f, chunk, o, w0_bf16, &P);
@@ -605,10 +623,10 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   const int64_t sh_btd[3] = {B, T, d}, sh_fd[2] = {f, d}, sh_df[2] = {d, f}, sh_dd[2] = {d, d},
                 sh_d3[2] = {d, 3}, sh_sdf[3] = {S, d, f}, sh_btf[3] = {B, T, f},
                 sh_snap[4] = {B, P.nslots / B, d, f};
-  if ((s = check_tensor(H, "H", 3, sh_btd, true, false))) return s;
-  if ((s = check_tensor(X0, "X0", 3, sh_btd, true, false))) return s;
-  if ((s = check_tensor(W_gate, "W_gate", 2, sh_fd, true, false))) return s;
-  if ((s = check_tensor(W_up, "W_up", 2, sh_fd, true, false))) return s;
+  if ((s = check_tensor(H, "H", 3, sh_btd, !fp32_in, fp32_in))) return s;
+  if ((s = check_tensor(X0, "X0", 3, sh_btd, !fp32_in, fp32_in))) return s;
+  if ((s = check_tensor(W_gate, "W_gate", 2, sh_fd, !fp32_in, fp32_in))) return s;
+  if ((s = check_tensor(W_up, "W_up", 2, sh_fd, !fp32_in, fp32_in))) return s;
   // Folding chunks only, with neither state_in nor W_down0, starts from zero.
   const bool zero_start = update_only && o.state_in == nullptr && W_down0 == nullptr;
   if (o.state_in) {
@@ -616,7 +634,7 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   } else if (!zero_start && (s = check_tensor(W_down0, "W_down0", 2, sh_df, true, true))) {
     return s;
   }
-  if ((s = check_tensor(W_target, "W_target", 2, sh_dd, true, false))) return s;
+  if ((s = check_tensor(W_target, "W_target", 2, sh_dd, !fp32_in, fp32_in))) return s;
   if ((s = check_tensor(conv_w, "conv_w", 2, sh_d3, false, true))) return s;
   // Nothing is applied when folding chunks only: out is ignored.
   if (update_only) out = nullptr;
@@ -720,17 +738,29 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   CUtensorMap tm_vs, tm_ss, tm_os;
   memset(&tm_ss, 0, sizeof(tm_ss));
   memset(&tm_os, 0, sizeof(tm_os));
+  // fp32 inputs: the GEMMs read bf16 hi/lo split copies over K = 3d,
+  // A as [A_hi|A_hi|A_lo] (H; Xc) and B as [B_hi|B_lo|B_hi] (W_gate, W_up;
+  // W_target), so each product is hi*hi + hi*lo + lo*hi.
+  const int64_t k_gu = fp32_in ? 3 * d : d, k_t = fp32_in ? 3 * d : d;
+  auto* h3 = reinterpret_cast<__nv_bfloat16*>(ws + L.h3);
+  auto* wg3 = reinterpret_cast<__nv_bfloat16*>(ws + L.wg3);
+  auto* wu3 = reinterpret_cast<__nv_bfloat16*>(ws + L.wu3);
+  auto* wt3 = reinterpret_cast<__nv_bfloat16*>(ws + L.wt3);
   if (!reuse) {  // the producers of Z and eta*Vhat
-    if ((s = make_map(&tm_h, H->data, d, M, 64, 128, "H"))) return s;
-    if ((s = make_map(&tm_wg, W_gate->data, d, f, 64, 128, "W_gate"))) return s;
-    if ((s = make_map(&tm_wu, W_up->data, d, f, 64, 128, "W_up"))) return s;
+    const void* a_h = fp32_in ? static_cast<const void*>(h3) : H->data;
+    const void* a_wg = fp32_in ? static_cast<const void*>(wg3) : W_gate->data;
+    const void* a_wu = fp32_in ? static_cast<const void*>(wu3) : W_up->data;
+    const void* a_wt = fp32_in ? static_cast<const void*>(wt3) : W_target->data;
+    if ((s = make_map(&tm_h, a_h, k_gu, M, 64, 128, "H"))) return s;
+    if ((s = make_map(&tm_wg, a_wg, k_gu, f, 64, 128, "W_gate"))) return s;
+    if ((s = make_map(&tm_wu, a_wu, k_gu, f, 64, 128, "W_up"))) return s;
     if (fused) {
       if ((s = make_map(&tm_a, X0->data, d, M, 64, 130, "X0"))) return s;
-    } else if ((s = make_map(&tm_a, xc, d, M, 64, 128, "Xc"))) {
+    } else if ((s = make_map(&tm_a, xc, k_t, M, 64, 128, "Xc"))) {
       return s;
     }
-    if ((s = make_map(&tm_wt, W_target->data, d, d, 64, 256, "W_target"))) return s;
-    if ((s = make_map(&tm_wt128, W_target->data, d, d, 64, 128, "W_target (pair)"))) return s;
+    if ((s = make_map(&tm_wt, a_wt, k_t, d, 64, 256, "W_target"))) return s;
+    if ((s = make_map(&tm_wt128, a_wt, k_t, d, 64, 128, "W_target (pair)"))) return s;
     if ((s = make_map(&tm_vs, vhat, d, M, 64, 128, "Vhat (store)"))) return s;
   }
   if (out && out->dtype == ITTT_BF16 &&
@@ -795,7 +825,25 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   if (what == nullptr && P.packed &&
       (s = stage_table(ds, tab, P.table.data(), P.table.size(), stream)) != ITTT_OK)
     return s;
-  if (!fused && !reuse) {
+  if (!fused && !reuse && fp32_in) {
+    // hi/lo split copies of the fp32 operands, then the fp32 convolution,
+    // split the same way into [Xc_hi | Xc_hi | Xc_lo].
+    ITTT_STEP(ittt::launch_split_bf16(env, static_cast<const float*>(H->data), int64_t(M), int(d),
+                                      h3, 3, 4u),
+              "split launch (H)");
+    ITTT_STEP(ittt::launch_split_bf16(env, static_cast<const float*>(W_gate->data), f, int(d),
+                                      wg3, 3, 2u),
+              "split launch (W_gate)");
+    ITTT_STEP(ittt::launch_split_bf16(env, static_cast<const float*>(W_up->data), f, int(d), wu3,
+                                      3, 2u),
+              "split launch (W_up)");
+    ITTT_STEP(ittt::launch_split_bf16(env, static_cast<const float*>(W_target->data), d, int(d),
+                                      wt3, 3, 2u),
+              "split launch (W_target)");
+    ITTT_STEP(ittt::launch_conv_fp32(env, static_cast<const float*>(X0->data), cw, xc, int64_t(M),
+                                     docs, int(d), int(o.pad_mode)),
+              "conv launch (fp32)");
+  } else if (!fused && !reuse) {
     CUtensorMap tm_x0;
     if (what == nullptr &&
         (s = make_map(&tm_x0, X0->data, d, M, ittt::kConvMapBoxCols, ittt::kConvMapBoxRows,
@@ -811,11 +859,11 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
     // CTA pairs where two can be resident (split convolution), else one CTA.
     e = fused || single ? cudaErrorNotSupported
                         : ittt::launch_target_pair(env, tm_a, tm_wt128, tm_vs, et, vhat, eta,
-                                                   int(M), int(d));
+                                                   int(M), int(d), int(k_t));
     if (e == cudaErrorNotSupported) {
       cudaGetLastError();
       e = ittt::launch_target(env, tm_a, tm_wt, tm_vs, cw, et, vhat, eta, int(M), int(T), int(d),
-                              int(chunk), int(o.pad_mode), fused);
+                              int(chunk), int(o.pad_mode), fused, int(k_t));
     }
     if (e != cudaSuccess) what = "target launch";
   }
@@ -823,10 +871,11 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   ITTT_STEP(rec(2 * ITTT_PHASE_GATEUP, stream), "event record");
   if (what == nullptr && !reuse) {
     e = single ? cudaErrorNotSupported
-               : ittt::launch_gateup_pair(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d));
+               : ittt::launch_gateup_pair(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f),
+                                          int(k_gu));
     if (e == cudaErrorNotSupported) {
       cudaGetLastError();
-      e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(d));
+      e = ittt::launch_gateup(env, tm_h, tm_wg, tm_wu, tm_zk, int(M), int(f), int(k_gu));
     }
     if (e != cudaSuccess) what = "gate/up launch";
   }

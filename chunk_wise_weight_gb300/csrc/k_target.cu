@@ -547,7 +547,8 @@ cudaError_t launch_conv(const LaunchEnv& env, const CUtensorMap& tm_x0, const fl
 cudaError_t launch_target_pair(const LaunchEnv& env, const CUtensorMap& tm_xc,
                                const CUtensorMap& tm_wt, const CUtensorMap& tm_vs,
                                const float* eta_tok, __nv_bfloat16* vhat, float eta, int M,
-                               int d) {
+                               int d, int K) {
+  if (K <= 0) K = d;
   TargetParams p;
   memset(&p, 0, sizeof(p));
   p.eta_tok = eta_tok;
@@ -560,7 +561,7 @@ cudaError_t launch_target_pair(const LaunchEnv& env, const CUtensorMap& tm_xc,
   p.d = d;
   p.m_tiles = (M + 2 * kBM - 1) / (2 * kBM);
   p.n_tiles = (d + kBN - 1) / kBN;
-  p.kblocks = (d + kBK - 1) / kBK;
+  p.kblocks = (K + kBK - 1) / kBK;
   p.raster = p.n_tiles < 16 ? p.n_tiles : 16;
   const int units = p.m_tiles * p.n_tiles;
   if (units == 0) return cudaSuccess;
@@ -581,7 +582,8 @@ cudaError_t launch_target_pair(const LaunchEnv& env, const CUtensorMap& tm_xc,
 cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a, const CUtensorMap& tm_wt,
                           const CUtensorMap& tm_vs, const float* conv_w, const float* eta_tok,
                           __nv_bfloat16* vhat, float eta, int M, int T, int d, int C, int pad_mode,
-                          bool fused) {
+                          bool fused, int K) {
+  if (K <= 0 || fused) K = d;
   TargetParams p;
   p.eta_tok = eta_tok;
   p.tm_a = tm_a;
@@ -597,7 +599,7 @@ cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a, const C
   p.pad_mode = pad_mode;
   p.m_tiles = (M + kBM - 1) / kBM;
   p.n_tiles = (d + kBN - 1) / kBN;
-  p.kblocks = (d + kBK - 1) / kBK;
+  p.kblocks = (K + kBK - 1) / kBK;
   p.raster = p.n_tiles < 16 ? p.n_tiles : 16;
   const int units = p.m_tiles * p.n_tiles;
   if (units == 0) return cudaSuccess;

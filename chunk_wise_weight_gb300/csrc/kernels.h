@@ -142,6 +142,18 @@ cudaError_t launch_gateup_pair(const LaunchEnv& env, const CUtensorMap& tm_h,
 cudaError_t launch_conv(const LaunchEnv& env, const CUtensorMap& tm_x0, const float* conv_w,
                         __nv_bfloat16* xc, int64_t rows, const DocMap& docs, int d,
                         int pad_mode);
+// fp32 inputs (k_fp32_inputs.cu): dst[r, k*cols + c] = part k of src[r, c]
+// for k < nseg, the bf16 rounding hi = bf16(x) or, where bit k of lo_mask is
+// set, the remainder lo = bf16(x - hi).  src [rows, cols] fp32, cols a
+// multiple of 8; dst [rows, nseg*cols] bf16.
+cudaError_t launch_split_bf16(const LaunchEnv& env, const float* src, int64_t rows, int cols,
+                              __nv_bfloat16* dst, int nseg, unsigned lo_mask);
+// The convolution of an fp32 X0 [rows, d] (as launch_conv, in fp32), split
+// into xc3 [rows, 3d] bf16 as [Xc_hi | Xc_hi | Xc_lo].
+cudaError_t launch_conv_fp32(const LaunchEnv& env, const float* x0, const float* conv_w,
+                             __nv_bfloat16* xc3, int64_t rows, const DocMap& docs, int d,
+                             int pad_mode);
+
 // The box launch_conv's X0 map must have: {channels, rows}.
 constexpr uint32_t kConvMapBoxCols = 256, kConvMapBoxRows = 66;
 
@@ -151,10 +163,13 @@ constexpr uint32_t kConvMapBoxCols = 256, kConvMapBoxRows = 66;
 // output goes out through tm_vs (vhat [M, d], box {64,128}).
 // Fused: tm_a maps X0 [M, d] with box {64,130}, the kernel computes the conv
 // itself and stores vhat directly.  tm_wt: W_target [d, d] box {64,256}.
+// K: the split variant's contraction length (0: d; 2d for fp32 inputs, whose
+// A operand is [Xc | Xc] and B [W_target hi | lo]); the fused variant has K = d.
 cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a,
                           const CUtensorMap& tm_wt, const CUtensorMap& tm_vs,
                           const float* conv_w, const float* eta_tok, __nv_bfloat16* vhat,
-                          float eta, int M, int T, int d, int C, int pad_mode, bool fused);
+                          float eta, int M, int T, int d, int C, int pad_mode, bool fused,
+                          int K = 0);
 
 // The split variant on CTA pairs (256-row tiles): tm_xc maps Xc [M, d] box
 // {64,128}, tm_wt maps W_target [d, d] box {64,128}, tm_vs as above.
@@ -162,7 +177,7 @@ cudaError_t launch_target(const LaunchEnv& env, const CUtensorMap& tm_a,
 cudaError_t launch_target_pair(const LaunchEnv& env, const CUtensorMap& tm_xc,
                                const CUtensorMap& tm_wt, const CUtensorMap& tm_vs,
                                const float* eta_tok, __nv_bfloat16* vhat, float eta, int M,
-                               int d);
+                               int d, int K = 0);
 
 // Slot docs.first_chunk(k) of snap = bf16(W_0 of document k) for every k.
 // w0 is bf16 or fp32, [d, f] shared (w0_bstride = 0) or one per document.

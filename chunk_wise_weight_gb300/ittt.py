@@ -29,6 +29,7 @@ FLAG_SINGLE_CTA = 8
 FLAG_UPDATE_ONLY = 16
 FLAG_REUSE_ZV = 32
 FLAG_PRIMAL = 64
+FLAG_FP32_INPUTS = 128
 FORM_PRIMAL, FORM_DUAL = 0, 1
 
 _DTYPES = {torch.bfloat16: BF16, torch.float32: FP32}
@@ -158,13 +159,14 @@ def _seqlens(cu_seqlens):
 
 def _opts(pad_mode, fused_conv, dual, cu_seqlens, keep: dict, l2norm=False,
           single_cta=False, update_only=False, reuse_zv=False, primal=False,
-          **tensors) -> Opts:
+          fp32_inputs=False, **tensors) -> Opts:
     opts = Opts()
     opts.pad_mode = int(pad_mode)
     opts.flags = ((FLAG_FUSED_CONV if fused_conv else 0) | (FLAG_DUAL if dual else 0)
                   | (FLAG_L2_NORM if l2norm else 0) | (FLAG_SINGLE_CTA if single_cta else 0)
                   | (FLAG_UPDATE_ONLY if update_only else 0)
-                  | (FLAG_REUSE_ZV if reuse_zv else 0) | (FLAG_PRIMAL if primal else 0))
+                  | (FLAG_REUSE_ZV if reuse_zv else 0) | (FLAG_PRIMAL if primal else 0)
+                  | (FLAG_FP32_INPUTS if fp32_inputs else 0))
     for name, t in tensors.items():
         if t is not None:
             keep[name] = describe(t)
@@ -193,7 +195,9 @@ def forward(H, X0, W_gate, W_up, W_down0, W_target, conv_w, eta: float, chunk: i
     (returns None; W_down0 None starts from zero); `reuse_zv` takes Z and
     eta * Vhat from `z_buf` / `vhat_buf` instead of computing them.  The
     library picks the primal or dual form by measured cost (plan_form);
-    `dual` / `primal` force one."""
+    `dual` / `primal` force one.  fp32 H, X0, W_gate, W_up and W_target
+    (all five) select the fp32-input mode: the library splits each into
+    bf16 hi/lo parts instead of rounding it."""
     lib = load()
     if update_only:
         out = None
@@ -280,26 +284,28 @@ def workspace_bytes(B: int, T: int, d: int, f: int, chunk: int) -> int:
 def workspace_bytes_ex(B: int, T: int, d: int, f: int, chunk: int, *, pad_mode: int = PAD_CHUNK,
                        fused_conv: bool = False, dual: bool = False, cu_seqlens=None,
                        l2norm: bool = False, update_only: bool = False, reuse_zv: bool = False,
-                       primal: bool = False, **buffers) -> int:
+                       primal: bool = False, fp32_inputs: bool = False, **buffers) -> int:
     """ittt_workspace_bytes_ex: scratch for a forward call with these
     options; `buffers` name the ittt_opts tensors the call passes (state_in,
     state_out, z_buf, vhat_buf, snap_buf, eta_tok) -- only whether each is
-    given matters."""
+    given matters; `fp32_inputs` sizes the hi/lo split copies."""
     keep = {}
     opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, keep, l2norm=l2norm,
-                 update_only=update_only, reuse_zv=reuse_zv, primal=primal, **buffers)
+                 update_only=update_only, reuse_zv=reuse_zv, primal=primal,
+                 fp32_inputs=fp32_inputs, **buffers)
     return int(load().ittt_workspace_bytes_ex(B, T, d, f, chunk, ctypes.byref(opts)))
 
 
 def plan_form(B: int, T: int, d: int, f: int, chunk: int, *, pad_mode: int = PAD_CHUNK,
               fused_conv: bool = False, dual: bool = False, cu_seqlens=None,
               l2norm: bool = False, update_only: bool = False, reuse_zv: bool = False,
-              primal: bool = False, **buffers) -> int:
+              primal: bool = False, fp32_inputs: bool = False, **buffers) -> int:
     """ittt_plan_form: FORM_PRIMAL or FORM_DUAL for a call with these sizes
     and options (-1 if it would be rejected)."""
     keep = {}
     opts = _opts(pad_mode, fused_conv, dual, cu_seqlens, keep, l2norm=l2norm,
-                 update_only=update_only, reuse_zv=reuse_zv, primal=primal, **buffers)
+                 update_only=update_only, reuse_zv=reuse_zv, primal=primal,
+                 fp32_inputs=fp32_inputs, **buffers)
     return int(load().ittt_plan_form(B, T, d, f, chunk, ctypes.byref(opts)))
 
 

@@ -27,6 +27,8 @@
  *   - Shapes: H, X0 [B,T,d] bf16; W_gate, W_up [f,d] bf16; W_down0 [d,f]
  *     bf16 or fp32; W_target [d,d] bf16; conv_w [d,3] fp32; out [B,T,d]
  *     bf16 or fp32.  Weights use the [out_features, in_features] layout.
+ *     H, X0, W_gate, W_up and W_target may instead all be fp32
+ *     (ITTT_FLAG_FP32_INPUTS).
  *   - Supported sizes: d and f multiples of 8 (16-byte rows), any chunk
  *     >= 1, any T >= 1, B*T < 2^31.  When chunk does not divide T the last
  *     chunk is the shorter remainder (a stream that ends mid-chunk).  Chunks
@@ -219,6 +221,23 @@ typedef struct {
 #define ITTT_FLAG_REUSE_ZV 32
 /* Never use the dual form (see "Form choice" below). */
 #define ITTT_FLAG_PRIMAL 64
+/* fp32 inputs.  A call whose H is fp32 takes H, X0, W_gate, W_up and
+ * W_target as fp32 (all five; W_down0, state_in and conv_w as usual).  The
+ * inputs are not rounded to bf16: each fp32 value x is split into two bf16
+ * parts, hi = bf16(x) and lo = bf16(x - hi), and the gate/up and target
+ * products are formed as hi*hi + hi*lo + lo*hi on the same tensor-core
+ * kernels by contracting over a concatenated K of 3 d; the dropped lo*lo
+ * term is below 2^-16 relative.  The convolution Xc of X0 is computed in
+ * fp32 and split the same way.  Z and eta*Vhat are then the fp32 products
+ * rounded once to bf16; the fast-weight walk and the apply are as for bf16
+ * inputs.  The gate/up and target phases cost 3x the FLOPs of bf16 inputs;
+ * the scratch gains the split copies (H and Xc M x 3d, W_gate and W_up
+ * f x 3d, W_target d x 3d, all bf16) in place of the bf16 Xc.  Not with
+ * ITTT_FLAG_FUSED_CONV.  ittt_forward / ittt_forward_ex infer the mode from
+ * H's dtype (setting this flag with bf16 H is an error);
+ * ittt_workspace_bytes_ex and ittt_plan_form size and plan for it when the
+ * flag is set. */
+#define ITTT_FLAG_FP32_INPUTS 128
 
 /*
  * Form choice.  Without ITTT_FLAG_DUAL or ITTT_FLAG_PRIMAL a call uses the
@@ -295,7 +314,9 @@ ITTT_API ittt_status ittt_forward_ex(const ittt_tensor* H, const ittt_tensor* X0
  * race: serialise them on one stream.  The first call on a device does a
  * one-time set-up (it looks up the array's device address); make that first
  * call before any stream capture.  Pad mode is ITTT_PAD_CHUNK; sizes as for
- * ittt_forward.  Device-side failures are reported by ittt_stream_status().
+ * ittt_forward; inputs bf16 only (an fp32 H, X0, W_gate, W_up or W_target
+ * returns ITTT_ERR_INVALID_ARG).  Device-side failures are reported by
+ * ittt_stream_status().
  */
 #define ITTT_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 ITTT_API ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_tensor* X0,

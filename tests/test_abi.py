@@ -98,6 +98,39 @@ def test_rejects_bad_descriptors(lib, mutate, status, msg):
     assert msg in ittt.last_error()
 
 
+def _fp32_args(**kw):
+    a = _args(**kw)
+    for k in ("H", "X0", "Wg", "Wu", "Wt"):
+        a[k].dtype = ittt.FP32
+    # fp32 tensors are twice as large: spread the fake addresses apart again
+    for j, k in enumerate(("H", "X0", "Wg", "Wu", "W0", "Wt", "cw", "out")):
+        a[k].data = FAKE * (j + 1) * 4096
+    return a
+
+
+def test_fp32_inputs_validation(lib):
+    """fp32 inputs: H's dtype selects the mode, and then all five of H, X0,
+    W_gate, W_up and W_target must be fp32; the flag with a bf16 H and the
+    fused convolution are refused before any work."""
+    for k, name in (("X0", "X0"), ("Wg", "W_gate"), ("Wu", "W_up"), ("Wt", "W_target")):
+        a = _fp32_args()
+        a[k].dtype = ittt.BF16
+        assert _call(lib, a) == ittt.ERR_INVALID_ARG, k
+        assert name in ittt.last_error()
+    a = _args()
+    a["H"].dtype = ittt.FP32                  # H alone fp32: X0 is the first mismatch
+    assert _call(lib, a) == ittt.ERR_INVALID_ARG and "X0" in ittt.last_error()
+    o = ittt.Opts()
+    o.flags = ittt.FLAG_FP32_INPUTS            # flag set, H bf16
+    assert _call(lib, _args(), opts=o) == ittt.ERR_INVALID_ARG
+    assert "FP32_INPUTS" in ittt.last_error()
+    o = ittt.Opts()
+    o.flags = ittt.FLAG_FUSED_CONV
+    assert _call(lib, _fp32_args(), opts=o) == ittt.ERR_UNSUPPORTED
+    assert "split convolution" in ittt.last_error()
+    assert ittt.workspace_bytes_ex(1, 256, 64, 256, 64, fused_conv=True, fp32_inputs=True) == 0
+
+
 def test_rejects_bad_sizes(lib):
     assert _call(lib, _args(), chunk=0) == ittt.ERR_INVALID_ARG
     assert "positive" in ittt.last_error()
@@ -131,7 +164,7 @@ def test_rejects_bad_options(lib):
     o.pad_mode = 7
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     o = ittt.Opts()
-    o.flags = 128
+    o.flags = 256
     assert _call(lib, a, opts=o) == ittt.ERR_INVALID_ARG
     assert "flags" in ittt.last_error()
     o = ittt.Opts()
@@ -205,6 +238,17 @@ def test_workspace_bytes_and_launch_count(lib):
     assert (ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True)
             == want + r(B * tiles * 128 * 32 * 4) + r(2 * B * 2 * nblk * d * 4) + walk)
     assert ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True, dual=True) == 0
+    # fp32 inputs: the split copies [A_hi | A_hi | A_lo] of Xc and H
+    # (M x 3d each, Xc's in place of the bf16 Xc), [W_hi | W_lo | W_hi] of
+    # W_gate and W_up (f x 3d each) and of W_target (d x 3d)
+    M = B * T
+    want_fp32 = (want - r(M * d * 2) + 2 * r(M * 3 * d * 2)
+                 + 2 * r(f * 3 * d * 2) + r(d * 3 * d * 2))
+    assert ittt.workspace_bytes_ex(B, T, d, f, C, fp32_inputs=True, primal=True) == want_fp32
+    assert (ittt.workspace_bytes_ex(B, T, d, f, C, fp32_inputs=True, reuse_zv=True,
+                                    z_buf=fake_z, vhat_buf=fake_z)
+            == ittt.workspace_bytes_ex(B, T, d, f, C, reuse_zv=True, z_buf=fake_z,
+                                       vhat_buf=fake_z))
     assert ittt.launch_count(B, T, d, f, C) == 5
     assert ittt.launch_count(B, T, d, f, T) == 4
     assert ittt.launch_count(B, 1000, d, f, 512) == 5   # two chunks, the last partial
