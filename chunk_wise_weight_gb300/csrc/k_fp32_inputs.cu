@@ -24,115 +24,151 @@ __device__ __forceinline__ void split_hi_lo(float x, __nv_bfloat16& hi, __nv_bfl
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return uint32_t(__bfloat16_as_ushort(a)) | (uint32_t(__bfloat16_as_ushort(b)) << 16);
+}
+
+// Eight fp32 values -> their bf16 hi and lo parts, 16 bytes each.
+__device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
+  __nv_bfloat16 h[8], l[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) split_hi_lo(x[j], h[j], l[j]);
+  hi = make_uint4(pack2(h[0], h[1]), pack2(h[2], h[3]), pack2(h[4], h[5]), pack2(h[6], h[7]));
+  lo = make_uint4(pack2(l[0], l[1]), pack2(l[2], l[3]), pack2(l[4], l[5]), pack2(l[6], l[7]));
+}
+
+__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(p));  // read once: streaming
+  const float4 b = __ldcs(reinterpret_cast<const float4*>(p + 4));
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
 // dst[r, k*cols + c] = part k of src[r, c] for k < nseg: the lo part when
-// bit k of lo_mask is set, else the hi part.  Four columns per thread step
-// (cols is a multiple of 8).
+// bit k of lo_mask is set, else the hi part.  One thread per eight columns
+// of a row (cols is a multiple of 8): 16-byte loads and stores, one item per
+// thread on a grid as large as the work (the block scheduler then balances
+// the SMs; a single wave of grid-stride blocks measured 10-15% slower).
 __global__ void __launch_bounds__(256)
     split_bf16_kernel(const float* __restrict__ src, int64_t rows, int cols,
                       __nv_bfloat16* __restrict__ dst, int nseg, unsigned lo_mask) {
   griddep_wait();  // programmatic launch: the previous grid is done
   griddep_launch_dependents();
-  const int q4 = cols >> 2;
-  const int64_t total = rows * q4;
-  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = idx / q4;
-    const int c = int(idx - r * q4) * 4;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(src + r * cols + c));
-    const float x[4] = {v.x, v.y, v.z, v.w};
-    __nv_bfloat16 h[4], l[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) split_hi_lo(x[j], h[j], l[j]);
-    uint2 hi, lo;
-    hi.x = uint32_t(__bfloat16_as_ushort(h[0])) | (uint32_t(__bfloat16_as_ushort(h[1])) << 16);
-    hi.y = uint32_t(__bfloat16_as_ushort(h[2])) | (uint32_t(__bfloat16_as_ushort(h[3])) << 16);
-    lo.x = uint32_t(__bfloat16_as_ushort(l[0])) | (uint32_t(__bfloat16_as_ushort(l[1])) << 16);
-    lo.y = uint32_t(__bfloat16_as_ushort(l[2])) | (uint32_t(__bfloat16_as_ushort(l[3])) << 16);
+  const int q8 = cols >> 3;
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx < rows * q8) {
+    const int64_t r = idx / q8;
+    const int c = int(idx - r * q8) * 8;
+    float x[8];
+    load8(src + r * cols + c, x);
+    uint4 hi, lo;
+    split8(x, hi, lo);
+    __nv_bfloat16* row = dst + r * int64_t(nseg) * cols + c;
     for (int k = 0; k < nseg; ++k)
-      *reinterpret_cast<uint2*>(dst + r * int64_t(nseg) * cols + int64_t(k) * cols + c) =
-          (lo_mask >> k) & 1u ? lo : hi;
+      *reinterpret_cast<uint4*>(row + int64_t(k) * cols) = (lo_mask >> k) & 1u ? lo : hi;
   }
   fence_proxy_async_global();  // the GEMMs read dst through TMA
+}
+
+constexpr int kConvFp32Rows = 4;  // rows per thread: a 6-row window of loads
+
+struct TapRange {
+  int lo, hi;  // taps read rows in [lo, hi)
+};
+
+// The rows a token's taps may read: its document and, with chunk padding,
+// its chunk (as conv3_kernel).
+__device__ __forceinline__ TapRange tap_range(const DocMap& docs, int t, int pad_mode) {
+  const int k = docs.doc_of_token(t);
+  int lo = docs.start(k);
+  int hi = lo + docs.len(k);
+  if (pad_mode == 0) {
+    lo += ((t - lo) / docs.C) * docs.C;
+    hi = min(lo + docs.C, hi);
+  }
+  return {lo, hi};
 }
 
 // Xc = three-tap depthwise conv of an fp32 X0 (as conv3_kernel: taps at
 // t-1, t, t+1 inside the token's document and, with chunk padding, its
 // chunk; fp32 taps in the same order), written as the split A operand of
 // the target GEMM: row t of xc3 (3 d wide) is [Xc_hi | Xc_hi | Xc_lo].  A
-// thread owns four channels of one row.
+// thread owns eight channels of kConvFp32Rows consecutive rows and loads
+// their window of kConvFp32Rows + 2 rows once (one row per thread, each row
+// read three times, measured 2.3x slower).
 __global__ void __launch_bounds__(256)
     conv3_fp32_kernel(const float* __restrict__ x0, const float* __restrict__ conv_w,
                       __nv_bfloat16* __restrict__ xc3, int rows, DocMap docs, int d,
                       int pad_mode) {
   griddep_wait();
   griddep_launch_dependents();
-  const int q4 = d >> 2;
-  const int64_t total = int64_t(rows) * q4;
-  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += int64_t(gridDim.x) * blockDim.x) {
-    const int t = int(idx / q4);
-    const int c = int(idx - int64_t(t) * q4) * 4;
-    const int k = docs.doc_of_token(t);
-    int t_lo = docs.start(k);
-    int t_hi = t_lo + docs.len(k);
-    if (pad_mode == 0) {
-      t_lo += ((t - t_lo) / docs.C) * docs.C;
-      t_hi = min(t_lo + docs.C, t_hi);
-    }
-    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 xm = t - 1 >= t_lo ? __ldg(reinterpret_cast<const float4*>(x0 + size_t(t - 1) * d + c)) : zero;
-    const float4 x = __ldg(reinterpret_cast<const float4*>(x0 + size_t(t) * d + c));
-    const float4 xp = t + 1 < t_hi ? __ldg(reinterpret_cast<const float4*>(x0 + size_t(t + 1) * d + c)) : zero;
-    const float am[4] = {xm.x, xm.y, xm.z, xm.w};
-    const float a0[4] = {x.x, x.y, x.z, x.w};
-    const float ap[4] = {xp.x, xp.y, xp.z, xp.w};
-    float y[4];
+  const int q8 = d >> 3;
+  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int rb = int(idx / q8);
+  const int c = int(idx - int64_t(rb) * q8) * 8;
+  const int t0 = rb * kConvFp32Rows;
+  if (t0 < rows) {
+    float w0[8], w1[8], w2[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float* w = conv_w + size_t(c + j) * 3;
-      float v = __ldg(w) * am[j];
-      v = fmaf(__ldg(w + 1), a0[j], v);
-      y[j] = fmaf(__ldg(w + 2), ap[j], v);
+    for (int j = 0; j < 8; ++j) {
+      w0[j] = __ldg(conv_w + size_t(c + j) * 3);
+      w1[j] = __ldg(conv_w + size_t(c + j) * 3 + 1);
+      w2[j] = __ldg(conv_w + size_t(c + j) * 3 + 2);
     }
-    __nv_bfloat16 h[4], l[4];
+    float x[kConvFp32Rows + 2][8];  // rows t0-1 .. t0+kConvFp32Rows
 #pragma unroll
-    for (int j = 0; j < 4; ++j) split_hi_lo(y[j], h[j], l[j]);
-    uint2 hi, lo;
-    hi.x = uint32_t(__bfloat16_as_ushort(h[0])) | (uint32_t(__bfloat16_as_ushort(h[1])) << 16);
-    hi.y = uint32_t(__bfloat16_as_ushort(h[2])) | (uint32_t(__bfloat16_as_ushort(h[3])) << 16);
-    lo.x = uint32_t(__bfloat16_as_ushort(l[0])) | (uint32_t(__bfloat16_as_ushort(l[1])) << 16);
-    lo.y = uint32_t(__bfloat16_as_ushort(l[2])) | (uint32_t(__bfloat16_as_ushort(l[3])) << 16);
-    __nv_bfloat16* row = xc3 + size_t(t) * (3 * size_t(d));
-    *reinterpret_cast<uint2*>(row + c) = hi;
-    *reinterpret_cast<uint2*>(row + d + c) = hi;
-    *reinterpret_cast<uint2*>(row + 2 * d + c) = lo;
+    for (int i = 0; i < kConvFp32Rows + 2; ++i) {
+      const int t = t0 - 1 + i;
+      if (t >= 0 && t < rows) {
+        load8(x0 + size_t(t) * d + c, x[i]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[i][j] = 0.f;
+      }
+    }
+    TapRange tr = tap_range(docs, t0, pad_mode);
+#pragma unroll
+    for (int i = 0; i < kConvFp32Rows; ++i) {
+      const int t = t0 + i;
+      if (t < rows) {
+        if (t >= tr.hi) tr = tap_range(docs, t, pad_mode);  // next chunk or document
+        const bool has_m = t - 1 >= tr.lo, has_p = t + 1 < tr.hi;
+        float y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float v = w0[j] * (has_m ? x[i][j] : 0.f);
+          v = fmaf(w1[j], x[i + 1][j], v);
+          y[j] = fmaf(w2[j], has_p ? x[i + 2][j] : 0.f, v);
+        }
+        uint4 hi, lo;
+        split8(y, hi, lo);
+        __nv_bfloat16* row = xc3 + size_t(t) * (3 * size_t(d)) + c;
+        *reinterpret_cast<uint4*>(row) = hi;
+        *reinterpret_cast<uint4*>(row + d) = hi;
+        *reinterpret_cast<uint4*>(row + 2 * d) = lo;
+      }
+    }
   }
   fence_proxy_async_global();  // the target GEMM reads xc3 through TMA
-}
-
-int64_t grid_for(int64_t items, int num_sms) {
-  int64_t blocks = (items + 255) / 256;
-  const int64_t cap = int64_t(num_sms) * 8;
-  return blocks > cap ? cap : (blocks < 1 ? 1 : blocks);
 }
 
 }  // namespace
 
 cudaError_t launch_split_bf16(const LaunchEnv& env, const float* src, int64_t rows, int cols,
                               __nv_bfloat16* dst, int nseg, unsigned lo_mask) {
-  const int64_t items = rows * (cols / 4);
+  const int64_t items = rows * (cols / 8);
   if (items == 0) return cudaSuccess;
-  return launch_pdl(split_bf16_kernel, dim3(unsigned(grid_for(items, env.num_sms))), dim3(256),
-                    0, env.stream, src, rows, cols, dst, nseg, lo_mask);
+  return launch_pdl(split_bf16_kernel, dim3(unsigned((items + 255) / 256)), dim3(256), 0,
+                    env.stream, src, rows, cols, dst, nseg, lo_mask);
 }
 
 cudaError_t launch_conv_fp32(const LaunchEnv& env, const float* x0, const float* conv_w,
                              __nv_bfloat16* xc3, int64_t rows, const DocMap& docs, int d,
                              int pad_mode) {
-  const int64_t items = rows * (d / 4);
+  const int64_t items = (rows + kConvFp32Rows - 1) / kConvFp32Rows * (d / 8);
   if (items == 0) return cudaSuccess;
-  return launch_pdl(conv3_fp32_kernel, dim3(unsigned(grid_for(items, env.num_sms))), dim3(256),
-                    0, env.stream, x0, conv_w, xc3, int(rows), docs, d, pad_mode);
+  return launch_pdl(conv3_fp32_kernel, dim3(unsigned((items + 255) / 256)), dim3(256), 0,
+                    env.stream, x0, conv_w, xc3, int(rows), docs, d, pad_mode);
 }
 
 }  // namespace ittt
