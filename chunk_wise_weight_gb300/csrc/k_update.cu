@@ -314,19 +314,26 @@ __global__ void __launch_bounds__(kBaseThreads, 1)
 // state_out.
 // ----------------------------------------------------------------------------
 
-// Sum of a row's per-block partial sums of squares, four independent
-// accumulators (the loads overlap).  The update kernel's preload and the
-// finalising kernel both call it, so they agree bit for bit.
-__device__ __forceinline__ float sum_partials(const float* base, size_t stride, int nblk) {
+// Sum of a row's partial sums of squares (two 128-column parts per
+// 256-column block), four independent accumulators (the loads overlap).
+// The update kernel's preload and the finalising kernel both call it, so
+// they agree bit for bit.
+__device__ __forceinline__ float sum_partials(const float* base, size_t stride, int nparts) {
+  // One term per 256-column block, its two 128-column parts added first;
+  // the block terms go round four accumulators in block order.
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  const int nblk = nparts >> 1;
+  auto blk = [&](int b) {
+    return __ldcg(base + size_t(2 * b) * stride) + __ldcg(base + size_t(2 * b + 1) * stride);
+  };
   int b = 0;
   for (; b + 4 <= nblk; b += 4) {
-    a0 += __ldcg(base + size_t(b) * stride);
-    a1 += __ldcg(base + size_t(b + 1) * stride);
-    a2 += __ldcg(base + size_t(b + 2) * stride);
-    a3 += __ldcg(base + size_t(b + 3) * stride);
+    a0 += blk(b);
+    a1 += blk(b + 1);
+    a2 += blk(b + 2);
+    a3 += blk(b + 3);
   }
-  for (; b < nblk; ++b) a0 += __ldcg(base + size_t(b) * stride);
+  for (; b < nblk; ++b) a0 += blk(b);
   return (a0 + a1) + (a2 + a3);
 }
 
@@ -581,11 +588,11 @@ __global__ void __launch_bounds__(pair_threads<NormUpdatePairSched>(), 1)
 //
 // At a boundary the epilogue of accumulator h (state S_{i+1} = W_i + eta
 // dW_i in TMEM):
-//   1. sums the squares of its row over its 128 columns (one part per
-//      epilogue group, as the per-launch walk does) and publishes the sum;
+//   1. sums the squares of its row over each 128-column half of its block
+//      (the per-launch walk's two parts) and publishes the two parts' sum;
 //   2. arrives on its (accumulator, group) counter and waits until every CTA
 //      of the group has published (a bounded spin on the counter);
-//   3. adds the 2 nf partial sums of its row in block order, forms
+//   3. adds the nf block sums of its row in block order, forms
 //      W_{i+1} = S_{i+1} / ||row||, writes it back into TMEM for the next
 //      chunk and out as the bf16 snapshot (or, after the last update, the
 //      fp32 state_out).
@@ -603,15 +610,15 @@ struct NormWalkParams {
   int w0_fp32;
   int64_t w0_bstride;
   float* state_out;      // [B, d, f] fp32, or nullptr
-  float* part;           // [2][G][2][nparts][256] row sums of squares
+  float* part;           // [2][G][2][nparts][256] row sums of squares, one per 256-column block
   unsigned int* arrive;  // [2][G] arrival counters, zero at launch
   int B, T, C, n, nupd;  // sequences, tokens each, chunk, chunks, updates per sequence
   int d, f, nd, nf, G, nparts, rounds;
 };
 
-// sum_partials' sum of one row's `n` partial sums, `stride` floats apart:
-// the same four accumulators in the same order, fed by loads issued 64 at a
-// time instead of four.
+// sum_partials' sum of one row's `n` block terms, `stride` floats apart
+// (each already the sum of its block's two 128-column parts): the same four
+// accumulators in the same order, fed by loads issued 64 at a time.
 __device__ __forceinline__ float sum_partials_batched(const float* base, size_t stride, int n) {
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   const int full = n & ~3;
@@ -748,9 +755,9 @@ struct NormWalkSched : PairDefaults {
       }
       if (c < kPartCols) ss[0] = a; else ss[1] = a;
     }
-    float* pw = const_cast<float*>(pbase) + size_t(2 * fb) * (2 * kBM);
-    __stcg(pw, ss[0]);
-    __stcg(pw + 2 * kBM, ss[1]);
+    // published as one term per block, the two parts added as the HBM
+    // walks' readers add them
+    __stcg(const_cast<float*>(pbase) + size_t(fb) * (2 * kBM), ss[0] + ss[1]);
     // 2. every CTA of the group has published
     epilogue_group_bar(st.group);
     if (row == 0) {
@@ -1020,7 +1027,7 @@ cudaError_t launch_update(const LaunchEnv& env, const CUtensorMap& tm_vhat, cons
 size_t norm_walk_part_bytes(int f, int pairs) {
   const int nf = (f + kBN - 1) / kBN;
   const int groups = pairs / nf > 0 ? pairs / nf : 1;
-  return size_t(2) * groups * 2 * size_t(2 * nf) * (2 * kBM) * sizeof(float);
+  return size_t(2) * groups * 2 * size_t(nf) * (2 * kBM) * sizeof(float);
 }
 
 size_t norm_walk_arrive_bytes(int pairs) { return size_t(2) * pairs * sizeof(unsigned int); }
@@ -1070,7 +1077,7 @@ cudaError_t launch_norm_walk(const LaunchEnv& env, const CUtensorMap& tm_vhat,
   p.nd = a.d / (2 * kBM);
   p.nf = nf;
   p.G = G;
-  p.nparts = 2 * nf;
+  p.nparts = nf;
   const int tasks = p.B * p.nd;
   p.rounds = (tasks + 2 * G - 1) / (2 * G);
   if ((e = cudaMemsetAsync(a.walk_arrive, 0, norm_walk_arrive_bytes(G), env.stream)) !=

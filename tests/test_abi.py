@@ -234,7 +234,7 @@ def test_workspace_bytes_and_launch_count(lib):
     nblk = -(-f // 256)
     tiles = -(-d // 128) * -(-f // 32)      # the fp32 state in 128 x 32 tiles
     groups = max(1, 128 // nblk)
-    walk = r(2 * groups * 2 * (2 * nblk) * 256 * 4) + r(2 * 128 * 4)
+    walk = r(2 * groups * 2 * nblk * 256 * 4) + r(2 * 128 * 4)
     assert (ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True)
             == want + r(B * tiles * 128 * 32 * 4) + r(2 * B * 2 * nblk * d * 4) + walk)
     assert ittt.workspace_bytes_ex(B, T, d, f, C, l2norm=True, dual=True) == 0
