@@ -308,6 +308,8 @@ struct Layout {
          partial = 0, walk_part = 0, walk_arrive = 0, total = 0;
   // fp32 inputs: the bf16 split operands of the gate/up and target GEMMs
   size_t h3 = 0, wg3 = 0, wu3 = 0, wt3 = 0;
+  size_t tickets = 0;  // the pair GEMMs' unit counters (zeroed by the call)
+  bool has_tickets = false;
 };
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -517,6 +519,10 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
     off += round_up(bytes);
     return at;
   };
+  // The unit counter of the apply on CTA pairs (it takes its units
+  // dynamically): every call that runs the primal apply.
+  L.has_tickets = !P->update_only && !P->dual;
+  if (L.has_tickets) L.tickets = take(ittt::kNumTickets * sizeof(unsigned int));
   if (o.z_buf == nullptr) L.z = take(size_t(P->M) * f * 2);
   if (o.vhat_buf == nullptr) L.vhat = take(size_t(P->M) * d * 2);
   if (!P->fused && !P->reuse) L.xc = take(size_t(P->M) * d * 2 * (P->fp32_in ? 3 : 1));
@@ -802,7 +808,8 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
       return s;
   }
 
-  const ittt::LaunchEnv env{stream, ds->num_sms, ds->status};
+  auto* tickets = L.has_tickets ? reinterpret_cast<unsigned int*>(ws + L.tickets) : nullptr;
+  const ittt::LaunchEnv env{stream, ds->num_sms, ds->status, tickets};
   // w0 == nullptr: the walk starts from zero (folding chunks only).
   const void* w0 = o.state_in ? o.state_in->data : (zero_start ? nullptr : W_down0->data);
   const bool w0_fp32 = o.state_in ? true : (!zero_start && W_down0->dtype == ITTT_FP32);
@@ -821,6 +828,9 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   const char* what = nullptr;
 #define ITTT_STEP(call, name) \
   if (what == nullptr && (e = (call)) != cudaSuccess) what = name
+  if (tickets != nullptr)
+    ITTT_STEP(cudaMemsetAsync(tickets, 0, ittt::kNumTickets * sizeof(unsigned int), stream),
+              "unit counter reset");
   ITTT_STEP(rec(2 * ITTT_PHASE_CONV, stream), "event record");
   if (what == nullptr && P.packed &&
       (s = stage_table(ds, tab, P.table.data(), P.table.size(), stream)) != ITTT_OK)

@@ -43,6 +43,9 @@ constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // 64 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// The pair GEMMs' unit counters, zeroed at the start of every call (shared
+// like the scratch: calls are serialised on one stream).
+static __device__ __align__(16) unsigned int g_noalloc_tickets[ittt::kNumTickets];
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -52,6 +55,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 struct NoAllocDevice {
   bool ready = false;
   unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch
+  unsigned int* tickets = nullptr;   // device address of g_noalloc_tickets
   unsigned int* status = nullptr;
   int num_sms = 0;
 };
@@ -104,6 +108,11 @@ ittt_status na_setup(NoAllocDevice** out) {
     if (e != cudaSuccess)
       return na_fail(ITTT_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
     nd.scratch = static_cast<unsigned char*>(scratch);
+    void* tickets = nullptr;
+    e = cudaGetSymbolAddress(&tickets, g_noalloc_tickets);
+    if (e != cudaSuccess)
+      return na_fail(ITTT_ERR_CUDA, "cudaGetSymbolAddress(tickets): %s", cudaGetErrorString(e));
+    nd.tickets = static_cast<unsigned int*>(tickets);
     e = ittt::status_word_address(&nd.status);
     if (e != cudaSuccess)
       return na_fail(ITTT_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
@@ -287,7 +296,7 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   if (out->dtype == ITTT_BF16 && (s = na_map(&tm_os, out->data, d, M, 64, 64, "O (store)")))
     return s;
 
-  const ittt::LaunchEnv env{stream, nd->num_sms, nd->status};
+  const ittt::LaunchEnv env{stream, nd->num_sms, nd->status, nd->tickets};
   ittt::DocMap docs;
   memset(&docs, 0, sizeof(docs));
   docs.ndocs = int(B);
@@ -304,7 +313,10 @@ extern "C" ittt_status ittt_forward_noalloc(const ittt_tensor* H, const ittt_ten
   const bool w0_fp32 = W_down0->dtype == ITTT_FP32;
   cudaError_t e;
   const char* what = nullptr;
-  if ((e = ittt::launch_conv(env, tm_x0, static_cast<const float*>(conv_w->data), xc,
+  if ((e = cudaMemsetAsync(nd->tickets, 0, ittt::kNumTickets * sizeof(unsigned int), stream)) !=
+      cudaSuccess) {
+    what = "unit counters";
+  } else if ((e = ittt::launch_conv(env, tm_x0, static_cast<const float*>(conv_w->data), xc,
                              int64_t(M), docs, int(d), ITTT_PAD_CHUNK)) != cudaSuccess) {
     what = "conv";
   } else if ((e = target_pair_or_single(env, tm_xc, tm_wt, tm_wt128, tm_vs,

@@ -32,6 +32,7 @@ struct ApplyParams {
   int w0_direct;        // a document's first chunk reads W_0 itself, not its snapshot slot
   int d, f;
   int nt, kblocks;
+  unsigned int* ticket;  // the pair kernel's unit counter (LaunchEnv::tickets)
 };
 
 // bf16 O in whole 64-row halves: 64-column TMA stores (columns >= d are
@@ -160,6 +161,7 @@ struct ApplyPairSched : PairDefaults {
   using Params = ApplyParams;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(2 * kBM, kBN, false, false);
   static constexpr bool kStagedStores = true;
+  static constexpr bool kDynamicUnits = true;
 
   const Params& p;
   const int rank;
@@ -167,6 +169,7 @@ struct ApplyPairSched : PairDefaults {
   const CUtensorMap* bmap = nullptr;
 
   __device__ ApplyPairSched(const Params& pp, uint32_t r) : p(pp), rank(int(r)) {}
+  __device__ unsigned int* unit_ticket() const { return p.ticket; }
   __device__ int num_units() const { return p.docs.ntiles2 * p.nt; }
   __device__ void begin_unit(int u, int local) {
     const int nt = u % p.nt;
@@ -230,6 +233,8 @@ cudaError_t launch_apply_pair(const LaunchEnv& env, const CUtensorMap& tm_z,
   p.f = f;
   p.nt = (d + kBN - 1) / kBN;
   p.kblocks = (f + kBK - 1) / kBK;
+  p.ticket = env.tickets != nullptr ? env.tickets + kTicketApply : nullptr;
+  if (p.ticket == nullptr) return cudaErrorInvalidValue;
   const int64_t units = int64_t(docs.ntiles2) * p.nt;
   if (units == 0) return cudaSuccess;
   const size_t smem = pair_smem_bytes<ApplyPairSched>();
@@ -250,6 +255,7 @@ cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z, const CU
                          const CUtensorMap* tm_w0, const CUtensorMap& tm_os, void* out,
                          bool out_fp32, const DocMap& docs, int d, int f) {
   ApplyParams p;
+  p.ticket = nullptr;  // one CTA per SM: fixed stride
   p.tm_z = tm_z;
   p.tm_snap = tm_snap;
   p.w0_direct = tm_w0 != nullptr ? 1 : 0;

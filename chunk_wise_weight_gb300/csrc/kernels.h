@@ -37,7 +37,12 @@ struct LaunchEnv {
   cudaStream_t stream;
   int num_sms;
   unsigned int* status;  // device status word (kStatusTimeout bits)
+  // kNumTickets unit counters in device memory, zero before the call's first
+  // kernel: a pair GEMM that takes its units dynamically (the apply) draws
+  // from its own.
+  unsigned int* tickets = nullptr;
 };
+enum TicketSlot : int { kTicketApply = 0, kNumTickets = 4 };
 
 // The documents along the packed token axis, each with its own fast-weight
 // state that starts from W_0 (the state is reset at document boundaries:

@@ -150,6 +150,13 @@ struct SchedDefaults {
   // the two accumulators' epilogues then run side by side instead of in
   // turn on the same warps.
   static constexpr bool kAccTeams = false;
+  // With kDynamicUnits (CTA-pair pipeline only; not with kPreload or
+  // kAccTeams) the pairs take units in increasing order from a counter in
+  // global memory, zero at launch, instead of each walking a fixed stride:
+  //   unsigned int* unit_ticket()
+  // Units then start in index order whatever the pairs' speeds, so the
+  // units in flight stay within about one round of each other.
+  static constexpr bool kDynamicUnits = false;
 };
 
 template <class S>

@@ -19,7 +19,11 @@
 //   warps 2..5     : epilogue on this CTA's accumulator rows (with two epilogue
 //   (and 6..9)       groups, each group on its share of the columns); a release
 //                    arrives on the leader's acc_empty barrier.
-// Both CTAs walk the same units in the same order.  Every wait is bounded
+// Both CTAs walk the same units in the same order: a fixed stride of the
+// unit index, or (kDynamicUnits) the units the leader's producer draws from
+// a global counter and hands to every role of both CTAs through a small ring
+// in shared memory (unit_full: the slot holds the next unit; unit_empty:
+// every reader took it).  Every wait is bounded
 // (kWaitLimitNs); a CTA that gives up records kStatusTimeout and unwinds,
 // and its peer's waits then run out too.  Cluster barriers after set-up and
 // before TMEM release keep each CTA's barriers and shared memory alive while
@@ -46,6 +50,7 @@
 namespace ittt {
 
 constexpr int kMaxPairStages = 8;
+constexpr int kUnitRing = 8;  // units handed out ahead of the slowest reader
 constexpr uint32_t kPairATileBytes = 128 * kBK * 2;  // 16 KiB: 128 rows of A
 constexpr uint32_t kPairBTileBytes = 128 * kBK * 2;  // 16 KiB: 128 rows of B
 constexpr uint32_t kPairStageBytes = kPairATileBytes + kPairBTileBytes;
@@ -70,7 +75,17 @@ struct __align__(8) PairSync {
   uint32_t tmem_base;
   int abort_flag;
   int vote[8];                     // epilogue warps' go/unwind votes, four per group
+  uint64_t unit_full[kUnitRing];   // both: the slot holds the next unit (kDynamicUnits)
+  uint64_t unit_empty[kUnitRing];  // leader: every reader of both CTAs took the slot
+  int unit_ring[kUnitRing];        // the unit, or -1 once the counter passed the last
 };
+
+// Readers of a unit slot: the leader's MMA thread, the peer's producer and
+// every epilogue warp of both CTAs (the leader's producer writes it).
+template <class S>
+__host__ __device__ constexpr uint32_t unit_readers() {
+  return 2u + 2u * 4u * uint32_t(S::kEpilogueGroups);
+}
 
 template <class S>
 __host__ __device__ constexpr size_t pair_smem_bytes() {
@@ -108,6 +123,13 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
                 2 * kEpilogueThreads * (S::kAccTeams ? 1 : S::kEpilogueGroups));
     }
     mbar_init(&sync->drain, 1);
+    if constexpr (S::kDynamicUnits) {
+      static_assert(!S::kPreload && !S::kAccTeams, "dynamic units need neither");
+      for (int r = 0; r < kUnitRing; ++r) {
+        mbar_init(&sync->unit_full[r], 1);
+        mbar_init(&sync->unit_empty[r], unit_readers<S>());
+      }
+    }
     sync->abort_flag = 0;
     fence_mbar_init();
   }
@@ -124,6 +146,27 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
   griddep_wait();
   griddep_launch_dependents();
 
+  // The unit of this CTA's `local`-th step: a fixed stride, or
+  // (kDynamicUnits) the ring's slot.  -1: no more units; -2: a wait ran out.
+  // take_unit waits and reads; give_unit (after every reader of the calling
+  // warp or thread has read) frees the slot.
+  auto take_unit = [&](int local, int nunits) -> int {
+    if constexpr (S::kDynamicUnits) {
+      const int slot = local % kUnitRing;
+      if (!mbar_wait_cluster(&sync->unit_full[slot], uint32_t(local / kUnitRing) & 1u,
+                             abort_flag))
+        return -2;
+      return *reinterpret_cast<volatile int*>(&sync->unit_ring[slot]);
+    } else {
+      const int u = pair + local * npairs;
+      return u < nunits ? u : -1;
+    }
+  };
+  auto give_unit = [&](int local) {
+    if constexpr (S::kDynamicUnits)
+      mbar_arrive_cluster(mapa_shared(smem_u32(&sync->unit_empty[local % kUnitRing]), 0));
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
@@ -132,8 +175,36 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
       uint32_t phase = 0;
       uint32_t issued = 0;
       const int nunits = sched.num_units();
-      int local = 0;
-      for (int u = pair; u < nunits && !*abort_flag; u += npairs, ++local) {
+      for (int local = 0; !*abort_flag; ++local) {
+        int u = -1;
+        bool drawn = false;
+        if constexpr (S::kDynamicUnits) {
+          if (leader) {
+            // Draw the next unit and hand it to both CTAs.
+            const int slot = local % kUnitRing;
+            if (!mbar_wait_cluster(&sync->unit_empty[slot],
+                                   (uint32_t(local / kUnitRing) & 1u) ^ 1u, abort_flag)) {
+              raise_abort(abort_flag, status, kStatusTimeout);
+              break;
+            }
+            u = int(atomicAdd(sched.unit_ticket(), 1u));
+            if (u >= nunits) u = -1;
+            sync->unit_ring[slot] = u;
+            st_shared_cluster_s32(mapa_shared(smem_u32(&sync->unit_ring[slot]), 1), u);
+            mbar_arrive_cluster(mapa_shared(smem_u32(&sync->unit_full[slot]), 0));
+            mbar_arrive_cluster(mapa_shared(smem_u32(&sync->unit_full[slot]), 1));
+            drawn = true;
+          }
+        }
+        if (!drawn) {
+          u = take_unit(local, nunits);
+          if (u == -2) {
+            raise_abort(abort_flag, status, kStatusTimeout);
+            break;
+          }
+          give_unit(local);
+        }
+        if (u < 0) break;
         sched.begin_unit(u, local);
         const int nseg = sched.num_segments();
         for (int s = 0; s < nseg && !*abort_flag; ++s) {
@@ -173,9 +244,15 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
       uint32_t phase = 0;
       uint32_t acc_use[2] = {0u, 0u};
       const int nunits = sched.num_units();
-      int local = 0;
       bool ok = true;
-      for (int u = pair; u < nunits && ok; u += npairs, ++local) {
+      for (int local = 0; ok; ++local) {
+        const int u = take_unit(local, nunits);
+        if (u == -2) {
+          raise_abort(abort_flag, status, kStatusTimeout);
+          break;
+        }
+        give_unit(local);
+        if (u < 0) break;
         sched.begin_unit(u, local);
         const int nseg = sched.num_segments();
         for (int s = 0; s < nseg && ok; ++s) {
@@ -244,10 +321,48 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
                                           mapa_shared(smem_u32(&sync->acc_empty[1]), 0)};
     uint32_t acc_use[2] = {0u, 0u};
     bool preloaded[2] = {false, false};
+    // The warps that meet at epilogue barriers agree on whether a wait
+    // succeeded, so that they unwind together.
+    auto agree = [&](bool got) -> bool {
+      if constexpr (S::kBindsSync && !S::kAccTeams) {
+        // One vote over both groups: such an epilogue meets the other
+        // group at CTA-wide barriers.
+        static_assert(S::kEpilogueGroups == 2, "CTA-wide vote over two groups");
+        volatile int* vote = sync->vote;
+        if (lane == 0) vote[warp - 2] = got ? 1 : 0;
+        epilogue_all_bar();
+        got = (vote[0] & vote[1] & vote[2] & vote[3] & vote[4] & vote[5] & vote[6] & vote[7]) != 0;
+        epilogue_all_bar();
+      } else if constexpr (S::kStagedStores) {
+        volatile int* vote = sync->vote + 4 * group;
+        if (lane == 0) vote[quad] = got ? 1 : 0;
+        epilogue_group_bar(group);
+        got = (vote[0] & vote[1] & vote[2] & vote[3]) != 0;
+        epilogue_group_bar(group);
+      }
+      return got;
+    };
     const int nunits = sched.num_units();
-    int local = 0;
     bool ok = true;
-    for (int u = pair; u < nunits && ok; u += npairs, ++local) {
+    for (int local = 0; ok; ++local) {
+      int u;
+      if constexpr (S::kDynamicUnits) {
+        const int slot = local % kUnitRing;
+        const bool got = agree(__all_sync(
+            0xffffffffu, mbar_wait_cluster(&sync->unit_full[slot],
+                                           uint32_t(local / kUnitRing) & 1u, abort_flag)));
+        if (!got) {
+          raise_abort(abort_flag, status, kStatusTimeout);
+          ok = false;
+          break;
+        }
+        u = *reinterpret_cast<volatile int*>(&sync->unit_ring[slot]);
+        __syncwarp();
+        if (lane == 0) give_unit(local);
+      } else {
+        u = take_unit(local, nunits);
+      }
+      if (u < 0) break;
       sched.begin_unit(u, local);
       const int nseg = sched.num_segments();
       if constexpr (S::kPreload) {
@@ -271,24 +386,8 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
           static_assert(S::kEpilogueGroups == 2, "one epilogue group per accumulator");
           if (h != group) continue;  // the other group's accumulator
         }
-        bool got = __all_sync(0xffffffffu, mbar_wait(&sync->acc_full[h], acc_use[h] & 1u,
-                                                     abort_flag));
-        if constexpr (S::kBindsSync && !S::kAccTeams) {
-          // One vote over both groups: such an epilogue meets the other
-          // group at CTA-wide barriers, so the groups unwind together.
-          static_assert(S::kEpilogueGroups == 2, "CTA-wide vote over two groups");
-          volatile int* vote = sync->vote;
-          if (lane == 0) vote[warp - 2] = got ? 1 : 0;
-          epilogue_all_bar();
-          got = (vote[0] & vote[1] & vote[2] & vote[3] & vote[4] & vote[5] & vote[6] & vote[7]) != 0;
-          epilogue_all_bar();
-        } else if constexpr (S::kStagedStores) {
-          volatile int* vote = sync->vote + 4 * group;
-          if (lane == 0) vote[quad] = got ? 1 : 0;
-          epilogue_group_bar(group);
-          got = (vote[0] & vote[1] & vote[2] & vote[3]) != 0;
-          epilogue_group_bar(group);
-        }
+        const bool got = agree(__all_sync(
+            0xffffffffu, mbar_wait(&sync->acc_full[h], acc_use[h] & 1u, abort_flag)));
         if (!got) {
           raise_abort(abort_flag, status, kStatusTimeout);
           ok = false;

@@ -78,6 +78,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// mbar_try_wait / mbar_wait with acquire at cluster scope: a phase that the
+// other CTA of the pair completed (its arrive carries release at cluster
+// scope) makes that CTA's earlier writes to this CTA's shared memory
+// visible.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  const volatile int* abort_flag,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // Records a device failure and tells the CTA's other roles to unwind.
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, unsigned int* status,
                                             uint32_t bits) {
@@ -346,6 +374,12 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
                : "memory");
+}
+
+// 32-bit store to the shared-memory word at shared::cluster address `addr`
+// (either CTA of the cluster).
+__device__ __forceinline__ void st_shared_cluster_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Barrier of every thread of both CTAs of the cluster (each thread arrives

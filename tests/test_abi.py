@@ -204,10 +204,11 @@ def test_workspace_bytes_and_launch_count(lib):
         return (x + 255) // 256 * 256
     B, T, d, f, C = 2, 1024, 320, 1000, 256
     n = T // C
-    want = r(B * T * f * 2) + 2 * r(B * T * d * 2) + r(B * n * d * f * 2)
+    tk = 256   # the apply's unit counter block (four 4-byte counters, rounded up)
+    want = tk + r(B * T * f * 2) + 2 * r(B * T * d * 2) + r(B * n * d * f * 2)
     assert ittt.workspace_bytes(B, T, d, f, C) == want
     assert ittt.workspace_bytes_ex(B, T, d, f, C) == want
-    want3 = r(B * T * f * 2) + 2 * r(B * T * d * 2) + r(B * 3 * d * f * 2)   # 1024 = 2*384+256
+    want3 = tk + r(B * T * f * 2) + 2 * r(B * T * d * 2) + r(B * 3 * d * f * 2)  # 1024 = 2*384+256
     assert ittt.workspace_bytes(B, T, d, f, 384) == want3
     assert ittt.workspace_bytes(B, T, d, f, 0) == 0
     assert ittt.workspace_bytes(B, T, 60, f, C) == 0
@@ -224,7 +225,7 @@ def test_workspace_bytes_and_launch_count(lib):
     # document map 5, the 128- and 256-row tile bases 2*(5+1) and the
     # updating documents 2 ints
     cu = [0, 300, 1024]
-    want_packed = (r(T * f * 2) + 2 * r(T * d * 2) + r(5 * d * f * 2)
+    want_packed = (tk + r(T * f * 2) + 2 * r(T * d * 2) + r(5 * d * f * 2)
                    + r((6 + 5 + 12 + 2) * 4))
     assert ittt.workspace_bytes_ex(1, T, d, f, C, cu_seqlens=cu) == want_packed
     # the normalised walk keeps an fp32 state and row partial sums per
@@ -338,6 +339,7 @@ def test_update_only_and_reuse_scratch():
     B, T, d, f, C = 2, 1024, 320, 1000, 256
     n = T // C
     z, vh, xc, snap = r(B * T * f * 2), r(B * T * d * 2), r(B * T * d * 2), r(B * n * d * f * 2)
+    tk = 256   # the apply's unit counters (none when the call applies nothing)
     fake = torch.empty(0)
     # folding chunks only forms no snapshots
     assert (ittt.workspace_bytes_ex(B, T, d, f, C, update_only=True, state_out=fake)
@@ -345,7 +347,7 @@ def test_update_only_and_reuse_scratch():
     assert ittt.workspace_bytes_ex(B, T, d, f, C, update_only=True) == 0   # needs state_out
     # reusing Z and eta*Vhat needs neither the producers' scratch nor Xc
     assert (ittt.workspace_bytes_ex(B, T, d, f, C, reuse_zv=True, z_buf=fake, vhat_buf=fake)
-            == snap)
+            == tk + snap)
     assert ittt.workspace_bytes_ex(B, T, d, f, C, reuse_zv=True, z_buf=fake) == 0
     assert ittt.workspace_bytes_ex(B, T, d, f, C, update_only=True, reuse_zv=True,
                                    state_out=fake, z_buf=fake, vhat_buf=fake) == 0
