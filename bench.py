@@ -124,6 +124,10 @@ def parse_args():
     ap.add_argument("--graph", action="store_true",
                     help="capture one step (with a caller workspace) into a CUDA graph and time "
                          "its replays; per-kernel phases then come from an eager pass")
+    ap.add_argument("--fp32-inputs", action="store_true",
+                    help="draw H, X0, W_gate, W_up and W_target unrounded and pass them as "
+                         "fp32: the library splits each value into bf16 hi/lo parts and "
+                         "runs the gate/up and target contractions over K = 3 d")
     ap.add_argument("--seq-shards", type=int, default=0,
                     help="run the sequence-sharded schedule with this many spans, the spans "
                          "run in turn on this GPU (fold, exclusive prefix, apply); one rank only")
@@ -249,25 +253,35 @@ class ClockSampler:
                 "samples": len(rows), "source": "nvidia-smi every 200 ms"}
 
 
-def phase_model(B, T, d, f, C, dual=False, cu=None):
+def phase_model(B, T, d, f, C, dual=False, cu=None, fp32_inputs=False):
     """Algorithmic work per phase: ('tensor', FLOPs) or ('hbm', bytes).  The
     dual form's extra work (scores Z Z^T, S Vhat) is charged at the primal
     form's FLOPs, the work the layer needs.  With packed documents (cu) B is
     1, every document is chunked on its own and only the tokens before each
-    document's last chunk update."""
+    document's last chunk update.  fp32 inputs: the conv phase also splits
+    H and the three weights (4 B read, 6 B written per element: three bf16
+    segments) and writes Xc split the same way; the target and gate/up
+    contractions run over K = 3 d (three bf16 products per input product)."""
     lens = [b - a for a, b in zip(cu, cu[1:])] if cu else [T] * B
     upd_tokens = sum(L - (L - (-(-L // C) - 1) * C) for L in lens)
+    M = B * T
+    if fp32_inputs:
+        conv = (2.0 * M * d + 2.0 * f * d + 1.0 * d * d) * (4 + 6) + d * 3 * 4
+    else:
+        conv = 2.0 * M * d * 2 + d * 3 * 4
+    kx = 3.0 if fp32_inputs else 1.0
     return {
-        "conv": ("hbm", 2.0 * B * T * d * 2 + d * 3 * 4),
-        "target": ("tensor", 2.0 * B * T * d * d),
-        "gateup": ("tensor", 4.0 * B * T * d * f),
+        "conv": ("hbm", conv),
+        "target": ("tensor", kx * 2.0 * B * T * d * d),
+        "gateup": ("tensor", kx * 4.0 * B * T * d * f),
         "snapshot0": ("hbm", 1.0 * d * f * 2 + len(lens) * d * f * 2),
         "update": ("tensor", 2.0 * upd_tokens * d * f),
         "apply": ("tensor", 2.0 * B * T * d * f),
     }
 
 
-def launches_per_step(B, T, C, cu, l2norm, dual=False, d=2560, f=9728, pairs=76):
+def launches_per_step(B, T, C, cu, l2norm, dual=False, d=2560, f=9728, pairs=76,
+                      fp32_inputs=False):
     """Kernel launches of one forward with the bench's bf16 W_down0 and no
     snapshot buffer: conv, target, gate/up, the update walk, apply (the
     apply reads W_0 itself, so no snapshot-0 copy); packed documents add the
@@ -276,14 +290,16 @@ def launches_per_step(B, T, C, cu, l2norm, dual=False, d=2560, f=9728, pairs=76)
     the batch is regular, d a multiple of 256, every chunk a multiple of 64
     tokens and a group of ceil(f/256) CTA pairs fits in the GPU's 76 (the
     state stays in TMEM), else one launch per chunk that updates plus a
-    finalising launch."""
+    finalising launch.  fp32 inputs add the four hi/lo splits (H, W_gate,
+    W_up, W_target); their convolution kernel replaces the bf16 one."""
     lens = [b - a for a, b in zip(cu, cu[1:])] if cu else [T] * B
     steps = max(-(-L // C) - 1 for L in lens)
+    splits = 4 if fp32_inputs else 0
     if dual:
-        return 5
+        return 5 + splits + (1 if cu else 0)
     in_tmem = not cu and d % 256 == 0 and C % 64 == 0 and -(-f // 256) <= pairs
     walk = (steps + 1 if l2norm and not in_tmem else 1) if steps > 0 else 0
-    return 4 + walk + (1 if cu else 0)
+    return 4 + walk + (1 if cu else 0) + splits
 
 
 def run_seq_shards(args, cfg, tensors, stream, dev, peaks, peak_src, rates, local, cpu):
@@ -425,6 +441,8 @@ def arm_config(cfg, args, world, cu=None):
             "eta_tok": "per-token rates" if args.eta_tok else None,
             "update_rule": "L2-normalised rows" if args.l2norm else "additive",
             "launch": "CUDA graph replay" if getattr(args, "graph", False) else "eager",
+            "inputs": ("fp32, split into bf16 hi/lo parts (K = 3d)"
+                       if getattr(args, "fp32_inputs", False) else "bf16"),
             "l2": l2_note(cfg, T)}
 
 
@@ -598,11 +616,14 @@ def main():
     # sequences and each rank draws and runs its own contiguous share.
     first, last = shard_range(B * world, world, rank)
     assert last - first == B
-    inp = make_inputs(B, T, d, f, seed=1234 + args.config)
+    inp = make_inputs(B, T, d, f, seed=1234 + args.config, round_bf16=not args.fp32_inputs)
     if first > 0:
         g = torch.Generator().manual_seed(1234 + args.config + 1000 * first)
-        inp["H"] = torch.randn(B, T, d, generator=g).to(torch.bfloat16).float()
-        inp["X0"] = torch.randn(B, T, d, generator=g).to(torch.bfloat16).float()
+        inp["H"] = torch.randn(B, T, d, generator=g)
+        inp["X0"] = torch.randn(B, T, d, generator=g)
+        if not args.fp32_inputs:
+            inp["H"] = inp["H"].to(torch.bfloat16).float()
+            inp["X0"] = inp["X0"].to(torch.bfloat16).float()
     cu = None
     if args.packed:
         # The same tokens as one packed row of documents.
@@ -611,10 +632,11 @@ def main():
         inp["X0"] = inp["X0"].reshape(1, B * T, d)
         B, T = 1, B * T
     bf = torch.bfloat16
-    H = inp["H"].to(dev, bf)
-    X0 = inp["X0"].to(dev, bf)
-    Wg, Wu = inp["W_gate"].to(dev, bf), inp["W_up"].to(dev, bf)
-    W0, Wt = inp["W_down0"].to(dev, bf), inp["W_target"].to(dev, bf)
+    adt = torch.float32 if args.fp32_inputs else bf  # H, X0, W_gate, W_up, W_target
+    H = inp["H"].to(dev, adt)
+    X0 = inp["X0"].to(dev, adt)
+    Wg, Wu = inp["W_gate"].to(dev, adt), inp["W_up"].to(dev, adt)
+    W0, Wt = inp["W_down0"].to(dev, bf), inp["W_target"].to(dev, adt)
     cw = inp["conv_w"].to(dev, torch.float32)
     out = torch.empty(B, T, d, dtype=bf, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -623,11 +645,13 @@ def main():
         g_rates = torch.Generator().manual_seed(4321 + first)
         rates = (torch.rand(B, T, generator=g_rates) + 0.5).to(dev)
 
+    if args.fp32_inputs and args.fused_conv:
+        raise SystemExit("--fp32-inputs runs the split convolution (no --fused-conv)")
     if args.seq_shards:
         if world > 1:
             raise SystemExit("--seq-shards runs its spans in turn on one GPU: one rank only")
-        if args.packed or args.l2norm or args.dual or dual_form(cfg, args):
-            raise SystemExit("--seq-shards needs regular sequences and the additive update")
+        if args.packed or args.l2norm or args.dual or dual_form(cfg, args) or args.fp32_inputs:
+            raise SystemExit("--seq-shards needs regular bf16 sequences and the additive update")
         return run_seq_shards(args, cfg, (H, X0, Wg, Wu, W0, Wt, cw), stream, dev, peaks,
                               peak_src, rates, local, cpu)
 
@@ -637,7 +661,7 @@ def main():
             raise SystemExit("--graph: packed documents stage host tables and cannot be captured")
         ws_bytes = ittt.workspace_bytes_ex(B, T, d, f, C, fused_conv=args.fused_conv,
                                            dual=args.dual, primal=args.primal,
-                                           l2norm=args.l2norm,
+                                           l2norm=args.l2norm, fp32_inputs=args.fp32_inputs,
                                            eta_tok=rates)
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
@@ -723,7 +747,7 @@ def main():
     assert form_dual == (ittt.plan_form(B, T, d, f, C, dual=args.dual, primal=args.primal,
                                         fused_conv=args.fused_conv, l2norm=args.l2norm,
                                         cu_seqlens=cu) == ittt.FORM_DUAL)
-    model = phase_model(B, T, d, f, C, form_dual, cu)
+    model = phase_model(B, T, d, f, C, form_dual, cu, args.fp32_inputs)
     phases = {}
     for name in ittt.PHASES:
         ms = pass_ms[name]
@@ -775,8 +799,8 @@ def main():
         if near:
             os.sched_setaffinity(0, near)
         try:
-            H_h = inp["H"].to(bf).pin_memory()
-            X0_h = inp["X0"].to(bf).pin_memory()
+            H_h = inp["H"].to(adt).pin_memory()
+            X0_h = inp["X0"].to(adt).pin_memory()
             O_h = [torch.empty(B, T, d, dtype=bf).pin_memory() for _ in range(2)]
         finally:
             os.sched_setaffinity(0, allowed)
@@ -845,8 +869,8 @@ def main():
         e2e_steps(e2e_n, e0, e1)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
-        h2d_b = H_h.numel() * 2 + X0_h.numel() * 2
-        d2h_b = O_h[0].numel() * 2
+        h2d_b = H_h.numel() * H_h.element_size() + X0_h.numel() * X0_h.element_size()
+        d2h_b = O_h[0].numel() * O_h[0].element_size()
         ms_up = copies_only(e2e_n, True, False)
         ms_down = copies_only(e2e_n, False, True)
         ms_both = copies_only(e2e_n, True, True)
@@ -884,7 +908,8 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": launches_per_step(B, T, C, cu, args.l2norm, form_dual, d, f) * args.steps,
+            "gpu_launches": launches_per_step(B, T, C, cu, args.l2norm, form_dual, d, f,
+                                              fp32_inputs=args.fp32_inputs) * args.steps,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
