@@ -48,15 +48,17 @@ __device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
 // bit k of lo_mask is set, else the hi part.  One thread per eight columns
 // of a row (cols is a multiple of 8): 16-byte loads and stores, one item per
 // thread on a grid as large as the work (the block scheduler then balances
-// the SMs; a single wave of grid-stride blocks measured 10-15% slower).
+// the SMs; a single wave of grid-stride blocks measured 10-15% slower).  The
+// loop only strides past a grid capped at kMaxGridBlocks.
 __global__ void __launch_bounds__(256)
     split_bf16_kernel(const float* __restrict__ src, int64_t rows, int cols,
                       __nv_bfloat16* __restrict__ dst, int nseg, unsigned lo_mask) {
   griddep_wait();  // programmatic launch: the previous grid is done
   griddep_launch_dependents();
   const int q8 = cols >> 3;
-  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx < rows * q8) {
+  const int64_t total = rows * q8;
+  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
     const int64_t r = idx / q8;
     const int c = int(idx - r * q8) * 8;
     float x[8];
@@ -71,6 +73,7 @@ __global__ void __launch_bounds__(256)
 }
 
 constexpr int kConvFp32Rows = 4;  // rows per thread: a 6-row window of loads
+constexpr int64_t kMaxGridBlocks = int64_t(1) << 30;
 
 struct TapRange {
   int lo, hi;  // taps read rows in [lo, hi)
@@ -103,11 +106,12 @@ __global__ void __launch_bounds__(256)
   griddep_wait();
   griddep_launch_dependents();
   const int q8 = d >> 3;
-  const int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int rb = int(idx / q8);
-  const int c = int(idx - int64_t(rb) * q8) * 8;
-  const int t0 = rb * kConvFp32Rows;
-  if (t0 < rows) {
+  const int64_t total = int64_t((rows + kConvFp32Rows - 1) / kConvFp32Rows) * q8;
+  for (int64_t idx = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int rb = int(idx / q8);
+    const int c = int(idx - int64_t(rb) * q8) * 8;
+    const int t0 = rb * kConvFp32Rows;
     float w0[8], w1[8], w2[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -158,7 +162,8 @@ cudaError_t launch_split_bf16(const LaunchEnv& env, const float* src, int64_t ro
                               __nv_bfloat16* dst, int nseg, unsigned lo_mask) {
   const int64_t items = rows * (cols / 8);
   if (items == 0) return cudaSuccess;
-  return launch_pdl(split_bf16_kernel, dim3(unsigned((items + 255) / 256)), dim3(256), 0,
+  const int64_t blocks = (items + 255) / 256;
+  return launch_pdl(split_bf16_kernel, dim3(unsigned(blocks < kMaxGridBlocks ? blocks : kMaxGridBlocks)), dim3(256), 0,
                     env.stream, src, rows, cols, dst, nseg, lo_mask);
 }
 
@@ -167,7 +172,8 @@ cudaError_t launch_conv_fp32(const LaunchEnv& env, const float* x0, const float*
                              int pad_mode) {
   const int64_t items = (rows + kConvFp32Rows - 1) / kConvFp32Rows * (d / 8);
   if (items == 0) return cudaSuccess;
-  return launch_pdl(conv3_fp32_kernel, dim3(unsigned((items + 255) / 256)), dim3(256), 0,
+  const int64_t blocks = (items + 255) / 256;
+  return launch_pdl(conv3_fp32_kernel, dim3(unsigned(blocks < kMaxGridBlocks ? blocks : kMaxGridBlocks)), dim3(256), 0,
                     env.stream, x0, conv_w, xc3, int(rows), docs, d, pad_mode);
 }
 

@@ -130,6 +130,7 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
   static constexpr bool kPreload = true;
   static constexpr bool kStagedStores = true;
   static constexpr bool kRaggedK = !kPair;
+  static constexpr bool kEarlyRelease = kPair;
 
   const Params& p;
   const int rank;
@@ -227,6 +228,15 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
   // >= f are not written) and, after the last update, the fp32 state when
   // the caller wants it (direct stores).
   __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& stg) const {
+    AccRelease none{0u};
+    epilogue(s, row, trow, stg, none);
+  }
+  // On CTA pairs the epilogue releases the accumulator itself: a snapshot
+  // row is read whole from TMEM into registers (as bf16 pairs) first, so the
+  // next chunk's MMAs into this accumulator start while it is staged and
+  // stored.  (Behind the other half's MMAs that wait was hidden; a unit
+  // walking a single half waited for the whole epilogue at every chunk.)
+  __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& stg, AccRelease& rel) const {
     const int i = seg_chunk(s);
     const int h = s - i * nh;
     const int m = m0 + row;
@@ -237,6 +247,31 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
                     ? p.state_out + (size_t(doc) * p.d + size_t(row_ok ? m : 0)) * size_t(p.f)
                     : nullptr;
     const int slot = slot0 + i + 1;
+    if (write_snap && st == nullptr) {
+      uint32_t pk[kBN / 2];  // the row's 256 columns as bf16 pairs
+#pragma unroll
+      for (int c = 0; c < kBN; c += 32) {
+        uint32_t v[32];
+        tmem_ld_32cols(trow + uint32_t(c), v);
+        tmem_wait_ld();
+        pin_regs(v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[c / 2 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+      }
+      rel();
+#pragma unroll
+      for (int g = 0; g < kBN / 64; ++g) {
+        uint8_t* buf = stg.acquire();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          stg.put(buf, q,
+                  make_uint4(pk[g * 32 + 4 * q], pk[g * 32 + 4 * q + 1], pk[g * 32 + 4 * q + 2],
+                             pk[g * 32 + 4 * q + 3]));
+        stg.commit(buf, [&](uint8_t* src) { tma_store_3d(&p.tm_ss, src, n0 + g * 64, m0, slot); });
+      }
+      return;
+    }
 #pragma unroll 1
     for (int g = 0; g < kBN / 64; ++g) {
       uint8_t* buf = write_snap ? stg.acquire() : nullptr;
@@ -272,6 +307,7 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
       if (write_snap)
         stg.commit(buf, [&](uint8_t* src) { tma_store_3d(&p.tm_ss, src, n0 + g * 64, m0, slot); });
     }
+    rel();
   }
 };
 

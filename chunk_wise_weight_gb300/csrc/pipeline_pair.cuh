@@ -395,14 +395,19 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
         }
         tc_fence_after_sync();
         const uint32_t trow = tlane + uint32_t(h * kBN);
-        if constexpr (S::kStagedStores) {
+        // The unit's last segments keep their accumulators for the next
+        // unit's preload (kPreload); every other segment releases its own.
+        bool release = true;
+        if constexpr (S::kPreload) release = s < nseg - sched.unit_accs();
+        AccRelease rel{release ? acc_empty_leader[h] : 0u};
+        if constexpr (S::kStagedStores && S::kEarlyRelease) {
+          sched.epilogue(s, row, trow, stager, rel);
+        } else if constexpr (S::kStagedStores) {
           sched.epilogue(s, row, trow, stager);
         } else {
           sched.epilogue(s, row, trow);
         }
-        bool release = true;
         if constexpr (S::kPreload) {
-          release = s < nseg - sched.unit_accs();
           const int un = u + npairs;
           if (!release && un < nunits) {
             next.begin_unit(un, local + 1);
@@ -419,10 +424,7 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
             }
           }
         }
-        if (release) {
-          tc_fence_before_sync();
-          mbar_arrive_cluster(acc_empty_leader[h]);
-        }
+        rel();  // (a no-op if the epilogue released it already)
         ++acc_use[h];
       }
     }
