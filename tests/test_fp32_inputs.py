@@ -18,7 +18,8 @@ any input would show):
     values.
   * Regular batches, a ragged length with chunks that are not multiples of
     64 and widths that are not multiples of 64 (d = 200: a K block straddles
-    the hi/lo segments), packed documents, per-token rates and the dual form.
+    the hi/lo segments), packed documents, per-token rates, the dual form,
+    the normalised update, and two calls chained through the fp32 state.
 """
 import numpy as np
 import pytest
@@ -153,3 +154,54 @@ def test_fp32_inputs_plain_call_equals_export(cuda_device):
     ittt.stream_status()
     assert ittt.plan_form(B, T, d, f, C, fp32_inputs=True) == ittt.FORM_PRIMAL
     assert torch.equal(out.cpu().double(), torch.from_numpy(o_exp))
+
+
+@pytest.mark.gpu
+def test_fp32_inputs_l2_normalised_walk(cuda_device):
+    """fp32 inputs with the normalised update: O within the bar against the
+    oracle on the unrounded values, and closer than the same values rounded
+    to bf16 first."""
+    B, T, d, f, C, eta = 2, 1024, 256, 512, 128, 0.05
+    inp = make_inputs(B, T, d, f, seed=77, round_bf16=False)
+    want = oracle.forward(inp, eta, C, l2norm=True)["O"]
+    errs = []
+    for dt in (torch.float32, torch.bfloat16):
+        t = _dev(inp, cuda_device, dt)
+        out = ittt.forward(t["H"], t["X0"], t["W_gate"], t["W_up"], t["W_down0"], t["W_target"],
+                           t["conv_w"], eta, C, out_dtype=torch.float32, l2norm=True)
+        ittt.stream_status()
+        errs.append(_o_err(out.double().cpu().numpy(), want))
+    rel, mx = errs[0]
+    assert rel <= REL_FRO and mx <= MAX_RATIO, f"O: rel={rel:.3e} max={mx:.3e}"
+    assert rel < errs[1][0], (errs[0], errs[1])
+
+
+@pytest.mark.gpu
+def test_fp32_inputs_streaming_two_calls_equal_one(cuda_device):
+    """fp32 inputs across two calls chained through state_out / state_in (a
+    split at a chunk boundary): the final state matches the oracle, and O
+    equals the single call's bit for bit (the same products, splits and
+    walk)."""
+    B, T, d, f, C, eta = 2, 1024, 256, 512, 128, 0.03
+    inp = make_inputs(B, T, d, f, seed=78, round_bf16=False)
+    ref = oracle.forward(inp, eta, C, want_states=True)
+    t = _dev(inp, cuda_device, torch.float32)
+    half = T // 2
+
+    def call(H, X0, state_in=None):
+        state = torch.empty(B, d, f, dtype=torch.float32, device=cuda_device)
+        out = ittt.forward(H, X0, t["W_gate"], t["W_up"], t["W_down0"], t["W_target"],
+                           t["conv_w"], eta, C, out_dtype=torch.float32, state_in=state_in,
+                           state_out=state, primal=True)
+        return out, state
+
+    whole, s_whole = call(t["H"], t["X0"])
+    a, s_a = call(t["H"][:, :half].contiguous(), t["X0"][:, :half].contiguous())
+    b, s_b = call(t["H"][:, half:].contiguous(), t["X0"][:, half:].contiguous(), state_in=s_a)
+    ittt.stream_status()
+    assert torch.equal(torch.cat([a, b], dim=1), whole)
+    assert torch.equal(s_b, s_whole)
+    rel, mx = _o_err(s_b.double().cpu().numpy(), ref["states"][:, T // C])
+    assert rel <= REL_FRO and mx <= MAX_RATIO, f"final state: rel={rel:.3e} max={mx:.3e}"
+    rel, mx = _o_err(whole.double().cpu().numpy(), ref["O"])
+    assert rel <= REL_FRO and mx <= MAX_RATIO, f"O: rel={rel:.3e} max={mx:.3e}"
