@@ -310,6 +310,8 @@ struct Layout {
   size_t h3 = 0, wg3 = 0, wu3 = 0, wt3 = 0;
   size_t tickets = 0;  // the pair GEMMs' unit counters (zeroed by the call)
   bool has_tickets = false;
+  size_t apply_part = 0;  // fp32 partials of the apply's split last round
+  bool has_apply_part = false;
 };
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -523,6 +525,11 @@ ittt_status make_plan(int64_t B, int64_t T, int64_t d, int64_t f, int64_t chunk,
   // dynamically): every call that runs the primal apply.
   L.has_tickets = !P->update_only && !P->dual;
   if (L.has_tickets) L.tickets = take(ittt::kNumTickets * sizeof(unsigned int));
+  // Partials for splitting the apply's partial last round, where it can have
+  // one: at least two full rounds of its 256 x 256 units on the GPU's pairs.
+  const int64_t apply_pair_units = P->ntiles2 * ((d + 255) / 256);
+  L.has_apply_part = L.has_tickets && apply_pair_units >= 2 * ittt::kMaxApplyTailPieces;
+  if (L.has_apply_part) L.apply_part = take(ittt::kApplyPartBytes);
   if (o.z_buf == nullptr) L.z = take(size_t(P->M) * f * 2);
   if (o.vhat_buf == nullptr) L.vhat = take(size_t(P->M) * d * 2);
   if (!P->fused && !P->reuse) L.xc = take(size_t(P->M) * d * 2 * (P->fp32_in ? 3 : 1));
@@ -809,7 +816,8 @@ ittt_status forward_impl(const ittt_tensor* H, const ittt_tensor* X0, const ittt
   }
 
   auto* tickets = L.has_tickets ? reinterpret_cast<unsigned int*>(ws + L.tickets) : nullptr;
-  const ittt::LaunchEnv env{stream, ds->num_sms, ds->status, tickets};
+  ittt::LaunchEnv env{stream, ds->num_sms, ds->status, tickets};
+  if (L.has_apply_part) env.apply_part = reinterpret_cast<float*>(ws + L.apply_part);
   // w0 == nullptr: the walk starts from zero (folding chunks only).
   const void* w0 = o.state_in ? o.state_in->data : (zero_start ? nullptr : W_down0->data);
   const bool w0_fp32 = o.state_in ? true : (!zero_start && W_down0->dtype == ITTT_FP32);

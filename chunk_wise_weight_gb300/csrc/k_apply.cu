@@ -33,6 +33,12 @@ struct ApplyParams {
   int d, f;
   int nt, kblocks;
   unsigned int* ticket;  // the pair kernel's unit counter (LaunchEnv::tickets)
+  // CTA pairs: units [0, nfull) whole; each later unit (the partial last
+  // round) as ksplit pieces over consecutive K ranges, whose fp32 partials
+  // go to part and whose arrivals count in tail_ctr.
+  int nfull, ksplit;
+  float* part;
+  unsigned int* tail_ctr;
 };
 
 // bf16 O in whole 64-row halves: 64-column TMA stores (columns >= d are
@@ -166,15 +172,30 @@ struct ApplyPairSched : PairDefaults {
   const Params& p;
   const int rank;
   int arow0 = 0, brow0 = 0, rows_valid = 0, n0 = 0, acc = 0;
+  int kb0 = 0, nkb = 0, piece = -1, tail = 0;  // K range; piece of a tail unit (-1: whole)
   const CUtensorMap* bmap = nullptr;
 
   __device__ ApplyPairSched(const Params& pp, uint32_t r) : p(pp), rank(int(r)) {}
   __device__ unsigned int* unit_ticket() const { return p.ticket; }
-  __device__ int num_units() const { return p.docs.ntiles2 * p.nt; }
+  __device__ int num_units() const {
+    return p.nfull + (p.docs.ntiles2 * p.nt - p.nfull) * p.ksplit;
+  }
   __device__ void begin_unit(int u, int local) {
-    const int nt = u % p.nt;
+    int w = u;
+    piece = -1;
+    kb0 = 0;
+    nkb = p.kblocks;
+    if (u >= p.nfull) {
+      const int q = u - p.nfull;
+      tail = q / p.ksplit;
+      piece = q - tail * p.ksplit;
+      w = p.nfull + tail;
+      kb0 = piece * p.kblocks / p.ksplit;
+      nkb = (piece + 1) * p.kblocks / p.ksplit - kb0;
+    }
+    const int nt = w % p.nt;
     int mt = 0;
-    const int g = p.docs.slot_of_tile(u / p.nt, &mt, true);
+    const int g = p.docs.slot_of_tile(w / p.nt, &mt, true);
     const int k = p.docs.doc_of_chunk(g);
     const int i = g - p.docs.first_chunk(k);
     const int len = p.docs.len(k);
@@ -189,10 +210,10 @@ struct ApplyPairSched : PairDefaults {
   }
   __device__ int num_segments() const { return 1; }
   __device__ int seg_acc(int) const { return acc; }
-  __device__ int seg_kblocks(int) const { return p.kblocks; }
+  __device__ int seg_kblocks(int) const { return nkb; }
   __device__ bool seg_fresh(int) const { return true; }
   __device__ void load(int, int kb, uint8_t* stage, uint32_t bar) const {
-    const int k = kb * kBK;
+    const int k = (kb0 + kb) * kBK;
     tma_load_2d_pair(stage, &p.tm_z, bar, k, arow0);
     tma_load_2d_pair(stage + kPairATileBytes, bmap, bar, k, brow0);
   }
@@ -205,7 +226,87 @@ struct ApplyPairSched : PairDefaults {
   // The second half of a tile may lie past its chunk (rows_valid <= 0):
   // computed, nothing stored.
   __device__ void epilogue(int, int row, uint32_t trow, EpiStager& st) const {
+    if (piece >= 0 && !sum_pieces(row, trow, st)) return;
     apply_epilogue(p, arow0, rows_valid, n0, row, trow, st);
+  }
+
+  // A piece of a split unit: publish this CTA's fp32 partial (its 128 rows),
+  // count the arrival, and -- in the CTA that completes the count -- add the
+  // pieces' partials in piece order into TMEM (true: the caller stores the
+  // sum as the unit's output).  Nobody waits for another CTA here.
+  __device__ bool sum_pieces(int row, uint32_t trow, EpiStager& st) const {
+    // A piece's partial (both CTAs, 2 x 128 rows x 256 columns) is stored
+    // column-group-major: [64 groups of 4 columns][128 rows][4], so a warp's
+    // 16-byte accesses to one group cover 512 contiguous bytes.
+    const size_t tile = size_t(2 * kBM) * kBN;
+    float4* base = reinterpret_cast<float4*>(p.part + size_t(tail) * p.ksplit * tile +
+                                             size_t(rank) * kBM * kBN) + row;
+    float4* mine = base + size_t(piece) * (tile / 4);
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 32) {
+      uint32_t v[32];
+      tmem_ld_32cols(trow + uint32_t(c), v);
+      tmem_wait_ld();
+      pin_regs(v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        __stcg(mine + size_t(c / 4 + q) * kBM,
+               make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+    }
+    __threadfence();  // this row's partial before the arrival below
+    // A staging buffer (not stored from) carries the verdict to every row.
+    volatile int* flag = reinterpret_cast<volatile int*>(st.acquire());
+    if (row == 0)
+      *flag = atomicAdd(p.tail_ctr + 2 * tail + rank, 1u) == unsigned(p.ksplit - 1) ? 1 : 0;
+    epilogue_group_bar(st.group);
+    const bool last = *flag != 0;
+    epilogue_group_bar(st.group);
+    if (!last) return false;
+    __threadfence();  // the other pieces' partials after their arrivals
+    // 32 columns per step: every other piece's loads are issued before the
+    // sum, which then adds the pieces in order.
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 32) {
+      float4 x[4][8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (q < p.ksplit && q != piece) {
+          const float4* src = base + size_t(q) * (tile / 4) + size_t(c / 4) * kBM;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) x[q][j] = __ldcg(src + size_t(j) * kBM);
+        }
+      }
+      uint32_t v[32];
+      tmem_ld_32cols(trow + uint32_t(c), v);
+      tmem_wait_ld();
+      pin_regs(v);
+      float sum[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) sum[j] = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (q < p.ksplit) {
+          if (q == piece) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sum[j] += __uint_as_float(v[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              sum[4 * j] += x[q][j].x;
+              sum[4 * j + 1] += x[q][j].y;
+              sum[4 * j + 2] += x[q][j].z;
+              sum[4 * j + 3] += x[q][j].w;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(sum[j]);
+      tmem_st_32cols(trow + uint32_t(c), v);
+    }
+    tmem_wait_st();
+    return true;
   }
 };
 
@@ -247,7 +348,29 @@ cudaError_t launch_apply_pair(const LaunchEnv& env, const CUtensorMap& tm_z,
                      &resident)) != cudaSuccess)
     return e;
   if (pairs < 1) return cudaErrorNotSupported;
-  if (units < pairs) pairs = int(units);
+  // A partial last round of t units (after at least two full rounds) runs
+  // each unit as S pieces over disjoint K ranges, S <= 4 and t S <= pairs,
+  // so that round takes about 1/S of a unit's MMAs plus the partials' round
+  // trip (1 x 8192 tokens: 320 units on 76 pairs, t = 16, S = 4; the apply
+  // 247.6 -> 228.4 us in a per-unit trace).
+  p.nfull = int(units);
+  p.ksplit = 1;
+  p.part = nullptr;
+  p.tail_ctr = nullptr;
+  const int64_t t = units % pairs;
+  if (env.apply_part != nullptr && units >= 2 * int64_t(pairs) && t > 0 && 2 * t <= pairs) {
+    int S = int(pairs / t);
+    S = S < 4 ? S : 4;
+    S = S < p.kblocks ? S : p.kblocks;
+    if (S >= 2 && t * S <= kMaxApplyTailPieces) {
+      p.nfull = int(units - t);
+      p.ksplit = S;
+      p.part = env.apply_part;
+      p.tail_ctr = env.tickets + kTicketApplyTail;
+    }
+  }
+  const int64_t total = p.nfull + (units - p.nfull) * p.ksplit;
+  if (total < pairs) pairs = int(total);
   return launch_on_pairs(reinterpret_cast<const void*>(apply_pair_kernel), pairs, smem, env, &p);
 }
 
@@ -255,7 +378,11 @@ cudaError_t launch_apply(const LaunchEnv& env, const CUtensorMap& tm_z, const CU
                          const CUtensorMap* tm_w0, const CUtensorMap& tm_os, void* out,
                          bool out_fp32, const DocMap& docs, int d, int f) {
   ApplyParams p;
-  p.ticket = nullptr;  // one CTA per SM: fixed stride
+  p.ticket = nullptr;  // one CTA per SM: fixed stride, no split round
+  p.nfull = 0;
+  p.ksplit = 1;
+  p.part = nullptr;
+  p.tail_ctr = nullptr;
   p.tm_z = tm_z;
   p.tm_snap = tm_snap;
   p.w0_direct = tm_w0 != nullptr ? 1 : 0;

@@ -37,12 +37,25 @@ struct LaunchEnv {
   cudaStream_t stream;
   int num_sms;
   unsigned int* status;  // device status word (kStatusTimeout bits)
-  // kNumTickets unit counters in device memory, zero before the call's first
-  // kernel: a pair GEMM that takes its units dynamically (the apply) draws
-  // from its own.
+  // kNumTickets counters in device memory, zero before the call's first
+  // kernel: the apply's unit counter (it takes its units dynamically) and
+  // the arrival counters of its split last round.
   unsigned int* tickets = nullptr;
+  // kApplyPartBytes of fp32 scratch for the partial sums of the apply's
+  // split last round, or nullptr (the round is then not split).
+  float* apply_part = nullptr;
 };
-enum TicketSlot : int { kTicketApply = 0, kNumTickets = 4 };
+// The apply's partial last round of t units on P CTA pairs (2t <= P) may run
+// each unit as up to four pieces over disjoint K ranges; a piece's CTA writes
+// its 128 x 256 fp32 partial, and the last of the pieces adds them.
+constexpr int kMaxApplyTailPieces = 76;  // t x pieces <= P <= 76 pairs (152 SMs)
+constexpr size_t kApplyPieceBytes = size_t(2) * 128 * 256 * 4;  // both CTAs' partials
+constexpr size_t kApplyPartBytes = size_t(kMaxApplyTailPieces) * kApplyPieceBytes;
+enum TicketSlot : int {
+  kTicketApply = 0,
+  kTicketApplyTail = 4,  // one counter per (tail unit, CTA of the pair)
+  kNumTickets = kTicketApplyTail + 2 * kMaxApplyTailPieces
+};
 
 // The documents along the packed token axis, each with its own fast-weight
 // state that starts from W_0 (the state is reset at document boundaries:

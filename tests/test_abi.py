@@ -204,7 +204,7 @@ def test_workspace_bytes_and_launch_count(lib):
         return (x + 255) // 256 * 256
     B, T, d, f, C = 2, 1024, 320, 1000, 256
     n = T // C
-    tk = 256   # the apply's unit counter block (four 4-byte counters, rounded up)
+    tk = 768   # the apply's counters: its unit counter (4 slots) and 152 tail counters
     want = tk + r(B * T * f * 2) + 2 * r(B * T * d * 2) + r(B * n * d * f * 2)
     assert ittt.workspace_bytes(B, T, d, f, C) == want
     assert ittt.workspace_bytes_ex(B, T, d, f, C) == want
@@ -250,6 +250,16 @@ def test_workspace_bytes_and_launch_count(lib):
                                     z_buf=fake_z, vhat_buf=fake_z)
             == ittt.workspace_bytes_ex(B, T, d, f, C, reuse_zv=True, z_buf=fake_z,
                                        vhat_buf=fake_z))
+    # the apply's split last round: fp32 partials for up to 76 pieces of
+    # 256 x 256 tiles, planned when the apply has at least two rounds of
+    # units on 76 CTA pairs: 8 sequences x 4 chunks of 256 rows x 5 column
+    # tiles (d 1280) = 160 units; half the sequences, 80 units: none
+    def plain(Bq, Tq, dq, fq, Cq):
+        return (tk + r(Bq * Tq * fq * 2) + 2 * r(Bq * Tq * dq * 2)
+                + r(Bq * (Tq // Cq) * dq * fq * 2))
+    assert (ittt.workspace_bytes(8, 1024, 1280, 512, 256)
+            == plain(8, 1024, 1280, 512, 256) + r(76 * 2 * 128 * 256 * 4))
+    assert ittt.workspace_bytes(4, 1024, 1280, 512, 256) == plain(4, 1024, 1280, 512, 256)
     assert ittt.launch_count(B, T, d, f, C) == 5
     assert ittt.launch_count(B, T, d, f, T) == 4
     assert ittt.launch_count(B, 1000, d, f, 512) == 5   # two chunks, the last partial
@@ -339,7 +349,7 @@ def test_update_only_and_reuse_scratch():
     B, T, d, f, C = 2, 1024, 320, 1000, 256
     n = T // C
     z, vh, xc, snap = r(B * T * f * 2), r(B * T * d * 2), r(B * T * d * 2), r(B * n * d * f * 2)
-    tk = 256   # the apply's unit counters (none when the call applies nothing)
+    tk = 768   # the apply's counters (none when the call applies nothing)
     fake = torch.empty(0)
     # folding chunks only forms no snapshots
     assert (ittt.workspace_bytes_ex(B, T, d, f, C, update_only=True, state_out=fake)

@@ -265,6 +265,40 @@ def test_single_cta_kernels(cuda_device, B, T, d, f, C, eta):
         assert torch.equal(one[k], pair[k]), k
 
 
+def test_apply_split_last_round(cuda_device):
+    """The apply on CTA pairs runs a partial last round of t units (after at
+    least two full rounds, 2t <= 76 pairs) as pieces over disjoint K ranges
+    whose fp32 partials the last piece adds in piece order.  Here 160
+    units (one 256-row tile per 256-token chunk, d = 256): the last 8 units
+    (chunks 152..159) run as 4 pieces each.  Everything outside those chunks
+    is bit-identical to the single-CTA path; inside, O differs from it only
+    by the fp32 rounding of the other summation order, and the whole output
+    is within the bar of the oracle."""
+    B, T, d, f, C, eta = 1, 160 * 256, 256, 1024, 256, 0.02
+    inp = make_inputs(B, T, d, f, seed=1777)
+    ref = oracle.forward(inp, eta, C)
+    g = to_device(inp, cuda_device)
+    assert ittt.plan_form(B, T, d, f, C) == ittt.FORM_PRIMAL
+    pair = run(g, eta, C)
+    one = run(g, eta, C, single_cta=True)
+    assert_parity(host(pair["O"]), ref["O"], "O (split last round)")
+    split0 = 152 * 256
+    assert torch.equal(pair["O"][:, :split0], one["O"][:, :split0])
+    # Inside: the same products summed in another fp32 order, so the bf16
+    # results differ by at most one unit in the last place -- where O is
+    # not much smaller than its terms (elsewhere by an fp32 rounding of
+    # the terms' scale, 2^-14 of max |O| bounds it here).
+    a = pair["O"][:, split0:].double()
+    b = one["O"][:, split0:].double()
+    ulp = torch.exp2(torch.floor(torch.log2(b.abs().clamp_min(1e-30))) - 7)
+    bound = ulp + 2.0 ** -14 * b.abs().max()
+    err = (a - b).abs() - bound
+    worst = int(torch.argmax(err))
+    assert bool((err <= 0).all()), (
+        f"split tiles: element {worst} pair {a.flatten()[worst].item()!r} "
+        f"single {b.flatten()[worst].item()!r}")
+
+
 # --------------------------------------------------------------------------
 # Chunks and lengths that are not multiples of 64: the update masks the
 # token lines past a chunk's end, the apply stores ragged tiles row by row
