@@ -130,7 +130,9 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
   static constexpr bool kPreload = true;
   static constexpr bool kStagedStores = true;
   static constexpr bool kRaggedK = !kPair;
+  static constexpr bool kStagedPreload = true;  // W_0 read coalesced through a staging tile
   static constexpr bool kEarlyRelease = kPair;
+  static constexpr bool kPrefetchPreload = kPair;
 
   const Params& p;
   const int rank;
@@ -202,24 +204,81 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
   static __device__ uint64_t a_desc(uint32_t base, int k) { return mn_desc(base, k); }
   static __device__ uint64_t b_desc(uint32_t base, int k) { return mn_desc(base, k); }
 
-  // W_0 rows of half h into its accumulator (zeros outside the state).
-  __device__ void preload(int h, int row, uint32_t trow) const {
+  // This unit's W_0 rows (what preload reads) into L2, a unit ahead: the
+  // preload at the unit boundary then reads from L2, not DRAM.
+  __device__ void prefetch_preload(int row) const {
     const int m = m0 + row;
-    const bool row_ok = m < p.d;
+    if (p.w0 == nullptr || m >= p.d) return;
+    const size_t es = p.w0_fp32 ? 4 : 2;
+    const char* base = static_cast<const char*>(p.w0) +
+                       (size_t(doc) * size_t(p.w0_bstride) + size_t(m) * size_t(p.f)) * es;
+    for (int h = 0; h < nh; ++h) {
+      const int ncols = min(kBN, p.f - hn0[h]);
+      for (size_t b = 0; b < size_t(ncols) * es; b += 128) prefetch_l2(base + size_t(hn0[h]) * es + b);
+    }
+  }
+
+  // W_0 rows of half h into its accumulator (zeros outside the state).  A
+  // unit's first chunk waits for this, so the rows are read coalesced: per
+  // pass, the 128 threads load the block's 128 rows x 128 bytes (four rows
+  // per warp instruction) into a staging tile, and each thread then takes
+  // its own row from shared memory into TMEM.  (One thread per row, each
+  // warp load touching 32 rows of W_0, took ~11 us a preload and held up
+  // every unit's first chunks.)
+  __device__ void preload(int h, int row, uint32_t trow, EpiStager& st) const {
     const int n0 = h ? hn0[1] : hn0[0];
-    const size_t off = size_t(doc) * size_t(p.w0_bstride) + size_t(row_ok ? m : 0) * size_t(p.f);
+    const bool f32 = p.w0_fp32 != 0;
+    const size_t es = f32 ? 4 : 2;
+    const int cols = int(128 / es);  // columns per pass: 64 bf16 or 32 fp32
+    const char* w0 = static_cast<const char*>(p.w0);
+    const size_t doc_off = size_t(doc) * size_t(p.w0_bstride);
 #pragma unroll 1
-    for (int c = 0; c < kBN; c += 32) {
-      uint32_t v[32];
+    for (int c0 = 0; c0 < kBN; c0 += cols) {
+      uint8_t* buf = st.acquire();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int col = n0 + c + 8 * q;
-        float w[8];
-        load_w0_8(p.w0, p.w0_fp32 != 0, off + col, row_ok && col < p.f, w);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[8 * q + j] = __float_as_uint(w[j]);
+      for (int i = 0; i < 8; ++i) {
+        const int idx = i * kEpilogueThreads + row;  // 16-byte piece of the tile
+        const int r = idx >> 3, ch = idx & 7;
+        const int m = m0 + r;
+        const int col = n0 + c0 + ch * int(16 / es);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (w0 != nullptr && m < p.d && col < p.f)
+          v = __ldg(reinterpret_cast<const uint4*>(w0 + (doc_off + size_t(m) * p.f + col) * es));
+        *reinterpret_cast<uint4*>(buf + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
       }
-      tmem_st_32cols(trow + uint32_t(c), v);
+      epilogue_group_bar(st.group);
+      const uint8_t* mine = buf + row * 128;
+      if (f32) {
+        uint32_t v[32];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 x = *reinterpret_cast<const uint4*>(mine + ((ch ^ (row & 7)) << 4));
+          v[4 * ch] = x.x;
+          v[4 * ch + 1] = x.y;
+          v[4 * ch + 2] = x.z;
+          v[4 * ch + 3] = x.w;
+        }
+        tmem_st_32cols(trow + uint32_t(c0), v);
+      } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int ch = 4 * half + k;
+            const uint4 x = *reinterpret_cast<const uint4*>(mine + ((ch ^ (row & 7)) << 4));
+            const uint32_t r4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float2 f2 = unpack_bf16x2(r4[j]);
+              v[8 * k + 2 * j] = __float_as_uint(f2.x);
+              v[8 * k + 2 * j + 1] = __float_as_uint(f2.y);
+            }
+          }
+          tmem_st_32cols(trow + uint32_t(c0 + 32 * half), v);
+        }
+      }
+      epilogue_group_bar(st.group);  // every row taken before the next pass refills the tile
     }
   }
 
@@ -228,15 +287,19 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
   // >= f are not written) and, after the last update, the fp32 state when
   // the caller wants it (direct stores).
   __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& stg) const {
-    AccRelease none{0u};
-    epilogue(s, row, trow, stg, none);
+    epilogue(s, row, trow, stg, [] {});
   }
-  // On CTA pairs the epilogue releases the accumulator itself: a snapshot
-  // row is read whole from TMEM into registers (as bf16 pairs) first, so the
-  // next chunk's MMAs into this accumulator start while it is staged and
-  // stored.  (Behind the other half's MMAs that wait was hidden; a unit
-  // walking a single half waited for the whole epilogue at every chunk.)
-  __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& stg, AccRelease& rel) const {
+  // On CTA pairs the epilogue hands the accumulator on itself: a snapshot
+  // row is read whole from TMEM into registers (as bf16 pairs) first, then
+  // `handoff` releases the accumulator -- or, after a unit's last chunk,
+  // preloads the next unit's W_0 into it and releases it -- so the next MMAs
+  // into it start while the snapshot is staged and stored.  (Behind the
+  // other half's MMAs that wait was hidden between chunks; a unit walking a
+  // single half waited for the whole epilogue at every chunk, and every
+  // unit's first chunks for the last snapshot's stores and the preload.)
+  template <class Handoff>
+  __device__ void epilogue(int s, int row, uint32_t trow, EpiStager& stg,
+                           Handoff&& handoff) const {
     const int i = seg_chunk(s);
     const int h = s - i * nh;
     const int m = m0 + row;
@@ -259,7 +322,7 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
         for (int j = 0; j < 16; ++j)
           pk[c / 2 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
       }
-      rel();
+      handoff();
 #pragma unroll
       for (int g = 0; g < kBN / 64; ++g) {
         uint8_t* buf = stg.acquire();
@@ -307,7 +370,7 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
       if (write_snap)
         stg.commit(buf, [&](uint8_t* src) { tma_store_3d(&p.tm_ss, src, n0 + g * 64, m0, slot); });
     }
-    rel();
+    handoff();
   }
 };
 

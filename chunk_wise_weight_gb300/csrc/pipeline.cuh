@@ -109,23 +109,6 @@ struct EpiStager {
   }
 };
 
-// Release of an accumulator by the epilogue itself (kEarlyRelease): the
-// epilogue calls it once its last TMEM read has completed, so the next MMAs
-// into the accumulator can start while it still converts and stores.  Calls
-// after the first do nothing; bar == 0: the accumulator is not the
-// epilogue's to release (the pipeline preloads it instead).
-struct AccRelease {
-  uint32_t bar;
-  bool done = false;
-  __device__ __forceinline__ void operator()() {
-    if (bar != 0u && !done) {
-      tc_fence_before_sync();
-      mbar_arrive_cluster(bar);
-      done = true;
-    }
-  }
-};
-
 struct SchedDefaults {
   static constexpr int kNumStages = 4;
   static constexpr uint32_t kExtraStageBytes = 0;
@@ -175,10 +158,17 @@ struct SchedDefaults {
   // units in flight stay within about one round of each other.
   static constexpr bool kDynamicUnits = false;
   // With kEarlyRelease (CTA-pair pipeline, kStagedStores) the epilogue gets
-  // the accumulator's release and calls it after its last TMEM read:
-  //   void epilogue(int s, int row, uint32_t tmem_row_base, EpiStager& st,
-  //                 AccRelease& release)
+  // a callable to invoke once its last TMEM read has completed; it hands the
+  // accumulator on (releases it, or preloads the next unit's initial state
+  // into it and releases it), so the next MMAs can start while the epilogue
+  // still converts and stores:
+  //   template <class F> void epilogue(int s, int row, uint32_t tmem_row_base,
+  //                                    EpiStager& st, F&& handoff)
   static constexpr bool kEarlyRelease = false;
+  // With kPrefetchPreload (CTA-pair pipeline, kPreload, fixed stride) the
+  // epilogue asks the next unit's schedule, as each unit starts, to pull
+  // what its preload will read into L2:   void prefetch_preload(int row)
+  static constexpr bool kPrefetchPreload = false;
 };
 
 template <class S>

@@ -365,6 +365,13 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
       if (u < 0) break;
       sched.begin_unit(u, local);
       const int nseg = sched.num_segments();
+      if constexpr (S::kPrefetchPreload) {
+        static_assert(S::kPreload && !S::kDynamicUnits, "prefetches the next stride unit");
+        if (u + npairs < nunits) {
+          next.begin_unit(u + npairs, local + 1);
+          next.prefetch_preload(row);
+        }
+      }
       if constexpr (S::kPreload) {
         for (int h = 0; h < sched.unit_accs(); ++h) {
           if (!preloaded[h] && (!S::kAccTeams || h == group)) {
@@ -397,34 +404,45 @@ __device__ __forceinline__ void run_pipeline_pair(const typename S::Params& p,
         const uint32_t trow = tlane + uint32_t(h * kBN);
         // The unit's last segments keep their accumulators for the next
         // unit's preload (kPreload); every other segment releases its own.
+        // The hand-off runs once: called by a kEarlyRelease epilogue after
+        // its last TMEM read, else here after the epilogue.
         bool release = true;
         if constexpr (S::kPreload) release = s < nseg - sched.unit_accs();
-        AccRelease rel{release ? acc_empty_leader[h] : 0u};
+        bool handed = false;
+        auto handoff = [&]() {
+          if (handed) return;
+          handed = true;
+          if (release) {
+            tc_fence_before_sync();
+            mbar_arrive_cluster(acc_empty_leader[h]);
+            return;
+          }
+          if constexpr (S::kPreload) {
+            const int un = u + npairs;
+            if (un < nunits) {
+              next.begin_unit(un, local + 1);
+              if (h < next.unit_accs()) {
+                if constexpr (S::kStagedPreload) {
+                  next.preload(h, row, trow, stager);
+                } else {
+                  next.preload(h, row, trow);
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                mbar_arrive_cluster(acc_empty_leader[h]);
+                preloaded[h] = true;
+              }
+            }
+          }
+        };
         if constexpr (S::kStagedStores && S::kEarlyRelease) {
-          sched.epilogue(s, row, trow, stager, rel);
+          sched.epilogue(s, row, trow, stager, handoff);
         } else if constexpr (S::kStagedStores) {
           sched.epilogue(s, row, trow, stager);
         } else {
           sched.epilogue(s, row, trow);
         }
-        if constexpr (S::kPreload) {
-          const int un = u + npairs;
-          if (!release && un < nunits) {
-            next.begin_unit(un, local + 1);
-            if (h < next.unit_accs()) {
-              if constexpr (S::kStagedPreload) {
-                next.preload(h, row, trow, stager);
-              } else {
-                next.preload(h, row, trow);
-              }
-              tmem_wait_st();
-              tc_fence_before_sync();
-              mbar_arrive_cluster(acc_empty_leader[h]);
-              preloaded[h] = true;
-            }
-          }
-        }
-        rel();  // (a no-op if the epilogue released it already)
+        handoff();
         ++acc_use[h];
       }
     }

@@ -445,6 +445,11 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return pol;
 }
 
+// Pulls the 128-byte line holding `p` into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // 16-byte global store carrying an L2 cache policy.
 __device__ __forceinline__ void st_global_v4_hint(void* ptr, uint4 v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x),
