@@ -123,6 +123,70 @@ struct UpdateParams {
 // d_model rows: each CTA keeps its 128 rows of eta*Vhat^T and 128 of the
 // half's 256 Z columns in shared memory, and its 128 state rows of both
 // halves in its own TMEM.
+// W_0 (bf16 or fp32, rows of f elements, the document's at doc_off) rows
+// [m0, m0 + 128) x columns [n0, n0 + 256) into this epilogue group's TMEM
+// rows (zeros outside [d, f], or everywhere without W_0).  The rows are
+// read coalesced: per pass the group's 128 threads load the block's 128
+// rows x 128 bytes (four rows per warp instruction) into a staging tile,
+// then each thread takes its own row from shared memory into TMEM.  (One
+// thread per row, each warp load touching 32 rows, took ~11 us and held up
+// the first chunks of every unit.)
+__device__ __forceinline__ void preload_w0_staged(const void* w0v, bool f32, size_t doc_off,
+                                                  int m0, int n0, int d, int f, int row,
+                                                  uint32_t trow, EpiStager& st) {
+  const size_t es = f32 ? 4 : 2;
+  const int cols = int(128 / es);  // columns per pass: 64 bf16 or 32 fp32
+  const char* w0 = static_cast<const char*>(w0v);
+#pragma unroll 1
+  for (int c0 = 0; c0 < kBN; c0 += cols) {
+    uint8_t* buf = st.acquire();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = i * kEpilogueThreads + row;  // 16-byte piece of the tile
+      const int r = idx >> 3, ch = idx & 7;
+      const int m = m0 + r;
+      const int col = n0 + c0 + ch * int(16 / es);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (w0 != nullptr && m < d && col < f)
+        v = __ldg(reinterpret_cast<const uint4*>(w0 + (doc_off + size_t(m) * f + col) * es));
+      *reinterpret_cast<uint4*>(buf + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
+    }
+    epilogue_group_bar(st.group);
+    const uint8_t* mine = buf + row * 128;
+    if (f32) {
+      uint32_t v[32];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 x = *reinterpret_cast<const uint4*>(mine + ((ch ^ (row & 7)) << 4));
+        v[4 * ch] = x.x;
+        v[4 * ch + 1] = x.y;
+        v[4 * ch + 2] = x.z;
+        v[4 * ch + 3] = x.w;
+      }
+      tmem_st_32cols(trow + uint32_t(c0), v);
+    } else {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ch = 4 * half + k;
+          const uint4 x = *reinterpret_cast<const uint4*>(mine + ((ch ^ (row & 7)) << 4));
+          const uint32_t r4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f2 = unpack_bf16x2(r4[j]);
+            v[8 * k + 2 * j] = __float_as_uint(f2.x);
+            v[8 * k + 2 * j + 1] = __float_as_uint(f2.y);
+          }
+        }
+        tmem_st_32cols(trow + uint32_t(c0 + 32 * half), v);
+      }
+    }
+    epilogue_group_bar(st.group);  // every row taken before the next pass refills the tile
+  }
+}
+
 template <bool kPair>
 struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
   using Params = UpdateParams;
@@ -218,68 +282,11 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
     }
   }
 
-  // W_0 rows of half h into its accumulator (zeros outside the state).  A
-  // unit's first chunk waits for this, so the rows are read coalesced: per
-  // pass, the 128 threads load the block's 128 rows x 128 bytes (four rows
-  // per warp instruction) into a staging tile, and each thread then takes
-  // its own row from shared memory into TMEM.  (One thread per row, each
-  // warp load touching 32 rows of W_0, took ~11 us a preload and held up
-  // every unit's first chunks.)
+  // W_0 rows of half h into its accumulator (zeros outside the state): a
+  // unit's first chunk waits for this (see preload_w0_staged).
   __device__ void preload(int h, int row, uint32_t trow, EpiStager& st) const {
-    const int n0 = h ? hn0[1] : hn0[0];
-    const bool f32 = p.w0_fp32 != 0;
-    const size_t es = f32 ? 4 : 2;
-    const int cols = int(128 / es);  // columns per pass: 64 bf16 or 32 fp32
-    const char* w0 = static_cast<const char*>(p.w0);
-    const size_t doc_off = size_t(doc) * size_t(p.w0_bstride);
-#pragma unroll 1
-    for (int c0 = 0; c0 < kBN; c0 += cols) {
-      uint8_t* buf = st.acquire();
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int idx = i * kEpilogueThreads + row;  // 16-byte piece of the tile
-        const int r = idx >> 3, ch = idx & 7;
-        const int m = m0 + r;
-        const int col = n0 + c0 + ch * int(16 / es);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (w0 != nullptr && m < p.d && col < p.f)
-          v = __ldg(reinterpret_cast<const uint4*>(w0 + (doc_off + size_t(m) * p.f + col) * es));
-        *reinterpret_cast<uint4*>(buf + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
-      }
-      epilogue_group_bar(st.group);
-      const uint8_t* mine = buf + row * 128;
-      if (f32) {
-        uint32_t v[32];
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 x = *reinterpret_cast<const uint4*>(mine + ((ch ^ (row & 7)) << 4));
-          v[4 * ch] = x.x;
-          v[4 * ch + 1] = x.y;
-          v[4 * ch + 2] = x.z;
-          v[4 * ch + 3] = x.w;
-        }
-        tmem_st_32cols(trow + uint32_t(c0), v);
-      } else {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t v[32];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int ch = 4 * half + k;
-            const uint4 x = *reinterpret_cast<const uint4*>(mine + ((ch ^ (row & 7)) << 4));
-            const uint32_t r4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 f2 = unpack_bf16x2(r4[j]);
-              v[8 * k + 2 * j] = __float_as_uint(f2.x);
-              v[8 * k + 2 * j + 1] = __float_as_uint(f2.y);
-            }
-          }
-          tmem_st_32cols(trow + uint32_t(c0 + 32 * half), v);
-        }
-      }
-      epilogue_group_bar(st.group);  // every row taken before the next pass refills the tile
-    }
+    preload_w0_staged(p.w0, p.w0_fp32 != 0, size_t(doc) * size_t(p.w0_bstride), m0,
+                      h ? hn0[1] : hn0[0], p.d, p.f, row, trow, st);
   }
 
   // State after chunk i of this half: snapshot W_{i+1} (bf16, four 64-column
@@ -804,25 +811,11 @@ struct NormWalkSched : PairDefaults {
   static __device__ uint64_t a_desc(uint32_t base, int k) { return mn_desc(base, k); }
   static __device__ uint64_t b_desc(uint32_t base, int k) { return mn_desc(base, k); }
 
-  // W_0 (as given, not normalised) into accumulator h: this row's 256
-  // columns (the group that owns the accumulator).
-  __device__ void preload(int h, int row, uint32_t trow, EpiStager&) const {
-    const int m = row0_of(h) + row;
-    const int n0 = fb * kBN;
-    const size_t off = size_t(doc_of(h)) * size_t(p.w0_bstride) + size_t(m) * size_t(p.f);
-#pragma unroll 1
-    for (int c = 0; c < kBN; c += 32) {
-      uint32_t v[32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int col = n0 + c + 8 * q;
-        float w[8];
-        load_w0_8(p.w0, p.w0_fp32 != 0, off + col, col < p.f, w);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[8 * q + j] = __float_as_uint(w[j]);
-      }
-      tmem_st_32cols(trow + uint32_t(c), v);
-    }
+  // W_0 (as given, not normalised) into accumulator h: these rows' 256
+  // columns (the group that owns the accumulator; see preload_w0_staged).
+  __device__ void preload(int h, int row, uint32_t trow, EpiStager& st) const {
+    preload_w0_staged(p.w0, p.w0_fp32 != 0, size_t(doc_of(h)) * size_t(p.w0_bstride),
+                      row0_of(h), fb * kBN, p.d, p.f, row, trow, st);
   }
 
   // Publish, exchange within the group, normalise (see above); run by the
