@@ -66,3 +66,41 @@ def test_bench_form_rule_matches_the_library():
             if form < 0:
                 continue  # the library rejects the call (e.g. a forced dual form)
             assert bench.dual_form(cfg, args) == (form == ittt.FORM_DUAL), (cfg, flags)
+
+
+def test_roofline_peak_follows_the_power_state():
+    """A tensor-bound kernel is held to the measured sustained peak when the
+    timed region's clock record shows the power cap active, else to the
+    burst peak (no clock record: burst)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks = {"bf16_tflops": 1925.7, "bf16_tflops_sustained": 1714.9}
+    peak, kind = bench.tensor_peak(peaks, "measured", {"reasons": ["sw_power_cap"]})
+    assert peak == 1714.9 and "sustained" in kind and "sw_power_cap" in kind
+    for clocks in ({"reasons": []}, {"reasons": None}, None, {}):
+        peak, kind = bench.tensor_peak(peaks, "measured", clocks)
+        assert peak == 1925.7 and "burst" in kind
+
+
+def test_fp32_input_accounting():
+    """fp32 inputs add the four hi/lo split launches per step, triple the
+    gate/up and target contractions in the phase model and move 10 bytes per
+    split element; the tiny workload runs them by default."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    for B, T, C in ((2, 32768, 2048), (1, 256, 64)):
+        assert (bench.launches_per_step(B, T, C, None, False, fp32_inputs=True)
+                == bench.launches_per_step(B, T, C, None, False) + 4)
+    B, T, d, f, C = 2, 1024, 256, 512, 256
+    plain = bench.phase_model(B, T, d, f, C)
+    split = bench.phase_model(B, T, d, f, C, fp32_inputs=True)
+    assert split["gateup"][1] == 3 * plain["gateup"][1]
+    assert split["target"][1] == 3 * plain["target"][1]
+    assert split["apply"] == plain["apply"] and split["update"] == plain["update"]
+    assert split["conv"][1] == (2 * B * T * d + 2 * f * d + d * d) * 10 + d * 3 * 4
+    ns = dict(fp32_inputs=False, bf16_inputs=False, fused_conv=False, shape=None)
+    assert bench.fp32_inputs_for(argparse.Namespace(config=0, **ns))
+    assert not bench.fp32_inputs_for(argparse.Namespace(config=2, **ns))
+    assert not bench.fp32_inputs_for(argparse.Namespace(config=0, **dict(ns, bf16_inputs=True)))
+    assert bench.fp32_inputs_for(argparse.Namespace(config=2, **dict(ns, fp32_inputs=True)))
