@@ -320,14 +320,19 @@ struct UpdateSchedT : std::conditional_t<kPair, PairDefaults, SchedDefaults> {
     if (write_snap && st == nullptr) {
       uint32_t pk[kBN / 2];  // the row's 256 columns as bf16 pairs
 #pragma unroll
-      for (int c = 0; c < kBN; c += 32) {
-        uint32_t v[32];
+      for (int c = 0; c < kBN; c += 64) {  // two loads per wait: the hand-off waits on this
+        uint32_t v[32], w[32];
         tmem_ld_32cols(trow + uint32_t(c), v);
+        tmem_ld_32cols(trow + uint32_t(c + 32), w);
         tmem_wait_ld();
         pin_regs(v);
+        pin_regs(w);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
+        for (int j = 0; j < 16; ++j) {
           pk[c / 2 + j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          pk[c / 2 + 16 + j] =
+              pack_bf16x2(__uint_as_float(w[2 * j]), __uint_as_float(w[2 * j + 1]));
+        }
       }
       handoff();
 #pragma unroll
